@@ -1,0 +1,460 @@
+/*
+ * lmoe_oracle.c -- plain, slow, fp64 CPU oracle for the Stable LatentMoE layer
+ * forward pass and its Quantile Balancing (QB) histogram / quantile read.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no source, header, table or helper with the CUDA library.
+ *
+ * Sources (web pages on Kimi K3's architecture):
+ *   [DD]  "Kimi-K3-Architecture-Deep-Dive" (jianyuh.github.io)
+ *         section 1 "SiTU-GLU", section 2 "Stable LatentMoE", section 3
+ *         "Quantile Balancing: A Histogram Trick for 896 Experts".
+ *   [IN]  "Inside K3: How Stable Latent MoE and MLA Attention Are Designed"
+ *         (besthub.dev), sections "SiTU-GLU", "RMSNorm insertion",
+ *         "Quantile Balancing (QB)".
+ *   [NW]  "Notes on the MoE and Attention of K3" news write-up (robotbelt.com),
+ *         sections "LatentMoE: paying for a bigger pool" and "Keeping the
+ *         numbers in range".
+ *
+ * Every function below is the plain definition, one step at a time, in fp64
+ * from the bf16 bit patterns the caller passes (decoded exactly).  Places where
+ * the pages are silent carry a "reading:" note; the same readings are listed in
+ * the repository's design notes.
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -fPIC -shared
+ *        (no -ffast-math: the fp32 steps below must be IEEE round-to-nearest).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> fp64                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Exact decode: a bf16 is the top 16 bits of an IEEE binary32. */
+double orc_bf16_to_f64(uint16_t b)
+{
+    uint32_t bits = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Round an fp64 value to the nearest bf16, ties to even, in ONE rounding
+ * (no detour through fp32, which could round twice).  bf16 keeps 8
+ * significant bits; normal exponents go down to -126, subnormals are spaced
+ * 2^-133. */
+uint16_t orc_f64_to_bf16(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80);
+    int e;
+    (void)frexp(a, &e);            /* a = m * 2^e, m in [0.5, 1) */
+    int spacing_exp = e - 8;       /* 8 significant bits */
+    if (spacing_exp < -133)
+        spacing_exp = -133;        /* bf16 subnormal grid */
+    double q = ldexp(a, -spacing_exp);       /* exact */
+    double qr = nearbyint(q);                /* ties to even (default mode) */
+    double v = ldexp(qr, spacing_exp);       /* exact */
+    if (v > 3.3895313892515355e38)          /* beyond the largest finite bf16 */
+        return (uint16_t)(sign | 0x7F80);
+    float f = (float)v;                      /* exact: v has <= 8 bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+static double dot_bf16(const uint16_t *w, const uint16_t *v, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        acc += orc_bf16_to_f64(w[i]) * orc_bf16_to_f64(v[i]);
+    return acc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scalar functions                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Logistic sigmoid 1/(1+e^-x), evaluated without overflow for either sign. */
+double orc_sigmoid(double x)
+{
+    if (x >= 0.0)
+        return 1.0 / (1.0 + exp(-x));
+    double ex = exp(x);
+    return ex / (1.0 + ex);
+}
+
+/* [DD] section 1, the SiTU definition: softcap(x; beta) = beta * tanh(x / beta),
+ * a smooth bound of x into (-beta, beta). */
+double orc_softcap(double x, double beta)
+{
+    return beta * tanh(x / beta);
+}
+
+/* [DD] section 1: SiTU(x; beta) = softcap(x; beta) * sigma(x).  [IN] "SiTU-GLU":
+ * the gate is clamped to (-beta, beta) with beta = 4. */
+double orc_situ(double x, double beta)
+{
+    return orc_softcap(x, beta) * orc_sigmoid(x);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Layer configuration                                                       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t d;            /* hidden size (7168 in K3, [NW] LatentMoE section)   */
+    int32_t latent;       /* d/2 latent the routed experts see (3584 in K3)     */
+    int32_t n_experts;    /* 2n routed experts (896 in K3)                      */
+    int32_t top_k;        /* 2k active per token (16 in K3)                     */
+    int32_t inter;        /* routed expert intermediate size                   */
+    int32_t n_shared;     /* always-on shared experts (2 in K3)                 */
+    int32_t shared_inter; /* intermediate size of each shared expert            */
+    double beta1;         /* SiTU cap, 4 ([DD] section 1)                       */
+    double beta2;         /* linear-branch softcap, 25 ([DD] section 1)         */
+    double rms_eps;       /* reading: 1e-6, inside the square root              */
+} orc_config;
+
+/* ------------------------------------------------------------------------ */
+/* a1: down-projection d -> d/2, no norm after it                            */
+/* ------------------------------------------------------------------------ */
+
+/* [DD] section 2, the LatentMoE diagram: d -> (down) -> d/2 before routing;
+ * [DD] section 2 "one RMS Norm before up-projection": the norm after the
+ * down-projection was ablated and dropped, so h is the plain linear map.
+ * h[t][l] = sum_i W_down[l][i] * x[t][i], in fp64, then rounded once to bf16
+ * (reading: the layer's activations are bf16).  w_down is [latent][d]. */
+void orc_down_proj(const orc_config *c, int64_t T, const uint16_t *x,
+                   const uint16_t *w_down, uint16_t *h_out)
+{
+    const int64_t d = c->d, L = c->latent;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t l = 0; l < L; ++l)
+            h_out[t * L + l] = orc_f64_to_bf16(dot_bf16(w_down + l * d, x + t * d, d));
+}
+
+/* ------------------------------------------------------------------------ */
+/* a2: router scores in the latent                                           */
+/* ------------------------------------------------------------------------ */
+
+/* [DD] section 2: routing happens in the d/2 latent, after the down-
+ * projection.  Reading: scores are sigma(w_e . h) (the pages only say
+ * "router scores"); they lie in (0,1), so the QB map into [0,1] is the
+ * identity.  The logit is fp64; the score is stored as fp32.
+ * w_router is [n_experts][latent]; s_out is [T][n_experts]. */
+void orc_router(const orc_config *c, int64_t T, const uint16_t *h,
+                const uint16_t *w_router, float *s_out)
+{
+    const int64_t L = c->latent, E = c->n_experts;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t e = 0; e < E; ++e)
+            s_out[t * E + e] = (float)orc_sigmoid(dot_bf16(w_router + e * L, h + t * L, L));
+}
+
+/* ------------------------------------------------------------------------ */
+/* a3: biased top-k selection                                                */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float u;
+    int32_t id;
+} scored_id;
+
+/* Larger biased score first; on equal scores the lower expert id first
+ * (reading: the pages give no tie rule). */
+static int by_score_then_id(const void *pa, const void *pb)
+{
+    const scored_id *a = (const scored_id *)pa, *b = (const scored_id *)pb;
+    if (a->u > b->u) return -1;
+    if (a->u < b->u) return 1;
+    return (a->id > b->id) - (a->id < b->id);
+}
+
+/* [DD] section 3 and [NW] "Keeping the numbers in range": loss-free balancing
+ * steers traffic by a per-expert selection bias; the bias changes which
+ * experts are chosen, not how their outputs are weighted.
+ *   u[t][e] = fp32(s[t][e] + b[e])             (an fp32 add)
+ *   idx[t]  = the top_k experts by u, ordered by (u descending, id ascending)
+ *   gate[t][j] = s[t][idx[t][j]]                (the unbiased score)
+ * Reading: no normalisation of the gates (the RMSNorm after aggregation makes
+ * any positive per-token rescaling irrelevant up to eps).
+ * margin_out[t] (nullable) = u_(k) - u_(k+1), +inf when top_k == n_experts. */
+void orc_topk(const orc_config *c, int64_t T, const float *s, const float *bias,
+              int32_t *idx_out, float *gate_out, double *margin_out)
+{
+    const int64_t E = c->n_experts, K = c->top_k;
+#pragma omp parallel
+    {
+        scored_id *row = (scored_id *)malloc((size_t)E * sizeof(scored_id));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t e = 0; e < E; ++e) {
+                float u = s[t * E + e] + bias[e];   /* fp32 + fp32 -> fp32 */
+                row[e].u = u;
+                row[e].id = (int32_t)e;
+            }
+            qsort(row, (size_t)E, sizeof(scored_id), by_score_then_id);
+            for (int64_t j = 0; j < K; ++j) {
+                idx_out[t * K + j] = row[j].id;
+                gate_out[t * K + j] = s[t * E + row[j].id];
+            }
+            if (margin_out)
+                margin_out[t] = (K < E) ? (double)row[K - 1].u - (double)row[K].u : INFINITY;
+        }
+        free(row);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a4: token permutation (group the T*k assignments by expert)               */
+/* ------------------------------------------------------------------------ */
+
+/* Stable counting sort of assignment ids a = t*top_k + j by expert idx[a].
+ *   counts[e]   = number of assignments to e
+ *   offsets[e]  = exclusive prefix sum of counts (offsets[E] = T*top_k)
+ *   perm[p]     = the assignment at permuted row p (experts in id order,
+ *                 assignments of one expert in increasing a)
+ *   inv[a]      = the permuted row of assignment a (inv[perm[p]] = p). */
+void orc_permute(const orc_config *c, int64_t T, const int32_t *idx, int32_t *counts,
+                 int32_t *offsets, int32_t *perm, int32_t *inv)
+{
+    const int64_t E = c->n_experts, N = T * (int64_t)c->top_k;
+    for (int64_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t a = 0; a < N; ++a)
+        counts[idx[a]] += 1;
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *fill = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t a = 0; a < N; ++a) {
+        int32_t e = idx[a];
+        int32_t p = offsets[e] + fill[e]++;
+        perm[p] = (int32_t)a;
+        inv[a] = p;
+    }
+    free(fill);
+}
+
+/* ------------------------------------------------------------------------ */
+/* a5 + a6 + a7: routed SiTU-GLU experts, gate-weighted combine, RMSNorm     */
+/* ------------------------------------------------------------------------ */
+
+/* One routed expert on one latent row, [DD] section 1:
+ *   p1 = W1 h, p2 = W2 h                     (W1, W2: [inter][latent])
+ *   act = SiTU(p1; beta1) * softcap(p2; beta2), rounded to bf16
+ *         (reading: the expert's intermediate activation is stored in bf16)
+ *   o  = W3 act                              (W3: [latent][inter])
+ * |SiTU| < beta1 and |softcap| < beta2, so |act| < beta1*beta2 = 100. */
+static void expert_row(const orc_config *c, const uint16_t *w1, const uint16_t *w2,
+                       const uint16_t *w3, const uint16_t *h, uint16_t *act, double *o)
+{
+    const int64_t L = c->latent, I = c->inter;
+    for (int64_t i = 0; i < I; ++i) {
+        double p1 = dot_bf16(w1 + i * L, h, L);
+        double p2 = dot_bf16(w2 + i * L, h, L);
+        act[i] = orc_f64_to_bf16(orc_situ(p1, c->beta1) * orc_softcap(p2, c->beta2));
+    }
+    for (int64_t l = 0; l < L; ++l)
+        o[l] = dot_bf16(w3 + l * I, act, I);
+}
+
+/* Routed branch for every token:
+ *   z[t] = sum_j gate[t][j] * E_{idx[t][j]}(h[t])        ([NW]: aggregation)
+ *   r[t] = z[t] / sqrt(mean_l z[t][l]^2 + eps)          ([DD] section 2 and
+ *          [IN] "RMSNorm insertion": the single norm sits after aggregation and
+ *          before the up-projection; reading: no learnable scale, eps = 1e-6)
+ * w1[e], w2[e], w3[e] point at expert e's matrices (an expert no token uses may
+ * be NULL).  Outputs (each nullable): act_out [T*top_k][inter] bf16 in
+ * assignment order, o_out [T*top_k][latent] fp64 gate-weighted expert outputs,
+ * z_out [T][latent] fp64, r_out [T][latent] bf16, r64_out [T][latent] fp64. */
+void orc_routed(const orc_config *c, int64_t T, const uint16_t *h, const int32_t *idx,
+                const float *gate, const uint16_t *const *w1, const uint16_t *const *w2,
+                const uint16_t *const *w3, uint16_t *act_out, double *o_out, double *z_out,
+                uint16_t *r_out, double *r64_out)
+{
+    const int64_t L = c->latent, I = c->inter, K = c->top_k;
+#pragma omp parallel
+    {
+        uint16_t *act = (uint16_t *)malloc((size_t)I * sizeof(uint16_t));
+        double *o = (double *)malloc((size_t)L * sizeof(double));
+        double *z = (double *)malloc((size_t)L * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t l = 0; l < L; ++l)
+                z[l] = 0.0;
+            for (int64_t j = 0; j < K; ++j) {
+                int64_t a = t * K + j;
+                int32_t e = idx[a];
+                double g = (double)gate[a];
+                expert_row(c, w1[e], w2[e], w3[e], h + t * L, act, o);
+                for (int64_t l = 0; l < L; ++l)
+                    z[l] += g * o[l];
+                if (act_out)
+                    memcpy(act_out + a * I, act, (size_t)I * sizeof(uint16_t));
+                if (o_out)
+                    for (int64_t l = 0; l < L; ++l)
+                        o_out[a * L + l] = g * o[l];
+            }
+            double ss = 0.0;
+            for (int64_t l = 0; l < L; ++l)
+                ss += z[l] * z[l];
+            double inv_rms = 1.0 / sqrt(ss / (double)L + c->rms_eps);
+            for (int64_t l = 0; l < L; ++l) {
+                double r = z[l] * inv_rms;
+                if (z_out) z_out[t * L + l] = z[l];
+                if (r_out) r_out[t * L + l] = orc_f64_to_bf16(r);
+                if (r64_out) r64_out[t * L + l] = r;
+            }
+        }
+        free(act);
+        free(o);
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a8: shared experts and the up-projection                                  */
+/* ------------------------------------------------------------------------ */
+
+/* [NW] "LatentMoE": two shared experts always participate.  Reading: each is
+ * a SiTU-GLU expert d -> shared_inter -> d acting on x itself, added after the
+ * up-projection.  ws1, ws2 are [n_shared*shared_inter][d] (expert s owns rows
+ * s*shared_inter ...); the activation is rounded to bf16:
+ *   as[t][s*Is + i] = bf16(SiTU(ws1[s*Is+i] . x[t]; beta1) * softcap(ws2[s*Is+i] . x[t]; beta2)) */
+void orc_shared_act(const orc_config *c, int64_t T, const uint16_t *x, const uint16_t *ws1,
+                    const uint16_t *ws2, uint16_t *as_out)
+{
+    const int64_t d = c->d, S = (int64_t)c->n_shared * c->shared_inter;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t i = 0; i < S; ++i) {
+            double p1 = dot_bf16(ws1 + i * d, x + t * d, d);
+            double p2 = dot_bf16(ws2 + i * d, x + t * d, d);
+            as_out[t * S + i] = orc_f64_to_bf16(orc_situ(p1, c->beta1) * orc_softcap(p2, c->beta2));
+        }
+}
+
+/* [DD] section 2: d/2 -> (up) -> d after the norm; plus the shared experts'
+ * W3 (ws3 is [d][n_shared*shared_inter], expert s owns columns s*Is ...):
+ *   y[t][m] = sum_l W_up[m][l] r[t][l] + sum_s sum_i ws3[m][s*Is+i] as[t][s*Is+i]
+ * w_up is [d][latent].  r is the bf16 normalised latent.  No residual add
+ * (the residual stream is outside the layer).  y is fp64. */
+void orc_up_shared(const orc_config *c, int64_t T, const uint16_t *r, const uint16_t *as,
+                   const uint16_t *w_up, const uint16_t *ws3, double *y_out)
+{
+    const int64_t d = c->d, L = c->latent, Is = c->shared_inter, ns = c->n_shared;
+    const int64_t S = ns * Is;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t m = 0; m < d; ++m) {
+            double acc = dot_bf16(w_up + m * L, r + t * L, L);
+            for (int64_t s = 0; s < ns; ++s)
+                for (int64_t i = 0; i < Is; ++i)
+                    acc += orc_bf16_to_f64(ws3[m * S + s * Is + i]) *
+                           orc_bf16_to_f64(as[t * S + s * Is + i]);
+            y_out[t * d + m] = acc;
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a9: QB histogram                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* [DD] section 3, steps 1-2 and [IN] "Quantile Balancing (QB)": map the
+ * scores into [0,1] (the identity for sigmoid scores) and keep a B-bin
+ * frequency histogram per expert over all scores, biased or not chosen.
+ *   bin(s) = min(B-1, floor(fp32(s * B)))   -- fp32 multiply, then floor
+ *   hist[e][bin(s[t][e])] += 1   for every token t
+ * s has row stride ld (elements).  accumulate = 0 clears hist first; 1 adds
+ * to it (histograms are additive, [DD] section 3 step 3).  Reading: scores
+ * below 0 go to bin 0 (they cannot occur for sigmoid outputs). */
+void orc_qb_histogram(const float *s, int64_t T, int32_t E, int64_t ld, int32_t B,
+                      uint32_t *hist, int accumulate)
+{
+    if (!accumulate)
+        memset(hist, 0, (size_t)E * (size_t)B * sizeof(uint32_t));
+    const float fB = (float)B;
+#pragma omp parallel for schedule(static)
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t t = 0; t < T; ++t) {
+            float v = s[t * ld + e] * fB;   /* one fp32 rounding */
+            float f = floorf(v);
+            int64_t bin = (f < 0.0f) ? 0 : (int64_t)f;
+            if (bin > B - 1)
+                bin = B - 1;
+            hist[e * (int64_t)B + bin] += 1u;
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a10: QB quantile read -> per-expert bias                                  */
+/* ------------------------------------------------------------------------ */
+
+/* [DD] section 3 (QB replaces the fixed-step bias update; zero extra
+ * hyper-parameters), [IN] "Quantile Balancing (QB)" (read the quantile from
+ * the histogram) and [NW] "Keeping the numbers in range" (estimate where
+ * each expert's threshold must sit to receive its target share).
+ * Reading, per expert e:
+ *   N      = sum_j hist[e][j]
+ *   r      = clamp(ceil(level * N), 1, N)            (rank of the quantile)
+ *   C_j    = hist[e][0] + ... + hist[e][j]
+ *   j*     = min { j : C_j >= r }
+ *   q[e]   = (j* + (r - C_{j*-1}) / hist[e][j*]) / B  (linear inside the bin)
+ *   b[e]   = -q[e]
+ * level = 1 - top_k/n_experts.  With b = -q every expert clears a common
+ * threshold of 0 on a top_k/n_experts share of tokens.  An empty row
+ * (N = 0) gives q = 0, b = 0.  q_out is nullable. */
+void orc_qb_quantile_bias(const uint32_t *hist, int32_t E, int32_t B, double level,
+                          float *q_out, float *b_out)
+{
+    for (int64_t e = 0; e < E; ++e) {
+        const uint32_t *row = hist + e * (int64_t)B;
+        uint64_t n = 0;
+        for (int64_t j = 0; j < B; ++j)
+            n += row[j];
+        double q = 0.0;
+        if (n > 0) {
+            double rr = ceil(level * (double)n);
+            if (rr < 1.0) rr = 1.0;
+            if (rr > (double)n) rr = (double)n;
+            uint64_t r = (uint64_t)rr;
+            uint64_t below = 0;   /* C_{j-1} */
+            for (int64_t j = 0; j < B; ++j) {
+                if (below + row[j] >= r) {
+                    q = ((double)j + (double)(r - below) / (double)row[j]) / (double)B;
+                    break;
+                }
+                below += row[j];
+            }
+        }
+        if (q_out) q_out[e] = (float)q;
+        b_out[e] = (float)(-q);
+    }
+}
+
+/* Number of OpenMP threads the oracle will use (1 without OpenMP). */
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

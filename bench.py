@@ -1,0 +1,473 @@
+"""Benchmark: the Stable LatentMoE layer forward at K3 prefill shape plus its
+Quantile Balancing histogram and bias read, on GB300, through the C ABI.
+
+One step = lmoe_forward over T=8192 tokens (d=7168 -> 3584 latent, 896 routed
+experts, top-16, 2 shared experts of 1024, routed intermediate 512) + the
+QB histogram (B=1000) of that batch's router scores + the quantile/bias read.
+Inputs are seeded synthetic data of that shape (see sparse_moe_layer_bias_gb300
+/synth.py); weights (10.3 GB) and activations are resident in HBM.
+
+Also measured in the same run (reported inside the one JSON line):
+  * e2e: the same step with x/bias copied from pinned host memory and y/bias
+    copied back, inside the timed region;
+  * the K3 decode layer (T=64) and the QB histogram at T=2^20 x 896;
+  * per-stage kernel times from CUDA events on the launching stream, and the
+    roofline of the dominant kernel against MEASURED_PEAKS.json;
+  * cpu_baseline: the CPU oracle on a bounded sample of the same workload.
+
+`--impl reference` times the CPU oracle (the reference arm) instead.
+Multi-GPU (torchrun): every rank runs its own batch (replicas, no collective
+on the data path; "scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_moe_layer_bias_gb300 import synth  # noqa: E402
+
+METRIC = "LatentMoE layer tokens/s & %bf16 TC peak (K3 shape); QB histogram HBM GB/s"
+QB_B = 1000
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def layer_work(shape, T, touched_experts):
+    """Algorithmic FLOPs and bytes per stage for T tokens (bf16 = 2 bytes)."""
+    d, L, E, k, I = shape.d, shape.latent, shape.n_experts, shape.top_k, shape.inter
+    S = shape.n_shared * shape.shared_inter
+    n = T * k
+    w = {}
+    w["down"] = (2.0 * T * d * L, 2.0 * (T * d + L * d + T * L))
+    w["shared"] = (4.0 * T * d * S, 2.0 * (T * d + 2 * S * d + T * S))
+    w["router"] = (2.0 * T * L * E, 2.0 * (T * L + E * L) + 4.0 * T * E)
+    w["topk"] = (0.0, 4.0 * T * E + 4.0 * E + 8.0 * n)
+    w["scan"] = (0.0, 8.0 * E * math.ceil(T / 32))
+    w["offsets"] = (0.0, 8.0 * E)
+    w["scatter"] = (0.0, 16.0 * n)
+    w["expert_w12"] = (4.0 * n * L * I, 2.0 * (touched_experts * 2 * I * L + T * L + n * I))
+    w["expert_w3"] = (2.0 * n * I * L, 2.0 * (touched_experts * L * I + n * I + n * L))
+    w["combine"] = (0.0, 2.0 * (n * L + T * L))
+    w["up"] = (2.0 * T * (L + S) * d, 2.0 * (T * (L + S) + d * (L + S) + T * d))
+    return w
+
+
+def layer_flops_per_token(shape):
+    d, L, k, I = shape.d, shape.latent, shape.top_k, shape.inter
+    S = shape.n_shared * shape.shared_inter
+    return 2.0 * d * L + 2.0 * L * shape.n_experts + 6.0 * k * L * I + 2.0 * L * d + 6.0 * d * S
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for n, v in zip(names[1:], flags[1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def oracle_tokens_per_s(shape, w_bits, x_bits, bias, n_tokens, scores_for_qb=None):
+    """Time the CPU oracle on n_tokens of the layer (+ QB over scores_for_qb);
+    returns (tokens/s, seconds, threads)."""
+    import oracle
+    cfg = oracle.LayerConfig(**shape.layer_dict())
+    t0 = time.perf_counter()
+    out = oracle.layer_forward(cfg, x_bits[:n_tokens], w_bits, bias)
+    t_layer = time.perf_counter() - t0
+    t_qb, qb_tokens = 0.0, 0
+    if scores_for_qb is not None:
+        t1 = time.perf_counter()
+        hist = oracle.qb_histogram(scores_for_qb, QB_B)
+        oracle.qb_quantile_bias(hist, 1.0 - shape.top_k / shape.n_experts)
+        t_qb = time.perf_counter() - t1
+        qb_tokens = scores_for_qb.shape[0]
+    per_token = t_layer / n_tokens + (t_qb / qb_tokens if qb_tokens else 0.0)
+    del out
+    return 1.0 / per_token, t_layer + t_qb, oracle.num_threads()
+
+
+def host_weights_bits(w):
+    return {k: synth.bits(v) for k, v in w.items()}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    shape = synth.K3_PREFILL
+    w = synth.layer_weights_device(shape)
+    x, bias = synth.activations_device(shape)
+    wb = host_weights_bits(w)
+    del w
+    torch.cuda.empty_cache()
+    xb = synth.bits(x)
+    b = bias.cpu().numpy()
+    per_step = 8
+    for i in range(args.warmup):
+        oracle_tokens_per_s(shape, wb, xb[i * per_step:], b, per_step)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        off = ((args.warmup + i) * per_step) % (shape.T - per_step)
+        oracle_tokens_per_s(shape, wb, xb[off:], b, per_step)
+    dt = time.perf_counter() - t0
+    v = per_step * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "k3_prefill layer forward (T=8192, d=7168, latent=3584, E=896, k=16, "
+                                   "I=512, 2x1024 shared)", "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{per_step} tokens of the K3 prefill batch per step (fp64 C oracle, OpenMP)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=128)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(world)
+    import sparse_moe_layer_bias_gb300 as lm
+    lm.load_library()
+    peaks, peak_src = load_peaks()
+
+    shape = synth.K3_PREFILL
+    T, E, k = shape.T, shape.n_experts, shape.top_k
+    level = 1.0 - k / E
+    w = synth.layer_weights_device(shape)
+    x, bias = synth.activations_device(shape, seed_offset=rank)
+    handle = lm.lmoe_create(shape.layer_dict(), w, max_tokens=T)
+    ws = lm.alloc_workspace(handle, T)
+    y = torch.empty_like(x)
+    scores = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    hist = torch.empty((E, QB_B), dtype=torch.int32, device="cuda")
+    q_out = torch.empty(E, dtype=torch.float32, device="cuda")
+    b_new = torch.empty(E, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(xin, bin_, yout):
+        lm.lmoe_forward(handle, xin, bin_, y=yout, workspace=ws, scores_out=scores,
+                        expert_counts_out=counts, stream=stream)
+        lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
+        lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
+
+    kernels_per_step = len(lm.STAGES) + 2      # 11 forward kernels + QB histogram + quantile
+
+    for _ in range(args.warmup):
+        step(x, bias, y)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(handle) == 0
+    touched = int((counts > 0).sum().item())
+
+    # per-stage events for every timed step (read after the timed region)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)]
+               for _ in range(args.steps)]
+    for evs in ev_sets:       # create the cudaEvent_t handles outside the timed region
+        for e in evs:
+            e.record(stream)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    qb_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            lm.lmoe_set_stage_events(handle, ev_sets[i])
+            lm.lmoe_forward(handle, x, bias, y=y, workspace=ws, scores_out=scores,
+                            expert_counts_out=counts, stream=stream)
+            qb_ev[i][0].record(stream)
+            lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
+            lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
+            qb_ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    lm.lmoe_set_stage_events(handle, None)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(world, ms)
+    assert lm.lmoe_device_status(handle) == 0
+
+    stage_ms = {}
+    for j, name in enumerate(lm.STAGES):
+        stage_ms[name] = float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in ev_sets]))
+    stage_ms["qb"] = float(np.mean([a.elapsed_time(b) for a, b in qb_ev]))
+    work = layer_work(shape, T, touched)
+    stages = {}
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    for name in lm.STAGES:
+        fl, by = work[name]
+        t = stage_ms[name] * 1e-3
+        bound = "tensor" if (fl > 0 and fl / by > ridge) else "hbm"
+        if bound == "tensor":
+            ach, peak, unit = fl / t / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        else:
+            ach, peak, unit = by / t / 1e9, peaks["hbm_gbs"], "GB/s"
+        stages[name] = {"ms": round(stage_ms[name], 4), "bound": bound, "achieved": round(ach, 2),
+                        "peak": peak, "unit": unit, "frac": round(ach / peak, 4),
+                        "share": round(stage_ms[name] / ms, 4)}
+    dom = max(lm.STAGES, key=lambda n: stage_ms[n])
+    dfl, dby = work[dom]
+    roof = dict(stages[dom])
+    roof.pop("ms")
+    roof.pop("share")
+    roof["kernel"] = dom
+    roof["per_launch"] = {"flop": dfl, "bytes": dby}
+    roof["traffic"] = None
+    roof["peak_source"] = peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " hbm copy")
+
+    total_flop = layer_flops_per_token(shape) * T
+    tps = world * T / (ms * 1e-3)
+    layer_ms = sum(stage_ms[n] for n in lm.STAGES)
+    tflops = total_flop / (layer_ms * 1e-3) / 1e12
+
+    # --------------------------------------------------------------- e2e (host buffers)
+    x_host = x.cpu().pin_memory()
+    b_host = bias.cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    bn_host = torch.empty(E, dtype=torch.float32).pin_memory()
+    x_dev, b_dev = torch.empty_like(x), torch.empty_like(bias)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        b_dev.copy_(b_host, non_blocking=True)
+        step(x_dev, b_dev, y)
+        y_host.copy_(y, non_blocking=True)
+        bn_host.copy_(b_new, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
+    h2d = x.numel() * 2 + bias.numel() * 4
+    d2h = y.numel() * 2 + E * 4
+
+    # --------------------------------------------------------------- QB sweep point T = 2^20
+    Tq = 1 << 20
+    sq = synth.qb_scores(Tq, E, device="cuda")
+    hq = torch.empty((E, QB_B), dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        lm.qb_histogram(sq, QB_B, hist=hq, stream=stream)
+    torch.cuda.synchronize()
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nq = max(10, args.steps)
+    q0.record(stream)
+    for _ in range(nq):
+        lm.qb_histogram(sq, QB_B, hist=hq, stream=stream)
+    q1.record(stream)
+    torch.cuda.synchronize()
+    qb_ms = q0.elapsed_time(q1) / nq
+    qb_bytes = 4.0 * Tq * E + 4.0 * E * QB_B
+    qb_gbs = qb_bytes / (qb_ms * 1e-3) / 1e9
+    del sq
+    torch.cuda.empty_cache()
+
+    # --------------------------------------------------------------- decode layer T = 64
+    dshape = synth.K3_DECODE
+    wd = dict(w)
+    lim = math.sqrt(3.0 / dshape.latent)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(dshape.seed)
+    wd["w_router"] = ((torch.rand((E, dshape.latent), generator=gen, device="cuda") * 2 - 1) * lim).to(torch.bfloat16)
+    hd = lm.lmoe_create(dshape.layer_dict(), wd, max_tokens=dshape.T)
+    wsd = lm.alloc_workspace(hd, dshape.T)
+    xd, bd = synth.activations_device(dshape)
+    yd = torch.empty_like(xd)
+    cd = torch.empty(E, dtype=torch.int32, device="cuda")
+    for _ in range(args.warmup):
+        lm.lmoe_forward(hd, xd, bd, y=yd, workspace=wsd, expert_counts_out=cd, stream=stream)
+    torch.cuda.synchronize()
+    touched_d = int((cd > 0).sum().item())
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nd = max(20, args.steps)
+    d0.record(stream)
+    for _ in range(nd):
+        lm.lmoe_forward(hd, xd, bd, y=yd, workspace=wsd, expert_counts_out=cd, stream=stream)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = d0.elapsed_time(d1) / nd
+    wdec = layer_work(dshape, dshape.T, touched_d)
+    dec_bytes = sum(v[1] for v in wdec.values())
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    assert lm.lmoe_device_status(hd) == 0
+
+    # --------------------------------------------------------------- CPU oracle baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        wb = host_weights_bits(w)
+        xb = synth.bits(x)
+        v, secs, cores = oracle_tokens_per_s(shape, wb, xb, bias.cpu().numpy(), args.cpu_tokens,
+                                             scores_for_qb=scores.cpu().numpy())
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "seconds": round(secs, 2),
+               "sample": f"{args.cpu_tokens} tokens of the K3 prefill batch through the fp64 C oracle "
+                         f"(OpenMP) + the QB histogram/quantile of all {T}x{E} scores"}
+
+    line = {
+        "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "k3_prefill: Stable LatentMoE layer forward T=8192, d=7168, latent=3584, "
+                               "E=896, top-16, I=512, 2 shared experts x 1024 + QB histogram B=1000 + "
+                               "quantile bias",
+                   "T": T, "l2": "inputs larger than L2 (10.3 GB of weights streamed per step)",
+                   "parallelism": f"replicas x{world}"},
+        "layer_tflops": round(tflops, 2),
+        "frac_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
+        "roofline": roof,
+        "stages": stages,
+        "qb_ms_in_step": round(stage_ms["qb"], 4),
+        "qb_hist_sweep": {"T": Tq, "E": E, "B": QB_B, "ms": round(qb_ms, 4), "gbs": round(qb_gbs, 1),
+                          "frac_hbm": round(qb_gbs / peaks["hbm_gbs"], 4)},
+        "decode": {"T": dshape.T, "ms": round(dec_ms, 4), "tokens_per_s": dshape.T / (dec_ms * 1e-3),
+                   "touched_experts": touched_d, "bytes": dec_bytes, "gbs": round(dec_gbs, 1),
+                   "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "peaks": dict(peaks, source=peak_src),
+        "cpu_baseline": cpu,
+        "touched_experts": touched,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

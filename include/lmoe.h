@@ -1,0 +1,204 @@
+/*
+ * lmoe.h -- C ABI of the GB300 (sm_103a) Stable LatentMoE layer forward and
+ * Quantile Balancing (QB) library, liblmoe.so.
+ *
+ * The operations follow three public write-ups of Kimi K3's architecture:
+ *   [DD] "Kimi-K3-Architecture-Deep-Dive": section 1 (SiTU-GLU), section 2
+ *        (Stable LatentMoE), section 3 (Quantile Balancing).
+ *   [IN] "Inside K3: How Stable Latent MoE and MLA Attention Are Designed":
+ *        sections "SiTU-GLU", "RMSNorm insertion", "Quantile Balancing (QB)".
+ *   [NW] "Notes on the MoE and Attention of K3" (news write-up): sections
+ *        "LatentMoE: paying for a bigger pool", "Keeping the numbers in range".
+ *
+ * Conventions shared by every call:
+ *   - Tensors are caller-owned DEVICE memory, dense row-major.  bf16 tensors are
+ *     passed as uint16_t bit patterns.  Every tensor pointer must be 16-byte
+ *     aligned (LMOE_ERR_ALIGNMENT otherwise).
+ *   - Calls enqueue kernels on `stream` and return without synchronising.
+ *     Errors found on the host (bad arguments, shapes, alignment, workspace
+ *     size) are reported synchronously and then nothing is enqueued; errors the
+ *     GPU raises surface at the caller's next synchronisation of the stream.
+ *   - No call allocates device memory except lmoe_create (handle state).
+ *   - Every call returns an lmoe_status (0 = success).
+ */
+#ifndef LMOE_H_
+#define LMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    LMOE_OK = 0,
+    LMOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum          */
+    LMOE_ERR_UNSUPPORTED_SHAPE = 2, /* a dimension outside what the kernels tile      */
+    LMOE_ERR_ALIGNMENT = 3,         /* a pointer not 16-byte aligned                  */
+    LMOE_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required     */
+    LMOE_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed           */
+    LMOE_ERR_TIMEOUT = 6,           /* a kernel's bounded wait gave up (device error) */
+    LMOE_ERR_NO_DEVICE = 7          /* the current device is not sm_103 (GB300)       */
+} lmoe_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *lmoe_status_string(int status);
+
+/* ------------------------------------------------------------------------ */
+/* Layer configuration and weights                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Shape of one Stable LatentMoE layer.  [DD] section 2: d -> d/2 latent,
+ * 2n routed experts of which 2k are active per token; [NW] "LatentMoE": K3 has
+ * d = 7168, latent 3584, 896 experts, 16 active, 2 shared experts.
+ * Supported: d, latent, inter, n_shared*shared_inter multiples of 64;
+ * 1 <= top_k <= 32; top_k <= n_experts <= 1024; max_tokens >= 0. */
+typedef struct {
+    int32_t d;            /* hidden size                                      */
+    int32_t latent;       /* routed latent width (d/2 in K3)                  */
+    int32_t n_experts;    /* routed experts E                                 */
+    int32_t top_k;        /* experts chosen per token                         */
+    int32_t inter;        /* routed expert intermediate size I                */
+    int32_t n_shared;     /* shared experts (always active)                   */
+    int32_t shared_inter; /* intermediate size of each shared expert Is       */
+    float beta1;          /* SiTU cap; 4 in K3 ([DD] section 1)               */
+    float beta2;          /* linear-branch softcap; 25 in K3 ([DD] section 1) */
+    float rms_eps;        /* epsilon inside the RMSNorm square root (1e-6)    */
+    int64_t max_tokens;   /* largest T a forward call will be given           */
+} lmoe_config;
+
+/* Weight pointers (device, bf16, row-major, K-major rows as "out x in").
+ * The handle keeps these POINTERS: the caller must keep the weights alive and
+ * unchanged until lmoe_destroy.  S = n_shared * shared_inter. */
+typedef struct {
+    const uint16_t *w_down;   /* [latent][d]           down-projection            */
+    const uint16_t *w_router; /* [n_experts][latent]   router rows                */
+    const uint16_t *w1;       /* [n_experts][inter][latent]  SiTU branch          */
+    const uint16_t *w2;       /* [n_experts][inter][latent]  softcapped branch    */
+    const uint16_t *w3;       /* [n_experts][latent][inter]  expert output        */
+    const uint16_t *ws1;      /* [S][d]  shared SiTU branch (expert s: rows s*Is..) */
+    const uint16_t *ws2;      /* [S][d]  shared softcapped branch                */
+    const uint16_t *ws3;      /* [d][S]  shared output (expert s: columns s*Is..) */
+    const uint16_t *w_up;     /* [d][latent]           up-projection              */
+} lmoe_weights;
+
+typedef struct lmoe_handle lmoe_handle;
+
+/* Validate `cfg`, check the device (sm_103), and build the handle: the TMA
+ * descriptors of the weights and a small device status word.  On success
+ * *out owns a handle to release with lmoe_destroy.  Synchronous. */
+int lmoe_create(const lmoe_config *cfg, const lmoe_weights *weights, lmoe_handle **out);
+
+/* Release the handle and its device state (synchronises the device first). */
+int lmoe_destroy(lmoe_handle *handle);
+
+/* Bytes of caller-provided device workspace lmoe_forward needs for T tokens
+ * (0 <= T <= max_tokens).  The workspace holds the routing maps and the
+ * intermediate activations; see lmoe_workspace_layout. */
+int lmoe_workspace_size(const lmoe_handle *handle, int64_t T, size_t *bytes);
+
+/* Byte offsets, inside the workspace, of the intermediates a forward of T
+ * tokens leaves behind (for inspection and tests; valid after the stream has
+ * reached the end of the forward).  Every slot is always reserved; when the
+ * caller passes its own buffer for scores, topk_idx, gates or counts, the
+ * values go there and that slot is left untouched. */
+typedef struct {
+    int64_t h;        /* [T][latent] bf16        latent after the down-projection */
+    int64_t scores;   /* [T][n_experts] fp32     sigmoid router scores            */
+    int64_t topk_idx; /* [T][top_k] int32        chosen experts                   */
+    int64_t gates;    /* [T][top_k] fp32         unbiased scores of those experts */
+    int64_t counts;   /* [n_experts] int32       assignments per expert           */
+    int64_t offsets;  /* [n_experts+1] int32     exclusive scan of counts         */
+    int64_t perm;     /* [T*top_k] int32         assignment at each permuted row  */
+    int64_t inv;      /* [T*top_k] int32         permuted row of each assignment  */
+    int64_t act;      /* [T*top_k][inter] bf16   expert SiTU-GLU activations, permuted order */
+    int64_t o;        /* [T*top_k][latent] bf16  gate-weighted expert outputs, assignment order */
+    int64_t r;        /* [T][latent] bf16        RMS-normalised aggregate          */
+    int64_t shared_act; /* [T][S] bf16           shared-expert activations        */
+} lmoe_ws_layout;
+
+int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *layout);
+
+/* One forward pass of the Stable LatentMoE layer on T tokens:
+ *   h  = W_down x                              (a1; [DD] section 2)
+ *   s  = sigmoid(W_router h)                   (a2; routing in the latent)
+ *   u  = fp32(s + bias); pick the top_k experts by u (ties: lower id)
+ *        gates = s at the chosen experts       (a3; [DD] section 3, [NW])
+ *   group the T*top_k assignments by expert    (a4; stable)
+ *   act = SiTU(W1[e] h; beta1) * softcap(W2[e] h; beta2)   (a5; [DD] section 1)
+ *   o   = gate * W3[e] act                     (a6)
+ *   z   = sum over the token's experts of o;  r = z / sqrt(mean(z^2) + eps)
+ *                                              (a7; [DD] section 2, [IN] "RMSNorm insertion")
+ *   y  = W_up r + sum_s Ws3_s (SiTU(Ws1_s x) * softcap(Ws2_s x))   (a8; [NW] shared experts)
+ * x: [T][d] bf16 input.  bias: [n_experts] fp32 selection bias.  y: [T][d]
+ * bf16 output.  Optional outputs (NULL = keep them in the workspace):
+ * scores_out [T][n_experts] fp32, topk_idx_out [T][top_k] int32, gates_out
+ * [T][top_k] fp32, expert_counts_out [n_experts] int32.  workspace: at least
+ * lmoe_workspace_size(T) bytes, 256-byte aligned.  T = 0 enqueues nothing.
+ * A handle may be used from one stream at a time per workspace. */
+int lmoe_forward(lmoe_handle *handle, const uint16_t *x, int64_t T, const float *bias,
+                 uint16_t *y, float *scores_out, int32_t *topk_idx_out, float *gates_out,
+                 int32_t *expert_counts_out, void *workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
+/* Stages of lmoe_forward, in launch order (for lmoe_set_stage_events). */
+typedef enum {
+    LMOE_STAGE_DOWN = 0,       /* a1 down-projection GEMM                          */
+    LMOE_STAGE_SHARED = 1,     /* shared experts' W1|W2 GEMM + SiTU-GLU            */
+    LMOE_STAGE_ROUTER = 2,     /* a2 router GEMM + sigmoid                         */
+    LMOE_STAGE_TOPK = 3,       /* a3 biased top-k                                  */
+    LMOE_STAGE_SCAN = 4,       /* a4 per-expert counts                             */
+    LMOE_STAGE_OFFSETS = 5,    /* a4 offsets and grouped-GEMM tile list            */
+    LMOE_STAGE_SCATTER = 6,    /* a4 permutation maps                              */
+    LMOE_STAGE_EXPERT_W12 = 7, /* a5 grouped expert W1|W2 GEMM + SiTU-GLU          */
+    LMOE_STAGE_EXPERT_W3 = 8,  /* a6 grouped expert W3 GEMM + gate scatter         */
+    LMOE_STAGE_COMBINE = 9,    /* a7 aggregation + RMSNorm                         */
+    LMOE_STAGE_UP = 10,        /* a8 up-projection + shared W3 GEMM                */
+    LMOE_NUM_STAGES = 11
+} lmoe_stage;
+
+/* Timing hook: with n_events == LMOE_NUM_STAGES + 1 (cudaEvent_t handles
+ * created by the caller), every later lmoe_forward records events[i] on its
+ * stream just before stage i and events[LMOE_NUM_STAGES] after the last one.
+ * events = NULL (n_events = 0) turns it off.  The handle keeps the array
+ * pointer: it must stay valid while set. */
+int lmoe_set_stage_events(lmoe_handle *handle, cudaEvent_t *events, int n_events);
+
+/* Device-side status of the handle's kernels (bounded waits that gave up).
+ * Synchronises `stream`, copies the status word, and clears it when `clear`
+ * is non-zero.  *device_status is LMOE_OK or LMOE_ERR_TIMEOUT. */
+int lmoe_device_status(lmoe_handle *handle, cudaStream_t stream, int clear, int *device_status);
+
+/* ------------------------------------------------------------------------ */
+/* Quantile Balancing                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* QB histogram ([DD] section 3, steps 1-3; [IN] "Quantile Balancing (QB)").
+ * scores: [T][ld] fp32 (the first E columns are the experts), values in [0,1]
+ * (sigmoid scores need no further map).  hist: [E][B] uint32.
+ *   bin(s) = min(B-1, floor(fp32(s*B)))  (fp32 multiply; s < 0 -> bin 0)
+ *   hist[e][bin(scores[t][e])] += 1 for all t < T.
+ * accumulate = 0 clears hist first; 1 adds to it (histograms are additive).
+ * Constraints: T >= 0, 1 <= E <= ld, 1 <= B <= 65536.  NaN scores are not
+ * allowed (their bin is undefined). */
+int qb_histogram(const float *scores, int64_t T, int32_t E, int64_t ld, int32_t B,
+                 uint32_t *hist, int accumulate, cudaStream_t stream);
+
+/* QB quantile read and bias ([DD] section 3; [IN] "Quantile Balancing (QB)";
+ * [NW] "Keeping the numbers in range").  For each expert e with N = sum of its
+ * row: r = clamp(ceil(level*N), 1, N); j* = first bin whose cumulative count
+ * reaches r; q[e] = (j* + (r - C_{j*-1}) / hist[e][j*]) / B (linear inside
+ * the bin, computed in fp64, stored fp32); bias[e] = -q[e].  An empty row
+ * gives q = 0, bias = 0.  level is normally 1 - top_k/n_experts.
+ * hist: [E][B] uint32; quantile_out: [E] fp32 (nullable); bias_out: [E] fp32. */
+int qb_quantile_bias(const uint32_t *hist, int32_t E, int32_t B, double level,
+                     float *quantile_out, float *bias_out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMOE_H_ */

@@ -1,1 +1,26 @@
-"""GB300-native Stable LatentMoE layer forward and Quantile Balancing histogram."""
+"""GB300-native Stable LatentMoE layer forward and Quantile Balancing histogram.
+
+The compute lives in liblmoe.so (hand-written CUDA for sm_103a, C ABI in
+include/lmoe.h); this package is its ctypes binding plus the seeded input
+generators (``synth``).  Importing it does not load the library; the first
+call does, and raises if the library has not been built.
+"""
+from .binding import (  # noqa: F401
+    EXPORTED,
+    Handle,
+    LmoeError,
+    alloc_workspace,
+    library_path,
+    lmoe_create,
+    lmoe_destroy,
+    lmoe_device_status,
+    lmoe_forward,
+    lmoe_set_stage_events,
+    STAGES,
+    lmoe_status_string,
+    lmoe_workspace_layout,
+    lmoe_workspace_size,
+    load_library,
+    qb_histogram,
+    qb_quantile_bias,
+)

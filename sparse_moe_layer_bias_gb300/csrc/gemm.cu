@@ -1,0 +1,404 @@
+// gemm.cu -- persistent bf16 GEMM on the sm_103a tensor cores (tcgen05),
+// used for every contraction of the Stable LatentMoE layer:
+//   a1  h   = x W_down^T                       (A dense, B plain, bf16 out)
+//   a2  s   = sigmoid(h W_router^T)            (A dense, B plain, fp32 out)
+//   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows gathered by the
+//            expert permutation, B = the expert's W1|W2 rows, grouped by expert)
+//   a6  o   = gate * act W3^T                  (A = permuted act rows, B = the
+//            expert's W3, rows scattered back to assignment order)
+//   a8  y   = r W_up^T + shared_act Ws3^T       (K split over two A/B sources)
+//   a8' shared_act = SiTU(x Ws1^T) * softcap(x Ws2^T)
+// (SiTU-GLU: "Kimi-K3-Architecture-Deep-Dive" section 1; the layer's chain of
+// projections: same page, section 2.)
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: per 64-wide K block, one box of A (or 32 gather4
+//               row quads) and one or two boxes of B into a STAGES-deep ring
+//               of 128B-swizzled shared-memory tiles;
+//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
+//               (M=128, N=BN, K=16) x4 per stage into one of two TMEM
+//               accumulators and commits stage release / tile completion;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               the fused activation, and the global stores; releases the
+//               accumulator so the next tile's MMAs overlap this epilogue.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;  // two accumulators of up to 256 fp32 columns
+constexpr int kAccStride = 256;
+
+template <int BN>
+struct Cfg {
+    static constexpr int kABytes = kBM * kBK * 2;       // 16 KB
+    static constexpr int kBBytes = BN * kBK * 2;        // 16 or 32 KB
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (BN == 256) ? 4 : 6;
+    static constexpr int kBarBytes = 256;
+    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes;
+};
+
+struct Tile {
+    int row0;    // first output row (dense) / first permuted row (grouped)
+    int nrows;   // valid rows in this tile (<= 128)
+    int nt;      // N tile index
+    int expert;  // grouped: expert id
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
+    Tile ti;
+    if (GROUPED) {
+        // N-tile major: every M tile (of every expert) for N tile 0, then N
+        // tile 1, ... -- the M tiles of one expert's weight tile run side by
+        // side, so the weight tile is read from HBM once and shared via L2.
+        const int mt = t % n_m;
+        ti.nt = t / n_m;
+        const int4 d = a.tiles[mt];
+        ti.expert = d.x;
+        ti.row0 = d.y;
+        ti.nrows = d.z;
+    } else {
+        // Rasterise in groups of 16 M tiles so the A rows of a group stay in L2
+        // while every N tile visits them.
+        constexpr int G = 16;
+        const int group = G * a.n_tiles;
+        const int g = t / group, r = t % group;
+        const int m_first = g * G;
+        const int gm = min(G, a.m_tiles - m_first);
+        ti.nt = r / gm;
+        const int mt = m_first + r % gm;
+        ti.row0 = mt * kBM;
+        ti.nrows = min(kBM, a.m_rows - ti.row0);
+        ti.expert = 0;
+    }
+    return ti;
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Store 32 fp32 values as bf16 at dst (64 bytes, 16-byte aligned), masking
+// columns >= ncols.
+__device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32], int ncols) {
+    if (ncols >= 32) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+            w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+            w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+            w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+            d4[q] = w;
+        }
+    } else {
+        __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(dst);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) d[j] = __float2bfloat16_rn(v[j]);
+    }
+}
+
+__device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], int ncols) {
+    if (ncols >= 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < ncols) dst[j] = v[j];
+    }
+}
+
+template <int BN, int AM, int BMD, int EPI, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                const GemmArgs args) {
+    using C = Cfg<BN>;
+    constexpr int S = C::kStages;
+    constexpr int H = BN / 2;  // GLU: features per tile
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *smA = smem;
+    uint8_t *smB = smem + S * C::kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
+    uint64_t *full = bars;             // [S]  TMA -> MMA
+    uint64_t *empty = bars + S;        // [S]  MMA -> TMA
+    uint64_t *tfull = bars + 2 * S;    // [2]  MMA -> epilogue
+    uint64_t *tempty = bars + 2 * S + 2;  // [2]  epilogue -> MMA
+    uint64_t *drain = bars + 2 * S + 4;   // [1]  final MMA completion
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), 128);
+        }
+        mbar_init(smem_u32(&drain[0]), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_m = GROUPED ? *args.n_mtiles : args.m_tiles;
+    const int total = n_m * args.n_tiles;
+    const uint64_t lim = args.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = tile_at<GROUPED>(args, t, n_m);
+            int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
+            bool gvalid = false;
+            uint32_t a_bytes = C::kABytes;
+            if (AM == A_GATHER) {
+                const int base = lane * 4;
+                gvalid = base < ti.nrows;
+                if (gvalid) {
+                    const int last = ti.nrows - 1;
+                    g0 = args.gather_rows[ti.row0 + min(base + 0, last)];
+                    g1 = args.gather_rows[ti.row0 + min(base + 1, last)];
+                    g2 = args.gather_rows[ti.row0 + min(base + 2, last)];
+                    g3 = args.gather_rows[ti.row0 + min(base + 3, last)];
+                }
+                a_bytes = static_cast<uint32_t>((ti.nrows + 3) / 4) * 4u * (kBK * 2);
+            }
+            const int brow = ti.expert * args.b_expert_rows + ti.nt * (BMD == B_GLU ? H : BN);
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                // every lane waits; the warp proceeds only if all lanes saw the slot free
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
+                                                       args.err, lim))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full[stage]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + C::kBBytes);
+                __syncwarp();
+                const uint32_t sa = smem_u32(smA + stage * C::kABytes);
+                const uint32_t sb = smem_u32(smB + stage * C::kBBytes);
+                const bool second = (AM == A_SPLIT || BMD == B_SPLIT) && kb >= args.k_split;
+                const int kx = (second ? kb - args.k_split : kb) * kBK;
+                if (AM == A_GATHER) {
+                    if (gvalid) tma_gather4(sa + lane * 4 * (kBK * 2), &tmA0, kx, g0, g1, g2, g3, fb);
+                } else if (lane == 0) {
+                    tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
+                }
+                if (lane == 0) {
+                    if (BMD == B_GLU) {
+                        tma_load_2d(sb, &tmB0, kx, brow, fb);
+                        tma_load_2d(sb + H * (kBK * 2), &tmB1, kx, brow, fb);
+                    } else {
+                        tma_load_2d(sb, (BMD == B_SPLIT && second) ? &tmB1 : &tmB0, kx, brow, fb);
+                    }
+                }
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // Never leave while a copy into this CTA's shared memory is in flight.
+        if (lane == 0) {
+            for (int s = 0; s < S; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait(smem_u32(&full[s]), (issued_parity >> s) & 1u, abort_flag, args.err,
+                              lim, /*watch_abort=*/false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_m128(BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err, lim)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smA + stage * C::kABytes);
+                    const uint32_t sb = smem_u32(smB + stage * C::kBBytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma_bf16(d, sdesc_sw128(sa + k * 32), sdesc_sw128(sb + k * 32), idesc,
+                                    (kb | k) != 0 ? 1u : 0u);
+                    tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // All MMAs this thread issued must finish before TMEM is freed.
+            tc_commit(smem_u32(&drain[0]));
+            mbar_wait(smem_u32(&drain[0]), 0, abort_flag, args.err, lim, /*watch_abort=*/false);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;       // row of the tile held by this thread
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile ti = tile_at<GROUPED>(args, t, n_m);
+            // the whole warp must agree before the warp-collective tcgen05.ld
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err, lim)))
+                break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * kAccStride);
+            const bool rv = row < ti.nrows;
+            if (EPI == EPI_SITU_GLU) {
+                const float b1 = args.beta1, b2 = args.beta2;
+                const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
+                uint16_t *orow = reinterpret_cast<uint16_t *>(args.out) +
+                                 (int64_t)(ti.row0 + row) * args.ld_out + (int64_t)ti.nt * H;
+#pragma unroll 1
+                for (int c = 0; c < H; c += 32) {
+                    float p1[32], p2[32];
+                    tmem_ld32(taddr + c, p1);
+                    tmem_ld32(taddr + H + c, p2);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float g = b1 * tanhf(p1[j] * ib1) * sigmoid_f(p1[j]);
+                        const float l = b2 * tanhf(p2[j] * ib2);
+                        p1[j] = g * l;
+                    }
+                    if (rv) store_bf16_32(orow + c, p1, args.out_cols - (ti.nt * H + c));
+                }
+            } else {
+                int64_t orow_idx = ti.row0 + row;
+                float scale = 1.0f;
+                if (EPI == EPI_SCATTER_BF16 && rv) {
+                    orow_idx = args.scatter_rows[ti.row0 + row];
+                    scale = args.row_scale[orow_idx];
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);
+                    const int col = ti.nt * BN + c;
+                    if (!rv) continue;
+                    if (EPI == EPI_SIGMOID_F32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = sigmoid_f(v[j]);
+                        store_f32_32(reinterpret_cast<float *>(args.out) + orow_idx * args.ld_out + col,
+                                     v, args.out_cols - col);
+                    } else {
+                        if (EPI == EPI_SCATTER_BF16) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] *= scale;
+                        }
+                        store_bf16_32(reinterpret_cast<uint16_t *>(args.out) + orow_idx * args.ld_out + col,
+                                      v, args.out_cols - col);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int BN, int AM, int BMD, int EPI, bool GROUPED>
+cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t st) {
+    auto kern = gemm_kernel<BN, AM, BMD, EPI, GROUPED>;
+    const size_t smem = Cfg<BN>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, st>>>(m.a0, m.a1, m.b0, m.b1, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
+
+#define LMOE_GEMM_CASE(BN_, AM_, BM_, EPI_, G_)                                   \
+    if (bn == BN_ && am == AM_ && bm == BM_ && epi == EPI_ && grouped == G_)       \
+        return launch_one<BN_, AM_, BM_, EPI_, G_>(maps, args, grid, stream);
+
+cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
+                        const GemmArgs &args, int grid, cudaStream_t stream) {
+    // a1 down-projection, a8 up-projection + shared W3
+    LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_BF16, false)
+    LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_BF16, false)
+    LMOE_GEMM_CASE(256, A_SPLIT, B_SPLIT, EPI_BF16, false)
+    LMOE_GEMM_CASE(128, A_SPLIT, B_SPLIT, EPI_BF16, false)
+    // a8' shared experts W1|W2 with the SiTU-GLU epilogue
+    LMOE_GEMM_CASE(256, A_DENSE, B_GLU, EPI_SITU_GLU, false)
+    LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, false)
+    // a2 router scores
+    LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
+    // a5 routed experts W1|W2 (gathered rows) with the SiTU-GLU epilogue
+    LMOE_GEMM_CASE(256, A_GATHER, B_GLU, EPI_SITU_GLU, true)
+    LMOE_GEMM_CASE(128, A_GATHER, B_GLU, EPI_SITU_GLU, true)
+    // a6 routed experts W3 with the gate-weighted scatter
+    LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
+    LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
+    return cudaErrorInvalidValue;
+}
+
+#undef LMOE_GEMM_CASE
+
+}  // namespace lmoe

@@ -1,0 +1,78 @@
+// kernels.h -- internal interface between the C-ABI host code and the CUDA
+// kernels of liblmoe.so (not installed, not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmoe {
+
+// Device status bits written by kernels (see lmoe_device_status).
+constexpr unsigned kDevErrTimeout = 1u;
+
+// ------------------------------------------------------------------ GEMM
+// A operand source.
+enum AMode { A_DENSE = 0, A_GATHER = 1, A_SPLIT = 2 };
+// B operand source.
+enum BMode { B_PLAIN = 0, B_GLU = 1, B_SPLIT = 2 };
+// Epilogue.
+enum Epi { EPI_BF16 = 0, EPI_SITU_GLU = 1, EPI_SIGMOID_F32 = 2, EPI_SCATTER_BF16 = 3 };
+
+constexpr int kBM = 128;  // rows per tile (one tcgen05 M=128 tile)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzled row of bf16
+
+struct GemmMaps {
+    CUtensorMap a0, a1, b0, b1;
+};
+
+struct GemmArgs {
+    int32_t m_rows;          // dense: rows of A / output
+    int32_t m_tiles;         // dense: ceil(m_rows / 128)
+    int32_t n_tiles;         // tiles along N
+    int32_t k_blocks;        // ceil(K / 64)
+    int32_t k_split;         // A_SPLIT/B_SPLIT: k-blocks served by map 0
+    int32_t b_expert_rows;   // grouped: B-map rows per expert
+    const int4 *tiles;       // grouped: {expert, first permuted row, rows, 0}
+    const int32_t *n_mtiles; // grouped: number of entries in `tiles` (device)
+    const int32_t *gather_rows;   // A_GATHER: source row of A for each permuted row
+    void *out;               // output base
+    int64_t ld_out;          // output row stride (elements)
+    int32_t out_cols;        // output columns that exist (masking of ragged N)
+    const int32_t *scatter_rows;  // EPI_SCATTER_BF16: destination row per permuted row
+    const float *row_scale;       // EPI_SCATTER_BF16: scale per destination row
+    float beta1, beta2;
+    unsigned *err;           // device status word
+    uint64_t wait_limit_ns;  // bound on every mbarrier wait
+};
+
+// Launch one persistent GEMM.  `bn` in {128, 256}.  Returns cudaErrorInvalidValue
+// for a combination that is not compiled.
+cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
+                        const GemmArgs &args, int grid, cudaStream_t stream);
+size_t gemm_smem_bytes(int bn);
+
+// ------------------------------------------------------------------ routing
+cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E, int k,
+                        int32_t *idx, float *gate, uint32_t *bitmap, int words_per_expert,
+                        cudaStream_t stream);
+cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words_per_expert,
+                               uint32_t *word_prefix, int32_t *counts, cudaStream_t stream);
+cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
+                                 int32_t *n_mtiles, cudaStream_t stream);
+cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
+                           const uint32_t *word_prefix, int words_per_expert,
+                           const int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *tokrow,
+                           cudaStream_t stream);
+
+// ------------------------------------------------------------------ combine
+cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,
+                                   uint16_t *r, cudaStream_t stream);
+
+// ------------------------------------------------------------------ QB
+cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t ld, int B,
+                                uint32_t *hist, int accumulate, int num_sms, cudaStream_t stream);
+cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level, float *q,
+                               float *bias, cudaStream_t stream);
+
+}  // namespace lmoe

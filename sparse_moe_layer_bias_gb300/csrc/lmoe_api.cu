@@ -1,0 +1,496 @@
+// lmoe_api.cu -- host side of the C ABI declared in include/lmoe.h: argument
+// validation, workspace layout, TMA descriptors, and the launch sequence of
+// one Stable LatentMoE forward pass.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/lmoe.h"
+#include "kernels.h"
+
+using namespace lmoe;
+
+struct lmoe_handle {
+    lmoe_config cfg;
+    lmoe_weights w;
+    int device;
+    int num_sms;
+    unsigned *d_status;  // device status word (bounded-wait timeouts)
+    // Weight-side TMA descriptors, built once.
+    int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up;
+    CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
+    cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
+};
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder_ready() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// 2-D bf16 row-major [rows][cols] (row stride ld elements), box = 64 columns
+// (128 bytes, 128B swizzle) x box_rows rows.
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+              uint32_t box_rows) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, nmt, perm, inv, tokrow,
+        act, o, r, sact, total;
+};
+
+Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
+                      bool own_gates, bool own_counts) {
+    Layout l{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    const int64_t L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
+    const int64_t S = int64_t(c.n_shared) * c.shared_inter;
+    const int64_t words = ceil_div(T, 32);
+    const int64_t n = T * K;
+    const size_t none = SIZE_MAX;
+    l.h = take(size_t(T * L * 2));
+    l.scores = own_scores ? take(size_t(T * E * 4)) : none;
+    l.idx = own_idx ? take(size_t(n * 4)) : none;
+    l.gates = own_gates ? take(size_t(n * 4)) : none;
+    l.counts = own_counts ? take(size_t(E * 4)) : none;
+    l.offsets = take(size_t((E + 1) * 4));
+    l.bitmap = take(size_t(E * words * 4));
+    l.wprefix = take(size_t(E * words * 4));
+    l.tiles = take(size_t((ceil_div(n, kBM) + E) * 16));
+    l.nmt = take(16);
+    l.perm = take(size_t(n * 4));
+    l.inv = take(size_t(n * 4));
+    l.tokrow = take(size_t(n * 4));
+    l.act = take(size_t(n * I * 2));
+    l.o = take(size_t(n * L * 2));
+    l.r = take(size_t(T * L * 2));
+    l.sact = take(size_t(T * S * 2));
+    l.total = off;
+    return l;
+}
+
+int validate_config(const lmoe_config *c) {
+    if (!c) return LMOE_ERR_INVALID_ARG;
+    if (c->d <= 0 || c->latent <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->inter <= 0 ||
+        c->n_shared <= 0 || c->shared_inter <= 0 || c->max_tokens < 0)
+        return LMOE_ERR_INVALID_ARG;
+    if (!(c->beta1 > 0.0f) || !(c->beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
+    const int64_t S = int64_t(c->n_shared) * c->shared_inter;
+    if (c->d % 64 || c->latent % 64 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->latent > 8192 || c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024)
+        return LMOE_ERR_UNSUPPORTED_SHAPE;
+    // 32-bit row coordinates of the TMA descriptors and permuted-row indices
+    if (int64_t(c->n_experts) * c->latent >= (int64_t(1) << 31) ||
+        int64_t(c->n_experts) * c->inter >= (int64_t(1) << 31) ||
+        c->max_tokens * c->top_k >= (int64_t(1) << 31))
+        return LMOE_ERR_UNSUPPORTED_SHAPE;
+    return LMOE_OK;
+}
+
+int check_device(int *dev, int *sms) {
+    if (cudaGetDevice(dev) != cudaSuccess) return LMOE_ERR_NO_DEVICE;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess)
+        return LMOE_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return LMOE_ERR_NO_DEVICE;
+    return LMOE_OK;
+}
+
+GemmArgs base_args(const lmoe_handle *h) {
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.beta1 = h->cfg.beta1;
+    a.beta2 = h->cfg.beta2;
+    a.err = h->d_status;
+    a.wait_limit_ns = kWaitLimitNs;
+    return a;
+}
+
+int gemm_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *lmoe_status_string(int s) {
+    switch (s) {
+        case LMOE_OK: return "LMOE_OK";
+        case LMOE_ERR_INVALID_ARG: return "LMOE_ERR_INVALID_ARG";
+        case LMOE_ERR_UNSUPPORTED_SHAPE: return "LMOE_ERR_UNSUPPORTED_SHAPE";
+        case LMOE_ERR_ALIGNMENT: return "LMOE_ERR_ALIGNMENT";
+        case LMOE_ERR_WORKSPACE: return "LMOE_ERR_WORKSPACE";
+        case LMOE_ERR_CUDA: return "LMOE_ERR_CUDA";
+        case LMOE_ERR_TIMEOUT: return "LMOE_ERR_TIMEOUT";
+        case LMOE_ERR_NO_DEVICE: return "LMOE_ERR_NO_DEVICE";
+        default: return "LMOE_ERR_UNKNOWN";
+    }
+}
+
+int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out) {
+    if (!out) return LMOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    int st = validate_config(cfg);
+    if (st) return st;
+    if (!w || !w->w_down || !w->w_router || !w->w1 || !w->w2 || !w->w3 || !w->ws1 || !w->ws2 ||
+        !w->ws3 || !w->w_up)
+        return LMOE_ERR_INVALID_ARG;
+    const void *ptrs[] = {w->w_down, w->w_router, w->w1, w->w2, w->w3, w->ws1, w->ws2, w->ws3, w->w_up};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return LMOE_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    st = check_device(&dev, &sms);
+    if (st) return st;
+    if (!encoder_ready()) return LMOE_ERR_CUDA;
+
+    lmoe_handle *h = new (std::nothrow) lmoe_handle;
+    if (!h) return LMOE_ERR_CUDA;
+    std::memset(h, 0, sizeof *h);
+    h->cfg = *cfg;
+    h->w = *w;
+    h->device = dev;
+    h->num_sms = sms;
+    const lmoe_config &c = h->cfg;
+    const uint64_t d = c.d, L = c.latent, E = c.n_experts, I = c.inter;
+    const uint64_t S = uint64_t(c.n_shared) * c.shared_inter;
+    h->bn_down = (L % 256 == 0) ? 256 : 128;
+    h->bn_shared = (S % 128 == 0) ? 256 : 128;
+    h->bn_exp1 = (I % 128 == 0) ? 256 : 128;
+    h->bn_exp3 = (L % 256 == 0) ? 256 : 128;
+    h->bn_up = (d % 256 == 0) ? 256 : 128;
+    bool ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->bn_down) &&
+              make_map(&h->m_wrouter, w->w_router, E, L, L, 128) &&
+              make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
+              make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
+              make_map(&h->m_w1, w->w1, E * I, L, L, h->bn_exp1 / 2) &&
+              make_map(&h->m_w2, w->w2, E * I, L, L, h->bn_exp1 / 2) &&
+              make_map(&h->m_w3, w->w3, E * L, I, I, h->bn_exp3) &&
+              make_map(&h->m_wup, w->w_up, d, L, L, h->bn_up) &&
+              make_map(&h->m_ws3, w->ws3, d, S, S, h->bn_up);
+    if (!ok) {
+        delete h;
+        return LMOE_ERR_CUDA;
+    }
+    if (cudaMalloc(&h->d_status, 256) != cudaSuccess) {
+        delete h;
+        return LMOE_ERR_CUDA;
+    }
+    if (cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
+        cudaFree(h->d_status);
+        delete h;
+        return LMOE_ERR_CUDA;
+    }
+    *out = h;
+    return LMOE_OK;
+}
+
+int lmoe_destroy(lmoe_handle *h) {
+    if (!h) return LMOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t f = cudaFree(h->d_status);
+    delete h;
+    return (e == cudaSuccess && f == cudaSuccess) ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+int lmoe_workspace_size(const lmoe_handle *h, int64_t T, size_t *bytes) {
+    if (!h || !bytes || T < 0) return LMOE_ERR_INVALID_ARG;
+    if (T > h->cfg.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    *bytes = compute_layout(h->cfg, T, true, true, true, true).total;
+    return LMOE_OK;
+}
+
+int lmoe_workspace_layout(const lmoe_handle *h, int64_t T, lmoe_ws_layout *out) {
+    if (!h || !out || T < 0) return LMOE_ERR_INVALID_ARG;
+    if (T > h->cfg.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    const Layout l = compute_layout(h->cfg, T, true, true, true, true);
+    out->h = int64_t(l.h);
+    out->scores = int64_t(l.scores);
+    out->topk_idx = int64_t(l.idx);
+    out->gates = int64_t(l.gates);
+    out->counts = int64_t(l.counts);
+    out->offsets = int64_t(l.offsets);
+    out->perm = int64_t(l.perm);
+    out->inv = int64_t(l.inv);
+    out->act = int64_t(l.act);
+    out->o = int64_t(l.o);
+    out->r = int64_t(l.r);
+    out->shared_act = int64_t(l.sact);
+    return LMOE_OK;
+}
+
+int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias, uint16_t *y,
+                 float *scores_out, int32_t *topk_idx_out, float *gates_out,
+                 int32_t *expert_counts_out, void *workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
+    if (!h || T < 0) return LMOE_ERR_INVALID_ARG;
+    const lmoe_config &c = h->cfg;
+    if (T > c.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return LMOE_OK;
+    if (!x || !bias || !y || !workspace) return LMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(bias) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) || (scores_out && !aligned16(scores_out)) ||
+        (topk_idx_out && !aligned16(topk_idx_out)) || (gates_out && !aligned16(gates_out)) ||
+        (expert_counts_out && !aligned16(expert_counts_out)))
+        return LMOE_ERR_ALIGNMENT;
+    // The workspace is sized for every intermediate; caller-provided outputs
+    // simply leave their slot unused, so the documented offsets never move.
+    const Layout l = compute_layout(c, T, true, true, true, true);
+    if (workspace_bytes < l.total) return LMOE_ERR_WORKSPACE;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t d = c.d, L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
+    const int64_t S = int64_t(c.n_shared) * c.shared_inter;
+    const int64_t n = T * K;
+    const int words = static_cast<int>(ceil_div(T, 32));
+    uint16_t *hbuf = reinterpret_cast<uint16_t *>(ws + l.h);
+    float *scores = scores_out ? scores_out : reinterpret_cast<float *>(ws + l.scores);
+    int32_t *idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t *>(ws + l.idx);
+    float *gates = gates_out ? gates_out : reinterpret_cast<float *>(ws + l.gates);
+    int32_t *counts = expert_counts_out ? expert_counts_out : reinterpret_cast<int32_t *>(ws + l.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + l.offsets);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(ws + l.bitmap);
+    uint32_t *wprefix = reinterpret_cast<uint32_t *>(ws + l.wprefix);
+    int4 *tiles = reinterpret_cast<int4 *>(ws + l.tiles);
+    int32_t *nmt = reinterpret_cast<int32_t *>(ws + l.nmt);
+    int32_t *perm = reinterpret_cast<int32_t *>(ws + l.perm);
+    int32_t *inv = reinterpret_cast<int32_t *>(ws + l.inv);
+    int32_t *tokrow = reinterpret_cast<int32_t *>(ws + l.tokrow);
+    uint16_t *act = reinterpret_cast<uint16_t *>(ws + l.act);
+    uint16_t *obuf = reinterpret_cast<uint16_t *>(ws + l.o);
+    uint16_t *rbuf = reinterpret_cast<uint16_t *>(ws + l.r);
+    uint16_t *sact = reinterpret_cast<uint16_t *>(ws + l.sact);
+
+    // Activation-side TMA descriptors for this T and workspace.
+    CUtensorMap m_x, m_h, m_hg, m_act, m_r, m_sact;
+    if (!make_map(&m_x, x, T, d, d, kBM) || !make_map(&m_h, hbuf, T, L, L, kBM) ||
+        !make_map(&m_hg, hbuf, T, L, L, 1) || !make_map(&m_act, act, n, I, I, kBM) ||
+        !make_map(&m_r, rbuf, T, L, L, kBM) || !make_map(&m_sact, sact, T, S, S, kBM))
+        return LMOE_ERR_CUDA;
+
+    const int m_tiles = static_cast<int>(ceil_div(T, kBM));
+    auto mark = [&](int stage) {
+        if (h->stage_events) cudaEventRecord(h->stage_events[stage], stream);
+    };
+    auto grid_for = [&](int64_t tiles_) {
+        return static_cast<int>(tiles_ < h->num_sms ? tiles_ : h->num_sms);
+    };
+    int st;
+
+    if (cudaMemsetAsync(bitmap, 0, size_t(E) * words * 4, stream) != cudaSuccess) return LMOE_ERR_CUDA;
+
+    mark(LMOE_STAGE_DOWN);
+    {   // a1: h = x W_down^T
+        GemmMaps m{m_x, m_x, h->m_wdown, h->m_wdown};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
+        a.k_blocks = static_cast<int32_t>(d / kBK);
+        a.out = hbuf;
+        a.ld_out = L;
+        a.out_cols = static_cast<int32_t>(L);
+        st = gemm_status(launch_gemm(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    mark(LMOE_STAGE_SHARED);
+    {   // a8': shared experts, act_s = SiTU(x Ws1^T) * softcap(x Ws2^T)
+        GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(S / (h->bn_shared / 2));
+        a.k_blocks = static_cast<int32_t>(d / kBK);
+        a.out = sact;
+        a.ld_out = S;
+        a.out_cols = static_cast<int32_t>(S);
+        st = gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    mark(LMOE_STAGE_ROUTER);
+    {   // a2: s = sigmoid(h W_router^T), fp32
+        GemmMaps m{m_h, m_h, h->m_wrouter, h->m_wrouter};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(ceil_div(E, 128));
+        a.k_blocks = static_cast<int32_t>(L / kBK);
+        a.out = scores;
+        a.ld_out = E;
+        a.out_cols = static_cast<int32_t>(E);
+        st = gemm_status(launch_gemm(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    // a3 + a4: biased top-k, then the stable grouping of assignments by expert
+    mark(LMOE_STAGE_TOPK);
+    if (launch_topk(scores, bias, T, static_cast<int>(E), static_cast<int>(K), idx, gates, bitmap,
+                    words, stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    mark(LMOE_STAGE_SCAN);
+    if (launch_expert_scan(bitmap, static_cast<int>(E), words, wprefix, counts, stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    mark(LMOE_STAGE_OFFSETS);
+    if (launch_offsets_tiles(counts, static_cast<int>(E), offsets, tiles, nmt, stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    mark(LMOE_STAGE_SCATTER);
+    if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
+                       stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    mark(LMOE_STAGE_EXPERT_W12);
+    {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the gathered rows of each expert
+        GemmMaps m{m_hg, m_hg, h->m_w1, h->m_w2};
+        GemmArgs a = base_args(h);
+        a.n_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
+        a.k_blocks = static_cast<int32_t>(L / kBK);
+        a.b_expert_rows = static_cast<int32_t>(I);
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
+        a.gather_rows = tokrow;
+        a.out = act;
+        a.ld_out = I;
+        a.out_cols = static_cast<int32_t>(I);
+        const int64_t max_tiles = (ceil_div(n, kBM) + E) * a.n_tiles;
+        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
+                                     grid_for(max_tiles), stream));
+        if (st) return st;
+    }
+    mark(LMOE_STAGE_EXPERT_W3);
+    {   // a6: o[a] = gate[a] * W3[e] act, written back in assignment order
+        GemmMaps m{m_act, m_act, h->m_w3, h->m_w3};
+        GemmArgs a = base_args(h);
+        a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_exp3));
+        a.k_blocks = static_cast<int32_t>(I / kBK);
+        a.b_expert_rows = static_cast<int32_t>(L);
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
+        a.out = obuf;
+        a.ld_out = L;
+        a.out_cols = static_cast<int32_t>(L);
+        a.scatter_rows = perm;
+        a.row_scale = gates;
+        const int64_t max_tiles = (ceil_div(n, kBM) + E) * a.n_tiles;
+        st = gemm_status(launch_gemm(h->bn_exp3, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true, m, a,
+                                     grid_for(max_tiles), stream));
+        if (st) return st;
+    }
+    mark(LMOE_STAGE_COMBINE);
+    // a7: z = sum of the token's gate-weighted expert rows; r = RMSNorm(z)
+    if (launch_combine_rmsnorm(obuf, T, static_cast<int>(K), static_cast<int>(L), c.rms_eps, rbuf,
+                               stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    mark(LMOE_STAGE_UP);
+    {   // a8: y = r W_up^T + act_s Ws3^T  (one GEMM, K split over the two sources)
+        GemmMaps m{m_r, m_sact, h->m_wup, h->m_ws3};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(ceil_div(d, h->bn_up));
+        a.k_split = static_cast<int32_t>(L / kBK);
+        a.k_blocks = static_cast<int32_t>((L + S) / kBK);
+        a.out = y;
+        a.ld_out = d;
+        a.out_cols = static_cast<int32_t>(d);
+        st = gemm_status(launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    mark(LMOE_NUM_STAGES);
+    return LMOE_OK;
+}
+
+int lmoe_set_stage_events(lmoe_handle *h, cudaEvent_t *events, int n_events) {
+    if (!h) return LMOE_ERR_INVALID_ARG;
+    if (!events) {
+        if (n_events != 0) return LMOE_ERR_INVALID_ARG;
+        h->stage_events = nullptr;
+        return LMOE_OK;
+    }
+    if (n_events != LMOE_NUM_STAGES + 1) return LMOE_ERR_INVALID_ARG;
+    h->stage_events = events;
+    return LMOE_OK;
+}
+
+int lmoe_device_status(lmoe_handle *h, cudaStream_t stream, int clear, int *device_status) {
+    if (!h || !device_status) return LMOE_ERR_INVALID_ARG;
+    unsigned v = 0;
+    if (cudaMemcpyAsync(&v, h->d_status, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    if (clear && v) {
+        if (cudaMemsetAsync(h->d_status, 0, sizeof v, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return LMOE_ERR_CUDA;
+    }
+    *device_status = (v & kDevErrTimeout) ? LMOE_ERR_TIMEOUT : LMOE_OK;
+    return LMOE_OK;
+}
+
+int qb_histogram(const float *scores, int64_t T, int32_t E, int64_t ld, int32_t B, uint32_t *hist,
+                 int accumulate, cudaStream_t stream) {
+    if (T < 0 || E < 1 || ld < E || B < 1 || B > 65536 || !hist || (T > 0 && !scores) ||
+        (accumulate != 0 && accumulate != 1))
+        return LMOE_ERR_INVALID_ARG;
+    if (!aligned16(hist) || (scores && !aligned16(scores))) return LMOE_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    int st = check_device(&dev, &sms);
+    if (st) return st;
+    return launch_qb_histogram(scores, T, E, ld, B, hist, accumulate, sms, stream) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+}
+
+int qb_quantile_bias(const uint32_t *hist, int32_t E, int32_t B, double level, float *quantile_out,
+                     float *bias_out, cudaStream_t stream) {
+    if (!hist || !bias_out || E < 1 || B < 1 || B > 65536 || !(level >= 0.0 && level <= 1.0))
+        return LMOE_ERR_INVALID_ARG;
+    if (!aligned16(hist) || !aligned16(bias_out) || (quantile_out && !aligned16(quantile_out)))
+        return LMOE_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    int st = check_device(&dev, &sms);
+    if (st) return st;
+    return launch_qb_quantile(hist, E, B, level, quantile_out, bias_out, stream) == cudaSuccess
+               ? LMOE_OK
+               : LMOE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,236 @@
+// qb.cu -- Quantile Balancing: per-expert B-bin histogram of router scores
+// and the quantile read that sets each expert's selection bias.
+// ("Kimi-K3-Architecture-Deep-Dive" section 3: map scores into [0,1], keep a
+// local B-bin histogram, histograms are additive so one all-reduce of the
+// counts rebuilds the global distribution, 1000 bins suffice; "Inside K3"
+// section "Quantile Balancing (QB)": read the quantile from that histogram;
+// news write-up "Keeping the numbers in range": solve for each expert's
+// threshold directly.)
+//
+// Histogram layout on the GPU: CTA (expert group g, token chunk c) owns the
+// counters of EPC consecutive experts in shared memory, streams its chunk of
+// rows with 16-byte loads (EPC = 32 -> each row segment is one 128-byte line),
+// counts with shared-memory atomics, and adds its non-zero counters into the
+// global histogram at the end.  The global adds are the on-chip analogue of
+// the cross-node all-reduce.
+#include "kernels.h"
+
+namespace lmoe {
+
+namespace {
+
+constexpr int kHistThreads = 1024;
+constexpr size_t kHistSmemBudget = 200 * 1024;
+
+__device__ __forceinline__ int bin_of(float s, float fB, int B) {
+    const float f = floorf(__fmul_rn(s, fB));  // one fp32 rounding, then floor
+    // s < 1/B (and NaN) -> bin 0; large values clamp to B-1
+    return (f >= 1.0f) ? min(static_cast<int>(fminf(f, 2147483520.0f)), B - 1) : 0;
+}
+
+// Vector path: E % 4 == 0, ld % 4 == 0, 16-byte aligned rows; EPC in {4..32}.
+template <int EPC>
+__global__ void __launch_bounds__(kHistThreads)
+    qb_hist_vec_kernel(const float *__restrict__ s, int64_t T, int E, int64_t ld, int B,
+                       uint32_t *__restrict__ hist, int n_groups, int64_t rows_per_chunk) {
+    extern __shared__ uint32_t cnt[];  // [EPC][B]
+    constexpr int NQ = EPC / 4;                 // float4 per row segment
+    constexpr int ROWS = kHistThreads / NQ;     // rows per sweep
+    constexpr int U = 4;                        // sweeps in flight
+    const int g = blockIdx.x % n_groups;
+    const int64_t chunk = blockIdx.x / n_groups;
+    const int e0 = g * EPC;
+    const int ne = min(EPC, E - e0);
+    const int64_t r_begin = chunk * rows_per_chunk;
+    const int64_t r_end = min(T, r_begin + rows_per_chunk);
+    for (int i = threadIdx.x; i < ne * B; i += kHistThreads) cnt[i] = 0u;
+    __syncthreads();
+
+    const float fB = static_cast<float>(B);
+    const int q = threadIdx.x % NQ;
+    const int rl = threadIdx.x / NQ;
+    const bool qv = 4 * q < ne;
+    const float *col = s + e0 + 4 * q;
+    for (int64_t r0 = r_begin; r0 < r_end; r0 += int64_t(ROWS) * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = r0 + int64_t(u) * ROWS + rl;
+            v[u] = (qv && row < r_end) ? __ldcs(reinterpret_cast<const float4 *>(col + row * ld))
+                                       : make_float4(-1.f, -1.f, -1.f, -1.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = r0 + int64_t(u) * ROWS + rl;
+            if (!(qv && row < r_end)) continue;
+            const int c = 4 * q;
+            atomicAdd(&cnt[(c + 0) * B + bin_of(v[u].x, fB, B)], 1u);
+            atomicAdd(&cnt[(c + 1) * B + bin_of(v[u].y, fB, B)], 1u);
+            atomicAdd(&cnt[(c + 2) * B + bin_of(v[u].z, fB, B)], 1u);
+            atomicAdd(&cnt[(c + 3) * B + bin_of(v[u].w, fB, B)], 1u);
+        }
+    }
+    __syncthreads();
+    uint32_t *dst = hist + int64_t(e0) * B;
+    for (int i = threadIdx.x; i < ne * B; i += kHistThreads) {
+        const uint32_t c = cnt[i];
+        if (c) atomicAdd(&dst[i], c);
+    }
+}
+
+// Scalar path for any E / ld / alignment.
+__global__ void __launch_bounds__(kHistThreads)
+    qb_hist_scalar_kernel(const float *__restrict__ s, int64_t T, int E, int64_t ld, int B,
+                          uint32_t *__restrict__ hist, int epc, int n_groups,
+                          int64_t rows_per_chunk) {
+    extern __shared__ uint32_t cnt[];
+    const int g = blockIdx.x % n_groups;
+    const int64_t chunk = blockIdx.x / n_groups;
+    const int e0 = g * epc;
+    const int ne = min(epc, E - e0);
+    const int64_t r_begin = chunk * rows_per_chunk;
+    const int64_t r_end = min(T, r_begin + rows_per_chunk);
+    for (int i = threadIdx.x; i < ne * B; i += kHistThreads) cnt[i] = 0u;
+    __syncthreads();
+    const float fB = static_cast<float>(B);
+    const int64_t n = (r_end - r_begin) * ne;
+    for (int64_t i = threadIdx.x; i < n; i += kHistThreads) {
+        const int64_t row = r_begin + i / ne;
+        const int c = static_cast<int>(i % ne);
+        atomicAdd(&cnt[c * B + bin_of(s[row * ld + e0 + c], fB, B)], 1u);
+    }
+    __syncthreads();
+    uint32_t *dst = hist + int64_t(e0) * B;
+    for (int i = threadIdx.x; i < ne * B; i += kHistThreads) {
+        const uint32_t c = cnt[i];
+        if (c) atomicAdd(&dst[i], c);
+    }
+}
+
+// Bins too many for shared memory: count straight into the global histogram.
+__global__ void qb_hist_global_kernel(const float *__restrict__ s, int64_t T, int E, int64_t ld,
+                                      int B, uint32_t *__restrict__ hist) {
+    const float fB = static_cast<float>(B);
+    const int64_t n = T * E;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t row = i / E;
+        const int c = static_cast<int>(i % E);
+        atomicAdd(&hist[int64_t(c) * B + bin_of(s[row * ld + c], fB, B)], 1u);
+    }
+}
+
+// One warp per expert: N, the rank r, the first bin whose cumulative count
+// reaches r, and the in-bin linear interpolation, all in fp64.
+__global__ void qb_quantile_kernel(const uint32_t *__restrict__ hist, int E, int B, double level,
+                                   float *__restrict__ q_out, float *__restrict__ b_out) {
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (e >= E) return;
+    const uint32_t *row = hist + int64_t(e) * B;
+    unsigned long long n = 0;
+    for (int j = lane; j < B; j += 32) n += row[j];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    double q = 0.0;
+    if (n > 0) {
+        double rr = ceil(level * static_cast<double>(n));
+        if (rr < 1.0) rr = 1.0;
+        if (rr > static_cast<double>(n)) rr = static_cast<double>(n);
+        const unsigned long long r = static_cast<unsigned long long>(rr);
+        unsigned long long below = 0;  // cumulative count before this chunk
+        for (int j0 = 0; j0 < B; j0 += 32) {
+            const int j = j0 + lane;
+            const unsigned long long c = (j < B) ? row[j] : 0ull;
+            unsigned long long incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const unsigned ballot = __ballot_sync(0xffffffffu, j < B && below + incl >= r);
+            if (ballot) {
+                const int f = __ffs(ballot) - 1;
+                const unsigned long long cf = __shfl_sync(0xffffffffu, c, f);
+                const unsigned long long inf = __shfl_sync(0xffffffffu, incl, f);
+                const unsigned long long before = below + inf - cf;  // C_{j*-1}
+                q = (static_cast<double>(j0 + f) +
+                     static_cast<double>(r - before) / static_cast<double>(cf)) /
+                    static_cast<double>(B);
+                break;
+            }
+            below += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    if (lane == 0) {
+        if (q_out) q_out[e] = static_cast<float>(q);
+        b_out[e] = static_cast<float>(-q);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t ld, int B,
+                                uint32_t *hist, int accumulate, int num_sms, cudaStream_t st) {
+    cudaError_t err;
+    if (!accumulate) {
+        err = cudaMemsetAsync(hist, 0, size_t(E) * size_t(B) * sizeof(uint32_t), st);
+        if (err != cudaSuccess) return err;
+    }
+    if (T == 0) return cudaSuccess;
+    const size_t per_expert = size_t(B) * sizeof(uint32_t);
+    if (per_expert > kHistSmemBudget) {
+        qb_hist_global_kernel<<<num_sms * 4, 512, 0, st>>>(scores, T, E, ld, B, hist);
+        return cudaGetLastError();
+    }
+    int epc = 32;
+    while (epc > 1 && size_t(epc) * per_expert > kHistSmemBudget) epc >>= 1;
+    const bool vec = epc >= 4 && (E % 4 == 0) && (ld % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
+    const int n_groups = (E + epc - 1) / epc;
+    const size_t smem = size_t(epc) * per_expert;
+    const int ctas_per_sm = max(1, min(2, static_cast<int>((227 * 1024) / (smem + 1024))));
+    int n_chunks = max(1, (num_sms * ctas_per_sm) / n_groups);
+    const int64_t min_rows = 512;
+    const int64_t max_chunks = (T + min_rows - 1) / min_rows;
+    if (n_chunks > max_chunks) n_chunks = static_cast<int>(max_chunks);
+    n_chunks = max(n_chunks, 1);
+    const int64_t rows_per_chunk = (T + n_chunks - 1) / n_chunks;
+    const unsigned grid = static_cast<unsigned>(n_groups) * static_cast<unsigned>(n_chunks);
+
+#define LMOE_QB_VEC(N_)                                                                       \
+    case N_:                                                                                  \
+        err = cudaFuncSetAttribute(qb_hist_vec_kernel<N_>,                                    \
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);   \
+        if (err != cudaSuccess) return err;                                                   \
+        qb_hist_vec_kernel<N_><<<grid, kHistThreads, smem, st>>>(scores, T, E, ld, B, hist,    \
+                                                                 n_groups, rows_per_chunk);   \
+        break;
+    if (vec) {
+        switch (epc) {
+            LMOE_QB_VEC(4)
+            LMOE_QB_VEC(8)
+            LMOE_QB_VEC(16)
+            LMOE_QB_VEC(32)
+            default:
+                return cudaErrorInvalidValue;
+        }
+    } else {
+        err = cudaFuncSetAttribute(qb_hist_scalar_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem);
+        if (err != cudaSuccess) return err;
+        qb_hist_scalar_kernel<<<grid, kHistThreads, smem, st>>>(scores, T, E, ld, B, hist, epc,
+                                                               n_groups, rows_per_chunk);
+    }
+#undef LMOE_QB_VEC
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level, float *q,
+                               float *bias, cudaStream_t st) {
+    const int wpb = 8;
+    qb_quantile_kernel<<<(E + wpb - 1) / wpb, wpb * 32, 0, st>>>(hist, E, B, level, q, bias);
+    return cudaGetLastError();
+}
+
+}  // namespace lmoe

@@ -1,0 +1,80 @@
+"""Shared helpers for the GPU-vs-oracle parity tests (test infrastructure)."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from sparse_moe_layer_bias_gb300 import synth
+
+# Tolerances (floating point).  The layer output bar is the one the method
+# targets: rel. Frobenius <= 1e-2 and max-abs <= 5e-2 * RMS over tokens whose
+# k-th/(k+1)-th biased-score margin exceeds 1e-4.
+Y_REL_FRO = 1e-2
+Y_MAX_ABS_RMS = 5e-2
+MARGIN = 1e-4
+# fp32 accumulation: a bf16 result of a K-long dot product may differ from the
+# nearest bf16 of the exact value by one ulp plus the accumulation error, which
+# under cancellation is bounded by a small multiple of 2^-24 * sum|x_i w_i|.
+ACC_REL = 2.0 ** -20
+# Router scores from the same bf16 latent: the logit carries the accumulation
+# error ACC_REL * sum|h_l w_l|, scaled by the sigmoid's slope s(1-s), plus a
+# few fp32 ulps from evaluating the sigmoid itself.
+S_EVAL = 1e-6
+
+
+def score_tol(s, absum):
+    s = s.astype(np.float64)
+    return s * (1.0 - s) * ACC_REL * absum + S_EVAL
+
+
+def dec(bits):
+    return synth.from_bits(np.asarray(bits)).double().numpy()
+
+
+def ulp_bf16(v):
+    """Spacing of bf16 numbers at |v| (normal range)."""
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def ws_view(ws: torch.Tensor, layout: dict, key: str, dtype, shape):
+    off = layout[key]
+    assert off >= 0
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    return ws[off:off + n].view(dtype).view(*shape)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return synth.bits(t.cpu())
+
+
+def rel_fro(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def check_layer_output(y_gpu_bf16: torch.Tensor, y_ref: np.ndarray, margin: np.ndarray):
+    """The acceptance test on the layer output; returns (rel_fro, max_abs/rms, kept).
+
+    The layer's output is bf16, so rounding it costs up to half a bf16 ulp of
+    |y| by itself; on the x50 outlier tokens |y| reaches ~40x RMS(out), where
+    that alone is ~10% of RMS.  The max-abs bar is therefore applied to the
+    error beyond the output's own rounding: max(0, |dy| - ulp(y_ref)/2)."""
+    yg = y_gpu_bf16.float().cpu().numpy().astype(np.float64)
+    keep = margin > MARGIN
+    assert keep.sum() > 0
+    d = np.abs(yg - y_ref)[keep]
+    ref = y_ref[keep]
+    rf = rel_fro(yg[keep], ref)
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    beyond = np.maximum(0.0, d - 0.5 * ulp_bf16(ref))
+    mx = float(np.max(beyond)) / rms
+    assert rf <= Y_REL_FRO, f"rel Frobenius {rf:.3e}"
+    assert mx <= Y_MAX_ABS_RMS, f"max abs / RMS {mx:.3e}"
+    return rf, mx, int(keep.sum())
+
+
+def oracle_cfg(shape: synth.LayerShape) -> oracle.LayerConfig:
+    return oracle.LayerConfig(**shape.layer_dict())

@@ -1,0 +1,47 @@
+"""The C-ABI library loads and exports every entry point include/lmoe.h
+declares (no compute: this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:lmoe|qb)_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    from sparse_moe_layer_bias_gb300 import build, binding
+    lib_path = build.build()
+    lib = ctypes.CDLL(lib_path)
+    names = declared_functions()
+    assert {"lmoe_create", "lmoe_forward", "lmoe_destroy", "qb_histogram", "qb_quantile_bias"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding.EXPORTED) == names
+
+
+def test_status_strings_without_gpu():
+    import sparse_moe_layer_bias_gb300 as lm
+    from sparse_moe_layer_bias_gb300 import build
+    build.build()
+    assert lm.lmoe_status_string(0) == "LMOE_OK"
+    assert lm.lmoe_status_string(4) == "LMOE_ERR_WORKSPACE"
+    assert lm.lmoe_status_string(99) == "LMOE_ERR_UNKNOWN"
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_moe_layer_bias_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "lmoe_oracle" not in text, f

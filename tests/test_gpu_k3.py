@@ -1,0 +1,143 @@
+"""K3-shape layers (d=7168, latent 3584, 896 experts, top-16, 2 shared experts
+of 1024, routed intermediate 512) through the C ABI, in the launch
+configuration the benchmark times.
+
+At these sizes the oracle runs on every token for the discrete steps (top-k
+and the permutation, bit-exact) and on a sample of tokens for the float steps;
+the layer is token-independent, so a sampled token's oracle forward is exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_moe_layer_bias_gb300 import synth
+
+from layer_check import (ACC_REL, check_layer_output, score_tol, dec, host_bits, oracle_cfg, rel_fro,
+                         ulp_bf16, ws_view)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_moe_layer_bias_gb300 as m
+    m.load_library()
+    return m
+
+
+def expert_bits(w, e):
+    return {n: synth.bits(w[n][e]) for n in ("w1", "w2", "w3")}
+
+
+def run_k3(lm, shape):
+    torch.manual_seed(0)
+    w = synth.layer_weights_device(shape)
+    x, bias = synth.activations_device(shape)
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
+    ws = lm.alloc_workspace(h, shape.T)
+    y = lm.lmoe_forward(h, x, bias, workspace=ws)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    return dict(h=h, ws=ws, lay=lm.lmoe_workspace_layout(h, shape.T), y=y, x=x, bias=bias, w=w)
+
+
+def check_k3(shape, run, sample):
+    cfg = oracle_cfg(shape)
+    T, E, K, L, I = shape.T, shape.n_experts, shape.top_k, shape.latent, shape.inter
+    S = shape.n_shared * shape.shared_inter
+    ws, lay, w = run["ws"], run["lay"], run["w"]
+    bias = run["bias"].cpu().numpy()
+
+    # a3/a4 on every token: bit-exact against the oracle on the GPU's own scores/idx
+    s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, E)).cpu().numpy()
+    idx_gpu = ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).cpu().numpy()
+    g_gpu = ws_view(ws, lay, "gates", torch.float32, (T, K)).cpu().numpy()
+    idx_ref, g_ref, _ = oracle.topk(cfg, s_gpu, bias)
+    assert np.array_equal(idx_gpu, idx_ref)
+    assert np.array_equal(g_gpu, g_ref)
+    counts, offsets, perm, inv = oracle.permute(cfg, idx_gpu)
+    assert np.array_equal(ws_view(ws, lay, "counts", torch.int32, (E,)).cpu().numpy(), counts)
+    assert np.array_equal(ws_view(ws, lay, "offsets", torch.int32, (E + 1,)).cpu().numpy(), offsets)
+    assert np.array_equal(ws_view(ws, lay, "perm", torch.int32, (T * K,)).cpu().numpy(), perm)
+    assert np.array_equal(ws_view(ws, lay, "inv", torch.int32, (T * K,)).cpu().numpy(), inv)
+
+    # float stages on sampled tokens, each fed the GPU's own inputs
+    sm = np.asarray(sample)
+    xb = host_bits(run["x"][torch.from_numpy(sm).cuda()])
+    wd = synth.bits(w["w_down"])
+    X, Wd = dec(xb), dec(wd)
+    exact_h = X @ Wd.T
+    h_all = ws_view(ws, lay, "h", torch.bfloat16, (T, L))
+    h_gpu = host_bits(h_all[torch.from_numpy(sm).cuda()])
+    assert np.all(np.abs(dec(h_gpu) - exact_h) <= ulp_bf16(exact_h) + ACC_REL * (np.abs(X) @ np.abs(Wd).T))
+    wr = synth.bits(w["w_router"])
+    s_ref = oracle.router(cfg, h_gpu, wr)
+    absum_s = np.abs(dec(h_gpu)) @ np.abs(dec(wr)).T
+    assert np.all(np.abs(s_gpu[sm] - s_ref) <= score_tol(s_ref, absum_s))
+
+    used = np.unique(idx_gpu[sm])
+    we = {n: {int(e): synth.bits(w[n][int(e)]) for e in used} for n in ("w1", "w2", "w3")}
+    rt = oracle.routed(cfg, h_gpu, idx_gpu[sm], g_gpu[sm], we["w1"], we["w2"], we["w3"], want_act=True,
+                       want_o=True)
+    rows = (sm[:, None] * K + np.arange(K)[None, :]).reshape(-1)       # assignment ids
+    prow = inv[rows]                                                    # their permuted rows
+    act_all = ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))
+    act_gpu = dec(host_bits(act_all[torch.from_numpy(prow).cuda()]))
+    assert rel_fro(act_gpu, dec(rt["act"])) <= 5e-3
+    o_all = ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))
+    o_gpu = dec(host_bits(o_all[torch.from_numpy(rows).cuda()]))
+    assert rel_fro(o_gpu, rt["o"]) <= 5e-3
+    r_all = ws_view(ws, lay, "r", torch.bfloat16, (T, L))
+    r_bits = host_bits(r_all[torch.from_numpy(sm).cuda()])
+    assert rel_fro(dec(r_bits), rt["r64"]) <= 5e-3
+    sa_all = ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))
+    sa_bits = host_bits(sa_all[torch.from_numpy(sm).cuda()])
+    sa_ref = oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"]))
+    assert rel_fro(dec(sa_bits), dec(sa_ref)) <= 5e-3
+    wup, ws3 = synth.bits(w["w_up"]), synth.bits(w["ws3"])
+    y_stage = oracle.up_shared(cfg, r_bits, sa_bits, wup, ws3)
+    y_gpu = run["y"][torch.from_numpy(sm).cuda()]
+    assert rel_fro(y_gpu.float().cpu().numpy().astype(np.float64), y_stage) <= 5e-3
+
+    # end to end on the sampled tokens, with the oracle's own routing
+    h_o = oracle.down_proj(cfg, xb, wd)
+    s_o = oracle.router(cfg, h_o, wr)
+    idx_o, g_o, margin = oracle.topk(cfg, s_o, bias)
+    used_o = np.unique(idx_o)
+    we_o = {n: {int(e): synth.bits(w[n][int(e)]) for e in used_o} for n in ("w1", "w2", "w3")}
+    rt_o = oracle.routed(cfg, h_o, idx_o, g_o, we_o["w1"], we_o["w2"], we_o["w3"])
+    y_o = oracle.up_shared(cfg, rt_o["r"], oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"])),
+                           wup, ws3)
+    keep = margin > 1e-4
+    if keep.any():
+        check_layer_output(y_gpu, y_o, margin)
+        # on those tokens the GPU chose the same experts
+        assert np.array_equal(np.sort(idx_gpu[sm][keep], 1), np.sort(idx_o[keep], 1))
+    return counts
+
+
+def outlier_tokens(x, n=1):
+    rms = x.float().pow(2).mean(dim=1).sqrt()
+    return torch.nonzero(rms > 10.0).flatten()[:n].cpu().tolist()
+
+
+def test_k3_decode_layer(lm):
+    shape = synth.K3_DECODE
+    run = run_k3(lm, shape)
+    sample = sorted(set([0, 17, 40, 63] + outlier_tokens(run["x"])))
+    counts = check_k3(shape, run, sample)
+    touched = int((counts > 0).sum())
+    assert 500 <= touched <= 700            # ~613 distinct experts expected for 64 x 16 picks
+
+
+def test_k3_prefill_layer(lm):
+    shape = synth.K3_PREFILL
+    run = run_k3(lm, shape)
+    sample = sorted(set([0, 1, 4095, 8191] + outlier_tokens(run["x"], 2)))
+    counts = check_k3(shape, run, sample)
+    assert counts.sum() == shape.T * shape.top_k
+    load = counts / counts.mean()
+    assert load.max() > 5.0                 # the router weights make the loads Zipf-skewed

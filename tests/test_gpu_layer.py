@@ -1,0 +1,183 @@
+"""GPU parity of the Stable LatentMoE forward (through the C ABI) against the
+CPU oracle.  Each stage is checked on the GPU's own input to that stage (so a
+discontinuous step -- the top-k -- is compared bit for bit), and the layer
+output is checked end to end against the oracle's full forward."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_moe_layer_bias_gb300 import synth
+
+from layer_check import (ACC_REL, check_layer_output, score_tol, dec, host_bits, oracle_cfg, rel_fro, ulp_bf16,
+                         ws_view)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_moe_layer_bias_gb300 as m
+    m.load_library()
+    return m
+
+
+def run_host_shape(lm, shape, T=None, seed_offset=0):
+    w_host = synth.layer_weights_host(shape)
+    x_host, b_host = synth.activations_host(shape, T=T, seed_offset=seed_offset)
+    w = {k: v.cuda() for k, v in w_host.items()}
+    x, bias = x_host.cuda(), b_host.cuda()
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=x.shape[0])
+    ws = lm.alloc_workspace(h, x.shape[0])
+    y = lm.lmoe_forward(h, x, bias, workspace=ws)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    layout = lm.lmoe_workspace_layout(h, x.shape[0])
+    return dict(h=h, ws=ws, layout=layout, y=y, x_host=x_host, b_host=b_host, w_host=w_host)
+
+
+def staged_checks(shape, run):
+    """Compare every stage with the oracle fed the GPU's own stage inputs."""
+    cfg = oracle_cfg(shape)
+    T = run["x_host"].shape[0]
+    E, K, L, I = shape.n_experts, shape.top_k, shape.latent, shape.inter
+    S = shape.n_shared * shape.shared_inter
+    ws, lay = run["ws"], run["layout"]
+    wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
+    xb = synth.bits(run["x_host"])
+    bias = run["b_host"].numpy()
+
+    # a1: h within one bf16 ulp of the exact fp64 product
+    h_gpu = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L)))
+    X, Wd = dec(xb), dec(wb["w_down"])
+    exact_h = X @ Wd.T
+    absum_h = np.abs(X) @ np.abs(Wd).T
+    assert np.all(np.abs(dec(h_gpu) - exact_h) <= ulp_bf16(exact_h) + ACC_REL * absum_h)
+
+    # a2: scores on the GPU's h
+    s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, E)).cpu().numpy()
+    s_ref = oracle.router(cfg, h_gpu, wb["w_router"])
+    absum_s = np.abs(dec(h_gpu)) @ np.abs(dec(wb["w_router"])).T
+    assert np.all(np.abs(s_gpu - s_ref) <= score_tol(s_ref, absum_s))
+
+    # a3: top-k on the GPU's scores -- bit-exact
+    idx_gpu = ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).cpu().numpy()
+    g_gpu = ws_view(ws, lay, "gates", torch.float32, (T, K)).cpu().numpy()
+    idx_ref, g_ref, _ = oracle.topk(cfg, s_gpu, bias)
+    assert np.array_equal(idx_gpu, idx_ref)
+    assert np.array_equal(g_gpu, g_ref)
+
+    # a4: permutation maps on the GPU's idx -- bit-exact
+    counts, offsets, perm, inv = oracle.permute(cfg, idx_gpu)
+    assert np.array_equal(ws_view(ws, lay, "counts", torch.int32, (E,)).cpu().numpy(), counts)
+    assert np.array_equal(ws_view(ws, lay, "offsets", torch.int32, (E + 1,)).cpu().numpy(), offsets)
+    assert np.array_equal(ws_view(ws, lay, "perm", torch.int32, (T * K,)).cpu().numpy(), perm)
+    assert np.array_equal(ws_view(ws, lay, "inv", torch.int32, (T * K,)).cpu().numpy(), inv)
+
+    # a5/a6: expert activations and gate-weighted outputs on the GPU's h and routing
+    rt = oracle.routed(cfg, h_gpu, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"], want_act=True, want_o=True)
+    act_gpu = dec(host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))))
+    act_ref = dec(rt["act"])[perm]                       # oracle rows are in assignment order
+    # |d act/d p1| <= 1.1 * beta2 and |d act/d p2| <= beta1: the accumulation
+    # error of p1, p2 carries over with those factors
+    Hd = np.abs(dec(h_gpu))
+    tok = perm // K
+    ex = idx_gpu.reshape(-1)[perm]
+    acc_tol = np.zeros_like(act_ref)
+    for e in np.unique(ex):
+        rows = np.nonzero(ex == e)[0]
+        a1 = Hd[tok[rows]] @ np.abs(dec(wb["w1"][e])).T
+        a2 = Hd[tok[rows]] @ np.abs(dec(wb["w2"][e])).T
+        acc_tol[rows] = ACC_REL * (1.1 * shape.beta2 * a1 + shape.beta1 * a2)
+    assert np.all(np.abs(act_gpu - act_ref) <= 2 * ulp_bf16(act_ref) + acc_tol)
+    o_gpu = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))))
+    assert rel_fro(o_gpu, rt["o"]) <= 5e-3
+
+    # a7: RMS-normalised aggregate
+    r_gpu = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))
+    assert rel_fro(r_gpu, rt["r64"]) <= 5e-3
+    assert np.allclose(np.mean(r_gpu ** 2, axis=1), 1.0, atol=2e-2)   # unit RMS after the norm
+
+    # a8': shared-expert activations on x
+    sact_gpu = host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S)))
+    sact_ref = oracle.shared_act(cfg, xb, wb["ws1"], wb["ws2"])
+    ds = dec(sact_ref)
+    Xa = np.abs(X)
+    stol = ACC_REL * (1.1 * shape.beta2 * (Xa @ np.abs(dec(wb["ws1"])).T) +
+                      shape.beta1 * (Xa @ np.abs(dec(wb["ws2"])).T))
+    assert np.all(np.abs(dec(sact_gpu) - ds) <= 2 * ulp_bf16(ds) + stol)
+
+    # a8: up-projection + shared add on the GPU's r and shared activations
+    y_gpu = run["y"].float().cpu().numpy().astype(np.float64)
+    y_stage = oracle.up_shared(cfg, host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))), sact_gpu,
+                               wb["w_up"], wb["ws3"])
+    assert rel_fro(y_gpu, y_stage) <= 5e-3
+
+
+def end_to_end(shape, run):
+    cfg = oracle_cfg(shape)
+    wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
+    ref = oracle.layer_forward(cfg, synth.bits(run["x_host"]), wb, run["b_host"].numpy())
+    rf, mx, kept = check_layer_output(run["y"], ref["y"], ref["margin"])
+    return rf, mx, kept, ref
+
+
+def test_tiny_layer_stages(lm):
+    run = run_host_shape(lm, synth.TINY)
+    staged_checks(synth.TINY, run)
+
+
+def test_tiny_layer_end_to_end(lm):
+    run = run_host_shape(lm, synth.TINY)
+    rf, mx, kept, ref = end_to_end(synth.TINY, run)
+    assert kept >= 0.8 * synth.TINY.T
+
+
+def test_small_layer_stages_and_end_to_end(lm):
+    run = run_host_shape(lm, synth.SMALL)
+    staged_checks(synth.SMALL, run)
+    rf, mx, kept, _ = end_to_end(synth.SMALL, run)
+    assert kept >= 0.8 * synth.SMALL.T
+
+
+@pytest.mark.parametrize("T", [1, 3, 33, 127, 129, 200])
+def test_tiny_layer_ragged_token_counts(lm, T):
+    run = run_host_shape(lm, synth.TINY, T=T, seed_offset=T)
+    staged_checks(synth.TINY, run)
+    end_to_end(synth.TINY, run)
+
+
+def test_forward_is_deterministic(lm):
+    shape = synth.TINY
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, b = (t.cuda() for t in synth.activations_host(shape))
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=x.shape[0])
+    y1 = lm.lmoe_forward(h, x, b).clone()
+    y2 = lm.lmoe_forward(h, x, b)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_host_errors_enqueue_nothing(lm):
+    shape = synth.TINY
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=64)
+    x = torch.zeros((65, shape.d), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(shape.n_experts, dtype=torch.float32, device="cuda")
+    with pytest.raises(lm.LmoeError) as e:
+        lm.lmoe_forward(h, x, b, workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 2                       # T > max_tokens
+    x = x[:64]
+    small_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lm.LmoeError) as e:
+        lm.lmoe_forward(h, x, b, workspace=small_ws)
+    assert e.value.status == 4                       # workspace too small
+    bad = dict(shape.layer_dict())
+    bad["latent"] = 100
+    with pytest.raises(lm.LmoeError) as e:
+        lm.lmoe_create(bad, w, max_tokens=8)
+    assert e.value.status == 2
+    y = lm.lmoe_forward(h, x[:0], b)                 # T = 0: nothing to do
+    assert y.shape[0] == 0

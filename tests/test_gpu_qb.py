@@ -1,0 +1,95 @@
+"""GPU parity of the Quantile Balancing histogram (bit-exact counts) and the
+quantile/bias read, through the C ABI, against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_moe_layer_bias_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_moe_layer_bias_gb300 as m
+    m.load_library()
+    return m
+
+
+def hist_np(h: torch.Tensor) -> np.ndarray:
+    return h.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("T,E,B", [(65536, 896, 1000), (4096, 128, 1000), (4099, 896, 10000),
+                                   (1000, 40, 37), (1, 896, 1000)])
+def test_histogram_bit_exact(lm, T, E, B):
+    s = synth.qb_scores(T, E, seed=T + E + B)
+    s[0, 0] = 1.0
+    s[-1, -1] = 0.0
+    hg = lm.qb_histogram(s.cuda(), B)
+    torch.cuda.synchronize()
+    ref = oracle.qb_histogram(s.numpy(), B)
+    assert np.array_equal(hist_np(hg), ref)
+    assert hist_np(hg).sum(dtype=np.uint64) == T * E
+
+
+def test_histogram_strided_and_unaligned_columns(lm):
+    T, ld, E, B = 3001, 19, 13, 1000
+    s = synth.qb_scores(T, ld, seed=7)
+    hg = lm.qb_histogram(s.cuda(), B, n_cols=E)
+    ref = oracle.qb_histogram(s.numpy(), B, n_cols=E)
+    assert np.array_equal(hist_np(hg), ref)
+
+
+def test_histogram_accumulates(lm):
+    s = synth.qb_scores(9000, 64, seed=3)
+    B = 1000
+    hg = lm.qb_histogram(s[:4000].cuda(), B)
+    lm.qb_histogram(s[4000:].cuda(), B, hist=hg, accumulate=True)
+    assert np.array_equal(hist_np(hg), oracle.qb_histogram(s.numpy(), B))
+
+
+def test_histogram_full_size_sampled(lm):
+    """T = 2^20 x 896 (the largest sweep point): every row sums to T and a
+    sample of expert columns matches the oracle bit for bit."""
+    T, E, B = 1 << 20, 896, 1000
+    s = synth.qb_scores(T, E, device="cuda")
+    hg = lm.qb_histogram(s, B)
+    h = hist_np(hg)
+    assert np.all(h.sum(axis=1, dtype=np.uint64) == T)
+    cols = np.array([0, 1, 255, 256, 511, 640, 895])
+    sub = s[:, torch.from_numpy(cols).cuda()].contiguous().cpu().numpy()
+    ref = oracle.qb_histogram(sub, B)
+    assert np.array_equal(h[cols], ref)
+
+
+@pytest.mark.parametrize("B", [10, 1000, 10000])
+def test_quantile_bias_matches_oracle(lm, B):
+    rng = np.random.default_rng(B)
+    E = 896
+    hist = rng.integers(0, 50, size=(E, B)).astype(np.uint32)
+    hist[3] = 0                                  # empty row
+    hist[4] = 0
+    hist[4, B - 1] = 7                           # all mass in the last bin
+    hist[5] = 0
+    hist[5, 0] = 1                               # a single count
+    level = 1 - 16 / 896
+    hg = torch.from_numpy(hist.view(np.int32)).cuda()
+    q, b = lm.qb_quantile_bias(hg, level)
+    q_ref, b_ref = oracle.qb_quantile_bias(hist, level)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(b.cpu().numpy(), b_ref)
+
+
+def test_quantile_within_one_bin_of_exact_sort(lm):
+    T, E, B = 65536, 896, 1000
+    s = synth.qb_scores(T, E, seed=11)
+    hg = lm.qb_histogram(s.cuda(), B)
+    level = 1 - 16 / 896
+    q, _ = lm.qb_quantile_bias(hg, level)
+    r = int(np.ceil(level * T))
+    exact = torch.kthvalue(s, r, dim=0).values.numpy().astype(np.float64)
+    assert np.all(np.abs(q.cpu().numpy() - exact) <= 1.0 / B + 1e-6)

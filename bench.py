@@ -228,6 +228,38 @@ def run_reference(args, world, rank):
     return 0
 
 
+# ----------------------------------------------------------------------------- ncu case
+def run_profile_case(args):
+    """A few forwards of a reduced K3-width layer (E=256, T=2048: ~3.3 GB on
+    the device) and a QB histogram at T=262144, for ncu captures.  Prints one
+    JSON line with its own timing; not a benchmark result."""
+    import dataclasses
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_moe_layer_bias_gb300 as lm
+    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="normal")
+    w = synth.layer_weights_device(shape)
+    x, bias = synth.activations_device(shape)
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
+    ws = lm.alloc_workspace(h, shape.T)
+    scores = torch.empty((shape.T, shape.n_experts), dtype=torch.float32, device="cuda")
+    sq = synth.qb_scores(262144, 896, device="cuda")
+    hq = torch.empty((896, QB_B), dtype=torch.int32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            e0.record()
+        y = lm.lmoe_forward(h, x, bias, workspace=ws, scores_out=scores)
+        lm.qb_histogram(sq, QB_B, hist=hq)
+    e1.record()
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    print(json.dumps({"case": "ncu_case", "T": shape.T, "n_experts": shape.n_experts,
+                      "ms_per_iter": e0.elapsed_time(e1) / max(args.steps, 1),
+                      "y_finite": bool(torch.isfinite(y.float()).all().item())}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
     ap = argparse.ArgumentParser()
@@ -237,11 +269,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=128)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="small case for ncu captures: K3 widths, 256 experts, T=2048 (~3.3 GB)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.profile_case:
+        return run_profile_case(args)
 
     import __graft_entry__
     if rank == 0:

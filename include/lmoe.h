@@ -167,6 +167,27 @@ typedef enum {
  * pointer: it must stay valid while set. */
 int lmoe_set_stage_events(lmoe_handle *handle, cudaEvent_t *events, int n_events);
 
+/* Routing without caller scratch: the biased top-k (a3) and the stable
+ * grouping of assignments by expert (a4) of lmoe_forward, for callers that
+ * cannot allocate device memory -- e.g. an inference-engine plugin given no
+ * allocator, or a serving loop that forbids allocation once running.  The
+ * pages describe no such call; it is an interface addition of this library.
+ * Inputs: scores [T][E] fp32 (sigmoid router scores), bias [E] fp32.
+ * Outputs (caller memory, same meaning as in lmoe_forward): topk_idx [T][top_k]
+ * int32, gates [T][top_k] fp32, counts [E] int32, offsets [E+1] int32,
+ * perm [T*top_k] int32, inv [T*top_k] int32.
+ * Scratch lives in one fixed 8 MiB array inside the library (every GPU that
+ * loads the library holds it until exit); problems whose scratch exceeds it
+ * (about 16*E*ceil(T/32) + 20*T*top_k + 16*E bytes) return
+ * LMOE_ERR_UNSUPPORTED_SHAPE.  It calls no cudaMalloc/cudaFree.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress), so
+ * make that first call before any stream capture.  All calls share the array:
+ * calls whose work overlaps on the GPU (other streams, other threads) race and
+ * must be serialised by the caller.  1 <= top_k <= 32, top_k <= E <= 1024. */
+int lmoe_route_static(const float *scores, int64_t T, int32_t E, int32_t top_k, const float *bias,
+                      int32_t *topk_idx, float *gates, int32_t *counts, int32_t *offsets,
+                      int32_t *perm, int32_t *inv, cudaStream_t stream);
+
 /* Device-side status of the handle's kernels (bounded waits that gave up).
  * Synchronises `stream`, copies the status word, and clears it when `clear`
  * is non-zero.  *device_status is LMOE_OK or LMOE_ERR_TIMEOUT. */

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     lmoe_destroy,
     lmoe_device_status,
     lmoe_forward,
+    lmoe_route_static,
     lmoe_set_stage_events,
     STAGES,
     lmoe_status_string,

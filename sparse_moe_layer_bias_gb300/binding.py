@@ -21,7 +21,7 @@ STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED_SHAP
 
 EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size",
             "lmoe_workspace_layout", "lmoe_forward", "lmoe_device_status", "lmoe_set_stage_events",
-            "qb_histogram", "qb_quantile_bias")
+            "lmoe_route_static", "qb_histogram", "qb_quantile_bias")
 
 STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12", "expert_w3",
           "combine", "up")
@@ -84,6 +84,8 @@ def load_library():
     lib.lmoe_device_status.argtypes = [P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.lmoe_set_stage_events.restype = ctypes.c_int
     lib.lmoe_set_stage_events.argtypes = [P, P, ctypes.c_int]
+    lib.lmoe_route_static.restype = ctypes.c_int
+    lib.lmoe_route_static.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P]
     lib.qb_histogram.restype = ctypes.c_int
     lib.qb_histogram.argtypes = [P, I64, I32, I64, I32, P, ctypes.c_int, P]
     lib.qb_quantile_bias.restype = ctypes.c_int
@@ -230,6 +232,25 @@ def lmoe_device_status(handle: Handle, clear: bool = True, stream=None) -> int:
     _check("lmoe_device_status",
            load_library().lmoe_device_status(handle.ptr, _stream(stream), 1 if clear else 0, ctypes.byref(v)))
     return v.value
+
+
+def lmoe_route_static(scores: torch.Tensor, bias: torch.Tensor, top_k: int, stream=None) -> dict:
+    """Top-k + permutation with the library's fixed scratch array (no
+    allocation inside the library; the outputs are allocated here by torch)."""
+    scores = _dev(scores, torch.float32, "scores")
+    bias = _dev(bias, torch.float32, "bias")
+    T, E = scores.shape
+    dev = scores.device
+    out = {"topk_idx": torch.empty((T, top_k), dtype=torch.int32, device=dev),
+           "gates": torch.empty((T, top_k), dtype=torch.float32, device=dev),
+           "counts": torch.empty(E, dtype=torch.int32, device=dev),
+           "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+           "perm": torch.empty(T * top_k, dtype=torch.int32, device=dev),
+           "inv": torch.empty(T * top_k, dtype=torch.int32, device=dev)}
+    _check("lmoe_route_static", load_library().lmoe_route_static(
+        _ptr(scores), T, E, int(top_k), _ptr(bias), _ptr(out["topk_idx"]), _ptr(out["gates"]),
+        _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv"]), _stream(stream)))
+    return out
 
 
 def qb_histogram(scores: torch.Tensor, B: int, hist: torch.Tensor | None = None, accumulate: bool = False,

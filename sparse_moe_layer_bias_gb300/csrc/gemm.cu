@@ -2,8 +2,8 @@
 // used for every contraction of the Stable LatentMoE layer:
 //   a1  h   = x W_down^T                       (A dense, B plain, bf16 out)
 //   a2  s   = sigmoid(h W_router^T)            (A dense, B plain, fp32 out)
-//   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows gathered by the
-//            expert permutation, B = the expert's W1|W2 rows, grouped by expert)
+//   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows grouped by expert,
+//            B = the expert's W1|W2 rows)
 //   a6  o   = gate * act W3^T                  (A = permuted act rows, B = the
 //            expert's W3, rows scattered back to assignment order)
 //   a8  y   = r W_up^T + shared_act Ws3^T       (K split over two A/B sources)
@@ -12,8 +12,8 @@
 // projections: same page, section 2.)
 //
 // Structure (one CTA per SM, 192 threads):
-//   warp 0      TMA producer: per 64-wide K block, one box of A (or 32 gather4
-//               row quads) and one or two boxes of B into a STAGES-deep ring
+//   warp 0      TMA producer: per 64-wide K block, one box of A and one or two
+//               boxes of B into a STAGES-deep ring
 //               of 128B-swizzled shared-memory tiles;
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //               (M=128, N=BN, K=16) x4 per stage into one of two TMEM
@@ -55,11 +55,12 @@ template <bool GROUPED>
 __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
     Tile ti;
     if (GROUPED) {
-        // N-tile major: every M tile (of every expert) for N tile 0, then N
-        // tile 1, ... -- the M tiles of one expert's weight tile run side by
-        // side, so the weight tile is read from HBM once and shared via L2.
-        const int mt = t % n_m;
-        ti.nt = t / n_m;
+        // M-tile major: the N tiles of one M tile run side by side on
+        // neighbouring SMs and share its activation rows through L2; the M
+        // tiles of one expert follow each other, so its weights are read from
+        // HBM about once and re-served from L2.
+        const int mt = t / a.n_tiles;
+        ti.nt = t % a.n_tiles;
         const int4 d = a.tiles[mt];
         ti.expert = d.x;
         ti.row0 = d.y;
@@ -182,21 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED>(args, t, n_m);
-            int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
-            bool gvalid = false;
-            uint32_t a_bytes = C::kABytes;
-            if (AM == A_GATHER) {
-                const int base = lane * 4;
-                gvalid = base < ti.nrows;
-                if (gvalid) {
-                    const int last = ti.nrows - 1;
-                    g0 = args.gather_rows[ti.row0 + min(base + 0, last)];
-                    g1 = args.gather_rows[ti.row0 + min(base + 1, last)];
-                    g2 = args.gather_rows[ti.row0 + min(base + 2, last)];
-                    g3 = args.gather_rows[ti.row0 + min(base + 3, last)];
-                }
-                a_bytes = static_cast<uint32_t>((ti.nrows + 3) / 4) * 4u * (kBK * 2);
-            }
+            constexpr uint32_t a_bytes = C::kABytes;
             const int brow = ti.expert * args.b_expert_rows + ti.nt * (BMD == B_GLU ? H : BN);
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 // every lane waits; the warp proceeds only if all lanes saw the slot free
@@ -212,12 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sb = smem_u32(smB + stage * C::kBBytes);
                 const bool second = (AM == A_SPLIT || BMD == B_SPLIT) && kb >= args.k_split;
                 const int kx = (second ? kb - args.k_split : kb) * kBK;
-                if (AM == A_GATHER) {
-                    if (gvalid) tma_gather4(sa + lane * 4 * (kBK * 2), &tmA0, kx, g0, g1, g2, g3, fb);
-                } else if (lane == 0) {
-                    tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
-                }
                 if (lane == 0) {
+                    tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
                     if (BMD == B_GLU) {
                         tma_load_2d(sb, &tmB0, kx, brow, fb);
                         tma_load_2d(sb + H * (kBK * 2), &tmB1, kx, brow, fb);
@@ -390,9 +373,9 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, false)
     // a2 router scores
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
-    // a5 routed experts W1|W2 (gathered rows) with the SiTU-GLU epilogue
-    LMOE_GEMM_CASE(256, A_GATHER, B_GLU, EPI_SITU_GLU, true)
-    LMOE_GEMM_CASE(128, A_GATHER, B_GLU, EPI_SITU_GLU, true)
+    // a5 routed experts W1|W2 (rows already grouped by expert) with the SiTU-GLU epilogue
+    LMOE_GEMM_CASE(256, A_DENSE, B_GLU, EPI_SITU_GLU, true)
+    LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, true)
     // a6 routed experts W3 with the gate-weighted scatter
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)

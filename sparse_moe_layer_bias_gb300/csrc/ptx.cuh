@@ -1,5 +1,6 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled and
-// gather4), and the 5th-generation tensor core (tcgen05 MMA, TMEM alloc/ld).
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA tiled loads
+// (with optional L2 eviction hints), and the 5th-generation tensor core
+// (tcgen05 MMA, TMEM alloc/ld).
 // Every spin on an mbarrier is bounded in wall time (%globaltimer); a wait that
 // runs out raises a CTA-wide abort flag and a device status bit instead of
 // hanging the GPU.
@@ -77,18 +78,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Gather four rows (r0..r3) of a 2-D tensor, columns [x, x + box width), into
-// four consecutive box rows at dst.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int32_t x,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
         : "memory");
 }
 

@@ -6,7 +6,8 @@
 //   u_e = fp32(s_e + b_e); take the top_k largest u (ties: lower expert id),
 //   gate_j = s at the chosen expert (unbiased).
 // a4: the T*top_k assignments are grouped by expert with a deterministic,
-// stable counting sort.  A token picks an expert at most once, so "stable by
+// stable counting sort (and, for the forward, each assignment's latent row is
+// copied into its grouped position).  A token picks an expert at most once, so "stable by
 // assignment id" is "ordered by token": each expert keeps a bitmap over
 // tokens, the rank of token t inside expert e is a popcount prefix of that
 // bitmap, and no atomic ever decides an order.
@@ -167,6 +168,49 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int k
     tokrow[p] = static_cast<int32_t>(t);
 }
 
+// Same maps as scatter_kernel, one warp per assignment, plus the copy of the
+// assignment's latent row into its permuted slot: h_perm[p] = h[t].  The
+// grouped expert GEMM then reads each expert's rows as dense TMA boxes.
+constexpr int kCopyWarps = 8;
+__global__ void __launch_bounds__(kCopyWarps * 32)
+    scatter_copy_kernel(const int32_t *__restrict__ idx, int64_t T, int k,
+                        const uint32_t *__restrict__ bitmap, const uint32_t *__restrict__ word_prefix,
+                        int words, const int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                        int32_t *__restrict__ inv, int32_t *__restrict__ tokrow,
+                        const uint16_t *__restrict__ h, int L, uint16_t *__restrict__ h_perm) {
+    const int lane = threadIdx.x & 31;
+    const int64_t a = int64_t(blockIdx.x) * kCopyWarps + (threadIdx.x >> 5);
+    if (a >= T * k) return;
+    const int64_t t = a / k;
+    int32_t p = 0;
+    if (lane == 0) {
+        const int e = idx[a];
+        const int64_t w = int64_t(e) * words + (t >> 5);
+        const uint32_t below = bitmap[w] & ((1u << (t & 31)) - 1u);
+        p = offsets[e] + static_cast<int32_t>(word_prefix[w] + __popc(below));
+        perm[p] = static_cast<int32_t>(a);
+        inv[a] = p;
+        tokrow[p] = static_cast<int32_t>(t);
+    }
+    p = __shfl_sync(0xffffffffu, p, 0);
+    const uint4 *src = reinterpret_cast<const uint4 *>(h + t * int64_t(L));
+    uint4 *dst = reinterpret_cast<uint4 *>(h_perm + int64_t(p) * L);
+    const int nvec = L / 8;
+    for (int i0 = 0; i0 < nvec; i0 += 32 * 8) {   // 8 loads in flight per lane
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 32 + lane;
+            if (i < nvec) v[u] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * 32 + lane;
+            if (i < nvec) dst[i] = v[u];
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E, int k,
@@ -205,11 +249,18 @@ cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets,
 
 cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words, const int32_t *offsets,
-                           int32_t *perm, int32_t *inv, int32_t *tokrow, cudaStream_t st) {
+                           int32_t *perm, int32_t *inv, int32_t *tokrow, const uint16_t *h, int L,
+                           uint16_t *h_perm, cudaStream_t st) {
     const int64_t n = T * k;
     if (n == 0) return cudaSuccess;
-    scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-        idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
+    if (h) {
+        scatter_copy_kernel<<<static_cast<unsigned>((n + kCopyWarps - 1) / kCopyWarps), kCopyWarps * 32, 0,
+                              st>>>(idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow, h,
+                                    L, h_perm);
+    } else {
+        scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+            idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
+    }
     return cudaGetLastError();
 }
 

@@ -2,8 +2,8 @@
 // used for every contraction of the Stable LatentMoE layer:
 //   a1  h   = x W_down^T                       (A dense, B plain, bf16 out)
 //   a2  s   = sigmoid(h W_router^T)            (A dense, B plain, fp32 out)
-//   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows grouped by expert,
-//            B = the expert's W1|W2 rows)
+//   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows of the expert's
+//            tokens, gathered with cp.async; B = the expert's W1|W2 rows)
 //   a6  o   = gate * act W3^T                  (A = permuted act rows, B = the
 //            expert's W3, rows scattered back to assignment order)
 //   a8  y   = r W_up^T + shared_act Ws3^T       (K split over two A/B sources)
@@ -11,7 +11,7 @@
 // (SiTU-GLU: "Kimi-K3-Architecture-Deep-Dive" section 1; the layer's chain of
 // projections: same page, section 2.)
 //
-// Structure (one CTA per SM, 192 threads):
+// Structure (one CTA per SM, 192 threads; 320 with the A gather):
 //   warp 0      TMA producer: per 64-wide K block, one box of A and one or two
 //               boxes of B into a STAGES-deep ring
 //               of 128B-swizzled shared-memory tiles;
@@ -20,7 +20,9 @@
 //               accumulators and commits stage release / tile completion;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
 //               the fused activation, and the global stores; releases the
-//               accumulator so the next tile's MMAs overlap this epilogue.
+//               accumulator so the next tile's MMAs overlap this epilogue;
+//   warps 6..9  (gather mode only) copy the A rows named by a row list into
+//               the stage with cp.async.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -123,8 +125,11 @@ __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], i
     }
 }
 
+// A_GATHER adds four warps (6..9) that gather A rows with cp.async.
+__host__ __device__ constexpr int threads_for(int am) { return am == A_GATHER ? kThreads + 128 : kThreads; }
+
 template <int BN, int AM, int BMD, int EPI, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(AM), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const GemmArgs args) {
@@ -151,7 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+            // gather mode: one expect_tx arrival (B) + one per gathering thread
+            mbar_init(smem_u32(&full[s]), AM == A_GATHER ? 1 + 128 : 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -183,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED>(args, t, n_m);
-            constexpr uint32_t a_bytes = C::kABytes;
+            constexpr uint32_t a_bytes = (AM == A_GATHER) ? 0u : C::kABytes;
             const int brow = ti.expert * args.b_expert_rows + ti.nt * (BMD == B_GLU ? H : BN);
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 // every lane waits; the warp proceeds only if all lanes saw the slot free
@@ -200,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool second = (AM == A_SPLIT || BMD == B_SPLIT) && kb >= args.k_split;
                 const int kx = (second ? kb - args.k_split : kb) * kBK;
                 if (lane == 0) {
-                    tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
+                    if (AM != A_GATHER)
+                        tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
                     if (BMD == B_GLU) {
                         tma_load_2d(sb, &tmB0, kx, brow, fb);
                         tma_load_2d(sb + H * (kBK * 2), &tmB1, kx, brow, fb);
@@ -223,6 +230,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(smem_u32(&full[s]), (issued_parity >> s) & 1u, abort_flag, args.err,
                               lim, /*watch_abort=*/false);
         }
+    } else if (AM == A_GATHER && warp >= 6) {
+        // ------------------------------------------------------------ A gather
+        // 128 threads copy the tile's 128 rows x 128 bytes per stage with
+        // 16-byte cp.async straight into the 128B-swizzled layout the tensor
+        // core reads: thread i owns chunk c = i % 8 of rows i/8 + 16 j.  A
+        // thread arrives on a stage's full barrier once its copies of that
+        // stage have landed (two stages kept in flight), after a proxy fence.
+        constexpr int D = 2;
+        const int i = threadIdx.x - kThreads;
+        const int c = i & 7;
+        const int rb = i >> 3;
+        const uint32_t sw = static_cast<uint32_t>((c ^ (rb & 7)) * 16);  // (rb + 16 j) & 7 == rb & 7
+        bool ok = true;
+        int g = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = tile_at<GROUPED>(args, t, n_m);
+            const uint16_t *src[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = rb + 16 * j;
+                src[j] = (r < ti.nrows)
+                             ? args.gather_src + int64_t(args.gather_rows[ti.row0 + r]) * args.gather_ld + c * 8
+                             : nullptr;
+            }
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                const int slot = g % S;
+                const uint32_t par = static_cast<uint32_t>(g / S) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[slot]), par ^ 1u, abort_flag,
+                                                       args.err, lim))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = smem_u32(smA + slot * C::kABytes);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (src[j]) cp_async_16(sa + (rb + 16 * j) * (kBK * 2) + sw, src[j] + kb * kBK);
+                cp_async_commit();
+                if (g >= D) {
+                    cp_async_wait<D>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_u32(&full[(g - D) % S]));
+                }
+                ++g;
+            }
+        }
+        // finish (also after an abort): no copy may still be in flight
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (int q = (g > D ? g - D : 0); q < g; ++q) mbar_arrive(smem_u32(&full[q % S]));
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -266,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(smem_u32(&drain[0]), 0, abort_flag, args.err, lim, /*watch_abort=*/false);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;       // row of the tile held by this thread
@@ -349,7 +405,7 @@ cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStrea
     const size_t smem = Cfg<BN>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(m.a0, m.a1, m.b0, m.b1, a);
+    kern<<<grid, threads_for(AM), smem, st>>>(m.a0, m.a1, m.b0, m.b1, a);
     return cudaGetLastError();
 }
 
@@ -373,9 +429,9 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, false)
     // a2 router scores
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
-    // a5 routed experts W1|W2 (rows already grouped by expert) with the SiTU-GLU epilogue
-    LMOE_GEMM_CASE(256, A_DENSE, B_GLU, EPI_SITU_GLU, true)
-    LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, true)
+    // a5 routed experts W1|W2 (token rows gathered per expert) with the SiTU-GLU epilogue
+    LMOE_GEMM_CASE(256, A_GATHER, B_GLU, EPI_SITU_GLU, true)
+    LMOE_GEMM_CASE(128, A_GATHER, B_GLU, EPI_SITU_GLU, true)
     // a6 routed experts W3 with the gate-weighted scatter
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)

@@ -13,7 +13,9 @@ constexpr unsigned kDevErrTimeout = 1u;
 
 // ------------------------------------------------------------------ GEMM
 // A operand source.
-enum AMode { A_DENSE = 0, A_SPLIT = 2 };
+// A_GATHER: rows of A are gathered by a row-index list (cp.async by four
+// extra producer warps); used for the routed experts' W1|W2 GEMM.
+enum AMode { A_DENSE = 0, A_GATHER = 1, A_SPLIT = 2 };
 // B operand source.
 enum BMode { B_PLAIN = 0, B_GLU = 1, B_SPLIT = 2 };
 // Epilogue.
@@ -35,6 +37,9 @@ struct GemmArgs {
     int32_t b_expert_rows;   // grouped: B-map rows per expert
     const int4 *tiles;       // grouped: {expert, first permuted row, rows, 0}
     const int32_t *n_mtiles; // grouped: number of entries in `tiles` (device)
+    const uint16_t *gather_src;   // A_GATHER: base of the row-major [*, K] bf16 source
+    const int32_t *gather_rows;   // A_GATHER: source row for each grouped row
+    int64_t gather_ld;            // A_GATHER: source row stride (elements)
     void *out;               // output base
     int64_t ld_out;          // output row stride (elements)
     int32_t out_cols;        // output columns that exist (masking of ragged N)
@@ -59,12 +64,10 @@ cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words_per_expe
                                uint32_t *word_prefix, int32_t *counts, cudaStream_t stream);
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
                                  int32_t *n_mtiles, cudaStream_t stream);
-// perm/inv/tokrow maps; if h != nullptr also copies each assignment's latent
-// row h[t] (L bf16) to h_perm[p] (rows grouped by expert).
 cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words_per_expert,
                            const int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *tokrow,
-                           const uint16_t *h, int L, uint16_t *h_perm, cudaStream_t stream);
+                           cudaStream_t stream);
 
 // ------------------------------------------------------------------ combine
 cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,

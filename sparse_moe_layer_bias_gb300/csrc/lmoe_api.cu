@@ -68,7 +68,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, nmt, perm, inv, tokrow,
-        hperm, act, o, r, sact, total;
+        act, o, r, sact, total;
 };
 
 Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
@@ -98,7 +98,6 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.perm = take(size_t(n * 4));
     l.inv = take(size_t(n * 4));
     l.tokrow = take(size_t(n * 4));
-    l.hperm = take(size_t(n * L * 2));
     l.act = take(size_t(n * I * 2));
     l.o = take(size_t(n * L * 2));
     l.r = take(size_t(T * L * 2));
@@ -294,16 +293,15 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     int32_t *perm = reinterpret_cast<int32_t *>(ws + l.perm);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + l.inv);
     int32_t *tokrow = reinterpret_cast<int32_t *>(ws + l.tokrow);
-    uint16_t *hperm = reinterpret_cast<uint16_t *>(ws + l.hperm);
     uint16_t *act = reinterpret_cast<uint16_t *>(ws + l.act);
     uint16_t *obuf = reinterpret_cast<uint16_t *>(ws + l.o);
     uint16_t *rbuf = reinterpret_cast<uint16_t *>(ws + l.r);
     uint16_t *sact = reinterpret_cast<uint16_t *>(ws + l.sact);
 
     // Activation-side TMA descriptors for this T and workspace.
-    CUtensorMap m_x, m_h, m_hp, m_act, m_r, m_sact;
+    CUtensorMap m_x, m_h, m_act, m_r, m_sact;
     if (!make_map(&m_x, x, T, d, d, kBM) || !make_map(&m_h, hbuf, T, L, L, kBM) ||
-        !make_map(&m_hp, hperm, n, L, L, kBM) || !make_map(&m_act, act, n, I, I, kBM) ||
+        !make_map(&m_act, act, n, I, I, kBM) ||
         !make_map(&m_r, rbuf, T, L, L, kBM) || !make_map(&m_sact, sact, T, S, S, kBM))
         return LMOE_ERR_CUDA;
 
@@ -376,22 +374,25 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_SCATTER);
     if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
-                       hbuf, static_cast<int>(L), hperm, stream) != cudaSuccess)
+                       stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_EXPERT_W12);
-    {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over each expert's grouped rows
-        GemmMaps m{m_hp, m_hp, h->m_w1, h->m_w2};
+    {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the rows of each expert's tokens
+        GemmMaps m{m_h, m_h, h->m_w1, h->m_w2};
         GemmArgs a = base_args(h);
         a.n_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.b_expert_rows = static_cast<int32_t>(I);
         a.tiles = tiles;
         a.n_mtiles = nmt;
+        a.gather_src = hbuf;
+        a.gather_rows = tokrow;
+        a.gather_ld = L;
         a.out = act;
         a.ld_out = I;
         a.out_cols = static_cast<int32_t>(I);
         const int64_t max_tiles = (ceil_div(n, kBM) + E) * a.n_tiles;
-        st = gemm_status(launch_gemm(h->bn_exp1, A_DENSE, B_GLU, EPI_SITU_GLU, true, m, a,
+        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
                                      grid_for(max_tiles), stream));
         if (st) return st;
     }

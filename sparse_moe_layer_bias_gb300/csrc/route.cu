@@ -5,9 +5,10 @@
 // token picks, not how their outputs are weighted.  Per token, one warp:
 //   u_e = fp32(s_e + b_e); take the top_k largest u (ties: lower expert id),
 //   gate_j = s at the chosen expert (unbiased).
+// Each round takes two warp reductions (max of the lanes' best keys, then the
+// lowest expert id among the lanes holding it).
 // a4: the T*top_k assignments are grouped by expert with a deterministic,
-// stable counting sort (and, for the forward, each assignment's latent row is
-// copied into its grouped position).  A token picks an expert at most once, so "stable by
+// stable counting sort.  A token picks an expert at most once, so "stable by
 // assignment id" is "ordered by token": each expert keeps a bitmap over
 // tokens, the rank of token t inside expert e is a popcount prefix of that
 // bitmap, and no atomic ever decides an order.
@@ -19,6 +20,15 @@ namespace {
 
 constexpr int kTopkWarps = 8;
 
+// Order-preserving map of a float to uint32 (larger float -> larger key);
+// -0 is folded into +0 first so that the two compare equal, as floats do.
+// Key 0 is the NaN pattern 0xffffffff and never occurs for finite scores; it
+// marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float u) {
+    const uint32_t b = __float_as_uint(__fadd_rn(u, 0.0f));
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 template <int V>  // experts per lane (E <= 32*V)
 __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, int64_t T, int E,
@@ -28,63 +38,37 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     const int64_t t = int64_t(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const float *srow = scores + t * E;
-    float s[V], u[V];
+    uint32_t key[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
         const int e = i * 32 + lane;
-        s[i] = (e < E) ? srow[e] : 0.0f;
-        u[i] = (e < E) ? __fadd_rn(s[i], bias[e]) : 0.0f;
+        key[i] = (e < E) ? order_key(__fadd_rn(srow[e], bias[e])) : 0u;
     }
-    uint32_t taken = 0;
     int my_e = -1;
-    float my_g = 0.0f;
     for (int j = 0; j < k; ++j) {
-        // lane-local best: larger u, then lower id (ids grow with i)
-        float bv = 0.0f;
-        int be = 0x7fffffff;
-        bool have = false;
+        // lane-local best: largest key, lowest expert id (= lowest i) on ties
+        uint32_t bk = 0u;
+        int bi = 0;
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const int e = i * 32 + lane;
-            if (e < E && !(taken & (1u << i)) && (!have || u[i] > bv)) {
-                bv = u[i];
-                be = e;
-                have = true;
+        for (int i = V - 1; i >= 0; --i)
+            if (key[i] >= bk) {
+                bk = key[i];
+                bi = i;
             }
-        }
-        // warp argmax over (u desc, id asc); lanes without a candidate lose
+        // warp: the largest key, then the lowest expert id holding it
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        const int cand = (bk == wk && bk != 0u) ? bi * 32 + lane : 0x7fffffff;
+        const int we = __reduce_min_sync(0xffffffffu, cand);
+        if ((we & 31) == lane) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            const bool ohave = __shfl_xor_sync(0xffffffffu, have ? 1 : 0, off) != 0;
-            const bool better = ohave && (!have || ov > bv || (ov == bv && oe < be));
-            if (better) {
-                bv = ov;
-                be = oe;
-                have = true;
-            }
+            for (int i = 0; i < V; ++i)
+                if (i == (we >> 5)) key[i] = 0u;
         }
-        // the owner lane marks it taken and hands the unbiased score over
-        float gsc = 0.0f;
-        if ((be & 31) == lane) {
-            const int i = be >> 5;
-#pragma unroll
-            for (int ii = 0; ii < V; ++ii)
-                if (ii == i) {
-                    taken |= 1u << ii;
-                    gsc = s[ii];
-                }
-        }
-        gsc = __shfl_sync(0xffffffffu, gsc, be & 31);
-        if (lane == j) {
-            my_e = be;
-            my_g = gsc;
-        }
+        if (lane == j) my_e = we;
     }
     if (lane < k) {
         idx[t * k + lane] = my_e;
-        gate[t * k + lane] = my_g;
+        gate[t * k + lane] = srow[my_e];          // the unbiased score
         atomicOr(&bitmap[int64_t(my_e) * words + (t >> 5)], 1u << (t & 31));
     }
 }
@@ -168,49 +152,6 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int k
     tokrow[p] = static_cast<int32_t>(t);
 }
 
-// Same maps as scatter_kernel, one warp per assignment, plus the copy of the
-// assignment's latent row into its permuted slot: h_perm[p] = h[t].  The
-// grouped expert GEMM then reads each expert's rows as dense TMA boxes.
-constexpr int kCopyWarps = 8;
-__global__ void __launch_bounds__(kCopyWarps * 32)
-    scatter_copy_kernel(const int32_t *__restrict__ idx, int64_t T, int k,
-                        const uint32_t *__restrict__ bitmap, const uint32_t *__restrict__ word_prefix,
-                        int words, const int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-                        int32_t *__restrict__ inv, int32_t *__restrict__ tokrow,
-                        const uint16_t *__restrict__ h, int L, uint16_t *__restrict__ h_perm) {
-    const int lane = threadIdx.x & 31;
-    const int64_t a = int64_t(blockIdx.x) * kCopyWarps + (threadIdx.x >> 5);
-    if (a >= T * k) return;
-    const int64_t t = a / k;
-    int32_t p = 0;
-    if (lane == 0) {
-        const int e = idx[a];
-        const int64_t w = int64_t(e) * words + (t >> 5);
-        const uint32_t below = bitmap[w] & ((1u << (t & 31)) - 1u);
-        p = offsets[e] + static_cast<int32_t>(word_prefix[w] + __popc(below));
-        perm[p] = static_cast<int32_t>(a);
-        inv[a] = p;
-        tokrow[p] = static_cast<int32_t>(t);
-    }
-    p = __shfl_sync(0xffffffffu, p, 0);
-    const uint4 *src = reinterpret_cast<const uint4 *>(h + t * int64_t(L));
-    uint4 *dst = reinterpret_cast<uint4 *>(h_perm + int64_t(p) * L);
-    const int nvec = L / 8;
-    for (int i0 = 0; i0 < nvec; i0 += 32 * 8) {   // 8 loads in flight per lane
-        uint4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 32 + lane;
-            if (i < nvec) v[u] = __ldg(src + i);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * 32 + lane;
-            if (i < nvec) dst[i] = v[u];
-        }
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E, int k,
@@ -249,18 +190,11 @@ cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets,
 
 cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words, const int32_t *offsets,
-                           int32_t *perm, int32_t *inv, int32_t *tokrow, const uint16_t *h, int L,
-                           uint16_t *h_perm, cudaStream_t st) {
+                           int32_t *perm, int32_t *inv, int32_t *tokrow, cudaStream_t st) {
     const int64_t n = T * k;
     if (n == 0) return cudaSuccess;
-    if (h) {
-        scatter_copy_kernel<<<static_cast<unsigned>((n + kCopyWarps - 1) / kCopyWarps), kCopyWarps * 32, 0,
-                              st>>>(idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow, h,
-                                    L, h_perm);
-    } else {
-        scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-            idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
-    }
+    scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
     return cudaGetLastError();
 }
 

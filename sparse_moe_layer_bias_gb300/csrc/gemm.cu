@@ -3,7 +3,8 @@
 //   a1  h   = x W_down^T                       (A dense, B plain, bf16 out)
 //   a2  s   = sigmoid(h W_router^T)            (A dense, B plain, fp32 out)
 //   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows of the expert's
-//            tokens, gathered with cp.async; B = the expert's W1|W2 rows)
+//            tokens, gathered with cp.async, 256 rows per tile as two 128-row
+//            sub-tiles sharing each weight stage; B = the expert's W1|W2 rows)
 //   a6  o   = gate * act W3^T                  (A = permuted act rows, B = the
 //            expert's W3, rows scattered back to assignment order)
 //   a8  y   = r W_up^T + shared_act Ws3^T       (K split over two A/B sources)
@@ -16,8 +17,11 @@
 //               boxes of B into a STAGES-deep ring
 //               of 128B-swizzled shared-memory tiles;
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//               (M=128, N=BN, K=16) x4 per stage into one of two TMEM
-//               accumulators and commits stage release / tile completion;
+//               (M=128, N=BN, K=16) x4 per stage (x2 for the two sub-tiles
+//               of a pair tile) into TMEM and commits stage release / tile
+//               completion.  Single tiles use two TMEM accumulators (the
+//               epilogue of one overlaps the MMAs of the next); pair tiles
+//               use the 512 columns for their two sub-tiles;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
 //               the fused activation, and the global stores; releases the
 //               accumulator so the next tile's MMAs overlap this epilogue;
@@ -36,19 +40,24 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;  // two accumulators of up to 256 fp32 columns
 constexpr int kAccStride = 256;
 
-template <int BN>
+template <int BN, bool PAIR>
 struct Cfg {
-    static constexpr int kABytes = kBM * kBK * 2;       // 16 KB
+    static constexpr int kSub = PAIR ? 2 : 1;           // 128-row sub-tiles per tile
+    static constexpr int kABytes = kSub * kBM * kBK * 2; // 16 or 32 KB
     static constexpr int kBBytes = BN * kBK * 2;        // 16 or 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (BN == 256) ? 4 : 6;
+    static constexpr int kStages = (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
     static constexpr int kBarBytes = 256;
-    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes;
+    // per epilogue warp: 32 rows x 64 bf16, row pitch 144 B (16 B of padding
+    // keeps the 16-byte row writes and the 128-byte row reads conflict-free)
+    static constexpr int kStgPitch = 144;
+    static constexpr int kStgWarpBytes = 32 * kStgPitch;
+    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes;
 };
 
 struct Tile {
     int row0;    // first output row (dense) / first permuted row (grouped)
-    int nrows;   // valid rows in this tile (<= 128)
+    int nrows;   // valid rows in this tile (<= 128, or <= 256 for pair tiles)
     int nt;      // N tile index
     int expert;  // grouped: expert id
 };
@@ -86,31 +95,22 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// Hardware tanh (max relative error about 2^-11, far below the bf16 output's
+// 2^-8).  sigma(x) = (1 + tanh(x/2)) / 2, so SiTU(x; b1) * softcap(y; b2)
+// costs three tanh evaluations.
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float situ_glu(float p1, float p2, float b1, float ib1, float b2, float ib2) {
+    const float sig = fmaf(0.5f, tanh_fast(0.5f * p1), 0.5f);
+    return (b1 * tanh_fast(p1 * ib1) * sig) * (b2 * tanh_fast(p2 * ib2));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Store 32 fp32 values as bf16 at dst (64 bytes, 16-byte aligned), masking
-// columns >= ncols.
-__device__ __forceinline__ void store_bf16_32(uint16_t *dst, const float (&v)[32], int ncols) {
-    if (ncols >= 32) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-            w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-            w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-            w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-            d4[q] = w;
-        }
-    } else {
-        __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(dst);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncols) d[j] = __float2bfloat16_rn(v[j]);
-    }
 }
 
 __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], int ncols) {
@@ -128,14 +128,17 @@ __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], i
 // A_GATHER adds four warps (6..9) that gather A rows with cp.async.
 __host__ __device__ constexpr int threads_for(int am) { return am == A_GATHER ? kThreads + 128 : kThreads; }
 
-template <int BN, int AM, int BMD, int EPI, bool GROUPED>
+template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR>
 __global__ void __launch_bounds__(threads_for(AM), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const GemmArgs args) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, PAIR>;
     constexpr int S = C::kStages;
     constexpr int H = BN / 2;  // GLU: features per tile
+    constexpr int NSUB = C::kSub;
+    constexpr int NACC = PAIR ? 1 : 2;  // TMEM accumulator buffers (each NSUB x 256 columns)
+    static_assert(!PAIR || (AM == A_GATHER && GROUPED), "pair tiles are built for the gathered expert GEMM");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             mbar_init(smem_u32(&full[s]), AM == A_GATHER ? 1 + 128 : 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NACC; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
             mbar_init(smem_u32(&tempty[b]), 128);
         }
@@ -232,12 +235,13 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         }
     } else if (AM == A_GATHER && warp >= 6) {
         // ------------------------------------------------------------ A gather
-        // 128 threads copy the tile's 128 rows x 128 bytes per stage with
-        // 16-byte cp.async straight into the 128B-swizzled layout the tensor
-        // core reads: thread i owns chunk c = i % 8 of rows i/8 + 16 j.  A
-        // thread arrives on a stage's full barrier once its copies of that
-        // stage have landed (two stages kept in flight), after a proxy fence.
-        constexpr int D = 2;
+        // 128 threads copy the tile's 128 (pair: 256) rows x 128 bytes per
+        // stage with 16-byte cp.async straight into the 128B-swizzled layout
+        // the tensor core reads: thread i owns chunk c = i % 8 of rows i/8 + 16 j.
+        // Each thread's arrival on the stage's full barrier fires when its
+        // copies have landed (cp.async.mbarrier.arrive.noinc), so the threads
+        // never wait on their own copies and run up to STAGES ahead; the MMA
+        // thread issues the generic->async proxy fence after its wait.
         const int i = threadIdx.x - kThreads;
         const int c = i & 7;
         const int rb = i >> 3;
@@ -246,9 +250,9 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         int g = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED>(args, t, n_m);
-            const uint16_t *src[8];
+            const uint16_t *src[8 * NSUB];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 8 * NSUB; ++j) {
                 const int r = rb + 16 * j;
                 src[j] = (r < ti.nrows)
                              ? args.gather_src + int64_t(args.gather_rows[ti.row0 + r]) * args.gather_ld + c * 8
@@ -264,21 +268,14 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 }
                 const uint32_t sa = smem_u32(smA + slot * C::kABytes);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 8 * NSUB; ++j)
                     if (src[j]) cp_async_16(sa + (rb + 16 * j) * (kBK * 2) + sw, src[j] + kb * kBK);
-                cp_async_commit();
-                if (g >= D) {
-                    cp_async_wait<D>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(smem_u32(&full[(g - D) % S]));
-                }
+                cp_async_arrive_noinc(smem_u32(&full[slot]));
                 ++g;
             }
         }
         // finish (also after an abort): no copy may still be in flight
         cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (int q = (g > D ? g - D : 0); q < g; ++q) mbar_arrive(smem_u32(&full[q % S]));
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -292,18 +289,27 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err, lim)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccStride);
+                // a pair tile whose second sub-tile is empty skips its MMAs
+                int nsub = 1;
+                if (PAIR) nsub = (tile_at<GROUPED>(args, t, n_m).nrows > kBM) ? 2 : 1;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, lim)) {
                         ok = false;
                         break;
                     }
+                    if (AM == A_GATHER) fence_proxy_async_smem();  // A was written by cp.async
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smA + stage * C::kABytes);
                     const uint32_t sb = smem_u32(smB + stage * C::kBBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_bf16(d, sdesc_sw128(sa + k * 32), sdesc_sw128(sb + k * 32), idesc,
-                                    (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t bdesc = sdesc_sw128(sb + k * 32);
+#pragma unroll
+                        for (int sub = 0; sub < NSUB; ++sub)
+                            if (sub < nsub)
+                                tc_mma_bf16(d + sub * kAccStride, sdesc_sw128(sa + sub * (kBM * kBK * 2) + k * 32),
+                                            bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == S) {
                         stage = 0;
@@ -312,7 +318,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 }
                 if (!ok) break;
                 tc_commit(smem_u32(&tfull[acc]));
-                if (++acc == 2) {
+                if (++acc == NACC) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -326,6 +332,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;       // row of the tile held by this thread
+        uint8_t *stg = smem + S * C::kStageBytes + C::kBarBytes + (warp - 2) * C::kStgWarpBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -335,58 +342,84 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                             mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err, lim)))
                 break;
             tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * kAccStride);
-            const bool rv = row < ti.nrows;
-            if (EPI == EPI_SITU_GLU) {
-                const float b1 = args.beta1, b2 = args.beta2;
-                const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
-                uint16_t *orow = reinterpret_cast<uint16_t *>(args.out) +
-                                 (int64_t)(ti.row0 + row) * args.ld_out + (int64_t)ti.nt * H;
 #pragma unroll 1
-                for (int c = 0; c < H; c += 32) {
-                    float p1[32], p2[32];
-                    tmem_ld32(taddr + c, p1);
-                    tmem_ld32(taddr + H + c, p2);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float g = b1 * tanhf(p1[j] * ib1) * sigmoid_f(p1[j]);
-                        const float l = b2 * tanhf(p2[j] * ib2);
-                        p1[j] = g * l;
-                    }
-                    if (rv) store_bf16_32(orow + c, p1, args.out_cols - (ti.nt * H + c));
-                }
-            } else {
-                int64_t orow_idx = ti.row0 + row;
-                float scale = 1.0f;
-                if (EPI == EPI_SCATTER_BF16 && rv) {
-                    orow_idx = args.scatter_rows[ti.row0 + row];
-                    scale = args.row_scale[orow_idx];
-                }
+            for (int sub = 0; sub < NSUB; ++sub) {
+            if (sub * kBM >= ti.nrows) break;  // uniform across the CTA
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>((acc + sub) * kAccStride);
+            const int trow = sub * kBM + row;    // row of the tile (pair tiles: 0..255)
+            const bool rv = trow < ti.nrows;
+            if (EPI == EPI_SIGMOID_F32) {
+                const int64_t orow = ti.row0 + trow;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
                     tmem_ld32(taddr + c, v);
                     const int col = ti.nt * BN + c;
                     if (!rv) continue;
-                    if (EPI == EPI_SIGMOID_F32) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = sigmoid_f(v[j]);
-                        store_f32_32(reinterpret_cast<float *>(args.out) + orow_idx * args.ld_out + col,
-                                     v, args.out_cols - col);
-                    } else {
-                        if (EPI == EPI_SCATTER_BF16) {
+                    for (int j = 0; j < 32; ++j) v[j] = sigmoid_f(v[j]);
+                    store_f32_32(reinterpret_cast<float *>(args.out) + orow * args.ld_out + col, v,
+                                 args.out_cols - col);
+                }
+            } else {
+                // bf16 outputs: each group of 64 columns goes through the warp's
+                // staging buffer so the global stores are whole 128-byte lines
+                // (4 rows x 128 B per warp instruction) instead of 16 bytes of
+                // 32 different rows.
+                int64_t drow = ti.row0 + trow;
+                float scale = 1.0f;
+                if (EPI == EPI_SCATTER_BF16 && rv) {
+                    drow = args.scatter_rows[ti.row0 + trow];
+                    scale = args.row_scale[drow];
+                }
+                constexpr int NOUT = (EPI == EPI_SITU_GLU) ? H : BN;   // output columns per tile
+                const int64_t col0 = int64_t(ti.nt) * NOUT;
+                const float b1 = args.beta1, b2 = args.beta2;
+                const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
+#pragma unroll 1
+                for (int c = 0; c < NOUT; c += 64) {
+                    uint32_t packed[32];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        float v[32];
+                        tmem_ld32(taddr + c + h2 * 32, v);
+                        if (EPI == EPI_SITU_GLU) {
+                            float p2[32];
+                            tmem_ld32(taddr + H + c + h2 * 32, p2);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = situ_glu(v[j], p2[j], b1, ib1, b2, ib2);
+                        } else if (EPI == EPI_SCATTER_BF16) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] *= scale;
                         }
-                        store_bf16_32(reinterpret_cast<uint16_t *>(args.out) + orow_idx * args.ld_out + col,
-                                      v, args.out_cols - col);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) packed[h2 * 16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                     }
+                    uint4 *mine = reinterpret_cast<uint4 *>(stg + lane * C::kStgPitch);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        mine[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                    __syncwarp();
+                    const int ch = lane & 7;                 // 16-byte chunk of a 128-byte row
+                    const int64_t gcol = col0 + c + ch * 8;  // first output column of the chunk
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int r = it * 4 + (lane >> 3);
+                        const int64_t dr = __shfl_sync(0xffffffffu, drow, r);
+                        const int ok = __shfl_sync(0xffffffffu, rv ? 1 : 0, r);
+                        const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * C::kStgPitch + ch * 16);
+                        if (ok && gcol + 8 <= args.out_cols)
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(args.out) + dr * args.ld_out +
+                                                       gcol) = val;
+                    }
+                    __syncwarp();
                 }
             }
+            }  // sub-tiles
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));
-            if (++acc == 2) {
+            if (++acc == NACC) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -399,10 +432,10 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int BN, int AM, int BMD, int EPI, bool GROUPED>
+template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR = false>
 cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t st) {
-    auto kern = gemm_kernel<BN, AM, BMD, EPI, GROUPED>;
-    const size_t smem = Cfg<BN>::kSmem;
+    auto kern = gemm_kernel<BN, AM, BMD, EPI, GROUPED, PAIR>;
+    const size_t smem = Cfg<BN, PAIR>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, threads_for(AM), smem, st>>>(m.a0, m.a1, m.b0, m.b1, a);
@@ -411,7 +444,7 @@ cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStrea
 
 }  // namespace
 
-size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
+size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256, false>::kSmem : Cfg<128, false>::kSmem; }
 
 #define LMOE_GEMM_CASE(BN_, AM_, BM_, EPI_, G_)                                   \
     if (bn == BN_ && am == AM_ && bm == BM_ && epi == EPI_ && grouped == G_)       \
@@ -429,9 +462,12 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, false)
     // a2 router scores
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
-    // a5 routed experts W1|W2 (token rows gathered per expert) with the SiTU-GLU epilogue
-    LMOE_GEMM_CASE(256, A_GATHER, B_GLU, EPI_SITU_GLU, true)
-    LMOE_GEMM_CASE(128, A_GATHER, B_GLU, EPI_SITU_GLU, true)
+    // a5 routed experts W1|W2 (token rows gathered per expert, pair tiles of
+    // 256 rows) with the SiTU-GLU epilogue
+    if (am == A_GATHER && bm == B_GLU && epi == EPI_SITU_GLU && grouped) {
+        if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
+        if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
+    }
     // a6 routed experts W3 with the gate-weighted scatter
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)

@@ -35,7 +35,7 @@ struct GemmArgs {
     int32_t k_blocks;        // ceil(K / 64)
     int32_t k_split;         // A_SPLIT/B_SPLIT: k-blocks served by map 0
     int32_t b_expert_rows;   // grouped: B-map rows per expert
-    const int4 *tiles;       // grouped: {expert, first permuted row, rows, 0}
+    const int4 *tiles;       // grouped: {expert, first permuted row, rows, 0} (pair tiles for A_GATHER)
     const int32_t *n_mtiles; // grouped: number of entries in `tiles` (device)
     const uint16_t *gather_src;   // A_GATHER: base of the row-major [*, K] bf16 source
     const int32_t *gather_rows;   // A_GATHER: source row for each grouped row
@@ -50,7 +50,8 @@ struct GemmArgs {
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
 
-// Launch one persistent GEMM.  `bn` in {128, 256}.  Returns cudaErrorInvalidValue
+// Launch one persistent GEMM.  `bn` in {128, 256}.  A_GATHER runs pair tiles
+// (two 128-row sub-tiles sharing each weight stage).  Returns cudaErrorInvalidValue
 // for a combination that is not compiled.
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream);
@@ -62,8 +63,11 @@ cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E
                         cudaStream_t stream);
 cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words_per_expert,
                                uint32_t *word_prefix, int32_t *counts, cudaStream_t stream);
+// tiles: up to 128 rows each (ceil(count/128) per expert); tiles2: pair tiles
+// of up to 256 rows (ceil(count/256) per expert).
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
-                                 int32_t *n_mtiles, cudaStream_t stream);
+                                 int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2,
+                                 cudaStream_t stream);
 cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words_per_expert,
                            const int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *tokrow,

@@ -25,6 +25,10 @@ struct lmoe_handle {
     int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up;
     CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
     cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
+    // The shared experts' W1|W2 GEMM depends only on x: it runs on a side
+    // stream, on side_sms SMs, while the routed part runs on the others.
+    cudaStream_t side;
+    cudaEvent_t ev_fork, ev_join;
 };
 
 namespace {
@@ -67,7 +71,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, nmt, perm, inv, tokrow,
+    size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, tiles2, nmt, perm, inv, tokrow,
         act, o, r, sact, total;
 };
 
@@ -94,6 +98,7 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.bitmap = take(size_t(E * words * 4));
     l.wprefix = take(size_t(E * words * 4));
     l.tiles = take(size_t((ceil_div(n, kBM) + E) * 16));
+    l.tiles2 = take(size_t((ceil_div(n, 2 * kBM) + E) * 16));
     l.nmt = take(16);
     l.perm = take(size_t(n * 4));
     l.inv = take(size_t(n * 4));
@@ -146,6 +151,14 @@ GemmArgs base_args(const lmoe_handle *h) {
 }
 
 int gemm_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
+
+// SMs given to the shared-expert GEMM while the routing and the routed
+// experts run on the rest (0: run it in stream order instead).
+int side_sms_for(const lmoe_handle *h, int64_t T) {
+    (void)T;
+    (void)h;
+    return 0;
+}
 
 }  // namespace
 
@@ -209,6 +222,12 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
         delete h;
         return LMOE_ERR_CUDA;
     }
+    if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        delete h;
+        return LMOE_ERR_CUDA;
+    }
     if (cudaMalloc(&h->d_status, 256) != cudaSuccess) {
         delete h;
         return LMOE_ERR_CUDA;
@@ -226,6 +245,9 @@ int lmoe_destroy(lmoe_handle *h) {
     if (!h) return LMOE_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
     cudaError_t f = cudaFree(h->d_status);
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     delete h;
     return (e == cudaSuccess && f == cudaSuccess) ? LMOE_OK : LMOE_ERR_CUDA;
 }
@@ -289,7 +311,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(ws + l.bitmap);
     uint32_t *wprefix = reinterpret_cast<uint32_t *>(ws + l.wprefix);
     int4 *tiles = reinterpret_cast<int4 *>(ws + l.tiles);
-    int32_t *nmt = reinterpret_cast<int32_t *>(ws + l.nmt);
+    int4 *tiles2 = reinterpret_cast<int4 *>(ws + l.tiles2);
+    int32_t *nmt = reinterpret_cast<int32_t *>(ws + l.nmt);   // [0]: 128-row tiles, [1]: pair tiles
     int32_t *perm = reinterpret_cast<int32_t *>(ws + l.perm);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + l.inv);
     int32_t *tokrow = reinterpret_cast<int32_t *>(ws + l.tokrow);
@@ -309,9 +332,18 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     auto mark = [&](int stage) {
         if (h->stage_events) cudaEventRecord(h->stage_events[stage], stream);
     };
+    const int side_sms = side_sms_for(h, T);
+    const int main_sms = h->num_sms - side_sms;
     auto grid_for = [&](int64_t tiles_) {
-        return static_cast<int>(tiles_ < h->num_sms ? tiles_ : h->num_sms);
+        return static_cast<int>(tiles_ < main_sms ? tiles_ : main_sms);
     };
+    cudaStream_t shared_stream = stream;
+    if (side_sms > 0) {   // fork: the side stream starts after everything before this call
+        if (cudaEventRecord(h->ev_fork, stream) != cudaSuccess ||
+            cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
+            return LMOE_ERR_CUDA;
+        shared_stream = h->side;
+    }
     int st;
 
     if (cudaMemsetAsync(bitmap, 0, size_t(E) * words * 4, stream) != cudaSuccess) return LMOE_ERR_CUDA;
@@ -342,9 +374,13 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = sact;
         a.ld_out = S;
         a.out_cols = static_cast<int32_t>(S);
-        st = gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        const int64_t tiles_s = int64_t(m_tiles) * a.n_tiles;
+        const int grid_s = side_sms > 0 ? static_cast<int>(tiles_s < side_sms ? tiles_s : side_sms)
+                                        : grid_for(tiles_s);
+        st = gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a, grid_s,
+                                     shared_stream));
         if (st) return st;
+        if (side_sms > 0 && cudaEventRecord(h->ev_join, h->side) != cudaSuccess) return LMOE_ERR_CUDA;
     }
     mark(LMOE_STAGE_ROUTER);
     {   // a2: s = sigmoid(h W_router^T), fp32
@@ -370,7 +406,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     if (launch_expert_scan(bitmap, static_cast<int>(E), words, wprefix, counts, stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_OFFSETS);
-    if (launch_offsets_tiles(counts, static_cast<int>(E), offsets, tiles, nmt, stream) != cudaSuccess)
+    if (launch_offsets_tiles(counts, static_cast<int>(E), offsets, tiles, nmt, tiles2, nmt + 1, stream) !=
+        cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_SCATTER);
     if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
@@ -378,20 +415,21 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_EXPERT_W12);
     {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the rows of each expert's tokens
+        // (pair tiles: two 128-row sub-tiles of one expert share each weight stage)
         GemmMaps m{m_h, m_h, h->m_w1, h->m_w2};
         GemmArgs a = base_args(h);
         a.n_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.b_expert_rows = static_cast<int32_t>(I);
-        a.tiles = tiles;
-        a.n_mtiles = nmt;
+        a.tiles = tiles2;
+        a.n_mtiles = nmt + 1;
         a.gather_src = hbuf;
         a.gather_rows = tokrow;
         a.gather_ld = L;
         a.out = act;
         a.ld_out = I;
         a.out_cols = static_cast<int32_t>(I);
-        const int64_t max_tiles = (ceil_div(n, kBM) + E) * a.n_tiles;
+        const int64_t max_tiles = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
         st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
                                      grid_for(max_tiles), stream));
         if (st) return st;
@@ -421,6 +459,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
                                stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_UP);
+    // join: the up-projection reads the shared activations
+    if (side_sms > 0 && cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     {   // a8: y = r W_up^T + act_s Ws3^T  (one GEMM, K split over the two sources)
         GemmMaps m{m_r, m_sact, h->m_wup, h->m_ws3};
         GemmArgs a = base_args(h);

@@ -94,8 +94,14 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// Make this thread's completed generic-proxy shared-memory writes visible to
-// later async-proxy readers (the tensor core) once released via an mbarrier.
+// Arrive once on `bar` when every cp.async this thread issued so far has
+// completed; the arrival counts against the barrier's expected count.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Order generic-proxy shared-memory writes that this thread has observed
+// (its own, or other threads' released through an mbarrier) before its later
+// async-proxy accesses (tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

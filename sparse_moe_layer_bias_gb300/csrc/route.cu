@@ -97,41 +97,51 @@ __global__ void expert_scan_kernel(const uint32_t *__restrict__ bitmap, int E, i
     if (lane == 0) counts[e] = static_cast<int32_t>(running);
 }
 
-// One CTA: offsets = exclusive scan of counts; the grouped-GEMM tile list
-// (expert, first permuted row, rows) with ceil(count/128) tiles per expert,
-// experts in id order.
+// One CTA: offsets = exclusive scan of counts, and two grouped-GEMM tile lists
+// (expert, first permuted row, rows), experts in id order: ceil(count/128)
+// tiles of up to 128 rows, and ceil(count/256) pair tiles of up to 256 rows.
 __global__ void __launch_bounds__(1024)
     offsets_tiles_kernel(const int32_t *__restrict__ counts, int E, int32_t *__restrict__ offsets,
-                         int4 *__restrict__ tiles, int32_t *__restrict__ n_mtiles) {
+                         int4 *__restrict__ tiles, int32_t *__restrict__ n_mtiles,
+                         int4 *__restrict__ tiles2, int32_t *__restrict__ n_mtiles2) {
     __shared__ int32_t s_cnt[1024];
     __shared__ int32_t s_til[1024];
+    __shared__ int32_t s_til2[1024];
     const int e = threadIdx.x;
     const int32_t c = (e < E) ? counts[e] : 0;
     const int32_t nt = (c + kBM - 1) / kBM;
+    const int32_t nt2 = (c + 2 * kBM - 1) / (2 * kBM);
     s_cnt[e] = c;
     s_til[e] = nt;
+    s_til2[e] = nt2;
     __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {  // Hillis-Steele inclusive scan
-        int32_t a = 0, b = 0;
+    for (int off = 1; off < 1024; off <<= 1) {  // Hillis-Steele inclusive scans
+        int32_t a = 0, b = 0, b2 = 0;
         if (e >= off) {
             a = s_cnt[e - off];
             b = s_til[e - off];
+            b2 = s_til2[e - off];
         }
         __syncthreads();
         s_cnt[e] += a;
         s_til[e] += b;
+        s_til2[e] += b2;
         __syncthreads();
     }
     if (e < E) {
         const int32_t row0 = s_cnt[e] - c;
-        const int32_t tile0 = s_til[e] - nt;
         offsets[e] = row0;
+        const int32_t tile0 = s_til[e] - nt;
         for (int32_t m = 0; m < nt; ++m)
             tiles[tile0 + m] = make_int4(e, row0 + m * kBM, min(kBM, c - m * kBM), 0);
+        const int32_t pair0 = s_til2[e] - nt2;
+        for (int32_t m = 0; m < nt2; ++m)
+            tiles2[pair0 + m] = make_int4(e, row0 + m * 2 * kBM, min(2 * kBM, c - m * 2 * kBM), 0);
     }
     if (e == E - 1) {
         offsets[E] = s_cnt[e];
         *n_mtiles = s_til[e];
+        *n_mtiles2 = s_til2[e];
     }
 }
 
@@ -183,8 +193,8 @@ cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words, uint32_
 }
 
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
-                                 int32_t *n_mtiles, cudaStream_t st) {
-    offsets_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, tiles, n_mtiles);
+                                 int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2, cudaStream_t st) {
+    offsets_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, tiles, n_mtiles, tiles2, n_mtiles2);
     return cudaGetLastError();
 }
 

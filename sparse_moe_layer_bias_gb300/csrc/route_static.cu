@@ -58,13 +58,16 @@ extern "C" int lmoe_route_static(const float *scores, int64_t T, int32_t E, int3
     if (T * top_k >= (int64_t(1) << 31)) return LMOE_ERR_UNSUPPORTED_SHAPE;
     const int64_t words = (T + 31) / 32;
     const int64_t n = T * top_k;
-    // scratch layout: bitmap | word prefix | tile list | tile count | token of each permuted row
+    // scratch layout: bitmap | word prefix | tile lists (128 and 256 rows) | tile counts |
+    // token of each permuted row
     const size_t b_bitmap = align256(size_t(E) * words * 4);
     const size_t b_prefix = align256(size_t(E) * words * 4);
     const size_t b_tiles = align256(size_t((n + lmoe::kBM - 1) / lmoe::kBM + E) * 16);
+    const size_t b_tiles2 = align256(size_t((n + 2 * lmoe::kBM - 1) / (2 * lmoe::kBM) + E) * 16);
     const size_t b_nmt = 256;
     const size_t b_tokrow = align256(size_t(n) * 4);
-    if (b_bitmap + b_prefix + b_tiles + b_nmt + b_tokrow > kScratchBytes) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (b_bitmap + b_prefix + b_tiles + b_tiles2 + b_nmt + b_tokrow > kScratchBytes)
+        return LMOE_ERR_UNSUPPORTED_SHAPE;
 
     void *base = nullptr;
     const int st = scratch_address(&base);
@@ -73,8 +76,9 @@ extern "C" int lmoe_route_static(const float *scores, int64_t T, int32_t E, int3
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(p);
     uint32_t *prefix = reinterpret_cast<uint32_t *>(p + b_bitmap);
     int4 *tiles = reinterpret_cast<int4 *>(p + b_bitmap + b_prefix);
-    int32_t *nmt = reinterpret_cast<int32_t *>(p + b_bitmap + b_prefix + b_tiles);
-    int32_t *tokrow = reinterpret_cast<int32_t *>(p + b_bitmap + b_prefix + b_tiles + b_nmt);
+    int4 *tiles2 = reinterpret_cast<int4 *>(p + b_bitmap + b_prefix + b_tiles);
+    int32_t *nmt = reinterpret_cast<int32_t *>(p + b_bitmap + b_prefix + b_tiles + b_tiles2);
+    int32_t *tokrow = reinterpret_cast<int32_t *>(p + b_bitmap + b_prefix + b_tiles + b_tiles2 + b_nmt);
 
     // The bitmap is the only scratch that must start at zero; the array keeps
     // the previous call's contents.
@@ -82,7 +86,7 @@ extern "C" int lmoe_route_static(const float *scores, int64_t T, int32_t E, int3
     const int w = static_cast<int>(words);
     if (lmoe::launch_topk(scores, bias, T, E, top_k, topk_idx, gates, bitmap, w, stream) != cudaSuccess ||
         lmoe::launch_expert_scan(bitmap, E, w, prefix, counts, stream) != cudaSuccess ||
-        lmoe::launch_offsets_tiles(counts, E, offsets, tiles, nmt, stream) != cudaSuccess ||
+        lmoe::launch_offsets_tiles(counts, E, offsets, tiles, nmt, tiles2, nmt + 1, stream) != cudaSuccess ||
         lmoe::launch_scatter(topk_idx, T, top_k, bitmap, prefix, w, offsets, perm, inv, tokrow, stream) !=
             cudaSuccess)
         return LMOE_ERR_CUDA;

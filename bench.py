@@ -230,14 +230,15 @@ def run_reference(args, world, rank):
 
 # ----------------------------------------------------------------------------- ncu case
 def run_profile_case(args):
-    """A few forwards of a reduced K3-width layer (E=256, T=2048: ~3.3 GB on
-    the device) and a QB histogram at T=262144, for ncu captures.  Prints one
-    JSON line with its own timing; not a benchmark result."""
+    """A few forwards of a reduced K3-width layer (E=256, T=2048, Zipf-skewed
+    router like the K3 prefill workload: ~3.3 GB on the device) and a QB
+    histogram at T=262144, for ncu captures.  Prints one JSON line with its own
+    timing; not a benchmark result."""
     import dataclasses
     import __graft_entry__
     __graft_entry__.build()
     import sparse_moe_layer_bias_gb300 as lm
-    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="normal")
+    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="zipf")
     w = synth.layer_weights_device(shape)
     x, bias = synth.activations_device(shape)
     h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)

@@ -350,17 +350,37 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             const int trow = sub * kBM + row;    // row of the tile (pair tiles: 0..255)
             const bool rv = trow < ti.nrows;
             if (EPI == EPI_SIGMOID_F32) {
+                // fp32 scores: 32 columns (128 B) per row and group, staged like
+                // the bf16 outputs below; the last partial group of a ragged N is
+                // stored element by element.
                 const int64_t orow = ti.row0 + trow;
+                float *outf = reinterpret_cast<float *>(args.out);
+                const bool vec_ok = (args.ld_out % 4) == 0;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
                     tmem_ld32(taddr + c, v);
-                    const int col = ti.nt * BN + c;
-                    if (!rv) continue;
+                    const int64_t col = int64_t(ti.nt) * BN + c;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = sigmoid_f(v[j]);
-                    store_f32_32(reinterpret_cast<float *>(args.out) + orow * args.ld_out + col, v,
-                                 args.out_cols - col);
+                    if (col + 32 <= args.out_cols && vec_ok) {
+                        float4 *mine = reinterpret_cast<float4 *>(stg + lane * C::kStgPitch);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) mine[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        __syncwarp();
+                        const int ch = lane & 7;
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int r = it * 4 + (lane >> 3);
+                            const int64_t orr = __shfl_sync(0xffffffffu, orow, r);
+                            const int ok = __shfl_sync(0xffffffffu, rv ? 1 : 0, r);
+                            const float4 val = *reinterpret_cast<const float4 *>(stg + r * C::kStgPitch + ch * 16);
+                            if (ok) *reinterpret_cast<float4 *>(outf + orr * args.ld_out + col + ch * 4) = val;
+                        }
+                        __syncwarp();
+                    } else if (rv) {
+                        store_f32_32(outf + orow * args.ld_out + col, v, static_cast<int>(args.out_cols - col));
+                    }
                 }
             } else {
                 // bf16 outputs: each group of 64 columns goes through the warp's
@@ -461,6 +481,7 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     LMOE_GEMM_CASE(256, A_DENSE, B_GLU, EPI_SITU_GLU, false)
     LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, false)
     // a2 router scores
+    LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
     // a5 routed experts W1|W2 (token rows gathered per expert, pair tiles of
     // 256 rows) with the SiTU-GLU epilogue

@@ -22,7 +22,7 @@ struct lmoe_handle {
     int num_sms;
     unsigned *d_status;  // device status word (bounded-wait timeouts)
     // Weight-side TMA descriptors, built once.
-    int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up;
+    int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up, bn_router;
     CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
     cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
     // The shared experts' W1|W2 GEMM depends only on x: it runs on a side
@@ -209,8 +209,10 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
     h->bn_exp1 = (I % 128 == 0) ? 256 : 128;
     h->bn_exp3 = (L % 256 == 0) ? 256 : 128;
     h->bn_up = (d % 256 == 0) ? 256 : 128;
+    // router: 256-wide N tiles unless E fits one 128-wide tile
+    h->bn_router = (E > 128) ? 256 : 128;
     bool ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->bn_down) &&
-              make_map(&h->m_wrouter, w->w_router, E, L, L, 128) &&
+              make_map(&h->m_wrouter, w->w_router, E, L, L, h->bn_router) &&
               make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
               make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
               make_map(&h->m_w1, w->w1, E * I, L, L, h->bn_exp1 / 2) &&
@@ -388,12 +390,12 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
         a.m_tiles = m_tiles;
-        a.n_tiles = static_cast<int32_t>(ceil_div(E, 128));
+        a.n_tiles = static_cast<int32_t>(ceil_div(E, h->bn_router));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.out = scores;
         a.ld_out = E;
         a.out_cols = static_cast<int32_t>(E);
-        st = gemm_status(launch_gemm(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
+        st = gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
                                      grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }

@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED>(args, t, n_m);
             constexpr uint32_t a_bytes = (AM == A_GATHER) ? 0u : C::kABytes;
-            const int brow = ti.expert * args.b_expert_rows + ti.nt * (BMD == B_GLU ? H : BN);
+            constexpr int TRB = (BMD == B_GLU) ? H : BN;     // rows per B box
+            const int brow = args.b_packed ? (ti.expert * args.b_row_tiles + ti.nt) * args.k_blocks * TRB
+                                           : ti.expert * args.b_expert_rows + ti.nt * TRB;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 // every lane waits; the warp proceeds only if all lanes saw the slot free
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
@@ -208,14 +210,17 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 const uint32_t sb = smem_u32(smB + stage * C::kBBytes);
                 const bool second = (AM == A_SPLIT || BMD == B_SPLIT) && kb >= args.k_split;
                 const int kx = (second ? kb - args.k_split : kb) * kBK;
+                // packed B: the K block is a row offset, the column is always 0
+                const int bx = args.b_packed ? 0 : kx;
+                const int by = args.b_packed ? brow + kb * TRB : brow;
                 if (lane == 0) {
                     if (AM != A_GATHER)
                         tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
                     if (BMD == B_GLU) {
-                        tma_load_2d(sb, &tmB0, kx, brow, fb);
-                        tma_load_2d(sb + H * (kBK * 2), &tmB1, kx, brow, fb);
+                        tma_load_2d(sb, &tmB0, bx, by, fb);
+                        tma_load_2d(sb + H * (kBK * 2), &tmB1, bx, by, fb);
                     } else {
-                        tma_load_2d(sb, (BMD == B_SPLIT && second) ? &tmB1 : &tmB0, kx, brow, fb);
+                        tma_load_2d(sb, (BMD == B_SPLIT && second) ? &tmB1 : &tmB0, bx, by, fb);
                     }
                 }
                 issued_mask |= 1u << stage;

@@ -35,6 +35,10 @@ struct GemmArgs {
     int32_t k_blocks;        // ceil(K / 64)
     int32_t k_split;         // A_SPLIT/B_SPLIT: k-blocks served by map 0
     int32_t b_expert_rows;   // grouped: B-map rows per expert
+    // grouped, tile-packed B (see launch_pack_tiles): B box (e, N tile nt, K
+    // block kb) sits at row ((e * b_row_tiles + nt) * k_blocks + kb) * box rows
+    int32_t b_packed;
+    int32_t b_row_tiles;     // N tiles per expert in the packed layout
     const int4 *tiles;       // grouped: {expert, first permuted row, rows, 0} (pair tiles for A_GATHER)
     const int32_t *n_mtiles; // grouped: number of entries in `tiles` (device)
     const uint16_t *gather_src;   // A_GATHER: base of the row-major [*, K] bf16 source
@@ -56,6 +60,12 @@ struct GemmArgs {
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream);
 size_t gemm_smem_bytes(int bn);
+
+// Repack per-expert weights [E][R][K] (row-major bf16) into tile-contiguous
+// order [E][R/TR][K/64][TR][64] so that one TMA box of TR rows x 64 columns is
+// one contiguous TR*128-byte block of HBM.  R % TR == 0, K % 64 == 0.
+cudaError_t launch_pack_tiles(const uint16_t *src, int64_t E, int R, int K, int TR, uint16_t *dst,
+                              cudaStream_t stream);
 
 // ------------------------------------------------------------------ routing
 cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E, int k,

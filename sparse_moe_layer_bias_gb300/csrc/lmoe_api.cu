@@ -24,6 +24,8 @@ struct lmoe_handle {
     // Weight-side TMA descriptors, built once.
     int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up, bn_router;
     CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
+    // routed experts' weights repacked tile-contiguously (handle-owned)
+    uint16_t *w1p, *w2p, *w3p;
     cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
     // The shared experts' W1|W2 GEMM depends only on x: it runs on a side
     // stream, on side_sms SMs, while the routed part runs on the others.
@@ -118,11 +120,13 @@ int validate_config(const lmoe_config *c) {
         return LMOE_ERR_INVALID_ARG;
     if (!(c->beta1 > 0.0f) || !(c->beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
     const int64_t S = int64_t(c->n_shared) * c->shared_inter;
-    if (c->d % 64 || c->latent % 64 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->d % 64 || c->latent % 128 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
     if (c->latent > 8192 || c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024)
         return LMOE_ERR_UNSUPPORTED_SHAPE;
     // 32-bit row coordinates of the TMA descriptors and permuted-row indices
-    if (int64_t(c->n_experts) * c->latent >= (int64_t(1) << 31) ||
+    if (int64_t(c->n_experts) * c->latent * (c->inter / 64) >= (int64_t(1) << 31) ||
+        int64_t(c->n_experts) * c->inter * (c->latent / 64) >= (int64_t(1) << 31) ||
+        int64_t(c->n_experts) * c->latent >= (int64_t(1) << 31) ||
         int64_t(c->n_experts) * c->inter >= (int64_t(1) << 31) ||
         c->max_tokens * c->top_k >= (int64_t(1) << 31))
         return LMOE_ERR_UNSUPPORTED_SHAPE;
@@ -207,20 +211,45 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
     h->bn_down = (L % 256 == 0) ? 256 : 128;
     h->bn_shared = (S % 128 == 0) ? 256 : 128;
     h->bn_exp1 = (I % 128 == 0) ? 256 : 128;
-    h->bn_exp3 = (L % 256 == 0) ? 256 : 128;
+    h->bn_exp3 = (L % 256 == 0) ? 256 : 128;   // latent % 128 == 0: the boxes tile each expert's W3
     h->bn_up = (d % 256 == 0) ? 256 : 128;
     // router: 256-wide N tiles unless E fits one 128-wide tile
     h->bn_router = (E > 128) ? 256 : 128;
+    // Repack W1, W2 (boxes of bn_exp1/2 rows) and W3 (boxes of bn_exp3 rows)
+    // so each box is one contiguous block of HBM.
+    const int tr12 = h->bn_exp1 / 2, tr3 = h->bn_exp3;
+    const size_t bytes12 = size_t(E) * I * L * 2, bytes3 = size_t(E) * L * I * 2;
+    if (cudaMalloc(&h->w1p, bytes12) != cudaSuccess || cudaMalloc(&h->w2p, bytes12) != cudaSuccess ||
+        cudaMalloc(&h->w3p, bytes3) != cudaSuccess) {
+        cudaFree(h->w1p);
+        cudaFree(h->w2p);
+        cudaFree(h->w3p);
+        delete h;
+        return LMOE_ERR_CUDA;
+    }
+    if (launch_pack_tiles(w->w1, E, static_cast<int>(I), static_cast<int>(L), tr12, h->w1p, 0) != cudaSuccess ||
+        launch_pack_tiles(w->w2, E, static_cast<int>(I), static_cast<int>(L), tr12, h->w2p, 0) != cudaSuccess ||
+        launch_pack_tiles(w->w3, E, static_cast<int>(L), static_cast<int>(I), tr3, h->w3p, 0) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(h->w1p);
+        cudaFree(h->w2p);
+        cudaFree(h->w3p);
+        delete h;
+        return LMOE_ERR_CUDA;
+    }
     bool ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->bn_down) &&
               make_map(&h->m_wrouter, w->w_router, E, L, L, h->bn_router) &&
               make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
               make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
-              make_map(&h->m_w1, w->w1, E * I, L, L, h->bn_exp1 / 2) &&
-              make_map(&h->m_w2, w->w2, E * I, L, L, h->bn_exp1 / 2) &&
-              make_map(&h->m_w3, w->w3, E * L, I, I, h->bn_exp3) &&
+              make_map(&h->m_w1, h->w1p, E * I * (L / 64), 64, 64, tr12) &&
+              make_map(&h->m_w2, h->w2p, E * I * (L / 64), 64, 64, tr12) &&
+              make_map(&h->m_w3, h->w3p, E * L * (I / 64), 64, 64, tr3) &&
               make_map(&h->m_wup, w->w_up, d, L, L, h->bn_up) &&
               make_map(&h->m_ws3, w->ws3, d, S, S, h->bn_up);
     if (!ok) {
+        cudaFree(h->w1p);
+        cudaFree(h->w2p);
+        cudaFree(h->w3p);
         delete h;
         return LMOE_ERR_CUDA;
     }
@@ -247,6 +276,9 @@ int lmoe_destroy(lmoe_handle *h) {
     if (!h) return LMOE_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
     cudaError_t f = cudaFree(h->d_status);
+    cudaFree(h->w1p);
+    cudaFree(h->w2p);
+    cudaFree(h->w3p);
     if (h->side) cudaStreamDestroy(h->side);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
@@ -423,6 +455,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.n_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.b_expert_rows = static_cast<int32_t>(I);
+        a.b_packed = 1;
+        a.b_row_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
         a.tiles = tiles2;
         a.n_mtiles = nmt + 1;
         a.gather_src = hbuf;
@@ -443,6 +477,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_exp3));
         a.k_blocks = static_cast<int32_t>(I / kBK);
         a.b_expert_rows = static_cast<int32_t>(L);
+        a.b_packed = 1;
+        a.b_row_tiles = static_cast<int32_t>(L / h->bn_exp3);
         a.tiles = tiles;
         a.n_mtiles = nmt;
         a.out = obuf;

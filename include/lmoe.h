@@ -71,8 +71,11 @@ typedef struct {
 } lmoe_config;
 
 /* Weight pointers (device, bf16, row-major, K-major rows as "out x in").
- * The handle keeps these POINTERS: the caller must keep the weights alive and
- * unchanged until lmoe_destroy.  S = n_shared * shared_inter. */
+ * w1, w2 and w3 are COPIED at lmoe_create into a handle-owned, tile-contiguous
+ * order (one more copy of the routed weights in device memory); the caller may
+ * free or change them afterwards.  For the other six the handle keeps the
+ * POINTERS: the caller must keep them alive and unchanged until lmoe_destroy.
+ * S = n_shared * shared_inter. */
 typedef struct {
     const uint16_t *w_down;   /* [latent][d]           down-projection            */
     const uint16_t *w_router; /* [n_experts][latent]   router rows                */
@@ -87,8 +90,9 @@ typedef struct {
 
 typedef struct lmoe_handle lmoe_handle;
 
-/* Validate `cfg`, check the device (sm_103), and build the handle: the TMA
- * descriptors of the weights and a small device status word.  On success
+/* Validate `cfg`, check the device (sm_103), and build the handle: the
+ * repacked routed weights, the TMA descriptors of all weights and a small
+ * device status word (LMOE_ERR_CUDA if the copy does not fit).  On success
  * *out owns a handle to release with lmoe_destroy.  Synchronous. */
 int lmoe_create(const lmoe_config *cfg, const lmoe_weights *weights, lmoe_handle **out);
 

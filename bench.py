@@ -8,16 +8,18 @@ Inputs are seeded synthetic data of that shape (see sparse_moe_layer_bias_gb300
 /synth.py); weights (10.3 GB) and activations are resident in HBM.
 
 Also measured in the same run (reported inside the one JSON line):
-  * e2e: the same step with x/bias copied from pinned host memory and y/bias
-    copied back, inside the timed region;
+  * e2e: the same step through the host-memory entry point (lmoe_forward_host):
+    x/bias copied in from pinned host memory and y/bias copied back every
+    step, inside the timed region, pipelined across steps;
   * the K3 decode layer (T=64) and the QB histogram at T=2^20 x 896;
   * per-stage kernel times from CUDA events on the launching stream, and the
     roofline of the dominant kernel against MEASURED_PEAKS.json;
   * cpu_baseline: the CPU oracle on a bounded sample of the same workload.
 
 `--impl reference` times the CPU oracle (the reference arm) instead.
-Multi-GPU (torchrun): every rank runs its own batch (replicas, no collective
-on the data path; "scaling": "weak").
+Multi-GPU (torchrun): every rank runs its own batch ("scaling": "weak"); the
+layer needs no exchange, and QB's one exchange step -- the sum of the ranks'
+histograms before the quantile read -- is an NCCL all-reduce of [E][B] int32.
 """
 from __future__ import annotations
 
@@ -229,6 +231,33 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- ncu case
+def qb_closed_loop(lm, stream, T=8192, E=896, k=16, n=12):
+    """The balancing loop on the GPU over a stationary stream of skewed score
+    batches (per-expert logit means mu_e ~ N(0, 0.5^2), fresh noise per batch):
+    route batch i with the current bias (top-k kernels), then set the bias from
+    batch i by QB (B = 1000 or 10000 bins) or move it by the fixed-step rule.
+    Reports max/mean expert load per batch for each rule."""
+    batches = synth.qb_score_stream(T, E, n, seed=synth.QB_SEED + 1, device="cuda")
+    level = 1.0 - k / E
+    rules = {"qb_B1000": ("qb", 1000), "qb_B10000": ("qb", 10000),
+             "sign_step1e-3": ("sign", 1e-3), "sign_step1e-2": ("sign", 1e-2)}
+    out = {"T": T, "E": E, "top_k": k, "batches": n, "metric": "max/mean expert load per batch"}
+    for name, (rule, p) in rules.items():
+        b = torch.zeros(E, dtype=torch.float32, device="cuda")
+        ratios = []
+        for i in range(n):
+            counts = lm.lmoe_route_static(batches[i], b, k, stream=stream)["counts"]
+            ratios.append(counts.max() / counts.float().mean())
+            if rule == "qb":
+                _, b = lm.qb_quantile_bias(lm.qb_histogram(batches[i], p, stream=stream), level, stream=stream)
+            else:
+                lm.qb_sign_update(counts, p, b, stream=stream)
+        out[name] = [round(float(r), 3) for r in ratios]
+    del batches
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_profile_case(args):
     """A few forwards of a reduced K3-width layer (E=256, T=2048, Zipf-skewed
     router like the K3 prefill workload: ~3.3 GB on the device) and a QB
@@ -285,6 +314,7 @@ def main():
         __graft_entry__.build()
     barrier(world)
     import sparse_moe_layer_bias_gb300 as lm
+    from sparse_moe_layer_bias_gb300.dist import qb_allreduce_histogram
     lm.load_library()
     peaks, peak_src = load_peaks()
 
@@ -307,6 +337,7 @@ def main():
         lm.lmoe_forward(handle, xin, bin_, y=yout, workspace=ws, scores_out=scores,
                         expert_counts_out=counts, stream=stream)
         lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
+        qb_allreduce_histogram(hist)          # data-parallel QB: sum over ranks (no-op at N=1)
         lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
 
     kernels_per_step = len(lm.STAGES) + 2      # 11 forward kernels + QB histogram + quantile
@@ -336,6 +367,7 @@ def main():
                             expert_counts_out=counts, stream=stream)
             qb_ev[i][0].record(stream)
             lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
+            qb_allreduce_histogram(hist)
             lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
             qb_ev[i][1].record(stream)
         t_end.record(stream)
@@ -387,21 +419,41 @@ def main():
     tflops = total_flop / (layer_ms * 1e-3) / 1e12
 
     # --------------------------------------------------------------- e2e (host buffers)
+    # The library's host-memory entry point, pipelined across steps: every step
+    # copies its x and bias in from pinned host memory (input copy stream),
+    # runs the forward + QB, and copies y and the new bias back out; a step's
+    # input copy overlaps the forward before it, its output copy the one after.
     x_host = x.cpu().pin_memory()
     b_host = bias.cpu().pin_memory()
     y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    bn_host = torch.empty(E, dtype=torch.float32).pin_memory()
-    x_dev, b_dev = torch.empty_like(x), torch.empty_like(bias)
+    io = lm.alloc_host_io(handle)
+    # the new QB bias also goes back to the host each step; its small copy runs
+    # on a stream of its own (two slots) so that it never waits, on the compute
+    # stream, behind the large output copy on the same copy engine
+    bn_dev = [torch.empty(E, dtype=torch.float32, device="cuda") for _ in range(2)]
+    bn_host = [torch.empty(E, dtype=torch.float32).pin_memory() for _ in range(2)]
+    bn_copied = [torch.cuda.Event(), torch.cuda.Event()]
+    bn_stream = torch.cuda.Stream()
+    n_e2e = [0]
 
     def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        b_dev.copy_(b_host, non_blocking=True)
-        step(x_dev, b_dev, y)
-        y_host.copy_(y, non_blocking=True)
-        bn_host.copy_(b_new, non_blocking=True)
+        j = n_e2e[0] & 1
+        n_e2e[0] += 1
+        lm.lmoe_forward_host(handle, x_host, b_host, y_host, io, ws, scores_out=scores,
+                             expert_counts_out=counts, stream=stream)
+        lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
+        qb_allreduce_histogram(hist)          # data-parallel QB: sum over ranks (no-op at N=1)
+        stream.wait_event(bn_copied[j])       # the copy that last read bn_dev[j] is done
+        lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=bn_dev[j], stream=stream)
+        bn_stream.wait_stream(stream)
+        with torch.cuda.stream(bn_stream):
+            bn_host[j].copy_(bn_dev[j], non_blocking=True)
+            bn_copied[j].record(bn_stream)
 
     for _ in range(args.warmup):
         e2e_step()
+    lm.lmoe_host_wait(handle, stream)
+    stream.wait_stream(bn_stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -409,9 +461,13 @@ def main():
     e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
+    lm.lmoe_host_wait(handle, stream)      # the last step's y has reached host memory
+    stream.wait_stream(bn_stream)          # and its bias
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
+    assert torch.equal(y_host.view(torch.int16), y.cpu().view(torch.int16))
+    assert torch.equal(bn_host[(n_e2e[0] - 1) & 1], b_new.cpu())
     h2d = x.numel() * 2 + bias.numel() * 4
     d2h = y.numel() * 2 + E * 4
 
@@ -434,6 +490,7 @@ def main():
     qb_gbs = qb_bytes / (qb_ms * 1e-3) / 1e9
     del sq
     torch.cuda.empty_cache()
+    qb_loop = qb_closed_loop(lm, stream)
 
     # --------------------------------------------------------------- decode layer T = 64
     dshape = synth.K3_DECODE
@@ -486,7 +543,7 @@ def main():
                                "E=896, top-16, I=512, 2 shared experts x 1024 + QB histogram B=1000 + "
                                "quantile bias",
                    "T": T, "l2": "inputs larger than L2 (10.3 GB of weights streamed per step)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"dp{world} (QB histograms all-reduced)" if world > 1 else "dp1"},
         "layer_tflops": round(tflops, 2),
         "frac_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
         "roofline": roof,
@@ -494,6 +551,7 @@ def main():
         "qb_ms_in_step": round(stage_ms["qb"], 4),
         "qb_hist_sweep": {"T": Tq, "E": E, "B": QB_B, "ms": round(qb_ms, 4), "gbs": round(qb_gbs, 1),
                           "frac_hbm": round(qb_gbs / peaks["hbm_gbs"], 4)},
+        "qb_closed_loop": qb_loop,
         "decode": {"T": dshape.T, "ms": round(dec_ms, 4), "tokens_per_s": dshape.T / (dec_ms * 1e-3),
                    "touched_experts": touched_d, "bytes": dec_bytes, "gbs": round(dec_gbs, 1),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},

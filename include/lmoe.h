@@ -68,6 +68,12 @@ typedef struct {
     float beta2;          /* linear-branch softcap; 25 in K3 ([DD] section 1) */
     float rms_eps;        /* epsilon inside the RMSNorm square root (1e-6)    */
     int64_t max_tokens;   /* largest T a forward call will be given           */
+    int32_t norm_after_down; /* 0: K3's layer.  1: ablation variant with a
+                           * second un-weighted RMSNorm right after the
+                           * down-projection, h = RMSNorm(W_down x), which the
+                           * router and the experts then see ([DD] section 2,
+                           * [IN] "RMSNorm insertion": the variant the ablation
+                           * dropped) */
 } lmoe_config;
 
 /* Weight pointers (device, bf16, row-major, K-major rows as "out x in").
@@ -122,12 +128,14 @@ typedef struct {
     int64_t o;        /* [T*top_k][latent] bf16  gate-weighted expert outputs, assignment order */
     int64_t r;        /* [T][latent] bf16        RMS-normalised aggregate          */
     int64_t shared_act; /* [T][S] bf16           shared-expert activations        */
+    int64_t h_norm;   /* [T][latent] bf16        RMSNorm(h) when norm_after_down, else -1 */
 } lmoe_ws_layout;
 
 int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *layout);
 
 /* One forward pass of the Stable LatentMoE layer on T tokens:
  *   h  = W_down x                              (a1; [DD] section 2)
+ *        (norm_after_down: h = RMSNorm(W_down x), same eps, no weight)
  *   s  = sigmoid(W_router h)                   (a2; routing in the latent)
  *   u  = fp32(s + bias); pick the top_k experts by u (ties: lower id)
  *        gates = s at the chosen experts       (a3; [DD] section 3, [NW])
@@ -147,6 +155,39 @@ int lmoe_forward(lmoe_handle *handle, const uint16_t *x, int64_t T, const float 
                  uint16_t *y, float *scores_out, int32_t *topk_idx_out, float *gates_out,
                  int32_t *expert_counts_out, void *workspace, size_t workspace_bytes,
                  cudaStream_t stream);
+
+/* Bytes of device staging memory lmoe_forward_host needs: two slots, each
+ * holding x [max_tokens][d] bf16, bias [n_experts] fp32 and y [max_tokens][d]
+ * bf16 (256-byte aligned sub-buffers).  The size depends only on the handle. */
+int lmoe_host_io_size(const lmoe_handle *handle, size_t *bytes);
+
+/* lmoe_forward from and to HOST memory, pipelined across calls.  Enqueues,
+ * without waiting for any of it:
+ *   1. on the handle's input copy stream, once the forward that last read
+ *      staging slot (call number % 2) is done: x_host [T][d] bf16 and
+ *      bias_host [n_experts] fp32 into that slot of io_dev;
+ *   2. on `stream`, once copy 1 has landed and the output copy that last read
+ *      the slot's y is done: lmoe_forward (y into the slot; the optional
+ *      device outputs and the workspace as in lmoe_forward);
+ *   3. on the handle's output copy stream, once 2 is done: y into y_host.
+ * So the input copy of one call overlaps the forward of the one before, and
+ * its output copy the forward of the one after.  y_host holds the result once
+ * `stream` has passed a later lmoe_host_wait (or after a device
+ * synchronisation).  The caller keeps x_host and bias_host unchanged, and
+ * y_host untouched, until then.  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously.
+ * io_dev: lmoe_host_io_size bytes, 256-byte aligned, used only through this
+ * call.  Errors are reported before anything is enqueued, as in lmoe_forward.
+ * One host thread and one `stream` per handle at a time.  The pages describe
+ * no host-memory interface; this is an addition of this library. */
+int lmoe_forward_host(lmoe_handle *handle, const uint16_t *x_host, int64_t T, const float *bias_host,
+                      uint16_t *y_host, float *scores_out, int32_t *topk_idx_out, float *gates_out,
+                      int32_t *expert_counts_out, void *io_dev, size_t io_bytes, void *workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
+/* Make `stream` wait for every output copy lmoe_forward_host has enqueued so
+ * far (enqueues a wait; does not block the host). */
+int lmoe_host_wait(lmoe_handle *handle, cudaStream_t stream);
 
 /* Stages of lmoe_forward, in launch order (for lmoe_set_stage_events). */
 typedef enum {
@@ -221,6 +262,17 @@ int qb_histogram(const float *scores, int64_t T, int32_t E, int64_t ld, int32_t 
  * hist: [E][B] uint32; quantile_out: [E] fp32 (nullable); bias_out: [E] fp32. */
 int qb_quantile_bias(const uint32_t *hist, int32_t E, int32_t B, double level,
                      float *quantile_out, float *bias_out, cudaStream_t stream);
+
+/* The fixed-step selection-bias update that Quantile Balancing replaces, for
+ * closed-loop comparisons ("Notes on the MoE and Attention of K3", paragraph
+ * on Quantile Balancing: K2 changed each expert's bias by a constant amount
+ * per update, which the page likens to SignSGD).  Reading:
+ *   mean = sum(counts) / E;  bias[e] += gamma * sign(mean - counts[e]),
+ * sign(0) = 0, the comparison exact in integers, the add one fp32 addition.
+ * counts: [E] int32 assignments per expert (e.g. lmoe_forward's
+ * expert_counts_out); bias: [E] fp32, updated in place.  1 <= E <= 65536;
+ * device pointers, 16-byte aligned; argument errors enqueue nothing. */
+int qb_sign_update(const int32_t *counts, int32_t E, float gamma, float *bias, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -56,6 +56,7 @@ class LayerConfig:
     beta1: float = 4.0
     beta2: float = 25.0
     rms_eps: float = 1e-6
+    norm_after_down: bool = False   # ablation variant: RMSNorm on h as well
 
     def c(self) -> OrcConfig:
         return OrcConfig(self.d, self.latent, self.n_experts, self.top_k, self.inter,
@@ -79,6 +80,7 @@ def _load():
             "orc_softcap": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
             "orc_situ": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
             "orc_down_proj": (None, [cfg, _I64, _P, _P, _P]),
+            "orc_rms_rows": (None, [_I64, _I64, ctypes.c_double, _P, _P]),
             "orc_router": (None, [cfg, _I64, _P, _P, _P]),
             "orc_topk": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
             "orc_permute": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
@@ -87,6 +89,7 @@ def _load():
             "orc_up_shared": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
             "orc_qb_histogram": (None, [_P, _I64, _I32, _I64, _I32, _P, ctypes.c_int]),
             "orc_qb_quantile_bias": (None, [_P, _I32, _I32, ctypes.c_double, _P, _P]),
+            "orc_sign_update": (None, [_P, _I32, ctypes.c_float, _P]),
             "orc_num_threads": (ctypes.c_int, []),
         }
         for name, (res, args) in sig.items():
@@ -153,6 +156,16 @@ def down_proj(cfg: LayerConfig, x, w_down):
     c = cfg.c()
     _load().orc_down_proj(ctypes.byref(c), T, _ptr(x), _ptr(w_down), _ptr(h))
     return h
+
+
+def rms_rows(cfg: LayerConfig, h):
+    """Un-weighted RMSNorm of each bf16 row of h (the ablation variant's norm
+    after the down-projection); returns bf16 bits."""
+    h = _need(h, np.uint16)
+    T, L = h.shape
+    out = np.empty_like(h)
+    _load().orc_rms_rows(T, L, float(cfg.rms_eps), _ptr(h), _ptr(out))
+    return out
 
 
 def router(cfg: LayerConfig, h, w_router):
@@ -271,14 +284,15 @@ def layer_forward(cfg: LayerConfig, x, w, bias):
     """The whole layer, step by step.  ``w`` maps names to bf16 bit arrays:
     w_down [L,d], w_router [E,L], w1/w2 [E,I,L] (or dicts of used experts),
     w3 [E,L,I], ws1/ws2 [nS*Is,d], ws3 [d,nS*Is], w_up [d,L]."""
-    h = down_proj(cfg, x, w["w_down"])
+    h_raw = down_proj(cfg, x, w["w_down"])
+    h = rms_rows(cfg, h_raw) if cfg.norm_after_down else h_raw
     s = router(cfg, h, w["w_router"])
     idx, gate, margin = topk(cfg, s, bias)
     counts, offsets, perm, inv = permute(cfg, idx)
     rt = routed(cfg, h, idx, gate, w["w1"], w["w2"], w["w3"])
     a_s = shared_act(cfg, x, w["ws1"], w["ws2"])
     y = up_shared(cfg, rt["r"], a_s, w["w_up"], w["ws3"])
-    return {"h": h, "s": s, "idx": idx, "gate": gate, "margin": margin, "counts": counts,
+    return {"h_raw": h_raw, "h": h, "s": s, "idx": idx, "gate": gate, "margin": margin, "counts": counts,
             "offsets": offsets, "perm": perm, "inv": inv, "z": rt["z"], "r": rt["r"],
             "r64": rt["r64"], "a_s": a_s, "y": y}
 
@@ -307,3 +321,17 @@ def qb_quantile_bias(hist, level: float):
     b = np.empty(E, np.float32)
     _load().orc_qb_quantile_bias(_ptr(hist), E, B, float(level), _ptr(q), _ptr(b))
     return q, b
+
+
+def sign_update(counts, gamma: float, bias):
+    """The fixed-step (SignSGD-like) bias update QB replaces; returns the new
+    fp32 bias (the input is not modified)."""
+    counts = _need(counts, np.int32)
+    out = np.array(bias, dtype=np.float32, copy=True)
+    _load().orc_sign_update(_ptr(counts), counts.shape[0], float(np.float32(gamma)), _ptr(out))
+    return out
+
+
+def expert_loads(idx, n_experts: int):
+    """Assignments per expert of a top-k index array [T][k] (int32)."""
+    return np.bincount(np.asarray(idx).reshape(-1), minlength=n_experts).astype(np.int32)

@@ -148,6 +148,31 @@ void orc_down_proj(const orc_config *c, int64_t T, const uint16_t *x,
             h_out[t * L + l] = orc_f64_to_bf16(dot_bf16(w_down + l * d, x + t * d, d));
 }
 
+/* Ablation variant: RMSNorm also after the down-projection.  [DD] section 2
+ * and [IN] "RMSNorm insertion": the first design put one RMSNorm after the
+ * reduction d -> d/2 and one before the expansion; the ablation kept only the
+ * second.  This is the first one, for running that variant:
+ *   hn[t] = h[t] / sqrt(mean_l h[t][l]^2 + eps)
+ * on the bf16 latent h (decoded exactly), in fp64, rounded once to bf16.
+ * Reading: un-weighted, with the same eps as the norm before the
+ * up-projection. */
+void orc_rms_rows(int64_t T, int64_t L, double eps, const uint16_t *h, uint16_t *hn)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int64_t l = 0; l < L; ++l) {
+            const double v = orc_bf16_to_f64(h[t * L + l]);
+            ss += v * v;
+        }
+        const double rms = sqrt(ss / (double)L + eps);
+        for (int64_t l = 0; l < L; ++l) {
+            const double v = orc_bf16_to_f64(h[t * L + l]);
+            hn[t * L + l] = orc_f64_to_bf16(rms > 0.0 ? v / rms : 0.0);
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* a2: router scores in the latent                                           */
 /* ------------------------------------------------------------------------ */
@@ -446,6 +471,33 @@ void orc_qb_quantile_bias(const uint32_t *hist, int32_t E, int32_t B, double lev
         }
         if (q_out) q_out[e] = (float)q;
         b_out[e] = (float)(-q);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The fixed-step bias update QB replaces (closed-loop comparison)           */
+/* ------------------------------------------------------------------------ */
+
+/* [NW] "Keeping the numbers in range" and [DD] section 3: K2's loss-free
+ * balancing changed each expert's selection bias by a constant amount per
+ * update, in the direction of its load error only (the page likens it to
+ * SignSGD).  Reading (the pages give no formula):
+ *   mean   = (counts[0] + ... + counts[E-1]) / E
+ *   b[e]  += gamma * sign(mean - counts[e]),   sign(0) = 0
+ * An under-loaded expert's bias rises, an over-loaded one's falls.  The
+ * comparison is done exactly in integers (counts[e] * E against the total);
+ * the add is one fp32 addition. */
+void orc_sign_update(const int32_t *counts, int32_t E, float gamma, float *bias)
+{
+    int64_t total = 0;
+    for (int64_t e = 0; e < E; ++e)
+        total += counts[e];
+    for (int64_t e = 0; e < E; ++e) {
+        const int64_t scaled = (int64_t)counts[e] * (int64_t)E;
+        if (scaled < total)
+            bias[e] = bias[e] + gamma;
+        else if (scaled > total)
+            bias[e] = bias[e] - gamma;
     }
 }
 

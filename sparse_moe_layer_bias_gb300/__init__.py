@@ -9,12 +9,16 @@ from .binding import (  # noqa: F401
     EXPORTED,
     Handle,
     LmoeError,
+    alloc_host_io,
     alloc_workspace,
     library_path,
     lmoe_create,
     lmoe_destroy,
     lmoe_device_status,
     lmoe_forward,
+    lmoe_forward_host,
+    lmoe_host_io_size,
+    lmoe_host_wait,
     lmoe_route_static,
     lmoe_set_stage_events,
     STAGES,
@@ -24,4 +28,5 @@ from .binding import (  # noqa: F401
     load_library,
     qb_histogram,
     qb_quantile_bias,
+    qb_sign_update,
 )

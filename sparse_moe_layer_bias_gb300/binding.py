@@ -20,8 +20,9 @@ STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED_SHAP
           6: "LMOE_ERR_TIMEOUT", 7: "LMOE_ERR_NO_DEVICE"}
 
 EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size",
-            "lmoe_workspace_layout", "lmoe_forward", "lmoe_device_status", "lmoe_set_stage_events",
-            "lmoe_route_static", "qb_histogram", "qb_quantile_bias")
+            "lmoe_workspace_layout", "lmoe_forward", "lmoe_host_io_size", "lmoe_forward_host",
+            "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_route_static",
+            "qb_histogram", "qb_quantile_bias", "qb_sign_update")
 
 STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12", "expert_w3",
           "combine", "up")
@@ -38,7 +39,7 @@ class LmoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("shared_inter", ctypes.c_int32), ("beta1", ctypes.c_float),
                 ("beta2", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("max_tokens", ctypes.c_int64)]
+                ("max_tokens", ctypes.c_int64), ("norm_after_down", ctypes.c_int32)]
 
 
 WEIGHT_NAMES = ("w_down", "w_router", "w1", "w2", "w3", "ws1", "ws2", "ws3", "w_up")
@@ -50,7 +51,7 @@ class LmoeWeights(ctypes.Structure):
 
 class LmoeWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("h", "scores", "topk_idx", "gates", "counts", "offsets",
-                                              "perm", "inv", "act", "o", "r", "shared_act")]
+                                              "perm", "inv", "act", "o", "r", "shared_act", "h_norm")]
 
 
 def library_path() -> str:
@@ -80,6 +81,12 @@ def load_library():
     lib.lmoe_workspace_layout.argtypes = [P, I64, ctypes.POINTER(LmoeWsLayout)]
     lib.lmoe_forward.restype = ctypes.c_int
     lib.lmoe_forward.argtypes = [P, P, I64, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.lmoe_host_io_size.restype = ctypes.c_int
+    lib.lmoe_host_io_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.lmoe_forward_host.restype = ctypes.c_int
+    lib.lmoe_forward_host.argtypes = [P, P, I64, P, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P]
+    lib.lmoe_host_wait.restype = ctypes.c_int
+    lib.lmoe_host_wait.argtypes = [P, P]
     lib.lmoe_device_status.restype = ctypes.c_int
     lib.lmoe_device_status.argtypes = [P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.lmoe_set_stage_events.restype = ctypes.c_int
@@ -88,6 +95,8 @@ def load_library():
     lib.lmoe_route_static.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P]
     lib.qb_histogram.restype = ctypes.c_int
     lib.qb_histogram.argtypes = [P, I64, I32, I64, I32, P, ctypes.c_int, P]
+    lib.qb_sign_update.restype = ctypes.c_int
+    lib.qb_sign_update.argtypes = [P, I32, ctypes.c_float, P, P]
     lib.qb_quantile_bias.restype = ctypes.c_int
     lib.qb_quantile_bias.argtypes = [P, I32, I32, ctypes.c_double, P, P, P]
     _lib = lib
@@ -144,13 +153,13 @@ class Handle:
 
 def lmoe_create(cfg: dict, weights: dict, max_tokens: int) -> Handle:
     """cfg: d, latent, n_experts, top_k, inter, n_shared, shared_inter and
-    optional beta1, beta2, rms_eps.  weights: bf16 CUDA tensors named as in
+    optional beta1, beta2, rms_eps, norm_after_down.  weights: bf16 CUDA tensors named as in
     lmoe_weights."""
     lib = load_library()
     c = LmoeConfig(int(cfg["d"]), int(cfg["latent"]), int(cfg["n_experts"]), int(cfg["top_k"]),
                    int(cfg["inter"]), int(cfg["n_shared"]), int(cfg["shared_inter"]),
                    float(cfg.get("beta1", 4.0)), float(cfg.get("beta2", 25.0)),
-                   float(cfg.get("rms_eps", 1e-6)), int(max_tokens))
+                   float(cfg.get("rms_eps", 1e-6)), int(max_tokens), int(bool(cfg.get("norm_after_down", False))))
     held = {}
     w = LmoeWeights()
     for n in WEIGHT_NAMES:
@@ -208,6 +217,54 @@ def lmoe_forward(handle: Handle, x: torch.Tensor, bias: torch.Tensor, y: torch.T
                           _ptr(workspace), workspace.numel(), _stream(stream))
     _check("lmoe_forward", st)
     return y
+
+
+def _host(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def lmoe_host_io_size(handle: Handle) -> int:
+    n = ctypes.c_size_t()
+    _check("lmoe_host_io_size", load_library().lmoe_host_io_size(handle.ptr, ctypes.byref(n)))
+    return n.value
+
+
+def alloc_host_io(handle: Handle, device=None) -> torch.Tensor:
+    return torch.empty(lmoe_host_io_size(handle), dtype=torch.uint8, device=device or "cuda")
+
+
+def lmoe_forward_host(handle: Handle, x_host: torch.Tensor, bias_host: torch.Tensor, y_host: torch.Tensor,
+                      io: torch.Tensor, workspace: torch.Tensor, scores_out=None, topk_idx_out=None,
+                      gates_out=None, expert_counts_out=None, stream=None) -> torch.Tensor:
+    """Pipelined forward from host tensors (pin them for asynchronous copies).
+    Returns y_host, which is complete once `stream` has passed a later
+    lmoe_host_wait."""
+    lib = load_library()
+    x_host = _host(x_host, torch.bfloat16, "x_host")
+    bias_host = _host(bias_host, torch.float32, "bias_host")
+    y_host = _host(y_host, torch.bfloat16, "y_host")
+    if y_host.shape != x_host.shape:
+        raise ValueError("y_host must have x_host's shape")
+    io = _dev(io, torch.uint8, "io")
+    workspace = _dev(workspace, torch.uint8, "workspace")
+    st = lib.lmoe_forward_host(handle.ptr, _ptr(x_host), x_host.shape[0], _ptr(bias_host), _ptr(y_host),
+                               _ptr(_dev(scores_out, torch.float32, "scores_out")),
+                               _ptr(_dev(topk_idx_out, torch.int32, "topk_idx_out")),
+                               _ptr(_dev(gates_out, torch.float32, "gates_out")),
+                               _ptr(_dev(expert_counts_out, torch.int32, "expert_counts_out")),
+                               _ptr(io), io.numel(), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("lmoe_forward_host", st)
+    return y_host
+
+
+def lmoe_host_wait(handle: Handle, stream=None):
+    _check("lmoe_host_wait", load_library().lmoe_host_wait(handle.ptr, _stream(stream)))
 
 
 def lmoe_set_stage_events(handle: Handle, events):
@@ -280,3 +337,15 @@ def qb_quantile_bias(hist: torch.Tensor, level: float, quantile_out=None, bias_o
         _ptr(hist), E, B, float(level), _ptr(_dev(quantile_out, torch.float32, "quantile_out")),
         _ptr(_dev(bias_out, torch.float32, "bias_out")), _stream(stream)))
     return quantile_out, bias_out
+
+
+def qb_sign_update(counts: torch.Tensor, gamma: float, bias: torch.Tensor, stream=None) -> torch.Tensor:
+    """bias[e] += gamma * sign(mean(counts) - counts[e]) in place (the
+    fixed-step rule QB replaces); returns bias."""
+    counts = _dev(counts, torch.int32, "counts")
+    bias = _dev(bias, torch.float32, "bias")
+    if counts.numel() != bias.numel():
+        raise ValueError("counts and bias must have one entry per expert")
+    _check("qb_sign_update", load_library().qb_sign_update(_ptr(counts), counts.numel(), float(gamma),
+                                                           _ptr(bias), _stream(stream)))
+    return bias

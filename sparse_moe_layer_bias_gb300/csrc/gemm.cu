@@ -476,7 +476,7 @@ size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256, false>::kSmem : Cfg
         return launch_one<BN_, AM_, BM_, EPI_, G_>(maps, args, grid, stream);
 
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
-                        const GemmArgs &args, int grid, cudaStream_t stream) {
+                        const GemmArgs &args, int grid, cudaStream_t stream, bool pair) {
     // a1 down-projection, a8 up-projection + shared W3
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_BF16, false)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_BF16, false)
@@ -488,11 +488,17 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     // a2 router scores
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
-    // a5 routed experts W1|W2 (token rows gathered per expert, pair tiles of
-    // 256 rows) with the SiTU-GLU epilogue
+    // a5 routed experts W1|W2 (token rows gathered per expert) with the
+    // SiTU-GLU epilogue: pair tiles of 256 rows for experts with many tokens,
+    // 128-row tiles (smaller stages, one more of them in flight) for the others
     if (am == A_GATHER && bm == B_GLU && epi == EPI_SITU_GLU && grouped) {
-        if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
-        if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
+        if (pair) {
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
+        } else {
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream);
+        }
     }
     // a6 routed experts W3 with the gate-weighted scatter
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)

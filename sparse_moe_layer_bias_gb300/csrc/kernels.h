@@ -54,11 +54,12 @@ struct GemmArgs {
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
 
-// Launch one persistent GEMM.  `bn` in {128, 256}.  A_GATHER runs pair tiles
-// (two 128-row sub-tiles sharing each weight stage).  Returns cudaErrorInvalidValue
-// for a combination that is not compiled.
+// Launch one persistent GEMM.  `bn` in {128, 256}.  With `pair`, A_GATHER runs
+// pair tiles (two 128-row sub-tiles sharing each weight stage); without, 128-row
+// tiles with a deeper stage ring.  Returns cudaErrorInvalidValue for a
+// combination that is not compiled.
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
-                        const GemmArgs &args, int grid, cudaStream_t stream);
+                        const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false);
 size_t gemm_smem_bytes(int bn);
 
 // Repack per-expert weights [E][R][K] (row-major bf16) into tile-contiguous
@@ -73,11 +74,13 @@ cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E
                         cudaStream_t stream);
 cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words_per_expert,
                                uint32_t *word_prefix, int32_t *counts, cudaStream_t stream);
-// tiles: up to 128 rows each (ceil(count/128) per expert); tiles2: pair tiles
-// of up to 256 rows (ceil(count/256) per expert).
+// tiles: up to 128 rows each (ceil(count/128) per expert).  With tiles3 ==
+// nullptr, tiles2 holds pair tiles of up to 256 rows for every expert
+// (ceil(count/256) each); otherwise tiles2 holds them only for experts with
+// more than 128 rows and tiles3 one tile for each expert with 1..128 rows.
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
-                                 int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2,
-                                 cudaStream_t stream);
+                                 int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2, int4 *tiles3,
+                                 int32_t *n_mtiles3, cudaStream_t stream);
 cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words_per_expert,
                            const int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *tokrow,
@@ -90,6 +93,7 @@ cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, f
 // ------------------------------------------------------------------ QB
 cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t ld, int B,
                                 uint32_t *hist, int accumulate, int num_sms, cudaStream_t stream);
+cudaError_t launch_sign_update(const int32_t *counts, int E, float gamma, float *bias, cudaStream_t stream);
 cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level, float *q,
                                float *bias, cudaStream_t stream);
 

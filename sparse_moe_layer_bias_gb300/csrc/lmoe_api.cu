@@ -27,10 +27,11 @@ struct lmoe_handle {
     // routed experts' weights repacked tile-contiguously (handle-owned)
     uint16_t *w1p, *w2p, *w3p;
     cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
-    // The shared experts' W1|W2 GEMM depends only on x: it runs on a side
-    // stream, on side_sms SMs, while the routed part runs on the others.
-    cudaStream_t side;
-    cudaEvent_t ev_fork, ev_join;
+    // lmoe_forward_host: input / output copy streams and, per staging slot, the
+    // events "input landed", "forward done" and "output copied".
+    cudaStream_t io_in, io_out;
+    cudaEvent_t ev_in[2], ev_fwd[2], ev_out[2];
+    unsigned io_calls;
 };
 
 namespace {
@@ -74,7 +75,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, tiles2, nmt, perm, inv, tokrow,
-        act, o, r, sact, total;
+        tiles3, act, o, r, sact, hn, total;
 };
 
 Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
@@ -101,6 +102,7 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.wprefix = take(size_t(E * words * 4));
     l.tiles = take(size_t((ceil_div(n, kBM) + E) * 16));
     l.tiles2 = take(size_t((ceil_div(n, 2 * kBM) + E) * 16));
+    l.tiles3 = take(size_t(E * 16));
     l.nmt = take(16);
     l.perm = take(size_t(n * 4));
     l.inv = take(size_t(n * 4));
@@ -109,6 +111,7 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.o = take(size_t(n * L * 2));
     l.r = take(size_t(T * L * 2));
     l.sact = take(size_t(T * S * 2));
+    l.hn = c.norm_after_down ? take(size_t(T * L * 2)) : none;
     l.total = off;
     return l;
 }
@@ -119,6 +122,7 @@ int validate_config(const lmoe_config *c) {
         c->n_shared <= 0 || c->shared_inter <= 0 || c->max_tokens < 0)
         return LMOE_ERR_INVALID_ARG;
     if (!(c->beta1 > 0.0f) || !(c->beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
+    if (c->norm_after_down != 0 && c->norm_after_down != 1) return LMOE_ERR_INVALID_ARG;
     const int64_t S = int64_t(c->n_shared) * c->shared_inter;
     if (c->d % 64 || c->latent % 128 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
     if (c->latent > 8192 || c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024)
@@ -156,12 +160,30 @@ GemmArgs base_args(const lmoe_handle *h) {
 
 int gemm_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
 
-// SMs given to the shared-expert GEMM while the routing and the routed
-// experts run on the rest (0: run it in stream order instead).
-int side_sms_for(const lmoe_handle *h, int64_t T) {
-    (void)T;
-    (void)h;
-    return 0;
+// Staging slot of lmoe_forward_host: x [max_tokens][d] bf16, bias [E] fp32,
+// y [max_tokens][d] bf16.
+struct IoSlot {
+    size_t x, bias, y, bytes;
+};
+
+IoSlot io_slot(const lmoe_config &c) {
+    IoSlot s;
+    const size_t xb = align256(size_t(c.max_tokens) * c.d * 2);
+    s.x = 0;
+    s.bias = xb;
+    s.y = xb + align256(size_t(c.n_experts) * 4);
+    s.bytes = s.y + xb;
+    return s;
+}
+
+void release_streams(lmoe_handle *h) {
+    if (h->io_in) cudaStreamDestroy(h->io_in);
+    if (h->io_out) cudaStreamDestroy(h->io_out);
+    for (int s = 0; s < 2; ++s) {
+        if (h->ev_in[s]) cudaEventDestroy(h->ev_in[s]);
+        if (h->ev_fwd[s]) cudaEventDestroy(h->ev_fwd[s]);
+        if (h->ev_out[s]) cudaEventDestroy(h->ev_out[s]);
+    }
 }
 
 }  // namespace
@@ -253,18 +275,26 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
         delete h;
         return LMOE_ERR_CUDA;
     }
-    if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
-        delete h;
-        return LMOE_ERR_CUDA;
-    }
-    if (cudaMalloc(&h->d_status, 256) != cudaSuccess) {
+    bool io_ok = cudaStreamCreateWithFlags(&h->io_in, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&h->io_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (int s = 0; s < 2 && io_ok; ++s)
+        io_ok = cudaEventCreateWithFlags(&h->ev_in[s], cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h->ev_fwd[s], cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h->ev_out[s], cudaEventDisableTiming) == cudaSuccess;
+    if (!io_ok || cudaMalloc(&h->d_status, 256) != cudaSuccess) {
+        release_streams(h);
+        cudaFree(h->w1p);
+        cudaFree(h->w2p);
+        cudaFree(h->w3p);
         delete h;
         return LMOE_ERR_CUDA;
     }
     if (cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
         cudaFree(h->d_status);
+        release_streams(h);
+        cudaFree(h->w1p);
+        cudaFree(h->w2p);
+        cudaFree(h->w3p);
         delete h;
         return LMOE_ERR_CUDA;
     }
@@ -279,9 +309,7 @@ int lmoe_destroy(lmoe_handle *h) {
     cudaFree(h->w1p);
     cudaFree(h->w2p);
     cudaFree(h->w3p);
-    if (h->side) cudaStreamDestroy(h->side);
-    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-    if (h->ev_join) cudaEventDestroy(h->ev_join);
+    release_streams(h);
     delete h;
     return (e == cudaSuccess && f == cudaSuccess) ? LMOE_OK : LMOE_ERR_CUDA;
 }
@@ -309,6 +337,7 @@ int lmoe_workspace_layout(const lmoe_handle *h, int64_t T, lmoe_ws_layout *out) 
     out->o = int64_t(l.o);
     out->r = int64_t(l.r);
     out->shared_act = int64_t(l.sact);
+    out->h_norm = (l.hn == SIZE_MAX) ? -1 : int64_t(l.hn);
     return LMOE_OK;
 }
 
@@ -346,7 +375,9 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     uint32_t *wprefix = reinterpret_cast<uint32_t *>(ws + l.wprefix);
     int4 *tiles = reinterpret_cast<int4 *>(ws + l.tiles);
     int4 *tiles2 = reinterpret_cast<int4 *>(ws + l.tiles2);
-    int32_t *nmt = reinterpret_cast<int32_t *>(ws + l.nmt);   // [0]: 128-row tiles, [1]: pair tiles
+    int4 *tiles3 = reinterpret_cast<int4 *>(ws + l.tiles3);
+    // [0]: 128-row tiles, [1]: pair tiles (heavy experts), [2]: light-expert tiles
+    int32_t *nmt = reinterpret_cast<int32_t *>(ws + l.nmt);
     int32_t *perm = reinterpret_cast<int32_t *>(ws + l.perm);
     int32_t *inv = reinterpret_cast<int32_t *>(ws + l.inv);
     int32_t *tokrow = reinterpret_cast<int32_t *>(ws + l.tokrow);
@@ -354,10 +385,13 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     uint16_t *obuf = reinterpret_cast<uint16_t *>(ws + l.o);
     uint16_t *rbuf = reinterpret_cast<uint16_t *>(ws + l.r);
     uint16_t *sact = reinterpret_cast<uint16_t *>(ws + l.sact);
+    // the latent the router and the experts read: h, or RMSNorm(h) in the
+    // norm-after-down variant
+    uint16_t *hlat = c.norm_after_down ? reinterpret_cast<uint16_t *>(ws + l.hn) : hbuf;
 
     // Activation-side TMA descriptors for this T and workspace.
     CUtensorMap m_x, m_h, m_act, m_r, m_sact;
-    if (!make_map(&m_x, x, T, d, d, kBM) || !make_map(&m_h, hbuf, T, L, L, kBM) ||
+    if (!make_map(&m_x, x, T, d, d, kBM) || !make_map(&m_h, hlat, T, L, L, kBM) ||
         !make_map(&m_act, act, n, I, I, kBM) ||
         !make_map(&m_r, rbuf, T, L, L, kBM) || !make_map(&m_sact, sact, T, S, S, kBM))
         return LMOE_ERR_CUDA;
@@ -366,18 +400,9 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     auto mark = [&](int stage) {
         if (h->stage_events) cudaEventRecord(h->stage_events[stage], stream);
     };
-    const int side_sms = side_sms_for(h, T);
-    const int main_sms = h->num_sms - side_sms;
     auto grid_for = [&](int64_t tiles_) {
-        return static_cast<int>(tiles_ < main_sms ? tiles_ : main_sms);
+        return static_cast<int>(tiles_ < h->num_sms ? tiles_ : h->num_sms);
     };
-    cudaStream_t shared_stream = stream;
-    if (side_sms > 0) {   // fork: the side stream starts after everything before this call
-        if (cudaEventRecord(h->ev_fork, stream) != cudaSuccess ||
-            cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
-            return LMOE_ERR_CUDA;
-        shared_stream = h->side;
-    }
     int st;
 
     if (cudaMemsetAsync(bitmap, 0, size_t(E) * words * 4, stream) != cudaSuccess) return LMOE_ERR_CUDA;
@@ -397,6 +422,9 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
                                      grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
+    if (c.norm_after_down &&   // ablation variant: hn = h / sqrt(mean(h^2) + eps), per token
+        launch_combine_rmsnorm(hbuf, T, 1, static_cast<int>(L), c.rms_eps, hlat, stream) != cudaSuccess)
+        return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_SHARED);
     {   // a8': shared experts, act_s = SiTU(x Ws1^T) * softcap(x Ws2^T)
         GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
@@ -408,13 +436,9 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = sact;
         a.ld_out = S;
         a.out_cols = static_cast<int32_t>(S);
-        const int64_t tiles_s = int64_t(m_tiles) * a.n_tiles;
-        const int grid_s = side_sms > 0 ? static_cast<int>(tiles_s < side_sms ? tiles_s : side_sms)
-                                        : grid_for(tiles_s);
-        st = gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a, grid_s,
-                                     shared_stream));
+        st = gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
-        if (side_sms > 0 && cudaEventRecord(h->ev_join, h->side) != cudaSuccess) return LMOE_ERR_CUDA;
     }
     mark(LMOE_STAGE_ROUTER);
     {   // a2: s = sigmoid(h W_router^T), fp32
@@ -440,16 +464,18 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     if (launch_expert_scan(bitmap, static_cast<int>(E), words, wprefix, counts, stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_OFFSETS);
-    if (launch_offsets_tiles(counts, static_cast<int>(E), offsets, tiles, nmt, tiles2, nmt + 1, stream) !=
-        cudaSuccess)
+    if (launch_offsets_tiles(counts, static_cast<int>(E), offsets, tiles, nmt, tiles2, nmt + 1, tiles3, nmt + 2,
+                             stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_SCATTER);
     if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
                        stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_EXPERT_W12);
-    {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the rows of each expert's tokens
-        // (pair tiles: two 128-row sub-tiles of one expert share each weight stage)
+    {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the rows of each expert's tokens.
+        // Experts with more than 128 rows run pair tiles (two 128-row sub-tiles
+        // share each weight stage); the others run 128-row tiles whose smaller
+        // stages leave room for more weight stages in flight.
         GemmMaps m{m_h, m_h, h->m_w1, h->m_w2};
         GemmArgs a = base_args(h);
         a.n_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
@@ -457,17 +483,22 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.b_expert_rows = static_cast<int32_t>(I);
         a.b_packed = 1;
         a.b_row_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
-        a.tiles = tiles2;
-        a.n_mtiles = nmt + 1;
-        a.gather_src = hbuf;
+        a.gather_src = hlat;
         a.gather_rows = tokrow;
         a.gather_ld = L;
         a.out = act;
         a.ld_out = I;
         a.out_cols = static_cast<int32_t>(I);
-        const int64_t max_tiles = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
+        a.tiles = tiles3;
+        a.n_mtiles = nmt + 2;
         st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
-                                     grid_for(max_tiles), stream));
+                                     grid_for(E * a.n_tiles), stream, /*pair=*/false));
+        if (st) return st;
+        a.tiles = tiles2;
+        a.n_mtiles = nmt + 1;
+        const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
+        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
+                                     grid_for(max_pairs), stream, /*pair=*/true));
         if (st) return st;
     }
     mark(LMOE_STAGE_EXPERT_W3);
@@ -497,8 +528,6 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
                                stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_UP);
-    // join: the up-projection reads the shared activations
-    if (side_sms > 0 && cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     {   // a8: y = r W_up^T + act_s Ws3^T  (one GEMM, K split over the two sources)
         GemmMaps m{m_r, m_sact, h->m_wup, h->m_ws3};
         GemmArgs a = base_args(h);
@@ -515,6 +544,67 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         if (st) return st;
     }
     mark(LMOE_NUM_STAGES);
+    return LMOE_OK;
+}
+
+int lmoe_host_io_size(const lmoe_handle *h, size_t *bytes) {
+    if (!h || !bytes) return LMOE_ERR_INVALID_ARG;
+    *bytes = 2 * io_slot(h->cfg).bytes;
+    return LMOE_OK;
+}
+
+int lmoe_forward_host(lmoe_handle *h, const uint16_t *x_host, int64_t T, const float *bias_host,
+                      uint16_t *y_host, float *scores_out, int32_t *topk_idx_out, float *gates_out,
+                      int32_t *expert_counts_out, void *io_dev, size_t io_bytes, void *workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+    if (!h || T < 0) return LMOE_ERR_INVALID_ARG;
+    const lmoe_config &c = h->cfg;
+    if (T > c.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return LMOE_OK;
+    if (!x_host || !bias_host || !y_host || !io_dev || !workspace) return LMOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(io_dev) & 255u) return LMOE_ERR_ALIGNMENT;
+    const IoSlot sl = io_slot(c);
+    if (io_bytes < 2 * sl.bytes) return LMOE_ERR_WORKSPACE;
+    if (workspace_bytes < compute_layout(c, T, true, true, true, true).total) return LMOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || (scores_out && !aligned16(scores_out)) ||
+        (topk_idx_out && !aligned16(topk_idx_out)) || (gates_out && !aligned16(gates_out)) ||
+        (expert_counts_out && !aligned16(expert_counts_out)))
+        return LMOE_ERR_ALIGNMENT;
+
+    const int s = static_cast<int>(h->io_calls & 1u);
+    uint8_t *base = static_cast<uint8_t *>(io_dev) + s * sl.bytes;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(base + sl.x);
+    float *bs = reinterpret_cast<float *>(base + sl.bias);
+    uint16_t *ys = reinterpret_cast<uint16_t *>(base + sl.y);
+    const size_t xbytes = size_t(T) * c.d * 2;
+    // 1. input copy, after the forward that last read this slot
+    if (cudaStreamWaitEvent(h->io_in, h->ev_fwd[s], 0) != cudaSuccess ||
+        cudaMemcpyAsync(xs, x_host, xbytes, cudaMemcpyHostToDevice, h->io_in) != cudaSuccess ||
+        cudaMemcpyAsync(bs, bias_host, size_t(c.n_experts) * 4, cudaMemcpyHostToDevice, h->io_in) !=
+            cudaSuccess ||
+        cudaEventRecord(h->ev_in[s], h->io_in) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    // 2. the forward, after its input landed and the slot's last output copy
+    if (cudaStreamWaitEvent(stream, h->ev_in[s], 0) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, h->ev_out[s], 0) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    const int st = lmoe_forward(h, xs, T, bs, ys, scores_out, topk_idx_out, gates_out, expert_counts_out,
+                                workspace, workspace_bytes, stream);
+    if (st) return st;
+    if (cudaEventRecord(h->ev_fwd[s], stream) != cudaSuccess) return LMOE_ERR_CUDA;
+    // 3. output copy
+    if (cudaStreamWaitEvent(h->io_out, h->ev_fwd[s], 0) != cudaSuccess ||
+        cudaMemcpyAsync(y_host, ys, xbytes, cudaMemcpyDeviceToHost, h->io_out) != cudaSuccess ||
+        cudaEventRecord(h->ev_out[s], h->io_out) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+    ++h->io_calls;
+    return LMOE_OK;
+}
+
+int lmoe_host_wait(lmoe_handle *h, cudaStream_t stream) {
+    if (!h) return LMOE_ERR_INVALID_ARG;
+    for (int s = 0; s < 2; ++s)
+        if (cudaStreamWaitEvent(stream, h->ev_out[s], 0) != cudaSuccess) return LMOE_ERR_CUDA;
     return LMOE_OK;
 }
 
@@ -571,6 +661,15 @@ int qb_quantile_bias(const uint32_t *hist, int32_t E, int32_t B, double level, f
     return launch_qb_quantile(hist, E, B, level, quantile_out, bias_out, stream) == cudaSuccess
                ? LMOE_OK
                : LMOE_ERR_CUDA;
+}
+
+int qb_sign_update(const int32_t *counts, int32_t E, float gamma, float *bias, cudaStream_t stream) {
+    if (!counts || !bias || E < 1 || E > 65536 || !(gamma == gamma)) return LMOE_ERR_INVALID_ARG;
+    if (!aligned16(counts) || !aligned16(bias)) return LMOE_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    int st = check_device(&dev, &sms);
+    if (st) return st;
+    return launch_sign_update(counts, E, gamma, bias, stream) == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -226,6 +226,34 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     return cudaGetLastError();
 }
 
+// Fixed-step bias update (the rule QB replaces): one CTA sums the loads, then
+// every expert's bias moves by +gamma (under-loaded), -gamma (over-loaded) or
+// not at all; the comparison counts[e] * E <=> total is exact in integers.
+__global__ void __launch_bounds__(1024) sign_update_kernel(const int32_t *__restrict__ counts, int E, float gamma,
+                                                           float *__restrict__ bias) {
+    __shared__ long long s_part[32];
+    long long part = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) part += counts[e];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = part;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < (int(blockDim.x) + 31) / 32; ++w) total += s_part[w];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const long long scaled = static_cast<long long>(counts[e]) * E;
+        if (scaled < total)
+            bias[e] = __fadd_rn(bias[e], gamma);
+        else if (scaled > total)
+            bias[e] = __fsub_rn(bias[e], gamma);
+    }
+}
+
+cudaError_t launch_sign_update(const int32_t *counts, int E, float gamma, float *bias, cudaStream_t st) {
+    sign_update_kernel<<<1, 1024, 0, st>>>(counts, E, gamma, bias);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level, float *q,
                                float *bias, cudaStream_t st) {
     const int wpb = 8;

@@ -103,29 +103,36 @@ __global__ void expert_scan_kernel(const uint32_t *__restrict__ bitmap, int E, i
 __global__ void __launch_bounds__(1024)
     offsets_tiles_kernel(const int32_t *__restrict__ counts, int E, int32_t *__restrict__ offsets,
                          int4 *__restrict__ tiles, int32_t *__restrict__ n_mtiles,
-                         int4 *__restrict__ tiles2, int32_t *__restrict__ n_mtiles2) {
+                         int4 *__restrict__ tiles2, int32_t *__restrict__ n_mtiles2,
+                         int4 *__restrict__ tiles3, int32_t *__restrict__ n_mtiles3) {
     __shared__ int32_t s_cnt[1024];
     __shared__ int32_t s_til[1024];
     __shared__ int32_t s_til2[1024];
+    __shared__ int32_t s_til3[1024];
     const int e = threadIdx.x;
+    const bool split = tiles3 != nullptr;
     const int32_t c = (e < E) ? counts[e] : 0;
     const int32_t nt = (c + kBM - 1) / kBM;
-    const int32_t nt2 = (c + 2 * kBM - 1) / (2 * kBM);
+    const int32_t nt3 = (split && c > 0 && c <= kBM) ? 1 : 0;   // light: one 128-row tile
+    const int32_t nt2 = nt3 ? 0 : (c + 2 * kBM - 1) / (2 * kBM);
     s_cnt[e] = c;
     s_til[e] = nt;
     s_til2[e] = nt2;
+    s_til3[e] = nt3;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {  // Hillis-Steele inclusive scans
-        int32_t a = 0, b = 0, b2 = 0;
+        int32_t a = 0, b = 0, b2 = 0, b3 = 0;
         if (e >= off) {
             a = s_cnt[e - off];
             b = s_til[e - off];
             b2 = s_til2[e - off];
+            b3 = s_til3[e - off];
         }
         __syncthreads();
         s_cnt[e] += a;
         s_til[e] += b;
         s_til2[e] += b2;
+        s_til3[e] += b3;
         __syncthreads();
     }
     if (e < E) {
@@ -137,11 +144,13 @@ __global__ void __launch_bounds__(1024)
         const int32_t pair0 = s_til2[e] - nt2;
         for (int32_t m = 0; m < nt2; ++m)
             tiles2[pair0 + m] = make_int4(e, row0 + m * 2 * kBM, min(2 * kBM, c - m * 2 * kBM), 0);
+        if (nt3) tiles3[s_til3[e] - 1] = make_int4(e, row0, c, 0);
     }
     if (e == E - 1) {
         offsets[E] = s_cnt[e];
         *n_mtiles = s_til[e];
         *n_mtiles2 = s_til2[e];
+        if (split) *n_mtiles3 = s_til3[e];
     }
 }
 
@@ -193,8 +202,10 @@ cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words, uint32_
 }
 
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
-                                 int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2, cudaStream_t st) {
-    offsets_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, tiles, n_mtiles, tiles2, n_mtiles2);
+                                 int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2, int4 *tiles3,
+                                 int32_t *n_mtiles3, cudaStream_t st) {
+    offsets_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, tiles, n_mtiles, tiles2, n_mtiles2,
+                                             tiles3, n_mtiles3);
     return cudaGetLastError();
 }
 

@@ -41,6 +41,7 @@ class LayerShape:
     beta1: float = 4.0
     beta2: float = 25.0
     rms_eps: float = 1e-6
+    norm_after_down: bool = False   # ablation variant: RMSNorm on the latent as well
 
     def layer_dict(self) -> dict:
         d = asdict(self)
@@ -235,4 +236,18 @@ def qb_scores(T: int, E: int = QB_SWEEP_E, seed: int = QB_SEED, device="cpu") ->
         n = min(rows, T - i)
         z = torch.randn((n, E), generator=gen, device=device, dtype=torch.float32)
         out[i:i + n] = torch.sigmoid(z + mu)
+    return out
+
+
+def qb_score_stream(T: int, E: int, n_batches: int, seed: int = QB_SEED, device="cpu") -> torch.Tensor:
+    """A stationary stream of score batches for closed-loop balancing runs:
+    the per-expert logit means mu_e ~ N(0, 0.5^2) are drawn once, every batch
+    draws fresh N(0, 1) noise; fp32 sigmoid scores, [n_batches, T, E]."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    mu = torch.randn(E, generator=gen, device=device, dtype=torch.float32) * 0.5
+    out = torch.empty((n_batches, T, E), dtype=torch.float32, device=device)
+    for i in range(n_batches):
+        z = torch.randn((T, E), generator=gen, device=device, dtype=torch.float32)
+        out[i] = torch.sigmoid(z + mu)
     return out

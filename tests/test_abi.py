@@ -45,3 +45,19 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "lmoe_oracle" not in text, f
+
+
+def test_host_entry_points_reject_bad_arguments_without_gpu():
+    """Argument errors return before any CUDA call, so they run here."""
+    from sparse_moe_layer_bias_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    P = ctypes.c_void_p
+    lib.lmoe_host_io_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.lmoe_host_wait.argtypes = [P, P]
+    lib.lmoe_forward_host.argtypes = [P, P, ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_size_t, P,
+                                      ctypes.c_size_t, P]
+    n = ctypes.c_size_t()
+    assert lib.lmoe_host_io_size(None, ctypes.byref(n)) == 1
+    assert lib.lmoe_host_wait(None, None) == 1
+    assert lib.lmoe_forward_host(None, None, 8, None, None, None, None, None, None, None, 0, None, 0,
+                                 None) == 1

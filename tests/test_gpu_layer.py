@@ -2,6 +2,8 @@
 CPU oracle.  Each stage is checked on the GPU's own input to that stage (so a
 discontinuous step -- the top-k -- is compared bit for bit), and the layer
 output is checked end to end against the oracle's full forward."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -56,10 +58,23 @@ def staged_checks(shape, run):
     absum_h = np.abs(X) @ np.abs(Wd).T
     assert np.all(np.abs(dec(h_gpu) - exact_h) <= ulp_bf16(exact_h) + ACC_REL * absum_h)
 
-    # a2: scores on the GPU's h
+    # norm-after-down variant: the routed latent is RMSNorm(h), within one
+    # bf16 ulp of the exact normalisation of the GPU's own h
+    h_lat = h_gpu
+    if shape.norm_after_down:
+        assert lay["h_norm"] >= 0
+        h_lat = host_bits(ws_view(ws, lay, "h_norm", torch.bfloat16, (T, L)))
+        hd = dec(h_gpu)
+        exact = hd / np.sqrt(np.mean(hd ** 2, axis=1, keepdims=True) + shape.rms_eps)
+        assert np.all(np.abs(dec(h_lat) - exact) <= ulp_bf16(exact))
+        assert np.allclose(np.sqrt(np.mean(dec(h_lat) ** 2, axis=1)), 1.0, atol=2.0 ** -7)
+    else:
+        assert lay["h_norm"] == -1
+
+    # a2: scores on the GPU's routed latent
     s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, E)).cpu().numpy()
-    s_ref = oracle.router(cfg, h_gpu, wb["w_router"])
-    absum_s = np.abs(dec(h_gpu)) @ np.abs(dec(wb["w_router"])).T
+    s_ref = oracle.router(cfg, h_lat, wb["w_router"])
+    absum_s = np.abs(dec(h_lat)) @ np.abs(dec(wb["w_router"])).T
     assert np.all(np.abs(s_gpu - s_ref) <= score_tol(s_ref, absum_s))
 
     # a3: top-k on the GPU's scores -- bit-exact
@@ -77,12 +92,12 @@ def staged_checks(shape, run):
     assert np.array_equal(ws_view(ws, lay, "inv", torch.int32, (T * K,)).cpu().numpy(), inv)
 
     # a5/a6: expert activations and gate-weighted outputs on the GPU's h and routing
-    rt = oracle.routed(cfg, h_gpu, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"], want_act=True, want_o=True)
+    rt = oracle.routed(cfg, h_lat, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"], want_act=True, want_o=True)
     act_gpu = dec(host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))))
     act_ref = dec(rt["act"])[perm]                       # oracle rows are in assignment order
     # |d act/d p1| <= 1.1 * beta2 and |d act/d p2| <= beta1: the accumulation
     # error of p1, p2 carries over with those factors
-    Hd = np.abs(dec(h_gpu))
+    Hd = np.abs(dec(h_lat))
     tok = perm // K
     ex = idx_gpu.reshape(-1)[perm]
     acc_tol = np.zeros_like(act_ref)
@@ -181,3 +196,66 @@ def test_host_errors_enqueue_nothing(lm):
     assert e.value.status == 2
     y = lm.lmoe_forward(h, x[:0], b)                 # T = 0: nothing to do
     assert y.shape[0] == 0
+
+
+def test_host_io_pipeline_matches_device_forward(lm):
+    """lmoe_forward_host over several queued batches (ragged T, distinct
+    inputs, both staging slots reused) gives the device forward's bits."""
+    shape = synth.TINY
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
+    ws = lm.alloc_workspace(h, shape.T)
+    io = lm.alloc_host_io(h)
+    xs, bs, ys = [], [], []
+    for i in range(5):
+        x, b = synth.activations_host(shape, seed_offset=100 + i)
+        T = shape.T - 37 * i
+        xs.append(x[:T].contiguous().pin_memory())
+        bs.append(b.pin_memory())
+        ys.append(torch.empty_like(xs[-1]).pin_memory())
+    for i in range(5):
+        lm.lmoe_forward_host(h, xs[i], bs[i], ys[i], io, ws)
+    lm.lmoe_host_wait(h)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    for i in range(5):
+        ref = lm.lmoe_forward(h, xs[i].cuda(), bs[i].cuda(), workspace=ws)
+        assert torch.equal(ys[i].view(torch.int16), ref.cpu().view(torch.int16)), i
+    with pytest.raises(lm.LmoeError) as e:
+        lm.lmoe_forward_host(h, xs[0], bs[0], ys[0], io[:1024], ws)
+    assert e.value.status == 4                       # staging buffer too small
+
+
+TINY_NORM = dataclasses.replace(synth.TINY, name="tiny_norm_after_down", norm_after_down=True)
+SMALL_NORM = dataclasses.replace(synth.SMALL, name="small_norm_after_down", norm_after_down=True)
+
+
+@pytest.mark.parametrize("T", [None, 1, 129])
+def test_norm_after_down_variant_tiny(lm, T):
+    """Ablation variant (RMSNorm after the down-projection as well): every
+    stage on the GPU's own inputs, and the output end to end."""
+    run = run_host_shape(lm, TINY_NORM, T=T, seed_offset=0 if T is None else T)
+    staged_checks(TINY_NORM, run)
+    end_to_end(TINY_NORM, run)
+
+
+def test_norm_after_down_variant_small(lm):
+    run = run_host_shape(lm, SMALL_NORM)
+    staged_checks(SMALL_NORM, run)
+    rf, mx, kept, _ = end_to_end(SMALL_NORM, run)
+    assert kept >= 0.8 * SMALL_NORM.T
+
+
+def test_norm_after_down_routing_ignores_token_scale(lm):
+    """With the variant on and eps = 0, scaling every token by 4 (exact in
+    bf16) leaves the routing unchanged on the GPU as well."""
+    shape = dataclasses.replace(TINY_NORM, rms_eps=0.0)
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, b = (t.cuda() for t in synth.activations_host(shape))
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=x.shape[0])
+    idx1 = torch.empty((x.shape[0], shape.top_k), dtype=torch.int32, device="cuda")
+    idx4 = torch.empty_like(idx1)
+    lm.lmoe_forward(h, x, b, topk_idx_out=idx1)
+    lm.lmoe_forward(h, (x.float() * 4).to(torch.bfloat16), b, topk_idx_out=idx4)
+    torch.cuda.synchronize()
+    assert torch.equal(idx1, idx4)

@@ -93,3 +93,40 @@ def test_quantile_within_one_bin_of_exact_sort(lm):
     r = int(np.ceil(level * T))
     exact = torch.kthvalue(s, r, dim=0).values.numpy().astype(np.float64)
     assert np.all(np.abs(q.cpu().numpy() - exact) <= 1.0 / B + 1e-6)
+
+
+@pytest.mark.parametrize("E", [1, 5, 896, 1500])
+def test_sign_update_bit_exact(lm, E):
+    rng = np.random.default_rng(E)
+    counts = rng.integers(0, 300, E).astype(np.int32)
+    counts[: E // 3] = int(np.round(counts.mean()))         # some experts exactly at (or near) the mean
+    bias = rng.normal(0, 0.1, E).astype(np.float32)
+    got = lm.qb_sign_update(torch.from_numpy(counts).cuda(), 1e-3, torch.from_numpy(bias).cuda())
+    assert np.array_equal(got.cpu().numpy(), oracle.sign_update(counts, 1e-3, bias))
+
+
+@pytest.mark.parametrize("method", ["qb", "sign"])
+def test_closed_loop_matches_oracle(lm, method):
+    """The balancing loop over a stationary stream of skewed score batches:
+    route each batch with the current bias (lmoe_route_static), then update the
+    bias by QB (histogram -> quantile -> b = -q) or by the fixed-step rule.
+    Loads and biases equal the oracle's bit for bit at every step."""
+    T, E, k, n = 4096, 896, 16, 4
+    batches = synth.qb_score_stream(T, E, n, seed=3, device="cuda")
+    host = batches.cpu().numpy()
+    cfg = oracle.LayerConfig(d=64, latent=64, n_experts=E, top_k=k, inter=64, n_shared=1, shared_inter=64)
+    b_gpu = torch.zeros(E, dtype=torch.float32, device="cuda")
+    b_ref = np.zeros(E, np.float32)
+    level = 1 - k / E
+    for i in range(n):
+        counts_gpu = lm.lmoe_route_static(batches[i], b_gpu, k)["counts"]
+        idx_ref, _, _ = oracle.topk(cfg, host[i], b_ref)
+        counts_ref = oracle.expert_loads(idx_ref, E)
+        assert np.array_equal(counts_gpu.cpu().numpy(), counts_ref), i
+        if method == "qb":
+            _, b_gpu = lm.qb_quantile_bias(lm.qb_histogram(batches[i], 1000), level)
+            _, b_ref = oracle.qb_quantile_bias(oracle.qb_histogram(host[i], 1000), level)
+        else:
+            lm.qb_sign_update(counts_gpu, 1e-3, b_gpu)
+            b_ref = oracle.sign_update(counts_ref, 1e-3, b_ref)
+        assert np.array_equal(b_gpu.cpu().numpy(), b_ref), i

@@ -475,6 +475,84 @@ def test_qb_bias_sign_flattens_loads(orc):
     assert cv2 > cv0 and mx2 > mx0                     # the opposite sign sharpens them
 
 
+def test_sign_update_closed_forms(orc):
+    """The fixed-step rule: under-loaded experts step up, over-loaded ones down,
+    experts at the mean stay; mean 2 for loads (3, 1, 2, 2); a non-integer mean
+    (1.5) moves both; one fp32 addition per step."""
+    b = orc.sign_update(np.array([3, 1, 2, 2], np.int32), 0.5, np.zeros(4, np.float32))
+    assert b.tolist() == [-0.5, 0.5, 0.0, 0.0]
+    b = orc.sign_update(np.array([1, 2], np.int32), 0.25, np.array([1.0, -1.0], np.float32))
+    assert b.tolist() == [1.25, -1.25]
+    flat = np.full(7, 9, np.int32)
+    b0 = np.linspace(-1, 1, 7).astype(np.float32)
+    assert np.array_equal(orc.sign_update(flat, 0.1, b0), b0)
+    # fp32 add: 1 + 2^-30 rounds back to 1 in fp32 (it would not in fp64)
+    b = orc.sign_update(np.array([0, 5], np.int32), 2.0 ** -30, np.array([1.0, 1.0], np.float32))
+    assert b.dtype == np.float32 and b.tolist() == [1.0, 1.0]
+
+
+def test_closed_loop_qb_settles_in_one_read_sign_steps_slowly(orc):
+    """On a stationary stream of skewed score batches, QB sets the biases
+    from one batch's quantiles and the next batch is already near balance
+    (direct distribution solving); the fixed-step rule needs many steps at a
+    small step and moves the loads far less after one."""
+    T, E, k = 4000, 64, 4
+    cfg = tiny_cfg(orc, n_experts=E, top_k=k)
+    batches = synth.qb_score_stream(T, E, 6, seed=5).numpy()
+
+    def max_over_mean(s, bias):
+        idx, _, _ = orc.topk(cfg, s, bias)
+        load = orc.expert_loads(idx, E)
+        return load.max() / load.mean(), load
+
+    m0, _ = max_over_mean(batches[0], np.zeros(E, np.float32))
+    _, b_qb = orc.qb_quantile_bias(orc.qb_histogram(batches[0], 1000), 1 - k / E)
+    m_qb, _ = max_over_mean(batches[1], b_qb)
+    b = np.zeros(E, np.float32)
+    m_sign = []
+    for i in range(5):
+        _, load = max_over_mean(batches[i], b)
+        b = orc.sign_update(load, 1e-3, b)
+        m_sign.append(max_over_mean(batches[i + 1], b)[0])
+    assert m0 > 3.0
+    assert m_qb < 1.5
+    assert m_sign[0] > 0.8 * m0 and m_sign[-1] < m_sign[0]   # small steps: slow, monotone progress
+
+
+def test_rms_rows_closed_form(orc):
+    """Row RMSNorm on exact bf16 values: (3, 4, 0, 0) has mean square 25/4, so
+    it becomes (1.2, 1.6, 0, 0) (rounded once to bf16); a zero row stays zero."""
+    cfg = tiny_cfg(orc, rms_eps=0.0)
+    h = synth.bits(torch.tensor([[3.0, 4.0, 0.0, 0.0], [0.0, 0.0, 0.0, 0.0]]).to(torch.bfloat16))
+    out = dec(orc.rms_rows(cfg, h))
+    assert out[1].tolist() == [0.0, 0.0, 0.0, 0.0] and out[0, 2:].tolist() == [0.0, 0.0]
+    assert bf16_nearest_ok(orc.rms_rows(cfg, h)[0, :2], np.array([1.2, 1.6])).all()
+
+
+def test_norm_after_down_makes_routing_scale_free(orc):
+    """Ablation variant with the RMSNorm also after the down-projection: the
+    latent has unit RMS and routing depends on the token's direction only --
+    with eps = 0, x and 4x (exact in bf16) give the same normalised latent,
+    scores, chosen experts and aggregate.  Without that norm the same scaling
+    changes the routing once a selection bias is present."""
+    rng = np.random.default_rng(31)
+    cfg = tiny_cfg(orc, n_experts=16, top_k=3, norm_after_down=True, rms_eps=0.0)
+    w = tiny_weights(cfg, rng)
+    x = rand_bf16(rng, (64, cfg.d))
+    x4 = synth.bits(torch.from_numpy(dec(x) * 4.0).to(torch.bfloat16))
+    bias = rng.uniform(-0.05, 0.05, cfg.n_experts).astype(np.float32)
+    a, b = orc.layer_forward(cfg, x, w, bias), orc.layer_forward(cfg, x4, w, bias)
+    for key in ("h", "s", "idx", "r"):
+        assert np.array_equal(a[key], b[key]), key
+    assert not np.array_equal(a["h_raw"], b["h_raw"])
+    hn = dec(a["h"])
+    assert np.allclose(np.sqrt(np.mean(hn ** 2, axis=1)), 1.0, atol=2.0 ** -7)
+    off = tiny_cfg(orc, n_experts=16, top_k=3, rms_eps=0.0)
+    a0, b0 = orc.layer_forward(off, x, w, bias), orc.layer_forward(off, x4, w, bias)
+    assert np.array_equal(a0["h"], a0["h_raw"])
+    assert not np.array_equal(a0["idx"], b0["idx"])
+
+
 def test_synth_k3_shape_matches_published_constants():
     consts = json.load(open(os.path.join(GOLDEN, "constants.json")))
     k3 = synth.K3_PREFILL

@@ -233,6 +233,14 @@ int lmoe_route_static(const float *scores, int64_t T, int32_t E, int32_t top_k, 
                       int32_t *topk_idx, float *gates, int32_t *counts, int32_t *offsets,
                       int32_t *perm, int32_t *inv, cudaStream_t stream);
 
+/* Self-test of the failure path (no fault, no hang): enqueues one CTA that
+ * waits, with the same bounded mbarrier wait every GEMM role uses, on a
+ * barrier nothing arrives on.  After limit_ns (1 us .. 1 s) the wait gives up
+ * and sets the handle's device status, so a following lmoe_device_status
+ * reports LMOE_ERR_TIMEOUT; the kernel returns normally and the context stays
+ * usable.  The pages describe no such call; it is an addition of this library. */
+int lmoe_selftest_timeout(lmoe_handle *handle, uint64_t limit_ns, cudaStream_t stream);
+
 /* Device-side status of the handle's kernels (bounded waits that gave up).
  * Synchronises `stream`, copies the status word, and clears it when `clear`
  * is non-zero.  *device_status is LMOE_OK or LMOE_ERR_TIMEOUT. */

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     lmoe_host_io_size,
     lmoe_host_wait,
     lmoe_route_static,
+    lmoe_selftest_timeout,
     lmoe_set_stage_events,
     STAGES,
     lmoe_status_string,

@@ -22,7 +22,7 @@ STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED_SHAP
 EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size",
             "lmoe_workspace_layout", "lmoe_forward", "lmoe_host_io_size", "lmoe_forward_host",
             "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_route_static",
-            "qb_histogram", "qb_quantile_bias", "qb_sign_update")
+            "lmoe_selftest_timeout", "qb_histogram", "qb_quantile_bias", "qb_sign_update")
 
 STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12", "expert_w3",
           "combine", "up")
@@ -87,6 +87,8 @@ def load_library():
     lib.lmoe_forward_host.argtypes = [P, P, I64, P, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P]
     lib.lmoe_host_wait.restype = ctypes.c_int
     lib.lmoe_host_wait.argtypes = [P, P]
+    lib.lmoe_selftest_timeout.restype = ctypes.c_int
+    lib.lmoe_selftest_timeout.argtypes = [P, ctypes.c_uint64, P]
     lib.lmoe_device_status.restype = ctypes.c_int
     lib.lmoe_device_status.argtypes = [P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.lmoe_set_stage_events.restype = ctypes.c_int
@@ -349,3 +351,9 @@ def qb_sign_update(counts: torch.Tensor, gamma: float, bias: torch.Tensor, strea
     _check("qb_sign_update", load_library().qb_sign_update(_ptr(counts), counts.numel(), float(gamma),
                                                            _ptr(bias), _stream(stream)))
     return bias
+
+
+def lmoe_selftest_timeout(handle: Handle, limit_ns: int = 1_000_000, stream=None):
+    """Enqueue the bounded-wait self-test (see include/lmoe.h)."""
+    _check("lmoe_selftest_timeout", load_library().lmoe_selftest_timeout(handle.ptr, int(limit_ns),
+                                                                         _stream(stream)))

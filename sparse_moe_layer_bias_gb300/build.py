@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblmoe.so")
-SOURCES = ["gemm.cu", "pack.cu", "route.cu", "route_static.cu", "combine.cu", "qb.cu", "lmoe_api.cu"]
+SOURCES = ["gemm.cu", "pack.cu", "route.cu", "route_static.cu", "combine.cu", "qb.cu", "selftest.cu",
+           "lmoe_api.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -93,6 +93,9 @@ cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, f
 // ------------------------------------------------------------------ QB
 cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t ld, int B,
                                 uint32_t *hist, int accumulate, int num_sms, cudaStream_t stream);
+// One CTA waits (bounded) on an mbarrier nothing arrives on; sets the timeout
+// bit in *err after limit_ns and *gave_up = 1 (nullable).
+cudaError_t launch_bounded_wait_selftest(unsigned *err, uint64_t limit_ns, int *gave_up, cudaStream_t stream);
 cudaError_t launch_sign_update(const int32_t *counts, int E, float gamma, float *bias, cudaStream_t stream);
 cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level, float *q,
                                float *bias, cudaStream_t stream);

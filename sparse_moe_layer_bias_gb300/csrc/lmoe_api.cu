@@ -620,6 +620,12 @@ int lmoe_set_stage_events(lmoe_handle *h, cudaEvent_t *events, int n_events) {
     return LMOE_OK;
 }
 
+int lmoe_selftest_timeout(lmoe_handle *h, uint64_t limit_ns, cudaStream_t stream) {
+    if (!h || limit_ns < 1000ull || limit_ns > 1000000000ull) return LMOE_ERR_INVALID_ARG;
+    return launch_bounded_wait_selftest(h->d_status, limit_ns, nullptr, stream) == cudaSuccess ? LMOE_OK
+                                                                                            : LMOE_ERR_CUDA;
+}
+
 int lmoe_device_status(lmoe_handle *h, cudaStream_t stream, int clear, int *device_status) {
     if (!h || !device_status) return LMOE_ERR_INVALID_ARG;
     unsigned v = 0;

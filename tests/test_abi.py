@@ -56,6 +56,8 @@ def test_host_entry_points_reject_bad_arguments_without_gpu():
     lib.lmoe_host_wait.argtypes = [P, P]
     lib.lmoe_forward_host.argtypes = [P, P, ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_size_t, P,
                                       ctypes.c_size_t, P]
+    lib.lmoe_selftest_timeout.argtypes = [P, ctypes.c_uint64, P]
+    assert lib.lmoe_selftest_timeout(None, 1000000, None) == 1
     n = ctypes.c_size_t()
     assert lib.lmoe_host_io_size(None, ctypes.byref(n)) == 1
     assert lib.lmoe_host_wait(None, None) == 1

@@ -259,3 +259,24 @@ def test_norm_after_down_routing_ignores_token_scale(lm):
     lm.lmoe_forward(h, (x.float() * 4).to(torch.bfloat16), b, topk_idx_out=idx4)
     torch.cuda.synchronize()
     assert torch.equal(idx1, idx4)
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives(lm):
+    """The failure path without a fault: a bounded mbarrier wait that nothing
+    satisfies gives up after its limit and sets the handle's status; the
+    status reads LMOE_ERR_TIMEOUT once, clears, and the next forward gives the
+    same bits as before."""
+    shape = synth.TINY
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, b = (t.cuda() for t in synth.activations_host(shape))
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=x.shape[0])
+    y0 = lm.lmoe_forward(h, x, b).clone()
+    assert lm.lmoe_device_status(h) == 0
+    lm.lmoe_selftest_timeout(h, 2_000_000)
+    assert lm.lmoe_device_status(h, clear=True) == 6     # LMOE_ERR_TIMEOUT
+    assert lm.lmoe_device_status(h) == 0
+    y1 = lm.lmoe_forward(h, x, b)
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    with pytest.raises(lm.LmoeError):
+        lm.lmoe_selftest_timeout(h, 10)                   # limit below 1 us: rejected on the host

@@ -404,11 +404,11 @@ def main():
     roof["kernel"] = dom
     roof["per_launch"] = {"flop": dfl, "bytes": dby}
     # DRAM bytes per launch: ncu on the reduced K3-width case (--profile-case,
-    # where the full workload is too large to capture) measured read+write =
-    # 1.05 x the algorithmic bytes of the expert W1|W2 GEMM; the traffic of that
-    # kernel grows with the weights of the touched experts, so the full
-    # launch's traffic is that ratio times its algorithmic bytes.
-    roof["traffic"] = round(1.05 * dby) if dom == "expert_w12" else None
+    # where the full workload is too large to capture) measured read+write of
+    # the expert W1|W2 stage's two launches (light + heavy experts) = 1.02 x
+    # its algorithmic bytes; the traffic grows with the weights of the touched
+    # experts, so the full stage's traffic is that ratio times its bytes.
+    roof["traffic"] = round(1.02 * dby) if dom == "expert_w12" else None
     roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum on --profile-case, "
                               "scaled by algorithmic bytes") if dom == "expert_w12" else None
     roof["peak_source"] = peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " hbm copy")

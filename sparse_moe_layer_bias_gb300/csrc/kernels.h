@@ -87,6 +87,8 @@ cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t 
                            cudaStream_t stream);
 
 // ------------------------------------------------------------------ combine
+// Row RMSNorm of bf16 rows (fp64 arithmetic, one rounding to bf16); L % 8 == 0.
+cudaError_t launch_rms_rows(const uint16_t *h, int64_t T, int L, double eps, uint16_t *out, cudaStream_t stream);
 cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,
                                    uint16_t *r, cudaStream_t stream);
 

@@ -423,7 +423,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         if (st) return st;
     }
     if (c.norm_after_down &&   // ablation variant: hn = h / sqrt(mean(h^2) + eps), per token
-        launch_combine_rmsnorm(hbuf, T, 1, static_cast<int>(L), c.rms_eps, hlat, stream) != cudaSuccess)
+        launch_rms_rows(hbuf, T, static_cast<int>(L), static_cast<double>(c.rms_eps), hlat, stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_SHARED);
     {   // a8': shared experts, act_s = SiTU(x Ws1^T) * softcap(x Ws2^T)

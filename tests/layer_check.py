@@ -55,7 +55,7 @@ def rel_fro(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
-def check_layer_output(y_gpu_bf16: torch.Tensor, y_ref: np.ndarray, margin: np.ndarray):
+def check_layer_output(y_gpu_bf16: torch.Tensor, y_ref: np.ndarray, margin: np.ndarray, also_keep=None):
     """The acceptance test on the layer output; returns (rel_fro, max_abs/rms, kept).
 
     The layer's output is bf16, so rounding it costs up to half a bf16 ulp of
@@ -64,6 +64,8 @@ def check_layer_output(y_gpu_bf16: torch.Tensor, y_ref: np.ndarray, margin: np.n
     error beyond the output's own rounding: max(0, |dy| - ulp(y_ref)/2)."""
     yg = y_gpu_bf16.float().cpu().numpy().astype(np.float64)
     keep = margin > MARGIN
+    if also_keep is not None:
+        keep &= also_keep
     assert keep.sum() > 0
     d = np.abs(yg - y_ref)[keep]
     ref = y_ref[keep]

@@ -58,15 +58,14 @@ def staged_checks(shape, run):
     absum_h = np.abs(X) @ np.abs(Wd).T
     assert np.all(np.abs(dec(h_gpu) - exact_h) <= ulp_bf16(exact_h) + ACC_REL * absum_h)
 
-    # norm-after-down variant: the routed latent is RMSNorm(h), within one
-    # bf16 ulp of the exact normalisation of the GPU's own h
+    # norm-after-down variant: the routed latent is RMSNorm(h); both sides
+    # round the fp64 quotient once to bf16, so it equals the oracle's norm of
+    # the GPU's own h bit for bit
     h_lat = h_gpu
     if shape.norm_after_down:
         assert lay["h_norm"] >= 0
         h_lat = host_bits(ws_view(ws, lay, "h_norm", torch.bfloat16, (T, L)))
-        hd = dec(h_gpu)
-        exact = hd / np.sqrt(np.mean(hd ** 2, axis=1, keepdims=True) + shape.rms_eps)
-        assert np.all(np.abs(dec(h_lat) - exact) <= ulp_bf16(exact))
+        assert np.array_equal(h_lat, oracle.rms_rows(cfg, h_gpu))
         assert np.allclose(np.sqrt(np.mean(dec(h_lat) ** 2, axis=1)), 1.0, atol=2.0 ** -7)
     else:
         assert lay["h_norm"] == -1
@@ -134,8 +133,23 @@ def staged_checks(shape, run):
 def end_to_end(shape, run):
     cfg = oracle_cfg(shape)
     wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
-    ref = oracle.layer_forward(cfg, synth.bits(run["x_host"]), wb, run["b_host"].numpy())
-    rf, mx, kept = check_layer_output(run["y"], ref["y"], ref["margin"])
+    bias = run["b_host"].numpy()
+    ref = oracle.layer_forward(cfg, synth.bits(run["x_host"]), wb, bias)
+    also = None
+    if shape.norm_after_down:
+        # In this variant every element of the routed latent depends on the
+        # whole row of h through its RMS, so a last-bit difference between the
+        # GPU's h and the oracle's (both correct roundings of the same
+        # product, fp32 vs fp64 accumulation) can move a score by ~1e-4 and
+        # swap an expert at a margin above the 1e-4 bar.  Such tokens are
+        # left out: those whose oracle routing, recomputed from the GPU's own
+        # h, differs from the oracle's routing from its own h.
+        T, L = run["x_host"].shape[0], shape.latent
+        h_gpu = host_bits(ws_view(run["ws"], run["layout"], "h", torch.bfloat16, (T, L)))
+        s_g = oracle.router(cfg, oracle.rms_rows(cfg, h_gpu), wb["w_router"])
+        idx_g, _, _ = oracle.topk(cfg, s_g, bias)
+        also = np.all(np.sort(idx_g, 1) == np.sort(ref["idx"], 1), axis=1)
+    rf, mx, kept = check_layer_output(run["y"], ref["y"], ref["margin"], also_keep=also)
     return rf, mx, kept, ref
 
 

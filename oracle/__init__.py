@@ -57,6 +57,7 @@ class LayerConfig:
     beta2: float = 25.0
     rms_eps: float = 1e-6
     norm_after_down: bool = False   # ablation variant: RMSNorm on h as well
+    expert_fp8: bool = False        # FP8 variant: e4m3 routed experts
 
     def c(self) -> OrcConfig:
         return OrcConfig(self.d, self.latent, self.n_experts, self.top_k, self.inter,
@@ -90,6 +91,11 @@ def _load():
             "orc_qb_histogram": (None, [_P, _I64, _I32, _I64, _I32, _P, ctypes.c_int]),
             "orc_qb_quantile_bias": (None, [_P, _I32, _I32, ctypes.c_double, _P, _P]),
             "orc_sign_update": (None, [_P, _I32, ctypes.c_float, _P]),
+            "orc_e4m3_to_f64": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_f64_to_e4m3": (ctypes.c_uint8, [ctypes.c_double]),
+            "orc_fp8_exp_for": (_I32, [ctypes.c_double]),
+            "orc_fp8_quantize_rows": (None, [_P, _I64, _I64, _P, _P]),
+            "orc_routed_fp8": (None, [cfg, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
             "orc_num_threads": (ctypes.c_int, []),
         }
         for name, (res, args) in sig.items():
@@ -255,6 +261,78 @@ def routed(cfg: LayerConfig, h, idx, gate, w1, w2, w3, want_act=False, want_o=Fa
     return out
 
 
+# ---------------------------------------------------------------- FP8 variant
+def e4m3_to_f64(codes):
+    codes = np.asarray(codes, np.uint8)
+    lib = _load()
+    return np.array([lib.orc_e4m3_to_f64(int(c)) for c in codes.reshape(-1)]).reshape(codes.shape)
+
+
+def f64_to_e4m3(x):
+    x = np.asarray(x, np.float64)
+    lib = _load()
+    return np.array([lib.orc_f64_to_e4m3(float(v)) for v in x.reshape(-1)], np.uint8).reshape(x.shape)
+
+
+def fp8_exp_for(amax: float) -> int:
+    return int(_load().orc_fp8_exp_for(float(amax)))
+
+
+def fp8_quantize_rows(src):
+    """bf16 bits [..., R, K] -> (e4m3 codes uint8 [..., R, K], exponents int8 [..., R])."""
+    src = np.ascontiguousarray(src, np.uint16)
+    K = src.shape[-1]
+    R = src.size // K
+    codes = np.empty(src.shape, np.uint8)
+    exps = np.empty(src.shape[:-1], np.int8)
+    _load().orc_fp8_quantize_rows(_ptr(src), R, K, _ptr(codes), _ptr(exps))
+    return codes, exps
+
+
+def _fp8_ptrs(mats, n_experts, shape):
+    """Per-expert code and exponent pointers from an [E, R, K] bf16 array or a
+    dict {expert: [R, K]} (quantised here, row by row)."""
+    codes_arr, exps_arr = (_P * n_experts)(), (_P * n_experts)()
+    keep = []
+    items = mats.items() if isinstance(mats, dict) else enumerate(_need(mats, np.uint16, (n_experts,) + shape))
+    for e, m in items:
+        q, x = fp8_quantize_rows(_need(m, np.uint16, shape))
+        keep += [q, x]
+        codes_arr[int(e)] = q.ctypes.data
+        exps_arr[int(e)] = x.ctypes.data
+    return codes_arr, exps_arr, keep
+
+
+def routed_fp8(cfg: LayerConfig, h, idx, gate, w1, w2, w3, want_act=False, want_o=False):
+    """FP8 variant of ``routed``: the experts' weights (given as bf16, quantised
+    here per row) and operands in e4m3.  ``act`` is the e4m3 code array."""
+    T = h.shape[0]
+    h = _need(h, np.uint16, (T, cfg.latent))
+    idx = _need(idx, np.int32, (T, cfg.top_k))
+    gate = _need(gate, np.float32, (T, cfg.top_k))
+    q1, e1, k1 = _fp8_ptrs(w1, cfg.n_experts, (cfg.inter, cfg.latent))
+    q2, e2, k2 = _fp8_ptrs(w2, cfg.n_experts, (cfg.inter, cfg.latent))
+    q3, e3, k3 = _fp8_ptrs(w3, cfg.n_experts, (cfg.latent, cfg.inter))
+    for e in np.unique(idx):
+        if not (q1[e] and q2[e] and q3[e]):
+            raise ValueError(f"weights of expert {e} were not supplied")
+    z = np.empty((T, cfg.latent), np.float64)
+    r = np.empty((T, cfg.latent), np.uint16)
+    r64 = np.empty((T, cfg.latent), np.float64)
+    act = np.empty((T * cfg.top_k, cfg.inter), np.uint8) if want_act else None
+    o = np.empty((T * cfg.top_k, cfg.latent), np.float64) if want_o else None
+    c = cfg.c()
+    _load().orc_routed_fp8(ctypes.byref(c), T, _ptr(h), _ptr(idx), _ptr(gate), q1, e1, q2, e2, q3, e3,
+                           _ptr(act), _ptr(o), _ptr(z), _ptr(r), _ptr(r64))
+    del k1, k2, k3
+    out = {"z": z, "r": r, "r64": r64}
+    if want_act:
+        out["act"] = act
+    if want_o:
+        out["o"] = o
+    return out
+
+
 def shared_act(cfg: LayerConfig, x, ws1, ws2):
     T = x.shape[0]
     S = cfg.n_shared * cfg.shared_inter
@@ -289,7 +367,8 @@ def layer_forward(cfg: LayerConfig, x, w, bias):
     s = router(cfg, h, w["w_router"])
     idx, gate, margin = topk(cfg, s, bias)
     counts, offsets, perm, inv = permute(cfg, idx)
-    rt = routed(cfg, h, idx, gate, w["w1"], w["w2"], w["w3"])
+    experts = routed_fp8 if cfg.expert_fp8 else routed
+    rt = experts(cfg, h, idx, gate, w["w1"], w["w2"], w["w3"])
     a_s = shared_act(cfg, x, w["ws1"], w["ws2"])
     y = up_shared(cfg, rt["r"], a_s, w["w_up"], w["ws3"])
     return {"h_raw": h_raw, "h": h, "s": s, "idx": idx, "gate": gate, "margin": margin, "counts": counts,

@@ -355,6 +355,158 @@ void orc_routed(const orc_config *c, int64_t T, const uint16_t *h, const int32_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 variant of the routed experts (e4m3 weights and activations)          */
+/* ------------------------------------------------------------------------ */
+
+/* [NW] "Keeping the numbers in range": SiTU-GLU bounds the expert activation
+ * (|act| < beta1*beta2 = 100), which is what makes low-precision experts
+ * practical.  The pages give no FP8 recipe; the reading implemented here:
+ *   - e4m3 (OCP FP8: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ *     bits; no infinities; largest finite 448 = 1.75 * 2^8; smallest normal
+ *     2^-6; subnormals k * 2^-9), round to nearest even, saturating at +-448;
+ *   - every weight row (one output channel of W1, W2 or W3 of one expert) and
+ *     every token's latent row gets a power-of-two scale 2^e, e the smallest
+ *     integer with max|row| <= 448 * 2^e (0 for an all-zero row); a code is
+ *     e4m3(v * 2^-e) -- the scaling is exact, so only the e4m3 rounding acts;
+ *   - the expert activation uses the fixed scale 2^-2: act8 = e4m3(4 * act),
+ *     which never saturates because |4 * act| < 400 <= 448;
+ *   - dot products of the decoded values in fp64, then the two power-of-two
+ *     scales. */
+
+double orc_e4m3_to_f64(uint8_t c)
+{
+    const int sign = c >> 7, ex = (c >> 3) & 15, m = c & 7;
+    if (ex == 15 && m == 7)
+        return NAN;
+    double v = (ex == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, ex - 7);
+    return sign ? -v : v;
+}
+
+uint8_t orc_f64_to_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);          /* saturate (also +-inf) */
+    if (a < ldexp(1.0, -6)) {                   /* subnormal grid k * 2^-9 */
+        double k = nearbyint(ldexp(a, 9));      /* ties to even */
+        return (uint8_t)(sign | (uint8_t)k);    /* k = 8 is the smallest normal */
+    }
+    int e;
+    (void)frexp(a, &e);                         /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                     /* a = (1 + m) * 2^e */
+    double q = nearbyint(ldexp(a, 3 - e));      /* 8..16, ties to even */
+    if (q == 16.0) {
+        q = 8.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && q > 14.0))          /* past 448 after rounding */
+        return (uint8_t)(sign | 0x7E);
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)(q - 8.0));
+}
+
+/* Smallest integer e with amax <= 448 * 2^e (amax >= 0); 0 for amax = 0.
+ * With amax = f * 2^x, f in [0.5, 1), and 448 = 0.875 * 2^9. */
+int32_t orc_fp8_exp_for(double amax)
+{
+    if (!(amax > 0.0))
+        return 0;
+    int x;
+    double f = frexp(amax, &x);
+    return (f <= 0.875) ? x - 9 : x - 8;
+}
+
+/* codes[r][k] = e4m3(src[r][k] * 2^-exps[r]) for the R rows of K bf16 values. */
+void orc_fp8_quantize_rows(const uint16_t *src, int64_t R, int64_t K, uint8_t *codes, int8_t *exps)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        double amax = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = fabs(orc_bf16_to_f64(src[r * K + k]));
+            if (v > amax) amax = v;
+        }
+        const int32_t e = orc_fp8_exp_for(amax);
+        exps[r] = (int8_t)e;
+        for (int64_t k = 0; k < K; ++k)
+            codes[r * K + k] = orc_f64_to_e4m3(ldexp(orc_bf16_to_f64(src[r * K + k]), -e));
+    }
+}
+
+static double dot_e4m3(const uint8_t *a, const uint8_t *b, int64_t n)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        s += orc_e4m3_to_f64(a[i]) * orc_e4m3_to_f64(b[i]);
+    return s;
+}
+
+/* The routed branch with e4m3 experts (same structure as orc_routed):
+ *   h8, he  = quantised latent row of the token
+ *   p1[f]   = (h8 . w1q[f]) * 2^(he + w1e[f]),  p2 likewise with W2
+ *   act8[f] = e4m3(4 * SiTU(p1[f]; beta1) * softcap(p2[f]; beta2))
+ *   o[l]    = (act8 . w3q[l]) * 2^(w3e[l] - 2)
+ *   z, r    as in orc_routed.
+ * Per expert e: w1q[e], w2q[e] [inter][latent] codes with w1e[e], w2e[e]
+ * [inter] exponents; w3q[e] [latent][inter] with w3e[e] [latent].  Outputs
+ * (nullable): act8_out [T*top_k][inter] codes in assignment order, o_out
+ * [T*top_k][latent] fp64 (gate-weighted), z_out, r_out (bf16), r64_out. */
+void orc_routed_fp8(const orc_config *c, int64_t T, const uint16_t *h, const int32_t *idx,
+                    const float *gate, const uint8_t *const *w1q, const int8_t *const *w1e,
+                    const uint8_t *const *w2q, const int8_t *const *w2e, const uint8_t *const *w3q,
+                    const int8_t *const *w3e, uint8_t *act8_out, double *o_out, double *z_out,
+                    uint16_t *r_out, double *r64_out)
+{
+    const int64_t L = c->latent, I = c->inter, K = c->top_k;
+#pragma omp parallel
+    {
+        uint8_t *h8 = (uint8_t *)malloc((size_t)L);
+        uint8_t *act8 = (uint8_t *)malloc((size_t)I);
+        double *z = (double *)malloc((size_t)L * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            int8_t he;
+            orc_fp8_quantize_rows(h + t * L, 1, L, h8, &he);
+            for (int64_t l = 0; l < L; ++l)
+                z[l] = 0.0;
+            for (int64_t j = 0; j < K; ++j) {
+                const int64_t a = t * K + j;
+                const int32_t e = idx[a];
+                const double g = (double)gate[a];
+                for (int64_t f = 0; f < I; ++f) {
+                    double p1 = ldexp(dot_e4m3(h8, w1q[e] + f * L, L), he + w1e[e][f]);
+                    double p2 = ldexp(dot_e4m3(h8, w2q[e] + f * L, L), he + w2e[e][f]);
+                    act8[f] = orc_f64_to_e4m3(4.0 * orc_situ(p1, c->beta1) * orc_softcap(p2, c->beta2));
+                }
+                if (act8_out)
+                    memcpy(act8_out + a * I, act8, (size_t)I);
+                for (int64_t l = 0; l < L; ++l) {
+                    const double o = ldexp(dot_e4m3(act8, w3q[e] + l * I, I), w3e[e][l] - 2);
+                    z[l] += g * o;
+                    if (o_out)
+                        o_out[a * L + l] = g * o;
+                }
+            }
+            double ss = 0.0;
+            for (int64_t l = 0; l < L; ++l)
+                ss += z[l] * z[l];
+            const double inv_rms = 1.0 / sqrt(ss / (double)L + c->rms_eps);
+            for (int64_t l = 0; l < L; ++l) {
+                const double r = z[l] * inv_rms;
+                if (z_out) z_out[t * L + l] = z[l];
+                if (r_out) r_out[t * L + l] = orc_f64_to_bf16(r);
+                if (r64_out) r64_out[t * L + l] = r;
+            }
+        }
+        free(h8);
+        free(act8);
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* a8: shared experts and the up-projection                                  */
 /* ------------------------------------------------------------------------ */
 

@@ -553,6 +553,102 @@ def test_norm_after_down_makes_routing_scale_free(orc):
     assert not np.array_equal(a0["idx"], b0["idx"])
 
 
+# --------------------------------------------------------------------- FP8 variant
+def test_e4m3_codec_hand_values_and_torch(orc):
+    """e4m3 (OCP FP8): 448 is the largest finite value, 2^-6 the smallest
+    normal, 2^-9 the subnormal step; ties go to the even code; beyond 448 the
+    encoder saturates.  Inside the range it agrees with torch's float8_e4m3fn
+    conversion of the same (fp32-exact) values, and decoding agrees too."""
+    hand = {448.0: 0x7E, 1.0: 0x38, 2.0 ** -6: 0x08, 2.0 ** -9: 0x01, 1.0625: 0x38, 1.1875: 0x3A,
+            -3.0: 0xC4, 0.0: 0x00, 2.0 ** -10: 0x00, 3 * 2.0 ** -11: 0x01, 500.0: 0x7E, -1e9: 0xFE}
+    for v, code in hand.items():
+        assert int(orc.f64_to_e4m3(v)) == code, v
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.standard_normal(3000) * 10 ** rng.uniform(-3, 2.6, 3000),
+                        np.arange(-464.0, 464.0, 0.125)]).astype(np.float32)
+    x = x[np.abs(x) < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.f64_to_e4m3(x.astype(np.float64)), ref)
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]                       # NaN codes
+    ref_dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(orc.e4m3_to_f64(codes), ref_dec.astype(np.float64))
+
+
+def test_fp8_scale_exponent_rule(orc):
+    """e is the smallest integer with max|row| <= 448 * 2^e."""
+    assert [orc.fp8_exp_for(a) for a in (448.0, 449.0, 224.0, 0.875, 0.8751, 0.0)] == [0, 1, -1, -9, -8, 0]
+    rng = np.random.default_rng(9)
+    for a in 10 ** rng.uniform(-8, 6, 500):
+        e = orc.fp8_exp_for(a)
+        assert a <= 448.0 * 2.0 ** e and a > 448.0 * 2.0 ** (e - 1)
+
+
+def test_fp8_quantize_rows_matches_torch_and_error_bound(orc):
+    rng = np.random.default_rng(10)
+    w = rand_bf16(rng, (40, 96), 0.05)
+    w[3] = 0                                                     # an all-zero row
+    codes, exps = orc.fp8_quantize_rows(w)
+    assert exps[3] == 0 and not codes[3].any()
+    scaled = dec(w) * np.exp2(-exps.astype(np.float64))[:, None]   # exact power-of-two scaling
+    ref = torch.from_numpy(scaled.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    back = orc.e4m3_to_f64(codes) * np.exp2(exps.astype(np.float64))[:, None]
+    big = np.abs(scaled) >= 2.0 ** -6                            # normal range: half a step, 2^-4 relative
+    assert np.all(np.abs(back - dec(w))[big] <= 2.0 ** -4 * np.abs(dec(w))[big])
+    assert np.all(np.abs(scaled).max(axis=1)[np.arange(40) != 3] > 224.0)   # the scale uses the top octave
+
+
+def test_routed_fp8_exact_on_power_of_two_data(orc):
+    """With every latent and weight value in {0, +-1/4, +-1/2, +-1, +-2}, every
+    quantisation is exact, so the FP8 path equals an independent numpy/torch
+    computation: exact products, the SiTU-GLU in fp64, act8 = e4m3(4 act)
+    (torch's conversion), o = act8 / 4 . W3, z, and the RMSNorm."""
+    rng = np.random.default_rng(11)
+    cfg = tiny_cfg(orc, n_experts=6, top_k=2, latent=32, inter=16)
+    vals = np.array([0.0, 0.25, -0.25, 0.5, -0.5, 1.0, -1.0, 2.0, -2.0])
+
+    def pick(shape):
+        return synth.bits(torch.from_numpy(rng.choice(vals, shape).astype(np.float32)).to(torch.bfloat16))
+
+    T, E, L, I = 10, cfg.n_experts, cfg.latent, cfg.inter
+    h = pick((T, L))
+    w1, w2, w3 = pick((E, I, L)), pick((E, I, L)), pick((E, L, I))
+    idx = np.stack([rng.choice(E, 2, replace=False) for _ in range(T)]).astype(np.int32)
+    gate = rng.uniform(0.1, 1.0, (T, 2)).astype(np.float32)
+    out = orc.routed_fp8(cfg, h, idx, gate, w1, w2, w3, want_act=True, want_o=True)
+    H, W1, W2, W3 = dec(h), dec(w1), dec(w2), dec(w3)
+    for t in range(T):
+        z = np.zeros(L)
+        for j in range(2):
+            e, a = idx[t, j], t * 2 + j
+            p1, p2 = W1[e] @ H[t], W2[e] @ H[t]
+            act = 4.0 * np.tanh(p1 / 4.0) * expit(p1) * 25.0 * np.tanh(p2 / 25.0)
+            code = torch.from_numpy((4.0 * act).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(out["act"][a], code)
+            o = gate[t, j] * (W3[e] @ (orc.e4m3_to_f64(code) / 4.0))
+            assert np.allclose(out["o"][a], o, rtol=1e-12, atol=1e-12)
+            z += o
+        assert np.allclose(out["z"][t], z, rtol=1e-12, atol=1e-12)
+        assert np.allclose(out["r64"][t], z / np.sqrt(np.mean(z ** 2) + cfg.rms_eps), rtol=1e-12)
+
+
+def test_layer_fp8_keeps_routing_and_stays_near_bf16(orc):
+    """The FP8 variant changes only the routed experts: same h, scores and
+    choices as the bf16 layer; the output moves by the e4m3 quantisation
+    noise (a few percent), not by factors of two."""
+    rng = np.random.default_rng(12)
+    cfg = tiny_cfg(orc, n_experts=8, top_k=2)
+    cfg8 = tiny_cfg(orc, n_experts=8, top_k=2, expert_fp8=True)
+    w = tiny_weights(cfg, rng)
+    x = rand_bf16(rng, (48, cfg.d))
+    bias = np.zeros(8, np.float32)
+    a, b = orc.layer_forward(cfg, x, w, bias), orc.layer_forward(cfg8, x, w, bias)
+    assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(a["s"], b["s"])
+    rel = np.linalg.norm(b["z"] - a["z"]) / np.linalg.norm(a["z"])
+    assert 1e-3 < rel < 0.1
+
+
 def test_synth_k3_shape_matches_published_constants():
     consts = json.load(open(os.path.join(GOLDEN, "constants.json")))
     k3 = synth.K3_PREFILL

@@ -55,8 +55,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def layer_work(shape, T, touched_experts):
-    """Algorithmic FLOPs and bytes per stage for T tokens (bf16 = 2 bytes)."""
+def layer_work(shape, T, touched_experts, fp8=False):
+    """Algorithmic FLOPs and bytes per stage for T tokens (bf16 = 2 bytes;
+    with fp8, the routed experts' weights, latent codes and activation codes
+    are 1 byte, plus one exponent byte per weight row and token)."""
     d, L, E, k, I = shape.d, shape.latent, shape.n_experts, shape.top_k, shape.inter
     S = shape.n_shared * shape.shared_inter
     n = T * k
@@ -70,6 +72,10 @@ def layer_work(shape, T, touched_experts):
     w["scatter"] = (0.0, 16.0 * n)
     w["expert_w12"] = (4.0 * n * L * I, 2.0 * (touched_experts * 2 * I * L + T * L + n * I))
     w["expert_w3"] = (2.0 * n * I * L, 2.0 * (touched_experts * L * I + n * I + n * L))
+    if fp8:
+        w["expert_w12"] = (4.0 * n * L * I, touched_experts * 2 * I * (L + 1) + 2.0 * T * L + T * (L + 1) +
+                           T * L + n * I)
+        w["expert_w3"] = (2.0 * n * I * L, touched_experts * L * (I + 1) + n * I + 2.0 * n * L)
     w["combine"] = (0.0, 2.0 * (n * L + T * L))
     w["up"] = (2.0 * T * (L + S) * d, 2.0 * (T * (L + S) + d * (L + S) + T * d))
     return w
@@ -231,6 +237,54 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- ncu case
+def fp8_experts_variant(lm, stream, steps, warmup, shape, w, x, bias, dshape, wd, xd, bd, peaks):
+    """The FP8 expert variant (e4m3 routed experts, kind::f8f6f4 MMA) on the
+    same K3 prefill batch and decode batch: forward-only step times, the two
+    expert stages' times, and the decode layer's HBM rate on its own bytes."""
+    out = {}
+    for name, shp, ww, xx, bb in (("prefill", shape, w, x, bias), ("decode", dshape, wd, xd, bd)):
+        cfg = dict(shp.layer_dict(), expert_fp8=True)
+        h8 = lm.lmoe_create(cfg, ww, max_tokens=shp.T)
+        ws8 = lm.alloc_workspace(h8, shp.T)
+        y8 = torch.empty_like(xx)
+        c8 = torch.empty(shp.n_experts, dtype=torch.int32, device="cuda")
+        for _ in range(warmup):
+            lm.lmoe_forward(h8, xx, bb, y=y8, workspace=ws8, expert_counts_out=c8, stream=stream)
+        torch.cuda.synchronize()
+        touched = int((c8 > 0).sum().item())
+        n = max(steps, 20)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)] for _ in range(n)]
+        for e_ in evs:
+            for e in e_:
+                e.record(stream)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(n):
+            lm.lmoe_set_stage_events(h8, evs[i])
+            lm.lmoe_forward(h8, xx, bb, y=y8, workspace=ws8, expert_counts_out=c8, stream=stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        lm.lmoe_set_stage_events(h8, None)
+        assert lm.lmoe_device_status(h8) == 0
+        ms = t0.elapsed_time(t1) / n
+        st = {nm: float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in evs])) for j, nm in enumerate(lm.STAGES)}
+        work = layer_work(shp, shp.T, touched, fp8=True)
+        byts = sum(v[1] for v in work.values())
+        r = {"T": shp.T, "ms": round(ms, 4), "tokens_per_s": shp.T / (ms * 1e-3), "touched_experts": touched,
+             "expert_w12_ms": round(st["expert_w12"], 4), "expert_w3_ms": round(st["expert_w3"], 4),
+             "expert_w12_gbs": round(work["expert_w12"][1] / (st["expert_w12"] * 1e-3) / 1e9, 1),
+             "expert_w3_gbs": round(work["expert_w3"][1] / (st["expert_w3"] * 1e-3) / 1e9, 1)}
+        if name == "decode":
+            r["bytes"] = byts
+            r["gbs"] = round(byts / (ms * 1e-3) / 1e9, 1)
+            r["frac_hbm"] = round(r["gbs"] / peaks["hbm_gbs"], 4)
+        out[name] = r
+        del h8, ws8
+        torch.cuda.empty_cache()
+    return out
+
+
 def qb_closed_loop(lm, stream, T=8192, E=896, k=16, n=12):
     """The balancing loop on the GPU over a stationary stream of skewed score
     batches (per-expert logit means mu_e ~ N(0, 0.5^2), fresh noise per batch):
@@ -521,6 +575,9 @@ def main():
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     assert lm.lmoe_device_status(hd) == 0
 
+    # --------------------------------------------------------------- FP8 expert variant
+    fp8 = fp8_experts_variant(lm, stream, args.steps, args.warmup, shape, w, x, bias, dshape, wd, xd, bd, peaks)
+
     # --------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -552,6 +609,7 @@ def main():
         "qb_hist_sweep": {"T": Tq, "E": E, "B": QB_B, "ms": round(qb_ms, 4), "gbs": round(qb_gbs, 1),
                           "frac_hbm": round(qb_gbs / peaks["hbm_gbs"], 4)},
         "qb_closed_loop": qb_loop,
+        "fp8_experts": fp8,
         "decode": {"T": dshape.T, "ms": round(dec_ms, 4), "tokens_per_s": dshape.T / (dec_ms * 1e-3),
                    "touched_experts": touched_d, "bytes": dec_bytes, "gbs": round(dec_gbs, 1),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},

@@ -74,6 +74,18 @@ typedef struct {
                            * router and the experts then see ([DD] section 2,
                            * [IN] "RMSNorm insertion": the variant the ablation
                            * dropped) */
+    int32_t expert_fp8;   /* 0: bf16 routed experts (K3's layer).  1: FP8
+                           * variant: lmoe_create quantises W1, W2, W3 to e4m3
+                           * with one power-of-two scale per weight row, each
+                           * forward quantises the routed latent per token the
+                           * same way, and the expert GEMMs run e4m3 x e4m3 on
+                           * the tensor cores (fp32 accumulation); the SiTU-GLU
+                           * activation is stored as e4m3(4 * act), exact scale
+                           * from its bound |act| < beta1*beta2 = 100 ([NW]
+                           * "Keeping the numbers in range").  Requires inter %
+                           * 128 == 0.  Codes round to nearest even and saturate
+                           * at 448; a row's scale is the smallest 2^e with
+                           * max|row| <= 448 * 2^e. */
 } lmoe_config;
 
 /* Weight pointers (device, bf16, row-major, K-major rows as "out x in").
@@ -124,11 +136,14 @@ typedef struct {
     int64_t offsets;  /* [n_experts+1] int32     exclusive scan of counts         */
     int64_t perm;     /* [T*top_k] int32         assignment at each permuted row  */
     int64_t inv;      /* [T*top_k] int32         permuted row of each assignment  */
-    int64_t act;      /* [T*top_k][inter] bf16   expert SiTU-GLU activations, permuted order */
+    int64_t act;      /* [T*top_k][inter] bf16   expert SiTU-GLU activations, permuted order
+                       * (expert_fp8: e4m3 codes of 4 * act, one byte each) */
     int64_t o;        /* [T*top_k][latent] bf16  gate-weighted expert outputs, assignment order */
     int64_t r;        /* [T][latent] bf16        RMS-normalised aggregate          */
     int64_t shared_act; /* [T][S] bf16           shared-expert activations        */
     int64_t h_norm;   /* [T][latent] bf16        RMSNorm(h) when norm_after_down, else -1 */
+    int64_t h_fp8;    /* [T][latent] e4m3 codes of the routed latent (expert_fp8), else -1 */
+    int64_t h_fp8_exp; /* [T] int8 scale exponents of those rows (expert_fp8), else -1 */
 } lmoe_ws_layout;
 
 int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *layout);

@@ -39,7 +39,8 @@ class LmoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("shared_inter", ctypes.c_int32), ("beta1", ctypes.c_float),
                 ("beta2", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("max_tokens", ctypes.c_int64), ("norm_after_down", ctypes.c_int32)]
+                ("max_tokens", ctypes.c_int64), ("norm_after_down", ctypes.c_int32),
+                ("expert_fp8", ctypes.c_int32)]
 
 
 WEIGHT_NAMES = ("w_down", "w_router", "w1", "w2", "w3", "ws1", "ws2", "ws3", "w_up")
@@ -51,7 +52,8 @@ class LmoeWeights(ctypes.Structure):
 
 class LmoeWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("h", "scores", "topk_idx", "gates", "counts", "offsets",
-                                              "perm", "inv", "act", "o", "r", "shared_act", "h_norm")]
+                                              "perm", "inv", "act", "o", "r", "shared_act", "h_norm",
+                                              "h_fp8", "h_fp8_exp")]
 
 
 def library_path() -> str:
@@ -155,13 +157,14 @@ class Handle:
 
 def lmoe_create(cfg: dict, weights: dict, max_tokens: int) -> Handle:
     """cfg: d, latent, n_experts, top_k, inter, n_shared, shared_inter and
-    optional beta1, beta2, rms_eps, norm_after_down.  weights: bf16 CUDA tensors named as in
+    optional beta1, beta2, rms_eps, norm_after_down, expert_fp8.  weights: bf16 CUDA tensors named as in
     lmoe_weights."""
     lib = load_library()
     c = LmoeConfig(int(cfg["d"]), int(cfg["latent"]), int(cfg["n_experts"]), int(cfg["top_k"]),
                    int(cfg["inter"]), int(cfg["n_shared"]), int(cfg["shared_inter"]),
                    float(cfg.get("beta1", 4.0)), float(cfg.get("beta2", 25.0)),
-                   float(cfg.get("rms_eps", 1e-6)), int(max_tokens), int(bool(cfg.get("norm_after_down", False))))
+                   float(cfg.get("rms_eps", 1e-6)), int(max_tokens), int(bool(cfg.get("norm_after_down", False))),
+                   int(bool(cfg.get("expert_fp8", False))))
     held = {}
     w = LmoeWeights()
     for n in WEIGHT_NAMES:

@@ -28,6 +28,7 @@
 //   warps 6..9  (gather mode only) copy the A rows named by a row list into
 //               the stage with cp.async.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -96,17 +97,31 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // Hardware tanh (max relative error about 2^-11, far below the bf16 output's
-// 2^-8).  sigma(x) = (1 + tanh(x/2)) / 2, so SiTU(x; b1) * softcap(y; b2)
-// costs three tanh evaluations.
+// 2^-8).  The sigmoid is 1 / (1 + e^-x) from the fast exponential and
+// division, which keeps its relative error small for very negative x, where
+// (1 + tanh(x/2)) / 2 would cancel (relative error growing like e^-x * 2^-11).
+// SiTU(x; b1) * softcap(y; b2) costs two tanh, one exp2 and one reciprocal.
 __device__ __forceinline__ float tanh_fast(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float situ_glu(float p1, float p2, float b1, float ib1, float b2, float ib2) {
-    const float sig = fmaf(0.5f, tanh_fast(0.5f * p1), 0.5f);
+    const float sig = __fdividef(1.0f, 1.0f + __expf(-p1));
     return (b1 * tanh_fast(p1 * ib1) * sig) * (b2 * tanh_fast(p2 * ib2));
 }
+
+// x * 2^k, exact (no rounding) while the result stays in the fp32 normal
+// range: two multiplications by powers of two built from exponent bits, each
+// factor within [2^-126, 2^127], for |k| up to 252 (k outside is clamped).
+__device__ __forceinline__ float scale_pow2(float x, int k) {
+    k = max(-252, min(252, k));
+    const int k1 = k >> 1, k2 = k - k1;
+    return x * __int_as_float((k1 + 127) << 23) * __int_as_float((k2 + 127) << 23);
+}
+
+// Exponent byte b (0..3) of a packed word of four int8 exponents.
+__device__ __forceinline__ int exp_byte(uint32_t w, int b) { return static_cast<int8_t>((w >> (8 * b)) & 0xffu); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -284,7 +299,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_m128(BN);
+            constexpr bool F8 = (EPI == EPI_SITU_GLU_F8 || EPI == EPI_SCATTER_F8);
+            constexpr uint32_t idesc = F8 ? idesc_e4m3_m128(BN) : idesc_bf16_m128(BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -311,9 +327,13 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         const uint64_t bdesc = sdesc_sw128(sb + k * 32);
 #pragma unroll
                         for (int sub = 0; sub < NSUB; ++sub)
-                            if (sub < nsub)
-                                tc_mma_bf16(d + sub * kAccStride, sdesc_sw128(sa + sub * (kBM * kBK * 2) + k * 32),
-                                            bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                            if (sub < nsub) {
+                                const uint64_t adesc = sdesc_sw128(sa + sub * (kBM * kBK * 2) + k * 32);
+                                if (F8)
+                                    tc_mma_e4m3(d + sub * kAccStride, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                                else
+                                    tc_mma_bf16(d + sub * kAccStride, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                            }
                     }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == S) {
@@ -342,6 +362,27 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED>(args, t, n_m);
+            // Per-row metadata of this thread's rows (destination row, gate,
+            // token exponent), fetched before waiting for the accumulator so
+            // their latency hides behind the MMAs.
+            int64_t pre_drow[NSUB];
+            float pre_scale[NSUB];
+            int pre_he[NSUB];
+#pragma unroll
+            for (int sub = 0; sub < NSUB; ++sub) {
+                const int trow = sub * kBM + row;
+                pre_drow[sub] = ti.row0 + trow;
+                pre_scale[sub] = 1.0f;
+                pre_he[sub] = 0;
+                if (trow < ti.nrows) {
+                    if (EPI == EPI_SCATTER_BF16 || EPI == EPI_SCATTER_F8) {
+                        pre_drow[sub] = args.scatter_rows[ti.row0 + trow];
+                        pre_scale[sub] = args.row_scale[pre_drow[sub]];
+                    } else if (EPI == EPI_SITU_GLU_F8) {
+                        pre_he[sub] = args.row_exp[args.gather_rows[ti.row0 + trow]];
+                    }
+                }
+            }
             // the whole warp must agree before the warp-collective tcgen05.ld
             if (!__all_sync(0xffffffffu,
                             mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err, lim)))
@@ -387,17 +428,54 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         store_f32_32(outf + orow * args.ld_out + col, v, static_cast<int>(args.out_cols - col));
                     }
                 }
+            } else if (EPI == EPI_SITU_GLU_F8) {
+                // e4m3 experts, W1|W2: p = acc * 2^(token exponent + weight-row
+                // exponent) (exact), SiTU-GLU, then the fixed activation scale:
+                // code = e4m3(4 * act), round to nearest even, saturating.  Each
+                // thread writes its row's 32 codes per group (one 32-byte sector).
+                const int ecol = ti.expert * args.col_exp_rows;
+                const int he = (NSUB > 1 && sub) ? pre_he[NSUB - 1] : pre_he[0];
+                uint8_t *orow = reinterpret_cast<uint8_t *>(args.out) + (ti.row0 + trow) * args.ld_out;
+                const float b1 = args.beta1, b2 = args.beta2;
+                const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
+#pragma unroll 1
+                for (int c = 0; c < H; c += 32) {
+                    float p1[32], p2[32];
+                    tmem_ld32(taddr + c, p1);
+                    tmem_ld32(taddr + H + c, p2);
+                    const int f0 = ti.nt * H + c;     // first feature of the group
+                    // the group's 32 W1 and W2 row exponents, four per 32-bit word
+                    const uint32_t *x1w = reinterpret_cast<const uint32_t *>(args.col_exp0 + ecol + f0);
+                    const uint32_t *x2w = reinterpret_cast<const uint32_t *>(args.col_exp1 + ecol + f0);
+                    uint32_t w[8];
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const uint32_t ew1 = __ldg(x1w + q4), ew2 = __ldg(x2w + q4);
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const int j = q4 * 4 + b;
+                            const float x1 = scale_pow2(p1[j], he + exp_byte(ew1, b));
+                            const float x2 = scale_pow2(p2[j], he + exp_byte(ew2, b));
+                            const float a4 = 4.0f * situ_glu(x1, x2, b1, ib1, b2, ib2);
+                            const uint32_t code = __nv_cvt_float_to_fp8(a4, __NV_SATFINITE, __NV_E4M3);
+                            word |= code << (8 * b);
+                        }
+                        w[q4] = word;
+                    }
+                    if (rv) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + f0);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                }
             } else {
                 // bf16 outputs: each group of 64 columns goes through the warp's
                 // staging buffer so the global stores are whole 128-byte lines
                 // (4 rows x 128 B per warp instruction) instead of 16 bytes of
                 // 32 different rows.
-                int64_t drow = ti.row0 + trow;
-                float scale = 1.0f;
-                if (EPI == EPI_SCATTER_BF16 && rv) {
-                    drow = args.scatter_rows[ti.row0 + trow];
-                    scale = args.row_scale[drow];
-                }
+                const int64_t drow = (NSUB > 1 && sub) ? pre_drow[NSUB - 1] : pre_drow[0];
+                const float scale = (NSUB > 1 && sub) ? pre_scale[NSUB - 1] : pre_scale[0];
                 constexpr int NOUT = (EPI == EPI_SITU_GLU) ? H : BN;   // output columns per tile
                 const int64_t col0 = int64_t(ti.nt) * NOUT;
                 const float b1 = args.beta1, b2 = args.beta2;
@@ -417,6 +495,18 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         } else if (EPI == EPI_SCATTER_BF16) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] *= scale;
+                        } else if (EPI == EPI_SCATTER_F8) {
+                            // e4m3 experts' W3: gate * 2^(weight-row exponent - 2); the
+                            // -2 undoes the activation's fixed scale of 4 (exact)
+                            const uint32_t *cw = reinterpret_cast<const uint32_t *>(
+                                args.col_exp0 + ti.expert * args.col_exp_rows + col0 + c + h2 * 32);
+#pragma unroll
+                            for (int q4 = 0; q4 < 8; ++q4) {
+                                const uint32_t ew = __ldg(cw + q4);
+#pragma unroll
+                                for (int b = 0; b < 4; ++b)
+                                    v[q4 * 4 + b] = scale_pow2(v[q4 * 4 + b] * scale, exp_byte(ew, b) - 2);
+                            }
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) packed[h2 * 16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
@@ -503,6 +593,18 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     // a6 routed experts W3 with the gate-weighted scatter
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
+    // FP8 variant: e4m3 experts (kind::f8f6f4)
+    if (am == A_GATHER && bm == B_GLU && epi == EPI_SITU_GLU_F8 && grouped) {
+        if (pair) {
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, true>(maps, args, grid, stream);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, true>(maps, args, grid, stream);
+        } else {
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, false>(maps, args, grid, stream);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, false>(maps, args, grid, stream);
+        }
+    }
+    LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_F8, true)
+    LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_F8, true)
     return cudaErrorInvalidValue;
 }
 

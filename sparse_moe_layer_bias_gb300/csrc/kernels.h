@@ -19,10 +19,15 @@ enum AMode { A_DENSE = 0, A_GATHER = 1, A_SPLIT = 2 };
 // B operand source.
 enum BMode { B_PLAIN = 0, B_GLU = 1, B_SPLIT = 2 };
 // Epilogue.
-enum Epi { EPI_BF16 = 0, EPI_SITU_GLU = 1, EPI_SIGMOID_F32 = 2, EPI_SCATTER_BF16 = 3 };
+// EPI_SITU_GLU_F8: e4m3 experts' W1|W2 -- rescale by the token's and the
+// weight rows' power-of-two scales, SiTU-GLU, write e4m3(4 * act) bytes.
+// EPI_SCATTER_F8: e4m3 experts' W3 -- rescale by 2^(row exponent - 2), gate,
+// scatter bf16 rows (as EPI_SCATTER_BF16).
+enum Epi { EPI_BF16 = 0, EPI_SITU_GLU = 1, EPI_SIGMOID_F32 = 2, EPI_SCATTER_BF16 = 3, EPI_SITU_GLU_F8 = 4,
+           EPI_SCATTER_F8 = 5 };
 
 constexpr int kBM = 128;  // rows per tile (one tcgen05 M=128 tile)
-constexpr int kBK = 64;   // K per stage: one 128-byte swizzled row of bf16
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzled row of bf16 (128 e4m3)
 
 struct GemmMaps {
     CUtensorMap a0, a1, b0, b1;
@@ -50,6 +55,11 @@ struct GemmArgs {
     const int32_t *scatter_rows;  // EPI_SCATTER_BF16: destination row per permuted row
     const float *row_scale;       // EPI_SCATTER_BF16: scale per destination row
     float beta1, beta2;
+    // e4m3 experts: power-of-two scale exponents
+    const int8_t *row_exp;        // EPI_SITU_GLU_F8: per source token row (indexed via gather_rows)
+    const int8_t *col_exp0;       // per weight row of expert e: [e * col_exp_rows + col] (W1 or W3)
+    const int8_t *col_exp1;       // EPI_SITU_GLU_F8: the W2 rows
+    int32_t col_exp_rows;
     unsigned *err;           // device status word
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
@@ -58,6 +68,8 @@ struct GemmArgs {
 // pair tiles (two 128-row sub-tiles sharing each weight stage); without, 128-row
 // tiles with a deeper stage ring.  Returns cudaErrorInvalidValue for a
 // combination that is not compiled.
+// The e4m3 epilogues select the kind::f8f6f4 MMA (A and B e4m3; a k-block is
+// then 128 elements); every other epilogue multiplies bf16.
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false);
 size_t gemm_smem_bytes(int bn);
@@ -87,6 +99,11 @@ cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t 
                            cudaStream_t stream);
 
 // ------------------------------------------------------------------ combine
+// e4m3 quantisation of R rows of K bf16 values: exps[r] = smallest e with
+// max|row| <= 448 * 2^e (0 for a zero row), codes = e4m3_rn_satfinite(v * 2^-e).
+// K % 8 == 0.
+cudaError_t launch_fp8_quantize_rows(const uint16_t *src, int64_t R, int K, uint8_t *codes, int8_t *exps,
+                                     cudaStream_t stream);
 // Row RMSNorm of bf16 rows (fp64 arithmetic, one rounding to bf16); L % 8 == 0.
 cudaError_t launch_rms_rows(const uint16_t *h, int64_t T, int L, double eps, uint16_t *out, cudaStream_t stream);
 cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,

@@ -24,8 +24,10 @@ struct lmoe_handle {
     // Weight-side TMA descriptors, built once.
     int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up, bn_router;
     CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
-    // routed experts' weights repacked tile-contiguously (handle-owned)
+    // routed experts' weights repacked tile-contiguously (handle-owned): bf16,
+    // or e4m3 codes (expert_fp8) with one int8 scale exponent per weight row
     uint16_t *w1p, *w2p, *w3p;
+    int8_t *w1e, *w2e, *w3e;
     cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
     // lmoe_forward_host: input / output copy streams and, per staging slot, the
     // events "input landed", "forward done" and "output copied".
@@ -75,7 +77,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, tiles2, nmt, perm, inv, tokrow,
-        tiles3, act, o, r, sact, hn, total;
+        tiles3, act, o, r, sact, hn, h8, h8e, total;
 };
 
 Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
@@ -112,6 +114,8 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.r = take(size_t(T * L * 2));
     l.sact = take(size_t(T * S * 2));
     l.hn = c.norm_after_down ? take(size_t(T * L * 2)) : none;
+    l.h8 = c.expert_fp8 ? take(size_t(T * L)) : none;
+    l.h8e = c.expert_fp8 ? take(size_t(T)) : none;
     l.total = off;
     return l;
 }
@@ -123,6 +127,8 @@ int validate_config(const lmoe_config *c) {
         return LMOE_ERR_INVALID_ARG;
     if (!(c->beta1 > 0.0f) || !(c->beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
     if (c->norm_after_down != 0 && c->norm_after_down != 1) return LMOE_ERR_INVALID_ARG;
+    if (c->expert_fp8 != 0 && c->expert_fp8 != 1) return LMOE_ERR_INVALID_ARG;
+    if (c->expert_fp8 && c->inter % 128) return LMOE_ERR_UNSUPPORTED_SHAPE;
     const int64_t S = int64_t(c->n_shared) * c->shared_inter;
     if (c->d % 64 || c->latent % 128 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
     if (c->latent > 8192 || c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024)
@@ -174,6 +180,40 @@ IoSlot io_slot(const lmoe_config &c) {
     s.y = xb + align256(size_t(c.n_experts) * 4);
     s.bytes = s.y + xb;
     return s;
+}
+
+void release_streams(lmoe_handle *h);
+
+// Free whatever a (possibly half-built) handle holds, then the handle.
+void free_handle(lmoe_handle *h) {
+    cudaFree(h->d_status);
+    cudaFree(h->w1p);
+    cudaFree(h->w2p);
+    cudaFree(h->w3p);
+    cudaFree(h->w1e);
+    cudaFree(h->w2e);
+    cudaFree(h->w3e);
+    release_streams(h);
+    delete h;
+}
+
+// e4m3 expert weights: quantise [E][R][K] bf16 rows (one scale exponent per
+// row) through a temporary code buffer, then pack the codes tile-contiguously
+// like the bf16 weights (a 128-byte box row holds 128 codes).
+bool quantize_pack(const uint16_t *src, uint64_t E, uint64_t R, uint64_t K, int TR, uint16_t **packed,
+                   int8_t **exps) {
+    uint8_t *codes = nullptr;
+    const size_t n = size_t(E) * R * K;
+    if (cudaMalloc(packed, n) != cudaSuccess || cudaMalloc(exps, size_t(E) * R) != cudaSuccess ||
+        cudaMalloc(&codes, n) != cudaSuccess)
+        return false;
+    const bool ok = launch_fp8_quantize_rows(src, int64_t(E * R), static_cast<int>(K), codes, *exps, 0) ==
+                        cudaSuccess &&
+                    launch_pack_tiles(reinterpret_cast<const uint16_t *>(codes), E, static_cast<int>(R),
+                                      static_cast<int>(K / 2), TR, *packed, 0) == cudaSuccess &&
+                    cudaDeviceSynchronize() == cudaSuccess;
+    cudaFree(codes);
+    return ok;
 }
 
 void release_streams(lmoe_handle *h) {
@@ -238,41 +278,41 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
     // router: 256-wide N tiles unless E fits one 128-wide tile
     h->bn_router = (E > 128) ? 256 : 128;
     // Repack W1, W2 (boxes of bn_exp1/2 rows) and W3 (boxes of bn_exp3 rows)
-    // so each box is one contiguous block of HBM.
+    // so each box is one contiguous block of HBM; in the FP8 variant the
+    // boxes hold e4m3 codes (128 per 128-byte row) instead of bf16.
     const int tr12 = h->bn_exp1 / 2, tr3 = h->bn_exp3;
-    const size_t bytes12 = size_t(E) * I * L * 2, bytes3 = size_t(E) * L * I * 2;
-    if (cudaMalloc(&h->w1p, bytes12) != cudaSuccess || cudaMalloc(&h->w2p, bytes12) != cudaSuccess ||
-        cudaMalloc(&h->w3p, bytes3) != cudaSuccess) {
-        cudaFree(h->w1p);
-        cudaFree(h->w2p);
-        cudaFree(h->w3p);
-        delete h;
-        return LMOE_ERR_CUDA;
+    bool ok = true;
+    uint64_t kb12 = L / 64, kb3 = I / 64;   // 128-byte K blocks per weight row
+    if (c.expert_fp8) {
+        kb12 = L / 128;
+        kb3 = I / 128;
+        ok = quantize_pack(w->w1, E, I, L, tr12, &h->w1p, &h->w1e) &&
+             quantize_pack(w->w2, E, I, L, tr12, &h->w2p, &h->w2e) &&
+             quantize_pack(w->w3, E, L, I, tr3, &h->w3p, &h->w3e);
+    } else {
+        const size_t bytes12 = size_t(E) * I * L * 2, bytes3 = size_t(E) * L * I * 2;
+        ok = cudaMalloc(&h->w1p, bytes12) == cudaSuccess && cudaMalloc(&h->w2p, bytes12) == cudaSuccess &&
+             cudaMalloc(&h->w3p, bytes3) == cudaSuccess &&
+             launch_pack_tiles(w->w1, E, static_cast<int>(I), static_cast<int>(L), tr12, h->w1p, 0) == cudaSuccess &&
+             launch_pack_tiles(w->w2, E, static_cast<int>(I), static_cast<int>(L), tr12, h->w2p, 0) == cudaSuccess &&
+             launch_pack_tiles(w->w3, E, static_cast<int>(L), static_cast<int>(I), tr3, h->w3p, 0) == cudaSuccess &&
+             cudaDeviceSynchronize() == cudaSuccess;
     }
-    if (launch_pack_tiles(w->w1, E, static_cast<int>(I), static_cast<int>(L), tr12, h->w1p, 0) != cudaSuccess ||
-        launch_pack_tiles(w->w2, E, static_cast<int>(I), static_cast<int>(L), tr12, h->w2p, 0) != cudaSuccess ||
-        launch_pack_tiles(w->w3, E, static_cast<int>(L), static_cast<int>(I), tr3, h->w3p, 0) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess) {
-        cudaFree(h->w1p);
-        cudaFree(h->w2p);
-        cudaFree(h->w3p);
-        delete h;
-        return LMOE_ERR_CUDA;
-    }
-    bool ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->bn_down) &&
-              make_map(&h->m_wrouter, w->w_router, E, L, L, h->bn_router) &&
-              make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
-              make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
-              make_map(&h->m_w1, h->w1p, E * I * (L / 64), 64, 64, tr12) &&
-              make_map(&h->m_w2, h->w2p, E * I * (L / 64), 64, 64, tr12) &&
-              make_map(&h->m_w3, h->w3p, E * L * (I / 64), 64, 64, tr3) &&
-              make_map(&h->m_wup, w->w_up, d, L, L, h->bn_up) &&
-              make_map(&h->m_ws3, w->ws3, d, S, S, h->bn_up);
     if (!ok) {
-        cudaFree(h->w1p);
-        cudaFree(h->w2p);
-        cudaFree(h->w3p);
-        delete h;
+        free_handle(h);
+        return LMOE_ERR_CUDA;
+    }
+    ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->bn_down) &&
+         make_map(&h->m_wrouter, w->w_router, E, L, L, h->bn_router) &&
+         make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
+         make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
+         make_map(&h->m_w1, h->w1p, E * I * kb12, 64, 64, tr12) &&
+         make_map(&h->m_w2, h->w2p, E * I * kb12, 64, 64, tr12) &&
+         make_map(&h->m_w3, h->w3p, E * L * kb3, 64, 64, tr3) &&
+         make_map(&h->m_wup, w->w_up, d, L, L, h->bn_up) &&
+         make_map(&h->m_ws3, w->ws3, d, S, S, h->bn_up);
+    if (!ok) {
+        free_handle(h);
         return LMOE_ERR_CUDA;
     }
     bool io_ok = cudaStreamCreateWithFlags(&h->io_in, cudaStreamNonBlocking) == cudaSuccess &&
@@ -281,21 +321,8 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
         io_ok = cudaEventCreateWithFlags(&h->ev_in[s], cudaEventDisableTiming) == cudaSuccess &&
                 cudaEventCreateWithFlags(&h->ev_fwd[s], cudaEventDisableTiming) == cudaSuccess &&
                 cudaEventCreateWithFlags(&h->ev_out[s], cudaEventDisableTiming) == cudaSuccess;
-    if (!io_ok || cudaMalloc(&h->d_status, 256) != cudaSuccess) {
-        release_streams(h);
-        cudaFree(h->w1p);
-        cudaFree(h->w2p);
-        cudaFree(h->w3p);
-        delete h;
-        return LMOE_ERR_CUDA;
-    }
-    if (cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
-        cudaFree(h->d_status);
-        release_streams(h);
-        cudaFree(h->w1p);
-        cudaFree(h->w2p);
-        cudaFree(h->w3p);
-        delete h;
+    if (!io_ok || cudaMalloc(&h->d_status, 256) != cudaSuccess || cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
+        free_handle(h);
         return LMOE_ERR_CUDA;
     }
     *out = h;
@@ -304,14 +331,9 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
 
 int lmoe_destroy(lmoe_handle *h) {
     if (!h) return LMOE_ERR_INVALID_ARG;
-    cudaError_t e = cudaDeviceSynchronize();
-    cudaError_t f = cudaFree(h->d_status);
-    cudaFree(h->w1p);
-    cudaFree(h->w2p);
-    cudaFree(h->w3p);
-    release_streams(h);
-    delete h;
-    return (e == cudaSuccess && f == cudaSuccess) ? LMOE_OK : LMOE_ERR_CUDA;
+    const cudaError_t e = cudaDeviceSynchronize();
+    free_handle(h);
+    return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
 int lmoe_workspace_size(const lmoe_handle *h, int64_t T, size_t *bytes) {
@@ -338,6 +360,8 @@ int lmoe_workspace_layout(const lmoe_handle *h, int64_t T, lmoe_ws_layout *out) 
     out->r = int64_t(l.r);
     out->shared_act = int64_t(l.sact);
     out->h_norm = (l.hn == SIZE_MAX) ? -1 : int64_t(l.hn);
+    out->h_fp8 = (l.h8 == SIZE_MAX) ? -1 : int64_t(l.h8);
+    out->h_fp8_exp = (l.h8e == SIZE_MAX) ? -1 : int64_t(l.h8e);
     return LMOE_OK;
 }
 
@@ -388,11 +412,14 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     // the latent the router and the experts read: h, or RMSNorm(h) in the
     // norm-after-down variant
     uint16_t *hlat = c.norm_after_down ? reinterpret_cast<uint16_t *>(ws + l.hn) : hbuf;
+    uint8_t *h8 = c.expert_fp8 ? ws + l.h8 : nullptr;              // e4m3 codes of hlat
+    int8_t *h8e = c.expert_fp8 ? reinterpret_cast<int8_t *>(ws + l.h8e) : nullptr;
 
     // Activation-side TMA descriptors for this T and workspace.
     CUtensorMap m_x, m_h, m_act, m_r, m_sact;
     if (!make_map(&m_x, x, T, d, d, kBM) || !make_map(&m_h, hlat, T, L, L, kBM) ||
-        !make_map(&m_act, act, n, I, I, kBM) ||
+        !(c.expert_fp8 ? make_map(&m_act, act, n, I / 2, I / 2, kBM)   // e4m3 codes as 2-byte pairs
+                       : make_map(&m_act, act, n, I, I, kBM)) ||
         !make_map(&m_r, rbuf, T, L, L, kBM) || !make_map(&m_sact, sact, T, S, S, kBM))
         return LMOE_ERR_CUDA;
 
@@ -476,37 +503,51 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         // Experts with more than 128 rows run pair tiles (two 128-row sub-tiles
         // share each weight stage); the others run 128-row tiles whose smaller
         // stages leave room for more weight stages in flight.
+        // FP8 variant: the latent rows are quantised to e4m3 first (one
+        // power-of-two scale per token) and the GEMM multiplies e4m3 codes;
+        // its epilogue writes the activation as e4m3(4 * act).
+        const bool f8 = c.expert_fp8 != 0;
+        if (f8 && launch_fp8_quantize_rows(hlat, T, static_cast<int>(L), h8, h8e, stream) != cudaSuccess)
+            return LMOE_ERR_CUDA;
         GemmMaps m{m_h, m_h, h->m_w1, h->m_w2};
         GemmArgs a = base_args(h);
         a.n_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
-        a.k_blocks = static_cast<int32_t>(L / kBK);
+        a.k_blocks = static_cast<int32_t>(f8 ? L / 128 : L / kBK);   // 128-byte K blocks
         a.b_expert_rows = static_cast<int32_t>(I);
         a.b_packed = 1;
         a.b_row_tiles = static_cast<int32_t>(I / (h->bn_exp1 / 2));
-        a.gather_src = hlat;
+        a.gather_src = f8 ? reinterpret_cast<const uint16_t *>(h8) : hlat;
         a.gather_rows = tokrow;
-        a.gather_ld = L;
+        a.gather_ld = f8 ? L / 2 : L;    // in 2-byte units
         a.out = act;
-        a.ld_out = I;
+        a.ld_out = I;                    // elements: bf16, or bytes of e4m3 codes
         a.out_cols = static_cast<int32_t>(I);
+        a.row_exp = h8e;
+        a.col_exp0 = h->w1e;
+        a.col_exp1 = h->w2e;
+        a.col_exp_rows = static_cast<int32_t>(I);
+        const Epi epi = f8 ? EPI_SITU_GLU_F8 : EPI_SITU_GLU;
         a.tiles = tiles3;
         a.n_mtiles = nmt + 2;
-        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
+        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a,
                                      grid_for(E * a.n_tiles), stream, /*pair=*/false));
         if (st) return st;
         a.tiles = tiles2;
         a.n_mtiles = nmt + 1;
         const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
-        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, EPI_SITU_GLU, true, m, a,
+        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a,
                                      grid_for(max_pairs), stream, /*pair=*/true));
         if (st) return st;
     }
     mark(LMOE_STAGE_EXPERT_W3);
     {   // a6: o[a] = gate[a] * W3[e] act, written back in assignment order
+        const bool f8 = c.expert_fp8 != 0;
         GemmMaps m{m_act, m_act, h->m_w3, h->m_w3};
         GemmArgs a = base_args(h);
         a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_exp3));
-        a.k_blocks = static_cast<int32_t>(I / kBK);
+        a.k_blocks = static_cast<int32_t>(f8 ? I / 128 : I / kBK);
+        a.col_exp0 = h->w3e;
+        a.col_exp_rows = static_cast<int32_t>(L);
         a.b_expert_rows = static_cast<int32_t>(L);
         a.b_packed = 1;
         a.b_row_tiles = static_cast<int32_t>(L / h->bn_exp3);
@@ -518,8 +559,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.scatter_rows = perm;
         a.row_scale = gates;
         const int64_t max_tiles = (ceil_div(n, kBM) + E) * a.n_tiles;
-        st = gemm_status(launch_gemm(h->bn_exp3, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true, m, a,
-                                     grid_for(max_tiles), stream));
+        st = gemm_status(launch_gemm(h->bn_exp3, A_DENSE, B_PLAIN, f8 ? EPI_SCATTER_F8 : EPI_SCATTER_BF16, true,
+                                     m, a, grid_for(max_tiles), stream));
         if (st) return st;
     }
     mark(LMOE_STAGE_COMBINE);

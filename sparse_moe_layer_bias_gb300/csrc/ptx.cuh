@@ -142,6 +142,18 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
+// e4m3 x e4m3 -> fp32 (kind::f8f6f4; K = 32 per instruction, i.e. the same
+// 32 bytes of each 128-byte swizzled row as one bf16 K = 16 step).
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Load 32 consecutive fp32 columns of this thread's TMEM lane (32x32b.x32)
 // and wait for the load inside the same asm block, so no consumer of the
 // registers can be scheduled before the data has arrived.
@@ -184,6 +196,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_m128(int n) {
     return (1u << 4)                                  // D format: f32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
+           | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(128 >> 4) << 24); // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0),
+// fp32 accumulation, M = 128.
+__host__ __device__ constexpr uint32_t idesc_e4m3_m128(int n) {
+    return (1u << 4)                                  // D format: f32
+           | (0u << 7)                                // A format: e4m3
+           | (0u << 10)                               // B format: e4m3
            | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(128 >> 4) << 24); // M / 16
 }

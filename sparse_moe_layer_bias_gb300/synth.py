@@ -42,6 +42,7 @@ class LayerShape:
     beta2: float = 25.0
     rms_eps: float = 1e-6
     norm_after_down: bool = False   # ablation variant: RMSNorm on the latent as well
+    expert_fp8: bool = False        # FP8 variant: e4m3 routed experts
 
     def layer_dict(self) -> dict:
         d = asdict(self)

@@ -91,28 +91,31 @@ def staged_checks(shape, run):
     assert np.array_equal(ws_view(ws, lay, "inv", torch.int32, (T * K,)).cpu().numpy(), inv)
 
     # a5/a6: expert activations and gate-weighted outputs on the GPU's h and routing
-    rt = oracle.routed(cfg, h_lat, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"], want_act=True, want_o=True)
-    act_gpu = dec(host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))))
-    act_ref = dec(rt["act"])[perm]                       # oracle rows are in assignment order
-    # |d act/d p1| <= 1.1 * beta2 and |d act/d p2| <= beta1: the accumulation
-    # error of p1, p2 carries over with those factors
-    Hd = np.abs(dec(h_lat))
-    tok = perm // K
-    ex = idx_gpu.reshape(-1)[perm]
-    acc_tol = np.zeros_like(act_ref)
-    for e in np.unique(ex):
-        rows = np.nonzero(ex == e)[0]
-        a1 = Hd[tok[rows]] @ np.abs(dec(wb["w1"][e])).T
-        a2 = Hd[tok[rows]] @ np.abs(dec(wb["w2"][e])).T
-        acc_tol[rows] = ACC_REL * (1.1 * shape.beta2 * a1 + shape.beta1 * a2)
-    assert np.all(np.abs(act_gpu - act_ref) <= 2 * ulp_bf16(act_ref) + acc_tol)
-    o_gpu = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))))
-    assert rel_fro(o_gpu, rt["o"]) <= 5e-3
+    if shape.expert_fp8:
+        fp8_expert_checks(shape, cfg, run, h_lat, idx_gpu, g_gpu, perm, inv, wb)
+    else:
+        rt = oracle.routed(cfg, h_lat, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"], want_act=True, want_o=True)
+        act_gpu = dec(host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))))
+        act_ref = dec(rt["act"])[perm]                       # oracle rows are in assignment order
+        # |d act/d p1| <= 1.1 * beta2 and |d act/d p2| <= beta1: the accumulation
+        # error of p1, p2 carries over with those factors
+        Hd = np.abs(dec(h_lat))
+        tok = perm // K
+        ex = idx_gpu.reshape(-1)[perm]
+        acc_tol = np.zeros_like(act_ref)
+        for e in np.unique(ex):
+            rows = np.nonzero(ex == e)[0]
+            a1 = Hd[tok[rows]] @ np.abs(dec(wb["w1"][e])).T
+            a2 = Hd[tok[rows]] @ np.abs(dec(wb["w2"][e])).T
+            acc_tol[rows] = ACC_REL * (1.1 * shape.beta2 * a1 + shape.beta1 * a2)
+        assert np.all(np.abs(act_gpu - act_ref) <= 2 * ulp_bf16(act_ref) + acc_tol)
+        o_gpu = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))))
+        assert rel_fro(o_gpu, rt["o"]) <= 5e-3
 
-    # a7: RMS-normalised aggregate
-    r_gpu = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))
-    assert rel_fro(r_gpu, rt["r64"]) <= 5e-3
-    assert np.allclose(np.mean(r_gpu ** 2, axis=1), 1.0, atol=2e-2)   # unit RMS after the norm
+        # a7: RMS-normalised aggregate
+        r_gpu = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))
+        assert rel_fro(r_gpu, rt["r64"]) <= 5e-3
+        assert np.allclose(np.mean(r_gpu ** 2, axis=1), 1.0, atol=2e-2)   # unit RMS after the norm
 
     # a8': shared-expert activations on x
     sact_gpu = host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S)))
@@ -128,6 +131,72 @@ def staged_checks(shape, run):
     y_stage = oracle.up_shared(cfg, host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))), sact_gpu,
                                wb["w_up"], wb["ws3"])
     assert rel_fro(y_gpu, y_stage) <= 5e-3
+
+
+E4M3_VALUES = None
+
+
+def e4m3_table():
+    global E4M3_VALUES
+    if E4M3_VALUES is None:
+        E4M3_VALUES = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    return E4M3_VALUES
+
+
+def to_e4m3(x):
+    """Vectorised e4m3 rounding (torch's float8_e4m3fn conversion; equal to
+    the oracle's encoder inside +-448, which is pinned on the CPU)."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def fp8_expert_checks(shape, cfg, run, h_lat, idx_gpu, g_gpu, perm, inv, wb):
+    """FP8 variant, stages a5-a7 on the GPU's own inputs:
+    - the e4m3 latent codes and their exponents equal the oracle's quantisation
+      of the GPU's latent bit for bit;
+    - each activation code is the e4m3 rounding of a value within 2^-9
+      (relative, plus 1e-6) of the exact 4*act computed in fp64 from the
+      quantised operands (the GPU evaluates the SiTU-GLU in fp32 with
+      tanh.approx, ~2^-11 relative, so a value next to a rounding midpoint may
+      round to the neighbouring code), and at least 97% of them equal the
+      rounding of the exact value;
+    - o = gate * act8/4 . W3 (e4m3) on the GPU's codes, and r = RMSNorm(sum o)."""
+    ws, lay = run["ws"], run["layout"]
+    T = run["x_host"].shape[0]
+    L, I, K = shape.latent, shape.inter, shape.top_k
+    assert lay["h_fp8"] >= 0 and lay["h_fp8_exp"] >= 0
+    h8 = ws[lay["h_fp8"]:lay["h_fp8"] + T * L].view(T, L).cpu().numpy()
+    he = ws[lay["h_fp8_exp"]:lay["h_fp8_exp"] + T].cpu().numpy().view(np.int8)
+    ref_codes, ref_exps = oracle.fp8_quantize_rows(h_lat)
+    assert np.array_equal(h8, ref_codes) and np.array_equal(he, ref_exps)
+    tab = e4m3_table()
+    Hq = tab[h8] * np.exp2(he.astype(np.float64))[:, None]
+    act8 = ws[lay["act"]:lay["act"] + T * K * I].view(T * K, I).cpu().numpy()
+    tok, ex = perm // K, idx_gpu.reshape(-1)[perm]
+    x_exact = np.zeros((T * K, I))
+    o_ref = np.zeros((T * K, L))
+    gates = g_gpu.reshape(-1).astype(np.float64)
+    for e in np.unique(ex):
+        rows = np.nonzero(ex == e)[0]
+        q1, e1 = oracle.fp8_quantize_rows(wb["w1"][e])
+        q2, e2 = oracle.fp8_quantize_rows(wb["w2"][e])
+        q3, e3 = oracle.fp8_quantize_rows(wb["w3"][e])
+        W1 = tab[q1] * np.exp2(e1.astype(np.float64))[:, None]
+        W2 = tab[q2] * np.exp2(e2.astype(np.float64))[:, None]
+        W3 = tab[q3] * np.exp2(e3.astype(np.float64))[:, None]
+        p1, p2 = Hq[tok[rows]] @ W1.T, Hq[tok[rows]] @ W2.T
+        situ = shape.beta1 * np.tanh(p1 / shape.beta1) / (1.0 + np.exp(-p1))
+        x_exact[rows] = 4.0 * situ * shape.beta2 * np.tanh(p2 / shape.beta2)
+        o_ref[perm[rows]] = gates[perm[rows], None] * ((tab[act8[rows]] / 4.0) @ W3.T)
+    tol = 2.0 ** -9 * np.abs(x_exact) + 1e-6
+    lo, mid, hi = to_e4m3(x_exact - tol), to_e4m3(x_exact), to_e4m3(x_exact + tol)
+    assert np.all((act8 == lo) | (act8 == mid) | (act8 == hi))
+    assert np.mean(act8 == mid) >= 0.97
+    o_gpu = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))))
+    assert rel_fro(o_gpu, o_ref) <= 5e-3
+    z = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L)))).reshape(T, K, L).sum(axis=1)
+    r_ref = z / np.sqrt(np.mean(z ** 2, axis=1, keepdims=True) + shape.rms_eps)
+    r_gpu = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))
+    assert rel_fro(r_gpu, r_ref) <= 5e-3
 
 
 def end_to_end(shape, run):
@@ -294,3 +363,32 @@ def test_bounded_wait_timeout_is_reported_and_context_survives(lm):
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
     with pytest.raises(lm.LmoeError):
         lm.lmoe_selftest_timeout(h, 10)                   # limit below 1 us: rejected on the host
+
+
+TINY_FP8 = dataclasses.replace(synth.TINY, name="tiny_fp8", inter=128, expert_fp8=True)
+SMALL_FP8 = dataclasses.replace(synth.SMALL, name="small_fp8", expert_fp8=True)
+
+
+@pytest.mark.parametrize("T", [None, 1, 129])
+def test_fp8_experts_variant_tiny(lm, T):
+    """FP8 variant (e4m3 routed experts): every stage on the GPU's own inputs
+    (quantised latent bit-exact, activation codes valid roundings, o, r, y),
+    and the output end to end against the oracle's FP8 layer."""
+    run = run_host_shape(lm, TINY_FP8, T=T, seed_offset=0 if T is None else T)
+    staged_checks(TINY_FP8, run)
+    end_to_end(TINY_FP8, run)
+
+
+def test_fp8_experts_variant_small(lm):
+    run = run_host_shape(lm, SMALL_FP8)
+    staged_checks(SMALL_FP8, run)
+    rf, mx, kept, _ = end_to_end(SMALL_FP8, run)
+    assert kept >= 0.8 * SMALL_FP8.T
+
+
+def test_fp8_experts_rejects_unaligned_inter(lm):
+    shape = dataclasses.replace(synth.TINY, expert_fp8=True)            # inter = 64
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    with pytest.raises(lm.LmoeError) as e:
+        lm.lmoe_create(shape.layer_dict(), w, max_tokens=8)
+    assert e.value.status == 2

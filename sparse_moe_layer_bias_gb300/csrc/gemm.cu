@@ -53,7 +53,11 @@ struct Cfg {
     // keeps the 16-byte row writes and the 128-byte row reads conflict-free)
     static constexpr int kStgPitch = 144;
     static constexpr int kStgWarpBytes = 32 * kStgPitch;
-    static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes;
+    // per epilogue warp: the current tile's per-column scale factors (e4m3
+    // epilogues; up to 256 fp32)
+    static constexpr int kColWarpBytes = 1024;
+    static constexpr size_t kSmem =
+        1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes;
 };
 
 struct Tile {
@@ -111,18 +115,14 @@ __device__ __forceinline__ float situ_glu(float p1, float p2, float b1, float ib
     return (b1 * tanh_fast(p1 * ib1) * sig) * (b2 * tanh_fast(p2 * ib2));
 }
 
-// x * 2^k, exact (no rounding) while the result stays in the fp32 normal
-// range: two multiplications by powers of two built from exponent bits, each
-// factor within [2^-126, 2^127], for |k| up to 252 (k outside is clamped).
-__device__ __forceinline__ float scale_pow2(float x, int k) {
-    k = max(-252, min(252, k));
-    const int k1 = k >> 1, k2 = k - k1;
-    return x * __int_as_float((k1 + 127) << 23) * __int_as_float((k2 + 127) << 23);
+// 2^k as an fp32 built from the exponent bits, k clamped to the normal range
+// [-126, 127] (an e4m3 scale exponent outside it belongs to a row whose
+// largest magnitude is below 448 * 2^-127 or above 448 * 2^127).  Multiplying
+// by it is exact while the product stays normal.
+__device__ __forceinline__ float pow2f(int k) {
+    k = max(-126, min(127, k));
+    return __int_as_float((k + 127) << 23);
 }
-
-// Exponent byte b (0..3) of a packed word of four int8 exponents.
-__device__ __forceinline__ int exp_byte(uint32_t w, int b) { return static_cast<int8_t>((w >> (8 * b)) & 0xffu); }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -358,6 +358,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;       // row of the tile held by this thread
         uint8_t *stg = smem + S * C::kStageBytes + C::kBarBytes + (warp - 2) * C::kStgWarpBytes;
+        float *cscale = reinterpret_cast<float *>(smem + S * C::kStageBytes + C::kBarBytes + 4 * C::kStgWarpBytes +
+                                                  (warp - 2) * C::kColWarpBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -382,6 +384,22 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         pre_he[sub] = args.row_exp[args.gather_rows[ti.row0 + trow]];
                     }
                 }
+            }
+            // e4m3 epilogues: this tile's per-column power-of-two factors, into
+            // the warp's own buffer (the warp finished reading the previous
+            // tile's factors before it got here)
+            if (EPI == EPI_SCATTER_F8) {        // 2^(W3 row exponent - 2) for the BN output columns
+                const int8_t *ce = args.col_exp0 + ti.expert * args.col_exp_rows + ti.nt * BN;
+                for (int i = lane; i < BN; i += 32) cscale[i] = pow2f(__ldg(ce + i) - 2);
+                __syncwarp();
+            } else if (EPI == EPI_SITU_GLU_F8) {   // 2^(W1 row exponent), then 2^(W2 row exponent)
+                const int8_t *c1 = args.col_exp0 + ti.expert * args.col_exp_rows + ti.nt * H;
+                const int8_t *c2 = args.col_exp1 + ti.expert * args.col_exp_rows + ti.nt * H;
+                for (int i = lane; i < H; i += 32) {
+                    cscale[i] = pow2f(__ldg(c1 + i));
+                    cscale[H + i] = pow2f(__ldg(c2 + i));
+                }
+                __syncwarp();
             }
             // the whole warp must agree before the warp-collective tcgen05.ld
             if (!__all_sync(0xffffffffu,
@@ -433,30 +451,27 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 // exponent) (exact), SiTU-GLU, then the fixed activation scale:
                 // code = e4m3(4 * act), round to nearest even, saturating.  Each
                 // thread writes its row's 32 codes per group (one 32-byte sector).
-                const int ecol = ti.expert * args.col_exp_rows;
-                const int he = (NSUB > 1 && sub) ? pre_he[NSUB - 1] : pre_he[0];
+                const float rowf = pow2f((NSUB > 1 && sub) ? pre_he[NSUB - 1] : pre_he[0]);
                 uint8_t *orow = reinterpret_cast<uint8_t *>(args.out) + (ti.row0 + trow) * args.ld_out;
                 const float b1 = args.beta1, b2 = args.beta2;
                 const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
 #pragma unroll 1
                 for (int c = 0; c < H; c += 32) {
                     float p1[32], p2[32];
-                    tmem_ld32(taddr + c, p1);
-                    tmem_ld32(taddr + H + c, p2);
+                    tmem_ld32x2(taddr + c, taddr + H + c, p1, p2);
                     const int f0 = ti.nt * H + c;     // first feature of the group
-                    // the group's 32 W1 and W2 row exponents, four per 32-bit word
-                    const uint32_t *x1w = reinterpret_cast<const uint32_t *>(args.col_exp0 + ecol + f0);
-                    const uint32_t *x2w = reinterpret_cast<const uint32_t *>(args.col_exp1 + ecol + f0);
                     uint32_t w[8];
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4) {
-                        const uint32_t ew1 = __ldg(x1w + q4), ew2 = __ldg(x2w + q4);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(cscale + c + 4 * q4);
+                        const float4 s2 = *reinterpret_cast<const float4 *>(cscale + H + c + 4 * q4);
+                        const float f1[4] = {s1.x, s1.y, s1.z, s1.w}, f2[4] = {s2.x, s2.y, s2.z, s2.w};
                         uint32_t word = 0;
 #pragma unroll
                         for (int b = 0; b < 4; ++b) {
                             const int j = q4 * 4 + b;
-                            const float x1 = scale_pow2(p1[j], he + exp_byte(ew1, b));
-                            const float x2 = scale_pow2(p2[j], he + exp_byte(ew2, b));
+                            const float x1 = p1[j] * rowf * f1[b];   // exact power-of-two scalings
+                            const float x2 = p2[j] * rowf * f2[b];
                             const float a4 = 4.0f * situ_glu(x1, x2, b1, ib1, b2, ib2);
                             const uint32_t code = __nv_cvt_float_to_fp8(a4, __NV_SATFINITE, __NV_E4M3);
                             word |= code << (8 * b);
@@ -483,29 +498,33 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 #pragma unroll 1
                 for (int c = 0; c < NOUT; c += 64) {
                     uint32_t packed[32];
+                    float va[32], vb[32];
+                    if (EPI != EPI_SITU_GLU) tmem_ld32x2(taddr + c, taddr + c + 32, va, vb);   // both halves
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         float v[32];
-                        tmem_ld32(taddr + c + h2 * 32, v);
                         if (EPI == EPI_SITU_GLU) {
                             float p2[32];
-                            tmem_ld32(taddr + H + c + h2 * 32, p2);
+                            tmem_ld32x2(taddr + c + h2 * 32, taddr + H + c + h2 * 32, v, p2);
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = situ_glu(v[j], p2[j], b1, ib1, b2, ib2);
-                        } else if (EPI == EPI_SCATTER_BF16) {
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = h2 ? vb[j] : va[j];
+                        }
+                        if (EPI == EPI_SCATTER_BF16) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] *= scale;
                         } else if (EPI == EPI_SCATTER_F8) {
                             // e4m3 experts' W3: gate * 2^(weight-row exponent - 2); the
                             // -2 undoes the activation's fixed scale of 4 (exact)
-                            const uint32_t *cw = reinterpret_cast<const uint32_t *>(
-                                args.col_exp0 + ti.expert * args.col_exp_rows + col0 + c + h2 * 32);
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4) {
-                                const uint32_t ew = __ldg(cw + q4);
-#pragma unroll
-                                for (int b = 0; b < 4; ++b)
-                                    v[q4 * 4 + b] = scale_pow2(v[q4 * 4 + b] * scale, exp_byte(ew, b) - 2);
+                                const float4 f = *reinterpret_cast<const float4 *>(cscale + c + h2 * 32 + 4 * q4);
+                                v[q4 * 4 + 0] = v[q4 * 4 + 0] * scale * f.x;
+                                v[q4 * 4 + 1] = v[q4 * 4 + 1] * scale * f.y;
+                                v[q4 * 4 + 2] = v[q4 * 4 + 2] * scale * f.z;
+                                v[q4 * 4 + 3] = v[q4 * 4 + 3] * scale * f.w;
                             }
                         }
 #pragma unroll

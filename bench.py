@@ -321,7 +321,8 @@ def run_profile_case(args):
     import __graft_entry__
     __graft_entry__.build()
     import sparse_moe_layer_bias_gb300 as lm
-    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="zipf")
+    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="zipf",
+                                expert_fp8=bool(args.fp8))
     w = synth.layer_weights_device(shape)
     x, bias = synth.activations_device(shape)
     h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
@@ -338,7 +339,7 @@ def run_profile_case(args):
     e1.record()
     torch.cuda.synchronize()
     assert lm.lmoe_device_status(h) == 0
-    print(json.dumps({"case": "ncu_case", "T": shape.T, "n_experts": shape.n_experts,
+    print(json.dumps({"case": "ncu_case", "T": shape.T, "n_experts": shape.n_experts, "fp8": bool(args.fp8),
                       "ms_per_iter": e0.elapsed_time(e1) / max(args.steps, 1),
                       "y_finite": bool(torch.isfinite(y.float()).all().item())}), flush=True)
     return 0
@@ -355,6 +356,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=128)
     ap.add_argument("--profile-case", action="store_true",
                     help="small case for ncu captures: K3 widths, 256 experts, T=2048 (~3.3 GB)")
+    ap.add_argument("--fp8", action="store_true", help="with --profile-case: the FP8 expert variant")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()

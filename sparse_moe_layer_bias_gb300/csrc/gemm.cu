@@ -596,6 +596,7 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     LMOE_GEMM_CASE(128, A_DENSE, B_GLU, EPI_SITU_GLU, false)
     // a2 router scores
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
+    LMOE_GEMM_CASE(224, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)   // E = 896 = 4 x 224: no padded columns
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false)
     // a5 routed experts W1|W2 (token rows gathered per expert) with the
     // SiTU-GLU epilogue: pair tiles of 256 rows for experts with many tokens,

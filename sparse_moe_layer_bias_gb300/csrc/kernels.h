@@ -64,7 +64,7 @@ struct GemmArgs {
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
 
-// Launch one persistent GEMM.  `bn` in {128, 256}.  With `pair`, A_GATHER runs
+// Launch one persistent GEMM.  `bn` in {128, 256} (224 for the router).  With `pair`, A_GATHER runs
 // pair tiles (two 128-row sub-tiles sharing each weight stage); without, 128-row
 // tiles with a deeper stage ring.  Returns cudaErrorInvalidValue for a
 // combination that is not compiled.

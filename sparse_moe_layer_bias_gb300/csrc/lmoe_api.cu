@@ -275,8 +275,9 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
     h->bn_exp1 = (I % 128 == 0) ? 256 : 128;
     h->bn_exp3 = (L % 256 == 0) ? 256 : 128;   // latent % 128 == 0: the boxes tile each expert's W3
     h->bn_up = (d % 256 == 0) ? 256 : 128;
-    // router: 256-wide N tiles unless E fits one 128-wide tile
-    h->bn_router = (E > 128) ? 256 : 128;
+    // router: 224-wide N tiles when they cover E exactly (K3: 896 = 4 x 224),
+    // else 256-wide unless E fits one 128-wide tile
+    h->bn_router = (E % 224 == 0) ? 224 : (E > 128) ? 256 : 128;
     // Repack W1, W2 (boxes of bn_exp1/2 rows) and W3 (boxes of bn_exp3 rows)
     // so each box is one contiguous block of HBM; in the FP8 variant the
     // boxes hold e4m3 codes (128 per 128-byte row) instead of bf16.

@@ -80,3 +80,20 @@ def check_layer_output(y_gpu_bf16: torch.Tensor, y_ref: np.ndarray, margin: np.n
 
 def oracle_cfg(shape: synth.LayerShape) -> oracle.LayerConfig:
     return oracle.LayerConfig(**shape.layer_dict())
+
+
+_E4M3_VALUES = None
+
+
+def e4m3_table():
+    """fp64 value of each of the 256 e4m3 codes (the oracle's decoder)."""
+    global _E4M3_VALUES
+    if _E4M3_VALUES is None:
+        _E4M3_VALUES = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    return _E4M3_VALUES
+
+
+def to_e4m3(x):
+    """Vectorised e4m3 rounding (torch's float8_e4m3fn conversion; equal to
+    the oracle's encoder inside +-448, which is pinned on the CPU)."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()

@@ -6,6 +6,8 @@ At these sizes the oracle runs on every token for the discrete steps (top-k
 and the permutation, bit-exact) and on a sample of tokens for the float steps;
 the layer is token-independent, so a sampled token's oracle forward is exact.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -13,8 +15,8 @@ import torch
 import oracle
 from sparse_moe_layer_bias_gb300 import synth
 
-from layer_check import (ACC_REL, check_layer_output, score_tol, dec, host_bits, oracle_cfg, rel_fro,
-                         ulp_bf16, ws_view)
+from layer_check import (ACC_REL, check_layer_output, e4m3_table, score_tol, dec, host_bits, oracle_cfg, rel_fro,
+                         to_e4m3, ulp_bf16, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -141,3 +143,102 @@ def test_k3_prefill_layer(lm):
     assert counts.sum() == shape.T * shape.top_k
     load = counts / counts.mean()
     assert load.max() > 5.0                 # the router weights make the loads Zipf-skewed
+
+
+# ------------------------------------------------------------------ FP8 variant at K3 size
+def check_k3_fp8(shape, run, sample):
+    """The FP8 expert variant at the benchmarked K3 shapes: routing is the bf16
+    layer's (bit-exact on every token), the e4m3 latent of every token is
+    bit-exact, and on the sampled tokens the activation codes are valid
+    roundings of the exact value (as in the tiny/small tests), o and y match
+    the oracle on the GPU's own inputs, and y matches the oracle's FP8 layer."""
+    cfg = oracle_cfg(shape)
+    T, E, K, L, I = shape.T, shape.n_experts, shape.top_k, shape.latent, shape.inter
+    S = shape.n_shared * shape.shared_inter
+    ws, lay, w = run["ws"], run["lay"], run["w"]
+    bias = run["bias"].cpu().numpy()
+    s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, E)).cpu().numpy()
+    idx_gpu = ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).cpu().numpy()
+    g_gpu = ws_view(ws, lay, "gates", torch.float32, (T, K)).cpu().numpy()
+    idx_ref, g_ref, _ = oracle.topk(cfg, s_gpu, bias)
+    assert np.array_equal(idx_gpu, idx_ref) and np.array_equal(g_gpu, g_ref)
+    counts, offsets, perm, inv = oracle.permute(cfg, idx_gpu)
+    assert np.array_equal(ws_view(ws, lay, "perm", torch.int32, (T * K,)).cpu().numpy(), perm)
+
+    h_all = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L)))
+    h8 = ws[lay["h_fp8"]:lay["h_fp8"] + T * L].view(T, L).cpu().numpy()
+    he = ws[lay["h_fp8_exp"]:lay["h_fp8_exp"] + T].cpu().numpy().view(np.int8)
+    rc, re_ = oracle.fp8_quantize_rows(h_all)
+    assert np.array_equal(h8, rc) and np.array_equal(he, re_)
+
+    tab = e4m3_table()
+    sm = np.asarray(sample)
+    rows = (sm[:, None] * K + np.arange(K)[None, :]).reshape(-1)      # assignment ids of the sample
+    prow = inv[rows]
+    act8 = ws[lay["act"]:lay["act"] + T * K * I].view(T * K, I)[torch.from_numpy(prow).cuda()].cpu().numpy()
+    o_all = ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))
+    o_gpu = dec(host_bits(o_all[torch.from_numpy(rows).cuda()]))
+    x_exact = np.zeros((rows.size, I))
+    o_ref = np.zeros((rows.size, L))
+    Hq = tab[h8[sm]] * np.exp2(he[sm].astype(np.float64))[:, None]
+    deq = {}
+
+    def dequant(name, e):
+        if (name, e) not in deq:
+            q, x = oracle.fp8_quantize_rows(synth.bits(w[name][e]))
+            deq[(name, e)] = tab[q] * np.exp2(x.astype(np.float64))[:, None]
+        return deq[(name, e)]
+
+    for n_, a in enumerate(rows):
+        e = int(idx_gpu.reshape(-1)[a])
+        hq = Hq[n_ // K]
+        p1, p2 = dequant("w1", e) @ hq, dequant("w2", e) @ hq
+        x_exact[n_] = 4.0 * shape.beta1 * np.tanh(p1 / shape.beta1) / (1.0 + np.exp(-p1)) * \
+            shape.beta2 * np.tanh(p2 / shape.beta2)
+        o_ref[n_] = float(g_gpu.reshape(-1)[a]) * (dequant("w3", e) @ (tab[act8[n_]] / 4.0))
+    tol = 2.0 ** -9 * np.abs(x_exact) + 1e-6
+    lo, mid, hi = to_e4m3(x_exact - tol), to_e4m3(x_exact), to_e4m3(x_exact + tol)
+    assert np.all((act8 == lo) | (act8 == mid) | (act8 == hi))
+    assert np.mean(act8 == mid) >= 0.97
+    assert rel_fro(o_gpu, o_ref) <= 5e-3
+
+    # y on the GPU's own r and shared activations
+    r_bits = host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))[torch.from_numpy(sm).cuda()])
+    sa_bits = host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))[torch.from_numpy(sm).cuda()])
+    wup, ws3 = synth.bits(w["w_up"]), synth.bits(w["ws3"])
+    y_gpu = run["y"][torch.from_numpy(sm).cuda()]
+    y_stage = oracle.up_shared(cfg, r_bits, sa_bits, wup, ws3)
+    assert rel_fro(y_gpu.float().cpu().numpy().astype(np.float64), y_stage) <= 5e-3
+
+    # end to end on the sampled tokens from the GPU's own latent h through the
+    # oracle's FP8 layer (quantisation of h, experts, combine, norm, up and
+    # shared experts).  Starting from x instead would compare two different
+    # e4m3 decisions: ~0.5% of h's elements round differently under fp32 and
+    # fp64 accumulation, and e4m3's coarse grid turns one or a few of them per
+    # token into whole-step code differences that move y by 1-2%.
+    xb = host_bits(run["x"][torch.from_numpy(sm).cuda()])
+    h_s = h_all[sm]
+    idx_s, g_s = idx_gpu[sm], g_gpu[sm]
+    used = np.unique(idx_s)
+    we = {n: {int(e): synth.bits(w[n][int(e)]) for e in used} for n in ("w1", "w2", "w3")}
+    rt = oracle.routed_fp8(cfg, h_s, idx_s, g_s, we["w1"], we["w2"], we["w3"])
+    y_o = oracle.up_shared(cfg, rt["r"], oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"])),
+                           wup, ws3)
+    _, _, margin = oracle.topk(cfg, s_gpu[sm], bias)
+    check_layer_output(y_gpu, y_o, margin)
+
+
+def fp8_shape(shape):
+    return dataclasses.replace(shape, name=shape.name + "_fp8", expert_fp8=True)
+
+
+def test_k3_decode_layer_fp8(lm):
+    shape = fp8_shape(synth.K3_DECODE)
+    run = run_k3(lm, shape)
+    check_k3_fp8(shape, run, sorted(set([0, 17, 40, 63] + outlier_tokens(run["x"]))))
+
+
+def test_k3_prefill_layer_fp8(lm):
+    shape = fp8_shape(synth.K3_PREFILL)
+    run = run_k3(lm, shape)
+    check_k3_fp8(shape, run, sorted(set([0, 1, 4095, 8191] + outlier_tokens(run["x"], 2))))

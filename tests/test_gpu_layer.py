@@ -11,8 +11,8 @@ import torch
 import oracle
 from sparse_moe_layer_bias_gb300 import synth
 
-from layer_check import (ACC_REL, check_layer_output, score_tol, dec, host_bits, oracle_cfg, rel_fro, ulp_bf16,
-                         ws_view)
+from layer_check import (ACC_REL, check_layer_output, score_tol, dec, e4m3_table, host_bits, oracle_cfg, rel_fro,
+                         to_e4m3, ulp_bf16, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -133,22 +133,6 @@ def staged_checks(shape, run):
     assert rel_fro(y_gpu, y_stage) <= 5e-3
 
 
-E4M3_VALUES = None
-
-
-def e4m3_table():
-    global E4M3_VALUES
-    if E4M3_VALUES is None:
-        E4M3_VALUES = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
-    return E4M3_VALUES
-
-
-def to_e4m3(x):
-    """Vectorised e4m3 rounding (torch's float8_e4m3fn conversion; equal to
-    the oracle's encoder inside +-448, which is pinned on the CPU)."""
-    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-
-
 def fp8_expert_checks(shape, cfg, run, h_lat, idx_gpu, g_gpu, perm, inv, wb):
     """FP8 variant, stages a5-a7 on the GPU's own inputs:
     - the e4m3 latent codes and their exponents equal the oracle's quantisation
@@ -218,6 +202,21 @@ def end_to_end(shape, run):
         s_g = oracle.router(cfg, oracle.rms_rows(cfg, h_gpu), wb["w_router"])
         idx_g, _, _ = oracle.topk(cfg, s_g, bias)
         also = np.all(np.sort(idx_g, 1) == np.sort(ref["idx"], 1), axis=1)
+    if shape.expert_fp8:
+        # FP8 variant: from the GPU's own latent h on (see fp8_expert_checks:
+        # e4m3's coarse grid turns last-bit differences of h into whole-step
+        # code differences, a different but equally valid quantisation)
+        T, L = run["x_host"].shape[0], shape.latent
+        ws, lay = run["ws"], run["layout"]
+        h_gpu = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L)))
+        idx_gpu = ws_view(ws, lay, "topk_idx", torch.int32, (T, shape.top_k)).cpu().numpy()
+        g_gpu = ws_view(ws, lay, "gates", torch.float32, (T, shape.top_k)).cpu().numpy()
+        s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, shape.n_experts)).cpu().numpy()
+        rt = oracle.routed_fp8(cfg, h_gpu, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"])
+        y_ref = oracle.up_shared(cfg, rt["r"], ref["a_s"], wb["w_up"], wb["ws3"])
+        _, _, margin = oracle.topk(cfg, s_gpu, bias)
+        rf, mx, kept = check_layer_output(run["y"], y_ref, margin)
+        return rf, mx, kept, ref
     rf, mx, kept = check_layer_output(run["y"], ref["y"], ref["margin"], also_keep=also)
     return rf, mx, kept, ref
 

@@ -404,34 +404,45 @@ def main():
     assert lm.lmoe_device_status(handle) == 0
     touched = int((counts > 0).sum().item())
 
-    # per-stage events for every timed step (read after the timed region)
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)]
-               for _ in range(args.steps)]
-    for evs in ev_sets:       # create the cudaEvent_t handles outside the timed region
-        for e in evs:
-            e.record(stream)
+    # Headline: K steps with nothing between the kernels but the kernels (the
+    # library launches them as programmatic dependent launches, so a kernel's
+    # prologue overlaps its predecessor's tail).
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    qb_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(args.steps)]
     with ClockSampler(torch.cuda.current_device()) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         t_start.record(stream)
         for i in range(args.steps):
-            lm.lmoe_set_stage_events(handle, ev_sets[i])
-            lm.lmoe_forward(handle, x, bias, y=y, workspace=ws, scores_out=scores,
-                            expert_counts_out=counts, stream=stream)
-            qb_ev[i][0].record(stream)
-            lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
-            qb_allreduce_histogram(hist)
-            lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
-            qb_ev[i][1].record(stream)
+            step(x, bias, y)
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    lm.lmoe_set_stage_events(handle, None)
     ms = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(world, ms)
+    assert lm.lmoe_device_status(handle) == 0
+
+    # Breakdown: K more steps with a CUDA event before every stage (the events
+    # serialise the kernels, so these per-stage times add up to a little more
+    # than the headline step)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)]
+               for _ in range(args.steps)]
+    for evs in ev_sets:       # create the cudaEvent_t handles before use
+        for e in evs:
+            e.record(stream)
+    qb_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        lm.lmoe_set_stage_events(handle, ev_sets[i])
+        lm.lmoe_forward(handle, x, bias, y=y, workspace=ws, scores_out=scores,
+                        expert_counts_out=counts, stream=stream)
+        qb_ev[i][0].record(stream)
+        lm.qb_histogram(scores, QB_B, hist=hist, stream=stream)
+        qb_allreduce_histogram(hist)
+        lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
+        qb_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    lm.lmoe_set_stage_events(handle, None)
     assert lm.lmoe_device_status(handle) == 0
 
     stage_ms = {}
@@ -527,25 +538,33 @@ def main():
     h2d = x.numel() * 2 + bias.numel() * 4
     d2h = y.numel() * 2 + E * 4
 
-    # --------------------------------------------------------------- QB sweep point T = 2^20
-    Tq = 1 << 20
-    sq = synth.qb_scores(Tq, E, device="cuda")
-    hq = torch.empty((E, QB_B), dtype=torch.int32, device="cuda")
-    for _ in range(3):
-        lm.qb_histogram(sq, QB_B, hist=hq, stream=stream)
-    torch.cuda.synchronize()
-    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nq = max(10, args.steps)
-    q0.record(stream)
-    for _ in range(nq):
-        lm.qb_histogram(sq, QB_B, hist=hq, stream=stream)
-    q1.record(stream)
-    torch.cuda.synchronize()
-    qb_ms = q0.elapsed_time(q1) / nq
-    qb_bytes = 4.0 * Tq * E + 4.0 * E * QB_B
-    qb_gbs = qb_bytes / (qb_ms * 1e-3) / 1e9
-    del sq
-    torch.cuda.empty_cache()
+    # --------------------------------------------------------------- QB histogram sweep
+    # T in {65536, 262144, 2^20} x 896 experts, B in {1000, 10000}; every
+    # score tensor is larger than L2, so back-to-back launches stream it from HBM
+    sweep = []
+    for Tq in synth.QB_SWEEP_T:
+        sq = synth.qb_scores(Tq, E, device="cuda")
+        for Bq in synth.QB_SWEEP_B:
+            hq = torch.empty((E, Bq), dtype=torch.int32, device="cuda")
+            for _ in range(3):
+                lm.qb_histogram(sq, Bq, hist=hq, stream=stream)
+            torch.cuda.synchronize()
+            q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            nq = max(10, args.steps)
+            q0.record(stream)
+            for _ in range(nq):
+                lm.qb_histogram(sq, Bq, hist=hq, stream=stream)
+            q1.record(stream)
+            torch.cuda.synchronize()
+            ms_q = q0.elapsed_time(q1) / nq
+            gbs_q = (4.0 * Tq * E + 4.0 * E * Bq) / (ms_q * 1e-3) / 1e9
+            sweep.append({"T": Tq, "E": E, "B": Bq, "ms": round(ms_q, 4), "gbs": round(gbs_q, 1),
+                          "frac_hbm": round(gbs_q / peaks["hbm_gbs"], 4)})
+            del hq
+        del sq
+        torch.cuda.empty_cache()
+    head = next(p for p in sweep if p["T"] == (1 << 20) and p["B"] == QB_B)
+    Tq, qb_ms, qb_gbs = head["T"], head["ms"], head["gbs"]
     qb_loop = qb_closed_loop(lm, stream)
 
     # --------------------------------------------------------------- decode layer T = 64
@@ -610,6 +629,7 @@ def main():
         "qb_ms_in_step": round(stage_ms["qb"], 4),
         "qb_hist_sweep": {"T": Tq, "E": E, "B": QB_B, "ms": round(qb_ms, 4), "gbs": round(qb_gbs, 1),
                           "frac_hbm": round(qb_gbs / peaks["hbm_gbs"], 4)},
+        "qb_hist_sweep_all": sweep,
         "qb_closed_loop": qb_loop,
         "fp8_experts": fp8,
         "decode": {"T": dshape.T, "ms": round(dec_ms, 4), "tokens_per_s": dshape.T / (dec_ms * 1e-3),

@@ -30,6 +30,7 @@ template <int VPT>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_rmsnorm_kernel(const uint16_t *__restrict__ o, int k, int L, float eps,
                            uint16_t *__restrict__ r) {
+    grid_dependency_wait();
     const int64_t t = blockIdx.x;
     const int nvec = L / 8;
     float acc[VPT][8];
@@ -112,6 +113,7 @@ __device__ __forceinline__ float f64_to_f32_round_odd(double d) {
 
 __global__ void __launch_bounds__(kCombineThreads)
     rms_rows_kernel(const uint16_t *__restrict__ h, int L, double eps, uint16_t *__restrict__ out) {
+    grid_dependency_wait();
     const int64_t t = blockIdx.x;
     const int nvec = L / 8;
     const uint4 *row = reinterpret_cast<const uint4 *>(h + t * int64_t(L));
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 cudaError_t launch_rms_rows(const uint16_t *h, int64_t T, int L, double eps, uint16_t *out, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    rms_rows_kernel<<<static_cast<unsigned>(T), kCombineThreads, 0, st>>>(h, L, eps, out);
-    return cudaGetLastError();
+    return launch_kernel(rms_rows_kernel, dim3(static_cast<unsigned>(T)), dim3(kCombineThreads), 0, st, true, h, L, eps,
+                         out);
 }
 
 cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,
@@ -166,15 +168,11 @@ cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, f
     const int nvec = L / 8;
     const int vpt = (nvec + kCombineThreads - 1) / kCombineThreads;
     const dim3 grid(static_cast<unsigned>(T));
-    if (vpt <= 1)
-        combine_rmsnorm_kernel<1><<<grid, kCombineThreads, 0, st>>>(o, k, L, eps, r);
-    else if (vpt <= 2)
-        combine_rmsnorm_kernel<2><<<grid, kCombineThreads, 0, st>>>(o, k, L, eps, r);
-    else if (vpt <= 4)
-        combine_rmsnorm_kernel<4><<<grid, kCombineThreads, 0, st>>>(o, k, L, eps, r);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    const dim3 block(kCombineThreads);
+    if (vpt <= 1) return launch_kernel(combine_rmsnorm_kernel<1>, grid, block, 0, st, true, o, k, L, eps, r);
+    if (vpt <= 2) return launch_kernel(combine_rmsnorm_kernel<2>, grid, block, 0, st, true, o, k, L, eps, r);
+    if (vpt <= 4) return launch_kernel(combine_rmsnorm_kernel<4>, grid, block, 0, st, true, o, k, L, eps, r);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace lmoe

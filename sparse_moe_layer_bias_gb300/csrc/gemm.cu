@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    grid_dependency_wait();   // inputs of this GEMM come from earlier kernels
     const int n_m = GROUPED ? *args.n_mtiles : args.m_tiles;
     const int total = n_m * args.n_tiles;
     const uint64_t lim = args.wait_limit_ns;
@@ -567,13 +568,12 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 }
 
 template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR = false>
-cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t st) {
+cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t st, bool dependent) {
     auto kern = gemm_kernel<BN, AM, BMD, EPI, GROUPED, PAIR>;
     const size_t smem = Cfg<BN, PAIR>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, threads_for(AM), smem, st>>>(m.a0, m.a1, m.b0, m.b1, a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(threads_for(AM)), smem, st, dependent, m.a0, m.a1, m.b0, m.b1, a);
 }
 
 }  // namespace
@@ -582,10 +582,10 @@ size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256, false>::kSmem : Cfg
 
 #define LMOE_GEMM_CASE(BN_, AM_, BM_, EPI_, G_)                                   \
     if (bn == BN_ && am == AM_ && bm == BM_ && epi == EPI_ && grouped == G_)       \
-        return launch_one<BN_, AM_, BM_, EPI_, G_>(maps, args, grid, stream);
+        return launch_one<BN_, AM_, BM_, EPI_, G_>(maps, args, grid, stream, dependent);
 
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
-                        const GemmArgs &args, int grid, cudaStream_t stream, bool pair) {
+                        const GemmArgs &args, int grid, cudaStream_t stream, bool pair, bool dependent) {
     // a1 down-projection, a8 up-projection + shared W3
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_BF16, false)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_BF16, false)
@@ -603,11 +603,11 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     // 128-row tiles (smaller stages, one more of them in flight) for the others
     if (am == A_GATHER && bm == B_GLU && epi == EPI_SITU_GLU && grouped) {
         if (pair) {
-            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
-            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream);
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream, dependent);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, true>(maps, args, grid, stream, dependent);
         } else {
-            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream);
-            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream);
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream, dependent);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream, dependent);
         }
     }
     // a6 routed experts W3 with the gate-weighted scatter
@@ -616,11 +616,11 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
     // FP8 variant: e4m3 experts (kind::f8f6f4)
     if (am == A_GATHER && bm == B_GLU && epi == EPI_SITU_GLU_F8 && grouped) {
         if (pair) {
-            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, true>(maps, args, grid, stream);
-            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, true>(maps, args, grid, stream);
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, true>(maps, args, grid, stream, dependent);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, true>(maps, args, grid, stream, dependent);
         } else {
-            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, false>(maps, args, grid, stream);
-            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, false>(maps, args, grid, stream);
+            if (bn == 256) return launch_one<256, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, false>(maps, args, grid, stream, dependent);
+            if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU_F8, true, false>(maps, args, grid, stream, dependent);
         }
     }
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_F8, true)

@@ -8,6 +8,35 @@
 
 namespace lmoe {
 
+// ------------------------------------------------------------------ launch
+// Launch a kernel; with `dependent`, as a programmatic dependent launch: its
+// CTAs may start while the previous kernel in the stream finishes, run their
+// prologue, and wait in grid_dependency_wait() until that kernel has completed
+// and its writes are visible.  Every kernel launched this way calls
+// grid_dependency_wait() in all threads before touching memory that earlier
+// work in the stream wrote, and before it can complete, so the chain of
+// completions stays transitive.  (A kernel whose predecessor is not a kernel,
+// e.g. a memset, is simply ordered after it.)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          bool dependent, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
 // Device status bits written by kernels (see lmoe_device_status).
 constexpr unsigned kDevErrTimeout = 1u;
 
@@ -71,7 +100,8 @@ struct GemmArgs {
 // The e4m3 epilogues select the kind::f8f6f4 MMA (A and B e4m3; a k-block is
 // then 128 elements); every other epilogue multiplies bf16.
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
-                        const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false);
+                        const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false,
+                        bool dependent = true);
 size_t gemm_smem_bytes(int bn);
 
 // Repack per-expert weights [E][R][K] (row-major bf16) into tile-contiguous

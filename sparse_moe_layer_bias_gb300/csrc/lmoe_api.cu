@@ -446,8 +446,10 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = hbuf;
         a.ld_out = L;
         a.out_cols = static_cast<int32_t>(L);
+        // the first kernel of the forward follows a memset: ordinary stream order
         st = gemm_status(launch_gemm(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream, /*pair=*/false,
+                                     /*dependent=*/false));
         if (st) return st;
     }
     if (c.norm_after_down &&   // ablation variant: hn = h / sqrt(mean(h^2) + eps), per token

@@ -47,6 +47,7 @@ constexpr int kQuantThreads = 128;
 __global__ void __launch_bounds__(kQuantThreads)
     fp8_quantize_rows_kernel(const uint4 *__restrict__ src, int K, uint2 *__restrict__ codes,
                              int8_t *__restrict__ exps) {
+    grid_dependency_wait();
     const int64_t r = blockIdx.x;
     const int nvec = K / 8;
     const uint4 *row = src + r * nvec;
@@ -97,9 +98,8 @@ cudaError_t launch_fp8_quantize_rows(const uint16_t *src, int64_t R, int K, uint
     if (K % 8 != 0 || R < 0) return cudaErrorInvalidValue;
     if (R == 0) return cudaSuccess;
     if (R > 0x7fffffffLL) return cudaErrorInvalidValue;
-    fp8_quantize_rows_kernel<<<static_cast<unsigned>(R), kQuantThreads, 0, st>>>(
-        reinterpret_cast<const uint4 *>(src), K, reinterpret_cast<uint2 *>(codes), exps);
-    return cudaGetLastError();
+    return launch_kernel(fp8_quantize_rows_kernel, dim3(static_cast<unsigned>(R)), dim3(kQuantThreads), 0, st, true,
+                         reinterpret_cast<const uint4 *>(src), K, reinterpret_cast<uint2 *>(codes), exps);
 }
 
 cudaError_t launch_pack_tiles(const uint16_t *src, int64_t E, int R, int K, int TR, uint16_t *dst,

@@ -190,11 +190,19 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     const int n_groups = (E + epc - 1) / epc;
     const size_t smem = size_t(epc) * per_expert;
     const int ctas_per_sm = max(1, min(2, static_cast<int>((227 * 1024) / (smem + 1024))));
-    int n_chunks = max(1, (num_sms * ctas_per_sm) / n_groups);
+    // Token chunks per expert group: the fewest (each chunk ends with one
+    // global add per non-zero counter) that fill the GPU in whole waves --
+    // the first count whose last wave is at least 90% full.
+    const int slots = num_sms * ctas_per_sm;
     const int64_t min_rows = 512;
     const int64_t max_chunks = (T + min_rows - 1) / min_rows;
-    if (n_chunks > max_chunks) n_chunks = static_cast<int>(max_chunks);
-    n_chunks = max(n_chunks, 1);
+    int n_chunks = 1;
+    for (int c = max(1, slots / n_groups); c <= 16 && c <= max_chunks; ++c) {
+        n_chunks = c;
+        const int ctas = n_groups * c;
+        const int waves = (ctas + slots - 1) / slots;
+        if (ctas * 10 >= waves * slots * 9) break;
+    }
     const int64_t rows_per_chunk = (T + n_chunks - 1) / n_chunks;
     const unsigned grid = static_cast<unsigned>(n_groups) * static_cast<unsigned>(n_chunks);
 

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, int64_t T, int E,
                 int k, int32_t *__restrict__ idx, float *__restrict__ gate,
                 uint32_t *__restrict__ bitmap, int words) {
+    grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = int64_t(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 // word_prefix[e][w] = number of tokens < 32*w that picked e; counts[e] = total.
 __global__ void expert_scan_kernel(const uint32_t *__restrict__ bitmap, int E, int words,
                                    uint32_t *__restrict__ word_prefix, int32_t *__restrict__ counts) {
+    grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (e >= E) return;
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(1024)
                          int4 *__restrict__ tiles, int32_t *__restrict__ n_mtiles,
                          int4 *__restrict__ tiles2, int32_t *__restrict__ n_mtiles2,
                          int4 *__restrict__ tiles3, int32_t *__restrict__ n_mtiles3) {
+    grid_dependency_wait();
     __shared__ int32_t s_cnt[1024];
     __shared__ int32_t s_til[1024];
     __shared__ int32_t s_til2[1024];
@@ -159,6 +162,7 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int k
                                const uint32_t *__restrict__ word_prefix, int words,
                                const int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                                int32_t *__restrict__ inv, int32_t *__restrict__ tokrow) {
+    grid_dependency_wait();
     const int64_t a = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (a >= T * k) return;
     const int64_t t = a / k;
@@ -180,33 +184,30 @@ cudaError_t launch_topk(const float *scores, const float *bias, int64_t T, int E
     const dim3 block(kTopkWarps * 32);
     const int v = (E + 31) / 32;
     if (v <= 1)
-        topk_kernel<1><<<grid, block, 0, st>>>(scores, bias, T, E, k, idx, gate, bitmap, words);
+        return launch_kernel(topk_kernel<1>, grid, block, 0, st, true, scores, bias, T, E, k, idx, gate, bitmap, words);
     else if (v <= 4)
-        topk_kernel<4><<<grid, block, 0, st>>>(scores, bias, T, E, k, idx, gate, bitmap, words);
+        return launch_kernel(topk_kernel<4>, grid, block, 0, st, true, scores, bias, T, E, k, idx, gate, bitmap, words);
     else if (v <= 8)
-        topk_kernel<8><<<grid, block, 0, st>>>(scores, bias, T, E, k, idx, gate, bitmap, words);
+        return launch_kernel(topk_kernel<8>, grid, block, 0, st, true, scores, bias, T, E, k, idx, gate, bitmap, words);
     else if (v <= 16)
-        topk_kernel<16><<<grid, block, 0, st>>>(scores, bias, T, E, k, idx, gate, bitmap, words);
+        return launch_kernel(topk_kernel<16>, grid, block, 0, st, true, scores, bias, T, E, k, idx, gate, bitmap, words);
     else if (v <= 28)
-        topk_kernel<28><<<grid, block, 0, st>>>(scores, bias, T, E, k, idx, gate, bitmap, words);
-    else
-        topk_kernel<32><<<grid, block, 0, st>>>(scores, bias, T, E, k, idx, gate, bitmap, words);
-    return cudaGetLastError();
+        return launch_kernel(topk_kernel<28>, grid, block, 0, st, true, scores, bias, T, E, k, idx, gate, bitmap, words);
+    return launch_kernel(topk_kernel<32>, grid, block, 0, st, true, scores, bias, T, E, k, idx, gate, bitmap, words);
 }
 
 cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words, uint32_t *word_prefix,
                                int32_t *counts, cudaStream_t st) {
     const int wpb = 8;
-    expert_scan_kernel<<<(E + wpb - 1) / wpb, wpb * 32, 0, st>>>(bitmap, E, words, word_prefix, counts);
-    return cudaGetLastError();
+    return launch_kernel(expert_scan_kernel, dim3((E + wpb - 1) / wpb), dim3(wpb * 32), 0, st, true, bitmap, E, words,
+                         word_prefix, counts);
 }
 
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
                                  int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2, int4 *tiles3,
                                  int32_t *n_mtiles3, cudaStream_t st) {
-    offsets_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, offsets, tiles, n_mtiles, tiles2, n_mtiles2,
-                                             tiles3, n_mtiles3);
-    return cudaGetLastError();
+    return launch_kernel(offsets_tiles_kernel, dim3(1), dim3(1024), 0, st, true, counts, E, offsets, tiles, n_mtiles,
+                         tiles2, n_mtiles2, tiles3, n_mtiles3);
 }
 
 cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
@@ -214,9 +215,8 @@ cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t 
                            int32_t *perm, int32_t *inv, int32_t *tokrow, cudaStream_t st) {
     const int64_t n = T * k;
     if (n == 0) return cudaSuccess;
-    scatter_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-        idx, T, k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
-    return cudaGetLastError();
+    return launch_kernel(scatter_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, true, idx, T,
+                         k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
 }
 
 }  // namespace lmoe

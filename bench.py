@@ -41,6 +41,9 @@ from sparse_moe_layer_bias_gb300 import synth  # noqa: E402
 
 METRIC = "LatentMoE layer tokens/s & %bf16 TC peak (K3 shape); QB histogram HBM GB/s"
 QB_B = 1000
+# DRAM read+write / algorithmic bytes, measured with ncu on `--profile-case`
+# for the kernels that can be the step's dominant one (profiles/ has the runs)
+TRAFFIC_RATIO = {"expert_w3": 0.985, "expert_w12_light": 1.021, "expert_w12_heavy": 1.063}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -55,13 +58,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def layer_work(shape, T, touched_experts, fp8=False):
-    """Algorithmic FLOPs and bytes per stage for T tokens (bf16 = 2 bytes;
-    with fp8, the routed experts' weights, latent codes and activation codes
-    are 1 byte, plus one exponent byte per weight row and token)."""
+def layer_work(shape, T, counts, fp8=False):
+    """Algorithmic FLOPs and bytes per stage for T tokens with per-expert
+    assignment counts `counts` (bf16 = 2 bytes; with fp8, the routed experts'
+    weights, latent codes and activation codes are 1 byte, plus one exponent
+    byte per weight row and token).  The expert W1|W2 GEMM runs as two
+    launches: experts with at most 128 rows ("light") and the others."""
     d, L, E, k, I = shape.d, shape.latent, shape.n_experts, shape.top_k, shape.inter
     S = shape.n_shared * shape.shared_inter
+    counts = np.asarray(counts)
     n = T * k
+    touched = int((counts > 0).sum())
+    light = (counts > 0) & (counts <= 128)
+    heavy = counts > 128
     w = {}
     w["down"] = (2.0 * T * d * L, 2.0 * (T * d + L * d + T * L))
     w["shared"] = (4.0 * T * d * S, 2.0 * (T * d + 2 * S * d + T * S))
@@ -70,12 +79,16 @@ def layer_work(shape, T, touched_experts, fp8=False):
     w["scan"] = (0.0, 8.0 * E * math.ceil(T / 32))
     w["offsets"] = (0.0, 8.0 * E)
     w["scatter"] = (0.0, 16.0 * n)
-    w["expert_w12"] = (4.0 * n * L * I, 2.0 * (touched_experts * 2 * I * L + T * L + n * I))
-    w["expert_w3"] = (2.0 * n * I * L, 2.0 * (touched_experts * L * I + n * I + n * L))
-    if fp8:
-        w["expert_w12"] = (4.0 * n * L * I, touched_experts * 2 * I * (L + 1) + 2.0 * T * L + T * (L + 1) +
-                           T * L + n * I)
-        w["expert_w3"] = (2.0 * n * I * L, touched_experts * L * (I + 1) + n * I + 2.0 * n * L)
+    wb = 1.0 if fp8 else 2.0        # bytes per weight / latent / activation element
+    for name, sel in (("expert_w12_light", light), ("expert_w12_heavy", heavy)):
+        ne, nr = int(sel.sum()), int(counts[sel].sum())
+        # weights of the stage's experts, the latent rows once (the gathered
+        # re-reads of a token's row for its several experts hit L2), act out
+        byts = ne * 2 * I * (L * wb + (1 if fp8 else 0)) + T * L * wb + nr * I * wb
+        w[name] = (4.0 * nr * L * I, byts)
+    if fp8:   # the latent's quantisation runs at the start of the light stage
+        w["expert_w12_light"] = (w["expert_w12_light"][0], w["expert_w12_light"][1] + 2.0 * T * L + T * (L + 1))
+    w["expert_w3"] = (2.0 * n * I * L, touched * L * (I * wb + (1 if fp8 else 0)) + n * I * wb + 2.0 * n * L)
     w["combine"] = (0.0, 2.0 * (n * L + T * L))
     w["up"] = (2.0 * T * (L + S) * d, 2.0 * (T * (L + S) + d * (L + S) + T * d))
     return w
@@ -251,30 +264,35 @@ def fp8_experts_variant(lm, stream, steps, warmup, shape, w, x, bias, dshape, wd
         for _ in range(warmup):
             lm.lmoe_forward(h8, xx, bb, y=y8, workspace=ws8, expert_counts_out=c8, stream=stream)
         torch.cuda.synchronize()
-        touched = int((c8 > 0).sum().item())
+        counts8 = c8.cpu().numpy()
+        touched = int((counts8 > 0).sum())
         n = max(steps, 20)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)] for _ in range(n)]
-        for e_ in evs:
-            for e in e_:
-                e.record(stream)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         t0.record(stream)
         for i in range(n):
-            lm.lmoe_set_stage_events(h8, evs[i])
             lm.lmoe_forward(h8, xx, bb, y=y8, workspace=ws8, expert_counts_out=c8, stream=stream)
         t1.record(stream)
         torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / n
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)] for _ in range(n)]
+        for e_ in evs:
+            for e in e_:
+                e.record(stream)
+        torch.cuda.synchronize()
+        for i in range(n):
+            lm.lmoe_set_stage_events(h8, evs[i])
+            lm.lmoe_forward(h8, xx, bb, y=y8, workspace=ws8, expert_counts_out=c8, stream=stream)
+        torch.cuda.synchronize()
         lm.lmoe_set_stage_events(h8, None)
         assert lm.lmoe_device_status(h8) == 0
-        ms = t0.elapsed_time(t1) / n
         st = {nm: float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in evs])) for j, nm in enumerate(lm.STAGES)}
-        work = layer_work(shp, shp.T, touched, fp8=True)
+        work = layer_work(shp, shp.T, counts8, fp8=True)
         byts = sum(v[1] for v in work.values())
-        r = {"T": shp.T, "ms": round(ms, 4), "tokens_per_s": shp.T / (ms * 1e-3), "touched_experts": touched,
-             "expert_w12_ms": round(st["expert_w12"], 4), "expert_w3_ms": round(st["expert_w3"], 4),
-             "expert_w12_gbs": round(work["expert_w12"][1] / (st["expert_w12"] * 1e-3) / 1e9, 1),
-             "expert_w3_gbs": round(work["expert_w3"][1] / (st["expert_w3"] * 1e-3) / 1e9, 1)}
+        r = {"T": shp.T, "ms": round(ms, 4), "tokens_per_s": shp.T / (ms * 1e-3), "touched_experts": touched}
+        for nm in ("expert_w12_light", "expert_w12_heavy", "expert_w3"):
+            r[nm + "_ms"] = round(st[nm], 4)
+            r[nm + "_gbs"] = round(work[nm][1] / max(st[nm] * 1e-3, 1e-12) / 1e9, 1)
         if name == "decode":
             r["bytes"] = byts
             r["gbs"] = round(byts / (ms * 1e-3) / 1e9, 1)
@@ -331,16 +349,20 @@ def run_profile_case(args):
     sq = synth.qb_scores(262144, 896, device="cuda")
     hq = torch.empty((896, QB_B), dtype=torch.int32, device="cuda")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cnt = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
     for i in range(args.warmup + args.steps):
         if i == args.warmup:
             e0.record()
-        y = lm.lmoe_forward(h, x, bias, workspace=ws, scores_out=scores)
+        y = lm.lmoe_forward(h, x, bias, workspace=ws, scores_out=scores, expert_counts_out=cnt)
         lm.qb_histogram(sq, QB_B, hist=hq)
     e1.record()
     torch.cuda.synchronize()
     assert lm.lmoe_device_status(h) == 0
+    work = layer_work(shape, shape.T, cnt.cpu().numpy(), fp8=bool(args.fp8))
     print(json.dumps({"case": "ncu_case", "T": shape.T, "n_experts": shape.n_experts, "fp8": bool(args.fp8),
                       "ms_per_iter": e0.elapsed_time(e1) / max(args.steps, 1),
+                      "touched_experts": int((cnt > 0).sum().item()),
+                      "algorithmic_bytes": {k: v[1] for k, v in work.items()},
                       "y_finite": bool(torch.isfinite(y.float()).all().item())}), flush=True)
     return 0
 
@@ -402,7 +424,8 @@ def main():
         step(x, bias, y)
     torch.cuda.synchronize()
     assert lm.lmoe_device_status(handle) == 0
-    touched = int((counts > 0).sum().item())
+    counts_host = counts.cpu().numpy()
+    touched = int((counts_host > 0).sum())
 
     # Headline: K steps with nothing between the kernels but the kernels (the
     # library launches them as programmatic dependent launches, so a kernel's
@@ -449,7 +472,7 @@ def main():
     for j, name in enumerate(lm.STAGES):
         stage_ms[name] = float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in ev_sets]))
     stage_ms["qb"] = float(np.mean([a.elapsed_time(b) for a, b in qb_ev]))
-    work = layer_work(shape, T, touched)
+    work = layer_work(shape, T, counts_host)
     stages = {}
     ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     for name in lm.STAGES:
@@ -470,14 +493,14 @@ def main():
     roof.pop("share")
     roof["kernel"] = dom
     roof["per_launch"] = {"flop": dfl, "bytes": dby}
-    # DRAM bytes per launch: ncu on the reduced K3-width case (--profile-case,
-    # where the full workload is too large to capture) measured read+write of
-    # the expert W1|W2 stage's two launches (light + heavy experts) = 1.02 x
-    # its algorithmic bytes; the traffic grows with the weights of the touched
-    # experts, so the full stage's traffic is that ratio times its bytes.
-    roof["traffic"] = round(1.02 * dby) if dom == "expert_w12" else None
+    # DRAM bytes per launch: the K3 launches are too large for an ncu capture,
+    # so ncu measured the same kernels on the reduced K3-width case
+    # (--profile-case); DRAM read+write over the launch's algorithmic bytes
+    # there (same work model, that run's expert counts) gives the ratio below,
+    # and the traffic grows with the touched experts' weights like the bytes.
+    roof["traffic"] = round(TRAFFIC_RATIO[dom] * dby) if dom in TRAFFIC_RATIO else None
     roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum on --profile-case, "
-                              "scaled by algorithmic bytes") if dom == "expert_w12" else None
+                              "ratio to algorithmic bytes scaled to this launch") if dom in TRAFFIC_RATIO else None
     roof["peak_source"] = peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " hbm copy")
 
     total_flop = layer_flops_per_token(shape) * T
@@ -582,7 +605,8 @@ def main():
     for _ in range(args.warmup):
         lm.lmoe_forward(hd, xd, bd, y=yd, workspace=wsd, expert_counts_out=cd, stream=stream)
     torch.cuda.synchronize()
-    touched_d = int((cd > 0).sum().item())
+    counts_d = cd.cpu().numpy()
+    touched_d = int((counts_d > 0).sum())
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     nd = max(20, args.steps)
     d0.record(stream)
@@ -591,7 +615,7 @@ def main():
     d1.record(stream)
     torch.cuda.synchronize()
     dec_ms = d0.elapsed_time(d1) / nd
-    wdec = layer_work(dshape, dshape.T, touched_d)
+    wdec = layer_work(dshape, dshape.T, counts_d)
     dec_bytes = sum(v[1] for v in wdec.values())
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     assert lm.lmoe_device_status(hd) == 0

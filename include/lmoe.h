@@ -213,11 +213,14 @@ typedef enum {
     LMOE_STAGE_SCAN = 4,       /* a4 per-expert counts                             */
     LMOE_STAGE_OFFSETS = 5,    /* a4 offsets and grouped-GEMM tile list            */
     LMOE_STAGE_SCATTER = 6,    /* a4 permutation maps                              */
-    LMOE_STAGE_EXPERT_W12 = 7, /* a5 grouped expert W1|W2 GEMM + SiTU-GLU          */
-    LMOE_STAGE_EXPERT_W3 = 8,  /* a6 grouped expert W3 GEMM + gate scatter         */
-    LMOE_STAGE_COMBINE = 9,    /* a7 aggregation + RMSNorm                         */
-    LMOE_STAGE_UP = 10,        /* a8 up-projection + shared W3 GEMM                */
-    LMOE_NUM_STAGES = 11
+    LMOE_STAGE_EXPERT_W12_LIGHT = 7, /* a5 grouped expert W1|W2 GEMM + SiTU-GLU, experts
+                                      * with at most 128 rows (FP8 variant: after the
+                                      * latent's e4m3 quantisation, also in this stage) */
+    LMOE_STAGE_EXPERT_W12_HEAVY = 8, /* a5 the same for experts with more rows (pair tiles) */
+    LMOE_STAGE_EXPERT_W3 = 9,  /* a6 grouped expert W3 GEMM + gate scatter         */
+    LMOE_STAGE_COMBINE = 10,   /* a7 aggregation + RMSNorm                         */
+    LMOE_STAGE_UP = 11,        /* a8 up-projection + shared W3 GEMM                */
+    LMOE_NUM_STAGES = 12
 } lmoe_stage;
 
 /* Timing hook: with n_events == LMOE_NUM_STAGES + 1 (cudaEvent_t handles

@@ -24,8 +24,8 @@ EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace
             "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_route_static",
             "lmoe_selftest_timeout", "qb_histogram", "qb_quantile_bias", "qb_sign_update")
 
-STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12", "expert_w3",
-          "combine", "up")
+STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12_light",
+          "expert_w12_heavy", "expert_w3", "combine", "up")
 
 
 class LmoeError(RuntimeError):

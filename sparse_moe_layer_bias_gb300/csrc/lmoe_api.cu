@@ -501,7 +501,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
                        stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
-    mark(LMOE_STAGE_EXPERT_W12);
+    mark(LMOE_STAGE_EXPERT_W12_LIGHT);
     {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the rows of each expert's tokens.
         // Experts with more than 128 rows run pair tiles (two 128-row sub-tiles
         // share each weight stage); the others run 128-row tiles whose smaller
@@ -535,6 +535,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a,
                                      grid_for(E * a.n_tiles), stream, /*pair=*/false));
         if (st) return st;
+        mark(LMOE_STAGE_EXPERT_W12_HEAVY);
         a.tiles = tiles2;
         a.n_mtiles = nmt + 1;
         const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;

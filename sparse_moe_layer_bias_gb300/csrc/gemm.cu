@@ -104,15 +104,27 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf
 // 2^-8).  The sigmoid is 1 / (1 + e^-x) from the fast exponential and
 // division, which keeps its relative error small for very negative x, where
 // (1 + tanh(x/2)) / 2 would cancel (relative error growing like e^-x * 2^-11).
-// SiTU(x; b1) * softcap(y; b2) costs two tanh, one exp2 and one reciprocal.
+// SiTU(x; b1) * softcap(y; b2) costs two tanh, one exp2 and one reciprocal;
+// for b1 = 4 one tanh, one exp2 and one reciprocal.
 __device__ __forceinline__ float tanh_fast(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float situ_glu(float p1, float p2, float b1, float ib1, float b2, float ib2) {
-    const float sig = __fdividef(1.0f, 1.0f + __expf(-p1));
-    return (b1 * tanh_fast(p1 * ib1) * sig) * (b2 * tanh_fast(p2 * ib2));
+    float situ;
+    if (b1 == 4.0f) {
+        // beta1 = 4 (K3): with u = e^(-x/2), tanh(x/4) = (1 - u) / (1 + u) and
+        // sigma(x) = 1 / (1 + u^2), so SiTU(x) = 4 (1 - u) / ((1 + u)(1 + u^2)):
+        // one exp2 and one reciprocal.  x is floored at -50, where
+        // |SiTU| < 1e-21 (and (1 + u)(1 + u^2) stays finite).
+        const float u = __expf(-0.5f * fmaxf(p1, -50.0f));
+        situ = 4.0f * __fdividef(1.0f - u, (1.0f + u) * fmaf(u, u, 1.0f));
+    } else {
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-p1));
+        situ = b1 * tanh_fast(p1 * ib1) * sig;
+    }
+    return situ * (b2 * tanh_fast(p2 * ib2));
 }
 
 // 2^k as an fp32 built from the exponent bits, k clamped to the normal range

@@ -1,5 +1,6 @@
-// gemm.cu -- persistent bf16 GEMM on the sm_103a tensor cores (tcgen05),
-// used for every contraction of the Stable LatentMoE layer:
+// gemm.cu -- persistent GEMM on the sm_103a tensor cores (tcgen05; bf16 x bf16,
+// or e4m3 x e4m3 for the FP8 expert variant), used for every contraction of
+// the Stable LatentMoE layer:
 //   a1  h   = x W_down^T                       (A dense, B plain, bf16 out)
 //   a2  s   = sigmoid(h W_router^T)            (A dense, B plain, fp32 out)
 //   a5  act = SiTU(h W1^T) * softcap(h W2^T)   (A = h rows of the expert's
@@ -10,7 +11,10 @@
 //   a8  y   = r W_up^T + shared_act Ws3^T       (K split over two A/B sources)
 //   a8' shared_act = SiTU(x Ws1^T) * softcap(x Ws2^T)
 // (SiTU-GLU: "Kimi-K3-Architecture-Deep-Dive" section 1; the layer's chain of
-// projections: same page, section 2.)
+// projections: same page, section 2.)  In the FP8 variant a5 and a6 take e4m3
+// operands (kind::f8f6f4, a K block of 128 elements = the same 128-byte rows)
+// and their epilogues apply the power-of-two row scales: a5 writes e4m3(4 act),
+// a6 undoes the 4 with the W3 row scale and the gate.
 //
 // Structure (one CTA per SM, 192 threads; 320 with the A gather):
 //   warp 0      TMA producer: per 64-wide K block, one box of A and one or two
@@ -27,6 +31,8 @@
 //               accumulator so the next tile's MMAs overlap this epilogue;
 //   warps 6..9  (gather mode only) copy the A rows named by a row list into
 //               the stage with cp.async.
+// All threads pass griddepcontrol.wait after the prologue (barrier init, TMEM
+// allocation), so the kernel can be a programmatic dependent launch.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 

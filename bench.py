@@ -213,6 +213,15 @@ def host_weights_bits(w):
 
 
 # ----------------------------------------------------------------------------- reference arm
+def bench_config(world):
+    """The workload both arms report (the reference arm adds its sample size)."""
+    return {"workload": "k3_prefill: Stable LatentMoE layer forward T=8192, d=7168, latent=3584, "
+                        "E=896, top-16, I=512, 2 shared experts x 1024 + QB histogram B=1000 + "
+                        "quantile bias",
+            "T": synth.K3_PREFILL.T, "l2": "inputs larger than L2 (10.3 GB of weights streamed per step)",
+            "parallelism": f"dp{world} (QB histograms all-reduced)" if world > 1 else "dp1"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
@@ -239,8 +248,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "k3_prefill layer forward (T=8192, d=7168, latent=3584, E=896, k=16, "
-                                   "I=512, 2x1024 shared)", "sample_tokens_per_step": per_step},
+            "config": dict(bench_config(world), sample_tokens_per_step=per_step),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
                              "kind": "oracle",
                              "sample": f"{per_step} tokens of the K3 prefill batch per step (fp64 C oracle, OpenMP)"},
@@ -641,11 +649,7 @@ def main():
         "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "k3_prefill: Stable LatentMoE layer forward T=8192, d=7168, latent=3584, "
-                               "E=896, top-16, I=512, 2 shared experts x 1024 + QB histogram B=1000 + "
-                               "quantile bias",
-                   "T": T, "l2": "inputs larger than L2 (10.3 GB of weights streamed per step)",
-                   "parallelism": f"dp{world} (QB histograms all-reduced)" if world > 1 else "dp1"},
+        "config": bench_config(world),
         "layer_tflops": round(tflops, 2),
         "frac_bf16_peak": round(tflops / peaks["bf16_tflops"], 4),
         "roofline": roof,

@@ -596,7 +596,6 @@ cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStrea
 
 }  // namespace
 
-size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256, false>::kSmem : Cfg<128, false>::kSmem; }
 
 #define LMOE_GEMM_CASE(BN_, AM_, BM_, EPI_, G_)                                   \
     if (bn == BN_ && am == AM_ && bm == BM_ && epi == EPI_ && grouped == G_)       \

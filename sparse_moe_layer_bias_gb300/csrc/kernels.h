@@ -102,7 +102,6 @@ struct GemmArgs {
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false,
                         bool dependent = true);
-size_t gemm_smem_bytes(int bn);
 
 // Repack per-expert weights [E][R][K] (row-major bf16) into tile-contiguous
 // order [E][R/TR][K/64][TR][64] so that one TMA box of TR rows x 64 columns is

@@ -24,7 +24,8 @@ def hist_np(h: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("T,E,B", [(65536, 896, 1000), (4096, 128, 1000), (4099, 896, 10000),
-                                   (1000, 40, 37), (1, 896, 1000)])
+                                   (1000, 40, 37), (1, 896, 1000),
+                                   (3000, 24, 60000)])   # bins beyond shared memory: global counters
 def test_histogram_bit_exact(lm, T, E, B):
     s = synth.qb_scores(T, E, seed=T + E + B)
     s[0, 0] = 1.0

@@ -235,7 +235,7 @@ def run_reference(args, world, rank):
     torch.cuda.empty_cache()
     xb = synth.bits(x)
     b = bias.cpu().numpy()
-    per_step = 8
+    per_step = max(16, oracle.num_threads())   # one token per host core: the oracle parallelises over tokens
     for i in range(args.warmup):
         oracle_tokens_per_s(shape, wb, xb[i * per_step:], b, per_step)
     t0 = time.perf_counter()

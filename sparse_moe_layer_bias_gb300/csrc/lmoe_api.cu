@@ -34,6 +34,10 @@ struct lmoe_handle {
     cudaStream_t io_in, io_out;
     cudaEvent_t ev_in[2], ev_fwd[2], ev_out[2];
     unsigned io_calls;
+    // The shared experts depend only on x: without the timing hook they run on
+    // this side stream, concurrently with the routing kernels.
+    cudaStream_t side;
+    cudaEvent_t ev_fork, ev_join;
 };
 
 namespace {
@@ -217,6 +221,9 @@ bool quantize_pack(const uint16_t *src, uint64_t E, uint64_t R, uint64_t K, int 
 }
 
 void release_streams(lmoe_handle *h) {
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     if (h->io_in) cudaStreamDestroy(h->io_in);
     if (h->io_out) cudaStreamDestroy(h->io_out);
     for (int s = 0; s < 2; ++s) {
@@ -317,7 +324,10 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
         return LMOE_ERR_CUDA;
     }
     bool io_ok = cudaStreamCreateWithFlags(&h->io_in, cudaStreamNonBlocking) == cudaSuccess &&
-                 cudaStreamCreateWithFlags(&h->io_out, cudaStreamNonBlocking) == cudaSuccess;
+                 cudaStreamCreateWithFlags(&h->io_out, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess;
     for (int s = 0; s < 2 && io_ok; ++s)
         io_ok = cudaEventCreateWithFlags(&h->ev_in[s], cudaEventDisableTiming) == cudaSuccess &&
                 cudaEventCreateWithFlags(&h->ev_fwd[s], cudaEventDisableTiming) == cudaSuccess &&
@@ -455,8 +465,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     if (c.norm_after_down &&   // ablation variant: hn = h / sqrt(mean(h^2) + eps), per token
         launch_rms_rows(hbuf, T, static_cast<int>(L), static_cast<double>(c.rms_eps), hlat, stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
-    mark(LMOE_STAGE_SHARED);
-    {   // a8': shared experts, act_s = SiTU(x Ws1^T) * softcap(x Ws2^T)
+    // a8': shared experts, act_s = SiTU(x Ws1^T) * softcap(x Ws2^T)
+    auto run_shared = [&](cudaStream_t s_) {
         GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
@@ -466,12 +476,11 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = sact;
         a.ld_out = S;
         a.out_cols = static_cast<int32_t>(S);
-        st = gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
-        if (st) return st;
-    }
-    mark(LMOE_STAGE_ROUTER);
-    {   // a2: s = sigmoid(h W_router^T), fp32
+        return gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
+                                       grid_for(int64_t(m_tiles) * a.n_tiles), s_));
+    };
+    // a2: s = sigmoid(h W_router^T), fp32
+    auto run_router = [&]() {
         GemmMaps m{m_h, m_h, h->m_wrouter, h->m_wrouter};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
@@ -481,8 +490,30 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = scores;
         a.ld_out = E;
         a.out_cols = static_cast<int32_t>(E);
-        st = gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        return gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
+                                       grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+    };
+    // Without the timing hook the shared experts run on the side stream once
+    // the router is done, while the routing kernels (small and latency-bound)
+    // run here on the same SMs; the join comes before the routed experts'
+    // GEMMs, which need every SM.  With the hook, the stages run in stream
+    // order so that each stage's events bracket it alone.
+    const bool overlap = (h->stage_events == nullptr);
+    if (overlap) {
+        st = run_router();
+        if (st) return st;
+        if (cudaEventRecord(h->ev_fork, stream) != cudaSuccess ||
+            cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
+            return LMOE_ERR_CUDA;
+        st = run_shared(h->side);
+        if (st) return st;
+        if (cudaEventRecord(h->ev_join, h->side) != cudaSuccess) return LMOE_ERR_CUDA;
+    } else {
+        mark(LMOE_STAGE_SHARED);
+        st = run_shared(stream);
+        if (st) return st;
+        mark(LMOE_STAGE_ROUTER);
+        st = run_router();
         if (st) return st;
     }
     // a3 + a4: biased top-k, then the stable grouping of assignments by expert
@@ -501,6 +532,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
                        stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
+    if (overlap && cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_EXPERT_W12_LIGHT);
     {   // a5: act = SiTU(W1[e] h) * softcap(W2[e] h) over the rows of each expert's tokens.
         // Experts with more than 128 rows run pair tiles (two 128-row sub-tiles

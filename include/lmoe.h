@@ -165,7 +165,11 @@ int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *
  * scores_out [T][n_experts] fp32, topk_idx_out [T][top_k] int32, gates_out
  * [T][top_k] fp32, expert_counts_out [n_experts] int32.  workspace: at least
  * lmoe_workspace_size(T) bytes, 256-byte aligned.  T = 0 enqueues nothing.
- * A handle may be used from one stream at a time per workspace. */
+ * A handle may be used from one stream at a time per workspace.  Unless the
+ * timing hook (lmoe_set_stage_events) is set, the shared experts' GEMM runs on
+ * a side stream of the handle, ordered after the work already in `stream`
+ * and joined back into `stream` before the routed experts, so everything the
+ * call enqueues is ordered within `stream` as seen from outside. */
 int lmoe_forward(lmoe_handle *handle, const uint16_t *x, int64_t T, const float *bias,
                  uint16_t *y, float *scores_out, int32_t *topk_idx_out, float *gates_out,
                  int32_t *expert_counts_out, void *workspace, size_t workspace_bytes,

@@ -96,6 +96,10 @@ def _load():
             "orc_fp8_exp_for": (_I32, [ctypes.c_double]),
             "orc_fp8_quantize_rows": (None, [_P, _I64, _I64, _P, _P]),
             "orc_routed_fp8": (None, [cfg, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+            "orc_softcap_grad": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
+            "orc_situ_grad": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
+            "orc_backward": (None, [cfg, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
+                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
             "orc_num_threads": (ctypes.c_int, []),
         }
         for name, (res, args) in sig.items():
@@ -147,6 +151,14 @@ def softcap(x: float, beta: float) -> float:
 
 def situ(x: float, beta: float) -> float:
     return _load().orc_situ(float(x), float(beta))
+
+
+def softcap_grad(x: float, beta: float) -> float:
+    return _load().orc_softcap_grad(float(x), float(beta))
+
+
+def situ_grad(x: float, beta: float) -> float:
+    return _load().orc_situ_grad(float(x), float(beta))
 
 
 def num_threads() -> int:
@@ -374,6 +386,50 @@ def layer_forward(cfg: LayerConfig, x, w, bias):
     return {"h_raw": h_raw, "h": h, "s": s, "idx": idx, "gate": gate, "margin": margin, "counts": counts,
             "offsets": offsets, "perm": perm, "inv": inv, "z": rt["z"], "r": rt["r"],
             "r64": rt["r64"], "a_s": a_s, "y": y}
+
+
+# ---------------------------------------------------------------- backward
+BACKWARD_GRADS = ("w_down", "w_router", "w1", "w2", "w3", "ws1", "ws2", "ws3", "w_up")
+
+
+def layer_backward(cfg: LayerConfig, x, w, idx, dy, round_mode: int = 1, weight_grads: bool = True):
+    """Gradient of the layer for the upstream gradient ``dy`` (bf16 bits
+    [T, d]) with the routing ``idx`` ([T, k] int32, from the forward) held
+    fixed.  ``round_mode`` 1 takes the gradient at the forward's bf16 / fp32
+    roundings (each passing the gradient through); 0 is the smooth, unrounded
+    function.  Returns fp64 arrays: "x" [T, d] and, with ``weight_grads``, one
+    per weight name in ``BACKWARD_GRADS`` shaped like that weight (w1/w2/w3
+    must then be full [E, ...] arrays)."""
+    if cfg.norm_after_down or cfg.expert_fp8:
+        raise ValueError("the backward covers the layer without the variant flags")
+    T = x.shape[0]
+    E, L, I, d = cfg.n_experts, cfg.latent, cfg.inter, cfg.d
+    S = cfg.n_shared * cfg.shared_inter
+    x = _need(x, np.uint16, (T, d))
+    dy = _need(dy, np.uint16, (T, d))
+    idx = _need(idx, np.int32, (T, cfg.top_k))
+    if T > 0 and (idx.min() < 0 or idx.max() >= E):
+        raise ValueError("expert index out of range")
+    dense = {k: _need(w[k], np.uint16) for k in ("w_down", "w_router", "ws1", "ws2", "ws3", "w_up")}
+    p1, k1 = _expert_ptrs(w["w1"], E, (I, L))
+    p2, k2 = _expert_ptrs(w["w2"], E, (I, L))
+    p3, k3 = _expert_ptrs(w["w3"], E, (L, I))
+    for e in np.unique(idx):
+        if not (p1[e] and p2[e] and p3[e]):
+            raise ValueError(f"weights of expert {e} were not supplied")
+    shapes = {"w_down": (L, d), "w_router": (E, L), "w1": (E, I, L), "w2": (E, I, L),
+              "w3": (E, L, I), "ws1": (S, d), "ws2": (S, d), "ws3": (d, S), "w_up": (d, L)}
+    out = {"x": np.empty((T, d), np.float64)}
+    if weight_grads:
+        for k in BACKWARD_GRADS:
+            out[k] = np.empty(shapes[k], np.float64)
+    g = [_ptr(out.get(k)) for k in BACKWARD_GRADS]
+    c = cfg.c()
+    _load().orc_backward(ctypes.byref(c), T, _ptr(x), _ptr(idx), _ptr(dy), _ptr(dense["w_down"]),
+                         _ptr(dense["w_router"]), p1, p2, p3, _ptr(dense["ws1"]), _ptr(dense["ws2"]),
+                         _ptr(dense["ws3"]), _ptr(dense["w_up"]), int(round_mode), _ptr(out["x"]), *g)
+    del k1, k2, k3
+    return out
 
 
 # ---------------------------------------------------------------- QB

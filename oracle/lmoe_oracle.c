@@ -1,6 +1,7 @@
 /*
  * lmoe_oracle.c -- plain, slow, fp64 CPU oracle for the Stable LatentMoE layer
- * forward pass and its Quantile Balancing (QB) histogram / quantile read.
+ * forward pass, its backward pass and its Quantile Balancing (QB) histogram /
+ * quantile read.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
  * this file; only the tests, the smoke check and the benchmark's CPU-baseline
@@ -651,6 +652,302 @@ void orc_sign_update(const int32_t *counts, int32_t E, float gamma, float *bias)
         else if (scaled > total)
             bias[e] = bias[e] - gamma;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass of the layer                                                */
+/* ------------------------------------------------------------------------ */
+
+/* [DD] section 1: the tanh softcap is continuous and differentiable everywhere:
+ *   d/dx softcap(x; beta) = 1 - tanh(x / beta)^2
+ *   d/dx SiTU(x; beta)    = softcap'(x) sigma(x) + softcap(x) sigma(x) (1 - sigma(x)) */
+double orc_softcap_grad(double x, double beta)
+{
+    double t = tanh(x / beta);
+    return 1.0 - t * t;
+}
+
+double orc_situ_grad(double x, double beta)
+{
+    double s = orc_sigmoid(x);
+    return orc_softcap_grad(x, beta) * s + orc_softcap(x, beta) * s * (1.0 - s);
+}
+
+static double dot_bf16_f64(const uint16_t *w, const double *v, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        acc += orc_bf16_to_f64(w[i]) * v[i];
+    return acc;
+}
+
+static double keep(double v, int round_mode)
+{
+    return round_mode ? orc_bf16_to_f64(orc_f64_to_bf16(v)) : v;
+}
+
+/* Gradient of the layer y(x) (the forward above) for an upstream gradient dy,
+ * with the forward's routing idx held fixed: the top-k choice has no
+ * gradient; the router's gradient flows through the gates
+ * g_j = sigma(w_router[e_j] . h).  The selection bias never enters y.
+ *
+ * round_mode 1: the forward's roundings (h, act, r and the shared activation
+ * in bf16, the gates in fp32) are applied to the values the gradient is taken
+ * at, and each rounding passes the gradient through unchanged.  round_mode 0:
+ * no rounding anywhere -- the gradient of the smooth function, which
+ * finite differences can check.
+ *
+ * Per token (tokens are independent):
+ *   dr  = W_up^T dy                 das  = Ws3^T dy
+ *   dps1 = das SiTU'(ps1) softcap(ps2)   dps2 = das SiTU(ps1) softcap'(ps2)
+ *   RMSNorm r = z / sqrt(ms + eps), ms = mean(z^2):
+ *   dz  = dr / sqrt(ms + eps) - z (dr . z) / (L (ms + eps)^(3/2))
+ *   per chosen expert j (e = idx, o_j = W3[e] act_j, the gate not applied):
+ *     dg_j = o_j . dz      do_j = g_j dz      dact_j = W3[e]^T do_j
+ *     dp1_j = dact_j SiTU'(p1_j) softcap(p2_j)
+ *     dp2_j = dact_j SiTU(p1_j) softcap'(p2_j)
+ *     dlogit_j = dg_j sigma'(logit_j)
+ *     dh += W1[e]^T dp1_j + W2[e]^T dp2_j + w_router[e] dlogit_j
+ *   dx  = W_down^T dh + Ws1^T dps1 + Ws2^T dps2
+ * Weights (sums over tokens in ascending order, over an expert's assignments
+ * in ascending assignment order):
+ *   dW_up = sum dy r^T  ([DD] section 2, effect 6: the gradient of the
+ *           projection after the norm is the outer product with the
+ *           normalised latent)
+ *   dWs3 = sum dy as^T, dWs1 = sum dps1 x^T, dWs2 = sum dps2 x^T,
+ *   dW_down = sum dh x^T, dW_router[e] = sum dlogit h^T,
+ *   dW3[e] = sum do act^T, dW1[e] = sum dp1 h^T, dW2[e] = sum dp2 h^T.
+ * Layouts as the weights: dw_down [L][d], dw_router [E][L], dw1/dw2 [E][I][L],
+ * dw3 [E][L][I], dws1/dws2 [S][d], dws3 [d][S], dw_up [d][L]; dx [T][d].
+ * Every output is nullable (a NULL weight gradient skips its sum).  w1, w2,
+ * w3 are per-expert pointers as in orc_routed. */
+void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32_t *idx,
+                  const uint16_t *dy, const uint16_t *w_down, const uint16_t *w_router,
+                  const uint16_t *const *w1, const uint16_t *const *w2, const uint16_t *const *w3,
+                  const uint16_t *ws1, const uint16_t *ws2, const uint16_t *ws3,
+                  const uint16_t *w_up, int round_mode, double *dx, double *dw_down,
+                  double *dw_router, double *dw1, double *dw2, double *dw3, double *dws1,
+                  double *dws2, double *dws3, double *dw_up)
+{
+    const int64_t d = c->d, L = c->latent, E = c->n_experts, K = c->top_k, I = c->inter;
+    const int64_t S = (int64_t)c->n_shared * c->shared_inter;
+    const int64_t n = T * K;
+    const double b1 = c->beta1, b2 = c->beta2;
+    /* values kept per token / per assignment for the weight sums */
+    double *hv = (double *)malloc((size_t)(T * L) * sizeof(double));
+    double *rv = (double *)malloc((size_t)(T * L) * sizeof(double));
+    double *asv = (double *)malloc((size_t)(T * S) * sizeof(double));
+    double *dps1v = (double *)malloc((size_t)(T * S) * sizeof(double));
+    double *dps2v = (double *)malloc((size_t)(T * S) * sizeof(double));
+    double *dhv = (double *)malloc((size_t)(T * L) * sizeof(double));
+    double *dlgv = (double *)malloc((size_t)n * sizeof(double));
+    double *dov = (double *)malloc((size_t)(n * L) * sizeof(double));
+    double *actv = (double *)malloc((size_t)(n * I) * sizeof(double));
+    double *dp1v = (double *)malloc((size_t)(n * I) * sizeof(double));
+    double *dp2v = (double *)malloc((size_t)(n * I) * sizeof(double));
+
+#pragma omp parallel
+    {
+        double *xd = (double *)malloc((size_t)d * sizeof(double));
+        double *dyd = (double *)malloc((size_t)d * sizeof(double));
+        double *ps1 = (double *)malloc((size_t)S * sizeof(double));
+        double *ps2 = (double *)malloc((size_t)S * sizeof(double));
+        double *p1 = (double *)malloc((size_t)(K * I) * sizeof(double));
+        double *p2 = (double *)malloc((size_t)(K * I) * sizeof(double));
+        double *o = (double *)malloc((size_t)(K * L) * sizeof(double));
+        double *g = (double *)malloc((size_t)K * sizeof(double));
+        double *dsig = (double *)malloc((size_t)K * sizeof(double));
+        double *z = (double *)malloc((size_t)L * sizeof(double));
+        double *dr = (double *)malloc((size_t)L * sizeof(double));
+        double *dz = (double *)malloc((size_t)L * sizeof(double));
+        double *das = (double *)malloc((size_t)S * sizeof(double));
+        double *dact = (double *)malloc((size_t)I * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            double *h = hv + t * L, *dh = dhv + t * L;
+            for (int64_t q = 0; q < d; ++q) {
+                xd[q] = orc_bf16_to_f64(x[t * d + q]);
+                dyd[q] = orc_bf16_to_f64(dy[t * d + q]);
+            }
+            /* forward values */
+            for (int64_t l = 0; l < L; ++l)
+                h[l] = keep(dot_bf16_f64(w_down + l * d, xd, d), round_mode);
+            for (int64_t i = 0; i < S; ++i) {
+                ps1[i] = dot_bf16_f64(ws1 + i * d, xd, d);
+                ps2[i] = dot_bf16_f64(ws2 + i * d, xd, d);
+                asv[t * S + i] = keep(orc_situ(ps1[i], b1) * orc_softcap(ps2[i], b2), round_mode);
+            }
+            for (int64_t l = 0; l < L; ++l)
+                z[l] = 0.0;
+            for (int64_t j = 0; j < K; ++j) {
+                const int64_t a = t * K + j;
+                const int32_t e = idx[a];
+                const double sig = orc_sigmoid(dot_bf16_f64(w_router + (int64_t)e * L, h, L));
+                g[j] = round_mode ? (double)(float)sig : sig;
+                dsig[j] = sig * (1.0 - sig);
+                for (int64_t i = 0; i < I; ++i) {
+                    p1[j * I + i] = dot_bf16_f64(w1[e] + i * L, h, L);
+                    p2[j * I + i] = dot_bf16_f64(w2[e] + i * L, h, L);
+                    actv[a * I + i] = keep(orc_situ(p1[j * I + i], b1) * orc_softcap(p2[j * I + i], b2),
+                                           round_mode);
+                }
+                for (int64_t l = 0; l < L; ++l) {
+                    o[j * L + l] = dot_bf16_f64(w3[e] + l * I, actv + a * I, I);
+                    z[l] += g[j] * o[j * L + l];
+                }
+            }
+            double ms = 0.0;
+            for (int64_t l = 0; l < L; ++l)
+                ms += z[l] * z[l];
+            const double den = ms / (double)L + c->rms_eps;
+            const double inv = 1.0 / sqrt(den);
+            for (int64_t l = 0; l < L; ++l)
+                rv[t * L + l] = keep(z[l] * inv, round_mode);
+            /* up-projection and shared experts */
+            for (int64_t l = 0; l < L; ++l)
+                dr[l] = 0.0;
+            for (int64_t i = 0; i < S; ++i)
+                das[i] = 0.0;
+            for (int64_t m = 0; m < d; ++m) {
+                for (int64_t l = 0; l < L; ++l)
+                    dr[l] += orc_bf16_to_f64(w_up[m * L + l]) * dyd[m];
+                for (int64_t i = 0; i < S; ++i)
+                    das[i] += orc_bf16_to_f64(ws3[m * S + i]) * dyd[m];
+            }
+            for (int64_t i = 0; i < S; ++i) {
+                dps1v[t * S + i] = das[i] * orc_situ_grad(ps1[i], b1) * orc_softcap(ps2[i], b2);
+                dps2v[t * S + i] = das[i] * orc_situ(ps1[i], b1) * orc_softcap_grad(ps2[i], b2);
+            }
+            /* RMSNorm */
+            double drz = 0.0;
+            for (int64_t l = 0; l < L; ++l)
+                drz += dr[l] * z[l];
+            for (int64_t l = 0; l < L; ++l)
+                dz[l] = dr[l] * inv - z[l] * drz * inv / ((double)L * den);
+            /* routed experts, gates and router */
+            for (int64_t l = 0; l < L; ++l)
+                dh[l] = 0.0;
+            for (int64_t j = 0; j < K; ++j) {
+                const int64_t a = t * K + j;
+                const int32_t e = idx[a];
+                double dg = 0.0;
+                for (int64_t l = 0; l < L; ++l) {
+                    dg += o[j * L + l] * dz[l];
+                    dov[a * L + l] = g[j] * dz[l];
+                }
+                for (int64_t i = 0; i < I; ++i)
+                    dact[i] = 0.0;
+                for (int64_t l = 0; l < L; ++l) {
+                    const uint16_t *w3row = w3[e] + l * I;
+                    for (int64_t i = 0; i < I; ++i)
+                        dact[i] += orc_bf16_to_f64(w3row[i]) * dov[a * L + l];
+                }
+                for (int64_t i = 0; i < I; ++i) {
+                    const double x1 = p1[j * I + i], x2 = p2[j * I + i];
+                    const double d1 = dact[i] * orc_situ_grad(x1, b1) * orc_softcap(x2, b2);
+                    const double d2 = dact[i] * orc_situ(x1, b1) * orc_softcap_grad(x2, b2);
+                    dp1v[a * I + i] = d1;
+                    dp2v[a * I + i] = d2;
+                    const uint16_t *r1 = w1[e] + i * L, *r2 = w2[e] + i * L;
+                    for (int64_t l = 0; l < L; ++l)
+                        dh[l] += orc_bf16_to_f64(r1[l]) * d1 + orc_bf16_to_f64(r2[l]) * d2;
+                }
+                dlgv[a] = dg * dsig[j];
+                for (int64_t l = 0; l < L; ++l)
+                    dh[l] += orc_bf16_to_f64(w_router[(int64_t)e * L + l]) * dlgv[a];
+            }
+            /* down-projection and the shared experts' input side */
+            if (dx) {
+                double *dxt = dx + t * d;
+                for (int64_t q = 0; q < d; ++q)
+                    dxt[q] = 0.0;
+                for (int64_t l = 0; l < L; ++l)
+                    for (int64_t q = 0; q < d; ++q)
+                        dxt[q] += orc_bf16_to_f64(w_down[l * d + q]) * dh[l];
+                for (int64_t i = 0; i < S; ++i)
+                    for (int64_t q = 0; q < d; ++q)
+                        dxt[q] += orc_bf16_to_f64(ws1[i * d + q]) * dps1v[t * S + i] +
+                                  orc_bf16_to_f64(ws2[i * d + q]) * dps2v[t * S + i];
+            }
+        }
+        free(xd); free(dyd); free(ps1); free(ps2); free(p1); free(p2); free(o); free(g);
+        free(dsig); free(z); free(dr); free(dz); free(das); free(dact);
+    }
+
+    /* weight gradients: one output row per iteration, tokens in order */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < d; ++m) {
+        if (dw_up)
+            for (int64_t l = 0; l < L; ++l)
+                dw_up[m * L + l] = 0.0;
+        if (dws3)
+            for (int64_t i = 0; i < S; ++i)
+                dws3[m * S + i] = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            const double gm = orc_bf16_to_f64(dy[t * d + m]);
+            if (dw_up)
+                for (int64_t l = 0; l < L; ++l)
+                    dw_up[m * L + l] += gm * rv[t * L + l];
+            if (dws3)
+                for (int64_t i = 0; i < S; ++i)
+                    dws3[m * S + i] += gm * asv[t * S + i];
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < S; ++i) {
+        for (int64_t q = 0; q < d; ++q) {
+            if (dws1) dws1[i * d + q] = 0.0;
+            if (dws2) dws2[i * d + q] = 0.0;
+        }
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t q = 0; q < d; ++q) {
+                const double xv = orc_bf16_to_f64(x[t * d + q]);
+                if (dws1) dws1[i * d + q] += dps1v[t * S + i] * xv;
+                if (dws2) dws2[i * d + q] += dps2v[t * S + i] * xv;
+            }
+    }
+    if (dw_down) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t l = 0; l < L; ++l) {
+            for (int64_t q = 0; q < d; ++q)
+                dw_down[l * d + q] = 0.0;
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t q = 0; q < d; ++q)
+                    dw_down[l * d + q] += dhv[t * L + l] * orc_bf16_to_f64(x[t * d + q]);
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t e = 0; e < E; ++e) {
+        if (dw_router)
+            for (int64_t l = 0; l < L; ++l)
+                dw_router[e * L + l] = 0.0;
+        if (dw3)
+            for (int64_t q = 0; q < L * I; ++q)
+                dw3[e * L * I + q] = 0.0;
+        for (int64_t q = 0; q < I * L; ++q) {
+            if (dw1) dw1[e * I * L + q] = 0.0;
+            if (dw2) dw2[e * I * L + q] = 0.0;
+        }
+        for (int64_t a = 0; a < n; ++a) {
+            if (idx[a] != e)
+                continue;
+            const double *h = hv + (a / K) * L;
+            if (dw_router)
+                for (int64_t l = 0; l < L; ++l)
+                    dw_router[e * L + l] += dlgv[a] * h[l];
+            if (dw3)
+                for (int64_t l = 0; l < L; ++l)
+                    for (int64_t i = 0; i < I; ++i)
+                        dw3[(e * L + l) * I + i] += dov[a * L + l] * actv[a * I + i];
+            for (int64_t i = 0; i < I; ++i)
+                for (int64_t l = 0; l < L; ++l) {
+                    if (dw1) dw1[(e * I + i) * L + l] += dp1v[a * I + i] * h[l];
+                    if (dw2) dw2[(e * I + i) * L + l] += dp2v[a * I + i] * h[l];
+                }
+        }
+    }
+    free(hv); free(rv); free(asv); free(dps1v); free(dps2v); free(dhv); free(dlgv); free(dov);
+    free(actv); free(dp1v); free(dp2v);
 }
 
 /* Number of OpenMP threads the oracle will use (1 without OpenMP). */

@@ -1,6 +1,6 @@
 /*
- * lmoe.h -- C ABI of the GB300 (sm_103a) Stable LatentMoE layer forward and
- * Quantile Balancing (QB) library, liblmoe.so.
+ * lmoe.h -- C ABI of the GB300 (sm_103a) Stable LatentMoE layer (forward and
+ * backward) and Quantile Balancing (QB) library, liblmoe.so.
  *
  * The operations follow three public write-ups of Kimi K3's architecture:
  *   [DD] "Kimi-K3-Architecture-Deep-Dive": section 1 (SiTU-GLU), section 2
@@ -86,6 +86,11 @@ typedef struct {
                            * 128 == 0.  Codes round to nearest even and saturate
                            * at 448; a row's scale is the smallest 2^e with
                            * max|row| <= 448 * 2^e. */
+    int32_t with_backward; /* 1: lmoe_create also keeps transposed copies of
+                           * every weight (about as much device memory again as
+                           * the weights) so that lmoe_backward can run; 0: the
+                           * handle serves forwards only.  The backward covers
+                           * K3's layer: norm_after_down = expert_fp8 = 0. */
 } lmoe_config;
 
 /* Weight pointers (device, bf16, row-major, K-major rows as "out x in").
@@ -233,6 +238,62 @@ typedef enum {
  * events = NULL (n_events = 0) turns it off.  The handle keeps the array
  * pointer: it must stay valid while set. */
 int lmoe_set_stage_events(lmoe_handle *handle, cudaEvent_t *events, int n_events);
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Weight gradients (device fp32, each laid out like its weight in
+ * lmoe_weights; all required, 16-byte aligned).  lmoe_backward overwrites
+ * them (no accumulation). */
+typedef struct {
+    float *w_down;   /* [latent][d]                  */
+    float *w_router; /* [n_experts][latent]          */
+    float *w1;       /* [n_experts][inter][latent]   */
+    float *w2;       /* [n_experts][inter][latent]   */
+    float *w3;       /* [n_experts][latent][inter]   */
+    float *ws1;      /* [S][d]                       */
+    float *ws2;      /* [S][d]                       */
+    float *ws3;      /* [d][S]                       */
+    float *w_up;     /* [d][latent]                  */
+} lmoe_grads;
+
+/* Bytes of device workspace lmoe_backward needs for T tokens (separate from
+ * the forward's workspace, which it reads). */
+int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *bytes);
+
+/* Gradient of the layer ("Kimi-K3-Architecture-Deep-Dive" sections 1 and 2):
+ * given dy = dL/dy [T][d] bf16 for the forward lmoe_forward ran on x [T][d]
+ * with this handle, computes dx [T][d] bf16 and the fp32 weight gradients.
+ * The forward's routing is held fixed: the top-k choice has no gradient; the
+ * router's gradient flows through the gates (gate = sigmoid(w_router[e] . h)).
+ * The selection bias gets none.  The bf16 roundings of the forward pass the
+ * gradient through unchanged.  Per token:
+ *   dr  = W_up^T dy,  da_s = Ws3^T dy  (shared experts: SiTU-GLU backward on
+ *         the recomputed Ws1 x, Ws2 x)
+ *   dz  = RMSNorm backward of dr at z = sum of the forward's rows o
+ *   per chosen expert: u = W3[e]^T dz; da = gate * u; dgate = u . act;
+ *         dp1, dp2 = SiTU-GLU backward on the recomputed W1[e] h, W2[e] h;
+ *         dh += W1[e]^T dp1 + W2[e]^T dp2 + w_router[e] dgate s (1 - s)
+ *   dx  = W_down^T dh + Ws1^T dp_s1 + Ws2^T dp_s2
+ * and the weight gradients are the sums over tokens of the matching outer
+ * products (dW_up = sum dy r^T, ..., dW3[e] = sum over e's assignments of
+ * gate dz act^T, dW1[e] = sum dp1 h^T).
+ * The forward's intermediates are read from fwd_workspace (the workspace of
+ * that forward, unchanged since; its layout for T): h, perm, inv, the
+ * permuted activations, the rows o, r, the shared activations and the tile
+ * lists.  topk_idx, gates, expert_counts: the forward's outputs when the
+ * caller had it write them to its own buffers, or NULL for the workspace's
+ * copies.  The router's logits of the chosen experts are recomputed from h,
+ * so that sigma'(logit) = sigma(logit) sigma(-logit) stays accurate where the
+ * fp32 score has rounded to 1.  workspace: lmoe_backward_workspace_size(T) bytes,
+ * 256-byte aligned.  The handle must have been created with with_backward =
+ * 1 (else LMOE_ERR_INVALID_ARG).  T = 0 enqueues nothing. */
+int lmoe_backward(lmoe_handle *handle, const uint16_t *x, int64_t T, const uint16_t *dy,
+                  const int32_t *topk_idx, const float *gates, const int32_t *expert_counts,
+                  const void *fwd_workspace, size_t fwd_workspace_bytes,
+                  uint16_t *dx, const lmoe_grads *grads, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
 
 /* Routing without caller scratch: the biased top-k (a3) and the stable
  * grouping of assignments by expert (a4) of lmoe_forward, for callers that

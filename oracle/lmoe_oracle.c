@@ -706,7 +706,7 @@ static double keep(double v, int round_mode)
  *     dg_j = o_j . dz      do_j = g_j dz      dact_j = W3[e]^T do_j
  *     dp1_j = dact_j SiTU'(p1_j) softcap(p2_j)
  *     dp2_j = dact_j SiTU(p1_j) softcap'(p2_j)
- *     dlogit_j = dg_j sigma'(logit_j)
+ *     dlogit_j = dg_j sigma'(logit_j),  sigma'(x) = sigma(x) sigma(-x)
  *     dh += W1[e]^T dp1_j + W2[e]^T dp2_j + w_router[e] dlogit_j
  *   dx  = W_down^T dh + Ws1^T dps1 + Ws2^T dps2
  * Weights (sums over tokens in ascending order, over an expert's assignments
@@ -782,9 +782,12 @@ void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32
             for (int64_t j = 0; j < K; ++j) {
                 const int64_t a = t * K + j;
                 const int32_t e = idx[a];
-                const double sig = orc_sigmoid(dot_bf16_f64(w_router + (int64_t)e * L, h, L));
+                const double logit = dot_bf16_f64(w_router + (int64_t)e * L, h, L);
+                const double sig = orc_sigmoid(logit);
                 g[j] = round_mode ? (double)(float)sig : sig;
-                dsig[j] = sig * (1.0 - sig);
+                /* sigma'(x) = sigma(x) sigma(-x): no cancellation in 1 - sigma
+                 * where sigma(x) rounds to 1 */
+                dsig[j] = sig * orc_sigmoid(-logit);
                 for (int64_t i = 0; i < I; ++i) {
                     p1[j * I + i] = dot_bf16_f64(w1[e] + i * L, h, L);
                     p2[j * I + i] = dot_bf16_f64(w2[e] + i * L, h, L);

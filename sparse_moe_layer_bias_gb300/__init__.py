@@ -1,4 +1,4 @@
-"""GB300-native Stable LatentMoE layer forward and Quantile Balancing histogram.
+"""GB300-native Stable LatentMoE layer (forward and backward) and Quantile Balancing histogram.
 
 The compute lives in liblmoe.so (hand-written CUDA for sm_103a, C ABI in
 include/lmoe.h); this package is its ctypes binding plus the seeded input
@@ -11,7 +11,10 @@ from .binding import (  # noqa: F401
     LmoeError,
     alloc_host_io,
     alloc_workspace,
+    grad_shapes,
     library_path,
+    lmoe_backward,
+    lmoe_backward_workspace_size,
     lmoe_create,
     lmoe_destroy,
     lmoe_device_status,

@@ -22,7 +22,8 @@ STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED_SHAP
 EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size",
             "lmoe_workspace_layout", "lmoe_forward", "lmoe_host_io_size", "lmoe_forward_host",
             "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_route_static",
-            "lmoe_selftest_timeout", "qb_histogram", "qb_quantile_bias", "qb_sign_update")
+            "lmoe_selftest_timeout", "lmoe_backward_workspace_size", "lmoe_backward", "qb_histogram",
+            "qb_quantile_bias", "qb_sign_update")
 
 STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12_light",
           "expert_w12_heavy", "expert_w3", "combine", "up")
@@ -40,13 +41,17 @@ class LmoeConfig(ctypes.Structure):
                 ("shared_inter", ctypes.c_int32), ("beta1", ctypes.c_float),
                 ("beta2", ctypes.c_float), ("rms_eps", ctypes.c_float),
                 ("max_tokens", ctypes.c_int64), ("norm_after_down", ctypes.c_int32),
-                ("expert_fp8", ctypes.c_int32)]
+                ("expert_fp8", ctypes.c_int32), ("with_backward", ctypes.c_int32)]
 
 
 WEIGHT_NAMES = ("w_down", "w_router", "w1", "w2", "w3", "ws1", "ws2", "ws3", "w_up")
 
 
 class LmoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES]
+
+
+class LmoeGrads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES]
 
 
@@ -83,6 +88,11 @@ def load_library():
     lib.lmoe_workspace_layout.argtypes = [P, I64, ctypes.POINTER(LmoeWsLayout)]
     lib.lmoe_forward.restype = ctypes.c_int
     lib.lmoe_forward.argtypes = [P, P, I64, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.lmoe_backward_workspace_size.restype = ctypes.c_int
+    lib.lmoe_backward_workspace_size.argtypes = [P, I64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.lmoe_backward.restype = ctypes.c_int
+    lib.lmoe_backward.argtypes = [P, P, I64, P, P, P, P, P, ctypes.c_size_t, P, ctypes.POINTER(LmoeGrads), P,
+                                  ctypes.c_size_t, P]
     lib.lmoe_host_io_size.restype = ctypes.c_int
     lib.lmoe_host_io_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
     lib.lmoe_forward_host.restype = ctypes.c_int
@@ -157,14 +167,14 @@ class Handle:
 
 def lmoe_create(cfg: dict, weights: dict, max_tokens: int) -> Handle:
     """cfg: d, latent, n_experts, top_k, inter, n_shared, shared_inter and
-    optional beta1, beta2, rms_eps, norm_after_down, expert_fp8.  weights: bf16 CUDA tensors named as in
-    lmoe_weights."""
+    optional beta1, beta2, rms_eps, norm_after_down, expert_fp8, with_backward.  weights: bf16 CUDA
+    tensors named as in lmoe_weights."""
     lib = load_library()
     c = LmoeConfig(int(cfg["d"]), int(cfg["latent"]), int(cfg["n_experts"]), int(cfg["top_k"]),
                    int(cfg["inter"]), int(cfg["n_shared"]), int(cfg["shared_inter"]),
                    float(cfg.get("beta1", 4.0)), float(cfg.get("beta2", 25.0)),
                    float(cfg.get("rms_eps", 1e-6)), int(max_tokens), int(bool(cfg.get("norm_after_down", False))),
-                   int(bool(cfg.get("expert_fp8", False))))
+                   int(bool(cfg.get("expert_fp8", False))), int(bool(cfg.get("with_backward", False))))
     held = {}
     w = LmoeWeights()
     for n in WEIGHT_NAMES:
@@ -222,6 +232,54 @@ def lmoe_forward(handle: Handle, x: torch.Tensor, bias: torch.Tensor, y: torch.T
                           _ptr(workspace), workspace.numel(), _stream(stream))
     _check("lmoe_forward", st)
     return y
+
+
+def lmoe_backward_workspace_size(handle: Handle, T: int) -> int:
+    n = ctypes.c_size_t()
+    _check("lmoe_backward_workspace_size",
+           load_library().lmoe_backward_workspace_size(handle.ptr, int(T), ctypes.byref(n)))
+    return n.value
+
+
+def grad_shapes(handle: Handle) -> dict:
+    """Shapes of the weight gradients (as the weights)."""
+    c = handle.cfg
+    S = c.n_shared * c.shared_inter
+    return {"w_down": (c.latent, c.d), "w_router": (c.n_experts, c.latent),
+            "w1": (c.n_experts, c.inter, c.latent), "w2": (c.n_experts, c.inter, c.latent),
+            "w3": (c.n_experts, c.latent, c.inter), "ws1": (S, c.d), "ws2": (S, c.d), "ws3": (c.d, S),
+            "w_up": (c.d, c.latent)}
+
+
+def lmoe_backward(handle: Handle, x: torch.Tensor, dy: torch.Tensor, fwd_workspace: torch.Tensor,
+                  dx: torch.Tensor | None = None, grads: dict | None = None, workspace: torch.Tensor | None = None,
+                  topk_idx=None, gates=None, expert_counts=None, stream=None):
+    """Backward of the forward that ran on ``x`` with ``fwd_workspace``.
+    Returns (dx bf16 [T, d], dict of fp32 weight gradients)."""
+    lib = load_library()
+    x = _dev(x, torch.bfloat16, "x")
+    dy = _dev(dy, torch.bfloat16, "dy")
+    fwd_workspace = _dev(fwd_workspace, torch.uint8, "fwd_workspace")
+    T = x.shape[0]
+    if dx is None:
+        dx = torch.empty_like(x)
+    dx = _dev(dx, torch.bfloat16, "dx")
+    if grads is None:
+        grads = {n: torch.empty(s, dtype=torch.float32, device=x.device) for n, s in grad_shapes(handle).items()}
+    g = LmoeGrads()
+    for n in WEIGHT_NAMES:
+        setattr(g, n, _dev(grads[n], torch.float32, "grad " + n).data_ptr())
+    if workspace is None:
+        workspace = torch.empty(max(lmoe_backward_workspace_size(handle, T), 256), dtype=torch.uint8,
+                                device=x.device)
+    workspace = _dev(workspace, torch.uint8, "workspace")
+    st = lib.lmoe_backward(handle.ptr, _ptr(x), T, _ptr(dy), _ptr(_dev(topk_idx, torch.int32, "topk_idx")),
+                           _ptr(_dev(gates, torch.float32, "gates")),
+                           _ptr(_dev(expert_counts, torch.int32, "expert_counts")), _ptr(fwd_workspace),
+                           fwd_workspace.numel(), _ptr(dx), ctypes.byref(g), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    _check("lmoe_backward", st)
+    return dx, grads
 
 
 def _host(t, dtype, name):

@@ -17,9 +17,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblmoe.so")
-SOURCES = ["gemm.cu", "pack.cu", "route.cu", "route_static.cu", "combine.cu", "qb.cu", "selftest.cu",
-           "lmoe_api.cu"]
-HEADERS = ["kernels.h", "ptx.cuh"]
+SOURCES = ["gemm.cu", "gemm_bwd.cu", "backward.cu", "pack.cu", "route.cu", "route_static.cu", "combine.cu", "qb.cu",
+           "selftest.cu", "lmoe_api.cu"]
+HEADERS = ["kernels.h", "ptx.cuh", "gemm_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -1,0 +1,408 @@
+// backward.cu -- the memory-bound kernels of the layer's backward pass:
+// transposes (plain, or gathering the rows of each expert's assignments into
+// a padded per-expert column segment), the per-expert segment maps and
+// weight-gradient tile lists, the RMSNorm backward, the router backward, the
+// latent-gradient sum and the zeroing of unused experts' weight gradients.
+//
+// The gradient follows "Kimi-K3-Architecture-Deep-Dive" section 2 (the chain
+// down-projection -> routed experts -> aggregate -> RMSNorm -> up-projection)
+// and section 1 (SiTU-GLU; the tanh softcap is differentiable everywhere);
+// the routing choice itself carries no gradient, the gates do.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace lmoe {
+
+namespace {
+
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+__device__ __forceinline__ uint16_t f_to_bf16(float v) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+constexpr int kTT = 64;  // transpose tile: 64 x 64 elements
+
+// out[b][c][q] = scale(q) * in[b][src(q)][c] for c < C, q < Q, where
+// src(q) = qsrc[q] (or q when q < R without qsrc) and a negative src gives 0.
+// Tiles whose first q is at or past *q_limit are skipped (never read later).
+__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restrict__ in, int64_t ldi, int64_t ibs,
+                                                        int64_t R, int C, uint16_t *__restrict__ out, int64_t ldo,
+                                                        int64_t obs, int64_t Q, const int32_t *__restrict__ qsrc,
+                                                        const float *__restrict__ qscale,
+                                                        const int32_t *__restrict__ q_limit) {
+    grid_dependency_wait();
+    __shared__ uint16_t tile[kTT][kTT + 2];
+    const int64_t q0 = int64_t(blockIdx.x) * kTT;
+    const int c0 = blockIdx.y * kTT;
+    const int64_t b = blockIdx.z;
+    if (q_limit && q0 >= *q_limit) return;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    const uint16_t *inb = in + b * ibs;
+    uint16_t *outb = out + b * obs;
+#pragma unroll
+    for (int i = 0; i < kTT / 8; ++i) {
+        const int qq = ty + 8 * i;
+        const int64_t q = q0 + qq;
+        int64_t src = -1;
+        float sc = 1.0f;
+        if (q < Q) {
+            src = qsrc ? qsrc[q] : (q < R ? q : -1);
+            if (qscale && src >= 0) sc = qscale[q];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int cc = tx + 32 * h;
+            const int c = c0 + cc;
+            uint16_t v = 0;
+            if (src >= 0 && c < C) {
+                v = inb[src * ldi + c];
+                if (qscale) v = f_to_bf16(sc * bf16_to_f(v));
+            }
+            tile[qq][cc] = v;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTT / 8; ++i) {
+        const int cc = ty + 8 * i;
+        const int c = c0 + cc;
+        if (c >= C) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int qq = tx + 32 * h;
+            const int64_t q = q0 + qq;
+            if (q < Q) outb[int64_t(c) * ldo + q] = tile[qq][cc];
+        }
+    }
+}
+
+// One block: the per-expert column segments (each expert's assignments padded
+// to a multiple of 64 columns), in expert order, and the weight-gradient tile
+// lists {expert, first K block, K blocks, first output row} for the experts
+// with at least one assignment: m_tiles_a (resp. b) 128-row tiles each.
+constexpr int kSegThreads = 1024;
+__global__ void __launch_bounds__(kSegThreads) segments_kernel(const int32_t *__restrict__ counts, int E,
+                                                               int32_t *__restrict__ segoff, int4 *__restrict__ tiles_a,
+                                                               int m_tiles_a, int4 *__restrict__ tiles_b, int m_tiles_b,
+                                                               int32_t *__restrict__ n_tiles2) {
+    grid_dependency_wait();
+    __shared__ int32_t s_pad[kSegThreads], s_ne[kSegThreads];
+    const int e = threadIdx.x;
+    const int cnt = (e < E) ? counts[e] : 0;
+    const int pad = (cnt + 63) / 64 * 64;
+    s_pad[e] = pad;
+    s_ne[e] = cnt > 0 ? 1 : 0;
+    __syncthreads();
+    // inclusive scans (Hillis-Steele over the block)
+    for (int off = 1; off < kSegThreads; off <<= 1) {
+        const int a = (e >= off) ? s_pad[e - off] : 0;
+        const int b = (e >= off) ? s_ne[e - off] : 0;
+        __syncthreads();
+        s_pad[e] += a;
+        s_ne[e] += b;
+        __syncthreads();
+    }
+    const int seg0 = s_pad[e] - pad;       // exclusive
+    const int ne0 = s_ne[e] - (cnt > 0 ? 1 : 0);
+    if (e < E) segoff[e] = seg0;
+    if (e == E - 1) {
+        segoff[E] = s_pad[e];
+        n_tiles2[0] = s_ne[e] * m_tiles_a;
+        n_tiles2[1] = s_ne[e] * m_tiles_b;
+        n_tiles2[2] = s_pad[e];   // columns in use
+    }
+    if (e < E && cnt > 0) {
+        for (int mt = 0; mt < m_tiles_a; ++mt)
+            tiles_a[ne0 * m_tiles_a + mt] = make_int4(e, seg0 / 64, pad / 64, mt * 128);
+        for (int mt = 0; mt < m_tiles_b; ++mt)
+            tiles_b[ne0 * m_tiles_b + mt] = make_int4(e, seg0 / 64, pad / 64, mt * 128);
+    }
+}
+
+// Column maps of the segments: for column q = segoff[e] + c (c < padded
+// count), qperm = the permuted row offsets[e] + c (or -1 past the count),
+// qtok = that row's token, qgate = its gate.  One block per expert.
+__global__ void __launch_bounds__(256) segment_maps_kernel(const int32_t *__restrict__ counts,
+                                                           const int32_t *__restrict__ offsets,
+                                                           const int32_t *__restrict__ segoff,
+                                                           const int32_t *__restrict__ perm,
+                                                           const int32_t *__restrict__ tokrow,
+                                                           const float *__restrict__ gates, int32_t *__restrict__ qperm,
+                                                           int32_t *__restrict__ qtok, float *__restrict__ qgate) {
+    grid_dependency_wait();
+    const int e = blockIdx.x;
+    const int cnt = counts[e];
+    const int pad = (cnt + 63) / 64 * 64;
+    const int64_t s0 = segoff[e];
+    for (int c = threadIdx.x; c < pad; c += blockDim.x) {
+        int32_t p = -1, t = -1;
+        float g = 0.0f;
+        if (c < cnt) {
+            p = offsets[e] + c;
+            t = tokrow[p];
+            g = gates[perm[p]];
+        }
+        qperm[s0 + c] = p;
+        qtok[s0 + c] = t;
+        qgate[s0 + c] = g;
+    }
+}
+
+// Zero the routed weight gradients of experts no token chose (the segment
+// GEMMs have no tile for them).  grid (E, chunks).
+__global__ void __launch_bounds__(256) zero_unused_kernel(const int32_t *__restrict__ counts, int64_t per_expert,
+                                                          float *__restrict__ g1, float *__restrict__ g2,
+                                                          float *__restrict__ g3) {
+    grid_dependency_wait();
+    const int e = blockIdx.x;
+    if (counts[e] != 0) return;
+    const int64_t n4 = per_expert / 4;
+    float4 *p1 = reinterpret_cast<float4 *>(g1 + int64_t(e) * per_expert);
+    float4 *p2 = reinterpret_cast<float4 *>(g2 + int64_t(e) * per_expert);
+    float4 *p3 = reinterpret_cast<float4 *>(g3 + int64_t(e) * per_expert);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = int64_t(blockIdx.y) * blockDim.x + threadIdx.x; i < n4; i += int64_t(gridDim.y) * blockDim.x) {
+        p1[i] = z;
+        p2[i] = z;
+        p3[i] = z;
+    }
+}
+
+// RMSNorm backward, one block per token.  z = sum_j o[t*k + j] (the
+// gate-weighted expert rows the forward stored, fp32 sum), ms = mean(z^2),
+// r = z / sqrt(ms + eps);
+// dz = dr / sqrt(ms + eps) - z (dr . z) / (L (ms + eps)^(3/2)), stored bf16.
+constexpr int kRmsThreads = 256;
+__global__ void __launch_bounds__(kRmsThreads) rms_bwd_kernel(const uint16_t *__restrict__ o, int k, int L, float eps,
+                                                              const uint16_t *__restrict__ dr, int64_t ld_dr,
+                                                              uint16_t *__restrict__ dz) {
+    grid_dependency_wait();
+    extern __shared__ float zs[];   // [L]
+    __shared__ float red[2][kRmsThreads / 32];
+    const int64_t t = blockIdx.x;
+    float ss = 0.0f, drz = 0.0f;
+    for (int c = threadIdx.x * 8; c < L; c += kRmsThreads * 8) {
+        float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < k; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(o + (t * k + j) * L + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                z[2 * i] += __uint_as_float(w[i] << 16);
+                z[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+            }
+        }
+        const uint4 dv = *reinterpret_cast<const uint4 *>(dr + t * ld_dr + c);
+        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ss = fmaf(z[2 * i], z[2 * i], ss);
+            ss = fmaf(z[2 * i + 1], z[2 * i + 1], ss);
+            drz = fmaf(__uint_as_float(dw[i] << 16), z[2 * i], drz);
+            drz = fmaf(__uint_as_float(dw[i] & 0xffff0000u), z[2 * i + 1], drz);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) zs[c + i] = z[i];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        drz += __shfl_xor_sync(0xffffffffu, drz, off);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red[0][threadIdx.x >> 5] = ss;
+        red[1][threadIdx.x >> 5] = drz;
+    }
+    __syncthreads();
+    ss = 0.0f;
+    drz = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRmsThreads / 32; ++w) {
+        ss += red[0][w];
+        drz += red[1][w];
+    }
+    const float den = ss / static_cast<float>(L) + eps;
+    const float inv = 1.0f / sqrtf(den);
+    const float coef = drz * inv / (static_cast<float>(L) * den);
+    for (int c = threadIdx.x * 8; c < L; c += kRmsThreads * 8) {
+        const uint4 dv = *reinterpret_cast<const uint4 *>(dr + t * ld_dr + c);
+        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = __uint_as_float(dw[i] << 16) * inv - zs[c + 2 * i] * coef;
+            const float b = __uint_as_float(dw[i] & 0xffff0000u) * inv - zs[c + 2 * i + 1] * coef;
+            w[i] = uint32_t(f_to_bf16(a)) | (uint32_t(f_to_bf16(b)) << 16);
+        }
+        *reinterpret_cast<uint4 *>(dz + t * L + c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Router backward, one warp per token.  For each chosen expert j the warp
+// recomputes the logit x_j = w_router[e_j] . h_t (fp32) and lane j forms
+// dg_j = sum of the partial products dgp[p][0..nq) (p = the assignment's
+// permuted row) and the logit gradient dg_j * sigma'(x_j), with
+// sigma'(x) = sigma(x) sigma(-x) evaluated from x: it stays accurate where
+// the fp32 score itself has rounded to 1 (s (1 - s) would give 0 there).
+// Written into a dense bf16 row dl[t][0..ldl) that is zero elsewhere.
+__global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict__ dgp, int nq,
+                                                         const int32_t *__restrict__ inv,
+                                                         const int32_t *__restrict__ idx,
+                                                         const uint16_t *__restrict__ h,
+                                                         const uint16_t *__restrict__ wr, int L, int64_t T, int k,
+                                                         int ldl, uint16_t *__restrict__ dl) {
+    grid_dependency_wait();
+    const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;   // whole warps
+    const uint16_t *hrow = h + t * L;
+    float my_logit = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        const int ej = idx[t * k + j];
+        const uint16_t *wrow = wr + int64_t(ej) * L;
+        float part = 0.0f;
+        for (int c = lane * 8; c < L; c += 256) {
+            const uint4 hv = *reinterpret_cast<const uint4 *>(hrow + c);
+            const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + c);
+            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                part = fmaf(__uint_as_float(hw[i] << 16), __uint_as_float(ww[i] << 16), part);
+                part = fmaf(__uint_as_float(hw[i] & 0xffff0000u), __uint_as_float(ww[i] & 0xffff0000u), part);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == j) my_logit = part;
+    }
+    int e = -1;
+    float v = 0.0f;
+    if (lane < k) {
+        const int64_t a = t * k + lane;
+        const int64_t p = inv[a];
+        float dg = 0.0f;
+        for (int q = 0; q < nq; ++q) dg += dgp[p * nq + q];
+        e = idx[a];
+        const float sp = 1.0f / (1.0f + __expf(-my_logit));
+        const float sm = 1.0f / (1.0f + __expf(my_logit));
+        v = dg * (sp * sm);
+    }
+    for (int c0 = 0; c0 < ldl; c0 += 64) {
+        const int c = c0 + 2 * lane;
+        float v0 = 0.0f, v1 = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, e, j);
+            const float vj = __shfl_sync(0xffffffffu, v, j);
+            if (ej == c) v0 = vj;
+            if (ej == c + 1) v1 = vj;
+        }
+        if (c < ldl)
+            *reinterpret_cast<uint32_t *>(dl + t * ldl + c) = uint32_t(f_to_bf16(v0)) | (uint32_t(f_to_bf16(v1)) << 16);
+    }
+}
+
+// dh[t] = dhr[t] (fp32, the router's share) + sum_j dhp[t*k + j] (bf16 rows
+// of the experts' shares, assignment order), stored bf16.  8 columns per thread.
+__global__ void __launch_bounds__(256) dh_sum_kernel(const uint16_t *__restrict__ dhp, const float *__restrict__ dhr,
+                                                     int64_t T, int k, int L, uint16_t *__restrict__ dh) {
+    grid_dependency_wait();
+    const int64_t per_row = L / 8;
+    const int64_t total = T * per_row;
+    for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = v / per_row;
+        const int c = static_cast<int>(v % per_row) * 8;
+        const float4 r0 = *reinterpret_cast<const float4 *>(dhr + t * L + c);
+        const float4 r1 = *reinterpret_cast<const float4 *>(dhr + t * L + c + 4);
+        float acc[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        for (int j = 0; j < k; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(dhp + (t * k + j) * L + c);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += __uint_as_float(w[i] << 16);
+                acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = uint32_t(f_to_bf16(acc[2 * i])) | (uint32_t(f_to_bf16(acc[2 * i + 1])) << 16);
+        *reinterpret_cast<uint4 *>(dh + t * L + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+__global__ void __launch_bounds__(256) fill_kernel(float *__restrict__ p, int64_t n, float v) {
+    grid_dependency_wait();
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
+int blocks_for(int64_t work, int per_block, int cap) {
+    const int64_t b = (work + per_block - 1) / per_block;
+    return static_cast<int>(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+}  // namespace
+
+cudaError_t launch_transpose(const uint16_t *in, int64_t ldi, int64_t in_batch_stride, int64_t R, int C,
+                             uint16_t *out, int64_t ldo, int64_t out_batch_stride, int64_t Q, int batch,
+                             const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream) {
+    if (Q <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>((Q + kTT - 1) / kTT), static_cast<unsigned>((C + kTT - 1) / kTT),
+                    static_cast<unsigned>(batch));
+    return launch_kernel(transpose_kernel, grid, dim3(256), 0, stream, true, in, ldi, in_batch_stride, R, C, out, ldo,
+                         out_batch_stride, Q, qsrc, qscale, q_limit);
+}
+
+cudaError_t launch_segments(const int32_t *counts, const int32_t *offsets, const int32_t *perm,
+                            const int32_t *tokrow, const float *gates, int E, int32_t *segoff, int32_t *qperm,
+                            int32_t *qtok, float *qgate, int4 *tiles_a, int m_tiles_a, int4 *tiles_b,
+                            int m_tiles_b, int32_t *n_tiles3, cudaStream_t stream) {
+    if (E > kSegThreads) return cudaErrorInvalidValue;
+    cudaError_t e = launch_kernel(segments_kernel, dim3(1), dim3(kSegThreads), 0, stream, true, counts, E, segoff,
+                                  tiles_a, m_tiles_a, tiles_b, m_tiles_b, n_tiles3);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(segment_maps_kernel, dim3(E), dim3(256), 0, stream, true, counts, offsets,
+                         static_cast<const int32_t *>(segoff), perm, tokrow, gates, qperm, qtok, qgate);
+}
+
+cudaError_t launch_zero_unused(const int32_t *counts, int E, int64_t per_expert, float *g1, float *g2, float *g3,
+                               cudaStream_t stream) {
+    return launch_kernel(zero_unused_kernel, dim3(E, 8), dim3(256), 0, stream, true, counts, per_expert, g1, g2, g3);
+}
+
+cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps, const uint16_t *dr, int64_t ld_dr,
+                           uint16_t *dz, cudaStream_t stream) {
+    if (T <= 0) return cudaSuccess;
+    const size_t smem = size_t(L) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(rms_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_kernel(rms_bwd_kernel, dim3(static_cast<unsigned>(T)), dim3(kRmsThreads), smem, stream, true, o, k,
+                         L, eps, dr, ld_dr, dz);
+}
+
+cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, const int32_t *idx, const uint16_t *h,
+                              const uint16_t *w_router, int L, int64_t T, int k, int ldl, uint16_t *dl,
+                              cudaStream_t stream) {
+    if (T <= 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((T * 32 + 255) / 256);
+    return launch_kernel(router_bwd_kernel, dim3(blocks), dim3(256), 0, stream, true, dgp, nq, inv, idx, h, w_router,
+                         L, T, k, ldl, dl);
+}
+
+cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,
+                          int num_sms, cudaStream_t stream) {
+    if (T <= 0) return cudaSuccess;
+    const int blocks = blocks_for(T * (L / 8), 256, num_sms * 8);
+    return launch_kernel(dh_sum_kernel, dim3(blocks), dim3(256), 0, stream, true, dhp, dhr, T, k, L, dh);
+}
+
+cudaError_t launch_fill(float *p, int64_t n, float v, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = blocks_for(n, 256, 1024);
+    return launch_kernel(fill_kernel, dim3(blocks), dim3(256), 0, stream, true, p, n, v);
+}
+
+}  // namespace lmoe

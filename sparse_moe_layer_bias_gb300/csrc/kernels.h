@@ -52,8 +52,19 @@ enum BMode { B_PLAIN = 0, B_GLU = 1, B_SPLIT = 2 };
 // weight rows' power-of-two scales, SiTU-GLU, write e4m3(4 * act) bytes.
 // EPI_SCATTER_F8: e4m3 experts' W3 -- rescale by 2^(row exponent - 2), gate,
 // scatter bf16 rows (as EPI_SCATTER_BF16).
+// Backward pass:
+// EPI_F32: plain fp32 output rows (weight gradients; the router's share of the
+// latent gradient).  With per-expert K segments (launch_gemm_bwd, kseg), the
+// rows of expert e's output block go to out (rows < m_split) or out2.
+// EPI_GLU_BWD: the accumulator holds a SiTU-GLU GEMM's p1 | p2 (recomputed);
+// with the gradient u of its activation (gin) and the row's gate g
+// (row_scale[scatter_rows[row]], 1 without row_scale) it writes
+// dp1 = g u SiTU'(p1) softcap(p2) and dp2 = g u SiTU(p1) softcap'(p2) as bf16
+// (dp1 in columns [0, out_cols), dp2 in [out_cols, 2 out_cols)), and, with dgp,
+// the partial dot products sum u * act of the tile's columns (fp32,
+// dgp[row * n_tiles + nt]).
 enum Epi { EPI_BF16 = 0, EPI_SITU_GLU = 1, EPI_SIGMOID_F32 = 2, EPI_SCATTER_BF16 = 3, EPI_SITU_GLU_F8 = 4,
-           EPI_SCATTER_F8 = 5 };
+           EPI_SCATTER_F8 = 5, EPI_F32 = 6, EPI_GLU_BWD = 7 };
 
 constexpr int kBM = 128;  // rows per tile (one tcgen05 M=128 tile)
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzled row of bf16 (128 e4m3)
@@ -89,6 +100,13 @@ struct GemmArgs {
     const int8_t *col_exp0;       // per weight row of expert e: [e * col_exp_rows + col] (W1 or W3)
     const int8_t *col_exp1;       // EPI_SITU_GLU_F8: the W2 rows
     int32_t col_exp_rows;
+    // backward epilogues
+    const uint16_t *gin;          // EPI_GLU_BWD: gradient of the activation, bf16 rows
+    int64_t gin_ld;               //   its row stride (elements)
+    int32_t gin_col0;             //   column of feature 0 in a gin row
+    float *dgp;                   //   partial sums of u * act (nullable)
+    void *out2;                   // EPI_F32 with K segments: rows >= m_split of an expert's block
+    int32_t m_split;
     unsigned *err;           // device status word
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
@@ -102,6 +120,14 @@ struct GemmArgs {
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false,
                         bool dependent = true);
+
+// Backward-pass GEMMs (gemm_bwd.cu); same operand conventions.  With `kseg`
+// (grouped, A and B dense): `tiles` holds {expert, first K block, K blocks,
+// first row of the expert's output block} per 128-row tile, both operands are
+// K-major over one shared column space in which each expert owns a segment,
+// and m_rows is the height of an expert's output block.
+cudaError_t launch_gemm_bwd(int bn, AMode am, BMode bm, Epi epi, bool grouped, bool kseg, const GemmMaps &maps,
+                            const GemmArgs &args, int grid, cudaStream_t stream);
 
 // Repack per-expert weights [E][R][K] (row-major bf16) into tile-contiguous
 // order [E][R/TR][K/64][TR][64] so that one TMA box of TR rows x 64 columns is
@@ -147,5 +173,29 @@ cudaError_t launch_bounded_wait_selftest(unsigned *err, uint64_t limit_ns, int *
 cudaError_t launch_sign_update(const int32_t *counts, int E, float gamma, float *bias, cudaStream_t stream);
 cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level, float *q,
                                float *bias, cudaStream_t stream);
+
+// ------------------------------------------------------------------ backward
+// out[b][c][q] = scale(q) * in[b][src(q)][c] (c < C, q < Q); src(q) = qsrc[q],
+// or q when q < R without qsrc; a negative src gives 0.  Tiles starting at or
+// past *q_limit (when given) are skipped.
+cudaError_t launch_transpose(const uint16_t *in, int64_t ldi, int64_t in_batch_stride, int64_t R, int C,
+                             uint16_t *out, int64_t ldo, int64_t out_batch_stride, int64_t Q, int batch,
+                             const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream);
+// Per-expert column segments (assignments padded to 64), their column maps and
+// the segment GEMMs' tile lists; n_tiles3 = {tiles in a, tiles in b, columns}.
+cudaError_t launch_segments(const int32_t *counts, const int32_t *offsets, const int32_t *perm,
+                            const int32_t *tokrow, const float *gates, int E, int32_t *segoff, int32_t *qperm,
+                            int32_t *qtok, float *qgate, int4 *tiles_a, int m_tiles_a, int4 *tiles_b,
+                            int m_tiles_b, int32_t *n_tiles3, cudaStream_t stream);
+cudaError_t launch_zero_unused(const int32_t *counts, int E, int64_t per_expert, float *g1, float *g2, float *g3,
+                               cudaStream_t stream);
+cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps, const uint16_t *dr, int64_t ld_dr,
+                           uint16_t *dz, cudaStream_t stream);
+cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, const int32_t *idx, const uint16_t *h,
+                              const uint16_t *w_router, int L, int64_t T, int k, int ldl, uint16_t *dl,
+                              cudaStream_t stream);
+cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,
+                          int num_sms, cudaStream_t stream);
+cudaError_t launch_fill(float *p, int64_t n, float v, cudaStream_t stream);
 
 }  // namespace lmoe

@@ -1,6 +1,6 @@
 // lmoe_api.cu -- host side of the C ABI declared in include/lmoe.h: argument
-// validation, workspace layout, TMA descriptors, and the launch sequence of
-// one Stable LatentMoE forward pass.
+// validation, workspace layout, TMA descriptors, and the launch sequences of
+// one Stable LatentMoE forward pass and of its backward pass.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -38,6 +38,17 @@ struct lmoe_handle {
     // this side stream, concurrently with the routing kernels.
     cudaStream_t side;
     cudaEvent_t ev_fork, ev_join;
+    // with_backward: transposed copies of the weights (handle-owned), K-major
+    // for the backward's data-gradient GEMMs:
+    //   t_ups3 [latent + S][d]        = [W_up^T ; Ws3^T]
+    //   t_w3   [E][inter][latent]     = W3[e]^T
+    //   t_w12  [E][latent][2 inter]   = [W1[e]^T | W2[e]^T]
+    //   t_wr   [latent][E rounded up to 64] = W_router^T (zero columns past E)
+    //   t_wd   [d][latent]            = W_down^T
+    //   t_ws12 [d][2 S]               = [Ws1^T | Ws2^T]
+    uint16_t *t_ups3, *t_w3, *t_w12, *t_wr, *t_wd, *t_ws12;
+    CUtensorMap m_t_ups3, m_t_w3, m_t_w12, m_t_wr, m_t_wd, m_t_ws12;
+    int bn_drs, bn_u, bn_s;
 };
 
 namespace {
@@ -132,6 +143,8 @@ int validate_config(const lmoe_config *c) {
     if (!(c->beta1 > 0.0f) || !(c->beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return LMOE_ERR_INVALID_ARG;
     if (c->norm_after_down != 0 && c->norm_after_down != 1) return LMOE_ERR_INVALID_ARG;
     if (c->expert_fp8 != 0 && c->expert_fp8 != 1) return LMOE_ERR_INVALID_ARG;
+    if (c->with_backward != 0 && c->with_backward != 1) return LMOE_ERR_INVALID_ARG;
+    if (c->with_backward && (c->norm_after_down || c->expert_fp8)) return LMOE_ERR_UNSUPPORTED_SHAPE;
     if (c->expert_fp8 && c->inter % 128) return LMOE_ERR_UNSUPPORTED_SHAPE;
     const int64_t S = int64_t(c->n_shared) * c->shared_inter;
     if (c->d % 64 || c->latent % 128 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
@@ -197,6 +210,12 @@ void free_handle(lmoe_handle *h) {
     cudaFree(h->w1e);
     cudaFree(h->w2e);
     cudaFree(h->w3e);
+    cudaFree(h->t_ups3);
+    cudaFree(h->t_w3);
+    cudaFree(h->t_w12);
+    cudaFree(h->t_wr);
+    cudaFree(h->t_wd);
+    cudaFree(h->t_ws12);
     release_streams(h);
     delete h;
 }
@@ -231,6 +250,108 @@ void release_streams(lmoe_handle *h) {
         if (h->ev_fwd[s]) cudaEventDestroy(h->ev_fwd[s]);
         if (h->ev_out[s]) cudaEventDestroy(h->ev_out[s]);
     }
+}
+
+int64_t round64(int64_t v) { return (v + 63) / 64 * 64; }
+
+// Transposed weight copies for the backward pass (see lmoe_handle).
+bool build_transposed(lmoe_handle *h) {
+    const lmoe_config &c = h->cfg;
+    const lmoe_weights &w = h->w;
+    const int64_t d = c.d, L = c.latent, E = c.n_experts, I = c.inter;
+    const int64_t S = int64_t(c.n_shared) * c.shared_inter;
+    const int64_t Ep = round64(E);
+    h->bn_drs = ((L + S) % 256 == 0) ? 256 : 128;
+    h->bn_u = (I % 256 == 0) ? 256 : 128;
+    h->bn_s = (S % 256 == 0) ? 256 : 128;
+    if (cudaMalloc(&h->t_ups3, size_t((L + S) * d) * 2) != cudaSuccess ||
+        cudaMalloc(&h->t_w3, size_t(E * I * L) * 2) != cudaSuccess ||
+        cudaMalloc(&h->t_w12, size_t(E * L * 2 * I) * 2) != cudaSuccess ||
+        cudaMalloc(&h->t_wr, size_t(L * Ep) * 2) != cudaSuccess ||
+        cudaMalloc(&h->t_wd, size_t(d * L) * 2) != cudaSuccess ||
+        cudaMalloc(&h->t_ws12, size_t(d * 2 * S) * 2) != cudaSuccess)
+        return false;
+    const int Li = static_cast<int>(L), Ii = static_cast<int>(I), di = static_cast<int>(d);
+    const int Si = static_cast<int>(S), Ei = static_cast<int>(E);
+    // launch_transpose(in, ldi, in_batch, R, C, out, ldo, out_batch, Q, batch, ...):
+    // out[b][c][q] = in[b][q][c]
+    bool ok = launch_transpose(w.w_up, L, 0, d, Li, h->t_ups3, d, 0, d, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.ws3, S, 0, d, Si, h->t_ups3 + L * d, d, 0, d, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.w3, I, L * I, L, Ii, h->t_w3, L, I * L, L, Ei, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.w1, L, I * L, I, Li, h->t_w12, 2 * I, L * 2 * I, I, Ei, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.w2, L, I * L, I, Li, h->t_w12 + I, 2 * I, L * 2 * I, I, Ei, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.w_router, L, 0, E, Li, h->t_wr, Ep, 0, Ep, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.w_down, d, 0, L, di, h->t_wd, L, 0, L, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.ws1, d, 0, S, di, h->t_ws12, 2 * S, 0, S, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              launch_transpose(w.ws2, d, 0, S, di, h->t_ws12 + S, 2 * S, 0, S, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) return false;
+    return make_map(&h->m_t_ups3, h->t_ups3, L + S, d, d, h->bn_drs) &&
+           make_map(&h->m_t_w3, h->t_w3, E * I, L, L, h->bn_u) &&
+           make_map(&h->m_t_w12, h->t_w12, E * L, 2 * I, 2 * I, h->bn_exp3) &&
+           make_map(&h->m_t_wr, h->t_wr, L, Ep, Ep, h->bn_down) &&
+           make_map(&h->m_t_wd, h->t_wd, d, L, L, h->bn_up) &&
+           make_map(&h->m_t_ws12, h->t_ws12, d, 2 * S, 2 * S, h->bn_up);
+}
+
+// Backward workspace: gradients of the intermediates, their K-major
+// (transposed) copies for the weight-gradient GEMMs, and the per-expert
+// column segments.  Tp = T and Qmax = T*top_k + 64 E rounded up to 64;
+// Ep = E rounded up to 64.
+struct BwdLayout {
+    size_t ones, drs, dps, dz, u, dp, dgp, dl, dhp, dhr, dh, dyT, xT, rT, sT, dpsT, dhT, hT, dlT, segoff, qperm,
+        qtok, qgate, kt_a, kt_b, nkt, doT, aT, hgT, dpT, total;
+    int64_t Tp, Ep, Qmax;
+};
+
+BwdLayout bwd_layout(const lmoe_handle *h, int64_t T) {
+    const lmoe_config &c = h->cfg;
+    BwdLayout l{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    const int64_t d = c.d, L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
+    const int64_t S = int64_t(c.n_shared) * c.shared_inter;
+    const int64_t n = T * K;
+    const int64_t nq = I / (h->bn_exp1 / 2);
+    l.Tp = round64(T);
+    l.Ep = round64(E);
+    l.Qmax = round64(n) + 64 * E;
+    l.ones = take(size_t(n) * 4);
+    l.drs = take(size_t(T * (L + S)) * 2);
+    l.dps = take(size_t(T * 2 * S) * 2);
+    l.dz = take(size_t(T * L) * 2);
+    l.u = take(size_t(n * I) * 2);
+    l.dp = take(size_t(n * 2 * I) * 2);
+    l.dgp = take(size_t(n * nq) * 4);
+    l.dl = take(size_t(T * l.Ep) * 2);
+    l.dhp = take(size_t(n * L) * 2);
+    l.dhr = take(size_t(T * L) * 4);
+    l.dh = take(size_t(T * L) * 2);
+    l.dyT = take(size_t(d * l.Tp) * 2);
+    l.xT = take(size_t(d * l.Tp) * 2);
+    l.rT = take(size_t(L * l.Tp) * 2);
+    l.sT = take(size_t(S * l.Tp) * 2);
+    l.dpsT = take(size_t(2 * S * l.Tp) * 2);
+    l.dhT = take(size_t(L * l.Tp) * 2);
+    l.hT = take(size_t(L * l.Tp) * 2);
+    l.dlT = take(size_t(E * l.Tp) * 2);
+    l.segoff = take(size_t(E + 1) * 4);
+    l.qperm = take(size_t(l.Qmax) * 4);
+    l.qtok = take(size_t(l.Qmax) * 4);
+    l.qgate = take(size_t(l.Qmax) * 4);
+    l.kt_a = take(size_t(E * (L / kBM)) * 16);
+    l.kt_b = take(size_t(E * ceil_div(2 * I, kBM)) * 16);
+    l.nkt = take(16);
+    l.doT = take(size_t(L * l.Qmax) * 2);
+    l.aT = take(size_t(I * l.Qmax) * 2);
+    l.hgT = take(size_t(L * l.Qmax) * 2);
+    l.dpT = take(size_t(2 * I * l.Qmax) * 2);
+    l.total = off;
+    return l;
 }
 
 }  // namespace
@@ -320,6 +441,10 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
          make_map(&h->m_wup, w->w_up, d, L, L, h->bn_up) &&
          make_map(&h->m_ws3, w->ws3, d, S, S, h->bn_up);
     if (!ok) {
+        free_handle(h);
+        return LMOE_ERR_CUDA;
+    }
+    if (c.with_backward && !build_transposed(h)) {
         free_handle(h);
         return LMOE_ERR_CUDA;
     }
@@ -621,6 +746,302 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         if (st) return st;
     }
     mark(LMOE_NUM_STAGES);
+    return LMOE_OK;
+}
+
+int lmoe_backward_workspace_size(const lmoe_handle *h, int64_t T, size_t *bytes) {
+    if (!h || !bytes || T < 0) return LMOE_ERR_INVALID_ARG;
+    if (!h->cfg.with_backward) return LMOE_ERR_INVALID_ARG;
+    if (T > h->cfg.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    *bytes = bwd_layout(h, T).total;
+    return LMOE_OK;
+}
+
+int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *dy, const int32_t *idx_in,
+                  const float *gates_in, const int32_t *counts_in, const void *fwd_workspace,
+                  size_t fwd_workspace_bytes, uint16_t *dx, const lmoe_grads *g, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+    if (!h || T < 0) return LMOE_ERR_INVALID_ARG;
+    const lmoe_config &c = h->cfg;
+    if (!c.with_backward) return LMOE_ERR_INVALID_ARG;
+    if (T > c.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return LMOE_OK;
+    if (!x || !dy || !fwd_workspace || !dx || !g || !workspace || !g->w_down || !g->w_router || !g->w1 ||
+        !g->w2 || !g->w3 || !g->ws1 || !g->ws2 || !g->ws3 || !g->w_up)
+        return LMOE_ERR_INVALID_ARG;
+    const void *al[] = {x, dy, dx, g->w_down, g->w_router, g->w1, g->w2, g->w3, g->ws1, g->ws2, g->ws3, g->w_up};
+    for (const void *p : al)
+        if (!aligned16(p)) return LMOE_ERR_ALIGNMENT;
+    if ((idx_in && !aligned16(idx_in)) || (gates_in && !aligned16(gates_in)) ||
+        (counts_in && !aligned16(counts_in)) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u))
+        return LMOE_ERR_ALIGNMENT;
+    const Layout fl = compute_layout(c, T, true, true, true, true);
+    const BwdLayout bl = bwd_layout(h, T);
+    if (fwd_workspace_bytes < fl.total || workspace_bytes < bl.total) return LMOE_ERR_WORKSPACE;
+
+    const int64_t d = c.d, L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
+    const int64_t S = int64_t(c.n_shared) * c.shared_inter;
+    const int64_t n = T * K;
+    const int64_t Tp = bl.Tp, Ep = bl.Ep, Qmax = bl.Qmax;
+    const int Li = static_cast<int>(L), Ii = static_cast<int>(I), di = static_cast<int>(d);
+    const int Si = static_cast<int>(S), Ei = static_cast<int>(E), Ki = static_cast<int>(K);
+    // the forward's intermediates
+    const uint8_t *fw = static_cast<const uint8_t *>(fwd_workspace);
+    const uint16_t *hbuf = reinterpret_cast<const uint16_t *>(fw + fl.h);
+    const int32_t *idx = idx_in ? idx_in : reinterpret_cast<const int32_t *>(fw + fl.idx);
+    const float *gates = gates_in ? gates_in : reinterpret_cast<const float *>(fw + fl.gates);
+    const int32_t *counts = counts_in ? counts_in : reinterpret_cast<const int32_t *>(fw + fl.counts);
+    const int32_t *offsets = reinterpret_cast<const int32_t *>(fw + fl.offsets);
+    const int4 *tiles = reinterpret_cast<const int4 *>(fw + fl.tiles);
+    const int32_t *nmt = reinterpret_cast<const int32_t *>(fw + fl.nmt);
+    const int32_t *perm = reinterpret_cast<const int32_t *>(fw + fl.perm);
+    const int32_t *inv = reinterpret_cast<const int32_t *>(fw + fl.inv);
+    const int32_t *tokrow = reinterpret_cast<const int32_t *>(fw + fl.tokrow);
+    const uint16_t *act = reinterpret_cast<const uint16_t *>(fw + fl.act);
+    const uint16_t *obuf = reinterpret_cast<const uint16_t *>(fw + fl.o);
+    const uint16_t *rbuf = reinterpret_cast<const uint16_t *>(fw + fl.r);
+    const uint16_t *sact = reinterpret_cast<const uint16_t *>(fw + fl.sact);
+    // the backward's own buffers
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto bf = [&](size_t off) { return reinterpret_cast<uint16_t *>(ws + off); };
+    float *ones = reinterpret_cast<float *>(ws + bl.ones);
+    uint16_t *drs = bf(bl.drs), *dps = bf(bl.dps), *dz = bf(bl.dz), *u = bf(bl.u), *dp = bf(bl.dp);
+    float *dgp = reinterpret_cast<float *>(ws + bl.dgp);
+    uint16_t *dl = bf(bl.dl), *dhp = bf(bl.dhp), *dh = bf(bl.dh);
+    float *dhr = reinterpret_cast<float *>(ws + bl.dhr);
+    uint16_t *dyT = bf(bl.dyT), *xT = bf(bl.xT), *rT = bf(bl.rT), *sT = bf(bl.sT), *dpsT = bf(bl.dpsT);
+    uint16_t *dhT = bf(bl.dhT), *hT = bf(bl.hT), *dlT = bf(bl.dlT);
+    int32_t *segoff = reinterpret_cast<int32_t *>(ws + bl.segoff);
+    int32_t *qperm = reinterpret_cast<int32_t *>(ws + bl.qperm);
+    int32_t *qtok = reinterpret_cast<int32_t *>(ws + bl.qtok);
+    float *qgate = reinterpret_cast<float *>(ws + bl.qgate);
+    int4 *kt_a = reinterpret_cast<int4 *>(ws + bl.kt_a);
+    int4 *kt_b = reinterpret_cast<int4 *>(ws + bl.kt_b);
+    int32_t *nkt = reinterpret_cast<int32_t *>(ws + bl.nkt);
+    uint16_t *doT = bf(bl.doT), *aT = bf(bl.aT), *hgT = bf(bl.hgT), *dpT = bf(bl.dpT);
+
+    CUtensorMap m_dy, m_x, m_dp, m_dl, m_dh, m_dps, m_dyT, m_xT, m_rT, m_sT, m_dps1T, m_dps2T, m_dhT, m_hT, m_dlT,
+        m_doT, m_aT, m_hgT, m_dpT;
+    if (!make_map(&m_dy, dy, T, d, d, kBM) || !make_map(&m_x, x, T, d, d, kBM) ||
+        !make_map(&m_dp, dp, n, 2 * I, 2 * I, kBM) || !make_map(&m_dl, dl, T, Ep, Ep, kBM) ||
+        !make_map(&m_dh, dh, T, L, L, kBM) || !make_map(&m_dps, dps, T, 2 * S, 2 * S, kBM) ||
+        !make_map(&m_dyT, dyT, d, Tp, Tp, kBM) || !make_map(&m_xT, xT, d, Tp, Tp, h->bn_up) ||
+        !make_map(&m_rT, rT, L, Tp, Tp, h->bn_down) || !make_map(&m_sT, sT, S, Tp, Tp, h->bn_s) ||
+        !make_map(&m_dps1T, dpsT, S, Tp, Tp, kBM) || !make_map(&m_dps2T, dpsT + S * Tp, S, Tp, Tp, kBM) ||
+        !make_map(&m_dhT, dhT, L, Tp, Tp, kBM) || !make_map(&m_hT, hT, L, Tp, Tp, h->bn_down) ||
+        !make_map(&m_dlT, dlT, E, Tp, Tp, kBM) || !make_map(&m_doT, doT, L, Qmax, Qmax, kBM) ||
+        !make_map(&m_aT, aT, I, Qmax, Qmax, h->bn_u) || !make_map(&m_hgT, hgT, L, Qmax, Qmax, h->bn_down) ||
+        !make_map(&m_dpT, dpT, 2 * I, Qmax, Qmax, kBM))
+        return LMOE_ERR_CUDA;
+
+    const int m_tiles = static_cast<int>(ceil_div(T, kBM));
+    auto grid_for = [&](int64_t tiles_) { return static_cast<int>(tiles_ < h->num_sms ? tiles_ : h->num_sms); };
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    int st;
+    const int64_t grouped_tiles = ceil_div(n, kBM) + E;   // bound on the forward's 128-row tile list
+
+    if (!ok(launch_fill(ones, n, 1.0f, stream))) return LMOE_ERR_CUDA;
+    {   // dr | da_s = dy [W_up | Ws3]
+        GemmMaps m{m_dy, m_dy, h->m_t_ups3, h->m_t_ups3};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(ceil_div(L + S, h->bn_drs));
+        a.k_blocks = static_cast<int32_t>(d / kBK);
+        a.out = drs;
+        a.ld_out = L + S;
+        a.out_cols = static_cast<int32_t>(L + S);
+        st = gemm_status(launch_gemm(h->bn_drs, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    {   // shared experts: dp_s = SiTU-GLU backward of the recomputed x Ws1^T | x Ws2^T
+        GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(S / (h->bn_shared / 2));
+        a.k_blocks = static_cast<int32_t>(d / kBK);
+        a.gin = drs;
+        a.gin_ld = L + S;
+        a.gin_col0 = static_cast<int32_t>(L);
+        a.out = dps;
+        a.ld_out = 2 * S;
+        a.out_cols = static_cast<int32_t>(S);
+        st = gemm_status(launch_gemm_bwd(h->bn_shared, A_DENSE, B_GLU, EPI_GLU_BWD, false, false, m, a,
+                                         grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    // RMSNorm backward: dz
+    if (!ok(launch_rms_bwd(obuf, T, Ki, Li, c.rms_eps, drs, L + S, dz, stream))) return LMOE_ERR_CUDA;
+    {   // u = W3[e]^T dz for every assignment (dz rows gathered by token), permuted order
+        GemmMaps m{h->m_t_w3, h->m_t_w3, h->m_t_w3, h->m_t_w3};
+        GemmArgs a = base_args(h);
+        a.n_tiles = static_cast<int32_t>(ceil_div(I, h->bn_u));
+        a.k_blocks = static_cast<int32_t>(L / kBK);
+        a.b_expert_rows = static_cast<int32_t>(I);
+        a.gather_src = dz;
+        a.gather_rows = tokrow;
+        a.gather_ld = L;
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
+        a.out = u;
+        a.ld_out = I;
+        a.out_cols = static_cast<int32_t>(I);
+        st = gemm_status(launch_gemm_bwd(h->bn_u, A_GATHER, B_PLAIN, EPI_BF16, true, false, m, a,
+                                         grid_for(grouped_tiles * a.n_tiles), stream));
+        if (st) return st;
+    }
+    const int nq = static_cast<int>(I / (h->bn_exp1 / 2));
+    {   // routed experts: dp = SiTU-GLU backward of the recomputed W1[e] h | W2[e] h with
+        // da = gate * u; partial sums of u * act for the gates' gradient
+        GemmMaps m{h->m_w1, h->m_w1, h->m_w1, h->m_w2};
+        GemmArgs a = base_args(h);
+        a.n_tiles = nq;
+        a.k_blocks = static_cast<int32_t>(L / kBK);
+        a.b_expert_rows = static_cast<int32_t>(I);
+        a.b_packed = 1;
+        a.b_row_tiles = nq;
+        a.gather_src = hbuf;
+        a.gather_rows = tokrow;
+        a.gather_ld = L;
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
+        a.gin = u;
+        a.gin_ld = I;
+        a.gin_col0 = 0;
+        a.scatter_rows = perm;
+        a.row_scale = gates;
+        a.dgp = dgp;
+        a.out = dp;
+        a.ld_out = 2 * I;
+        a.out_cols = static_cast<int32_t>(I);
+        st = gemm_status(launch_gemm_bwd(h->bn_exp1, A_GATHER, B_GLU, EPI_GLU_BWD, true, false, m, a,
+                                         grid_for(grouped_tiles * a.n_tiles), stream));
+        if (st) return st;
+    }
+    // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
+    if (!ok(launch_router_bwd(dgp, nq, inv, idx, hbuf, h->w.w_router, Li, T, Ki, static_cast<int>(Ep), dl, stream)))
+        return LMOE_ERR_CUDA;
+    {   // experts' share of dh: W1[e]^T dp1 + W2[e]^T dp2, rows back in assignment order
+        GemmMaps m{m_dp, m_dp, h->m_t_w12, h->m_t_w12};
+        GemmArgs a = base_args(h);
+        a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_exp3));
+        a.k_blocks = static_cast<int32_t>(2 * I / kBK);
+        a.b_expert_rows = static_cast<int32_t>(L);
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
+        a.out = dhp;
+        a.ld_out = L;
+        a.out_cols = static_cast<int32_t>(L);
+        a.scatter_rows = perm;
+        a.row_scale = ones;
+        st = gemm_status(launch_gemm(h->bn_exp3, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true, m, a,
+                                     grid_for(grouped_tiles * a.n_tiles), stream));
+        if (st) return st;
+    }
+    {   // router's share of dh: dl W_router (fp32)
+        GemmMaps m{m_dl, m_dl, h->m_t_wr, h->m_t_wr};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
+        a.k_blocks = static_cast<int32_t>(Ep / kBK);
+        a.out = dhr;
+        a.ld_out = L;
+        a.out_cols = static_cast<int32_t>(L);
+        st = gemm_status(launch_gemm_bwd(h->bn_down, A_DENSE, B_PLAIN, EPI_F32, false, false, m, a,
+                                         grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    if (!ok(launch_dh_sum(dhp, dhr, T, Ki, Li, dh, h->num_sms, stream))) return LMOE_ERR_CUDA;
+    {   // dx = dh W_down + dp_s [Ws1 ; Ws2]  (K split over the two sources)
+        GemmMaps m{m_dh, m_dps, h->m_t_wd, h->m_t_ws12};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(T);
+        a.m_tiles = m_tiles;
+        a.n_tiles = static_cast<int32_t>(ceil_div(d, h->bn_up));
+        a.k_split = static_cast<int32_t>(L / kBK);
+        a.k_blocks = static_cast<int32_t>((L + 2 * S) / kBK);
+        a.out = dx;
+        a.ld_out = d;
+        a.out_cols = static_cast<int32_t>(d);
+        st = gemm_status(launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
+                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (st) return st;
+    }
+    // ---- weight gradients of the dense weights: K = tokens (transposed operands, zero past T)
+    const int64_t Tl = T;
+    if (!ok(launch_transpose(dy, d, 0, Tl, di, dyT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(x, d, 0, Tl, di, xT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(rbuf, L, 0, Tl, Li, rT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(sact, S, 0, Tl, Si, sT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(dps, 2 * S, 0, Tl, 2 * Si, dpsT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(dh, L, 0, Tl, Li, dhT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(hbuf, L, 0, Tl, Li, hT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
+        !ok(launch_transpose(dl, Ep, 0, Tl, Ei, dlT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)))
+        return LMOE_ERR_CUDA;
+    auto wgrad = [&](const CUtensorMap &ma, const CUtensorMap &mb, int64_t M, int64_t N, int bn, float *out) {
+        GemmMaps m{ma, ma, mb, mb};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(M);
+        a.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
+        a.n_tiles = static_cast<int32_t>(ceil_div(N, bn));
+        a.k_blocks = static_cast<int32_t>(Tp / kBK);
+        a.out = out;
+        a.ld_out = N;
+        a.out_cols = static_cast<int32_t>(N);
+        return gemm_status(launch_gemm_bwd(bn, A_DENSE, B_PLAIN, EPI_F32, false, false, m, a,
+                                           grid_for(int64_t(a.m_tiles) * a.n_tiles), stream));
+    };
+    if ((st = wgrad(m_dyT, m_rT, d, L, h->bn_down, g->w_up)) || (st = wgrad(m_dyT, m_sT, d, S, h->bn_s, g->ws3)) ||
+        (st = wgrad(m_dps1T, m_xT, S, d, h->bn_up, g->ws1)) || (st = wgrad(m_dps2T, m_xT, S, d, h->bn_up, g->ws2)) ||
+        (st = wgrad(m_dhT, m_xT, L, d, h->bn_up, g->w_down)) || (st = wgrad(m_dlT, m_hT, E, L, h->bn_down, g->w_router)))
+        return st;
+    // ---- weight gradients of the routed experts: K = each expert's own assignments
+    const int mt_a = static_cast<int>(L / kBM), mt_b = static_cast<int>(ceil_div(2 * I, kBM));
+    if (!ok(launch_segments(counts, offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
+                            mt_b, nkt, stream)) ||
+        !ok(launch_zero_unused(counts, Ei, I * L, g->w1, g->w2, g->w3, stream)) ||
+        // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's column segment
+        !ok(launch_transpose(dz, L, 0, Tl, Li, doT, Qmax, 0, Qmax, 1, qtok, qgate, nkt + 2, stream)) ||
+        !ok(launch_transpose(act, I, 0, n, Ii, aT, Qmax, 0, Qmax, 1, qperm, nullptr, nkt + 2, stream)) ||
+        !ok(launch_transpose(hbuf, L, 0, Tl, Li, hgT, Qmax, 0, Qmax, 1, qtok, nullptr, nkt + 2, stream)) ||
+        !ok(launch_transpose(dp, 2 * I, 0, n, 2 * Ii, dpT, Qmax, 0, Qmax, 1, qperm, nullptr, nkt + 2, stream)))
+        return LMOE_ERR_CUDA;
+    {   // dW3[e] = sum over e's assignments of (gate dz) act^T
+        GemmMaps m{m_doT, m_doT, m_aT, m_aT};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(L);
+        a.m_split = static_cast<int32_t>(L);
+        a.n_tiles = static_cast<int32_t>(ceil_div(I, h->bn_u));
+        a.tiles = kt_a;
+        a.n_mtiles = nkt;
+        a.out = g->w3;
+        a.out2 = g->w3;
+        a.ld_out = I;
+        a.out_cols = static_cast<int32_t>(I);
+        st = gemm_status(launch_gemm_bwd(h->bn_u, A_DENSE, B_PLAIN, EPI_F32, true, true, m, a,
+                                         grid_for(E * mt_a * a.n_tiles), stream));
+        if (st) return st;
+    }
+    {   // dW1[e] | dW2[e] = sum over e's assignments of (dp1 | dp2) h^T
+        GemmMaps m{m_dpT, m_dpT, m_hgT, m_hgT};
+        GemmArgs a = base_args(h);
+        a.m_rows = static_cast<int32_t>(2 * I);
+        a.m_split = static_cast<int32_t>(I);
+        a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
+        a.tiles = kt_b;
+        a.n_mtiles = nkt + 1;
+        a.out = g->w1;
+        a.out2 = g->w2;
+        a.ld_out = L;
+        a.out_cols = static_cast<int32_t>(L);
+        st = gemm_status(launch_gemm_bwd(h->bn_down, A_DENSE, B_PLAIN, EPI_F32, true, true, m, a,
+                                         grid_for(E * mt_b * a.n_tiles), stream));
+        if (st) return st;
+    }
     return LMOE_OK;
 }
 

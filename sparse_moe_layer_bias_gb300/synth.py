@@ -226,6 +226,21 @@ def activations_device(shape: LayerShape, T: int | None = None, device="cuda", s
     return x.to(torch.bfloat16), bias
 
 
+def grad_output_host(shape: LayerShape, T: int | None = None, seed_offset: int = 0) -> torch.Tensor:
+    """Upstream gradient dy [T, d] bf16, i.i.d. N(0, 1), for the backward pass."""
+    T = shape.T if T is None else T
+    rng = np.random.default_rng(shape.seed + 15485863 * (1 + seed_offset))
+    return _to_bf16(rng.standard_normal((T, shape.d)))
+
+
+def grad_output_device(shape: LayerShape, T: int | None = None, device="cuda", seed_offset: int = 0):
+    """Same distribution as ``grad_output_host``, drawn on the GPU."""
+    T = shape.T if T is None else T
+    gen = torch.Generator(device=device)
+    gen.manual_seed(shape.seed + 15485863 * (1 + seed_offset))
+    return torch.randn((T, shape.d), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
 def qb_scores(T: int, E: int = QB_SWEEP_E, seed: int = QB_SEED, device="cpu") -> torch.Tensor:
     """fp32 sigmoid scores of logits N(mu_e, 1), mu_e ~ N(0, 0.5^2); [T, E]."""
     gen = torch.Generator(device=device)

@@ -1,0 +1,175 @@
+"""Backward pass through the C ABI against the oracle's fp64 gradient.
+
+The oracle takes the GPU forward's routing (top-k is a discrete choice the
+gradient does not pass through) and recomputes everything else in fp64 from
+the same bf16 inputs; it is itself pinned by finite differences
+(test_oracle_backward.py).  Every gradient (dx and the nine weights) must lie
+within BWD_REL_FRO in relative Frobenius norm: the GPU path rounds six
+intermediates to bf16 (dr, dz, u, dp, the experts' share of dh, dh), each a
+relative perturbation of at most 2^-9 (RMS about 2^-9/sqrt(3) = 1.1e-3 per
+element), so the expected error is about sqrt(6) * 1.1e-3 = 2.7e-3; the bar
+leaves a factor of about 4.  The largest element error must stay within
+BWD_MAX_REL of the gradient's largest element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_moe_layer_bias_gb300 import synth
+
+from layer_check import dec, host_bits, oracle_cfg, rel_fro, ws_view
+
+pytestmark = pytest.mark.gpu
+
+BWD_REL_FRO = 1e-2
+BWD_MAX_REL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_moe_layer_bias_gb300 as m
+    m.load_library()
+    return m
+
+
+def run_backward(lm, shape, T=None, seed_offset=0):
+    w_host = synth.layer_weights_host(shape)
+    x_host, b_host = synth.activations_host(shape, T=T, seed_offset=seed_offset)
+    T = x_host.shape[0]
+    dy_host = synth.grad_output_host(shape, T=T, seed_offset=seed_offset)
+    w = {k: v.cuda() for k, v in w_host.items()}
+    x, bias, dy = x_host.cuda(), b_host.cuda(), dy_host.cuda()
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    dx, grads = lm.lmoe_backward(h, x, dy, ws)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    lay = lm.lmoe_workspace_layout(h, T)
+    idx = ws_view(ws, lay, "topk_idx", torch.int32, (T, shape.top_k)).cpu().numpy()
+    return dict(h=h, ws=ws, x_host=x_host, dy_host=dy_host, w_host=w_host, idx=idx, dx=dx, grads=grads)
+
+
+def compare(name, gpu, ref):
+    assert np.all(np.isfinite(gpu)), name
+    rf = rel_fro(gpu, ref)
+    mx = float(np.max(np.abs(gpu - ref)) / max(np.max(np.abs(ref)), 1e-300))
+    assert rf <= BWD_REL_FRO and mx <= BWD_MAX_REL, (name, rf, mx)
+    return rf
+
+
+def check_backward(shape, run):
+    cfg = oracle_cfg(shape)
+    wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
+    ref = oracle.layer_backward(cfg, synth.bits(run["x_host"]), wb, run["idx"], synth.bits(run["dy_host"]))
+    errs = {"x": compare("x", dec(host_bits(run["dx"])), ref["x"])}
+    for name in oracle.BACKWARD_GRADS:
+        errs[name] = compare(name, run["grads"][name].cpu().double().numpy(), ref[name])
+    return errs
+
+
+def test_backward_tiny(lm):
+    shape = synth.TINY
+    check_backward(shape, run_backward(lm, shape))
+
+
+@pytest.mark.parametrize("T", [1, 37, 129])
+def test_backward_tiny_ragged(lm, T):
+    shape = synth.TINY
+    check_backward(shape, run_backward(lm, shape, T=T, seed_offset=T))
+
+
+def test_backward_small(lm):
+    # several tiles of every GEMM and a ragged token count
+    shape = synth.SMALL
+    check_backward(shape, run_backward(lm, shape, T=1000))
+
+
+def test_backward_is_deterministic(lm):
+    shape = synth.TINY
+    run = run_backward(lm, shape)
+    x, dy = run["x_host"].cuda(), run["dy_host"].cuda()
+    dx2, g2 = lm.lmoe_backward(run["h"], x, dy, run["ws"])
+    torch.cuda.synchronize()
+    assert torch.equal(run["dx"], dx2)
+    for n, t in run["grads"].items():
+        assert torch.equal(t, g2[n]), n
+
+
+def test_backward_unused_experts_get_zero(lm):
+    # few tokens: most of the 32 experts are chosen by none
+    shape = synth.TINY
+    run = run_backward(lm, shape, T=3, seed_offset=5)
+    used = set(run["idx"].reshape(-1).tolist())
+    unused = [e for e in range(shape.n_experts) if e not in used]
+    assert unused
+    for n in ("w1", "w2", "w3", "w_router"):
+        g = run["grads"][n].cpu()
+        for e in unused:
+            assert not torch.any(g[e] != 0), (n, e)
+
+
+def test_backward_needs_a_backward_handle(lm):
+    shape = synth.TINY
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, bias = (t.cuda() for t in synth.activations_host(shape, T=8))
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=8)
+    ws = lm.alloc_workspace(h, 8)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    with pytest.raises(lm.LmoeError) as e:
+        lm.lmoe_backward(h, x, torch.zeros_like(x), ws, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+
+
+def test_backward_k3_prefill_sampled(lm):
+    """K3 prefill (T = 8192) in the configuration the benchmark times: dx on
+    sampled tokens (outlier tokens included) against the oracle, which is
+    exact per token because dx_t depends on x_t and dy_t alone; dW_up and
+    dWs3 on sampled columns against their definition sum_t dy_t r_t^T and
+    sum_t dy_t as_t^T on the forward's own r and shared activations; every
+    gradient finite."""
+    shape = synth.K3_PREFILL
+    T, K, L = shape.T, shape.top_k, shape.latent
+    S = shape.n_shared * shape.shared_inter
+    torch.manual_seed(0)
+    w = synth.layer_weights_device(shape)
+    x, bias = synth.activations_device(shape)
+    dy = synth.grad_output_device(shape)
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    dx, grads = lm.lmoe_backward(h, x, dy, ws)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    lay = lm.lmoe_workspace_layout(h, T)
+    idx = ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).cpu().numpy()
+    for n, g in grads.items():
+        assert bool(torch.isfinite(g).all()), n
+    assert bool(torch.isfinite(dx.float()).all())
+
+    rng = np.random.default_rng(3)
+    big = torch.nonzero(x.float().abs().amax(dim=1) > 20).flatten().cpu().numpy()   # outlier tokens
+    sample = np.unique(np.concatenate([rng.choice(T, 5, replace=False), big[:1]]))
+    cfg = oracle_cfg(shape)
+    dense = {n: synth.bits(w[n]) for n in ("w_down", "w_router", "ws1", "ws2", "ws3", "w_up")}
+    used = np.unique(idx[sample])
+    wb = dict(dense)
+    for n in ("w1", "w2", "w3"):
+        wb[n] = {int(e): synth.bits(w[n][int(e)]) for e in used}
+    sm = torch.from_numpy(sample).cuda()
+    ref = oracle.layer_backward(cfg, host_bits(x[sm]), wb, idx[sample], host_bits(dy[sm]), weight_grads=False)
+    compare("x (sampled tokens)", dec(host_bits(dx[sm])), ref["x"])
+
+    # dW_up and dWs3 on sampled columns, in fp64 on the host from the
+    # forward's own bf16 r and shared activations
+    dyd = dec(host_bits(dy))
+    cols = np.sort(rng.choice(L, 24, replace=False))
+    r = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))[:, cols]
+    compare("w_up (sampled columns)", grads["w_up"].cpu().double().numpy()[:, cols], dyd.T @ r)
+    scols = np.sort(rng.choice(S, 24, replace=False))
+    a_s = dec(host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))))[:, scols]
+    compare("ws3 (sampled columns)", grads["ws3"].cpu().double().numpy()[:, scols], dyd.T @ a_s)

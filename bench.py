@@ -94,6 +94,39 @@ def layer_work(shape, T, counts, fp8=False):
     return w
 
 
+def backward_work(shape, T, counts):
+    """Algorithmic FLOPs and bytes of each backward stage for T tokens with
+    per-expert assignment counts `counts` (bf16 2 bytes, fp32 4 bytes; weight
+    gradients are written in fp32).  The routed and shared SiTU-GLU stages
+    recompute their pre-activations (counted in their FLOPs)."""
+    d, L, E, k, I = shape.d, shape.latent, shape.n_experts, shape.top_k, shape.inter
+    S = shape.n_shared * shape.shared_inter
+    counts = np.asarray(counts)
+    n = T * k
+    Ep = -(-E // 64) * 64
+    touched = int((counts > 0).sum())
+    cols = int(((counts + 63) // 64 * 64).sum())      # per-expert segments, padded to 64
+    nq = I // 128 if I % 128 == 0 else I // 64         # SiTU-GLU tiles per expert row
+    dense = d * L + d * S + 2 * S * d + L * d + E * L  # elements of the six dense weight gradients
+    w = {}
+    w["dr"] = (2.0 * T * d * (L + S), 2.0 * (T * d + (L + S) * d + T * (L + S)))
+    w["shared"] = (4.0 * T * d * S, 2.0 * (T * d + 2 * S * d + T * S + 2 * T * S))
+    w["rmsnorm"] = (0.0, 2.0 * (n * L + T * L + T * L))
+    w["expert_u"] = (2.0 * n * L * I, 2.0 * (touched * I * L + T * L + n * I))
+    w["expert_glu"] = (4.0 * n * L * I, 2.0 * (touched * 2 * I * L + T * L + n * I + 2 * n * I) + 4.0 * n * nq)
+    w["router"] = (2.0 * n * L, 2.0 * (T * L + E * L + T * Ep) + 4.0 * n * nq + 8.0 * n)
+    w["dh_experts"] = (4.0 * n * I * L, 2.0 * (touched * 2 * I * L + 2 * n * I + n * L))
+    w["dh_router"] = (2.0 * T * Ep * L, 2.0 * (T * Ep + L * Ep) + 4.0 * T * L)
+    w["dh_sum"] = (0.0, 2.0 * n * L + 4.0 * T * L + 2.0 * T * L)
+    w["dx"] = (2.0 * T * (L + 2 * S) * d, 2.0 * (T * (L + 2 * S) + d * (L + 2 * S) + T * d))
+    w["transpose"] = (0.0, 4.0 * T * (2 * d + 3 * L + 3 * S + E))
+    w["wgrad_dense"] = (2.0 * T * dense, 2.0 * T * (2 * d + 3 * L + 3 * S + E) + 4.0 * dense)
+    w["segments"] = (0.0, 2.0 * cols * (2 * L + 3 * I) + 2.0 * n * (2 * L + 3 * I) + 12.0 * (E - touched) * I * L)
+    w["wgrad_w3"] = (2.0 * n * L * I, 4.0 * touched * L * I + 2.0 * cols * (L + I))
+    w["wgrad_w12"] = (4.0 * n * I * L, 8.0 * touched * I * L + 2.0 * cols * (2 * I + L))
+    return w
+
+
 def layer_flops_per_token(shape):
     d, L, k, I = shape.d, shape.latent, shape.top_k, shape.inter
     S = shape.n_shared * shape.shared_inter
@@ -308,6 +341,80 @@ def fp8_experts_variant(lm, stream, steps, warmup, shape, w, x, bias, dshape, wd
         out[name] = r
         del h8, ws8
         torch.cuda.empty_cache()
+    return out
+
+
+def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src):
+    """The layer's backward at the K3 prefill shape: dx and the fp32 weight
+    gradients for an upstream gradient dy ~ N(0, 1), after one forward of the
+    same batch.  Timed over `steps` backward passes (weights and activations
+    exceed L2), then once more per stage with the timing hook."""
+    T = shape.T
+    hb = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(hb, T)
+    bws = torch.empty(lm.lmoe_backward_workspace_size(hb, T), dtype=torch.uint8, device="cuda")
+    grads = {n: torch.empty(sz, dtype=torch.float32, device="cuda") for n, sz in lm.grad_shapes(hb).items()}
+    dy = synth.grad_output_device(shape)
+    dx = torch.empty_like(x)
+    counts = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
+    lm.lmoe_forward(hb, x, bias, workspace=ws, expert_counts_out=counts, stream=stream)
+
+    def bstep():
+        lm.lmoe_backward(hb, x, dy, ws, dx=dx, grads=grads, workspace=bws, expert_counts=counts, stream=stream)
+
+    for _ in range(warmup):
+        bstep()
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(hb) == 0
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(steps):
+        bstep()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    ms = b0.elapsed_time(b1) / steps
+    nst = len(lm.BWD_STAGES)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    for evs in ev_sets:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for evs in ev_sets:
+        lm.lmoe_set_backward_events(hb, evs)
+        bstep()
+    torch.cuda.synchronize()
+    lm.lmoe_set_backward_events(hb, None)
+    assert lm.lmoe_device_status(hb) == 0
+    counts_host = counts.cpu().numpy()
+    work = backward_work(shape, T, counts_host)
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    stage_ms = {nm: float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in ev_sets]))
+                for j, nm in enumerate(lm.BWD_STAGES)}
+    stages = {}
+    for nm in lm.BWD_STAGES:
+        fl, by = work[nm]
+        t = stage_ms[nm] * 1e-3
+        bound = "tensor" if (fl > 0 and fl / by > ridge) else "hbm"
+        if bound == "tensor":
+            ach, peak, unit = fl / t / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        else:
+            ach, peak, unit = by / t / 1e9, peaks["hbm_gbs"], "GB/s"
+        stages[nm] = {"ms": round(stage_ms[nm], 4), "bound": bound, "achieved": round(ach, 2), "peak": peak,
+                      "unit": unit, "frac": round(ach / peak, 4), "share": round(stage_ms[nm] / ms, 4)}
+    dom = max(lm.BWD_STAGES, key=lambda nm: stage_ms[nm])
+    roof = {k: v for k, v in stages[dom].items() if k not in ("ms", "share")}
+    roof.update(kernel="backward_" + dom, per_launch={"flop": work[dom][0], "bytes": work[dom][1]}, traffic=None,
+                peak_source=peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " hbm copy"))
+    model_flop = 2.0 * layer_flops_per_token(shape) * T      # data + weight gradients of every GEMM
+    executed = sum(v[0] for v in work.values())
+    out = {"T": T, "ms": round(ms, 4), "tokens_per_s": T / (ms * 1e-3),
+           "model_tflops": round(model_flop / (ms * 1e-3) / 1e12, 2),
+           "frac_bf16_peak": round(model_flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+           "executed_tflop": round(executed / 1e12, 3), "weight_grad_dtype": "f32",
+           "roofline": roof, "stages": stages,
+           "gpu_launches_per_pass": 37}
+    del hb, ws, bws, grads, dy, dx
+    torch.cuda.empty_cache()
     return out
 
 
@@ -631,6 +738,9 @@ def main():
     # --------------------------------------------------------------- FP8 expert variant
     fp8 = fp8_experts_variant(lm, stream, args.steps, args.warmup, shape, w, x, bias, dshape, wd, xd, bd, peaks)
 
+    # --------------------------------------------------------------- backward pass
+    bwd = backward_pass(lm, stream, args.steps, args.warmup, shape, w, x, bias, peaks, peak_src)
+
     # --------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -660,6 +770,7 @@ def main():
         "qb_hist_sweep_all": sweep,
         "qb_closed_loop": qb_loop,
         "fp8_experts": fp8,
+        "backward": bwd,
         "decode": {"T": dshape.T, "ms": round(dec_ms, 4), "tokens_per_s": dshape.T / (dec_ms * 1e-3),
                    "touched_experts": touched_d, "bytes": dec_bytes, "gbs": round(dec_gbs, 1),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},

@@ -295,6 +295,31 @@ int lmoe_backward(lmoe_handle *handle, const uint16_t *x, int64_t T, const uint1
                   uint16_t *dx, const lmoe_grads *grads, void *workspace, size_t workspace_bytes,
                   cudaStream_t stream);
 
+/* Stages of lmoe_backward, in launch order (for lmoe_set_backward_events). */
+typedef enum {
+    LMOE_BWD_STAGE_DR = 0,          /* dr | da_s = dy [W_up | Ws3]                        */
+    LMOE_BWD_STAGE_SHARED = 1,      /* shared experts: SiTU-GLU backward (recomputed)    */
+    LMOE_BWD_STAGE_RMSNORM = 2,     /* RMSNorm backward: dz                              */
+    LMOE_BWD_STAGE_EXPERT_U = 3,    /* u = W3[e]^T dz per assignment (two launches)       */
+    LMOE_BWD_STAGE_EXPERT_GLU = 4,  /* routed SiTU-GLU backward (recomputed; two launches) */
+    LMOE_BWD_STAGE_ROUTER = 5,      /* gate and logit gradients                          */
+    LMOE_BWD_STAGE_DH_EXPERTS = 6,  /* experts' share of dh                              */
+    LMOE_BWD_STAGE_DH_ROUTER = 7,   /* router's share of dh                              */
+    LMOE_BWD_STAGE_DH_SUM = 8,      /* dh                                                */
+    LMOE_BWD_STAGE_DX = 9,          /* dx                                                */
+    LMOE_BWD_STAGE_TRANSPOSE = 10,  /* token-major copies for the dense weight gradients */
+    LMOE_BWD_STAGE_WGRAD_DENSE = 11, /* six dense weight gradients                       */
+    LMOE_BWD_STAGE_SEGMENTS = 12,   /* per-expert segments, their copies, unused experts */
+    LMOE_BWD_STAGE_WGRAD_W3 = 13,   /* routed experts' dW3                               */
+    LMOE_BWD_STAGE_WGRAD_W12 = 14,  /* routed experts' dW1 | dW2                         */
+    LMOE_BWD_NUM_STAGES = 15
+} lmoe_bwd_stage;
+
+/* Timing hook of lmoe_backward, as lmoe_set_stage_events for the forward:
+ * n_events == LMOE_BWD_NUM_STAGES + 1 events recorded before each stage and
+ * after the last; NULL / 0 turns it off. */
+int lmoe_set_backward_events(lmoe_handle *handle, cudaEvent_t *events, int n_events);
+
 /* Routing without caller scratch: the biased top-k (a3) and the stable
  * grouping of assignments by expert (a4) of lmoe_forward, for callers that
  * cannot allocate device memory -- e.g. an inference-engine plugin given no

@@ -26,6 +26,8 @@ from .binding import (  # noqa: F401
     lmoe_selftest_timeout,
     lmoe_set_stage_events,
     STAGES,
+    BWD_STAGES,
+    lmoe_set_backward_events,
     lmoe_status_string,
     lmoe_workspace_layout,
     lmoe_workspace_size,

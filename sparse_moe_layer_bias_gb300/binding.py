@@ -21,12 +21,16 @@ STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED_SHAP
 
 EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size",
             "lmoe_workspace_layout", "lmoe_forward", "lmoe_host_io_size", "lmoe_forward_host",
-            "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_route_static",
+            "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_set_backward_events",
+            "lmoe_route_static",
             "lmoe_selftest_timeout", "lmoe_backward_workspace_size", "lmoe_backward", "qb_histogram",
             "qb_quantile_bias", "qb_sign_update")
 
 STAGES = ("down", "shared", "router", "topk", "scan", "offsets", "scatter", "expert_w12_light",
           "expert_w12_heavy", "expert_w3", "combine", "up")
+
+BWD_STAGES = ("dr", "shared", "rmsnorm", "expert_u", "expert_glu", "router", "dh_experts", "dh_router", "dh_sum",
+              "dx", "transpose", "wgrad_dense", "segments", "wgrad_w3", "wgrad_w12")
 
 
 class LmoeError(RuntimeError):
@@ -105,6 +109,8 @@ def load_library():
     lib.lmoe_device_status.argtypes = [P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.lmoe_set_stage_events.restype = ctypes.c_int
     lib.lmoe_set_stage_events.argtypes = [P, P, ctypes.c_int]
+    lib.lmoe_set_backward_events.restype = ctypes.c_int
+    lib.lmoe_set_backward_events.argtypes = [P, P, ctypes.c_int]
     lib.lmoe_route_static.restype = ctypes.c_int
     lib.lmoe_route_static.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P]
     lib.qb_histogram.restype = ctypes.c_int
@@ -345,6 +351,22 @@ def lmoe_set_stage_events(handle: Handle, events):
     handle._event_array = arr  # the library keeps the pointer
     handle._events = list(events)
     _check("lmoe_set_stage_events", lib.lmoe_set_stage_events(handle.ptr, arr, len(events)))
+
+
+def lmoe_set_backward_events(handle: Handle, events):
+    """As lmoe_set_stage_events, for the backward's len(BWD_STAGES) + 1 events."""
+    lib = load_library()
+    if events is None:
+        handle._bwd_event_array = None
+        _check("lmoe_set_backward_events", lib.lmoe_set_backward_events(handle.ptr, None, 0))
+        return
+    for e in events:
+        if not e.cuda_event:
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    handle._bwd_event_array = arr  # the library keeps the pointer
+    handle._bwd_events = list(events)
+    _check("lmoe_set_backward_events", lib.lmoe_set_backward_events(handle.ptr, arr, len(events)))
 
 
 def lmoe_device_status(handle: Handle, clear: bool = True, stream=None) -> int:

@@ -27,23 +27,30 @@ constexpr int kTT = 64;  // transpose tile: 64 x 64 elements
 // out[b][c][q] = scale(q) * in[b][src(q)][c] for c < C, q < Q, where
 // src(q) = qsrc[q] (or q when q < R without qsrc) and a negative src gives 0.
 // Tiles whose first q is at or past *q_limit are skipped (never read later).
+// 16-byte accesses on both sides: a thread loads 8 columns of one source row
+// and stores 8 consecutive q of one output row.  The shared tile is stored
+// with its 16-byte chunks XOR-swizzled by (q / 8) % 8 so that the column reads
+// of the store phase spread over the banks.  Requires ldi, ldo, the batch
+// strides and the pointers to be multiples of 8 elements (16 bytes).
+__device__ __forceinline__ int swz(int q, int c) { return q * kTT + ((((c >> 3) ^ (q >> 3)) & 7) << 3) + (c & 7); }
+
 __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restrict__ in, int64_t ldi, int64_t ibs,
                                                         int64_t R, int C, uint16_t *__restrict__ out, int64_t ldo,
                                                         int64_t obs, int64_t Q, const int32_t *__restrict__ qsrc,
                                                         const float *__restrict__ qscale,
                                                         const int32_t *__restrict__ q_limit) {
     grid_dependency_wait();
-    __shared__ uint16_t tile[kTT][kTT + 2];
+    __shared__ __align__(16) uint16_t tile[kTT * kTT];
     const int64_t q0 = int64_t(blockIdx.x) * kTT;
     const int c0 = blockIdx.y * kTT;
     const int64_t b = blockIdx.z;
     if (q_limit && q0 >= *q_limit) return;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    const int chunk = threadIdx.x & 7, r8 = threadIdx.x >> 3;   // 8 chunks x 32 rows
     const uint16_t *inb = in + b * ibs;
     uint16_t *outb = out + b * obs;
 #pragma unroll
-    for (int i = 0; i < kTT / 8; ++i) {
-        const int qq = ty + 8 * i;
+    for (int i = 0; i < 2; ++i) {
+        const int qq = r8 + 32 * i;
         const int64_t q = q0 + qq;
         int64_t src = -1;
         float sc = 1.0f;
@@ -51,29 +58,45 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restri
             src = qsrc ? qsrc[q] : (q < R ? q : -1);
             if (qscale && src >= 0) sc = qscale[q];
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int cc = tx + 32 * h;
-            const int c = c0 + cc;
-            uint16_t v = 0;
-            if (src >= 0 && c < C) {
-                v = inb[src * ldi + c];
-                if (qscale) v = f_to_bf16(sc * bf16_to_f(v));
+        const int c = c0 + chunk * 8;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (src >= 0) {
+            const uint16_t *p = inb + src * ldi + c;
+            if (c + 8 <= C) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(p);
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            } else {
+                for (int e = 0; e < 8; ++e)
+                    if (c + e < C) w[e >> 1] |= uint32_t(p[e]) << (16 * (e & 1));
             }
-            tile[qq][cc] = v;
+            if (qscale) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint16_t lo = f_to_bf16(sc * bf16_to_f(uint16_t(w[e] & 0xffffu)));
+                    const uint16_t hi = f_to_bf16(sc * bf16_to_f(uint16_t(w[e] >> 16)));
+                    w[e] = uint32_t(lo) | (uint32_t(hi) << 16);
+                }
+            }
         }
+        *reinterpret_cast<uint4 *>(&tile[swz(qq, chunk * 8)]) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kTT / 8; ++i) {
-        const int cc = ty + 8 * i;
+    for (int i = 0; i < 2; ++i) {
+        const int cc = r8 + 32 * i;
         const int c = c0 + cc;
         if (c >= C) continue;
+        const int64_t q = q0 + chunk * 8;
+        uint32_t w[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int qq = tx + 32 * h;
-            const int64_t q = q0 + qq;
-            if (q < Q) outb[int64_t(c) * ldo + q] = tile[qq][cc];
+        for (int e = 0; e < 4; ++e)
+            w[e] = uint32_t(tile[swz(chunk * 8 + 2 * e, cc)]) | (uint32_t(tile[swz(chunk * 8 + 2 * e + 1, cc)]) << 16);
+        uint16_t *p = outb + int64_t(c) * ldo + q;
+        if (q + 8 <= Q) {
+            *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            for (int e = 0; e < 8; ++e)
+                if (q + e < Q) p[e] = uint16_t(w[e >> 1] >> (16 * (e & 1)));
         }
     }
 }
@@ -369,7 +392,7 @@ cudaError_t launch_segments(const int32_t *counts, const int32_t *offsets, const
 
 cudaError_t launch_zero_unused(const int32_t *counts, int E, int64_t per_expert, float *g1, float *g2, float *g3,
                                cudaStream_t stream) {
-    return launch_kernel(zero_unused_kernel, dim3(E, 8), dim3(256), 0, stream, true, counts, per_expert, g1, g2, g3);
+    return launch_kernel(zero_unused_kernel, dim3(E, 64), dim3(256), 0, stream, true, counts, per_expert, g1, g2, g3);
 }
 
 cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps, const uint16_t *dr, int64_t ld_dr,

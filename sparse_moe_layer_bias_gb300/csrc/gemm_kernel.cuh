@@ -49,13 +49,15 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;  // two accumulators of up to 256 fp32 columns
 constexpr int kAccStride = 256;
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool KSEG = false>
 struct Cfg {
     static constexpr int kSub = PAIR ? 2 : 1;           // 128-row sub-tiles per tile
     static constexpr int kABytes = kSub * kBM * kBK * 2; // 16 or 32 KB
     static constexpr int kBBytes = BN * kBK * 2;        // 16 or 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
+    // K segments are a few K blocks long: 3 stages leave room for the
+    // epilogue's TMA-store buffers
+    static constexpr int kStages = KSEG ? 3 : (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
     static constexpr int kBarBytes = 256;
     // per epilogue warp: 32 rows x 64 bf16, row pitch 144 B (16 B of padding
     // keeps the 16-byte row writes and the 128-byte row reads conflict-free)
@@ -64,8 +66,15 @@ struct Cfg {
     // per epilogue warp: the current tile's per-column scale factors (e4m3
     // epilogues; up to 256 fp32)
     static constexpr int kColWarpBytes = 1024;
+    // K segments (fp32 weight gradients): per epilogue warp two 4 KB buffers
+    // of a 32 x 32 fp32 block in the 128B-swizzled layout of a TMA store,
+    // 1024-byte aligned
+    static constexpr size_t kTmaStgOffset =
+        (size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes + 1023) / 1024 * 1024;
+    static constexpr int kTmaStgWarpBytes = 2 * 4096;
     static constexpr size_t kSmem =
-        1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes;
+        KSEG ? 1024 + kTmaStgOffset + 4 * kTmaStgWarpBytes
+             : 1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes;
 };
 
 struct Tile {
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const GemmArgs args) {
-    using C = Cfg<BN, PAIR>;
+    using C = Cfg<BN, PAIR, KSEG>;
     constexpr int S = C::kStages;
     constexpr int H = BN / 2;  // GLU: features per tile
     constexpr int NSUB = C::kSub;
@@ -432,6 +441,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                                                   (warp - 2) * C::kColWarpBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t n_tma_stores = 0;   // K segments: TMA stores issued by this warp
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED, KSEG>(args, t, n_m);
             // Per-row metadata of this thread's rows (destination row, gate,
@@ -518,21 +528,47 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         store_f32_32(outf + orow * args.ld_out + col, v, static_cast<int>(args.out_cols - col));
                     }
                 }
-            } else if (EPI == EPI_F32) {
-                // fp32 rows (weight gradients): staged like the scores above.
-                // Each thread's destination row pointer: the dense output row,
-                // or with K segments row r of expert e's block, in out
-                // (r < m_split) or out2.
-                const int64_t r = ti.row0 + trow;
-                float *dst;
-                if (KSEG) {
-                    dst = (r < args.m_split)
-                              ? reinterpret_cast<float *>(args.out) + (int64_t(ti.expert) * args.m_split + r) * args.ld_out
-                              : reinterpret_cast<float *>(args.out2) +
-                                    (int64_t(ti.expert) * (args.m_rows - args.m_split) + (r - args.m_split)) * args.ld_out;
-                } else {
-                    dst = reinterpret_cast<float *>(args.out) + r * args.ld_out;
+            } else if (EPI == EPI_F32 && KSEG) {
+                // K segments (the experts' fp32 weight gradients): each warp
+                // writes its 32 rows in 32 x 32 blocks by TMA store, through
+                // two swizzled 4 KB buffers, so the stores run asynchronously.
+                // Rows of the expert's block below m_split go to the map in
+                // tmA1 (out), the others to tmB1 (out2); m_split and the block
+                // heights are multiples of 32, so a warp's rows are all valid
+                // or all absent, and all in one output.
+                uint8_t *tbuf = smem + C::kTmaStgOffset + (warp - 2) * C::kTmaStgWarpBytes;
+                const int rblk = ti.row0 + q * 32;
+                const bool rows_ok = q * 32 < ti.nrows;
+                const bool first = rblk < args.m_split;
+                const CUtensorMap *om = first ? &tmA1 : &tmB1;
+                const int32_t y = first ? ti.expert * args.m_split + rblk
+                                        : ti.expert * (args.m_rows - args.m_split) + (rblk - args.m_split);
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c, v);       // warp-collective: all lanes
+                    const int col = ti.nt * BN + c;
+                    if (rows_ok && col < args.out_cols) {   // warp-uniform
+                        uint8_t *buf = tbuf + (n_tma_stores & 1) * 4096;
+                        if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(om, smem_u32(buf), col, y);
+                            bulk_commit();
+                        }
+                        ++n_tma_stores;
+                    }
                 }
+            } else if (EPI == EPI_F32) {
+                // fp32 rows (dense weight gradients, the router's share of the
+                // latent gradient): staged like the scores above
+                float *dst = reinterpret_cast<float *>(args.out) + int64_t(ti.row0 + trow) * args.ld_out;
                 const bool vec_ok = (args.ld_out % 4) == 0;
                 const unsigned long long dbits = reinterpret_cast<unsigned long long>(dst);
 #pragma unroll 1
@@ -716,6 +752,11 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 acc_phase ^= 1u;
             }
         }
+        // TMA stores read this CTA's shared memory: finish them before exit
+        if (KSEG) {
+            if (lane == 0) bulk_wait<0>();
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
@@ -727,7 +768,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR = false, bool KSEG = false>
 cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t st, bool dependent) {
     auto kern = gemm_kernel<BN, AM, BMD, EPI, GROUPED, PAIR, KSEG>;
-    const size_t smem = Cfg<BN, PAIR>::kSmem;
+    const size_t smem = Cfg<BN, PAIR, KSEG>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(grid), dim3(threads_for(AM)), smem, st, dependent, m.a0, m.a1, m.b0, m.b1, a);

@@ -125,7 +125,10 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
 // (grouped, A and B dense): `tiles` holds {expert, first K block, K blocks,
 // first row of the expert's output block} per 128-row tile, both operands are
 // K-major over one shared column space in which each expert owns a segment,
-// and m_rows is the height of an expert's output block.
+// m_rows is the height of an expert's output block, and the fp32 output goes
+// out by TMA store through maps.a1 (rows of the block below m_split; the map
+// covers [E * m_split][out_cols]) and maps.b1 (the other rows): fp32 maps with
+// 32 x 32 boxes and 128-byte swizzle (m_split and m_rows multiples of 32).
 cudaError_t launch_gemm_bwd(int bn, AMode am, BMode bm, Epi epi, bool grouped, bool kseg, const GemmMaps &maps,
                             const GemmArgs &args, int grid, cudaStream_t stream);
 

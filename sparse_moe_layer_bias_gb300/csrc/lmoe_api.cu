@@ -29,6 +29,7 @@ struct lmoe_handle {
     uint16_t *w1p, *w2p, *w3p;
     int8_t *w1e, *w2e, *w3e;
     cudaEvent_t *stage_events;  // optional timing hook (LMOE_NUM_STAGES + 1 events)
+    cudaEvent_t *bwd_events;    // optional timing hook of the backward (LMOE_BWD_NUM_STAGES + 1)
     // lmoe_forward_host: input / output copy streams and, per staging slot, the
     // events "input landed", "forward done" and "output copied".
     cudaStream_t io_in, io_out;
@@ -82,6 +83,19 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uin
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D fp32 row-major [rows][cols] (row stride ld elements) as a TMA store
+// target: 32 x 32 boxes (128-byte rows, 128B swizzle).
+bool make_store_map_f32(CUtensorMap *m, void *ptr, uint64_t rows, uint64_t cols, uint64_t ld) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 4};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -793,7 +807,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     const float *gates = gates_in ? gates_in : reinterpret_cast<const float *>(fw + fl.gates);
     const int32_t *counts = counts_in ? counts_in : reinterpret_cast<const int32_t *>(fw + fl.counts);
     const int32_t *offsets = reinterpret_cast<const int32_t *>(fw + fl.offsets);
-    const int4 *tiles = reinterpret_cast<const int4 *>(fw + fl.tiles);
+    const int4 *tiles = reinterpret_cast<const int4 *>(fw + fl.tiles);     // 128-row tiles, every expert
     const int32_t *nmt = reinterpret_cast<const int32_t *>(fw + fl.nmt);
     const int32_t *perm = reinterpret_cast<const int32_t *>(fw + fl.perm);
     const int32_t *inv = reinterpret_cast<const int32_t *>(fw + fl.inv);
@@ -841,6 +855,10 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     int st;
     const int64_t grouped_tiles = ceil_div(n, kBM) + E;   // bound on the forward's 128-row tile list
 
+    auto mark = [&](int stage) {
+        if (h->bwd_events) cudaEventRecord(h->bwd_events[stage], stream);
+    };
+    mark(LMOE_BWD_STAGE_DR);
     if (!ok(launch_fill(ones, n, 1.0f, stream))) return LMOE_ERR_CUDA;
     {   // dr | da_s = dy [W_up | Ws3]
         GemmMaps m{m_dy, m_dy, h->m_t_ups3, h->m_t_ups3};
@@ -856,6 +874,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                      grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_STAGE_SHARED);
     {   // shared experts: dp_s = SiTU-GLU backward of the recomputed x Ws1^T | x Ws2^T
         GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
         GemmArgs a = base_args(h);
@@ -873,8 +892,10 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_STAGE_RMSNORM);
     // RMSNorm backward: dz
     if (!ok(launch_rms_bwd(obuf, T, Ki, Li, c.rms_eps, drs, L + S, dz, stream))) return LMOE_ERR_CUDA;
+    mark(LMOE_BWD_STAGE_EXPERT_U);
     {   // u = W3[e]^T dz for every assignment (dz rows gathered by token), permuted order
         GemmMaps m{h->m_t_w3, h->m_t_w3, h->m_t_w3, h->m_t_w3};
         GemmArgs a = base_args(h);
@@ -884,16 +905,19 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.gather_src = dz;
         a.gather_rows = tokrow;
         a.gather_ld = L;
-        a.tiles = tiles;
-        a.n_mtiles = nmt;
         a.out = u;
         a.ld_out = I;
         a.out_cols = static_cast<int32_t>(I);
+        // 128-row tiles for every expert (pair tiles, which hold the whole
+        // TMEM, measured slower here: their epilogue cannot overlap the MMAs)
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
         st = gemm_status(launch_gemm_bwd(h->bn_u, A_GATHER, B_PLAIN, EPI_BF16, true, false, m, a,
                                          grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
     }
     const int nq = static_cast<int>(I / (h->bn_exp1 / 2));
+    mark(LMOE_BWD_STAGE_EXPERT_GLU);
     {   // routed experts: dp = SiTU-GLU backward of the recomputed W1[e] h | W2[e] h with
         // da = gate * u; partial sums of u * act for the gates' gradient
         GemmMaps m{h->m_w1, h->m_w1, h->m_w1, h->m_w2};
@@ -917,13 +941,17 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.out = dp;
         a.ld_out = 2 * I;
         a.out_cols = static_cast<int32_t>(I);
+        a.tiles = tiles;
+        a.n_mtiles = nmt;
         st = gemm_status(launch_gemm_bwd(h->bn_exp1, A_GATHER, B_GLU, EPI_GLU_BWD, true, false, m, a,
                                          grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_STAGE_ROUTER);
     // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
     if (!ok(launch_router_bwd(dgp, nq, inv, idx, hbuf, h->w.w_router, Li, T, Ki, static_cast<int>(Ep), dl, stream)))
         return LMOE_ERR_CUDA;
+    mark(LMOE_BWD_STAGE_DH_EXPERTS);
     {   // experts' share of dh: W1[e]^T dp1 + W2[e]^T dp2, rows back in assignment order
         GemmMaps m{m_dp, m_dp, h->m_t_w12, h->m_t_w12};
         GemmArgs a = base_args(h);
@@ -941,6 +969,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                      grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_STAGE_DH_ROUTER);
     {   // router's share of dh: dl W_router (fp32)
         GemmMaps m{m_dl, m_dl, h->m_t_wr, h->m_t_wr};
         GemmArgs a = base_args(h);
@@ -955,7 +984,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_STAGE_DH_SUM);
     if (!ok(launch_dh_sum(dhp, dhr, T, Ki, Li, dh, h->num_sms, stream))) return LMOE_ERR_CUDA;
+    mark(LMOE_BWD_STAGE_DX);
     {   // dx = dh W_down + dp_s [Ws1 ; Ws2]  (K split over the two sources)
         GemmMaps m{m_dh, m_dps, h->m_t_wd, h->m_t_ws12};
         GemmArgs a = base_args(h);
@@ -973,6 +1004,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     }
     // ---- weight gradients of the dense weights: K = tokens (transposed operands, zero past T)
     const int64_t Tl = T;
+    mark(LMOE_BWD_STAGE_TRANSPOSE);
     if (!ok(launch_transpose(dy, d, 0, Tl, di, dyT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
         !ok(launch_transpose(x, d, 0, Tl, di, xT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
         !ok(launch_transpose(rbuf, L, 0, Tl, Li, rT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
@@ -995,12 +1027,14 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         return gemm_status(launch_gemm_bwd(bn, A_DENSE, B_PLAIN, EPI_F32, false, false, m, a,
                                            grid_for(int64_t(a.m_tiles) * a.n_tiles), stream));
     };
+    mark(LMOE_BWD_STAGE_WGRAD_DENSE);
     if ((st = wgrad(m_dyT, m_rT, d, L, h->bn_down, g->w_up)) || (st = wgrad(m_dyT, m_sT, d, S, h->bn_s, g->ws3)) ||
         (st = wgrad(m_dps1T, m_xT, S, d, h->bn_up, g->ws1)) || (st = wgrad(m_dps2T, m_xT, S, d, h->bn_up, g->ws2)) ||
         (st = wgrad(m_dhT, m_xT, L, d, h->bn_up, g->w_down)) || (st = wgrad(m_dlT, m_hT, E, L, h->bn_down, g->w_router)))
         return st;
     // ---- weight gradients of the routed experts: K = each expert's own assignments
     const int mt_a = static_cast<int>(L / kBM), mt_b = static_cast<int>(ceil_div(2 * I, kBM));
+    mark(LMOE_BWD_STAGE_SEGMENTS);
     if (!ok(launch_segments(counts, offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
                             mt_b, nkt, stream)) ||
         !ok(launch_zero_unused(counts, Ei, I * L, g->w1, g->w2, g->w3, stream)) ||
@@ -1010,8 +1044,13 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         !ok(launch_transpose(hbuf, L, 0, Tl, Li, hgT, Qmax, 0, Qmax, 1, qtok, nullptr, nkt + 2, stream)) ||
         !ok(launch_transpose(dp, 2 * I, 0, n, 2 * Ii, dpT, Qmax, 0, Qmax, 1, qperm, nullptr, nkt + 2, stream)))
         return LMOE_ERR_CUDA;
+    mark(LMOE_BWD_STAGE_WGRAD_W3);
+    CUtensorMap m_g3, m_g1, m_g2;
+    if (!make_store_map_f32(&m_g3, g->w3, E * L, I, I) || !make_store_map_f32(&m_g1, g->w1, E * I, L, L) ||
+        !make_store_map_f32(&m_g2, g->w2, E * I, L, L))
+        return LMOE_ERR_CUDA;
     {   // dW3[e] = sum over e's assignments of (gate dz) act^T
-        GemmMaps m{m_doT, m_doT, m_aT, m_aT};
+        GemmMaps m{m_doT, m_g3, m_aT, m_g3};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(L);
         a.m_split = static_cast<int32_t>(L);
@@ -1026,8 +1065,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(E * mt_a * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_STAGE_WGRAD_W12);
     {   // dW1[e] | dW2[e] = sum over e's assignments of (dp1 | dp2) h^T
-        GemmMaps m{m_dpT, m_dpT, m_hgT, m_hgT};
+        GemmMaps m{m_dpT, m_g1, m_hgT, m_g2};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(2 * I);
         a.m_split = static_cast<int32_t>(I);
@@ -1042,6 +1082,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(E * mt_b * a.n_tiles), stream));
         if (st) return st;
     }
+    mark(LMOE_BWD_NUM_STAGES);
     return LMOE_OK;
 }
 
@@ -1115,6 +1156,17 @@ int lmoe_set_stage_events(lmoe_handle *h, cudaEvent_t *events, int n_events) {
     }
     if (n_events != LMOE_NUM_STAGES + 1) return LMOE_ERR_INVALID_ARG;
     h->stage_events = events;
+    return LMOE_OK;
+}
+
+int lmoe_set_backward_events(lmoe_handle *h, cudaEvent_t *events, int n_events) {
+    if (!h) return LMOE_ERR_INVALID_ARG;
+    if (events == nullptr && n_events == 0) {
+        h->bwd_events = nullptr;
+        return LMOE_OK;
+    }
+    if (!events || n_events != LMOE_BWD_NUM_STAGES + 1) return LMOE_ERR_INVALID_ARG;
+    h->bwd_events = events;
     return LMOE_OK;
 }
 

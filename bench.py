@@ -360,7 +360,7 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src)
     lm.lmoe_forward(hb, x, bias, workspace=ws, expert_counts_out=counts, stream=stream)
 
     def bstep():
-        lm.lmoe_backward(hb, x, dy, ws, dx=dx, grads=grads, workspace=bws, expert_counts=counts, stream=stream)
+        lm.lmoe_backward(hb, x, dy, ws, dx=dx, grads=grads, workspace=bws, stream=stream)
 
     for _ in range(warmup):
         bstep()
@@ -454,6 +454,8 @@ def run_profile_case(args):
     import __graft_entry__
     __graft_entry__.build()
     import sparse_moe_layer_bias_gb300 as lm
+    if args.backward:
+        return run_profile_backward(args, lm)
     shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="zipf",
                                 expert_fp8=bool(args.fp8))
     w = synth.layer_weights_device(shape)
@@ -482,6 +484,38 @@ def run_profile_case(args):
     return 0
 
 
+def run_profile_backward(args, lm):
+    """A few backward passes of a reduced K3-width layer (E=64, T=1024, k=16:
+    ~256 rows per expert like the K3 prefill batch; ~4.5 GB on the device
+    with the fp32 gradients), for ncu captures.  Not a benchmark result."""
+    import dataclasses
+    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case_backward", T=1024, n_experts=64, router="zipf")
+    w = synth.layer_weights_device(shape)
+    x, bias = synth.activations_device(shape)
+    dy = synth.grad_output_device(shape)
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=shape.T)
+    ws = lm.alloc_workspace(h, shape.T)
+    bws = torch.empty(lm.lmoe_backward_workspace_size(h, shape.T), dtype=torch.uint8, device="cuda")
+    grads = {n: torch.empty(sz, dtype=torch.float32, device="cuda") for n, sz in lm.grad_shapes(h).items()}
+    cnt = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
+    lm.lmoe_forward(h, x, bias, workspace=ws, expert_counts_out=cnt)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            e0.record()
+        dx, _ = lm.lmoe_backward(h, x, dy, ws, grads=grads, workspace=bws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    work = backward_work(shape, shape.T, cnt.cpu().numpy())
+    print(json.dumps({"case": "ncu_case_backward", "T": shape.T, "n_experts": shape.n_experts,
+                      "ms_per_iter": e0.elapsed_time(e1) / max(args.steps, 1),
+                      "touched_experts": int((cnt > 0).sum().item()),
+                      "algorithmic_bytes": {k: v[1] for k, v in work.items()},
+                      "dx_finite": bool(torch.isfinite(dx.float()).all().item())}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
     ap = argparse.ArgumentParser()
@@ -494,6 +528,8 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="small case for ncu captures: K3 widths, 256 experts, T=2048 (~3.3 GB)")
     ap.add_argument("--fp8", action="store_true", help="with --profile-case: the FP8 expert variant")
+    ap.add_argument("--backward", action="store_true",
+                    help="with --profile-case: backward passes of a K3-width layer with 64 experts, T=1024")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()

@@ -282,16 +282,18 @@ int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *b
  * The forward's intermediates are read from fwd_workspace (the workspace of
  * that forward, unchanged since; its layout for T): h, perm, inv, the
  * permuted activations, the rows o, r, the shared activations and the tile
- * lists.  topk_idx, gates, expert_counts: the forward's outputs when the
- * caller had it write them to its own buffers, or NULL for the workspace's
- * copies.  The router's logits of the chosen experts are recomputed from h,
+ * lists, and the offsets of the expert groups (always in the workspace; the
+ * per-expert counts are their differences).  topk_idx, gates: the forward's
+ * outputs when the caller had it write them to its own buffers (they are then
+ * not in the workspace), or NULL for the workspace's copies; an expert id
+ * outside [0, n_experts) contributes no gradient.  The router's logits of the chosen experts are recomputed from h,
  * so that sigma'(logit) = sigma(logit) sigma(-logit) stays accurate where the
  * fp32 score has rounded to 1.  workspace: lmoe_backward_workspace_size(T) bytes,
  * 256-byte aligned.  The handle must have been created with with_backward =
  * 1 (else LMOE_ERR_INVALID_ARG).  T = 0 enqueues nothing. */
 int lmoe_backward(lmoe_handle *handle, const uint16_t *x, int64_t T, const uint16_t *dy,
-                  const int32_t *topk_idx, const float *gates, const int32_t *expert_counts,
-                  const void *fwd_workspace, size_t fwd_workspace_bytes,
+                  const int32_t *topk_idx, const float *gates, const void *fwd_workspace,
+                  size_t fwd_workspace_bytes,
                   uint16_t *dx, const lmoe_grads *grads, void *workspace, size_t workspace_bytes,
                   cudaStream_t stream);
 

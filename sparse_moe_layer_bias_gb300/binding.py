@@ -95,7 +95,7 @@ def load_library():
     lib.lmoe_backward_workspace_size.restype = ctypes.c_int
     lib.lmoe_backward_workspace_size.argtypes = [P, I64, ctypes.POINTER(ctypes.c_size_t)]
     lib.lmoe_backward.restype = ctypes.c_int
-    lib.lmoe_backward.argtypes = [P, P, I64, P, P, P, P, P, ctypes.c_size_t, P, ctypes.POINTER(LmoeGrads), P,
+    lib.lmoe_backward.argtypes = [P, P, I64, P, P, P, P, ctypes.c_size_t, P, ctypes.POINTER(LmoeGrads), P,
                                   ctypes.c_size_t, P]
     lib.lmoe_host_io_size.restype = ctypes.c_int
     lib.lmoe_host_io_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
@@ -259,8 +259,9 @@ def grad_shapes(handle: Handle) -> dict:
 
 def lmoe_backward(handle: Handle, x: torch.Tensor, dy: torch.Tensor, fwd_workspace: torch.Tensor,
                   dx: torch.Tensor | None = None, grads: dict | None = None, workspace: torch.Tensor | None = None,
-                  topk_idx=None, gates=None, expert_counts=None, stream=None):
-    """Backward of the forward that ran on ``x`` with ``fwd_workspace``.
+                  topk_idx=None, gates=None, stream=None):
+    """Backward of the forward that ran on ``x`` with ``fwd_workspace``.  Pass
+    ``topk_idx`` / ``gates`` when that forward wrote them to caller buffers.
     Returns (dx bf16 [T, d], dict of fp32 weight gradients)."""
     lib = load_library()
     x = _dev(x, torch.bfloat16, "x")
@@ -280,8 +281,7 @@ def lmoe_backward(handle: Handle, x: torch.Tensor, dy: torch.Tensor, fwd_workspa
                                 device=x.device)
     workspace = _dev(workspace, torch.uint8, "workspace")
     st = lib.lmoe_backward(handle.ptr, _ptr(x), T, _ptr(dy), _ptr(_dev(topk_idx, torch.int32, "topk_idx")),
-                           _ptr(_dev(gates, torch.float32, "gates")),
-                           _ptr(_dev(expert_counts, torch.int32, "expert_counts")), _ptr(fwd_workspace),
+                           _ptr(_dev(gates, torch.float32, "gates")), _ptr(fwd_workspace),
                            fwd_workspace.numel(), _ptr(dx), ctypes.byref(g), _ptr(workspace), workspace.numel(),
                            _stream(stream))
     _check("lmoe_backward", st)

@@ -106,14 +106,15 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restri
 // lists {expert, first K block, K blocks, first output row} for the experts
 // with at least one assignment: m_tiles_a (resp. b) 128-row tiles each.
 constexpr int kSegThreads = 1024;
-__global__ void __launch_bounds__(kSegThreads) segments_kernel(const int32_t *__restrict__ counts, int E,
+// Each expert's count is offsets[e + 1] - offsets[e] (the forward's scan).
+__global__ void __launch_bounds__(kSegThreads) segments_kernel(const int32_t *__restrict__ offsets, int E,
                                                                int32_t *__restrict__ segoff, int4 *__restrict__ tiles_a,
                                                                int m_tiles_a, int4 *__restrict__ tiles_b, int m_tiles_b,
                                                                int32_t *__restrict__ n_tiles2) {
     grid_dependency_wait();
     __shared__ int32_t s_pad[kSegThreads], s_ne[kSegThreads];
     const int e = threadIdx.x;
-    const int cnt = (e < E) ? counts[e] : 0;
+    const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
     const int pad = (cnt + 63) / 64 * 64;
     s_pad[e] = pad;
     s_ne[e] = cnt > 0 ? 1 : 0;
@@ -147,8 +148,7 @@ __global__ void __launch_bounds__(kSegThreads) segments_kernel(const int32_t *__
 // Column maps of the segments: for column q = segoff[e] + c (c < padded
 // count), qperm = the permuted row offsets[e] + c (or -1 past the count),
 // qtok = that row's token, qgate = its gate.  One block per expert.
-__global__ void __launch_bounds__(256) segment_maps_kernel(const int32_t *__restrict__ counts,
-                                                           const int32_t *__restrict__ offsets,
+__global__ void __launch_bounds__(256) segment_maps_kernel(const int32_t *__restrict__ offsets,
                                                            const int32_t *__restrict__ segoff,
                                                            const int32_t *__restrict__ perm,
                                                            const int32_t *__restrict__ tokrow,
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256) segment_maps_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ qtok, float *__restrict__ qgate) {
     grid_dependency_wait();
     const int e = blockIdx.x;
-    const int cnt = counts[e];
+    const int cnt = offsets[e + 1] - offsets[e];
     const int pad = (cnt + 63) / 64 * 64;
     const int64_t s0 = segoff[e];
     for (int c = threadIdx.x; c < pad; c += blockDim.x) {
@@ -175,12 +175,12 @@ __global__ void __launch_bounds__(256) segment_maps_kernel(const int32_t *__rest
 
 // Zero the routed weight gradients of experts no token chose (the segment
 // GEMMs have no tile for them).  grid (E, chunks).
-__global__ void __launch_bounds__(256) zero_unused_kernel(const int32_t *__restrict__ counts, int64_t per_expert,
+__global__ void __launch_bounds__(256) zero_unused_kernel(const int32_t *__restrict__ offsets, int64_t per_expert,
                                                           float *__restrict__ g1, float *__restrict__ g2,
                                                           float *__restrict__ g3) {
     grid_dependency_wait();
     const int e = blockIdx.x;
-    if (counts[e] != 0) return;
+    if (offsets[e + 1] != offsets[e]) return;
     const int64_t n4 = per_expert / 4;
     float4 *p1 = reinterpret_cast<float4 *>(g1 + int64_t(e) * per_expert);
     float4 *p2 = reinterpret_cast<float4 *>(g2 + int64_t(e) * per_expert);
@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict
                                                          const int32_t *__restrict__ inv,
                                                          const int32_t *__restrict__ idx,
                                                          const uint16_t *__restrict__ h,
-                                                         const uint16_t *__restrict__ wr, int L, int64_t T, int k,
-                                                         int ldl, uint16_t *__restrict__ dl) {
+                                                         const uint16_t *__restrict__ wr, int L, int E, int64_t T,
+                                                         int k, int ldl, uint16_t *__restrict__ dl) {
     grid_dependency_wait();
     const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict
     float my_logit = 0.0f;
     for (int j = 0; j < k; ++j) {
         const int ej = idx[t * k + j];
+        if (ej < 0 || ej >= E) continue;   // not a routing the forward produced: no gradient
         const uint16_t *wrow = wr + int64_t(ej) * L;
         float part = 0.0f;
         for (int c = lane * 8; c < L; c += 256) {
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict
         float dg = 0.0f;
         for (int q = 0; q < nq; ++q) dg += dgp[p * nq + q];
         e = idx[a];
+        if (e < 0 || e >= E) dg = 0.0f;
         const float sp = 1.0f / (1.0f + __expf(-my_logit));
         const float sm = 1.0f / (1.0f + __expf(my_logit));
         v = dg * (sp * sm);
@@ -378,21 +380,21 @@ cudaError_t launch_transpose(const uint16_t *in, int64_t ldi, int64_t in_batch_s
                          out_batch_stride, Q, qsrc, qscale, q_limit);
 }
 
-cudaError_t launch_segments(const int32_t *counts, const int32_t *offsets, const int32_t *perm,
+cudaError_t launch_segments(const int32_t *offsets, const int32_t *perm,
                             const int32_t *tokrow, const float *gates, int E, int32_t *segoff, int32_t *qperm,
                             int32_t *qtok, float *qgate, int4 *tiles_a, int m_tiles_a, int4 *tiles_b,
                             int m_tiles_b, int32_t *n_tiles3, cudaStream_t stream) {
     if (E > kSegThreads) return cudaErrorInvalidValue;
-    cudaError_t e = launch_kernel(segments_kernel, dim3(1), dim3(kSegThreads), 0, stream, true, counts, E, segoff,
+    cudaError_t e = launch_kernel(segments_kernel, dim3(1), dim3(kSegThreads), 0, stream, true, offsets, E, segoff,
                                   tiles_a, m_tiles_a, tiles_b, m_tiles_b, n_tiles3);
     if (e != cudaSuccess) return e;
-    return launch_kernel(segment_maps_kernel, dim3(E), dim3(256), 0, stream, true, counts, offsets,
+    return launch_kernel(segment_maps_kernel, dim3(E), dim3(256), 0, stream, true, offsets,
                          static_cast<const int32_t *>(segoff), perm, tokrow, gates, qperm, qtok, qgate);
 }
 
-cudaError_t launch_zero_unused(const int32_t *counts, int E, int64_t per_expert, float *g1, float *g2, float *g3,
+cudaError_t launch_zero_unused(const int32_t *offsets, int E, int64_t per_expert, float *g1, float *g2, float *g3,
                                cudaStream_t stream) {
-    return launch_kernel(zero_unused_kernel, dim3(E, 64), dim3(256), 0, stream, true, counts, per_expert, g1, g2, g3);
+    return launch_kernel(zero_unused_kernel, dim3(E, 64), dim3(256), 0, stream, true, offsets, per_expert, g1, g2, g3);
 }
 
 cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps, const uint16_t *dr, int64_t ld_dr,
@@ -407,12 +409,12 @@ cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps
 }
 
 cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, const int32_t *idx, const uint16_t *h,
-                              const uint16_t *w_router, int L, int64_t T, int k, int ldl, uint16_t *dl,
+                              const uint16_t *w_router, int L, int E, int64_t T, int k, int ldl, uint16_t *dl,
                               cudaStream_t stream) {
     if (T <= 0) return cudaSuccess;
     const unsigned blocks = static_cast<unsigned>((T * 32 + 255) / 256);
     return launch_kernel(router_bwd_kernel, dim3(blocks), dim3(256), 0, stream, true, dgp, nq, inv, idx, h, w_router,
-                         L, T, k, ldl, dl);
+                         L, E, T, k, ldl, dl);
 }
 
 cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,

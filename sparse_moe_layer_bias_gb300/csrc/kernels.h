@@ -186,16 +186,17 @@ cudaError_t launch_transpose(const uint16_t *in, int64_t ldi, int64_t in_batch_s
                              const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream);
 // Per-expert column segments (assignments padded to 64), their column maps and
 // the segment GEMMs' tile lists; n_tiles3 = {tiles in a, tiles in b, columns}.
-cudaError_t launch_segments(const int32_t *counts, const int32_t *offsets, const int32_t *perm,
+// Counts come from the forward's offsets ([E+1] exclusive scan).
+cudaError_t launch_segments(const int32_t *offsets, const int32_t *perm,
                             const int32_t *tokrow, const float *gates, int E, int32_t *segoff, int32_t *qperm,
                             int32_t *qtok, float *qgate, int4 *tiles_a, int m_tiles_a, int4 *tiles_b,
                             int m_tiles_b, int32_t *n_tiles3, cudaStream_t stream);
-cudaError_t launch_zero_unused(const int32_t *counts, int E, int64_t per_expert, float *g1, float *g2, float *g3,
+cudaError_t launch_zero_unused(const int32_t *offsets, int E, int64_t per_expert, float *g1, float *g2, float *g3,
                                cudaStream_t stream);
 cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps, const uint16_t *dr, int64_t ld_dr,
                            uint16_t *dz, cudaStream_t stream);
 cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, const int32_t *idx, const uint16_t *h,
-                              const uint16_t *w_router, int L, int64_t T, int k, int ldl, uint16_t *dl,
+                              const uint16_t *w_router, int L, int E, int64_t T, int k, int ldl, uint16_t *dl,
                               cudaStream_t stream);
 cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,
                           int num_sms, cudaStream_t stream);

@@ -772,7 +772,7 @@ int lmoe_backward_workspace_size(const lmoe_handle *h, int64_t T, size_t *bytes)
 }
 
 int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *dy, const int32_t *idx_in,
-                  const float *gates_in, const int32_t *counts_in, const void *fwd_workspace,
+                  const float *gates_in, const void *fwd_workspace,
                   size_t fwd_workspace_bytes, uint16_t *dx, const lmoe_grads *g, void *workspace,
                   size_t workspace_bytes, cudaStream_t stream) {
     if (!h || T < 0) return LMOE_ERR_INVALID_ARG;
@@ -787,7 +787,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     for (const void *p : al)
         if (!aligned16(p)) return LMOE_ERR_ALIGNMENT;
     if ((idx_in && !aligned16(idx_in)) || (gates_in && !aligned16(gates_in)) ||
-        (counts_in && !aligned16(counts_in)) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
         (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u))
         return LMOE_ERR_ALIGNMENT;
     const Layout fl = compute_layout(c, T, true, true, true, true);
@@ -805,7 +805,6 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     const uint16_t *hbuf = reinterpret_cast<const uint16_t *>(fw + fl.h);
     const int32_t *idx = idx_in ? idx_in : reinterpret_cast<const int32_t *>(fw + fl.idx);
     const float *gates = gates_in ? gates_in : reinterpret_cast<const float *>(fw + fl.gates);
-    const int32_t *counts = counts_in ? counts_in : reinterpret_cast<const int32_t *>(fw + fl.counts);
     const int32_t *offsets = reinterpret_cast<const int32_t *>(fw + fl.offsets);
     const int4 *tiles = reinterpret_cast<const int4 *>(fw + fl.tiles);     // 128-row tiles, every expert
     const int32_t *nmt = reinterpret_cast<const int32_t *>(fw + fl.nmt);
@@ -949,7 +948,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     }
     mark(LMOE_BWD_STAGE_ROUTER);
     // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
-    if (!ok(launch_router_bwd(dgp, nq, inv, idx, hbuf, h->w.w_router, Li, T, Ki, static_cast<int>(Ep), dl, stream)))
+    if (!ok(launch_router_bwd(dgp, nq, inv, idx, hbuf, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
+                              stream)))
         return LMOE_ERR_CUDA;
     mark(LMOE_BWD_STAGE_DH_EXPERTS);
     {   // experts' share of dh: W1[e]^T dp1 + W2[e]^T dp2, rows back in assignment order
@@ -1035,9 +1035,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     // ---- weight gradients of the routed experts: K = each expert's own assignments
     const int mt_a = static_cast<int>(L / kBM), mt_b = static_cast<int>(ceil_div(2 * I, kBM));
     mark(LMOE_BWD_STAGE_SEGMENTS);
-    if (!ok(launch_segments(counts, offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
+    if (!ok(launch_segments(offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
                             mt_b, nkt, stream)) ||
-        !ok(launch_zero_unused(counts, Ei, I * L, g->w1, g->w2, g->w3, stream)) ||
+        !ok(launch_zero_unused(offsets, Ei, I * L, g->w1, g->w2, g->w3, stream)) ||
         // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's column segment
         !ok(launch_transpose(dz, L, 0, Tl, Li, doT, Qmax, 0, Qmax, 1, qtok, qgate, nkt + 2, stream)) ||
         !ok(launch_transpose(act, I, 0, n, Ii, aT, Qmax, 0, Qmax, 1, qperm, nullptr, nkt + 2, stream)) ||

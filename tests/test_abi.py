@@ -64,7 +64,7 @@ def test_host_entry_points_reject_bad_arguments_without_gpu():
     assert lib.lmoe_forward_host(None, None, 8, None, None, None, None, None, None, None, 0, None, 0,
                                  None) == 1
     lib.lmoe_backward_workspace_size.argtypes = [P, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]
-    lib.lmoe_backward.argtypes = [P, P, ctypes.c_int64, P, P, P, P, P, ctypes.c_size_t, P, P, P,
+    lib.lmoe_backward.argtypes = [P, P, ctypes.c_int64, P, P, P, P, ctypes.c_size_t, P, P, P,
                                   ctypes.c_size_t, P]
     assert lib.lmoe_backward_workspace_size(None, 8, ctypes.byref(n)) == 1
-    assert lib.lmoe_backward(None, None, 8, None, None, None, None, None, 0, None, None, None, 0, None) == 1
+    assert lib.lmoe_backward(None, None, 8, None, None, None, None, 0, None, None, None, 0, None) == 1

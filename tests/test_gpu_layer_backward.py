@@ -173,3 +173,35 @@ def test_backward_k3_prefill_sampled(lm):
     scols = np.sort(rng.choice(S, 24, replace=False))
     a_s = dec(host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))))[:, scols]
     compare("ws3 (sampled columns)", grads["ws3"].cpu().double().numpy()[:, scols], dyd.T @ a_s)
+
+
+def test_backward_with_forward_outputs_in_caller_buffers(lm):
+    """A forward that wrote its routing outputs to caller buffers leaves those
+    workspace slots untouched (here: filled with 0xff bytes); the backward
+    takes topk_idx and gates from the caller and derives the per-expert counts
+    from the workspace's offsets, so it gives the same bits as the default
+    path."""
+    shape = synth.TINY
+    T = 64
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, bias = (t.cuda() for t in synth.activations_host(shape, T=T, seed_offset=9))
+    dy = synth.grad_output_host(shape, T=T, seed_offset=9).cuda()
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    dx_a, g_a = lm.lmoe_backward(h, x, dy, ws)
+    ws2 = lm.alloc_workspace(h, T)
+    ws2.fill_(255)
+    E, K = shape.n_experts, shape.top_k
+    scores = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    lm.lmoe_forward(h, x, bias, workspace=ws2, scores_out=scores, topk_idx_out=idx, gates_out=gates,
+                    expert_counts_out=counts)
+    dx_b, g_b = lm.lmoe_backward(h, x, dy, ws2, topk_idx=idx, gates=gates)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    assert torch.equal(dx_a, dx_b)
+    for n in g_a:
+        assert torch.equal(g_a[n], g_b[n]), n

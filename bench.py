@@ -94,6 +94,12 @@ def layer_work(shape, T, counts, fp8=False):
     return w
 
 
+# DRAM read+write over algorithmic bytes of the backward's per-expert weight-
+# gradient GEMMs, from ncu on --profile-case --backward
+# (profiles/backward_expert_wgrad_gemm_ncu_small.md)
+BWD_TRAFFIC_RATIO = {"wgrad_w3": 0.904, "wgrad_w12": 0.946}
+
+
 def backward_work(shape, T, counts):
     """Algorithmic FLOPs and bytes of each backward stage for T tokens with
     per-expert assignment counts `counts` (bf16 2 bytes, fp32 4 bytes; weight
@@ -403,7 +409,14 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src)
                       "unit": unit, "frac": round(ach / peak, 4), "share": round(stage_ms[nm] / ms, 4)}
     dom = max(lm.BWD_STAGES, key=lambda nm: stage_ms[nm])
     roof = {k: v for k, v in stages[dom].items() if k not in ("ms", "share")}
-    roof.update(kernel="backward_" + dom, per_launch={"flop": work[dom][0], "bytes": work[dom][1]}, traffic=None,
+    # DRAM bytes per launch: ncu measured the segment GEMMs on the reduced
+    # backward case (--profile-case --backward); read+write over the launch's
+    # algorithmic bytes there gives the ratio, scaled to this launch
+    ratio = BWD_TRAFFIC_RATIO.get(dom)
+    roof.update(kernel="backward_" + dom, per_launch={"flop": work[dom][0], "bytes": work[dom][1]},
+                traffic=round(ratio * work[dom][1]) if ratio else None,
+                traffic_source=("ncu dram__bytes_read.sum + dram__bytes_write.sum on --profile-case --backward, "
+                                "ratio to algorithmic bytes scaled to this launch") if ratio else None,
                 peak_source=peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " hbm copy"))
     model_flop = 2.0 * layer_flops_per_token(shape) * T      # data + weight gradients of every GEMM
     executed = sum(v[0] for v in work.values())

@@ -15,6 +15,11 @@
 // operands (kind::f8f6f4, a K block of 128 elements = the same 128-byte rows)
 // and their epilogues apply the power-of-two row scales: a5 writes e4m3(4 act),
 // a6 undoes the 4 with the W3 row scale and the gate.
+// The backward pass (gemm_bwd.cu) adds two epilogues: EPI_GLU_BWD (the
+// accumulator holds a recomputed SiTU-GLU GEMM's p1 | p2; with the gradient of
+// its activation it writes dp1 | dp2) and EPI_F32 (fp32 weight gradients), and
+// per-expert K segments (KSEG: each tile names its own K range, for the routed
+// experts' weight gradients, whose output goes out by TMA store).
 //
 // Structure (one CTA per SM, 192 threads; 320 with the A gather):
 //   warp 0      TMA producer: per 64-wide K block, one box of A and one or two

@@ -205,3 +205,29 @@ def test_backward_with_forward_outputs_in_caller_buffers(lm):
     assert torch.equal(dx_a, dx_b)
     for n in g_a:
         assert torch.equal(g_a[n], g_b[n]), n
+
+
+def test_backward_host_errors_enqueue_nothing(lm):
+    shape = synth.TINY
+    T = 16
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, bias = (t.cuda() for t in synth.activations_host(shape, T=T))
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    dy = torch.zeros_like(x)
+    need = lm.lmoe_backward_workspace_size(h, T)
+    with pytest.raises(lm.LmoeError) as e:        # workspace too small
+        lm.lmoe_backward(h, x, dy, ws, workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 4
+    with pytest.raises(lm.LmoeError) as e:        # forward workspace too small
+        lm.lmoe_backward(h, x, dy, ws[:1024])
+    assert e.value.status == 4
+    with pytest.raises(lm.LmoeError) as e:        # more tokens than the handle was made for
+        lm.lmoe_backward_workspace_size(h, T + 1)
+    assert e.value.status == 2
+    # T = 0 enqueues nothing and succeeds
+    dx0, _ = lm.lmoe_backward(h, x[:0], dy[:0], ws, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert dx0.shape[0] == 0
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0

@@ -29,6 +29,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -148,7 +149,8 @@ class ClockSampler:
     def __init__(self, device_index):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples go to the system temp directory; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"lmoe_clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

@@ -50,6 +50,8 @@ struct lmoe_handle {
     uint16_t *t_ups3, *t_w3, *t_w12, *t_wr, *t_wd, *t_ws12;
     CUtensorMap m_t_ups3, m_t_w3, m_t_w12, m_t_wr, m_t_wd, m_t_ws12;
     int bn_drs, bn_u, bn_s;
+    // backward: fork / join events of the side-stream copies
+    cudaEvent_t bev[6];
 };
 
 namespace {
@@ -254,6 +256,8 @@ bool quantize_pack(const uint16_t *src, uint64_t E, uint64_t R, uint64_t K, int 
 }
 
 void release_streams(lmoe_handle *h) {
+    for (int i = 0; i < 6; ++i)
+        if (h->bev[i]) cudaEventDestroy(h->bev[i]);
     if (h->side) cudaStreamDestroy(h->side);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
@@ -467,6 +471,8 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
                  cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 6 && io_ok && c.with_backward; ++i)
+        io_ok = cudaEventCreateWithFlags(&h->bev[i], cudaEventDisableTiming) == cudaSuccess;
     for (int s = 0; s < 2 && io_ok; ++s)
         io_ok = cudaEventCreateWithFlags(&h->ev_in[s], cudaEventDisableTiming) == cudaSuccess &&
                 cudaEventCreateWithFlags(&h->ev_fwd[s], cudaEventDisableTiming) == cudaSuccess &&
@@ -857,6 +863,46 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     auto mark = [&](int stage) {
         if (h->bwd_events) cudaEventRecord(h->bwd_events[stage], stream);
     };
+    // The copies the weight-gradient GEMMs read (token-major transposes and the
+    // per-expert segments) are memory-bound and only read earlier results.
+    // Without the timing hook they run on the handle's side stream next to
+    // the tensor-core GEMMs of the main chain (whose one CTA per SM leaves
+    // shared memory and threads for the copies' blocks): the input copies
+    // beside dr and the shared experts, the segments beside dx and the dense
+    // weight gradients; each group is joined before the GEMMs that read it.
+    // With the hook, everything runs in stream order so each stage's events
+    // bracket it alone.
+    const bool overlap = (h->bwd_events == nullptr);
+    cudaStream_t s2 = overlap ? h->side : stream;
+    auto fork = [&](int i) {
+        return !overlap ||
+               (cudaEventRecord(h->bev[i], stream) == cudaSuccess && cudaStreamWaitEvent(s2, h->bev[i], 0) == cudaSuccess);
+    };
+    const int64_t Tl = T;
+    auto tr = [&](const uint16_t *in, int64_t ldi, int64_t R, int C, uint16_t *out, int64_t Q, const int32_t *qsrc,
+                  const float *qscale, const int32_t *qlim) {
+        return ok(launch_transpose(in, ldi, 0, R, C, out, Q, 0, Q, 1, qsrc, qscale, qlim, s2));
+    };
+    auto copies_inputs = [&]() {   // inputs of the backward: dy, x and the forward's r, act_s, h
+        return tr(dy, d, Tl, di, dyT, Tp, nullptr, nullptr, nullptr) && tr(x, d, Tl, di, xT, Tp, nullptr, nullptr, nullptr) &&
+               tr(rbuf, L, Tl, Li, rT, Tp, nullptr, nullptr, nullptr) &&
+               tr(sact, S, Tl, Si, sT, Tp, nullptr, nullptr, nullptr) && tr(hbuf, L, Tl, Li, hT, Tp, nullptr, nullptr, nullptr);
+    };
+    auto copies_dps = [&]() { return tr(dps, 2 * S, Tl, 2 * Si, dpsT, Tp, nullptr, nullptr, nullptr); };
+    auto copies_dl = [&]() { return tr(dl, Ep, Tl, Ei, dlT, Tp, nullptr, nullptr, nullptr); };
+    auto copies_dh = [&]() { return tr(dh, L, Tl, Li, dhT, Tp, nullptr, nullptr, nullptr); };
+    const int mt_a = static_cast<int>(L / kBM), mt_b = static_cast<int>(ceil_div(2 * I, kBM));
+    auto copies_segments = [&]() {   // after dz and dp exist
+        return ok(launch_segments(offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
+                                  mt_b, nkt, s2)) &&
+               ok(launch_zero_unused(offsets, Ei, I * L, g->w1, g->w2, g->w3, s2)) &&
+               // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's column segment
+               tr(dz, L, Tl, Li, doT, Qmax, qtok, qgate, nkt + 2) && tr(act, I, n, Ii, aT, Qmax, qperm, nullptr, nkt + 2) &&
+               tr(hbuf, L, Tl, Li, hgT, Qmax, qtok, nullptr, nkt + 2) &&
+               tr(dp, 2 * I, n, 2 * Ii, dpT, Qmax, qperm, nullptr, nkt + 2);
+    };
+    if (overlap && !(fork(0) && copies_inputs())) return LMOE_ERR_CUDA;
+
     mark(LMOE_BWD_STAGE_DR);
     if (!ok(launch_fill(ones, n, 1.0f, stream))) return LMOE_ERR_CUDA;
     {   // dr | da_s = dy [W_up | Ws3]
@@ -891,6 +937,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
+    if (overlap && !(fork(1) && copies_dps())) return LMOE_ERR_CUDA;
     mark(LMOE_BWD_STAGE_RMSNORM);
     // RMSNorm backward: dz
     if (!ok(launch_rms_bwd(obuf, T, Ki, Li, c.rms_eps, drs, L + S, dz, stream))) return LMOE_ERR_CUDA;
@@ -946,11 +993,13 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
     }
+
     mark(LMOE_BWD_STAGE_ROUTER);
     // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
     if (!ok(launch_router_bwd(dgp, nq, inv, idx, hbuf, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
                               stream)))
         return LMOE_ERR_CUDA;
+    if (overlap && !(fork(2) && copies_dl())) return LMOE_ERR_CUDA;
     mark(LMOE_BWD_STAGE_DH_EXPERTS);
     {   // experts' share of dh: W1[e]^T dp1 + W2[e]^T dp2, rows back in assignment order
         GemmMaps m{m_dp, m_dp, h->m_t_w12, h->m_t_w12};
@@ -986,6 +1035,12 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     }
     mark(LMOE_BWD_STAGE_DH_SUM);
     if (!ok(launch_dh_sum(dhp, dhr, T, Ki, Li, dh, h->num_sms, stream))) return LMOE_ERR_CUDA;
+    // side stream: the last token-major copy, then (join point 4 for the dense
+    // weight gradients) the per-expert segments, which so run next to dx and
+    // the dense weight-gradient GEMMs (join point 5 for the experts')
+    if (overlap && !(fork(3) && copies_dh() && cudaEventRecord(h->bev[4], s2) == cudaSuccess && copies_segments() &&
+                     cudaEventRecord(h->bev[5], s2) == cudaSuccess))
+        return LMOE_ERR_CUDA;
     mark(LMOE_BWD_STAGE_DX);
     {   // dx = dh W_down + dp_s [Ws1 ; Ws2]  (K split over the two sources)
         GemmMaps m{m_dh, m_dps, h->m_t_wd, h->m_t_ws12};
@@ -1003,17 +1058,12 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         if (st) return st;
     }
     // ---- weight gradients of the dense weights: K = tokens (transposed operands, zero past T)
-    const int64_t Tl = T;
     mark(LMOE_BWD_STAGE_TRANSPOSE);
-    if (!ok(launch_transpose(dy, d, 0, Tl, di, dyT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(x, d, 0, Tl, di, xT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(rbuf, L, 0, Tl, Li, rT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(sact, S, 0, Tl, Si, sT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(dps, 2 * S, 0, Tl, 2 * Si, dpsT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(dh, L, 0, Tl, Li, dhT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(hbuf, L, 0, Tl, Li, hT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)) ||
-        !ok(launch_transpose(dl, Ep, 0, Tl, Ei, dlT, Tp, 0, Tp, 1, nullptr, nullptr, nullptr, stream)))
+    if (overlap) {   // the token-major copies are done
+        if (cudaStreamWaitEvent(stream, h->bev[4], 0) != cudaSuccess) return LMOE_ERR_CUDA;
+    } else if (!(copies_inputs() && copies_dps() && copies_dh() && copies_dl())) {
         return LMOE_ERR_CUDA;
+    }
     auto wgrad = [&](const CUtensorMap &ma, const CUtensorMap &mb, int64_t M, int64_t N, int bn, float *out) {
         GemmMaps m{ma, ma, mb, mb};
         GemmArgs a = base_args(h);
@@ -1033,17 +1083,12 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         (st = wgrad(m_dhT, m_xT, L, d, h->bn_up, g->w_down)) || (st = wgrad(m_dlT, m_hT, E, L, h->bn_down, g->w_router)))
         return st;
     // ---- weight gradients of the routed experts: K = each expert's own assignments
-    const int mt_a = static_cast<int>(L / kBM), mt_b = static_cast<int>(ceil_div(2 * I, kBM));
     mark(LMOE_BWD_STAGE_SEGMENTS);
-    if (!ok(launch_segments(offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
-                            mt_b, nkt, stream)) ||
-        !ok(launch_zero_unused(offsets, Ei, I * L, g->w1, g->w2, g->w3, stream)) ||
-        // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's column segment
-        !ok(launch_transpose(dz, L, 0, Tl, Li, doT, Qmax, 0, Qmax, 1, qtok, qgate, nkt + 2, stream)) ||
-        !ok(launch_transpose(act, I, 0, n, Ii, aT, Qmax, 0, Qmax, 1, qperm, nullptr, nkt + 2, stream)) ||
-        !ok(launch_transpose(hbuf, L, 0, Tl, Li, hgT, Qmax, 0, Qmax, 1, qtok, nullptr, nkt + 2, stream)) ||
-        !ok(launch_transpose(dp, 2 * I, 0, n, 2 * Ii, dpT, Qmax, 0, Qmax, 1, qperm, nullptr, nkt + 2, stream)))
+    if (overlap) {   // the segments are done: every side-stream copy has finished
+        if (cudaStreamWaitEvent(stream, h->bev[5], 0) != cudaSuccess) return LMOE_ERR_CUDA;
+    } else if (!copies_segments()) {
         return LMOE_ERR_CUDA;
+    }
     mark(LMOE_BWD_STAGE_WGRAD_W3);
     CUtensorMap m_g3, m_g1, m_g2;
     if (!make_store_map_f32(&m_g3, g->w3, E * L, I, I) || !make_store_map_f32(&m_g1, g->w1, E * I, L, L) ||

@@ -12,7 +12,11 @@
 // rows with 16-byte loads (EPC = 32 -> each row segment is one 128-byte line),
 // counts with shared-memory atomics, and adds its non-zero counters into the
 // global histogram at the end.  The global adds are the on-chip analogue of
-// the cross-node all-reduce.
+// the cross-node all-reduce.  For large B (where 32-bit counters would leave
+// fewer than 32 experts per CTA) the counters are 16-bit, two bins per 32-bit
+// word, with token chunks of at most 65535 rows so that no counter can carry
+// into its neighbour: twice the experts per CTA, so each row segment a CTA
+// reads is a whole 32-byte sector or more.
 #include "kernels.h"
 
 namespace lmoe {
@@ -29,11 +33,14 @@ __device__ __forceinline__ int bin_of(float s, float fB, int B) {
 }
 
 // Vector path: E % 4 == 0, ld % 4 == 0, 16-byte aligned rows; EPC in {4..32}.
-template <int EPC>
+// PACK16: counters of bins 2w and 2w+1 share word w (low / high 16 bits);
+// requires rows_per_chunk <= 65535.
+template <int EPC, bool PACK16>
 __global__ void __launch_bounds__(kHistThreads)
     qb_hist_vec_kernel(const float *__restrict__ s, int64_t T, int E, int64_t ld, int B,
                        uint32_t *__restrict__ hist, int n_groups, int64_t rows_per_chunk) {
-    extern __shared__ uint32_t cnt[];  // [EPC][B]
+    extern __shared__ uint32_t cnt[];  // [EPC][WB] words
+    const int WB = PACK16 ? (B + 1) / 2 : B;   // counter words per expert
     constexpr int NQ = EPC / 4;                 // float4 per row segment
     constexpr int ROWS = kHistThreads / NQ;     // rows per sweep
     constexpr int U = 4;                        // sweeps in flight
@@ -43,10 +50,17 @@ __global__ void __launch_bounds__(kHistThreads)
     const int ne = min(EPC, E - e0);
     const int64_t r_begin = chunk * rows_per_chunk;
     const int64_t r_end = min(T, r_begin + rows_per_chunk);
-    for (int i = threadIdx.x; i < ne * B; i += kHistThreads) cnt[i] = 0u;
+    for (int i = threadIdx.x; i < ne * WB; i += kHistThreads) cnt[i] = 0u;
     __syncthreads();
 
     const float fB = static_cast<float>(B);
+    auto count = [&](int c, float v) {
+        const int b = bin_of(v, fB, B);
+        if (PACK16)
+            atomicAdd(&cnt[c * WB + (b >> 1)], 1u << ((b & 1) << 4));
+        else
+            atomicAdd(&cnt[c * WB + b], 1u);
+    };
     const int q = threadIdx.x % NQ;
     const int rl = threadIdx.x / NQ;
     const bool qv = 4 * q < ne;
@@ -64,17 +78,24 @@ __global__ void __launch_bounds__(kHistThreads)
             const int64_t row = r0 + int64_t(u) * ROWS + rl;
             if (!(qv && row < r_end)) continue;
             const int c = 4 * q;
-            atomicAdd(&cnt[(c + 0) * B + bin_of(v[u].x, fB, B)], 1u);
-            atomicAdd(&cnt[(c + 1) * B + bin_of(v[u].y, fB, B)], 1u);
-            atomicAdd(&cnt[(c + 2) * B + bin_of(v[u].z, fB, B)], 1u);
-            atomicAdd(&cnt[(c + 3) * B + bin_of(v[u].w, fB, B)], 1u);
+            count(c + 0, v[u].x);
+            count(c + 1, v[u].y);
+            count(c + 2, v[u].z);
+            count(c + 3, v[u].w);
         }
     }
     __syncthreads();
     uint32_t *dst = hist + int64_t(e0) * B;
-    for (int i = threadIdx.x; i < ne * B; i += kHistThreads) {
+    for (int i = threadIdx.x; i < ne * WB; i += kHistThreads) {
         const uint32_t c = cnt[i];
-        if (c) atomicAdd(&dst[i], c);
+        if (!c) continue;
+        if (PACK16) {
+            const int e = i / WB, b = 2 * (i % WB);
+            if (c & 0xffffu) atomicAdd(&dst[int64_t(e) * B + b], c & 0xffffu);
+            if (c >> 16) atomicAdd(&dst[int64_t(e) * B + b + 1], c >> 16);   // b + 1 < B when non-zero
+        } else {
+            atomicAdd(&dst[i], c);
+        }
     }
 }
 
@@ -187,8 +208,14 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     while (epc > 1 && size_t(epc) * per_expert > kHistSmemBudget) epc >>= 1;
     const bool vec = epc >= 4 && (E % 4 == 0) && (ld % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
+    // 16-bit counters where they let a CTA hold more experts (vector path)
+    const size_t per_expert16 = size_t((B + 1) / 2) * sizeof(uint32_t);
+    int epc16 = 32;
+    while (epc16 > 1 && size_t(epc16) * per_expert16 > kHistSmemBudget) epc16 >>= 1;
+    const bool pack16 = vec && epc16 > epc;
+    if (pack16) epc = epc16;
     const int n_groups = (E + epc - 1) / epc;
-    const size_t smem = size_t(epc) * per_expert;
+    const size_t smem = size_t(epc) * (pack16 ? per_expert16 : per_expert);
     const int ctas_per_sm = max(1, min(2, static_cast<int>((227 * 1024) / (smem + 1024))));
     // Token chunks per expert group: the fewest (each chunk ends with one
     // global add per non-zero counter) that fill the GPU in whole waves --
@@ -196,8 +223,11 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     const int slots = num_sms * ctas_per_sm;
     const int64_t min_rows = 512;
     const int64_t max_chunks = (T + min_rows - 1) / min_rows;
-    int n_chunks = 1;
-    for (int c = max(1, slots / n_groups); c <= 16 && c <= max_chunks; ++c) {
+    // 16-bit counters: no chunk longer than 65535 rows
+    const int min_chunks = pack16 ? static_cast<int>((T + 65534) / 65535) : 1;
+    int n_chunks = min_chunks;
+    for (int c = max(min_chunks, slots / n_groups); c <= max(16, min_chunks) && c <= max(max_chunks, int64_t(min_chunks));
+         ++c) {
         n_chunks = c;
         const int ctas = n_groups * c;
         const int waves = (ctas + slots - 1) / slots;
@@ -206,20 +236,28 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     const int64_t rows_per_chunk = (T + n_chunks - 1) / n_chunks;
     const unsigned grid = static_cast<unsigned>(n_groups) * static_cast<unsigned>(n_chunks);
 
-#define LMOE_QB_VEC(N_)                                                                       \
-    case N_:                                                                                  \
-        err = cudaFuncSetAttribute(qb_hist_vec_kernel<N_>,                                    \
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);   \
-        if (err != cudaSuccess) return err;                                                   \
-        qb_hist_vec_kernel<N_><<<grid, kHistThreads, smem, st>>>(scores, T, E, ld, B, hist,    \
-                                                                 n_groups, rows_per_chunk);   \
+#define LMOE_QB_VEC(N_, P_)                                                                         \
+    case N_:                                                                                        \
+        err = cudaFuncSetAttribute(qb_hist_vec_kernel<N_, P_>,                                      \
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
+        if (err != cudaSuccess) return err;                                                         \
+        qb_hist_vec_kernel<N_, P_><<<grid, kHistThreads, smem, st>>>(scores, T, E, ld, B, hist,      \
+                                                                     n_groups, rows_per_chunk);     \
         break;
-    if (vec) {
+    if (vec && pack16) {
         switch (epc) {
-            LMOE_QB_VEC(4)
-            LMOE_QB_VEC(8)
-            LMOE_QB_VEC(16)
-            LMOE_QB_VEC(32)
+            LMOE_QB_VEC(8, true)
+            LMOE_QB_VEC(16, true)
+            LMOE_QB_VEC(32, true)
+            default:
+                return cudaErrorInvalidValue;
+        }
+    } else if (vec) {
+        switch (epc) {
+            LMOE_QB_VEC(4, false)
+            LMOE_QB_VEC(8, false)
+            LMOE_QB_VEC(16, false)
+            LMOE_QB_VEC(32, false)
             default:
                 return cudaErrorInvalidValue;
         }

@@ -25,7 +25,9 @@ def hist_np(h: torch.Tensor) -> np.ndarray:
 
 @pytest.mark.parametrize("T,E,B", [(65536, 896, 1000), (4096, 128, 1000), (4099, 896, 10000),
                                    (1000, 40, 37), (1, 896, 1000),
-                                   (3000, 24, 60000)])   # bins beyond shared memory: global counters
+                                   (3000, 24, 60000),    # bins beyond shared memory: global counters
+                                   (200000, 64, 10000),  # 16-bit counters, several token chunks
+                                   (70001, 32, 9999)])   # 16-bit counters, odd B (last word half used)
 def test_histogram_bit_exact(lm, T, E, B):
     s = synth.qb_scores(T, E, seed=T + E + B)
     s[0, 0] = 1.0
@@ -35,6 +37,22 @@ def test_histogram_bit_exact(lm, T, E, B):
     ref = oracle.qb_histogram(s.numpy(), B)
     assert np.array_equal(hist_np(hg), ref)
     assert hist_np(hg).sum(dtype=np.uint64) == T * E
+
+
+def test_histogram_16bit_counters_do_not_carry(lm):
+    """Large B packs two 16-bit counters per word; one bin receiving every
+    token (T > 65535) must not carry into its neighbour: token chunks are
+    capped at 65535 rows."""
+    T, E, B = 140000, 32, 10000
+    s = synth.qb_scores(T, E, seed=5)
+    s[:, 0] = 0.5          # bin 5000: an even bin, the low half of its word
+    s[:, 1] = 0.50005      # bin 5000 as well (0.50005 * 10000 = 5000.5)
+    s[:, 2] = 0.5001       # bin 5001: the high half of the same word
+    hg = lm.qb_histogram(s.cuda(), B)
+    torch.cuda.synchronize()
+    h = hist_np(hg)
+    assert h[0, 5000] == T and h[1, 5000] == T and h[2, 5001] == T
+    assert np.array_equal(h, oracle.qb_histogram(s.numpy(), B))
 
 
 def test_histogram_strided_and_unaligned_columns(lm):

@@ -28,7 +28,11 @@ constexpr int kTT = 64;  // transpose tile: 64 x 64 elements
 // src(q) = qsrc[q] (or q when q < R without qsrc) and a negative src gives 0.
 // Tiles whose first q is at or past *q_limit are skipped (never read later).
 // 16-byte accesses on both sides: a thread loads 8 columns of one source row
-// and stores 8 consecutive q of one output row.  The shared tile is stored
+// and stores 8 consecutive q of one output row.  With packed_rows > 0 the
+// output is K-block packed: element (c, q) sits at
+// ((q / 64) * packed_rows + c) * 64 + q % 64, so each 64-column block of q is
+// one contiguous [packed_rows][64] slab and a TMA box of consecutive rows in
+// it is one contiguous run of memory (ldo and obs are then unused).  The shared tile is stored
 // with its 16-byte chunks XOR-swizzled by (q / 8) % 8 so that the column reads
 // of the store phase spread over the banks.  Requires ldi, ldo, the batch
 // strides and the pointers to be multiples of 8 elements (16 bytes).
@@ -38,7 +42,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restri
                                                         int64_t R, int C, uint16_t *__restrict__ out, int64_t ldo,
                                                         int64_t obs, int64_t Q, const int32_t *__restrict__ qsrc,
                                                         const float *__restrict__ qscale,
-                                                        const int32_t *__restrict__ q_limit) {
+                                                        const int32_t *__restrict__ q_limit, int64_t packed_rows) {
     grid_dependency_wait();
     __shared__ __align__(16) uint16_t tile[kTT * kTT];
     const int64_t q0 = int64_t(blockIdx.x) * kTT;
@@ -91,7 +95,8 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restri
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             w[e] = uint32_t(tile[swz(chunk * 8 + 2 * e, cc)]) | (uint32_t(tile[swz(chunk * 8 + 2 * e + 1, cc)]) << 16);
-        uint16_t *p = outb + int64_t(c) * ldo + q;
+        uint16_t *p = packed_rows > 0 ? out + ((q0 >> 6) * packed_rows + c) * kTT + chunk * 8
+                                      : outb + int64_t(c) * ldo + q;
         if (q + 8 <= Q) {
             *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
         } else {
@@ -372,12 +377,14 @@ int blocks_for(int64_t work, int per_block, int cap) {
 
 cudaError_t launch_transpose(const uint16_t *in, int64_t ldi, int64_t in_batch_stride, int64_t R, int C,
                              uint16_t *out, int64_t ldo, int64_t out_batch_stride, int64_t Q, int batch,
-                             const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream) {
+                             const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream,
+                             int64_t packed_rows) {
     if (Q <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
+    if (packed_rows > 0 && (batch != 1 || packed_rows != C || Q % kTT != 0)) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>((Q + kTT - 1) / kTT), static_cast<unsigned>((C + kTT - 1) / kTT),
                     static_cast<unsigned>(batch));
     return launch_kernel(transpose_kernel, grid, dim3(256), 0, stream, true, in, ldi, in_batch_stride, R, C, out, ldo,
-                         out_batch_stride, Q, qsrc, qscale, q_limit);
+                         out_batch_stride, Q, qsrc, qscale, q_limit, packed_rows);
 }
 
 cudaError_t launch_segments(const int32_t *offsets, const int32_t *perm,

@@ -309,11 +309,14 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 const bool second = (AM == A_SPLIT || BMD == B_SPLIT) && kabs >= args.k_split;
                 const int kx = (second ? kabs - args.k_split : kabs) * kBK;
                 // packed B: the K block is a row offset, the column is always 0
-                const int bx = args.b_packed ? 0 : kx;
-                const int by = args.b_packed ? brow + kabs * TRB : brow;
+                // (K segments: both operands are packed by K block)
+                const int bx = (KSEG || args.b_packed) ? 0 : kx;
+                const int by = KSEG ? kabs * args.kseg_b_rows + ti.nt * TRB : args.b_packed ? brow + kabs * TRB : brow;
+                const int ax = KSEG ? 0 : kx;
+                const int ay = KSEG ? kabs * args.kseg_a_rows + ti.row0 : ti.row0;
                 if (lane == 0) {
                     if (AM != A_GATHER)
-                        tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, kx, ti.row0, fb);
+                        tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, ax, ay, fb);
                     if (BMD == B_GLU) {
                         tma_load_2d(sb, &tmB0, bx, by, fb);
                         tma_load_2d(sb + H * (kBK * 2), &tmB1, bx, by, fb);

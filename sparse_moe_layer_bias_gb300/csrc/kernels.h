@@ -107,6 +107,9 @@ struct GemmArgs {
     float *dgp;                   //   partial sums of u * act (nullable)
     void *out2;                   // EPI_F32 with K segments: rows >= m_split of an expert's block
     int32_t m_split;
+    // K segments: operand heights of the K-block packed A and B ([K blocks][rows][64]);
+    // the box of K block kb, rows r.. sits at map row kb * rows + r
+    int32_t kseg_a_rows, kseg_b_rows;
     unsigned *err;           // device status word
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
@@ -180,10 +183,12 @@ cudaError_t launch_qb_quantile(const uint32_t *hist, int E, int B, double level,
 // ------------------------------------------------------------------ backward
 // out[b][c][q] = scale(q) * in[b][src(q)][c] (c < C, q < Q); src(q) = qsrc[q],
 // or q when q < R without qsrc; a negative src gives 0.  Tiles starting at or
-// past *q_limit (when given) are skipped.
+// past *q_limit (when given) are skipped.  packed_rows = C (batch 1, Q % 64
+// == 0): K-block packed output, (c, q) at ((q / 64) * C + c) * 64 + q % 64.
 cudaError_t launch_transpose(const uint16_t *in, int64_t ldi, int64_t in_batch_stride, int64_t R, int C,
                              uint16_t *out, int64_t ldo, int64_t out_batch_stride, int64_t Q, int batch,
-                             const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream);
+                             const int32_t *qsrc, const float *qscale, const int32_t *q_limit, cudaStream_t stream,
+                             int64_t packed_rows = 0);
 // Per-expert column segments (assignments padded to 64), their column maps and
 // the segment GEMMs' tile lists; n_tiles3 = {tiles in a, tiles in b, columns}.
 // Counts come from the forward's offsets ([E+1] exclusive scan).

@@ -849,9 +849,11 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         !make_map(&m_rT, rT, L, Tp, Tp, h->bn_down) || !make_map(&m_sT, sT, S, Tp, Tp, h->bn_s) ||
         !make_map(&m_dps1T, dpsT, S, Tp, Tp, kBM) || !make_map(&m_dps2T, dpsT + S * Tp, S, Tp, Tp, kBM) ||
         !make_map(&m_dhT, dhT, L, Tp, Tp, kBM) || !make_map(&m_hT, hT, L, Tp, Tp, h->bn_down) ||
-        !make_map(&m_dlT, dlT, E, Tp, Tp, kBM) || !make_map(&m_doT, doT, L, Qmax, Qmax, kBM) ||
-        !make_map(&m_aT, aT, I, Qmax, Qmax, h->bn_u) || !make_map(&m_hgT, hgT, L, Qmax, Qmax, h->bn_down) ||
-        !make_map(&m_dpT, dpT, 2 * I, Qmax, Qmax, kBM))
+        !make_map(&m_dlT, dlT, E, Tp, Tp, kBM) ||
+        // K-block packed segment copies: [Qmax / 64 * rows][64]
+        !make_map(&m_doT, doT, Qmax / 64 * L, 64, 64, kBM) || !make_map(&m_aT, aT, Qmax / 64 * I, 64, 64, h->bn_u) ||
+        !make_map(&m_hgT, hgT, Qmax / 64 * L, 64, 64, h->bn_down) ||
+        !make_map(&m_dpT, dpT, Qmax / 64 * 2 * I, 64, 64, kBM))
         return LMOE_ERR_CUDA;
 
     const int m_tiles = static_cast<int>(ceil_div(T, kBM));
@@ -880,8 +882,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     };
     const int64_t Tl = T;
     auto tr = [&](const uint16_t *in, int64_t ldi, int64_t R, int C, uint16_t *out, int64_t Q, const int32_t *qsrc,
-                  const float *qscale, const int32_t *qlim) {
-        return ok(launch_transpose(in, ldi, 0, R, C, out, Q, 0, Q, 1, qsrc, qscale, qlim, s2));
+                  const float *qscale, const int32_t *qlim, bool packed = false) {
+        return ok(launch_transpose(in, ldi, 0, R, C, out, Q, 0, Q, 1, qsrc, qscale, qlim, s2, packed ? C : 0));
     };
     auto copies_inputs = [&]() {   // inputs of the backward: dy, x and the forward's r, act_s, h
         return tr(dy, d, Tl, di, dyT, Tp, nullptr, nullptr, nullptr) && tr(x, d, Tl, di, xT, Tp, nullptr, nullptr, nullptr) &&
@@ -896,10 +898,12 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         return ok(launch_segments(offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
                                   mt_b, nkt, s2)) &&
                ok(launch_zero_unused(offsets, Ei, I * L, g->w1, g->w2, g->w3, s2)) &&
-               // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's column segment
-               tr(dz, L, Tl, Li, doT, Qmax, qtok, qgate, nkt + 2) && tr(act, I, n, Ii, aT, Qmax, qperm, nullptr, nkt + 2) &&
-               tr(hbuf, L, Tl, Li, hgT, Qmax, qtok, nullptr, nkt + 2) &&
-               tr(dp, 2 * I, n, 2 * Ii, dpT, Qmax, qperm, nullptr, nkt + 2);
+               // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's
+               // column segment, K-block packed ([Qmax / 64][rows][64])
+               tr(dz, L, Tl, Li, doT, Qmax, qtok, qgate, nkt + 2, true) &&
+               tr(act, I, n, Ii, aT, Qmax, qperm, nullptr, nkt + 2, true) &&
+               tr(hbuf, L, Tl, Li, hgT, Qmax, qtok, nullptr, nkt + 2, true) &&
+               tr(dp, 2 * I, n, 2 * Ii, dpT, Qmax, qperm, nullptr, nkt + 2, true);
     };
     if (overlap && !(fork(0) && copies_inputs())) return LMOE_ERR_CUDA;
 
@@ -1099,6 +1103,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(L);
         a.m_split = static_cast<int32_t>(L);
+        a.kseg_a_rows = static_cast<int32_t>(L);
+        a.kseg_b_rows = static_cast<int32_t>(I);
         a.n_tiles = static_cast<int32_t>(ceil_div(I, h->bn_u));
         a.tiles = kt_a;
         a.n_mtiles = nkt;
@@ -1116,6 +1122,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(2 * I);
         a.m_split = static_cast<int32_t>(I);
+        a.kseg_a_rows = static_cast<int32_t>(2 * I);
+        a.kseg_b_rows = static_cast<int32_t>(L);
         a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
         a.tiles = kt_b;
         a.n_mtiles = nkt + 1;

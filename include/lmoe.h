@@ -274,7 +274,7 @@ int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *b
  *   dz  = RMSNorm backward of dr at z = sum of the forward's rows o
  *   per chosen expert: u = W3[e]^T dz; da = gate * u; dgate = u . act;
  *         dp1, dp2 = SiTU-GLU backward on the recomputed W1[e] h, W2[e] h;
- *         dh += W1[e]^T dp1 + W2[e]^T dp2 + w_router[e] dgate s (1 - s)
+ *         dh += W1[e]^T dp1 + W2[e]^T dp2 + w_router[e] dgate sigma'(logit)
  *   dx  = W_down^T dh + Ws1^T dp_s1 + Ws2^T dp_s2
  * and the weight gradients are the sums over tokens of the matching outer
  * products (dW_up = sum dy r^T, ..., dW3[e] = sum over e's assignments of
@@ -286,16 +286,20 @@ int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *b
  * per-expert counts are their differences).  topk_idx, gates: the forward's
  * outputs when the caller had it write them to its own buffers (they are then
  * not in the workspace), or NULL for the workspace's copies; an expert id
- * outside [0, n_experts) contributes no gradient.  The router's logits of the chosen experts are recomputed from h,
- * so that sigma'(logit) = sigma(logit) sigma(-logit) stays accurate where the
- * fp32 score has rounded to 1.  workspace: lmoe_backward_workspace_size(T) bytes,
+ * outside [0, n_experts) contributes no gradient.  The router's logits of the
+ * chosen experts are recomputed from h, so that
+ * sigma'(logit) = sigma(logit) sigma(-logit) stays accurate where the fp32
+ * score has rounded to 1.  workspace: lmoe_backward_workspace_size(T) bytes,
  * 256-byte aligned.  The handle must have been created with with_backward =
- * 1 (else LMOE_ERR_INVALID_ARG).  T = 0 enqueues nothing. */
+ * 1 (else LMOE_ERR_INVALID_ARG).  Errors are reported before anything is
+ * enqueued, as in lmoe_forward.  Unless lmoe_set_backward_events is set, the
+ * memory-bound copies run on a side stream of the handle, forked from and
+ * joined back into `stream`, so the call is ordered within `stream` as seen
+ * from outside.  T = 0 enqueues nothing (the gradients are left untouched). */
 int lmoe_backward(lmoe_handle *handle, const uint16_t *x, int64_t T, const uint16_t *dy,
                   const int32_t *topk_idx, const float *gates, const void *fwd_workspace,
-                  size_t fwd_workspace_bytes,
-                  uint16_t *dx, const lmoe_grads *grads, void *workspace, size_t workspace_bytes,
-                  cudaStream_t stream);
+                  size_t fwd_workspace_bytes, uint16_t *dx, const lmoe_grads *grads, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
 
 /* Stages of lmoe_backward, in launch order (for lmoe_set_backward_events). */
 typedef enum {

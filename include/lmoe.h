@@ -244,8 +244,10 @@ int lmoe_set_stage_events(lmoe_handle *handle, cudaEvent_t *events, int n_events
 /* ------------------------------------------------------------------------ */
 
 /* Weight gradients (device fp32, each laid out like its weight in
- * lmoe_weights; all required, 16-byte aligned).  lmoe_backward overwrites
- * them (no accumulation). */
+ * lmoe_weights; all required, 16-byte aligned).  accumulate = 0: lmoe_backward
+ * overwrites them; 1: it adds this pass's gradients to their contents (one
+ * fp32 addition per element, e.g. to sum micro-batches without an extra
+ * pass over the gradients). */
 typedef struct {
     float *w_down;   /* [latent][d]                  */
     float *w_router; /* [n_experts][latent]          */
@@ -256,6 +258,7 @@ typedef struct {
     float *ws2;      /* [S][d]                       */
     float *ws3;      /* [d][S]                       */
     float *w_up;     /* [d][latent]                  */
+    int32_t accumulate; /* 0 or 1 (else LMOE_ERR_INVALID_ARG)            */
 } lmoe_grads;
 
 /* Bytes of device workspace lmoe_backward needs for T tokens (separate from

@@ -56,7 +56,7 @@ class LmoeWeights(ctypes.Structure):
 
 
 class LmoeGrads(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES]
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_NAMES] + [("accumulate", ctypes.c_int32)]
 
 
 class LmoeWsLayout(ctypes.Structure):
@@ -259,9 +259,10 @@ def grad_shapes(handle: Handle) -> dict:
 
 def lmoe_backward(handle: Handle, x: torch.Tensor, dy: torch.Tensor, fwd_workspace: torch.Tensor,
                   dx: torch.Tensor | None = None, grads: dict | None = None, workspace: torch.Tensor | None = None,
-                  topk_idx=None, gates=None, stream=None):
+                  topk_idx=None, gates=None, accumulate: bool = False, stream=None):
     """Backward of the forward that ran on ``x`` with ``fwd_workspace``.  Pass
     ``topk_idx`` / ``gates`` when that forward wrote them to caller buffers.
+    With ``accumulate`` the weight gradients are added to ``grads``' contents.
     Returns (dx bf16 [T, d], dict of fp32 weight gradients)."""
     lib = load_library()
     x = _dev(x, torch.bfloat16, "x")
@@ -272,10 +273,12 @@ def lmoe_backward(handle: Handle, x: torch.Tensor, dy: torch.Tensor, fwd_workspa
         dx = torch.empty_like(x)
     dx = _dev(dx, torch.bfloat16, "dx")
     if grads is None:
-        grads = {n: torch.empty(s, dtype=torch.float32, device=x.device) for n, s in grad_shapes(handle).items()}
+        alloc = torch.zeros if accumulate else torch.empty
+        grads = {n: alloc(s, dtype=torch.float32, device=x.device) for n, s in grad_shapes(handle).items()}
     g = LmoeGrads()
     for n in WEIGHT_NAMES:
         setattr(g, n, _dev(grads[n], torch.float32, "grad " + n).data_ptr())
+    g.accumulate = 1 if accumulate else 0
     if workspace is None:
         workspace = torch.empty(max(lmoe_backward_workspace_size(handle, T), 256), dtype=torch.uint8,
                                 device=x.device)

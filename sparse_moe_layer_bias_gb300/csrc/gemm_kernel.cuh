@@ -538,7 +538,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 }
             } else if (EPI == EPI_F32 && KSEG) {
                 // K segments (the experts' fp32 weight gradients): each warp
-                // writes its 32 rows in 32 x 32 blocks by TMA store, through
+                // writes (accumulate: adds) its 32 rows in 32 x 32 blocks by
+                // TMA store (reduction), through
                 // two swizzled 4 KB buffers, so the stores run asynchronously.
                 // Rows of the expert's block below m_split go to the map in
                 // tmA1 (out), the others to tmB1 (out2); m_split and the block
@@ -567,7 +568,10 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(om, smem_u32(buf), col, y);
+                            if (args.accumulate)
+                                tma_reduce_add_2d(om, smem_u32(buf), col, y);
+                            else
+                                tma_store_2d(om, smem_u32(buf), col, y);
                             bulk_commit();
                         }
                         ++n_tma_stores;
@@ -575,7 +579,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 }
             } else if (EPI == EPI_F32) {
                 // fp32 rows (dense weight gradients, the router's share of the
-                // latent gradient): staged like the scores above
+                // latent gradient): staged like the scores above; accumulate
+                // adds instead of storing (each element has one writer)
                 float *dst = reinterpret_cast<float *>(args.out) + int64_t(ti.row0 + trow) * args.ld_out;
                 const bool vec_ok = (args.ld_out % 4) == 0;
                 const unsigned long long dbits = reinterpret_cast<unsigned long long>(dst);
@@ -596,11 +601,24 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                             const unsigned long long db = __shfl_sync(0xffffffffu, dbits, rr);
                             const int ok = __shfl_sync(0xffffffffu, rv ? 1 : 0, rr);
                             const float4 val = *reinterpret_cast<const float4 *>(stg + rr * C::kStgPitch + ch * 16);
-                            if (ok) *reinterpret_cast<float4 *>(reinterpret_cast<float *>(db) + col + ch * 4) = val;
+                            float4 *to = reinterpret_cast<float4 *>(reinterpret_cast<float *>(db) + col + ch * 4);
+                            if (ok) {
+                                if (args.accumulate)
+                                    atomicAdd(to, val);   // the only writer of these 4 floats
+                                else
+                                    *to = val;
+                            }
                         }
                         __syncwarp();
                     } else if (rv) {
-                        store_f32_32(dst + col, v, static_cast<int>(args.out_cols - col));
+                        const int nc = static_cast<int>(args.out_cols - col);
+                        if (args.accumulate) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nc) atomicAdd(dst + col + j, v[j]);
+                        } else {
+                            store_f32_32(dst + col, v, nc);
+                        }
                     }
                 }
             } else if (EPI == EPI_GLU_BWD) {

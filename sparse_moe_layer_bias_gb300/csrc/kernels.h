@@ -110,6 +110,7 @@ struct GemmArgs {
     // K segments: operand heights of the K-block packed A and B ([K blocks][rows][64]);
     // the box of K block kb, rows r.. sits at map row kb * rows + r
     int32_t kseg_a_rows, kseg_b_rows;
+    int32_t accumulate;           // EPI_F32: add to the output instead of overwriting it
     unsigned *err;           // device status word
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };

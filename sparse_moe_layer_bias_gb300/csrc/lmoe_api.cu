@@ -787,7 +787,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     if (T > c.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return LMOE_OK;
     if (!x || !dy || !fwd_workspace || !dx || !g || !workspace || !g->w_down || !g->w_router || !g->w1 ||
-        !g->w2 || !g->w3 || !g->ws1 || !g->ws2 || !g->ws3 || !g->w_up)
+        !g->w2 || !g->w3 || !g->ws1 || !g->ws2 || !g->ws3 || !g->w_up || (g->accumulate != 0 && g->accumulate != 1))
         return LMOE_ERR_INVALID_ARG;
     const void *al[] = {x, dy, dx, g->w_down, g->w_router, g->w1, g->w2, g->w3, g->ws1, g->ws2, g->ws3, g->w_up};
     for (const void *p : al)
@@ -897,7 +897,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     auto copies_segments = [&]() {   // after dz and dp exist
         return ok(launch_segments(offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
                                   mt_b, nkt, s2)) &&
-               ok(launch_zero_unused(offsets, Ei, I * L, g->w1, g->w2, g->w3, s2)) &&
+               (g->accumulate || ok(launch_zero_unused(offsets, Ei, I * L, g->w1, g->w2, g->w3, s2))) &&
                // do = gate * dz rows, act rows, h rows, dp rows, each in its expert's
                // column segment, K-block packed ([Qmax / 64][rows][64])
                tr(dz, L, Tl, Li, doT, Qmax, qtok, qgate, nkt + 2, true) &&
@@ -1078,6 +1078,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.out = out;
         a.ld_out = N;
         a.out_cols = static_cast<int32_t>(N);
+        a.accumulate = g->accumulate;
         return gemm_status(launch_gemm_bwd(bn, A_DENSE, B_PLAIN, EPI_F32, false, false, m, a,
                                            grid_for(int64_t(a.m_tiles) * a.n_tiles), stream));
     };
@@ -1105,6 +1106,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.m_split = static_cast<int32_t>(L);
         a.kseg_a_rows = static_cast<int32_t>(L);
         a.kseg_b_rows = static_cast<int32_t>(I);
+        a.accumulate = g->accumulate;
         a.n_tiles = static_cast<int32_t>(ceil_div(I, h->bn_u));
         a.tiles = kt_a;
         a.n_mtiles = nkt;
@@ -1124,6 +1126,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.m_split = static_cast<int32_t>(I);
         a.kseg_a_rows = static_cast<int32_t>(2 * I);
         a.kseg_b_rows = static_cast<int32_t>(L);
+        a.accumulate = g->accumulate;
         a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
         a.tiles = kt_b;
         a.n_mtiles = nkt + 1;

@@ -231,3 +231,28 @@ def test_backward_host_errors_enqueue_nothing(lm):
     assert dx0.shape[0] == 0
     torch.cuda.synchronize()
     assert lm.lmoe_device_status(h) == 0
+
+
+def test_backward_accumulates_into_gradients(lm):
+    """accumulate = 1 adds the pass's weight gradients to the buffers: one fp32
+    addition per element, so the result equals init + (the overwriting
+    pass's gradients) bit for bit, unchosen experts included."""
+    shape = synth.TINY
+    T = 200
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, bias = (t.cuda() for t in synth.activations_host(shape, T=T, seed_offset=13))
+    dy = synth.grad_output_host(shape, T=T, seed_offset=13).cuda()
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    dx1, g1 = lm.lmoe_backward(h, x, dy, ws)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(17)
+    init = {n: torch.randn(t.shape, generator=gen, device="cuda") for n, t in g1.items()}
+    acc = {n: t.clone() for n, t in init.items()}
+    dx2, _ = lm.lmoe_backward(h, x, dy, ws, grads=acc, accumulate=True)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    assert torch.equal(dx1, dx2)
+    for n in g1:
+        assert torch.equal(acc[n], init[n] + g1[n]), n

@@ -99,7 +99,7 @@ def _load():
             "orc_softcap_grad": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
             "orc_situ_grad": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
             "orc_backward": (None, [cfg, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
-                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+                                    ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
             "orc_num_threads": (ctypes.c_int, []),
         }
         for name, (res, args) in sig.items():
@@ -400,8 +400,8 @@ def layer_backward(cfg: LayerConfig, x, w, idx, dy, round_mode: int = 1, weight_
     function.  Returns fp64 arrays: "x" [T, d] and, with ``weight_grads``, one
     per weight name in ``BACKWARD_GRADS`` shaped like that weight (w1/w2/w3
     must then be full [E, ...] arrays)."""
-    if cfg.norm_after_down or cfg.expert_fp8:
-        raise ValueError("the backward covers the layer without the variant flags")
+    if cfg.expert_fp8:
+        raise ValueError("the backward covers the bf16 layer (with or without the norm after the down-projection)")
     T = x.shape[0]
     E, L, I, d = cfg.n_experts, cfg.latent, cfg.inter, cfg.d
     S = cfg.n_shared * cfg.shared_inter
@@ -427,7 +427,8 @@ def layer_backward(cfg: LayerConfig, x, w, idx, dy, round_mode: int = 1, weight_
     c = cfg.c()
     _load().orc_backward(ctypes.byref(c), T, _ptr(x), _ptr(idx), _ptr(dy), _ptr(dense["w_down"]),
                          _ptr(dense["w_router"]), p1, p2, p3, _ptr(dense["ws1"]), _ptr(dense["ws2"]),
-                         _ptr(dense["ws3"]), _ptr(dense["w_up"]), int(round_mode), _ptr(out["x"]), *g)
+                         _ptr(dense["ws3"]), _ptr(dense["w_up"]), int(round_mode), int(bool(cfg.norm_after_down)),
+                         _ptr(out["x"]), *g)
     del k1, k2, k3
     return out
 

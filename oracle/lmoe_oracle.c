@@ -720,14 +720,20 @@ static double keep(double v, int round_mode)
  * Layouts as the weights: dw_down [L][d], dw_router [E][L], dw1/dw2 [E][I][L],
  * dw3 [E][L][I], dws1/dws2 [S][d], dws3 [d][S], dw_up [d][L]; dx [T][d].
  * Every output is nullable (a NULL weight gradient skips its sum).  w1, w2,
- * w3 are per-expert pointers as in orc_routed. */
+ * w3 are per-expert pointers as in orc_routed.
+ * norm_after_down (the ablation variant): the latent the router and the
+ * experts see is h = h_raw / sqrt(mean(h_raw^2) + eps) of the down-
+ * projection's h_raw, so the gradient dh reaching it goes through the same
+ * RMSNorm backward as dz above before the down-projection:
+ *   dh_raw = dh / sqrt(ms + eps) - h_raw (dh . h_raw) / (L (ms + eps)^(3/2)),
+ * and dx and dW_down use dh_raw. */
 void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32_t *idx,
                   const uint16_t *dy, const uint16_t *w_down, const uint16_t *w_router,
                   const uint16_t *const *w1, const uint16_t *const *w2, const uint16_t *const *w3,
                   const uint16_t *ws1, const uint16_t *ws2, const uint16_t *ws3,
-                  const uint16_t *w_up, int round_mode, double *dx, double *dw_down,
-                  double *dw_router, double *dw1, double *dw2, double *dw3, double *dws1,
-                  double *dws2, double *dws3, double *dw_up)
+                  const uint16_t *w_up, int round_mode, int norm_after_down, double *dx,
+                  double *dw_down, double *dw_router, double *dw1, double *dw2, double *dw3,
+                  double *dws1, double *dws2, double *dws3, double *dw_up)
 {
     const int64_t d = c->d, L = c->latent, E = c->n_experts, K = c->top_k, I = c->inter;
     const int64_t S = (int64_t)c->n_shared * c->shared_inter;
@@ -750,6 +756,7 @@ void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32
     {
         double *xd = (double *)malloc((size_t)d * sizeof(double));
         double *dyd = (double *)malloc((size_t)d * sizeof(double));
+        double *hraw = (double *)malloc((size_t)L * sizeof(double));
         double *ps1 = (double *)malloc((size_t)S * sizeof(double));
         double *ps2 = (double *)malloc((size_t)S * sizeof(double));
         double *p1 = (double *)malloc((size_t)(K * I) * sizeof(double));
@@ -771,7 +778,17 @@ void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32
             }
             /* forward values */
             for (int64_t l = 0; l < L; ++l)
-                h[l] = keep(dot_bf16_f64(w_down + l * d, xd, d), round_mode);
+                hraw[l] = keep(dot_bf16_f64(w_down + l * d, xd, d), round_mode);
+            double den_h = 1.0, inv_h = 1.0;
+            if (norm_after_down) {
+                double msh = 0.0;
+                for (int64_t l = 0; l < L; ++l)
+                    msh += hraw[l] * hraw[l];
+                den_h = msh / (double)L + c->rms_eps;
+                inv_h = 1.0 / sqrt(den_h);
+            }
+            for (int64_t l = 0; l < L; ++l)
+                h[l] = norm_after_down ? keep(hraw[l] * inv_h, round_mode) : hraw[l];
             for (int64_t i = 0; i < S; ++i) {
                 ps1[i] = dot_bf16_f64(ws1 + i * d, xd, d);
                 ps2[i] = dot_bf16_f64(ws2 + i * d, xd, d);
@@ -859,6 +876,14 @@ void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32
                 for (int64_t l = 0; l < L; ++l)
                     dh[l] += orc_bf16_to_f64(w_router[(int64_t)e * L + l]) * dlgv[a];
             }
+            /* the variant's RMSNorm after the down-projection */
+            if (norm_after_down) {
+                double dhh = 0.0;
+                for (int64_t l = 0; l < L; ++l)
+                    dhh += dh[l] * hraw[l];
+                for (int64_t l = 0; l < L; ++l)
+                    dh[l] = dh[l] * inv_h - hraw[l] * dhh * inv_h / ((double)L * den_h);
+            }
             /* down-projection and the shared experts' input side */
             if (dx) {
                 double *dxt = dx + t * d;
@@ -873,7 +898,7 @@ void orc_backward(const orc_config *c, int64_t T, const uint16_t *x, const int32
                                   orc_bf16_to_f64(ws2[i * d + q]) * dps2v[t * S + i];
             }
         }
-        free(xd); free(dyd); free(ps1); free(ps2); free(p1); free(p2); free(o); free(g);
+        free(xd); free(dyd); free(hraw); free(ps1); free(ps2); free(p1); free(p2); free(o); free(g);
         free(dsig); free(z); free(dr); free(dz); free(das); free(dact);
     }
 

@@ -29,8 +29,8 @@ def make_case(seed, **kw):
     curvature matters), distinct experts per token."""
     shape = dict(d=24, latent=12, n_experts=6, top_k=2, inter=8, n_shared=2, shared_inter=4)
     shape.update(kw)
-    beta = {k: shape.pop(k) for k in ("beta1", "beta2") if k in shape}
-    cfg = oracle.LayerConfig(**shape, **beta)
+    extra = {k: shape.pop(k) for k in ("beta1", "beta2", "norm_after_down") if k in shape}
+    cfg = oracle.LayerConfig(**shape, **extra)
     rng = np.random.default_rng(seed)
     d, L, E, I, k = cfg.d, cfg.latent, cfg.n_experts, cfg.inter, cfg.top_k
     S = cfg.n_shared * cfg.shared_inter
@@ -58,6 +58,8 @@ def smooth_loss(cfg, xf, wf, idx, dyf):
     situ = lambda v: b1 * np.tanh(v / b1) * sig(v)
     cap = lambda v: b2 * np.tanh(v / b2)
     h = xf @ wf["w_down"].T
+    if cfg.norm_after_down:   # the ablation variant's RMSNorm after the down-projection
+        h = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + cfg.rms_eps)
     s = sig(h @ wf["w_router"].T)
     z = np.zeros_like(h)
     for t in range(xf.shape[0]):
@@ -71,7 +73,8 @@ def smooth_loss(cfg, xf, wf, idx, dyf):
 
 
 @pytest.mark.parametrize("seed,kw", [(1, {}), (2, {"beta1": 1.5, "beta2": 2.0}),
-                                     (3, {"top_k": 6})])
+                                     (3, {"top_k": 6}), (8, {"norm_after_down": True}),
+                                     (9, {"norm_after_down": True, "beta1": 1.5, "beta2": 2.0})])
 def test_backward_matches_finite_differences(seed, kw):
     cfg, w, x, dy, idx = make_case(seed, **kw)
     g = oracle.layer_backward(cfg, x, w, idx, dy, round_mode=0)

@@ -160,7 +160,7 @@ int validate_config(const lmoe_config *c) {
     if (c->norm_after_down != 0 && c->norm_after_down != 1) return LMOE_ERR_INVALID_ARG;
     if (c->expert_fp8 != 0 && c->expert_fp8 != 1) return LMOE_ERR_INVALID_ARG;
     if (c->with_backward != 0 && c->with_backward != 1) return LMOE_ERR_INVALID_ARG;
-    if (c->with_backward && (c->norm_after_down || c->expert_fp8)) return LMOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->with_backward && c->expert_fp8) return LMOE_ERR_UNSUPPORTED_SHAPE;
     if (c->expert_fp8 && c->inter % 128) return LMOE_ERR_UNSUPPORTED_SHAPE;
     const int64_t S = int64_t(c->n_shared) * c->shared_inter;
     if (c->d % 64 || c->latent % 128 || c->inter % 64 || S % 64) return LMOE_ERR_UNSUPPORTED_SHAPE;
@@ -317,7 +317,7 @@ bool build_transposed(lmoe_handle *h) {
 // column segments.  Tp = T and Qmax = T*top_k + 64 E rounded up to 64;
 // Ep = E rounded up to 64.
 struct BwdLayout {
-    size_t ones, drs, dps, dz, u, dp, dgp, dl, dhp, dhr, dh, dyT, xT, rT, sT, dpsT, dhT, hT, dlT, segoff, qperm,
+    size_t ones, drs, dps, dz, u, dp, dgp, dl, dhp, dhr, dh, dhraw, dyT, xT, rT, sT, dpsT, dhT, hT, dlT, segoff, qperm,
         qtok, qgate, kt_a, kt_b, nkt, doT, aT, hgT, dpT, total;
     int64_t Tp, Ep, Qmax;
 };
@@ -349,6 +349,7 @@ BwdLayout bwd_layout(const lmoe_handle *h, int64_t T) {
     l.dhp = take(size_t(n * L) * 2);
     l.dhr = take(size_t(T * L) * 4);
     l.dh = take(size_t(T * L) * 2);
+    l.dhraw = take(size_t(T * L) * 2);   // norm-after-down variant: gradient at the down-projection's output
     l.dyT = take(size_t(d * l.Tp) * 2);
     l.xT = take(size_t(d * l.Tp) * 2);
     l.rT = take(size_t(L * l.Tp) * 2);
@@ -809,6 +810,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     // the forward's intermediates
     const uint8_t *fw = static_cast<const uint8_t *>(fwd_workspace);
     const uint16_t *hbuf = reinterpret_cast<const uint16_t *>(fw + fl.h);
+    // the latent the router and the experts read: h, or RMSNorm(h) in the
+    // norm-after-down variant (whose backward ends in that norm's backward)
+    const uint16_t *hlat = c.norm_after_down ? reinterpret_cast<const uint16_t *>(fw + fl.hn) : hbuf;
     const int32_t *idx = idx_in ? idx_in : reinterpret_cast<const int32_t *>(fw + fl.idx);
     const float *gates = gates_in ? gates_in : reinterpret_cast<const float *>(fw + fl.gates);
     const int32_t *offsets = reinterpret_cast<const int32_t *>(fw + fl.offsets);
@@ -827,7 +831,10 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     float *ones = reinterpret_cast<float *>(ws + bl.ones);
     uint16_t *drs = bf(bl.drs), *dps = bf(bl.dps), *dz = bf(bl.dz), *u = bf(bl.u), *dp = bf(bl.dp);
     float *dgp = reinterpret_cast<float *>(ws + bl.dgp);
-    uint16_t *dl = bf(bl.dl), *dhp = bf(bl.dhp), *dh = bf(bl.dh);
+    uint16_t *dl = bf(bl.dl), *dhp = bf(bl.dhp), *dh = bf(bl.dh), *dhraw = bf(bl.dhraw);
+    // the gradient at the down-projection's output: dh, or in the variant dh
+    // taken back through the norm after the down-projection
+    uint16_t *dhx = c.norm_after_down ? dhraw : dh;
     float *dhr = reinterpret_cast<float *>(ws + bl.dhr);
     uint16_t *dyT = bf(bl.dyT), *xT = bf(bl.xT), *rT = bf(bl.rT), *sT = bf(bl.sT), *dpsT = bf(bl.dpsT);
     uint16_t *dhT = bf(bl.dhT), *hT = bf(bl.hT), *dlT = bf(bl.dlT);
@@ -844,7 +851,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         m_doT, m_aT, m_hgT, m_dpT;
     if (!make_map(&m_dy, dy, T, d, d, kBM) || !make_map(&m_x, x, T, d, d, kBM) ||
         !make_map(&m_dp, dp, n, 2 * I, 2 * I, kBM) || !make_map(&m_dl, dl, T, Ep, Ep, kBM) ||
-        !make_map(&m_dh, dh, T, L, L, kBM) || !make_map(&m_dps, dps, T, 2 * S, 2 * S, kBM) ||
+        !make_map(&m_dh, dhx, T, L, L, kBM) || !make_map(&m_dps, dps, T, 2 * S, 2 * S, kBM) ||
         !make_map(&m_dyT, dyT, d, Tp, Tp, kBM) || !make_map(&m_xT, xT, d, Tp, Tp, h->bn_up) ||
         !make_map(&m_rT, rT, L, Tp, Tp, h->bn_down) || !make_map(&m_sT, sT, S, Tp, Tp, h->bn_s) ||
         !make_map(&m_dps1T, dpsT, S, Tp, Tp, kBM) || !make_map(&m_dps2T, dpsT + S * Tp, S, Tp, Tp, kBM) ||
@@ -888,11 +895,11 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     auto copies_inputs = [&]() {   // inputs of the backward: dy, x and the forward's r, act_s, h
         return tr(dy, d, Tl, di, dyT, Tp, nullptr, nullptr, nullptr) && tr(x, d, Tl, di, xT, Tp, nullptr, nullptr, nullptr) &&
                tr(rbuf, L, Tl, Li, rT, Tp, nullptr, nullptr, nullptr) &&
-               tr(sact, S, Tl, Si, sT, Tp, nullptr, nullptr, nullptr) && tr(hbuf, L, Tl, Li, hT, Tp, nullptr, nullptr, nullptr);
+               tr(sact, S, Tl, Si, sT, Tp, nullptr, nullptr, nullptr) && tr(hlat, L, Tl, Li, hT, Tp, nullptr, nullptr, nullptr);
     };
     auto copies_dps = [&]() { return tr(dps, 2 * S, Tl, 2 * Si, dpsT, Tp, nullptr, nullptr, nullptr); };
     auto copies_dl = [&]() { return tr(dl, Ep, Tl, Ei, dlT, Tp, nullptr, nullptr, nullptr); };
-    auto copies_dh = [&]() { return tr(dh, L, Tl, Li, dhT, Tp, nullptr, nullptr, nullptr); };
+    auto copies_dh = [&]() { return tr(dhx, L, Tl, Li, dhT, Tp, nullptr, nullptr, nullptr); };
     const int mt_a = static_cast<int>(L / kBM), mt_b = static_cast<int>(ceil_div(2 * I, kBM));
     auto copies_segments = [&]() {   // after dz and dp exist
         return ok(launch_segments(offsets, perm, tokrow, gates, Ei, segoff, qperm, qtok, qgate, kt_a, mt_a, kt_b,
@@ -902,7 +909,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                // column segment, K-block packed ([Qmax / 64][rows][64])
                tr(dz, L, Tl, Li, doT, Qmax, qtok, qgate, nkt + 2, true) &&
                tr(act, I, n, Ii, aT, Qmax, qperm, nullptr, nkt + 2, true) &&
-               tr(hbuf, L, Tl, Li, hgT, Qmax, qtok, nullptr, nkt + 2, true) &&
+               tr(hlat, L, Tl, Li, hgT, Qmax, qtok, nullptr, nkt + 2, true) &&
                tr(dp, 2 * I, n, 2 * Ii, dpT, Qmax, qperm, nullptr, nkt + 2, true);
     };
     if (overlap && !(fork(0) && copies_inputs())) return LMOE_ERR_CUDA;
@@ -977,7 +984,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.b_expert_rows = static_cast<int32_t>(I);
         a.b_packed = 1;
         a.b_row_tiles = nq;
-        a.gather_src = hbuf;
+        a.gather_src = hlat;
         a.gather_rows = tokrow;
         a.gather_ld = L;
         a.tiles = tiles;
@@ -1000,7 +1007,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
 
     mark(LMOE_BWD_STAGE_ROUTER);
     // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
-    if (!ok(launch_router_bwd(dgp, nq, inv, idx, hbuf, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
+    if (!ok(launch_router_bwd(dgp, nq, inv, idx, hlat, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
                               stream)))
         return LMOE_ERR_CUDA;
     if (overlap && !(fork(2) && copies_dl())) return LMOE_ERR_CUDA;
@@ -1039,6 +1046,12 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     }
     mark(LMOE_BWD_STAGE_DH_SUM);
     if (!ok(launch_dh_sum(dhp, dhr, T, Ki, Li, dh, h->num_sms, stream))) return LMOE_ERR_CUDA;
+    // norm-after-down variant: dh is the gradient at RMSNorm(h); take it back
+    // through that norm (the same kernel as the aggregate's norm, one row per
+    // token: z = h) to the down-projection's output
+    if (c.norm_after_down &&
+        !ok(launch_rms_bwd(hbuf, T, 1, Li, c.rms_eps, dh, L, dhraw, stream)))
+        return LMOE_ERR_CUDA;
     // side stream: the last token-major copy, then (join point 4 for the dense
     // weight gradients) the per-expert segments, which so run next to dx and
     // the dense weight-gradient GEMMs (join point 5 for the experts')

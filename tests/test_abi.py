@@ -71,8 +71,9 @@ def test_host_entry_points_reject_bad_arguments_without_gpu():
 
 
 def test_backward_handle_rejects_variants_without_gpu():
-    """with_backward covers K3's layer only: a config that also sets a variant
-    flag is rejected while validating the config (before any CUDA call)."""
+    """with_backward covers the bf16 layer (with or without the norm after the
+    down-projection): a config that also sets expert_fp8 is rejected while
+    validating the config (before any CUDA call)."""
     from sparse_moe_layer_bias_gb300 import build, binding
     lib = ctypes.CDLL(build.build())
     P = ctypes.c_void_p
@@ -80,9 +81,9 @@ def test_backward_handle_rejects_variants_without_gpu():
                                 ctypes.POINTER(P)]
     w = binding.LmoeWeights()
     out = P()
-    for norm, fp8, expect in ((1, 0, 2), (0, 1, 2), (0, 0, 1)):
+    for norm, fp8, expect in ((1, 0, 1), (0, 1, 2), (0, 0, 1)):
         cfg = binding.LmoeConfig(256, 128, 32, 4, 128, 2, 64, 4.0, 25.0, 1e-6, 64, norm, fp8, 1)
-        # (0, 0): valid config, so the null weights are what gets rejected
+        # valid configs: the null weights are what gets rejected
         assert lib.lmoe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(out)) == expect
     cfg = binding.LmoeConfig(256, 128, 32, 4, 128, 2, 64, 4.0, 25.0, 1e-6, 64, 0, 0, 2)
     assert lib.lmoe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(out)) == 1

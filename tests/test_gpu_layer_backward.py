@@ -11,6 +11,8 @@ element), so the expected error is about sqrt(6) * 1.1e-3 = 2.7e-3; the bar
 leaves a factor of about 4.  The largest element error must stay within
 BWD_MAX_REL of the gradient's largest element.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -86,6 +88,19 @@ def test_backward_small(lm):
     # several tiles of every GEMM and a ragged token count
     shape = synth.SMALL
     check_backward(shape, run_backward(lm, shape, T=1000))
+
+
+@pytest.mark.parametrize("T", [None, 129])
+def test_backward_norm_after_down_variant_tiny(lm, T):
+    """The ablation variant (RMSNorm after the down-projection as well): its
+    gradient also goes through that norm's backward."""
+    shape = dataclasses.replace(synth.TINY, norm_after_down=True)
+    check_backward(shape, run_backward(lm, shape, T=T, seed_offset=21))
+
+
+def test_backward_norm_after_down_variant_small(lm):
+    shape = dataclasses.replace(synth.SMALL, norm_after_down=True)
+    check_backward(shape, run_backward(lm, shape, T=1000, seed_offset=22))
 
 
 def test_backward_is_deterministic(lm):

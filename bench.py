@@ -98,7 +98,7 @@ def layer_work(shape, T, counts, fp8=False):
 # DRAM read+write over algorithmic bytes of the backward's per-expert weight-
 # gradient GEMMs, from ncu on --profile-case --backward
 # (profiles/backward_expert_wgrad_gemm_ncu_small.md)
-BWD_TRAFFIC_RATIO = {"wgrad_w3": 0.901, "wgrad_w12": 0.946}
+BWD_TRAFFIC_RATIO = {"wgrad_w3": 0.901, "wgrad_w12": 0.944}
 
 
 def backward_work(shape, T, counts):

@@ -60,9 +60,7 @@ struct Cfg {
     static constexpr int kABytes = kSub * kBM * kBK * 2; // 16 or 32 KB
     static constexpr int kBBytes = BN * kBK * 2;        // 16 or 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
-    // K segments are a few K blocks long: 3 stages leave room for the
-    // epilogue's TMA-store buffers
-    static constexpr int kStages = KSEG ? 3 : (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
+    static constexpr int kStages = (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
     static constexpr int kBarBytes = 256;
     // per epilogue warp: 32 rows x 64 bf16, row pitch 144 B (16 B of padding
     // keeps the 16-byte row writes and the 128-byte row reads conflict-free)
@@ -73,9 +71,9 @@ struct Cfg {
     static constexpr int kColWarpBytes = 1024;
     // K segments (fp32 weight gradients): per epilogue warp two 4 KB buffers
     // of a 32 x 32 fp32 block in the 128B-swizzled layout of a TMA store,
-    // 1024-byte aligned
-    static constexpr size_t kTmaStgOffset =
-        (size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes + 1023) / 1024 * 1024;
+    // 1024-byte aligned, in place of the staging and scale-factor areas the
+    // other epilogues use (which leaves room for the full stage ring)
+    static constexpr size_t kTmaStgOffset = (size_t(kStages) * kStageBytes + kBarBytes + 1023) / 1024 * 1024;
     static constexpr int kTmaStgWarpBytes = 2 * 4096;
     static constexpr size_t kSmem =
         KSEG ? 1024 + kTmaStgOffset + 4 * kTmaStgWarpBytes

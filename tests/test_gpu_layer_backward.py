@@ -271,3 +271,20 @@ def test_backward_accumulates_into_gradients(lm):
     assert torch.equal(dx1, dx2)
     for n in g1:
         assert torch.equal(acc[n], init[n] + g1[n]), n
+
+
+def test_backward_stage_hook_gives_the_same_bits(lm):
+    """With the timing hook the backward runs every stage in stream order (no
+    side stream); the gradients are the same bits as the overlapped default."""
+    shape = synth.TINY
+    run = run_backward(lm, shape, T=300, seed_offset=31)
+    x, dy = run["x_host"].cuda(), run["dy_host"].cuda()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(lm.BWD_STAGES) + 1)]
+    lm.lmoe_set_backward_events(run["h"], evs)
+    dx2, g2 = lm.lmoe_backward(run["h"], x, dy, run["ws"])
+    torch.cuda.synchronize()
+    lm.lmoe_set_backward_events(run["h"], None)
+    assert all(evs[j].elapsed_time(evs[j + 1]) >= 0 for j in range(len(evs) - 1))
+    assert torch.equal(run["dx"], dx2)
+    for n, t in run["grads"].items():
+        assert torch.equal(t, g2[n]), n

@@ -246,6 +246,20 @@ def test_tiny_layer_ragged_token_counts(lm, T):
     end_to_end(synth.TINY, run)
 
 
+# Widths off the usual tiles: d and the shared width not multiples of 128 (ragged
+# N tiles), E = 10 (router tile mostly empty, E not a multiple of 8), k = 3,
+# routed intermediate 192 (three 64-feature SiTU-GLU tiles), one shared expert,
+# T = 97.
+ODD = synth.LayerShape("odd", T=97, d=192, latent=128, n_experts=10, top_k=3, inter=192, n_shared=1,
+                       shared_inter=192, seed=1009)
+
+
+def test_odd_shape_layer_stages_and_end_to_end(lm):
+    run = run_host_shape(lm, ODD)
+    staged_checks(ODD, run)
+    end_to_end(ODD, run)
+
+
 def test_forward_is_deterministic(lm):
     shape = synth.TINY
     w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}

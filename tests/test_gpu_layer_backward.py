@@ -103,6 +103,14 @@ def test_backward_norm_after_down_variant_small(lm):
     check_backward(shape, run_backward(lm, shape, T=1000, seed_offset=22))
 
 
+def test_backward_odd_shape(lm):
+    """Widths off the usual tiles (see test_gpu_layer.ODD): ragged N tiles,
+    E = 10 (the router's transposes take their element-wise tail), k = 3,
+    intermediate 192 (dW1 | dW2 rows split inside a 128-row tile)."""
+    from test_gpu_layer import ODD
+    check_backward(ODD, run_backward(lm, ODD))
+
+
 def test_backward_is_deterministic(lm):
     shape = synth.TINY
     run = run_backward(lm, shape)

@@ -254,6 +254,18 @@ ODD = synth.LayerShape("odd", T=97, d=192, latent=128, n_experts=10, top_k=3, in
                        shared_inter=192, seed=1009)
 
 
+# Every expert chosen by every token (k = E): no routing margin at all, each
+# expert holds all T rows.
+ALL_EXPERTS = synth.LayerShape("all_experts", T=200, d=256, latent=128, n_experts=8, top_k=8, inter=64,
+                               n_shared=2, shared_inter=64, seed=1010)
+
+
+def test_all_experts_layer_stages_and_end_to_end(lm):
+    run = run_host_shape(lm, ALL_EXPERTS)
+    staged_checks(ALL_EXPERTS, run)
+    end_to_end(ALL_EXPERTS, run)
+
+
 def test_odd_shape_layer_stages_and_end_to_end(lm):
     run = run_host_shape(lm, ODD)
     staged_checks(ODD, run)

@@ -111,6 +111,13 @@ def test_backward_odd_shape(lm):
     check_backward(ODD, run_backward(lm, ODD))
 
 
+def test_backward_all_experts(lm):
+    """k = E: every expert holds all T rows (several 128-row tiles and K
+    segments per expert)."""
+    from test_gpu_layer import ALL_EXPERTS
+    check_backward(ALL_EXPERTS, run_backward(lm, ALL_EXPERTS))
+
+
 def test_backward_is_deterministic(lm):
     shape = synth.TINY
     run = run_backward(lm, shape)

@@ -260,6 +260,17 @@ ALL_EXPERTS = synth.LayerShape("all_experts", T=200, d=256, latent=128, n_expert
                                n_shared=2, shared_inter=64, seed=1010)
 
 
+# The largest routing the library takes: E = 1024 experts, top-32.
+MAX_ROUTING = synth.LayerShape("max_routing", T=150, d=256, latent=128, n_experts=1024, top_k=32, inter=64,
+                               n_shared=2, shared_inter=64, seed=1011)
+
+
+def test_max_routing_layer_stages_and_end_to_end(lm):
+    run = run_host_shape(lm, MAX_ROUTING)
+    staged_checks(MAX_ROUTING, run)
+    end_to_end(MAX_ROUTING, run)
+
+
 def test_all_experts_layer_stages_and_end_to_end(lm):
     run = run_host_shape(lm, ALL_EXPERTS)
     staged_checks(ALL_EXPERTS, run)

@@ -118,6 +118,12 @@ def test_backward_all_experts(lm):
     check_backward(ALL_EXPERTS, run_backward(lm, ALL_EXPERTS))
 
 
+def test_backward_max_routing(lm):
+    """E = 1024 (one thread per expert in the segment scan), top-32."""
+    from test_gpu_layer import MAX_ROUTING
+    check_backward(MAX_ROUTING, run_backward(lm, MAX_ROUTING))
+
+
 def test_backward_is_deterministic(lm):
     shape = synth.TINY
     run = run_backward(lm, shape)

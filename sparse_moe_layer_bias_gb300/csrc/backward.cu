@@ -28,14 +28,15 @@ constexpr int kTT = 64;  // transpose tile: 64 x 64 elements
 // src(q) = qsrc[q] (or q when q < R without qsrc) and a negative src gives 0.
 // Tiles whose first q is at or past *q_limit are skipped (never read later).
 // 16-byte accesses on both sides: a thread loads 8 columns of one source row
-// and stores 8 consecutive q of one output row.  With packed_rows > 0 the
-// output is K-block packed: element (c, q) sits at
-// ((q / 64) * packed_rows + c) * 64 + q % 64, so each 64-column block of q is
-// one contiguous [packed_rows][64] slab and a TMA box of consecutive rows in
-// it is one contiguous run of memory (ldo and obs are then unused).  The shared tile is stored
-// with its 16-byte chunks XOR-swizzled by (q / 8) % 8 so that the column reads
-// of the store phase spread over the banks.  Requires ldi, ldo, the batch
-// strides and the pointers to be multiples of 8 elements (16 bytes).
+// and stores 8 consecutive q of one output row (element-wise at a ragged C or
+// Q).  With packed_rows > 0 the output is K-block packed: element (c, q) sits
+// at ((q / 64) * packed_rows + c) * 64 + q % 64, so each 64-column block of q
+// is one contiguous [packed_rows][64] slab and a TMA box of consecutive rows
+// in it is one contiguous run of memory (ldo and obs are then unused).  The
+// shared tile is stored with its 16-byte chunks XOR-swizzled by (q / 8) % 8 so
+// that the column reads of the store phase spread over the banks.  Requires
+// ldi, ldo, the batch strides and the pointers to be multiples of 8 elements
+// (16 bytes).
 __device__ __forceinline__ int swz(int q, int c) { return q * kTT + ((((c >> 3) ^ (q >> 3)) & 7) << 3) + (c & 7); }
 
 __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restrict__ in, int64_t ldi, int64_t ibs,

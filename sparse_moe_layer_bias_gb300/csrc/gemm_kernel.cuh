@@ -579,7 +579,12 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 // fp32 rows (dense weight gradients, the router's share of the
                 // latent gradient): staged like the scores above; accumulate
                 // adds instead of storing (each element has one writer)
-                float *dst = reinterpret_cast<float *>(args.out) + int64_t(ti.row0 + trow) * args.ld_out;
+                // with out2, rows from m_split on go to out2 (two weights' gradients
+                // of one GEMM, e.g. the shared experts' dWs1 | dWs2)
+                const int64_t r = ti.row0 + trow;
+                float *dst = (args.out2 && r >= args.m_split)
+                                 ? reinterpret_cast<float *>(args.out2) + (r - args.m_split) * args.ld_out
+                                 : reinterpret_cast<float *>(args.out) + r * args.ld_out;
                 const bool vec_ok = (args.ld_out % 4) == 0;
                 const unsigned long long dbits = reinterpret_cast<unsigned long long>(dst);
 #pragma unroll 1

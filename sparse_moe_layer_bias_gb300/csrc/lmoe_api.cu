@@ -847,14 +847,14 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     int32_t *nkt = reinterpret_cast<int32_t *>(ws + bl.nkt);
     uint16_t *doT = bf(bl.doT), *aT = bf(bl.aT), *hgT = bf(bl.hgT), *dpT = bf(bl.dpT);
 
-    CUtensorMap m_dy, m_x, m_dp, m_dl, m_dh, m_dps, m_dyT, m_xT, m_rT, m_sT, m_dps1T, m_dps2T, m_dhT, m_hT, m_dlT,
+    CUtensorMap m_dy, m_x, m_dp, m_dl, m_dh, m_dps, m_dyT, m_xT, m_rT, m_sT, m_dpsT, m_dhT, m_hT, m_dlT,
         m_doT, m_aT, m_hgT, m_dpT;
     if (!make_map(&m_dy, dy, T, d, d, kBM) || !make_map(&m_x, x, T, d, d, kBM) ||
         !make_map(&m_dp, dp, n, 2 * I, 2 * I, kBM) || !make_map(&m_dl, dl, T, Ep, Ep, kBM) ||
         !make_map(&m_dh, dhx, T, L, L, kBM) || !make_map(&m_dps, dps, T, 2 * S, 2 * S, kBM) ||
         !make_map(&m_dyT, dyT, d, Tp, Tp, kBM) || !make_map(&m_xT, xT, d, Tp, Tp, h->bn_up) ||
         !make_map(&m_rT, rT, L, Tp, Tp, h->bn_down) || !make_map(&m_sT, sT, S, Tp, Tp, h->bn_s) ||
-        !make_map(&m_dps1T, dpsT, S, Tp, Tp, kBM) || !make_map(&m_dps2T, dpsT + S * Tp, S, Tp, Tp, kBM) ||
+        !make_map(&m_dpsT, dpsT, 2 * S, Tp, Tp, kBM) ||
         !make_map(&m_dhT, dhT, L, Tp, Tp, kBM) || !make_map(&m_hT, hT, L, Tp, Tp, h->bn_down) ||
         !make_map(&m_dlT, dlT, E, Tp, Tp, kBM) ||
         // K-block packed segment copies: [Qmax / 64 * rows][64]
@@ -1081,7 +1081,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     } else if (!(copies_inputs() && copies_dps() && copies_dh() && copies_dl())) {
         return LMOE_ERR_CUDA;
     }
-    auto wgrad = [&](const CUtensorMap &ma, const CUtensorMap &mb, int64_t M, int64_t N, int bn, float *out) {
+    auto wgrad = [&](const CUtensorMap &ma, const CUtensorMap &mb, int64_t M, int64_t N, int bn, float *out,
+                     float *out2 = nullptr, int64_t m_split = 0) {
         GemmMaps m{ma, ma, mb, mb};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(M);
@@ -1089,6 +1090,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.n_tiles = static_cast<int32_t>(ceil_div(N, bn));
         a.k_blocks = static_cast<int32_t>(Tp / kBK);
         a.out = out;
+        a.out2 = out2;
+        a.m_split = static_cast<int32_t>(m_split);
         a.ld_out = N;
         a.out_cols = static_cast<int32_t>(N);
         a.accumulate = g->accumulate;
@@ -1097,7 +1100,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     };
     mark(LMOE_BWD_STAGE_WGRAD_DENSE);
     if ((st = wgrad(m_dyT, m_rT, d, L, h->bn_down, g->w_up)) || (st = wgrad(m_dyT, m_sT, d, S, h->bn_s, g->ws3)) ||
-        (st = wgrad(m_dps1T, m_xT, S, d, h->bn_up, g->ws1)) || (st = wgrad(m_dps2T, m_xT, S, d, h->bn_up, g->ws2)) ||
+        // dWs1 | dWs2 in one GEMM over the 2S rows of dp_s^T (rows from S on go to dWs2)
+        (st = wgrad(m_dpsT, m_xT, 2 * S, d, h->bn_up, g->ws1, g->ws2, S)) ||
         (st = wgrad(m_dhT, m_xT, L, d, h->bn_up, g->w_down)) || (st = wgrad(m_dlT, m_hT, E, L, h->bn_down, g->w_router)))
         return st;
     // ---- weight gradients of the routed experts: K = each expert's own assignments

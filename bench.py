@@ -352,7 +352,7 @@ def fp8_experts_variant(lm, stream, steps, warmup, shape, w, x, bias, dshape, wd
     return out
 
 
-def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src):
+def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src, world=1):
     """The layer's backward at the K3 prefill shape: dx and the fp32 weight
     gradients for an upstream gradient dy ~ N(0, 1), after one forward of the
     same batch.  Timed over `steps` backward passes (weights and activations
@@ -380,7 +380,7 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src)
         bstep()
     b1.record(stream)
     torch.cuda.synchronize()
-    ms = b0.elapsed_time(b1) / steps
+    ms = max_over_ranks(world, b0.elapsed_time(b1) / steps)   # each rank runs its own batch
     nst = len(lm.BWD_STAGES)
     ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
     for evs in ev_sets:
@@ -422,7 +422,7 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src)
                 peak_source=peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " hbm copy"))
     model_flop = 2.0 * layer_flops_per_token(shape) * T      # data + weight gradients of every GEMM
     executed = sum(v[0] for v in work.values())
-    out = {"T": T, "ms": round(ms, 4), "tokens_per_s": T / (ms * 1e-3),
+    out = {"T": T, "ms": round(ms, 4), "tokens_per_s": world * T / (ms * 1e-3),
            "model_tflops": round(model_flop / (ms * 1e-3) / 1e12, 2),
            "frac_bf16_peak": round(model_flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
            "executed_tflop": round(executed / 1e12, 3), "weight_grad_dtype": "f32",
@@ -790,7 +790,7 @@ def main():
     fp8 = fp8_experts_variant(lm, stream, args.steps, args.warmup, shape, w, x, bias, dshape, wd, xd, bd, peaks)
 
     # --------------------------------------------------------------- backward pass
-    bwd = backward_pass(lm, stream, args.steps, args.warmup, shape, w, x, bias, peaks, peak_src)
+    bwd = backward_pass(lm, stream, args.steps, args.warmup, shape, w, x, bias, peaks, peak_src, world)
 
     # --------------------------------------------------------------- CPU oracle baseline
     cpu = None

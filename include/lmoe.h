@@ -54,7 +54,7 @@ const char *lmoe_status_string(int status);
 /* Shape of one Stable LatentMoE layer.  [DD] section 2: d -> d/2 latent,
  * 2n routed experts of which 2k are active per token; [NW] "LatentMoE": K3 has
  * d = 7168, latent 3584, 896 experts, 16 active, 2 shared experts.
- * Supported: d, latent, inter, n_shared*shared_inter multiples of 64;
+ * Supported: d, inter, n_shared*shared_inter multiples of 64, latent a multiple of 128;
  * 1 <= top_k <= 32; top_k <= n_experts <= 1024; max_tokens >= 0. */
 typedef struct {
     int32_t d;            /* hidden size                                      */
@@ -90,7 +90,9 @@ typedef struct {
                            * every weight (about as much device memory again as
                            * the weights) so that lmoe_backward can run; 0: the
                            * handle serves forwards only.  The backward covers
-                           * K3's layer: norm_after_down = expert_fp8 = 0. */
+                           * K3's layer and the norm_after_down variant;
+                           * with_backward together with expert_fp8 returns
+                           * LMOE_ERR_UNSUPPORTED_SHAPE. */
 } lmoe_config;
 
 /* Weight pointers (device, bf16, row-major, K-major rows as "out x in").

@@ -105,7 +105,8 @@ def backward_work(shape, T, counts):
     """Algorithmic FLOPs and bytes of each backward stage for T tokens with
     per-expert assignment counts `counts` (bf16 2 bytes, fp32 4 bytes; weight
     gradients are written in fp32).  The routed and shared SiTU-GLU stages
-    recompute their pre-activations (counted in their FLOPs)."""
+    are element-wise: they read the pre-activations p1 | p2 the training
+    forward kept (bf16) and the activation gradient, and write dp1 | dp2."""
     d, L, E, k, I = shape.d, shape.latent, shape.n_experts, shape.top_k, shape.inter
     S = shape.n_shared * shape.shared_inter
     counts = np.asarray(counts)
@@ -113,15 +114,15 @@ def backward_work(shape, T, counts):
     Ep = -(-E // 64) * 64
     touched = int((counts > 0).sum())
     cols = int(((counts + 63) // 64 * 64).sum())      # per-expert segments, padded to 64
-    nq = I // 128 if I % 128 == 0 else I // 64         # SiTU-GLU tiles per expert row
     dense = d * L + d * S + 2 * S * d + L * d + E * L  # elements of the six dense weight gradients
     w = {}
     w["dr"] = (2.0 * T * d * (L + S), 2.0 * (T * d + (L + S) * d + T * (L + S)))
-    w["shared"] = (4.0 * T * d * S, 2.0 * (T * d + 2 * S * d + T * S + 2 * T * S))
+    w["shared"] = (0.0, 2.0 * (2 * T * S + T * S + 2 * T * S))
     w["rmsnorm"] = (0.0, 2.0 * (n * L + T * L + T * L))
     w["expert_u"] = (2.0 * n * L * I, 2.0 * (touched * I * L + T * L + n * I))
-    w["expert_glu"] = (4.0 * n * L * I, 2.0 * (touched * 2 * I * L + T * L + n * I + 2 * n * I) + 4.0 * n * nq)
-    w["router"] = (2.0 * n * L, 2.0 * (T * L + E * L + T * Ep) + 4.0 * n * nq + 8.0 * n)
+    # p1 | p2 and u in, dp1 | dp2 out; the row's gate (through perm) in, dgate out
+    w["expert_glu"] = (0.0, 2.0 * (2 * n * I + n * I + 2 * n * I) + 12.0 * n)
+    w["router"] = (2.0 * n * L, 2.0 * (T * L + E * L + T * Ep) + 4.0 * n + 8.0 * n)
     w["dh_experts"] = (4.0 * n * I * L, 2.0 * (touched * 2 * I * L + 2 * n * I + n * L))
     w["dh_router"] = (2.0 * T * Ep * L, 2.0 * (T * Ep + L * Ep) + 4.0 * T * L)
     w["dh_sum"] = (0.0, 2.0 * n * L + 4.0 * T * L + 2.0 * T * L)
@@ -365,7 +366,19 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src,
     dy = synth.grad_output_device(shape)
     dx = torch.empty_like(x)
     counts = torch.empty(shape.n_experts, dtype=torch.int32, device="cuda")
-    lm.lmoe_forward(hb, x, bias, workspace=ws, expert_counts_out=counts, stream=stream)
+
+    def fstep():   # the training forward: also keeps the SiTU-GLU pre-activations
+        lm.lmoe_forward(hb, x, bias, workspace=ws, expert_counts_out=counts, stream=stream)
+
+    for _ in range(warmup):
+        fstep()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(steps):
+        fstep()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = max_over_ranks(world, f0.elapsed_time(f1) / steps)
 
     def bstep():
         lm.lmoe_backward(hb, x, dy, ws, dx=dx, grads=grads, workspace=bws, stream=stream)
@@ -423,6 +436,7 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src,
     model_flop = 2.0 * layer_flops_per_token(shape) * T      # data + weight gradients of every GEMM
     executed = sum(v[0] for v in work.values())
     out = {"T": T, "ms": round(ms, 4), "tokens_per_s": world * T / (ms * 1e-3),
+           "training_forward_ms": round(fwd_ms, 4), "training_step_ms": round(fwd_ms + ms, 4),
            "model_tflops": round(model_flop / (ms * 1e-3) / 1e12, 2),
            "frac_bf16_peak": round(model_flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
            "executed_tflop": round(executed / 1e12, 3), "weight_grad_dtype": "f32",

@@ -88,7 +88,10 @@ typedef struct {
                            * max|row| <= 448 * 2^e. */
     int32_t with_backward; /* 1: lmoe_create also keeps transposed copies of
                            * every weight (about as much device memory again as
-                           * the weights) so that lmoe_backward can run; 0: the
+                           * the weights) so that lmoe_backward can run, and
+                           * lmoe_forward also keeps the SiTU-GLU pre-activations
+                           * in its workspace (pre_act, shared_pre_act: p1 | p2
+                           * in bf16, 4 bytes per activation element) for it; 0: the
                            * handle serves forwards only.  The backward covers
                            * K3's layer and the norm_after_down variant;
                            * with_backward together with expert_fp8 returns
@@ -151,6 +154,9 @@ typedef struct {
     int64_t h_norm;   /* [T][latent] bf16        RMSNorm(h) when norm_after_down, else -1 */
     int64_t h_fp8;    /* [T][latent] e4m3 codes of the routed latent (expert_fp8), else -1 */
     int64_t h_fp8_exp; /* [T] int8 scale exponents of those rows (expert_fp8), else -1 */
+    int64_t pre_act;  /* [T*top_k][2*inter] bf16 SiTU-GLU pre-activations W1[e] h | W2[e] h of
+                       * each permuted row (with_backward, read by lmoe_backward), else -1 */
+    int64_t shared_pre_act; /* [T][2*S] bf16 the shared experts' Ws1 x | Ws2 x (with_backward), else -1 */
 } lmoe_ws_layout;
 
 int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *layout);
@@ -274,11 +280,12 @@ int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *b
  * router's gradient flows through the gates (gate = sigmoid(w_router[e] . h)).
  * The selection bias gets none.  The bf16 roundings of the forward pass the
  * gradient through unchanged.  Per token:
- *   dr  = W_up^T dy,  da_s = Ws3^T dy  (shared experts: SiTU-GLU backward on
- *         the recomputed Ws1 x, Ws2 x)
+ *   dr  = W_up^T dy,  da_s = Ws3^T dy  (shared experts: SiTU-GLU backward at
+ *         the forward's kept Ws1 x, Ws2 x)
  *   dz  = RMSNorm backward of dr at z = sum of the forward's rows o
  *   per chosen expert: u = W3[e]^T dz; da = gate * u; dgate = u . act;
- *         dp1, dp2 = SiTU-GLU backward on the recomputed W1[e] h, W2[e] h;
+ *         dp1, dp2 = SiTU-GLU backward at the forward's kept W1[e] h, W2[e] h
+ *         (bf16);
  *         dh += W1[e]^T dp1 + W2[e]^T dp2 + w_router[e] dgate sigma'(logit)
  *   dx  = W_down^T dh + Ws1^T dp_s1 + Ws2^T dp_s2
  * and the weight gradients are the sums over tokens of the matching outer
@@ -286,7 +293,8 @@ int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *b
  * gate dz act^T, dW1[e] = sum dp1 h^T).
  * The forward's intermediates are read from fwd_workspace (the workspace of
  * that forward, unchanged since; its layout for T): h, perm, inv, the
- * permuted activations, the rows o, r, the shared activations and the tile
+ * permuted activations and pre-activations, the rows o, r, the shared
+ * activations and pre-activations and the tile
  * lists, and the offsets of the expert groups (always in the workspace; the
  * per-expert counts are their differences).  topk_idx, gates: the forward's
  * outputs when the caller had it write them to its own buffers (they are then

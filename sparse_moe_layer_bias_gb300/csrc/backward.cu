@@ -2,7 +2,8 @@
 // transposes (plain, or gathering the rows of each expert's assignments into
 // a padded per-expert column segment), the per-expert segment maps and
 // weight-gradient tile lists, the RMSNorm backward, the router backward, the
-// latent-gradient sum and the zeroing of unused experts' weight gradients.
+// latent-gradient sum, the zeroing of unused experts' weight gradients and
+// the SiTU-GLU backward at the pre-activations the forward kept.
 //
 // The gradient follows "Kimi-K3-Architecture-Deep-Dive" section 2 (the chain
 // down-projection -> routed experts -> aggregate -> RMSNorm -> up-projection)
@@ -363,6 +364,106 @@ __global__ void __launch_bounds__(256) dh_sum_kernel(const uint16_t *__restrict_
     }
 }
 
+// SiTU-GLU backward of one row per warp, at the saved pre-activations:
+//   p1 = P[r][f], p2 = P[r][p_half + f], da = g_r * U[r][u_col0 + f]
+//   dP[r][f] = da SiTU'(p1) softcap(p2), dP[r][dp_half + f] = da SiTU(p1) softcap'(p2)
+//   dg[r] = sum_f U[r][u_col0 + f] SiTU(p1) softcap(p2)    (when dg is given)
+// with g_r = scale[scale_rows[r]] (1 without scale).  C features per row, a
+// multiple of 8; each lane takes 8 consecutive features per step (16-byte
+// accesses), two steps in flight.  Strides and offsets are multiples of 8
+// elements.
+// tanh(y) and its derivative 1 - tanh(y)^2 from one exponential: with
+// u = e^(-2|y|), tanh(y) = sign(y) (1 - u) / (1 + u) and
+// 1 - tanh(y)^2 = 4u / (1 + u)^2.  The derivative keeps its relative accuracy
+// where tanh saturates (1 - t*t from an approximate t would not).
+__device__ __forceinline__ void tanh_and_slope(float y, float &t, float &slope) {
+    const float u = __expf(-2.0f * fabsf(y));
+    const float inv = __fdividef(1.0f, 1.0f + u);   // 1 + u in [1, 2]
+    t = copysignf((1.0f - u) * inv, y);
+    slope = 4.0f * u * inv * inv;
+}
+
+// Backward of one SiTU-GLU element ("Kimi-K3-Architecture-Deep-Dive" section 1:
+// the tanh softcap is differentiable everywhere).  With sigma = sigmoid(p1):
+//   SiTU   = b1 tanh(p1/b1) sigma        SiTU'   = (1 - tanh^2) sigma + SiTU (1 - sigma)
+//   softcap = b2 tanh(p2/b2)             softcap' = 1 - tanh^2(p2/b2)
+// da is the activation's gradient; returns act = SiTU softcap as well.
+__device__ __forceinline__ void situ_glu_bwd(float p1, float p2, float da, float b1, float ib1, float b2,
+                                             float ib2, float &dp1, float &dp2, float &act) {
+    float t1, s1, t2, s2;
+    tanh_and_slope(p1 * ib1, t1, s1);
+    tanh_and_slope(p2 * ib2, t2, s2);
+    const float sig = __fdividef(1.0f, 1.0f + __expf(-p1));   // 0 once e^(-p1) passes 2^126
+    const float situ = b1 * t1 * sig;
+    const float dsitu = s1 * sig + situ * (1.0f - sig);
+    const float cap = b2 * t2;
+    dp1 = da * dsitu * cap;
+    dp2 = da * situ * s2;
+    act = situ * cap;
+}
+
+constexpr int kGluWarps = 8;
+__global__ void __launch_bounds__(kGluWarps * 32) glu_bwd_rows_kernel(
+    const uint16_t *__restrict__ P, int64_t p_ld, int p_half, const uint16_t *__restrict__ U, int64_t u_ld,
+    int u_col0, const int32_t *__restrict__ scale_rows, const float *__restrict__ scale, int64_t rows, int C,
+    float b1, float b2, uint16_t *__restrict__ dP, int64_t dp_ld, int dp_half, float *__restrict__ dg) {
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = int64_t(blockIdx.x) * kGluWarps + (threadIdx.x >> 5);
+    const int64_t nwarps = int64_t(gridDim.x) * kGluWarps;
+    const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;   // once per thread
+    const int chunks = C >> 3;
+    for (int64_t r = warp0; r < rows; r += nwarps) {
+        const float g = scale ? scale[scale_rows ? scale_rows[r] : r] : 1.0f;
+        const uint16_t *p1r = P + r * p_ld, *p2r = p1r + p_half, *ur = U + r * u_ld + u_col0;
+        uint16_t *d1r = dP + r * dp_ld, *d2r = d1r + dp_half;
+        float acc = 0.0f;
+        for (int j0 = lane; j0 < chunks; j0 += 64) {
+            uint4 a1[2], a2[2], au[2];
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const int j = j0 + 32 * s;
+                if (j < chunks) {
+                    a1[s] = *reinterpret_cast<const uint4 *>(p1r + 8 * j);
+                    a2[s] = *reinterpret_cast<const uint4 *>(p2r + 8 * j);
+                    au[s] = *reinterpret_cast<const uint4 *>(ur + 8 * j);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const int j = j0 + 32 * s;
+                if (j >= chunks) continue;
+                const uint32_t w1[4] = {a1[s].x, a1[s].y, a1[s].z, a1[s].w};
+                const uint32_t w2[4] = {a2[s].x, a2[s].y, a2[s].z, a2[s].w};
+                const uint32_t wu[4] = {au[s].x, au[s].y, au[s].z, au[s].w};
+                uint32_t o1[4], o2[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float d1[2], d2[2];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float p1 = __uint_as_float(hh ? (w1[b] & 0xffff0000u) : (w1[b] << 16));
+                        const float p2 = __uint_as_float(hh ? (w2[b] & 0xffff0000u) : (w2[b] << 16));
+                        const float uu = __uint_as_float(hh ? (wu[b] & 0xffff0000u) : (wu[b] << 16));
+                        float a;
+                        situ_glu_bwd(p1, p2, g * uu, b1, ib1, b2, ib2, d1[hh], d2[hh], a);
+                        acc = fmaf(uu, a, acc);
+                    }
+                    o1[b] = uint32_t(f_to_bf16(d1[0])) | (uint32_t(f_to_bf16(d1[1])) << 16);
+                    o2[b] = uint32_t(f_to_bf16(d2[0])) | (uint32_t(f_to_bf16(d2[1])) << 16);
+                }
+                *reinterpret_cast<uint4 *>(d1r + 8 * j) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                *reinterpret_cast<uint4 *>(d2r + 8 * j) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+            }
+        }
+        if (dg) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) dg[r] = acc;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256) fill_kernel(float *__restrict__ p, int64_t n, float v) {
     grid_dependency_wait();
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
@@ -430,6 +531,22 @@ cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int 
     if (T <= 0) return cudaSuccess;
     const int blocks = blocks_for(T * (L / 8), 256, num_sms * 8);
     return launch_kernel(dh_sum_kernel, dim3(blocks), dim3(256), 0, stream, true, dhp, dhr, T, k, L, dh);
+}
+
+cudaError_t launch_glu_bwd_rows(const uint16_t *P, int64_t p_ld, int p_half, const uint16_t *U, int64_t u_ld,
+                                int u_col0, const int32_t *scale_rows, const float *scale, int64_t rows, int C,
+                                float b1, float b2, uint16_t *dP, int64_t dp_ld, int dp_half, float *dg,
+                                int num_sms, cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    if (C <= 0 || (C & 7) || (p_ld & 7) || (p_half & 7) || (u_ld & 7) || (u_col0 & 7) || (dp_ld & 7) ||
+        (dp_half & 7) || p_half < C || dp_half < C || u_col0 + C > u_ld || p_half + C > p_ld ||
+        dp_half + C > dp_ld || num_sms <= 0)
+        return cudaErrorInvalidValue;
+    const int64_t want = (rows + kGluWarps - 1) / kGluWarps;
+    const int64_t cap = int64_t(num_sms) * 8;   // 8 blocks of 8 warps per SM, grid-stride beyond
+    return launch_kernel(glu_bwd_rows_kernel, dim3(static_cast<unsigned>(want < cap ? want : cap)),
+                         dim3(kGluWarps * 32), 0, stream, true, P, p_ld, p_half, U, u_ld, u_col0, scale_rows, scale,
+                         rows, C, b1, b2, dP, dp_ld, dp_half, dg);
 }
 
 cudaError_t launch_fill(float *p, int64_t n, float v, cudaStream_t stream) {

@@ -15,11 +15,10 @@
 // operands (kind::f8f6f4, a K block of 128 elements = the same 128-byte rows)
 // and their epilogues apply the power-of-two row scales: a5 writes e4m3(4 act),
 // a6 undoes the 4 with the W3 row scale and the gate.
-// The backward pass (gemm_bwd.cu) adds two epilogues: EPI_GLU_BWD (the
-// accumulator holds a recomputed SiTU-GLU GEMM's p1 | p2; with the gradient of
-// its activation it writes dp1 | dp2) and EPI_F32 (fp32 weight gradients), and
-// per-expert K segments (KSEG: each tile names its own K range, for the routed
-// experts' weight gradients, whose output goes out by TMA store).
+// For training (gemm_bwd.cu): EPI_SITU_GLU_SAVE (a5 / a8' that also keep the
+// pre-activations p1 | p2 for the backward), EPI_F32 (fp32 weight gradients)
+// and per-expert K segments (KSEG: each tile names its own K range, for the
+// routed experts' weight gradients, whose output goes out by TMA store).
 //
 // Structure (one CTA per SM, 192 threads; 320 with the A gather):
 //   warp 0      TMA producer: per 64-wide K block, one box of A and one or two
@@ -160,36 +159,6 @@ __device__ __forceinline__ float situ_glu(float p1, float p2, float b1, float ib
         situ = b1 * tanh_fast(p1 * ib1) * sig;
     }
     return situ * (b2 * tanh_fast(p2 * ib2));
-}
-
-// tanh(y) and its derivative 1 - tanh(y)^2 from one exponential: with
-// u = e^(-2|y|), tanh(y) = sign(y) (1 - u) / (1 + u) and
-// 1 - tanh(y)^2 = 4u / (1 + u)^2.  The derivative keeps its relative accuracy
-// where tanh saturates (1 - t*t from an approximate t would not).
-__device__ __forceinline__ void tanh_and_slope(float y, float &t, float &slope) {
-    const float u = __expf(-2.0f * fabsf(y));
-    const float inv = 1.0f / (1.0f + u);
-    t = copysignf((1.0f - u) * inv, y);
-    slope = 4.0f * u * inv * inv;
-}
-
-// Backward of one SiTU-GLU element ("Kimi-K3-Architecture-Deep-Dive" section 1:
-// the tanh softcap is differentiable everywhere).  With sigma = sigmoid(p1):
-//   SiTU   = b1 tanh(p1/b1) sigma        SiTU'   = (1 - tanh^2) sigma + SiTU (1 - sigma)
-//   softcap = b2 tanh(p2/b2)             softcap' = 1 - tanh^2(p2/b2)
-// da is the activation's gradient; returns act = SiTU softcap as well.
-__device__ __forceinline__ void situ_glu_bwd(float p1, float p2, float da, float b1, float ib1, float b2,
-                                             float ib2, float &dp1, float &dp2, float &act) {
-    float t1, s1, t2, s2;
-    tanh_and_slope(p1 * ib1, t1, s1);
-    tanh_and_slope(p2 * ib2, t2, s2);
-    const float sig = 1.0f / (1.0f + __expf(-p1));
-    const float situ = b1 * t1 * sig;
-    const float dsitu = s1 * sig + situ * (1.0f - sig);
-    const float cap = b2 * t2;
-    dp1 = da * dsitu * cap;
-    dp2 = da * situ * s2;
-    act = situ * cap;
 }
 
 // 2^k as an fp32 built from the exponent bits, k clamped to the normal range
@@ -468,8 +437,6 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         pre_scale[sub] = args.row_scale[pre_drow[sub]];
                     } else if (EPI == EPI_SITU_GLU_F8) {
                         pre_he[sub] = args.row_exp[args.gather_rows[ti.row0 + trow]];
-                    } else if (EPI == EPI_GLU_BWD) {
-                        if (args.row_scale) pre_scale[sub] = args.row_scale[args.scatter_rows[ti.row0 + trow]];
                     }
                 }
             }
@@ -624,51 +591,6 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                         }
                     }
                 }
-            } else if (EPI == EPI_GLU_BWD) {
-                // recomputed p1 | p2 and the activation's gradient: dp1 | dp2
-                // (bf16) and the partial sum of u * act over the tile's features
-                const int64_t orow = ti.row0 + trow;
-                const float g = (NSUB > 1 && sub) ? pre_scale[NSUB - 1] : pre_scale[0];
-                const float b1 = args.beta1, b2 = args.beta2;
-                const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
-                const int f0 = ti.nt * H;     // first feature of the tile
-                const uint16_t *urow = args.gin + orow * args.gin_ld + args.gin_col0 + f0;
-                uint16_t *o1 = reinterpret_cast<uint16_t *>(args.out) + orow * args.ld_out + f0;
-                uint16_t *o2 = o1 + args.out_cols;
-                float dg = 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < H; c += 32) {
-                    float p1[32], p2[32];
-                    tmem_ld32x2(taddr + c, taddr + H + c, p1, p2);   // warp-collective: all lanes
-                    if (rv && f0 + c < args.out_cols) {
-                        uint32_t w1[16], w2[16];
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const uint4 uu = *reinterpret_cast<const uint4 *>(urow + c + 8 * q4);
-                            const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-#pragma unroll
-                            for (int b = 0; b < 4; ++b) {
-                                const int j = q4 * 8 + 2 * b;
-                                const float u0 = __uint_as_float(uw[b] << 16);
-                                const float u1 = __uint_as_float(uw[b] & 0xffff0000u);
-                                float d10, d20, a0, d11, d21, a1;
-                                situ_glu_bwd(p1[j], p2[j], g * u0, b1, ib1, b2, ib2, d10, d20, a0);
-                                situ_glu_bwd(p1[j + 1], p2[j + 1], g * u1, b1, ib1, b2, ib2, d11, d21, a1);
-                                dg = fmaf(u0, a0, dg);
-                                dg = fmaf(u1, a1, dg);
-                                w1[q4 * 4 + b] = pack_bf16x2(d10, d11);
-                                w2[q4 * 4 + b] = pack_bf16x2(d20, d21);
-                            }
-                        }
-                        uint4 *d1 = reinterpret_cast<uint4 *>(o1 + c), *d2 = reinterpret_cast<uint4 *>(o2 + c);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            d1[q4] = make_uint4(w1[4 * q4], w1[4 * q4 + 1], w1[4 * q4 + 2], w1[4 * q4 + 3]);
-                            d2[q4] = make_uint4(w2[4 * q4], w2[4 * q4 + 1], w2[4 * q4 + 2], w2[4 * q4 + 3]);
-                        }
-                    }
-                }
-                if (rv && args.dgp) args.dgp[orow * args.n_tiles + ti.nt] = dg;
             } else if (EPI == EPI_SITU_GLU_F8) {
                 // e4m3 experts, W1|W2: p = acc * 2^(token exponent + weight-row
                 // exponent) (exact), SiTU-GLU, then the fixed activation scale:
@@ -714,7 +636,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 // 32 different rows.
                 const int64_t drow = (NSUB > 1 && sub) ? pre_drow[NSUB - 1] : pre_drow[0];
                 const float scale = (NSUB > 1 && sub) ? pre_scale[NSUB - 1] : pre_scale[0];
-                constexpr int NOUT = (EPI == EPI_SITU_GLU) ? H : BN;   // output columns per tile
+                constexpr bool GLU = (EPI == EPI_SITU_GLU || EPI == EPI_SITU_GLU_SAVE);
+                constexpr int NOUT = GLU ? H : BN;   // output columns per tile
                 const int64_t col0 = int64_t(ti.nt) * NOUT;
                 const float b1 = args.beta1, b2 = args.beta2;
                 const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
@@ -722,13 +645,26 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 for (int c = 0; c < NOUT; c += 64) {
                     uint32_t packed[32];
                     float va[32], vb[32];
-                    if (EPI != EPI_SITU_GLU) tmem_ld32x2(taddr + c, taddr + c + 32, va, vb);   // both halves
+                    if (!GLU) tmem_ld32x2(taddr + c, taddr + c + 32, va, vb);   // both halves
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         float v[32];
-                        if (EPI == EPI_SITU_GLU) {
+                        if (GLU) {
                             float p2[32];
                             tmem_ld32x2(taddr + c + h2 * 32, taddr + H + c + h2 * 32, v, p2);
+                            if (EPI == EPI_SITU_GLU_SAVE && rv) {
+                                // keep the pre-activations for the backward: p1 | p2 in bf16
+                                uint16_t *ps = args.pout + drow * args.pout_ld + col0 + c + h2 * 32;
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    reinterpret_cast<uint4 *>(ps)[q4] =
+                                        make_uint4(pack_bf16x2(v[8 * q4], v[8 * q4 + 1]), pack_bf16x2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                                                   pack_bf16x2(v[8 * q4 + 4], v[8 * q4 + 5]), pack_bf16x2(v[8 * q4 + 6], v[8 * q4 + 7]));
+                                    reinterpret_cast<uint4 *>(ps + args.pout_half)[q4] =
+                                        make_uint4(pack_bf16x2(p2[8 * q4], p2[8 * q4 + 1]), pack_bf16x2(p2[8 * q4 + 2], p2[8 * q4 + 3]),
+                                                   pack_bf16x2(p2[8 * q4 + 4], p2[8 * q4 + 5]), pack_bf16x2(p2[8 * q4 + 6], p2[8 * q4 + 7]));
+                                }
+                            }
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = situ_glu(v[j], p2[j], b1, ib1, b2, ib2);
                         } else {

@@ -56,15 +56,11 @@ enum BMode { B_PLAIN = 0, B_GLU = 1, B_SPLIT = 2 };
 // EPI_F32: plain fp32 output rows (weight gradients; the router's share of the
 // latent gradient).  With per-expert K segments (launch_gemm_bwd, kseg), the
 // rows of expert e's output block go to out (rows < m_split) or out2.
-// EPI_GLU_BWD: the accumulator holds a SiTU-GLU GEMM's p1 | p2 (recomputed);
-// with the gradient u of its activation (gin) and the row's gate g
-// (row_scale[scatter_rows[row]], 1 without row_scale) it writes
-// dp1 = g u SiTU'(p1) softcap(p2) and dp2 = g u SiTU(p1) softcap'(p2) as bf16
-// (dp1 in columns [0, out_cols), dp2 in [out_cols, 2 out_cols)), and, with dgp,
-// the partial dot products sum u * act of the tile's columns (fp32,
-// dgp[row * n_tiles + nt]).
+// EPI_SITU_GLU_SAVE: EPI_SITU_GLU that also writes the pre-activations p1 | p2
+// (bf16) to pout (p1 at the feature's column, p2 pout_half columns later), for
+// a backward pass that does not recompute them.
 enum Epi { EPI_BF16 = 0, EPI_SITU_GLU = 1, EPI_SIGMOID_F32 = 2, EPI_SCATTER_BF16 = 3, EPI_SITU_GLU_F8 = 4,
-           EPI_SCATTER_F8 = 5, EPI_F32 = 6, EPI_GLU_BWD = 7 };
+           EPI_SCATTER_F8 = 5, EPI_F32 = 6, EPI_SITU_GLU_SAVE = 7 };
 
 constexpr int kBM = 128;  // rows per tile (one tcgen05 M=128 tile)
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzled row of bf16 (128 e4m3)
@@ -100,17 +96,16 @@ struct GemmArgs {
     const int8_t *col_exp0;       // per weight row of expert e: [e * col_exp_rows + col] (W1 or W3)
     const int8_t *col_exp1;       // EPI_SITU_GLU_F8: the W2 rows
     int32_t col_exp_rows;
-    // backward epilogues
-    const uint16_t *gin;          // EPI_GLU_BWD: gradient of the activation, bf16 rows
-    int64_t gin_ld;               //   its row stride (elements)
-    int32_t gin_col0;             //   column of feature 0 in a gin row
-    float *dgp;                   //   partial sums of u * act (nullable)
+    // training epilogues
     void *out2;                   // EPI_F32 with K segments: rows >= m_split of an expert's block
     int32_t m_split;
     // K segments: operand heights of the K-block packed A and B ([K blocks][rows][64]);
     // the box of K block kb, rows r.. sits at map row kb * rows + r
     int32_t kseg_a_rows, kseg_b_rows;
     int32_t accumulate;           // EPI_F32: add to the output instead of overwriting it
+    uint16_t *pout;               // EPI_SITU_GLU_SAVE: pre-activation rows (bf16)
+    int64_t pout_ld;
+    int32_t pout_half;
     unsigned *err;           // device status word
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
 };
@@ -135,6 +130,11 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
 // 32 x 32 boxes and 128-byte swizzle (m_split and m_rows multiples of 32).
 cudaError_t launch_gemm_bwd(int bn, AMode am, BMode bm, Epi epi, bool grouped, bool kseg, const GemmMaps &maps,
                             const GemmArgs &args, int grid, cudaStream_t stream);
+// The forward's SiTU-GLU GEMMs that also keep their pre-activations
+// (EPI_SITU_GLU_SAVE): the routed experts' (A_GATHER, grouped, 128-row or
+// pair tiles) and the shared experts' (A_DENSE).
+cudaError_t launch_gemm_save(int bn, AMode am, bool grouped, bool pair, const GemmMaps &maps, const GemmArgs &args,
+                             int grid, cudaStream_t stream, bool dependent = true);
 
 // Repack per-expert weights [E][R][K] (row-major bf16) into tile-contiguous
 // order [E][R/TR][K/64][TR][64] so that one TMA box of TR rows x 64 columns is
@@ -207,5 +207,12 @@ cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, cons
 cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,
                           int num_sms, cudaStream_t stream);
 cudaError_t launch_fill(float *p, int64_t n, float v, cudaStream_t stream);
+// SiTU-GLU backward over rows at the pre-activations P (p1 | p2, p2 p_half
+// columns after p1): dP (dp1 | dp2) from the activation gradient
+// g_r * U[r][u_col0 ...], and dg[r] = sum of U * act when dg is not null.
+cudaError_t launch_glu_bwd_rows(const uint16_t *P, int64_t p_ld, int p_half, const uint16_t *U, int64_t u_ld,
+                                int u_col0, const int32_t *scale_rows, const float *scale, int64_t rows, int C,
+                                float b1, float b2, uint16_t *dP, int64_t dp_ld, int dp_half, float *dg,
+                                int num_sms, cudaStream_t stream);
 
 }  // namespace lmoe

@@ -108,7 +108,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, tiles2, nmt, perm, inv, tokrow,
-        tiles3, act, o, r, sact, hn, h8, h8e, total;
+        tiles3, act, o, r, sact, hn, h8, h8e, pre, spre, total;
 };
 
 Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
@@ -147,6 +147,10 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.hn = c.norm_after_down ? take(size_t(T * L * 2)) : none;
     l.h8 = c.expert_fp8 ? take(size_t(T * L)) : none;
     l.h8e = c.expert_fp8 ? take(size_t(T)) : none;
+    // with_backward: the SiTU-GLU pre-activations p1 | p2 (bf16), kept for
+    // the backward (routed rows in permuted order, shared rows by token)
+    l.pre = c.with_backward ? take(size_t(n * 2 * I * 2)) : none;
+    l.spre = c.with_backward ? take(size_t(T * 2 * S * 2)) : none;
     l.total = off;
     return l;
 }
@@ -334,7 +338,6 @@ BwdLayout bwd_layout(const lmoe_handle *h, int64_t T) {
     const int64_t d = c.d, L = c.latent, E = c.n_experts, K = c.top_k, I = c.inter;
     const int64_t S = int64_t(c.n_shared) * c.shared_inter;
     const int64_t n = T * K;
-    const int64_t nq = I / (h->bn_exp1 / 2);
     l.Tp = round64(T);
     l.Ep = round64(E);
     l.Qmax = round64(n) + 64 * E;
@@ -344,7 +347,7 @@ BwdLayout bwd_layout(const lmoe_handle *h, int64_t T) {
     l.dz = take(size_t(T * L) * 2);
     l.u = take(size_t(n * I) * 2);
     l.dp = take(size_t(n * 2 * I) * 2);
-    l.dgp = take(size_t(n * nq) * 4);
+    l.dgp = take(size_t(n) * 4);
     l.dl = take(size_t(T * l.Ep) * 2);
     l.dhp = take(size_t(n * L) * 2);
     l.dhr = take(size_t(T * L) * 4);
@@ -519,6 +522,8 @@ int lmoe_workspace_layout(const lmoe_handle *h, int64_t T, lmoe_ws_layout *out) 
     out->h_norm = (l.hn == SIZE_MAX) ? -1 : int64_t(l.hn);
     out->h_fp8 = (l.h8 == SIZE_MAX) ? -1 : int64_t(l.h8);
     out->h_fp8_exp = (l.h8e == SIZE_MAX) ? -1 : int64_t(l.h8e);
+    out->pre_act = (l.pre == SIZE_MAX) ? -1 : int64_t(l.pre);
+    out->shared_pre_act = (l.spre == SIZE_MAX) ? -1 : int64_t(l.spre);
     return LMOE_OK;
 }
 
@@ -571,6 +576,10 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     uint16_t *hlat = c.norm_after_down ? reinterpret_cast<uint16_t *>(ws + l.hn) : hbuf;
     uint8_t *h8 = c.expert_fp8 ? ws + l.h8 : nullptr;              // e4m3 codes of hlat
     int8_t *h8e = c.expert_fp8 ? reinterpret_cast<int8_t *>(ws + l.h8e) : nullptr;
+    // with_backward: the SiTU-GLU GEMMs also keep their pre-activations
+    const bool save = c.with_backward != 0;
+    uint16_t *pre = save ? reinterpret_cast<uint16_t *>(ws + l.pre) : nullptr;
+    uint16_t *spre = save ? reinterpret_cast<uint16_t *>(ws + l.spre) : nullptr;
 
     // Activation-side TMA descriptors for this T and workspace.
     CUtensorMap m_x, m_h, m_act, m_r, m_sact;
@@ -622,6 +631,13 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = sact;
         a.ld_out = S;
         a.out_cols = static_cast<int32_t>(S);
+        if (save) {
+            a.pout = spre;
+            a.pout_ld = 2 * S;
+            a.pout_half = static_cast<int32_t>(S);
+            return gemm_status(launch_gemm_save(h->bn_shared, A_DENSE, false, false, m, a,
+                                                grid_for(int64_t(m_tiles) * a.n_tiles), s_));
+        }
         return gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
                                        grid_for(int64_t(m_tiles) * a.n_tiles), s_));
     };
@@ -708,17 +724,22 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.col_exp1 = h->w2e;
         a.col_exp_rows = static_cast<int32_t>(I);
         const Epi epi = f8 ? EPI_SITU_GLU_F8 : EPI_SITU_GLU;
+        a.pout = pre;                    // with_backward: p1 | p2 per permuted row
+        a.pout_ld = 2 * I;
+        a.pout_half = static_cast<int32_t>(I);
+        auto w12 = [&](bool pair, int grid) {
+            return save ? launch_gemm_save(h->bn_exp1, A_GATHER, true, pair, m, a, grid, stream)
+                        : launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a, grid, stream, pair);
+        };
         a.tiles = tiles3;
         a.n_mtiles = nmt + 2;
-        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a,
-                                     grid_for(E * a.n_tiles), stream, /*pair=*/false));
+        st = gemm_status(w12(/*pair=*/false, grid_for(E * a.n_tiles)));
         if (st) return st;
         mark(LMOE_STAGE_EXPERT_W12_HEAVY);
         a.tiles = tiles2;
         a.n_mtiles = nmt + 1;
         const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
-        st = gemm_status(launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a,
-                                     grid_for(max_pairs), stream, /*pair=*/true));
+        st = gemm_status(w12(/*pair=*/true, grid_for(max_pairs)));
         if (st) return st;
     }
     mark(LMOE_STAGE_EXPERT_W3);
@@ -825,6 +846,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     const uint16_t *obuf = reinterpret_cast<const uint16_t *>(fw + fl.o);
     const uint16_t *rbuf = reinterpret_cast<const uint16_t *>(fw + fl.r);
     const uint16_t *sact = reinterpret_cast<const uint16_t *>(fw + fl.sact);
+    // the SiTU-GLU pre-activations the forward kept: p1 | p2 per row
+    const uint16_t *pre = reinterpret_cast<const uint16_t *>(fw + fl.pre);
+    const uint16_t *spre = reinterpret_cast<const uint16_t *>(fw + fl.spre);
     // the backward's own buffers
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     auto bf = [&](size_t off) { return reinterpret_cast<uint16_t *>(ws + off); };
@@ -931,23 +955,11 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         if (st) return st;
     }
     mark(LMOE_BWD_STAGE_SHARED);
-    {   // shared experts: dp_s = SiTU-GLU backward of the recomputed x Ws1^T | x Ws2^T
-        GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
-        GemmArgs a = base_args(h);
-        a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
-        a.n_tiles = static_cast<int32_t>(S / (h->bn_shared / 2));
-        a.k_blocks = static_cast<int32_t>(d / kBK);
-        a.gin = drs;
-        a.gin_ld = L + S;
-        a.gin_col0 = static_cast<int32_t>(L);
-        a.out = dps;
-        a.ld_out = 2 * S;
-        a.out_cols = static_cast<int32_t>(S);
-        st = gemm_status(launch_gemm_bwd(h->bn_shared, A_DENSE, B_GLU, EPI_GLU_BWD, false, false, m, a,
-                                         grid_for(int64_t(m_tiles) * a.n_tiles), stream));
-        if (st) return st;
-    }
+    // shared experts: dp_s = SiTU-GLU backward at the kept x Ws1^T | x Ws2^T with
+    // da_s from dr | da_s
+    if (!ok(launch_glu_bwd_rows(spre, 2 * S, Si, drs, L + S, Li, nullptr, nullptr, T, Si, c.beta1, c.beta2, dps,
+                                2 * S, Si, nullptr, h->num_sms, stream)))
+        return LMOE_ERR_CUDA;
     if (overlap && !(fork(1) && copies_dps())) return LMOE_ERR_CUDA;
     mark(LMOE_BWD_STAGE_RMSNORM);
     // RMSNorm backward: dz
@@ -973,41 +985,17 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                                          grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
     }
-    const int nq = static_cast<int>(I / (h->bn_exp1 / 2));
     mark(LMOE_BWD_STAGE_EXPERT_GLU);
-    {   // routed experts: dp = SiTU-GLU backward of the recomputed W1[e] h | W2[e] h with
-        // da = gate * u; partial sums of u * act for the gates' gradient
-        GemmMaps m{h->m_w1, h->m_w1, h->m_w1, h->m_w2};
-        GemmArgs a = base_args(h);
-        a.n_tiles = nq;
-        a.k_blocks = static_cast<int32_t>(L / kBK);
-        a.b_expert_rows = static_cast<int32_t>(I);
-        a.b_packed = 1;
-        a.b_row_tiles = nq;
-        a.gather_src = hlat;
-        a.gather_rows = tokrow;
-        a.gather_ld = L;
-        a.tiles = tiles;
-        a.n_mtiles = nmt;
-        a.gin = u;
-        a.gin_ld = I;
-        a.gin_col0 = 0;
-        a.scatter_rows = perm;
-        a.row_scale = gates;
-        a.dgp = dgp;
-        a.out = dp;
-        a.ld_out = 2 * I;
-        a.out_cols = static_cast<int32_t>(I);
-        a.tiles = tiles;
-        a.n_mtiles = nmt;
-        st = gemm_status(launch_gemm_bwd(h->bn_exp1, A_GATHER, B_GLU, EPI_GLU_BWD, true, false, m, a,
-                                         grid_for(grouped_tiles * a.n_tiles), stream));
-        if (st) return st;
-    }
+    // routed experts: dp = SiTU-GLU backward at the kept W1[e] h | W2[e] h with
+    // da = gate * u (permuted rows; the gate of the row's assignment), and
+    // dgate = u . act per row
+    if (!ok(launch_glu_bwd_rows(pre, 2 * I, Ii, u, I, 0, perm, gates, n, Ii, c.beta1, c.beta2, dp, 2 * I, Ii, dgp,
+                                h->num_sms, stream)))
+        return LMOE_ERR_CUDA;
 
     mark(LMOE_BWD_STAGE_ROUTER);
     // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
-    if (!ok(launch_router_bwd(dgp, nq, inv, idx, hlat, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
+    if (!ok(launch_router_bwd(dgp, 1, inv, idx, hlat, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
                               stream)))
         return LMOE_ERR_CUDA;
     if (overlap && !(fork(2) && copies_dl())) return LMOE_ERR_CUDA;

@@ -4,11 +4,12 @@ The oracle takes the GPU forward's routing (top-k is a discrete choice the
 gradient does not pass through) and recomputes everything else in fp64 from
 the same bf16 inputs; it is itself pinned by finite differences
 (test_oracle_backward.py).  Every gradient (dx and the nine weights) must lie
-within BWD_REL_FRO in relative Frobenius norm: the GPU path rounds six
-intermediates to bf16 (dr, dz, u, dp, the experts' share of dh, dh), each a
-relative perturbation of at most 2^-9 (RMS about 2^-9/sqrt(3) = 1.1e-3 per
-element), so the expected error is about sqrt(6) * 1.1e-3 = 2.7e-3; the bar
-leaves a factor of about 4.  The largest element error must stay within
+within BWD_REL_FRO in relative Frobenius norm: the GPU path rounds seven
+intermediates to bf16 (the SiTU-GLU pre-activations the training forward
+keeps, dr, dz, u, dp, the experts' share of dh, dh), each a relative
+perturbation of at most 2^-9 (RMS about 2^-9/sqrt(3) = 1.1e-3 per element),
+so the expected error is about sqrt(7) * 1.1e-3 = 2.9e-3; the bar leaves a
+factor of about 3.  The largest element error must stay within
 BWD_MAX_REL of the gradient's largest element.
 """
 import dataclasses
@@ -146,6 +147,69 @@ def test_backward_unused_experts_get_zero(lm):
         g = run["grads"][n].cpu()
         for e in unused:
             assert not torch.any(g[e] != 0), (n, e)
+
+
+@pytest.mark.parametrize("shape_name", ["tiny", "small"])
+def test_training_forward_output_is_the_inference_forward(lm, shape_name):
+    """A with_backward handle's forward (whose SiTU-GLU GEMMs also keep their
+    pre-activations) gives the inference forward's y and routing bit for bit."""
+    shape = synth.SHAPES[shape_name]
+    w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
+    x, bias = (t.cuda() for t in synth.activations_host(shape, T=777))
+    T = x.shape[0]
+    out = []
+    for wb in (False, True):
+        h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=wb), w, max_tokens=T)
+        ws = lm.alloc_workspace(h, T)
+        y = lm.lmoe_forward(h, x, bias, workspace=ws)
+        torch.cuda.synchronize()
+        assert lm.lmoe_device_status(h) == 0
+        lay = lm.lmoe_workspace_layout(h, T)
+        assert (lay["pre_act"] >= 0) == wb and (lay["shared_pre_act"] >= 0) == wb
+        out.append((y.clone(), ws_view(ws, lay, "topk_idx", torch.int32, (T, shape.top_k)).clone()))
+        lm.lmoe_destroy(h)
+    assert torch.equal(out[0][0], out[1][0])
+    assert torch.equal(out[0][1], out[1][1])
+
+
+@pytest.mark.parametrize("shape_name,T", [("tiny", 300), ("small", 1000)])
+def test_kept_pre_activations_match_their_definition(lm, shape_name, T):
+    """pre_act row p (permuted order) holds W1[e] h_t | W2[e] h_t for the
+    assignment perm[p] = t * top_k + j, e = idx[t][j], and shared_pre_act row t
+    holds Ws1 x_t | Ws2 x_t, each the bf16 rounding of the fp32-accumulated
+    product: within 2^-8 relative of the fp64 product of the same bf16
+    operands (plus fp32 accumulation error)."""
+    shape = synth.SHAPES[shape_name]
+    w_host = synth.layer_weights_host(shape)
+    w = {k: v.cuda() for k, v in w_host.items()}
+    x, bias = (t.cuda() for t in synth.activations_host(shape, T=T, seed_offset=3))
+    L, I, K = shape.latent, shape.inter, shape.top_k
+    S = shape.n_shared * shape.shared_inter
+    h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    lm.lmoe_forward(h, x, bias, workspace=ws)
+    torch.cuda.synchronize()
+    lay = lm.lmoe_workspace_layout(h, T)
+    hl = dec(host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L))))
+    idx = ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).cpu().numpy()
+    perm = ws_view(ws, lay, "perm", torch.int32, (T * K,)).cpu().numpy()
+    pre = dec(host_bits(ws_view(ws, lay, "pre_act", torch.bfloat16, (T * K, 2 * I))))
+    spre = dec(host_bits(ws_view(ws, lay, "shared_pre_act", torch.bfloat16, (T, 2 * S))))
+    tok = perm // K
+    ex = idx.reshape(-1)[perm]
+    w12 = np.concatenate([dec(synth.bits(w_host["w1"])), dec(synth.bits(w_host["w2"]))], axis=1)   # [E][2I][L]
+    ref, absum = np.zeros_like(pre), np.zeros_like(pre)
+    for e in np.unique(ex):
+        rows = np.nonzero(ex == e)[0]
+        ref[rows] = hl[tok[rows]] @ w12[e].T
+        absum[rows] = np.abs(hl[tok[rows]]) @ np.abs(w12[e]).T
+    assert np.all(np.abs(pre - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * absum)
+    xs = dec(synth.bits(x.cpu()))
+    ws12 = np.concatenate([dec(synth.bits(w_host["ws1"])), dec(synth.bits(w_host["ws2"]))], axis=0)   # [2S][d]
+    sref = xs @ ws12.T
+    sabs = np.abs(xs) @ np.abs(ws12).T
+    assert np.all(np.abs(spre - sref) <= 2.0 ** -8 * np.abs(sref) + 1e-5 * sabs)
+    lm.lmoe_destroy(h)
 
 
 def test_backward_needs_a_backward_handle(lm):

@@ -122,7 +122,8 @@ def backward_work(shape, T, counts):
     w["expert_u"] = (2.0 * n * L * I, 2.0 * (touched * I * L + T * L + n * I))
     # p1 | p2 and u in, dp1 | dp2 out; the row's gate (through perm) in, dgate out
     w["expert_glu"] = (0.0, 2.0 * (2 * n * I + n * I + 2 * n * I) + 12.0 * n)
-    w["router"] = (2.0 * n * L, 2.0 * (T * L + E * L + T * Ep) + 4.0 * n + 8.0 * n)
+    # dgate, inv, idx and the kept logit per assignment in, the dense dl row out
+    w["router"] = (0.0, 2.0 * T * Ep + 16.0 * n)
     w["dh_experts"] = (4.0 * n * I * L, 2.0 * (touched * 2 * I * L + 2 * n * I + n * L))
     w["dh_router"] = (2.0 * T * Ep * L, 2.0 * (T * Ep + L * Ep) + 4.0 * T * L)
     w["dh_sum"] = (0.0, 2.0 * n * L + 4.0 * T * L + 2.0 * T * L)

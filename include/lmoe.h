@@ -90,8 +90,9 @@ typedef struct {
                            * every weight (about as much device memory again as
                            * the weights) so that lmoe_backward can run, and
                            * lmoe_forward also keeps the SiTU-GLU pre-activations
-                           * in its workspace (pre_act, shared_pre_act: p1 | p2
-                           * in bf16, 4 bytes per activation element) for it; 0: the
+                           * (pre_act, shared_pre_act: p1 | p2 in bf16, 4 bytes per
+                           * activation element) and the router's fp32 logits in
+                           * its workspace for it; 0: the
                            * handle serves forwards only.  The backward covers
                            * K3's layer and the norm_after_down variant;
                            * with_backward together with expert_fp8 returns
@@ -157,6 +158,7 @@ typedef struct {
     int64_t pre_act;  /* [T*top_k][2*inter] bf16 SiTU-GLU pre-activations W1[e] h | W2[e] h of
                        * each permuted row (with_backward, read by lmoe_backward), else -1 */
     int64_t shared_pre_act; /* [T][2*S] bf16 the shared experts' Ws1 x | Ws2 x (with_backward), else -1 */
+    int64_t logits;   /* [T][n_experts] fp32 router logits W_router h (with_backward), else -1 */
 } lmoe_ws_layout;
 
 int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *layout);
@@ -293,16 +295,15 @@ int lmoe_backward_workspace_size(const lmoe_handle *handle, int64_t T, size_t *b
  * gate dz act^T, dW1[e] = sum dp1 h^T).
  * The forward's intermediates are read from fwd_workspace (the workspace of
  * that forward, unchanged since; its layout for T): h, perm, inv, the
- * permuted activations and pre-activations, the rows o, r, the shared
- * activations and pre-activations and the tile
+ * permuted activations and pre-activations, the router's logits, the rows
+ * o, r, the shared activations and pre-activations and the tile
  * lists, and the offsets of the expert groups (always in the workspace; the
  * per-expert counts are their differences).  topk_idx, gates: the forward's
  * outputs when the caller had it write them to its own buffers (they are then
  * not in the workspace), or NULL for the workspace's copies; an expert id
- * outside [0, n_experts) contributes no gradient.  The router's logits of the
- * chosen experts are recomputed from h, so that
- * sigma'(logit) = sigma(logit) sigma(-logit) stays accurate where the fp32
- * score has rounded to 1.  workspace: lmoe_backward_workspace_size(T) bytes,
+ * outside [0, n_experts) contributes no gradient.  sigma'(logit) is taken
+ * as sigma(logit) sigma(-logit) at the forward's kept fp32 logit, which stays
+ * accurate where the fp32 gate has rounded to 1.  workspace: lmoe_backward_workspace_size(T) bytes,
  * 256-byte aligned.  The handle must have been created with with_backward =
  * 1 (else LMOE_ERR_INVALID_ARG).  Errors are reported before anything is
  * enqueued, as in lmoe_forward.  Unless lmoe_set_backward_events is set, the

@@ -62,7 +62,8 @@ class LmoeGrads(ctypes.Structure):
 class LmoeWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("h", "scores", "topk_idx", "gates", "counts", "offsets",
                                               "perm", "inv", "act", "o", "r", "shared_act", "h_norm",
-                                              "h_fp8", "h_fp8_exp", "pre_act", "shared_pre_act")]
+                                              "h_fp8", "h_fp8_exp", "pre_act", "shared_pre_act",
+                                              "logits")]
 
 
 def library_path() -> str:

@@ -270,56 +270,35 @@ __global__ void __launch_bounds__(kRmsThreads) rms_bwd_kernel(const uint16_t *__
     }
 }
 
-// Router backward, one warp per token.  For each chosen expert j the warp
-// recomputes the logit x_j = w_router[e_j] . h_t (fp32) and lane j forms
-// dg_j = sum of the partial products dgp[p][0..nq) (p = the assignment's
-// permuted row) and the logit gradient dg_j * sigma'(x_j), with
-// sigma'(x) = sigma(x) sigma(-x) evaluated from x: it stays accurate where
-// the fp32 score itself has rounded to 1 (s (1 - s) would give 0 there).
-// Written into a dense bf16 row dl[t][0..ldl) that is zero elsewhere.
-__global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict__ dgp, int nq,
+// Router backward, one warp per token.  Lane j < k takes the token's j-th
+// chosen expert e_j: the gate's gradient dg[p] (p = the assignment's permuted
+// row) times sigma'(x) = sigma(x) sigma(-x) at the expert's fp32 logit x as
+// the forward's router GEMM computed it (kept in logits [T][E]); this form
+// stays accurate where the fp32 gate sigma(x) has rounded to 1 (g (1 - g)
+// would give 0 there).  Written into a dense bf16 row dl[t][0..ldl) that is
+// zero elsewhere.
+__global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict__ dg,
                                                          const int32_t *__restrict__ inv,
                                                          const int32_t *__restrict__ idx,
-                                                         const uint16_t *__restrict__ h,
-                                                         const uint16_t *__restrict__ wr, int L, int E, int64_t T,
+                                                         const float *__restrict__ logits, int E, int64_t T,
                                                          int k, int ldl, uint16_t *__restrict__ dl) {
     grid_dependency_wait();
     const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= T) return;   // whole warps
-    const uint16_t *hrow = h + t * L;
-    float my_logit = 0.0f;
-    for (int j = 0; j < k; ++j) {
-        const int ej = idx[t * k + j];
-        if (ej < 0 || ej >= E) continue;   // not a routing the forward produced: no gradient
-        const uint16_t *wrow = wr + int64_t(ej) * L;
-        float part = 0.0f;
-        for (int c = lane * 8; c < L; c += 256) {
-            const uint4 hv = *reinterpret_cast<const uint4 *>(hrow + c);
-            const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + c);
-            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                part = fmaf(__uint_as_float(hw[i] << 16), __uint_as_float(ww[i] << 16), part);
-                part = fmaf(__uint_as_float(hw[i] & 0xffff0000u), __uint_as_float(ww[i] & 0xffff0000u), part);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == j) my_logit = part;
-    }
     int e = -1;
     float v = 0.0f;
     if (lane < k) {
         const int64_t a = t * k + lane;
-        const int64_t p = inv[a];
-        float dg = 0.0f;
-        for (int q = 0; q < nq; ++q) dg += dgp[p * nq + q];
         e = idx[a];
-        if (e < 0 || e >= E) dg = 0.0f;
-        const float sp = 1.0f / (1.0f + __expf(-my_logit));
-        const float sm = 1.0f / (1.0f + __expf(my_logit));
-        v = dg * (sp * sm);
+        if (e >= 0 && e < E) {   // else not a routing the forward produced: no gradient
+            const float x = logits[t * E + e];
+            const float sp = 1.0f / (1.0f + __expf(-x));
+            const float sm = 1.0f / (1.0f + __expf(x));
+            v = dg[inv[a]] * (sp * sm);
+        } else {
+            e = -1;
+        }
     }
     for (int c0 = 0; c0 < ldl; c0 += 64) {
         const int c = c0 + 2 * lane;
@@ -517,13 +496,13 @@ cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps
                          L, eps, dr, ld_dr, dz);
 }
 
-cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, const int32_t *idx, const uint16_t *h,
-                              const uint16_t *w_router, int L, int E, int64_t T, int k, int ldl, uint16_t *dl,
-                              cudaStream_t stream) {
+cudaError_t launch_router_bwd(const float *dg, const int32_t *inv, const int32_t *idx, const float *logits, int E,
+                              int64_t T, int k, int ldl, uint16_t *dl, cudaStream_t stream) {
     if (T <= 0) return cudaSuccess;
+    if (k > 32) return cudaErrorInvalidValue;
     const unsigned blocks = static_cast<unsigned>((T * 32 + 255) / 256);
-    return launch_kernel(router_bwd_kernel, dim3(blocks), dim3(256), 0, stream, true, dgp, nq, inv, idx, h, w_router,
-                         L, E, T, k, ldl, dl);
+    return launch_kernel(router_bwd_kernel, dim3(blocks), dim3(256), 0, stream, true, dg, inv, idx, logits, E, T, k,
+                         ldl, dl);
 }
 
 cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,

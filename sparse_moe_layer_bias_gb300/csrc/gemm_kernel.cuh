@@ -480,6 +480,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                     float v[32];
                     tmem_ld32(taddr + c, v);
                     const int64_t col = int64_t(ti.nt) * BN + c;
+                    if (args.lout && rv)   // the logits themselves, for a backward pass
+                        store_f32_32(args.lout + orow * args.ld_out + col, v, static_cast<int>(args.out_cols - col));
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = sigmoid_f(v[j]);
                     if (col + 32 <= args.out_cols && vec_ok) {

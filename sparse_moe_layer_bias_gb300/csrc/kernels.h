@@ -103,6 +103,7 @@ struct GemmArgs {
     // the box of K block kb, rows r.. sits at map row kb * rows + r
     int32_t kseg_a_rows, kseg_b_rows;
     int32_t accumulate;           // EPI_F32: add to the output instead of overwriting it
+    float *lout;                  // EPI_SIGMOID_F32: also the raw fp32 logits, ld_out apart (nullable)
     uint16_t *pout;               // EPI_SITU_GLU_SAVE: pre-activation rows (bf16)
     int64_t pout_ld;
     int32_t pout_half;
@@ -201,9 +202,8 @@ cudaError_t launch_zero_unused(const int32_t *offsets, int E, int64_t per_expert
                                cudaStream_t stream);
 cudaError_t launch_rms_bwd(const uint16_t *o, int64_t T, int k, int L, float eps, const uint16_t *dr, int64_t ld_dr,
                            uint16_t *dz, cudaStream_t stream);
-cudaError_t launch_router_bwd(const float *dgp, int nq, const int32_t *inv, const int32_t *idx, const uint16_t *h,
-                              const uint16_t *w_router, int L, int E, int64_t T, int k, int ldl, uint16_t *dl,
-                              cudaStream_t stream);
+cudaError_t launch_router_bwd(const float *dg, const int32_t *inv, const int32_t *idx, const float *logits, int E,
+                              int64_t T, int k, int ldl, uint16_t *dl, cudaStream_t stream);
 cudaError_t launch_dh_sum(const uint16_t *dhp, const float *dhr, int64_t T, int k, int L, uint16_t *dh,
                           int num_sms, cudaStream_t stream);
 cudaError_t launch_fill(float *p, int64_t n, float v, cudaStream_t stream);

@@ -108,7 +108,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, tiles2, nmt, perm, inv, tokrow,
-        tiles3, act, o, r, sact, hn, h8, h8e, pre, spre, total;
+        tiles3, act, o, r, sact, hn, h8, h8e, pre, spre, logit, total;
 };
 
 Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
@@ -151,6 +151,7 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     // the backward (routed rows in permuted order, shared rows by token)
     l.pre = c.with_backward ? take(size_t(n * 2 * I * 2)) : none;
     l.spre = c.with_backward ? take(size_t(T * 2 * S * 2)) : none;
+    l.logit = c.with_backward ? take(size_t(T * E * 4)) : none;   // the router's fp32 logits
     l.total = off;
     return l;
 }
@@ -321,7 +322,7 @@ bool build_transposed(lmoe_handle *h) {
 // column segments.  Tp = T and Qmax = T*top_k + 64 E rounded up to 64;
 // Ep = E rounded up to 64.
 struct BwdLayout {
-    size_t ones, drs, dps, dz, u, dp, dgp, dl, dhp, dhr, dh, dhraw, dyT, xT, rT, sT, dpsT, dhT, hT, dlT, segoff, qperm,
+    size_t ones, drs, dps, dz, u, dp, dgate, dl, dhp, dhr, dh, dhraw, dyT, xT, rT, sT, dpsT, dhT, hT, dlT, segoff, qperm,
         qtok, qgate, kt_a, kt_b, nkt, doT, aT, hgT, dpT, total;
     int64_t Tp, Ep, Qmax;
 };
@@ -347,7 +348,7 @@ BwdLayout bwd_layout(const lmoe_handle *h, int64_t T) {
     l.dz = take(size_t(T * L) * 2);
     l.u = take(size_t(n * I) * 2);
     l.dp = take(size_t(n * 2 * I) * 2);
-    l.dgp = take(size_t(n) * 4);
+    l.dgate = take(size_t(n) * 4);   // the gates' gradients, per permuted row
     l.dl = take(size_t(T * l.Ep) * 2);
     l.dhp = take(size_t(n * L) * 2);
     l.dhr = take(size_t(T * L) * 4);
@@ -524,6 +525,7 @@ int lmoe_workspace_layout(const lmoe_handle *h, int64_t T, lmoe_ws_layout *out) 
     out->h_fp8_exp = (l.h8e == SIZE_MAX) ? -1 : int64_t(l.h8e);
     out->pre_act = (l.pre == SIZE_MAX) ? -1 : int64_t(l.pre);
     out->shared_pre_act = (l.spre == SIZE_MAX) ? -1 : int64_t(l.spre);
+    out->logits = (l.logit == SIZE_MAX) ? -1 : int64_t(l.logit);
     return LMOE_OK;
 }
 
@@ -580,6 +582,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     const bool save = c.with_backward != 0;
     uint16_t *pre = save ? reinterpret_cast<uint16_t *>(ws + l.pre) : nullptr;
     uint16_t *spre = save ? reinterpret_cast<uint16_t *>(ws + l.spre) : nullptr;
+    float *logit = save ? reinterpret_cast<float *>(ws + l.logit) : nullptr;
 
     // Activation-side TMA descriptors for this T and workspace.
     CUtensorMap m_x, m_h, m_act, m_r, m_sact;
@@ -650,6 +653,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.n_tiles = static_cast<int32_t>(ceil_div(E, h->bn_router));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.out = scores;
+        a.lout = logit;                  // with_backward: the logits as well
         a.ld_out = E;
         a.out_cols = static_cast<int32_t>(E);
         return gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
@@ -849,12 +853,13 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     // the SiTU-GLU pre-activations the forward kept: p1 | p2 per row
     const uint16_t *pre = reinterpret_cast<const uint16_t *>(fw + fl.pre);
     const uint16_t *spre = reinterpret_cast<const uint16_t *>(fw + fl.spre);
+    const float *logit = reinterpret_cast<const float *>(fw + fl.logit);   // the router's, [T][E]
     // the backward's own buffers
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     auto bf = [&](size_t off) { return reinterpret_cast<uint16_t *>(ws + off); };
     float *ones = reinterpret_cast<float *>(ws + bl.ones);
     uint16_t *drs = bf(bl.drs), *dps = bf(bl.dps), *dz = bf(bl.dz), *u = bf(bl.u), *dp = bf(bl.dp);
-    float *dgp = reinterpret_cast<float *>(ws + bl.dgp);
+    float *dgate = reinterpret_cast<float *>(ws + bl.dgate);
     uint16_t *dl = bf(bl.dl), *dhp = bf(bl.dhp), *dh = bf(bl.dh), *dhraw = bf(bl.dhraw);
     // the gradient at the down-projection's output: dh, or in the variant dh
     // taken back through the norm after the down-projection
@@ -989,14 +994,14 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     // routed experts: dp = SiTU-GLU backward at the kept W1[e] h | W2[e] h with
     // da = gate * u (permuted rows; the gate of the row's assignment), and
     // dgate = u . act per row
-    if (!ok(launch_glu_bwd_rows(pre, 2 * I, Ii, u, I, 0, perm, gates, n, Ii, c.beta1, c.beta2, dp, 2 * I, Ii, dgp,
+    if (!ok(launch_glu_bwd_rows(pre, 2 * I, Ii, u, I, 0, perm, gates, n, Ii, c.beta1, c.beta2, dp, 2 * I, Ii, dgate,
                                 h->num_sms, stream)))
         return LMOE_ERR_CUDA;
 
     mark(LMOE_BWD_STAGE_ROUTER);
-    // router: dl = dgate * sigma'(logit) at the chosen experts, dense [T][Ep]
-    if (!ok(launch_router_bwd(dgp, 1, inv, idx, hlat, h->w.w_router, Li, Ei, T, Ki, static_cast<int>(Ep), dl,
-                              stream)))
+    // router: dl = dgate * sigma'(logit) at the chosen experts (the forward's
+    // logits), dense [T][Ep]
+    if (!ok(launch_router_bwd(dgate, inv, idx, logit, Ei, T, Ki, static_cast<int>(Ep), dl, stream)))
         return LMOE_ERR_CUDA;
     if (overlap && !(fork(2) && copies_dl())) return LMOE_ERR_CUDA;
     mark(LMOE_BWD_STAGE_DH_EXPERTS);

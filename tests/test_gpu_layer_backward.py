@@ -21,7 +21,7 @@ import torch
 import oracle
 from sparse_moe_layer_bias_gb300 import synth
 
-from layer_check import dec, host_bits, oracle_cfg, rel_fro, ws_view
+from layer_check import ACC_REL, S_EVAL, dec, host_bits, oracle_cfg, rel_fro, ws_view
 
 pytestmark = pytest.mark.gpu
 
@@ -178,7 +178,8 @@ def test_kept_pre_activations_match_their_definition(lm, shape_name, T):
     assignment perm[p] = t * top_k + j, e = idx[t][j], and shared_pre_act row t
     holds Ws1 x_t | Ws2 x_t, each the bf16 rounding of the fp32-accumulated
     product: within 2^-8 relative of the fp64 product of the same bf16
-    operands (plus fp32 accumulation error)."""
+    operands (plus fp32 accumulation error).  logits holds W_router h_t in
+    fp32 (within the accumulation error), and the scores are its sigmoid."""
     shape = synth.SHAPES[shape_name]
     w_host = synth.layer_weights_host(shape)
     w = {k: v.cuda() for k, v in w_host.items()}
@@ -209,6 +210,12 @@ def test_kept_pre_activations_match_their_definition(lm, shape_name, T):
     sref = xs @ ws12.T
     sabs = np.abs(xs) @ np.abs(ws12).T
     assert np.all(np.abs(spre - sref) <= 2.0 ** -8 * np.abs(sref) + 1e-5 * sabs)
+    E = shape.n_experts
+    logits = ws_view(ws, lay, "logits", torch.float32, (T, E)).cpu().double().numpy()
+    wr = dec(synth.bits(w_host["w_router"]))
+    assert np.all(np.abs(logits - hl @ wr.T) <= ACC_REL * (np.abs(hl) @ np.abs(wr).T) + 1e-30)
+    scores = ws_view(ws, lay, "scores", torch.float32, (T, E)).cpu().double().numpy()
+    assert np.all(np.abs(scores - 1.0 / (1.0 + np.exp(-np.clip(logits, -700.0, 700.0)))) <= S_EVAL)
     lm.lmoe_destroy(h)
 
 

@@ -442,7 +442,7 @@ def backward_pass(lm, stream, steps, warmup, shape, w, x, bias, peaks, peak_src,
            "frac_bf16_peak": round(model_flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
            "executed_tflop": round(executed / 1e12, 3), "weight_grad_dtype": "f32",
            "roofline": roof, "stages": stages,
-           "gpu_launches_per_pass": 36}
+           "gpu_launches_per_pass": 33}
     del hb, ws, bws, grads, dy, dx
     torch.cuda.empty_cache()
     return out
@@ -599,7 +599,7 @@ def main():
         qb_allreduce_histogram(hist)          # data-parallel QB: sum over ranks (no-op at N=1)
         lm.qb_quantile_bias(hist, level, quantile_out=q_out, bias_out=b_new, stream=stream)
 
-    kernels_per_step = len(lm.STAGES) + 2      # 11 forward kernels + QB histogram + quantile
+    kernels_per_step = len(lm.STAGES) + 2      # 12 forward kernels + QB histogram + quantile
 
     for _ in range(args.warmup):
         step(x, bias, y)

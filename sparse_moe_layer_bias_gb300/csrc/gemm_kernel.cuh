@@ -69,7 +69,8 @@ struct Cfg {
     // epilogues; up to 256 fp32)
     static constexpr int kColWarpBytes = 1024;
     // K segments (fp32 weight gradients): per epilogue warp two 4 KB buffers
-    // of a 32 x 32 fp32 block in the 128B-swizzled layout of a TMA store,
+    // of a 32 x 32 fp32 block in the 128B-swizzled layout of a TMA store (one
+    // for the TMA stores, one for the threads' stores),
     // 1024-byte aligned, in place of the staging and scale-factor areas the
     // other epilogues use (which leaves room for the full stage ring)
     static constexpr size_t kTmaStgOffset = (size_t(kStages) * kStageBytes + kBarBytes + 1023) / 1024 * 1024;
@@ -416,7 +417,6 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                                                   (warp - 2) * C::kColWarpBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t n_tma_stores = 0;   // K segments: TMA stores issued by this warp
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED, KSEG>(args, t, n_m);
             // Per-row metadata of this thread's rows (destination row, gate,
@@ -505,9 +505,11 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 }
             } else if (EPI == EPI_F32 && KSEG) {
                 // K segments (the experts' fp32 weight gradients): each warp
-                // writes (accumulate: adds) its 32 rows in 32 x 32 blocks by
-                // TMA store (reduction), through
-                // two swizzled 4 KB buffers, so the stores run asynchronously.
+                // writes (accumulate: adds) its 32 rows in 32 x 32 blocks, half
+                // of them by TMA store (reduction) from a swizzled 4 KB buffer,
+                // the other half by the threads' own coalesced stores (atomic
+                // adds) through a second buffer: the two paths together carry
+                // more than the TMA store path alone.
                 // Rows of the expert's block below m_split go to the map in
                 // tmA1 (out), the others to tmB1 (out2); m_split and the block
                 // heights are multiples of 32, so a warp's rows are all valid
@@ -519,29 +521,52 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 const CUtensorMap *om = first ? &tmA1 : &tmB1;
                 const int32_t y = first ? ti.expert * args.m_split + rblk
                                         : ti.expert * (args.m_rows - args.m_split) + (rblk - args.m_split);
+                float *orow0 = reinterpret_cast<float *>(first ? args.out : args.out2) + int64_t(y) * args.ld_out;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     float v[32];
                     tmem_ld32(taddr + c, v);       // warp-collective: all lanes
                     const int col = ti.nt * BN + c;
                     if (rows_ok && col < args.out_cols) {   // warp-uniform
-                        uint8_t *buf = tbuf + (n_tma_stores & 1) * 4096;
-                        if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
-                        __syncwarp();
+                        // even 32-column groups leave by TMA store (buffer 0), odd
+                        // ones by coalesced 16-byte stores from the threads
+                        // (buffer 1), so both store paths of the SM carry output
+                        const bool by_tma = ((c >> 5) & 1) == 0;
+                        uint8_t *buf = tbuf + (by_tma ? 0 : 4096);
+                        if (by_tma) {
+                            if (lane == 0) bulk_wait_read<0>();   // the previous TMA store has read it
+                            __syncwarp();
+                        }
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             *reinterpret_cast<float4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
                                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if (args.accumulate)
-                                tma_reduce_add_2d(om, smem_u32(buf), col, y);
-                            else
-                                tma_store_2d(om, smem_u32(buf), col, y);
-                            bulk_commit();
+                        if (by_tma) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if (args.accumulate)
+                                    tma_reduce_add_2d(om, smem_u32(buf), col, y);
+                                else
+                                    tma_store_2d(om, smem_u32(buf), col, y);
+                                bulk_commit();
+                            }
+                        } else {
+                            __syncwarp();
+                            const int ch = lane & 7;
+#pragma unroll
+                            for (int it = 0; it < 8; ++it) {
+                                const int r = it * 4 + (lane >> 3);   // 8 lanes per 128-byte row
+                                const float4 val =
+                                    *reinterpret_cast<const float4 *>(buf + r * 128 + ((ch ^ (r & 7)) << 4));
+                                float4 *to = reinterpret_cast<float4 *>(orow0 + int64_t(r) * args.ld_out + col + ch * 4);
+                                if (args.accumulate)
+                                    atomicAdd(to, val);   // the only writer of these 4 floats
+                                else
+                                    *to = val;
+                            }
+                            __syncwarp();   // buffer 1 is read before the next odd group rewrites it
                         }
-                        ++n_tma_stores;
                     }
                 }
             } else if (EPI == EPI_F32) {

@@ -417,6 +417,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                                                   (warp - 2) * C::kColWarpBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t n_tma_stores = 0;   // K segments without split stores: TMA stores issued by this warp
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = tile_at<GROUPED, KSEG>(args, t, n_m);
             // Per-row metadata of this thread's rows (destination row, gate,
@@ -505,11 +506,12 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 }
             } else if (EPI == EPI_F32 && KSEG) {
                 // K segments (the experts' fp32 weight gradients): each warp
-                // writes (accumulate: adds) its 32 rows in 32 x 32 blocks, half
-                // of them by TMA store (reduction) from a swizzled 4 KB buffer,
+                // writes (accumulate: adds) its 32 rows in 32 x 32 blocks by
+                // TMA store (reduction) through two swizzled 4 KB buffers, or,
+                // with split_stores, half of them that way from one buffer and
                 // the other half by the threads' own coalesced stores (atomic
-                // adds) through a second buffer: the two paths together carry
-                // more than the TMA store path alone.
+                // adds) through the second: the two paths together carry more
+                // than the TMA store path alone.
                 // Rows of the expert's block below m_split go to the map in
                 // tmA1 (out), the others to tmB1 (out2); m_split and the block
                 // heights are multiples of 32, so a warp's rows are all valid
@@ -528,13 +530,21 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                     tmem_ld32(taddr + c, v);       // warp-collective: all lanes
                     const int col = ti.nt * BN + c;
                     if (rows_ok && col < args.out_cols) {   // warp-uniform
-                        // even 32-column groups leave by TMA store (buffer 0), odd
-                        // ones by coalesced 16-byte stores from the threads
-                        // (buffer 1), so both store paths of the SM carry output
-                        const bool by_tma = ((c >> 5) & 1) == 0;
-                        uint8_t *buf = tbuf + (by_tma ? 0 : 4096);
+                        // split_stores: even 32-column groups leave by TMA store
+                        // (buffer 0), odd ones by coalesced 16-byte stores from the
+                        // threads (buffer 1), so both store paths of the SM carry
+                        // output; else every group by TMA store, alternating buffers
+                        const bool split = args.split_stores != 0;
+                        const bool by_tma = !split || ((c >> 5) & 1) == 0;
+                        uint8_t *buf = tbuf + (split ? (by_tma ? 0 : 4096) : (n_tma_stores & 1) * 4096);
                         if (by_tma) {
-                            if (lane == 0) bulk_wait_read<0>();   // the previous TMA store has read it
+                            // the buffer's previous TMA store has read it
+                            if (lane == 0) {
+                                if (split)
+                                    bulk_wait_read<0>();
+                                else
+                                    bulk_wait_read<1>();
+                            }
                             __syncwarp();
                         }
 #pragma unroll
@@ -551,6 +561,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                                     tma_store_2d(om, smem_u32(buf), col, y);
                                 bulk_commit();
                             }
+                            ++n_tma_stores;
                         } else {
                             __syncwarp();
                             const int ch = lane & 7;

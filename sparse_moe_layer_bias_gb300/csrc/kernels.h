@@ -103,6 +103,7 @@ struct GemmArgs {
     // the box of K block kb, rows r.. sits at map row kb * rows + r
     int32_t kseg_a_rows, kseg_b_rows;
     int32_t accumulate;           // EPI_F32: add to the output instead of overwriting it
+    int32_t split_stores;         // EPI_F32 with K segments: half the output by the threads' stores
     float *lout;                  // EPI_SIGMOID_F32: also the raw fp32 logits, ld_out apart (nullable)
     uint16_t *pout;               // EPI_SITU_GLU_SAVE: pre-activation rows (bf16)
     int64_t pout_ld;

@@ -1142,6 +1142,10 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.n_mtiles = nkt + 1;
         a.out = g->w1;
         a.out2 = g->w2;
+        // dW1 | dW2 tiles hold few K blocks and are nearly all output: both
+        // store paths (measured faster; dW3 measured the same either way and
+        // keeps TMA stores alone)
+        a.split_stores = 1;
         a.ld_out = L;
         a.out_cols = static_cast<int32_t>(L);
         st = gemm_status(launch_gemm_bwd(h->bn_down, A_DENSE, B_PLAIN, EPI_F32, true, true, m, a,

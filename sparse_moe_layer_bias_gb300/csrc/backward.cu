@@ -343,14 +343,6 @@ __global__ void __launch_bounds__(256) dh_sum_kernel(const uint16_t *__restrict_
     }
 }
 
-// SiTU-GLU backward of one row per warp, at the saved pre-activations:
-//   p1 = P[r][f], p2 = P[r][p_half + f], da = g_r * U[r][u_col0 + f]
-//   dP[r][f] = da SiTU'(p1) softcap(p2), dP[r][dp_half + f] = da SiTU(p1) softcap'(p2)
-//   dg[r] = sum_f U[r][u_col0 + f] SiTU(p1) softcap(p2)    (when dg is given)
-// with g_r = scale[scale_rows[r]] (1 without scale).  C features per row, a
-// multiple of 8; each lane takes 8 consecutive features per step (16-byte
-// accesses), two steps in flight.  Strides and offsets are multiples of 8
-// elements.
 // tanh(y) and its derivative 1 - tanh(y)^2 from one exponential: with
 // u = e^(-2|y|), tanh(y) = sign(y) (1 - u) / (1 + u) and
 // 1 - tanh(y)^2 = 4u / (1 + u)^2.  The derivative keeps its relative accuracy
@@ -381,6 +373,14 @@ __device__ __forceinline__ void situ_glu_bwd(float p1, float p2, float da, float
     act = situ * cap;
 }
 
+// SiTU-GLU backward of one row per warp, at the saved pre-activations:
+//   p1 = P[r][f], p2 = P[r][p_half + f], da = g_r * U[r][u_col0 + f]
+//   dP[r][f] = da SiTU'(p1) softcap(p2), dP[r][dp_half + f] = da SiTU(p1) softcap'(p2)
+//   dg[r] = sum_f U[r][u_col0 + f] SiTU(p1) softcap(p2)    (when dg is given)
+// with g_r = scale[scale_rows[r]] (1 without scale).  C features per row, a
+// multiple of 8; each lane takes 8 consecutive features per step (16-byte
+// accesses), two steps in flight.  Strides and offsets are multiples of 8
+// elements.
 constexpr int kGluWarps = 8;
 __global__ void __launch_bounds__(kGluWarps * 32) glu_bwd_rows_kernel(
     const uint16_t *__restrict__ P, int64_t p_ld, int p_half, const uint16_t *__restrict__ U, int64_t u_ld,

@@ -86,6 +86,7 @@ def _load():
             "orc_topk": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
             "orc_permute": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
             "orc_routed": (None, [cfg, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+            "orc_expert_aggregate": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
             "orc_shared_act": (None, [cfg, _I64, _P, _P, _P, _P]),
             "orc_up_shared": (None, [cfg, _I64, _P, _P, _P, _P, _P]),
             "orc_qb_histogram": (None, [_P, _I64, _I32, _I64, _I32, _P, ctypes.c_int]),
@@ -271,6 +272,27 @@ def routed(cfg: LayerConfig, h, idx, gate, w1, w2, w3, want_act=False, want_o=Fa
     if want_o:
         out["o"] = o
     return out
+
+
+def expert_aggregate(cfg: LayerConfig, act, idx, gate, w3):
+    """z [T, latent] fp64 = sum_j gate[t, j] * W3[idx[t, j]] act[t*k + j] from
+    given bf16 activations ([T*k, inter], assignment order); ``w3`` as in
+    ``routed``.  The aggregation step of ``routed`` on its own."""
+    T = idx.shape[0]
+    idx = _need(idx, np.int32, (T, cfg.top_k))
+    gate = _need(gate, np.float32, (T, cfg.top_k))
+    act = _need(act, np.uint16, (T * cfg.top_k, cfg.inter))
+    if T > 0 and (idx.min() < 0 or idx.max() >= cfg.n_experts):
+        raise ValueError("expert index out of range")
+    p3, k3 = _expert_ptrs(w3, cfg.n_experts, (cfg.latent, cfg.inter))
+    for e in np.unique(idx):
+        if not p3[e]:
+            raise ValueError(f"weights of expert {e} were not supplied")
+    z = np.empty((T, cfg.latent), np.float64)
+    c = cfg.c()
+    _load().orc_expert_aggregate(ctypes.byref(c), T, _ptr(act), _ptr(idx), _ptr(gate), p3, _ptr(z))
+    del k3
+    return z
 
 
 # ---------------------------------------------------------------- FP8 variant

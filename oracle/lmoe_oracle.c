@@ -355,6 +355,33 @@ void orc_routed(const orc_config *c, int64_t T, const uint16_t *h, const int32_t
     }
 }
 
+/* The aggregation of the routed experts from given activations ([DD] section
+ * 2 and [NW] "Keeping the numbers in range": the routed outputs are summed,
+ * gate-weighted, before the single norm):
+ *   z[t] = sum_j gate[t][j] * W3[idx[t][j]] act[t*top_k + j]
+ * act: [T*top_k][inter] bf16 in assignment order (e.g. another
+ * implementation's activations, to check its aggregation alone); z_out
+ * [T][latent] fp64.  The same products and sums, in the same order, as the
+ * aggregation inside orc_routed. */
+void orc_expert_aggregate(const orc_config *c, int64_t T, const uint16_t *act, const int32_t *idx,
+                          const float *gate, const uint16_t *const *w3, double *z_out)
+{
+    const int64_t L = c->latent, I = c->inter, K = c->top_k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < T; ++t) {
+        double *z = z_out + t * L;
+        for (int64_t l = 0; l < L; ++l)
+            z[l] = 0.0;
+        for (int64_t j = 0; j < K; ++j) {
+            const int64_t a = t * K + j;
+            const double g = (double)gate[a];
+            const uint16_t *w = w3[idx[a]];
+            for (int64_t l = 0; l < L; ++l)
+                z[l] += g * dot_bf16(w + l * I, act + a * I, I);
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* FP8 variant of the routed experts (e4m3 weights and activations)          */
 /* ------------------------------------------------------------------------ */

@@ -260,6 +260,38 @@ def test_routed_reduces_to_swiglu_and_combines(orc):
     assert np.allclose(z, zref, rtol=1e-12, atol=1e-13)
 
 
+def test_expert_aggregate_from_given_activations(orc):
+    """The aggregation step on its own: on the routed experts' own
+    activations it gives routed's z bit for bit (same products, same order),
+    and on arbitrary activations it equals a numpy sum of gate * W3 act; an
+    expert listed twice with opposite gates cancels."""
+    rng = np.random.default_rng(61)
+    cfg = tiny_cfg(orc)
+    w = tiny_weights(cfg, rng)
+    T = 13
+    h = rand_bf16(rng, (T, cfg.latent))
+    idx = np.stack([rng.choice(cfg.n_experts, cfg.top_k, replace=False) for _ in range(T)]).astype(np.int32)
+    gate = rng.random((T, cfg.top_k)).astype(np.float32)
+    out = orc.routed(cfg, h, idx, gate, w["w1"], w["w2"], w["w3"], want_act=True)
+    z = orc.expert_aggregate(cfg, out["act"], idx, gate, w["w3"])
+    assert np.array_equal(z, out["z"])
+    act = rand_bf16(rng, (T * cfg.top_k, cfg.inter), 3.0)
+    z = orc.expert_aggregate(cfg, act, idx, gate, w["w3"])
+    A = dec(act).reshape(T, cfg.top_k, cfg.inter)
+    ref = np.zeros((T, cfg.latent))
+    for t in range(T):
+        for j in range(cfg.top_k):
+            ref[t] += float(gate[t, j]) * (dec(w["w3"][idx[t, j]]) @ A[t, j])
+    assert np.allclose(z, ref, rtol=1e-12, atol=1e-12)
+    # same expert and activation twice, gates g and -g: the token's z is 0
+    idx2 = np.tile(np.array([[3, 3]], np.int32), (2, 1))
+    g2 = np.array([[0.75, -0.75], [0.5, 0.25]], np.float32)
+    act2 = np.repeat(rand_bf16(rng, (2, cfg.inter)), 2, axis=0)
+    z2 = orc.expert_aggregate(cfg, act2, idx2, g2, w["w3"])
+    assert np.all(z2[0] == 0.0)
+    assert np.allclose(z2[1], 0.75 * (dec(w["w3"][3]) @ dec(act2[2])), rtol=1e-12, atol=1e-13)
+
+
 def test_rmsnorm_unit_rms_and_gate_scale_invariance(orc):
     rng = np.random.default_rng(7)
     cfg = tiny_cfg(orc)

@@ -57,7 +57,11 @@ def test_light_heavy_split_partitions_the_experts():
     touched = int((counts > 0).sum())
     n = shape.T * shape.top_k
     assert counts.sum() == n and 0 < light.sum() and 0 < heavy.sum()
-    assert w["expert_w3"][1] == touched * L * I * 2 + n * I * 2 + 2.0 * n * L
+    # W3 counts the method's bytes: the touched experts' weights and the
+    # activation rows; the o rows this design stores for the combine are not
+    # counted (they are an intermediate of the design)
+    assert w["expert_w3"][1] == touched * L * I * 2 + n * I * 2
+    assert w["combine"][1] == 2.0 * (n * L + shape.T * L)
 
 
 def test_fp8_bytes_halve_the_weight_streams():
@@ -70,8 +74,8 @@ def test_fp8_bytes_halve_the_weight_streams():
         assert b8[name][0] == b16[name][0]                 # same work
     # the heavy stage is weight-dominated: its bytes come close to halving
     assert b8["expert_w12_heavy"][1] < 0.6 * b16["expert_w12_heavy"][1]
-    # W3 still writes its output rows in bf16, so it shrinks less
-    assert b8["expert_w3"][1] < b16["expert_w3"][1]
+    # W3's activation rows are e4m3 codes too, plus one exponent byte per weight row
+    assert b8["expert_w3"][1] < 0.6 * b16["expert_w3"][1]
     for name in ("down", "shared", "router", "up", "combine"):
         assert b8[name] == b16[name]
 

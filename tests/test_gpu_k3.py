@@ -15,8 +15,8 @@ import torch
 import oracle
 from sparse_moe_layer_bias_gb300 import synth
 
-from layer_check import (ACC_REL, check_layer_output, e4m3_table, score_tol, dec, host_bits, oracle_cfg, rel_fro,
-                         to_e4m3, ulp_bf16, ws_view)
+from layer_check import (ACC_REL, check_layer_output, check_o, check_r_from_o, check_y_stage, e4m3_table,
+                         score_tol, dec, host_bits, oracle_cfg, rel_fro, to_e4m3, ulp_bf16, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,30 @@ def run_k3(lm, shape):
     return dict(h=h, ws=ws, lay=lm.lmoe_workspace_layout(h, shape.T), y=y, x=x, bias=bias, w=w)
 
 
-def check_k3(shape, run, sample):
+def k3_sample(idx_gpu, counts, offsets, perm, extra, n_min=128, seed=0):
+    """Tokens for the float checks: the fixed ones in ``extra``; for every
+    expert with more than 128 rows (the pair-tile launch) that no chosen token
+    uses yet, the token of its LAST permuted row (a row of its last, usually
+    partial, tile); then seeded random tokens up to n_min."""
+    K = idx_gpu.shape[1]
+    chosen = list(dict.fromkeys(int(t) for t in extra))
+    covered = set(np.unique(idx_gpu[chosen]).tolist()) if chosen else set()
+    for e in np.nonzero(counts > 128)[0]:
+        if int(e) in covered:
+            continue
+        t = int(perm[offsets[e + 1] - 1]) // K
+        chosen.append(t)
+        covered.update(idx_gpu[t].tolist())
+    rng = np.random.default_rng(seed)
+    T = idx_gpu.shape[0]
+    while len(chosen) < n_min:
+        t = int(rng.integers(T))
+        if t not in chosen:
+            chosen.append(t)
+    return np.array(sorted(chosen))
+
+
+def check_k3(shape, run, extra, n_min=128):
     cfg = oracle_cfg(shape)
     T, E, K, L, I = shape.T, shape.n_experts, shape.top_k, shape.latent, shape.inter
     S = shape.n_shared * shape.shared_inter
@@ -66,14 +89,18 @@ def check_k3(shape, run, sample):
     assert np.array_equal(ws_view(ws, lay, "perm", torch.int32, (T * K,)).cpu().numpy(), perm)
     assert np.array_equal(ws_view(ws, lay, "inv", torch.int32, (T * K,)).cpu().numpy(), inv)
 
-    # float stages on sampled tokens, each fed the GPU's own inputs
-    sm = np.asarray(sample)
-    xb = host_bits(run["x"][torch.from_numpy(sm).cuda()])
+    # float stages on sampled tokens (token-independent layer), each fed the
+    # GPU's own inputs and checked element by element
+    sm = k3_sample(idx_gpu, counts, offsets, perm, extra, n_min=n_min)
+    assert len(sm) >= n_min
+    heavy = np.nonzero(counts > 128)[0]
+    assert np.isin(heavy, idx_gpu[sm]).all()             # every pair-tile expert is exercised
+    smc = torch.from_numpy(sm).cuda()
+    xb = host_bits(run["x"][smc])
     wd = synth.bits(w["w_down"])
     X, Wd = dec(xb), dec(wd)
     exact_h = X @ Wd.T
-    h_all = ws_view(ws, lay, "h", torch.bfloat16, (T, L))
-    h_gpu = host_bits(h_all[torch.from_numpy(sm).cuda()])
+    h_gpu = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L))[smc])
     assert np.all(np.abs(dec(h_gpu) - exact_h) <= ulp_bf16(exact_h) + ACC_REL * (np.abs(X) @ np.abs(Wd).T))
     wr = synth.bits(w["w_router"])
     s_ref = oracle.router(cfg, h_gpu, wr)
@@ -82,42 +109,49 @@ def check_k3(shape, run, sample):
 
     used = np.unique(idx_gpu[sm])
     we = {n: {int(e): synth.bits(w[n][int(e)]) for e in used} for n in ("w1", "w2", "w3")}
-    rt = oracle.routed(cfg, h_gpu, idx_gpu[sm], g_gpu[sm], we["w1"], we["w2"], we["w3"], want_act=True,
-                       want_o=True)
+    rt = oracle.routed(cfg, h_gpu, idx_gpu[sm], g_gpu[sm], we["w1"], we["w2"], we["w3"], want_act=True)
     rows = (sm[:, None] * K + np.arange(K)[None, :]).reshape(-1)       # assignment ids
     prow = inv[rows]                                                    # their permuted rows
-    act_all = ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))
-    act_gpu = dec(host_bits(act_all[torch.from_numpy(prow).cuda()]))
-    assert rel_fro(act_gpu, dec(rt["act"])) <= 5e-3
-    o_all = ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))
-    o_gpu = dec(host_bits(o_all[torch.from_numpy(rows).cuda()]))
-    assert rel_fro(o_gpu, rt["o"]) <= 5e-3
-    r_all = ws_view(ws, lay, "r", torch.bfloat16, (T, L))
-    r_bits = host_bits(r_all[torch.from_numpy(sm).cuda()])
+    act_bits = host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))[torch.from_numpy(prow).cuda()])
+    act_gpu, act_ref = dec(act_bits), dec(rt["act"])
+    Hd = np.abs(dec(h_gpu))
+    acc_tol = np.zeros_like(act_ref)
+    ex = idx_gpu[sm].reshape(-1)
+    for e in np.unique(ex):
+        rr = np.nonzero(ex == e)[0]
+        a1 = Hd[rr // K] @ np.abs(dec(we["w1"][int(e)])).T
+        a2 = Hd[rr // K] @ np.abs(dec(we["w2"][int(e)])).T
+        acc_tol[rr] = ACC_REL * (1.1 * shape.beta2 * a1 + shape.beta1 * a2)
+    assert np.all(np.abs(act_gpu - act_ref) <= 2 * ulp_bf16(act_ref) + acc_tol)
+    o_bits = host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))[torch.from_numpy(rows).cuda()])
+    check_o(cfg, o_bits, act_bits, idx_gpu[sm], g_gpu[sm], we["w3"])
+    r_bits = host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))[smc])
+    check_r_from_o(r_bits, o_bits, K, shape.rms_eps)
     assert rel_fro(dec(r_bits), rt["r64"]) <= 5e-3
-    sa_all = ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))
-    sa_bits = host_bits(sa_all[torch.from_numpy(sm).cuda()])
-    sa_ref = oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"]))
-    assert rel_fro(dec(sa_bits), dec(sa_ref)) <= 5e-3
+    sa_bits = host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))[smc])
+    ws1, ws2 = synth.bits(w["ws1"]), synth.bits(w["ws2"])
+    sa_ref = dec(oracle.shared_act(cfg, xb, ws1, ws2))
+    Xa = np.abs(X)
+    stol = ACC_REL * (1.1 * shape.beta2 * (Xa @ np.abs(dec(ws1)).T) + shape.beta1 * (Xa @ np.abs(dec(ws2)).T))
+    assert np.all(np.abs(dec(sa_bits) - sa_ref) <= 2 * ulp_bf16(sa_ref) + stol)
     wup, ws3 = synth.bits(w["w_up"]), synth.bits(w["ws3"])
-    y_stage = oracle.up_shared(cfg, r_bits, sa_bits, wup, ws3)
-    y_gpu = run["y"][torch.from_numpy(sm).cuda()]
-    assert rel_fro(y_gpu.float().cpu().numpy().astype(np.float64), y_stage) <= 5e-3
+    y_gpu = run["y"][smc]
+    check_y_stage(cfg, y_gpu, r_bits, sa_bits, wup, ws3)
 
     # end to end on the sampled tokens, with the oracle's own routing
     h_o = oracle.down_proj(cfg, xb, wd)
     s_o = oracle.router(cfg, h_o, wr)
     idx_o, g_o, margin = oracle.topk(cfg, s_o, bias)
     used_o = np.unique(idx_o)
-    we_o = {n: {int(e): synth.bits(w[n][int(e)]) for e in used_o} for n in ("w1", "w2", "w3")}
+    we_o = {n: {int(e): we[n][int(e)] if int(e) in we[n] else synth.bits(w[n][int(e)]) for e in used_o}
+            for n in ("w1", "w2", "w3")}
     rt_o = oracle.routed(cfg, h_o, idx_o, g_o, we_o["w1"], we_o["w2"], we_o["w3"])
-    y_o = oracle.up_shared(cfg, rt_o["r"], oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"])),
-                           wup, ws3)
+    y_o = oracle.up_shared(cfg, rt_o["r"], oracle.shared_act(cfg, xb, ws1, ws2), wup, ws3)
     keep = margin > 1e-4
-    if keep.any():
-        check_layer_output(y_gpu, y_o, margin)
-        # on those tokens the GPU chose the same experts
-        assert np.array_equal(np.sort(idx_gpu[sm][keep], 1), np.sort(idx_o[keep], 1))
+    assert keep.sum() >= 0.5 * len(sm)
+    check_layer_output(y_gpu, y_o, margin)
+    # on those tokens the GPU chose the same experts
+    assert np.array_equal(np.sort(idx_gpu[sm][keep], 1), np.sort(idx_o[keep], 1))
     return counts
 
 
@@ -129,8 +163,7 @@ def outlier_tokens(x, n=1):
 def test_k3_decode_layer(lm):
     shape = synth.K3_DECODE
     run = run_k3(lm, shape)
-    sample = sorted(set([0, 17, 40, 63] + outlier_tokens(run["x"])))
-    counts = check_k3(shape, run, sample)
+    counts = check_k3(shape, run, list(range(shape.T)), n_min=shape.T)   # every decode token
     touched = int((counts > 0).sum())
     assert 500 <= touched <= 700            # ~613 distinct experts expected for 64 x 16 picks
 
@@ -138,20 +171,20 @@ def test_k3_decode_layer(lm):
 def test_k3_prefill_layer(lm):
     shape = synth.K3_PREFILL
     run = run_k3(lm, shape)
-    sample = sorted(set([0, 1, 4095, 8191] + outlier_tokens(run["x"], 2)))
-    counts = check_k3(shape, run, sample)
+    counts = check_k3(shape, run, [0, 1, 4095, 8191] + outlier_tokens(run["x"], 2))
     assert counts.sum() == shape.T * shape.top_k
     load = counts / counts.mean()
     assert load.max() > 5.0                 # the router weights make the loads Zipf-skewed
 
 
 # ------------------------------------------------------------------ FP8 variant at K3 size
-def check_k3_fp8(shape, run, sample):
+def check_k3_fp8(shape, run, extra, n_min=128):
     """The FP8 expert variant at the benchmarked K3 shapes: routing is the bf16
     layer's (bit-exact on every token), the e4m3 latent of every token is
     bit-exact, and on the sampled tokens the activation codes are valid
-    roundings of the exact value (as in the tiny/small tests), o and y match
-    the oracle on the GPU's own inputs, and y matches the oracle's FP8 layer."""
+    roundings of the exact value (as in the tiny/small tests), o, r and y
+    match the oracle on the GPU's own inputs element by element, and y
+    matches the oracle's FP8 layer run from the GPU's own latent h."""
     cfg = oracle_cfg(shape)
     T, E, K, L, I = shape.T, shape.n_experts, shape.top_k, shape.latent, shape.inter
     S = shape.n_shared * shape.shared_inter
@@ -172,60 +205,74 @@ def check_k3_fp8(shape, run, sample):
     assert np.array_equal(h8, rc) and np.array_equal(he, re_)
 
     tab = e4m3_table()
-    sm = np.asarray(sample)
+    sm = k3_sample(idx_gpu, counts, offsets, perm, extra, n_min=n_min)
     rows = (sm[:, None] * K + np.arange(K)[None, :]).reshape(-1)      # assignment ids of the sample
     prow = inv[rows]
     act8 = ws[lay["act"]:lay["act"] + T * K * I].view(T * K, I)[torch.from_numpy(prow).cuda()].cpu().numpy()
-    o_all = ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))
-    o_gpu = dec(host_bits(o_all[torch.from_numpy(rows).cuda()]))
     x_exact = np.zeros((rows.size, I))
     o_ref = np.zeros((rows.size, L))
+    o_abs = np.zeros((rows.size, L))
     Hq = tab[h8[sm]] * np.exp2(he[sm].astype(np.float64))[:, None]
-    deq = {}
+    ex = idx_gpu.reshape(-1)[rows]
+    gr = g_gpu.reshape(-1)[rows].astype(np.float64)
 
     def dequant(name, e):
-        if (name, e) not in deq:
-            q, x = oracle.fp8_quantize_rows(synth.bits(w[name][e]))
-            deq[(name, e)] = tab[q] * np.exp2(x.astype(np.float64))[:, None]
-        return deq[(name, e)]
+        q, x = oracle.fp8_quantize_rows(synth.bits(w[name][e]))
+        return tab[q] * np.exp2(x.astype(np.float64))[:, None]
 
-    for n_, a in enumerate(rows):
-        e = int(idx_gpu.reshape(-1)[a])
-        hq = Hq[n_ // K]
-        p1, p2 = dequant("w1", e) @ hq, dequant("w2", e) @ hq
-        x_exact[n_] = 4.0 * shape.beta1 * np.tanh(p1 / shape.beta1) / (1.0 + np.exp(-p1)) * \
+    for e in np.unique(ex):          # the sample's rows of each expert at once
+        rr = np.nonzero(ex == e)[0]
+        hq = Hq[rr // K]
+        p1, p2 = hq @ dequant("w1", int(e)).T, hq @ dequant("w2", int(e)).T
+        x_exact[rr] = 4.0 * shape.beta1 * np.tanh(p1 / shape.beta1) / (1.0 + np.exp(-p1)) * \
             shape.beta2 * np.tanh(p2 / shape.beta2)
-        o_ref[n_] = float(g_gpu.reshape(-1)[a]) * (dequant("w3", e) @ (tab[act8[n_]] / 4.0))
+        W3 = dequant("w3", int(e))
+        a4 = tab[act8[rr]] / 4.0
+        o_ref[rr] = gr[rr, None] * (a4 @ W3.T)
+        o_abs[rr] = gr[rr, None] * (np.abs(a4) @ np.abs(W3).T)
     tol = 2.0 ** -9 * np.abs(x_exact) + 1e-6
     lo, mid, hi = to_e4m3(x_exact - tol), to_e4m3(x_exact), to_e4m3(x_exact + tol)
     assert np.all((act8 == lo) | (act8 == mid) | (act8 == hi))
     assert np.mean(act8 == mid) >= 0.97
-    assert rel_fro(o_gpu, o_ref) <= 5e-3
+    # o on the GPU's codes, element by element (one bf16 rounding plus the
+    # e4m3 MMA's accumulation, allowed 2^-9 of gate * |W3| |act|), and r on
+    # the GPU's own rows o
+    o_bits = host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))[torch.from_numpy(rows).cuda()])
+    o_tol = ulp_bf16(np.abs(o_ref) + 2.0 ** -9 * o_abs) + 2.0 ** -9 * o_abs
+    assert np.all(np.abs(dec(o_bits) - o_ref) <= o_tol)
+    assert rel_fro(dec(o_bits), o_ref) <= 5e-3
+    check_r_from_o(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))[torch.from_numpy(sm).cuda()]), o_bits, K,
+                   shape.rms_eps)
 
     # y on the GPU's own r and shared activations
     r_bits = host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))[torch.from_numpy(sm).cuda()])
     sa_bits = host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))[torch.from_numpy(sm).cuda()])
     wup, ws3 = synth.bits(w["w_up"]), synth.bits(w["ws3"])
     y_gpu = run["y"][torch.from_numpy(sm).cuda()]
-    y_stage = oracle.up_shared(cfg, r_bits, sa_bits, wup, ws3)
+    y_stage = check_y_stage(cfg, y_gpu, r_bits, sa_bits, wup, ws3)
     assert rel_fro(y_gpu.float().cpu().numpy().astype(np.float64), y_stage) <= 5e-3
 
-    # end to end on the sampled tokens from the GPU's own latent h through the
-    # oracle's FP8 layer (quantisation of h, experts, combine, norm, up and
-    # shared experts).  Starting from x instead would compare two different
-    # e4m3 decisions: ~0.5% of h's elements round differently under fp32 and
-    # fp64 accumulation, and e4m3's coarse grid turns one or a few of them per
-    # token into whole-step code differences that move y by 1-2%.
+    # every stage after a1 at once: the oracle's FP8 layer from the GPU's own
+    # latent h (quantisation of h, experts, aggregation, norm, up and shared
+    # experts) on the sampled tokens
     xb = host_bits(run["x"][torch.from_numpy(sm).cuda()])
     h_s = h_all[sm]
     idx_s, g_s = idx_gpu[sm], g_gpu[sm]
     used = np.unique(idx_s)
     we = {n: {int(e): synth.bits(w[n][int(e)]) for e in used} for n in ("w1", "w2", "w3")}
     rt = oracle.routed_fp8(cfg, h_s, idx_s, g_s, we["w1"], we["w2"], we["w3"])
-    y_o = oracle.up_shared(cfg, rt["r"], oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"])),
-                           wup, ws3)
+    a_s = oracle.shared_act(cfg, xb, synth.bits(w["ws1"]), synth.bits(w["ws2"]))
+    y_o = oracle.up_shared(cfg, rt["r"], a_s, wup, ws3)
     _, _, margin = oracle.topk(cfg, s_gpu[sm], bias)
     check_layer_output(y_gpu, y_o, margin)
+
+    # No end-to-end check from x here: at K3 widths nearly every token's
+    # latent has some element whose e4m3 code depends on a last-bit rounding
+    # choice of h (one that a correct fp32 accumulation may take either way),
+    # so the oracle-only filter of the tiny and small FP8 tests keeps no token
+    # at T = 64.  Those tests run it; here the latent h is checked element by
+    # element against the exact product (above) and everything after it
+    # against the oracle from that h.
 
 
 def fp8_shape(shape):
@@ -235,10 +282,10 @@ def fp8_shape(shape):
 def test_k3_decode_layer_fp8(lm):
     shape = fp8_shape(synth.K3_DECODE)
     run = run_k3(lm, shape)
-    check_k3_fp8(shape, run, sorted(set([0, 17, 40, 63] + outlier_tokens(run["x"]))))
+    check_k3_fp8(shape, run, list(range(shape.T)), n_min=shape.T)   # every decode token
 
 
 def test_k3_prefill_layer_fp8(lm):
     shape = fp8_shape(synth.K3_PREFILL)
     run = run_k3(lm, shape)
-    check_k3_fp8(shape, run, sorted(set([0, 1, 4095, 8191] + outlier_tokens(run["x"], 2))))
+    check_k3_fp8(shape, run, [0, 1, 4095, 8191] + outlier_tokens(run["x"], 2))

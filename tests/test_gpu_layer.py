@@ -11,8 +11,8 @@ import torch
 import oracle
 from sparse_moe_layer_bias_gb300 import synth
 
-from layer_check import (ACC_REL, check_layer_output, score_tol, dec, e4m3_table, host_bits, oracle_cfg, rel_fro,
-                         to_e4m3, ulp_bf16, ws_view)
+from layer_check import (ACC_REL, check_layer_output, check_o, check_r_from_o, check_y_stage, fp8_codes_robust, latent_ambiguity, routing_robust_norm_after_down, score_tol, dec,
+                         e4m3_table, host_bits, oracle_cfg, rel_fro, to_e4m3, ulp_bf16, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -109,11 +109,18 @@ def staged_checks(shape, run):
             a2 = Hd[tok[rows]] @ np.abs(dec(wb["w2"][e])).T
             acc_tol[rows] = ACC_REL * (1.1 * shape.beta2 * a1 + shape.beta1 * a2)
         assert np.all(np.abs(act_gpu - act_ref) <= 2 * ulp_bf16(act_ref) + acc_tol)
-        o_gpu = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))))
-        assert rel_fro(o_gpu, rt["o"]) <= 5e-3
 
-        # a7: RMS-normalised aggregate
-        r_gpu = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))
+        # a6: the gate-weighted expert rows on the GPU's own activations,
+        # element by element, and close to the oracle's from its own ones
+        act_bits = host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I)))[inv]   # assignment order
+        o_bits = host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L)))
+        check_o(cfg, o_bits, act_bits, idx_gpu, g_gpu, wb["w3"])
+        assert rel_fro(dec(o_bits), rt["o"]) <= 5e-3
+
+        # a7: aggregate and RMSNorm on the GPU's own rows o, element by element
+        r_bits = host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L)))
+        check_r_from_o(r_bits, o_bits, K, shape.rms_eps)
+        r_gpu = dec(r_bits)
         assert rel_fro(r_gpu, rt["r64"]) <= 5e-3
         assert np.allclose(np.mean(r_gpu ** 2, axis=1), 1.0, atol=2e-2)   # unit RMS after the norm
 
@@ -126,10 +133,11 @@ def staged_checks(shape, run):
                       shape.beta1 * (Xa @ np.abs(dec(wb["ws2"])).T))
     assert np.all(np.abs(dec(sact_gpu) - ds) <= 2 * ulp_bf16(ds) + stol)
 
-    # a8: up-projection + shared add on the GPU's r and shared activations
+    # a8: up-projection + shared add on the GPU's r and shared activations,
+    # element by element
     y_gpu = run["y"].float().cpu().numpy().astype(np.float64)
-    y_stage = oracle.up_shared(cfg, host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))), sact_gpu,
-                               wb["w_up"], wb["ws3"])
+    y_stage = check_y_stage(cfg, y_gpu, host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))), sact_gpu,
+                            wb["w_up"], wb["ws3"])
     assert rel_fro(y_gpu, y_stage) <= 5e-3
 
 
@@ -143,7 +151,8 @@ def fp8_expert_checks(shape, cfg, run, h_lat, idx_gpu, g_gpu, perm, inv, wb):
       tanh.approx, ~2^-11 relative, so a value next to a rounding midpoint may
       round to the neighbouring code), and at least 97% of them equal the
       rounding of the exact value;
-    - o = gate * act8/4 . W3 (e4m3) on the GPU's codes, and r = RMSNorm(sum o)."""
+    - o = gate * act8/4 . W3 (e4m3) on the GPU's codes, element by element,
+      and r = RMSNorm(sum of the token's rows o) on the GPU's own rows."""
     ws, lay = run["ws"], run["layout"]
     T = run["x_host"].shape[0]
     L, I, K = shape.latent, shape.inter, shape.top_k
@@ -158,6 +167,7 @@ def fp8_expert_checks(shape, cfg, run, h_lat, idx_gpu, g_gpu, perm, inv, wb):
     tok, ex = perm // K, idx_gpu.reshape(-1)[perm]
     x_exact = np.zeros((T * K, I))
     o_ref = np.zeros((T * K, L))
+    o_abs = np.zeros((T * K, L))
     gates = g_gpu.reshape(-1).astype(np.float64)
     for e in np.unique(ex):
         rows = np.nonzero(ex == e)[0]
@@ -171,54 +181,65 @@ def fp8_expert_checks(shape, cfg, run, h_lat, idx_gpu, g_gpu, perm, inv, wb):
         situ = shape.beta1 * np.tanh(p1 / shape.beta1) / (1.0 + np.exp(-p1))
         x_exact[rows] = 4.0 * situ * shape.beta2 * np.tanh(p2 / shape.beta2)
         o_ref[perm[rows]] = gates[perm[rows], None] * ((tab[act8[rows]] / 4.0) @ W3.T)
+        o_abs[perm[rows]] = gates[perm[rows], None] * (np.abs(tab[act8[rows]] / 4.0) @ np.abs(W3).T)
     tol = 2.0 ** -9 * np.abs(x_exact) + 1e-6
     lo, mid, hi = to_e4m3(x_exact - tol), to_e4m3(x_exact), to_e4m3(x_exact + tol)
     assert np.all((act8 == lo) | (act8 == mid) | (act8 == hi))
     assert np.mean(act8 == mid) >= 0.97
-    o_gpu = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L))))
-    assert rel_fro(o_gpu, o_ref) <= 5e-3
-    z = dec(host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L)))).reshape(T, K, L).sum(axis=1)
-    r_ref = z / np.sqrt(np.mean(z ** 2, axis=1, keepdims=True) + shape.rms_eps)
-    r_gpu = dec(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))))
-    assert rel_fro(r_gpu, r_ref) <= 5e-3
+    # o per element: one bf16 rounding plus the e4m3 MMA's accumulation,
+    # allowed 2^-9 of gate * |W3| |act| (its internal accumulator width is not
+    # documented; the bf16 MMA gets 2^-20)
+    o_bits = host_bits(ws_view(ws, lay, "o", torch.bfloat16, (T * K, L)))
+    o_tol = ulp_bf16(np.abs(o_ref) + 2.0 ** -9 * o_abs) + 2.0 ** -9 * o_abs
+    assert np.all(np.abs(dec(o_bits) - o_ref) <= o_tol), "o"
+    assert rel_fro(dec(o_bits), o_ref) <= 5e-3
+    check_r_from_o(host_bits(ws_view(ws, lay, "r", torch.bfloat16, (T, L))), o_bits, K, shape.rms_eps)
 
 
-def end_to_end(shape, run):
+def end_to_end(shape, run, allow_empty=False):
+    """The layer output against the oracle's whole forward from x, over the
+    tokens the acceptance bar keeps (routing margin > 1e-4), further
+    filtered, in the two variants whose inputs pass a rounding that a correct
+    GPU result may take the other way, by the oracle alone: the tokens whose
+    oracle routing (norm-after-down) or e4m3 latent codes (FP8) do not change
+    when the ambiguous elements of the oracle's own h round the other way."""
     cfg = oracle_cfg(shape)
     wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
     bias = run["b_host"].numpy()
-    ref = oracle.layer_forward(cfg, synth.bits(run["x_host"]), wb, bias)
+    xb = synth.bits(run["x_host"])
+    ref = oracle.layer_forward(cfg, xb, wb, bias)
     also = None
-    if shape.norm_after_down:
-        # In this variant every element of the routed latent depends on the
-        # whole row of h through its RMS, so a last-bit difference between the
-        # GPU's h and the oracle's (both correct roundings of the same
-        # product, fp32 vs fp64 accumulation) can move a score by ~1e-4 and
-        # swap an expert at a margin above the 1e-4 bar.  Such tokens are
-        # left out: those whose oracle routing, recomputed from the GPU's own
-        # h, differs from the oracle's routing from its own h.
-        T, L = run["x_host"].shape[0], shape.latent
-        h_gpu = host_bits(ws_view(run["ws"], run["layout"], "h", torch.bfloat16, (T, L)))
-        s_g = oracle.router(cfg, oracle.rms_rows(cfg, h_gpu), wb["w_router"])
-        idx_g, _, _ = oracle.topk(cfg, s_g, bias)
-        also = np.all(np.sort(idx_g, 1) == np.sort(ref["idx"], 1), axis=1)
-    if shape.expert_fp8:
-        # FP8 variant: from the GPU's own latent h on (see fp8_expert_checks:
-        # e4m3's coarse grid turns last-bit differences of h into whole-step
-        # code differences, a different but equally valid quantisation)
-        T, L = run["x_host"].shape[0], shape.latent
-        ws, lay = run["ws"], run["layout"]
-        h_gpu = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L)))
-        idx_gpu = ws_view(ws, lay, "topk_idx", torch.int32, (T, shape.top_k)).cpu().numpy()
-        g_gpu = ws_view(ws, lay, "gates", torch.float32, (T, shape.top_k)).cpu().numpy()
-        s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, shape.n_experts)).cpu().numpy()
-        rt = oracle.routed_fp8(cfg, h_gpu, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"])
-        y_ref = oracle.up_shared(cfg, rt["r"], ref["a_s"], wb["w_up"], wb["ws3"])
-        _, _, margin = oracle.topk(cfg, s_gpu, bias)
-        rf, mx, kept = check_layer_output(run["y"], y_ref, margin)
-        return rf, mx, kept, ref
-    rf, mx, kept = check_layer_output(run["y"], ref["y"], ref["margin"], also_keep=also)
+    if shape.norm_after_down or shape.expert_fp8:
+        amb, alt = latent_ambiguity(cfg, xb, wb["w_down"], ref["h_raw"])
+        also = np.ones(xb.shape[0], bool)
+        if shape.norm_after_down:
+            also &= routing_robust_norm_after_down(cfg, ref["h_raw"], amb, alt, wb["w_router"], bias, ref["idx"])
+        if shape.expert_fp8:
+            also &= fp8_codes_robust(ref["h_raw"], amb, alt)
+    rf, mx, kept = check_layer_output(run["y"], ref["y"], ref["margin"], also_keep=also, allow_empty=allow_empty)
     return rf, mx, kept, ref
+
+
+def fp8_from_gpu_latent(shape, run):
+    """FP8 variant, every stage after a1 at once: the oracle's FP8 layer run
+    from the GPU's own latent h (quantisation, experts, aggregation, norm, up
+    and shared experts) against the GPU's y, over every token with routing
+    margin > 1e-4 -- including those whose e4m3 codes the end-to-end check
+    has to leave out."""
+    cfg = oracle_cfg(shape)
+    wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
+    bias = run["b_host"].numpy()
+    T, L = run["x_host"].shape[0], shape.latent
+    ws, lay = run["ws"], run["layout"]
+    h_gpu = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L)))
+    idx_gpu = ws_view(ws, lay, "topk_idx", torch.int32, (T, shape.top_k)).cpu().numpy()
+    g_gpu = ws_view(ws, lay, "gates", torch.float32, (T, shape.top_k)).cpu().numpy()
+    s_gpu = ws_view(ws, lay, "scores", torch.float32, (T, shape.n_experts)).cpu().numpy()
+    rt = oracle.routed_fp8(cfg, h_gpu, idx_gpu, g_gpu, wb["w1"], wb["w2"], wb["w3"])
+    a_s = oracle.shared_act(cfg, synth.bits(run["x_host"]), wb["ws1"], wb["ws2"])
+    y_ref = oracle.up_shared(cfg, rt["r"], a_s, wb["w_up"], wb["ws3"])
+    _, _, margin = oracle.topk(cfg, s_gpu, bias)
+    return check_layer_output(run["y"], y_ref, margin)
 
 
 def test_tiny_layer_stages(lm):
@@ -284,14 +305,26 @@ def test_odd_shape_layer_stages_and_end_to_end(lm):
 
 
 def test_forward_is_deterministic(lm):
-    shape = synth.TINY
+    """Two forwards of the same batch into two workspaces give the same bits:
+    y and every intermediate (no sum depends on thread timing)."""
+    shape = synth.SMALL
+    T, L, K, I = shape.T, shape.latent, shape.top_k, shape.inter
     w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
     x, b = (t.cuda() for t in synth.activations_host(shape))
-    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=x.shape[0])
-    y1 = lm.lmoe_forward(h, x, b).clone()
-    y2 = lm.lmoe_forward(h, x, b)
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=T)
+    lay = lm.lmoe_workspace_layout(h, T)
+    runs = []
+    for _ in range(2):
+        ws = lm.alloc_workspace(h, T)
+        y = lm.lmoe_forward(h, x, b, workspace=ws)
+        runs.append((y, ws))
     torch.cuda.synchronize()
+    (y1, ws1), (y2, ws2) = runs
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    for key, dt, shp in (("scores", torch.int32, (T, shape.n_experts)), ("topk_idx", torch.int32, (T, K)),
+                         ("perm", torch.int32, (T * K,)), ("h", torch.int16, (T, L)),
+                         ("act", torch.int16, (T * K, I)), ("o", torch.int16, (T * K, L)), ("r", torch.int16, (T, L))):
+        assert torch.equal(ws_view(ws1, lay, key, dt, shp), ws_view(ws2, lay, key, dt, shp)), key
 
 
 def test_host_errors_enqueue_nothing(lm):
@@ -355,7 +388,7 @@ def test_norm_after_down_variant_tiny(lm, T):
     stage on the GPU's own inputs, and the output end to end."""
     run = run_host_shape(lm, TINY_NORM, T=T, seed_offset=0 if T is None else T)
     staged_checks(TINY_NORM, run)
-    end_to_end(TINY_NORM, run)
+    end_to_end(TINY_NORM, run, allow_empty=T is not None)
 
 
 def test_norm_after_down_variant_small(lm):
@@ -412,14 +445,19 @@ def test_fp8_experts_variant_tiny(lm, T):
     and the output end to end against the oracle's FP8 layer."""
     run = run_host_shape(lm, TINY_FP8, T=T, seed_offset=0 if T is None else T)
     staged_checks(TINY_FP8, run)
-    end_to_end(TINY_FP8, run)
+    fp8_from_gpu_latent(TINY_FP8, run)
+    # with a handful of tokens the oracle-only filter may leave none
+    rf, mx, kept, _ = end_to_end(TINY_FP8, run, allow_empty=T is not None)
+    if T is None:
+        assert kept >= 0.5 * TINY_FP8.T
 
 
 def test_fp8_experts_variant_small(lm):
     run = run_host_shape(lm, SMALL_FP8)
     staged_checks(SMALL_FP8, run)
+    fp8_from_gpu_latent(SMALL_FP8, run)
     rf, mx, kept, _ = end_to_end(SMALL_FP8, run)
-    assert kept >= 0.8 * SMALL_FP8.T
+    assert kept >= 0.5 * SMALL_FP8.T
 
 
 def test_fp8_experts_rejects_unaligned_inter(lm):

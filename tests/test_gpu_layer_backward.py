@@ -286,17 +286,14 @@ def test_backward_with_forward_outputs_in_caller_buffers(lm):
     """A forward that wrote its routing outputs to caller buffers leaves those
     workspace slots untouched (here: filled with 0xff bytes); the backward
     takes topk_idx and gates from the caller and derives the per-expert counts
-    from the workspace's offsets, so it gives the same bits as the default
-    path."""
+    from the workspace's offsets.  It gives the same bits as the default path
+    on a copy of that workspace whose routing slots hold the same values."""
     shape = synth.TINY
     T = 64
     w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
     x, bias = (t.cuda() for t in synth.activations_host(shape, T=T, seed_offset=9))
     dy = synth.grad_output_host(shape, T=T, seed_offset=9).cuda()
     h = lm.lmoe_create(dict(shape.layer_dict(), with_backward=True), w, max_tokens=T)
-    ws = lm.alloc_workspace(h, T)
-    lm.lmoe_forward(h, x, bias, workspace=ws)
-    dx_a, g_a = lm.lmoe_backward(h, x, dy, ws)
     ws2 = lm.alloc_workspace(h, T)
     ws2.fill_(255)
     E, K = shape.n_experts, shape.top_k
@@ -306,7 +303,15 @@ def test_backward_with_forward_outputs_in_caller_buffers(lm):
     counts = torch.empty(E, dtype=torch.int32, device="cuda")
     lm.lmoe_forward(h, x, bias, workspace=ws2, scores_out=scores, topk_idx_out=idx, gates_out=gates,
                     expert_counts_out=counts)
+    torch.cuda.synchronize()
+    lay = lm.lmoe_workspace_layout(h, T)
+    for key in ("topk_idx", "gates"):      # the slots the forward left alone
+        assert torch.all(ws_view(ws2, lay, key, torch.int32, (T, K)) == -1)
+    ws = ws2.clone()
+    ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).copy_(idx)
+    ws_view(ws, lay, "gates", torch.float32, (T, K)).copy_(gates)
     dx_b, g_b = lm.lmoe_backward(h, x, dy, ws2, topk_idx=idx, gates=gates)
+    dx_a, g_a = lm.lmoe_backward(h, x, dy, ws)
     torch.cuda.synchronize()
     assert lm.lmoe_device_status(h) == 0
     assert torch.equal(dx_a, dx_b)

@@ -41,7 +41,8 @@ typedef enum {
     LMOE_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required     */
     LMOE_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed           */
     LMOE_ERR_TIMEOUT = 6,           /* a kernel's bounded wait gave up (device error) */
-    LMOE_ERR_NO_DEVICE = 7          /* the current device is not sm_103 (GB300)       */
+    LMOE_ERR_NO_DEVICE = 7,         /* the current device is not sm_103 (GB300)       */
+    LMOE_ERR_INDEX = 8              /* a debug build's index check failed (device error) */
 } lmoe_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -184,7 +185,9 @@ int lmoe_workspace_layout(const lmoe_handle *handle, int64_t T, lmoe_ws_layout *
  * timing hook (lmoe_set_stage_events) is set, the shared experts' GEMM runs on
  * a side stream of the handle, ordered after the work already in `stream`
  * and joined back into `stream` before the routed experts, so everything the
- * call enqueues is ordered within `stream` as seen from outside. */
+ * call enqueues is ordered within `stream` as seen from outside.  The
+ * result is bitwise reproducible: no sum depends on the order in which the
+ * kernels' threads run. */
 int lmoe_forward(lmoe_handle *handle, const uint16_t *x, int64_t T, const float *bias,
                  uint16_t *y, float *scores_out, int32_t *topk_idx_out, float *gates_out,
                  int32_t *expert_counts_out, void *workspace, size_t workspace_bytes,
@@ -211,7 +214,10 @@ int lmoe_host_io_size(const lmoe_handle *handle, size_t *bytes);
  * y_host untouched, until then.  Host buffers should be page-locked
  * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously.
  * io_dev: lmoe_host_io_size bytes, 256-byte aligned, used only through this
- * call.  Errors are reported before anything is enqueued, as in lmoe_forward.
+ * call.  Argument errors are reported before anything is enqueued, as in
+ * lmoe_forward.  A CUDA error after the input copy was queued leaves the
+ * staging slot ordered after the work the call did queue, so later calls stay
+ * correct; the failed call's y_host is not written.
  * One host thread and one `stream` per handle at a time.  The pages describe
  * no host-memory interface; this is an addition of this library. */
 int lmoe_forward_host(lmoe_handle *handle, const uint16_t *x_host, int64_t T, const float *bias_host,
@@ -351,8 +357,14 @@ int lmoe_set_backward_events(lmoe_handle *handle, cudaEvent_t *events, int n_eve
  * perm [T*top_k] int32, inv [T*top_k] int32.
  * Scratch lives in one fixed 8 MiB array inside the library (every GPU that
  * loads the library holds it until exit); problems whose scratch exceeds it
- * (about 16*E*ceil(T/32) + 20*T*top_k + 16*E bytes) return
- * LMOE_ERR_UNSUPPORTED_SHAPE.  It calls no cudaMalloc/cudaFree.  The first call
+ * return LMOE_ERR_UNSUPPORTED_SHAPE.  With n = T*top_k and each term rounded
+ * up to a multiple of 256 bytes, the scratch is
+ *   4*E*ceil(T/32)                (token bitmap of each expert)
+ * + 4*E*ceil(T/32)                (popcount prefix of each bitmap word)
+ * + 16*(ceil(n/128) + E)          (128-row tile list)
+ * + 16*(ceil(n/256) + E)          (256-row tile list)
+ * + 256                           (tile counts)
+ * + 4*n                           (token of each permuted row) bytes.  It calls no cudaMalloc/cudaFree.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress), so
  * make that first call before any stream capture.  All calls share the array:
  * calls whose work overlaps on the GPU (other streams, other threads) race and
@@ -369,10 +381,28 @@ int lmoe_route_static(const float *scores, int64_t T, int32_t E, int32_t top_k, 
  * usable.  The pages describe no such call; it is an addition of this library. */
 int lmoe_selftest_timeout(lmoe_handle *handle, uint64_t limit_ns, cudaStream_t stream);
 
-/* Device-side status of the handle's kernels (bounded waits that gave up).
- * Synchronises `stream`, copies the status word, and clears it when `clear`
- * is non-zero.  *device_status is LMOE_OK or LMOE_ERR_TIMEOUT. */
+/* Device-side status of the handle's kernels (bounded waits that gave up;
+ * in a debug build also failed index checks).  Synchronises `stream`, copies
+ * the status word, and clears it when `clear` is non-zero.  *device_status is
+ * LMOE_OK, LMOE_ERR_TIMEOUT or (debug builds) LMOE_ERR_INDEX, which takes
+ * precedence.  The index-check words are per library, not per handle. */
 int lmoe_device_status(lmoe_handle *handle, cudaStream_t stream, int clear, int *device_status);
+
+/* 1 if this library was built with index checks (-DLMOE_DEBUG), else 0.
+ * Such a build checks, before every use, each index that a kernel reads from
+ * a device list -- the rows the expert GEMMs gather and scatter (and their
+ * gates), the permutation maps, the grouped GEMMs' tile lists and their
+ * counts, the backward's column maps.  A failed check skips the access (the
+ * affected rows are left unwritten), records the failure, and
+ * lmoe_device_status then returns LMOE_ERR_INDEX.  Nothing traps.  The
+ * pages describe no such build; it is an addition of this library. */
+int lmoe_debug_checks(void);
+
+/* Self-test of that reporting path: in a debug build enqueues one thread that
+ * fails one index check without touching memory, so a following
+ * lmoe_device_status (any handle) reports LMOE_ERR_INDEX.  A release build
+ * returns LMOE_ERR_INVALID_ARG and enqueues nothing. */
+int lmoe_selftest_index(cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Quantile Balancing                                                        */

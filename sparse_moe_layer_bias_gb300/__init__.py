@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     lmoe_backward,
     lmoe_backward_workspace_size,
     lmoe_create,
+    lmoe_debug_checks,
     lmoe_destroy,
     lmoe_device_status,
     lmoe_forward,
@@ -23,6 +24,7 @@ from .binding import (  # noqa: F401
     lmoe_host_io_size,
     lmoe_host_wait,
     lmoe_route_static,
+    lmoe_selftest_index,
     lmoe_selftest_timeout,
     lmoe_set_stage_events,
     STAGES,

@@ -12,17 +12,19 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblmoe.so")
+# LMOE_LIBRARY=debug selects the build with index checks (build.build(debug=True))
+_LIB_NAME = "liblmoe_debug.so" if os.environ.get("LMOE_LIBRARY") == "debug" else "liblmoe.so"
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), _LIB_NAME)
 _lib = None
 
 STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED_SHAPE",
           3: "LMOE_ERR_ALIGNMENT", 4: "LMOE_ERR_WORKSPACE", 5: "LMOE_ERR_CUDA",
-          6: "LMOE_ERR_TIMEOUT", 7: "LMOE_ERR_NO_DEVICE"}
+          6: "LMOE_ERR_TIMEOUT", 7: "LMOE_ERR_NO_DEVICE", 8: "LMOE_ERR_INDEX"}
 
 EXPORTED = ("lmoe_status_string", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size",
             "lmoe_workspace_layout", "lmoe_forward", "lmoe_host_io_size", "lmoe_forward_host",
             "lmoe_host_wait", "lmoe_device_status", "lmoe_set_stage_events", "lmoe_set_backward_events",
-            "lmoe_route_static",
+            "lmoe_route_static", "lmoe_debug_checks", "lmoe_selftest_index",
             "lmoe_selftest_timeout", "lmoe_backward_workspace_size", "lmoe_backward", "qb_histogram",
             "qb_quantile_bias", "qb_sign_update")
 
@@ -71,7 +73,8 @@ def library_path() -> str:
 
 
 def load_library():
-    """Load liblmoe.so (built in-tree by build.build()); raise if it is absent."""
+    """Load liblmoe.so (built in-tree by build.build()), or with LMOE_LIBRARY=debug
+    liblmoe_debug.so (build.build(debug=True)); raise if it is absent."""
     global _lib
     if _lib is not None:
         return _lib
@@ -114,6 +117,10 @@ def load_library():
     lib.lmoe_set_backward_events.argtypes = [P, P, ctypes.c_int]
     lib.lmoe_route_static.restype = ctypes.c_int
     lib.lmoe_route_static.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P]
+    lib.lmoe_debug_checks.restype = ctypes.c_int
+    lib.lmoe_debug_checks.argtypes = []
+    lib.lmoe_selftest_index.restype = ctypes.c_int
+    lib.lmoe_selftest_index.argtypes = [P]
     lib.qb_histogram.restype = ctypes.c_int
     lib.qb_histogram.argtypes = [P, I64, I32, I64, I32, P, ctypes.c_int, P]
     lib.qb_sign_update.restype = ctypes.c_int
@@ -378,6 +385,14 @@ def lmoe_device_status(handle: Handle, clear: bool = True, stream=None) -> int:
     _check("lmoe_device_status",
            load_library().lmoe_device_status(handle.ptr, _stream(stream), 1 if clear else 0, ctypes.byref(v)))
     return v.value
+
+
+def lmoe_debug_checks() -> bool:
+    return bool(load_library().lmoe_debug_checks())
+
+
+def lmoe_selftest_index(stream=None):
+    _check("lmoe_selftest_index", load_library().lmoe_selftest_index(_stream(stream)))
 
 
 def lmoe_route_static(scores: torch.Tensor, bias: torch.Tensor, top_k: int, stream=None) -> dict:

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *__restri
         float sc = 1.0f;
         if (q < Q) {
             src = qsrc ? qsrc[q] : (q < R ? q : -1);
+            if (src >= 0 && !idx_ok(src, R)) src = -1;   // debug builds: a row outside the input
             if (qscale && src >= 0) sc = qscale[q];
         }
         const int c = c0 + chunk * 8;
@@ -172,7 +173,8 @@ __global__ void __launch_bounds__(256) segment_maps_kernel(const int32_t *__rest
         if (c < cnt) {
             p = offsets[e] + c;
             t = tokrow[p];
-            g = gates[perm[p]];
+            const int32_t a = perm[p];
+            g = idx_ok(a, offsets[gridDim.x]) ? gates[a] : 0.0f;   // offsets[E] = assignments
         }
         qperm[s0 + c] = p;
         qtok[s0 + c] = t;
@@ -295,7 +297,8 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict
             const float x = logits[t * E + e];
             const float sp = 1.0f / (1.0f + __expf(-x));
             const float sm = 1.0f / (1.0f + __expf(x));
-            v = dg[inv[a]] * (sp * sm);
+            const int32_t p = inv[a];
+            v = idx_ok(p, T * k) ? dg[p] * (sp * sm) : 0.0f;
         } else {
             e = -1;
         }
@@ -393,7 +396,8 @@ __global__ void __launch_bounds__(kGluWarps * 32) glu_bwd_rows_kernel(
     const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;   // once per thread
     const int chunks = C >> 3;
     for (int64_t r = warp0; r < rows; r += nwarps) {
-        const float g = scale ? scale[scale_rows ? scale_rows[r] : r] : 1.0f;
+        const int64_t si = scale_rows ? scale_rows[r] : r;
+        const float g = (scale && idx_ok(si, rows)) ? scale[si] : (scale ? 0.0f : 1.0f);
         const uint16_t *p1r = P + r * p_ld, *p2r = p1r + p_half, *ur = U + r * u_ld + u_col0;
         uint16_t *d1r = dP + r * dp_ld, *d2r = d1r + dp_half;
         float acc = 0.0f;
@@ -533,5 +537,7 @@ cudaError_t launch_fill(float *p, int64_t n, float v, cudaStream_t stream) {
     const int blocks = blocks_for(n, 256, 1024);
     return launch_kernel(fill_kernel, dim3(blocks), dim3(256), 0, stream, true, p, n, v);
 }
+
+LMOE_DEBUG_WORD_READER(debug_word_backward)
 
 }  // namespace lmoe

@@ -34,7 +34,8 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
             if (bn == 128) return launch_one<128, A_GATHER, B_GLU, EPI_SITU_GLU, true, false>(maps, args, grid, stream, dependent);
         }
     }
-    // a6 routed experts W3 with the gate-weighted scatter
+    // a6 routed experts W3 with the gate-weighted scatter (also the backward's
+    // experts' share of dh, rows scattered back to assignment order)
     LMOE_GEMM_CASE(256, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
     LMOE_GEMM_CASE(128, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true)
     // FP8 variant: e4m3 experts (kind::f8f6f4)
@@ -53,5 +54,7 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
 }
 
 #undef LMOE_GEMM_CASE
+
+LMOE_DEBUG_WORD_READER(debug_word_gemm)
 
 }  // namespace lmoe

@@ -48,4 +48,6 @@ cudaError_t launch_gemm_save(int bn, AMode am, bool grouped, bool pair, const Ge
     return cudaErrorInvalidValue;
 }
 
+LMOE_DEBUG_WORD_READER(debug_word_gemm_bwd)
+
 }  // namespace lmoe

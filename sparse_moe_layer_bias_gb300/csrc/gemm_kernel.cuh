@@ -105,6 +105,11 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
         ti.nk = d.z;
         ti.row0 = d.w;
         ti.nrows = min(kBM, a.m_rows - d.w);
+        if (kDebugChecks && !(idx_ok(mt, a.lim_tiles) && idx_ok(d.x, a.lim_experts) && d.y >= 0 && d.z >= 0 &&
+                              d.w >= 0)) {
+            ti.expert = 0;   // a bad entry becomes an empty tile
+            ti.k0 = ti.nk = ti.row0 = ti.nrows = 0;
+        }
     } else if (GROUPED) {
         // M-tile major: the N tiles of one M tile run side by side on
         // neighbouring SMs and share its activation rows through L2; the M
@@ -116,6 +121,11 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
         ti.expert = d.x;
         ti.row0 = d.y;
         ti.nrows = d.z;
+        if (kDebugChecks && !(idx_ok(mt, a.lim_tiles) && idx_ok(d.x, a.lim_experts) && d.z >= 1 &&
+                              d.z <= 2 * kBM && idx_ok(d.y, a.lim_rows) && idx_ok(d.y + d.z - 1, a.lim_rows))) {
+            ti.expert = 0;   // a bad entry becomes an empty tile
+            ti.row0 = ti.nrows = 0;
+        }
     } else {
         // Rasterise in groups of 16 M tiles so the A rows of a group stay in L2
         // while every N tile visits them.
@@ -245,7 +255,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     const uint32_t tmem_base = *tmem_slot;
 
     grid_dependency_wait();   // inputs of this GEMM come from earlier kernels
-    const int n_m = GROUPED ? *args.n_mtiles : args.m_tiles;
+    int n_m = GROUPED ? *args.n_mtiles : args.m_tiles;
+    if (kDebugChecks && GROUPED && args.lim_tiles > 0 && !idx_ok(n_m, args.lim_tiles + 1)) n_m = 0;   // n_m <= capacity
     const int total = n_m * args.n_tiles;
     const uint64_t lim = args.wait_limit_ns;
 
@@ -328,9 +339,11 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 #pragma unroll
             for (int j = 0; j < 8 * NSUB; ++j) {
                 const int r = rb + 16 * j;
-                src[j] = (r < ti.nrows)
-                             ? args.gather_src + int64_t(args.gather_rows[ti.row0 + r]) * args.gather_ld + c * 8
-                             : nullptr;
+                src[j] = nullptr;
+                if (r < ti.nrows) {
+                    const int32_t sr = args.gather_rows[ti.row0 + r];
+                    if (idx_ok(sr, args.lim_src_rows)) src[j] = args.gather_src + int64_t(sr) * args.gather_ld + c * 8;
+                }
             }
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 const int slot = g % S;
@@ -426,18 +439,23 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             int64_t pre_drow[NSUB];
             float pre_scale[NSUB];
             int pre_he[NSUB];
+            bool pre_ok[NSUB];   // false: a debug build's index check failed; the row is not written
 #pragma unroll
             for (int sub = 0; sub < NSUB; ++sub) {
                 const int trow = sub * kBM + row;
                 pre_drow[sub] = ti.row0 + trow;
                 pre_scale[sub] = 1.0f;
                 pre_he[sub] = 0;
+                pre_ok[sub] = true;
                 if (trow < ti.nrows) {
                     if (EPI == EPI_SCATTER_BF16 || EPI == EPI_SCATTER_F8) {
                         pre_drow[sub] = args.scatter_rows[ti.row0 + trow];
-                        pre_scale[sub] = args.row_scale[pre_drow[sub]];
+                        pre_ok[sub] = idx_ok(pre_drow[sub], args.lim_out_rows) && idx_ok(pre_drow[sub], args.lim_scale);
+                        if (pre_ok[sub]) pre_scale[sub] = args.row_scale[pre_drow[sub]];
                     } else if (EPI == EPI_SITU_GLU_F8) {
-                        pre_he[sub] = args.row_exp[args.gather_rows[ti.row0 + trow]];
+                        const int32_t sr = args.gather_rows[ti.row0 + trow];
+                        pre_ok[sub] = idx_ok(sr, args.lim_src_rows);
+                        if (pre_ok[sub]) pre_he[sub] = args.row_exp[sr];
                     }
                 }
             }
@@ -468,7 +486,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>((acc + sub) * kAccStride);
             const int trow = sub * kBM + row;    // row of the tile (pair tiles: 0..255)
-            const bool rv = trow < ti.nrows;
+            const bool rv = trow < ti.nrows && ((NSUB > 1 && sub) ? pre_ok[NSUB - 1] : pre_ok[0]);
             if (EPI == EPI_SIGMOID_F32) {
                 // fp32 scores: 32 columns (128 B) per row and group, staged like
                 // the bf16 outputs below; the last partial group of a ragged N is

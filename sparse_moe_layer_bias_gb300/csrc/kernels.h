@@ -40,6 +40,63 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 // Device status bits written by kernels (see lmoe_device_status).
 constexpr unsigned kDevErrTimeout = 1u;
 
+// ------------------------------------------------------------------ debug index checks
+// A build with -DLMOE_DEBUG checks every index a kernel reads from a device
+// list before using it: gathered and scattered rows, the permutation maps and
+// the grouped GEMMs' tile lists.  A failed check sets this translation unit's
+// debug word and the access is skipped (no trap); lmoe_device_status reports
+// it as LMOE_ERR_INDEX.  In a release build idx_ok() is constant true and the
+// checks compile away.
+#ifdef LMOE_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+#if defined(__CUDACC__) && defined(LMOE_DEBUG)
+static __device__ unsigned g_dbg_index_word;
+#endif
+
+#ifdef __CUDACC__
+// 0 <= i < n (n <= 0: no known limit).  Debug builds record a violation.
+__device__ __forceinline__ bool idx_ok(int64_t i, int64_t n) {
+#ifdef LMOE_DEBUG
+    if (n <= 0 || (i >= 0 && i < n)) return true;
+    atomicOr(&g_dbg_index_word, 1u);
+    return false;
+#else
+    (void)i;
+    (void)n;
+    return true;
+#endif
+}
+#endif
+
+// The debug word of each translation unit that checks indices (0 in a release
+// build); `clear` resets it.  Synchronous.
+unsigned debug_word_gemm(bool clear);
+unsigned debug_word_gemm_bwd(bool clear);
+unsigned debug_word_route(bool clear);
+unsigned debug_word_backward(bool clear);
+unsigned debug_word_selftest(bool clear);
+#ifdef LMOE_DEBUG
+#define LMOE_DEBUG_WORD_READER(fn)                                                         \
+    unsigned fn(bool clear) {                                                              \
+        unsigned v = 0;                                                                    \
+        if (cudaMemcpyFromSymbol(&v, g_dbg_index_word, sizeof v) != cudaSuccess) return ~0u; \
+        if (clear && v) {                                                                  \
+            const unsigned z = 0;                                                          \
+            if (cudaMemcpyToSymbol(g_dbg_index_word, &z, sizeof z) != cudaSuccess) return ~0u; \
+        }                                                                                  \
+        return v;                                                                          \
+    }
+#else
+#define LMOE_DEBUG_WORD_READER(fn) \
+    unsigned fn(bool) { return 0; }
+#endif
+// One thread fails one index check (debug builds; nothing in a release build).
+cudaError_t launch_index_check_selftest(cudaStream_t stream);
+
 // ------------------------------------------------------------------ GEMM
 // A operand source.
 // A_GATHER: rows of A are gathered by a row-index list (cp.async by four
@@ -88,8 +145,8 @@ struct GemmArgs {
     void *out;               // output base
     int64_t ld_out;          // output row stride (elements)
     int32_t out_cols;        // output columns that exist (masking of ragged N)
-    const int32_t *scatter_rows;  // EPI_SCATTER_BF16: destination row per permuted row
-    const float *row_scale;       // EPI_SCATTER_BF16: scale per destination row
+    const int32_t *scatter_rows;  // EPI_SCATTER_*: destination row per permuted row
+    const float *row_scale;       // EPI_SCATTER_*: scale per destination row
     float beta1, beta2;
     // e4m3 experts: power-of-two scale exponents
     const int8_t *row_exp;        // EPI_SITU_GLU_F8: per source token row (indexed via gather_rows)
@@ -110,6 +167,10 @@ struct GemmArgs {
     int32_t pout_half;
     unsigned *err;           // device status word
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
+    // limits for the debug build's index checks (0: no check): experts,
+    // entries of the tile list, rows of the grouped row lists, rows of the
+    // gathered source, rows of the scattered output, entries of row_scale
+    int64_t lim_experts, lim_tiles, lim_rows, lim_src_rows, lim_out_rows, lim_scale;
 };
 
 // Launch one persistent GEMM.  `bn` in {128, 256} (224 for the router).  With `pair`, A_GATHER runs
@@ -157,7 +218,7 @@ cudaError_t launch_expert_scan(const uint32_t *bitmap, int E, int words_per_expe
 cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets, int4 *tiles,
                                  int32_t *n_mtiles, int4 *tiles2, int32_t *n_mtiles2, int4 *tiles3,
                                  int32_t *n_mtiles3, cudaStream_t stream);
-cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
+cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, int E, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words_per_expert,
                            const int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *tokrow,
                            cudaStream_t stream);

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -391,6 +392,7 @@ const char *lmoe_status_string(int s) {
         case LMOE_ERR_CUDA: return "LMOE_ERR_CUDA";
         case LMOE_ERR_TIMEOUT: return "LMOE_ERR_TIMEOUT";
         case LMOE_ERR_NO_DEVICE: return "LMOE_ERR_NO_DEVICE";
+        case LMOE_ERR_INDEX: return "LMOE_ERR_INDEX";
         default: return "LMOE_ERR_UNKNOWN";
     }
 }
@@ -662,8 +664,11 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     // Without the timing hook the shared experts run on the side stream once
     // the router is done, while the routing kernels (small and latency-bound)
     // run here on the same SMs; the join comes before the routed experts'
-    // GEMMs, which need every SM.  With the hook, the stages run in stream
-    // order so that each stage's events bracket it alone.
+    // GEMMs, which need every SM: the HBM-bound expert launches reach the
+    // memory roofline only with every SM's loads in flight, so giving some
+    // SMs to the shared experts beside them measured slower (design notes).
+    // With the hook, the stages run in stream order so that each stage's
+    // events bracket it alone.
     const bool overlap = (h->stage_events == nullptr);
     if (overlap) {
         st = run_router();
@@ -695,7 +700,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
                              stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_SCATTER);
-    if (launch_scatter(idx, T, static_cast<int>(K), bitmap, wprefix, words, offsets, perm, inv, tokrow,
+    if (launch_scatter(idx, T, static_cast<int>(K), static_cast<int>(E), bitmap, wprefix, words, offsets, perm, inv, tokrow,
                        stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     if (overlap && cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess) return LMOE_ERR_CUDA;
@@ -735,13 +740,18 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
             return save ? launch_gemm_save(h->bn_exp1, A_GATHER, true, pair, m, a, grid, stream)
                         : launch_gemm(h->bn_exp1, A_GATHER, B_GLU, epi, true, m, a, grid, stream, pair);
         };
+        a.lim_experts = E;               // limits of the debug build's index checks
+        a.lim_rows = n;
+        a.lim_src_rows = T;
         a.tiles = tiles3;
         a.n_mtiles = nmt + 2;
+        a.lim_tiles = E;
         st = gemm_status(w12(/*pair=*/false, grid_for(E * a.n_tiles)));
         if (st) return st;
         mark(LMOE_STAGE_EXPERT_W12_HEAVY);
         a.tiles = tiles2;
         a.n_mtiles = nmt + 1;
+        a.lim_tiles = ceil_div(n, 2 * kBM) + E;
         const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
         st = gemm_status(w12(/*pair=*/true, grid_for(max_pairs)));
         if (st) return st;
@@ -760,6 +770,11 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.b_row_tiles = static_cast<int32_t>(L / h->bn_exp3);
         a.tiles = tiles;
         a.n_mtiles = nmt;
+        a.lim_tiles = ceil_div(n, kBM) + E;
+        a.lim_experts = E;
+        a.lim_rows = n;
+        a.lim_out_rows = n;
+        a.lim_scale = n;
         a.out = obuf;
         a.ld_out = L;
         a.out_cols = static_cast<int32_t>(L);
@@ -986,6 +1001,10 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         // TMEM, measured slower here: their epilogue cannot overlap the MMAs)
         a.tiles = tiles;
         a.n_mtiles = nmt;
+        a.lim_tiles = ceil_div(n, kBM) + E;
+        a.lim_experts = E;
+        a.lim_rows = n;
+        a.lim_src_rows = T;
         st = gemm_status(launch_gemm_bwd(h->bn_u, A_GATHER, B_PLAIN, EPI_BF16, true, false, m, a,
                                          grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
@@ -1018,6 +1037,11 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.out_cols = static_cast<int32_t>(L);
         a.scatter_rows = perm;
         a.row_scale = ones;
+        a.lim_tiles = ceil_div(n, kBM) + E;
+        a.lim_experts = E;
+        a.lim_rows = n;
+        a.lim_out_rows = n;
+        a.lim_scale = n;
         st = gemm_status(launch_gemm(h->bn_exp3, A_DENSE, B_PLAIN, EPI_SCATTER_BF16, true, m, a,
                                      grid_for(grouped_tiles * a.n_tiles), stream));
         if (st) return st;
@@ -1120,6 +1144,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.n_tiles = static_cast<int32_t>(ceil_div(I, h->bn_u));
         a.tiles = kt_a;
         a.n_mtiles = nkt;
+        a.lim_tiles = E * mt_a;
+        a.lim_experts = E;
         a.out = g->w3;
         a.out2 = g->w3;
         a.ld_out = I;
@@ -1140,6 +1166,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
         a.tiles = kt_b;
         a.n_mtiles = nkt + 1;
+        a.lim_tiles = E * mt_b;
+        a.lim_experts = E;
         a.out = g->w1;
         a.out2 = g->w2;
         // dW1 | dW2 tiles hold few K blocks and are nearly all output: both
@@ -1193,19 +1221,30 @@ int lmoe_forward_host(lmoe_handle *h, const uint16_t *x_host, int64_t T, const f
             cudaSuccess ||
         cudaEventRecord(h->ev_in[s], h->io_in) != cudaSuccess)
         return LMOE_ERR_CUDA;
+    // From here on the slot's input copy is queued.  If anything below fails,
+    // the slot's "forward done" event is still recorded after whatever this
+    // call queued on `stream`, and the call counter moves on, so that the
+    // next call that copies into this slot waits for that work first.
+    auto fail = [&](int status) {
+        cudaEventRecord(h->ev_fwd[s], stream);
+        ++h->io_calls;
+        return status;
+    };
     // 2. the forward, after its input landed and the slot's last output copy
     if (cudaStreamWaitEvent(stream, h->ev_in[s], 0) != cudaSuccess ||
         cudaStreamWaitEvent(stream, h->ev_out[s], 0) != cudaSuccess)
-        return LMOE_ERR_CUDA;
+        return fail(LMOE_ERR_CUDA);
     const int st = lmoe_forward(h, xs, T, bs, ys, scores_out, topk_idx_out, gates_out, expert_counts_out,
                                 workspace, workspace_bytes, stream);
-    if (st) return st;
-    if (cudaEventRecord(h->ev_fwd[s], stream) != cudaSuccess) return LMOE_ERR_CUDA;
+    if (st) return fail(st);
+    if (cudaEventRecord(h->ev_fwd[s], stream) != cudaSuccess) return fail(LMOE_ERR_CUDA);
     // 3. output copy
     if (cudaStreamWaitEvent(h->io_out, h->ev_fwd[s], 0) != cudaSuccess ||
         cudaMemcpyAsync(y_host, ys, xbytes, cudaMemcpyDeviceToHost, h->io_out) != cudaSuccess ||
-        cudaEventRecord(h->ev_out[s], h->io_out) != cudaSuccess)
+        cudaEventRecord(h->ev_out[s], h->io_out) != cudaSuccess) {
+        ++h->io_calls;   // the forward's event is recorded; a queued part of the copy runs on io_out in order
         return LMOE_ERR_CUDA;
+    }
     ++h->io_calls;
     return LMOE_OK;
 }
@@ -1257,8 +1296,20 @@ int lmoe_device_status(lmoe_handle *h, cudaStream_t stream, int clear, int *devi
             cudaStreamSynchronize(stream) != cudaSuccess)
             return LMOE_ERR_CUDA;
     }
-    *device_status = (v & kDevErrTimeout) ? LMOE_ERR_TIMEOUT : LMOE_OK;
+    // a debug build's failed index checks (every translation unit's word)
+    const bool cl = clear != 0;
+    const unsigned dbg = debug_word_gemm(cl) | debug_word_gemm_bwd(cl) | debug_word_route(cl) |
+                         debug_word_backward(cl) | debug_word_selftest(cl);
+    if (dbg == ~0u) return LMOE_ERR_CUDA;
+    *device_status = dbg ? LMOE_ERR_INDEX : (v & kDevErrTimeout) ? LMOE_ERR_TIMEOUT : LMOE_OK;
     return LMOE_OK;
+}
+
+int lmoe_debug_checks(void) { return kDebugChecks ? 1 : 0; }
+
+int lmoe_selftest_index(cudaStream_t stream) {
+    if (!kDebugChecks) return LMOE_ERR_INVALID_ARG;
+    return launch_index_check_selftest(stream) == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
 }
 
 int qb_histogram(const float *scores, int64_t T, int32_t E, int64_t ld, int32_t B, uint32_t *hist,

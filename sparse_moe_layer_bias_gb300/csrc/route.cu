@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(1024)
     }
 }
 
-__global__ void scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int k,
+__global__ void scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int k, int E,
                                const uint32_t *__restrict__ bitmap,
                                const uint32_t *__restrict__ word_prefix, int words,
                                const int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
@@ -167,9 +167,11 @@ __global__ void scatter_kernel(const int32_t *__restrict__ idx, int64_t T, int k
     if (a >= T * k) return;
     const int64_t t = a / k;
     const int e = idx[a];
+    if (!idx_ok(e, E)) return;
     const int64_t w = int64_t(e) * words + (t >> 5);
     const uint32_t below = bitmap[w] & ((1u << (t & 31)) - 1u);
     const int32_t p = offsets[e] + static_cast<int32_t>(word_prefix[w] + __popc(below));
+    if (!idx_ok(p, T * k)) return;
     perm[p] = static_cast<int32_t>(a);
     inv[a] = p;
     tokrow[p] = static_cast<int32_t>(t);
@@ -210,13 +212,15 @@ cudaError_t launch_offsets_tiles(const int32_t *counts, int E, int32_t *offsets,
                          tiles2, n_mtiles2, tiles3, n_mtiles3);
 }
 
-cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, const uint32_t *bitmap,
+cudaError_t launch_scatter(const int32_t *idx, int64_t T, int k, int E, const uint32_t *bitmap,
                            const uint32_t *word_prefix, int words, const int32_t *offsets,
                            int32_t *perm, int32_t *inv, int32_t *tokrow, cudaStream_t st) {
     const int64_t n = T * k;
     if (n == 0) return cudaSuccess;
     return launch_kernel(scatter_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, true, idx, T,
-                         k, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
+                         k, E, bitmap, word_prefix, words, offsets, perm, inv, tokrow);
 }
+
+LMOE_DEBUG_WORD_READER(debug_word_route)
 
 }  // namespace lmoe

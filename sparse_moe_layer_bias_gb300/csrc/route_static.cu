@@ -87,7 +87,7 @@ extern "C" int lmoe_route_static(const float *scores, int64_t T, int32_t E, int3
     if (lmoe::launch_topk(scores, bias, T, E, top_k, topk_idx, gates, bitmap, w, stream) != cudaSuccess ||
         lmoe::launch_expert_scan(bitmap, E, w, prefix, counts, stream) != cudaSuccess ||
         lmoe::launch_offsets_tiles(counts, E, offsets, tiles, nmt, tiles2, nmt + 1, nullptr, nullptr, stream) != cudaSuccess ||
-        lmoe::launch_scatter(topk_idx, T, top_k, bitmap, prefix, w, offsets, perm, inv, tokrow, stream) !=
+        lmoe::launch_scatter(topk_idx, T, top_k, E, bitmap, prefix, w, offsets, perm, inv, tokrow, stream) !=
             cudaSuccess)
         return LMOE_ERR_CUDA;
     return LMOE_OK;

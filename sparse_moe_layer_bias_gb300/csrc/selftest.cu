@@ -2,7 +2,8 @@
 // fault: one CTA waits, with the same bounded mbarrier wait the GEMM roles
 // use, on a barrier that nothing ever arrives on.  After the limit the wait
 // gives up, raises the CTA's abort flag and sets the timeout bit of the
-// handle's device status word; the kernel then returns normally.
+// handle's device status word; the kernel then returns normally.  A second
+// self-test fails one index check, which a debug build (-DLMOE_DEBUG) reports.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -25,11 +26,21 @@ __global__ void bounded_wait_kernel(unsigned *err, uint64_t limit_ns, int *gave_
     }
 }
 
+// One index check that fails (1 is not below 1); no memory is accessed.
+__global__ void index_check_kernel() { idx_ok(1, 1); }
+
 }  // namespace
+
+cudaError_t launch_index_check_selftest(cudaStream_t st) {
+    index_check_kernel<<<1, 1, 0, st>>>();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bounded_wait_selftest(unsigned *err, uint64_t limit_ns, int *gave_up, cudaStream_t st) {
     bounded_wait_kernel<<<1, 32, 0, st>>>(err, limit_ns, gave_up);
     return cudaGetLastError();
 }
+
+LMOE_DEBUG_WORD_READER(debug_word_selftest)
 
 }  // namespace lmoe

@@ -87,3 +87,20 @@ def test_backward_handle_rejects_variants_without_gpu():
         assert lib.lmoe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(out)) == expect
     cfg = binding.LmoeConfig(256, 128, 32, 4, 128, 2, 64, 4.0, 25.0, 1e-6, 64, 0, 0, 2)
     assert lib.lmoe_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(out)) == 1
+
+
+def test_debug_and_release_builds_without_gpu():
+    """The release library compiles the index checks away; the debug build
+    (-DLMOE_DEBUG) exports the same entry points and reports its checks.  The
+    index self-test returns LMOE_ERR_INVALID_ARG in a release build before any
+    CUDA call."""
+    from sparse_moe_layer_bias_gb300 import build
+    rel = ctypes.CDLL(build.build())
+    dbg = ctypes.CDLL(build.build(debug=True))
+    for lib, flag in ((rel, 0), (dbg, 1)):
+        lib.lmoe_debug_checks.restype = ctypes.c_int
+        assert lib.lmoe_debug_checks() == flag
+        for n in declared_functions():
+            assert hasattr(lib, n), n
+    rel.lmoe_selftest_index.argtypes = [ctypes.c_void_p]
+    assert rel.lmoe_selftest_index(None) == 1

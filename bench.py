@@ -43,8 +43,9 @@ from sparse_moe_layer_bias_gb300 import synth  # noqa: E402
 METRIC = "LatentMoE layer tokens/s & %bf16 TC peak (K3 shape); QB histogram HBM GB/s"
 QB_B = 1000
 # DRAM read+write / algorithmic bytes, measured with ncu on `--profile-case`
-# for the kernels that can be the step's dominant one (profiles/ has the runs)
-TRAFFIC_RATIO = {"expert_w3": 0.985, "expert_w12_light": 1.021, "expert_w12_heavy": 1.063}
+# for the kernels that can be the step's dominant one; a kernel changed since
+# its counters were taken has no entry (its traffic is reported as null)
+TRAFFIC_RATIO = {"expert_w12_light": 1.021, "expert_w12_heavy": 1.063}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -89,15 +90,18 @@ def layer_work(shape, T, counts, fp8=False):
         w[name] = (4.0 * nr * L * I, byts)
     if fp8:   # the latent's quantisation runs at the start of the light stage
         w["expert_w12_light"] = (w["expert_w12_light"][0], w["expert_w12_light"][1] + 2.0 * T * L + T * (L + 1))
-    w["expert_w3"] = (2.0 * n * I * L, touched * L * (I * wb + (1 if fp8 else 0)) + n * I * wb + 2.0 * n * L)
-    w["combine"] = (0.0, 2.0 * (n * L + T * L))
+    # W3: the method's bytes, i.e. the touched experts' weights and the
+    # activation rows in.  The gate-weighted rows o that this design stores
+    # for the combine (2 n L bytes) are an intermediate of the design, not of
+    # the method: they show in the launch's measured "traffic", not here.
+    w["expert_w3"] = (2.0 * n * I * L, touched * L * (I * wb + (1 if fp8 else 0)) + n * I * wb)
+    w["combine"] = (0.0, 2.0 * (n * L + T * L))           # o rows in, r out
     w["up"] = (2.0 * T * (L + S) * d, 2.0 * (T * (L + S) + d * (L + S) + T * d))
     return w
 
 
 # DRAM read+write over algorithmic bytes of the backward's per-expert weight-
 # gradient GEMMs, from ncu on --profile-case --backward
-# (profiles/backward_expert_wgrad_gemm_ncu_small.md)
 BWD_TRAFFIC_RATIO = {"wgrad_w3": 0.901, "wgrad_w12": 0.944}
 
 

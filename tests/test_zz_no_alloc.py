@@ -58,7 +58,7 @@ def test_route_static_matches_forward_routing_twice(lm):
 
 
 def test_route_static_rejects_oversized_problems(lm):
-    T, E = 1 << 17, 1024            # scratch needed ~ 16*E*T/32 + 20*T*16 >> 8 MiB
+    T, E = 1 << 17, 1024            # bitmaps and prefixes alone: 8 * E * T / 32 bytes = 32 MiB > 8 MiB
     scores = torch.zeros((T, E), dtype=torch.float32, device="cuda")
     bias = torch.zeros(E, dtype=torch.float32, device="cuda")
     with pytest.raises(lm.LmoeError) as e:

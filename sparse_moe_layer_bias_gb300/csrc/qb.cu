@@ -14,9 +14,9 @@
 // global histogram at the end.  The global adds are the on-chip analogue of
 // the cross-node all-reduce.  For large B (where 32-bit counters would leave
 // fewer than 32 experts per CTA) the counters are 16-bit, two bins per 32-bit
-// word, with token chunks of at most 65535 rows so that no counter can carry
-// into its neighbour: twice the experts per CTA, so each row segment a CTA
-// reads is a whole 32-byte sector or more.
+// word, spilled to the global histogram before they could carry into their
+// neighbour: twice the experts per CTA, so each row segment a CTA reads is a
+// whole 32-byte sector or more.
 #include "kernels.h"
 
 namespace lmoe {
@@ -33,9 +33,20 @@ __device__ __forceinline__ int bin_of(float s, float fB, int B) {
 }
 
 // Vector path: E % 4 == 0, ld % 4 == 0, 16-byte aligned rows; EPC in {4..32}.
-// PACK16: counters of bins 2w and 2w+1 share word w (low / high 16 bits);
-// requires rows_per_chunk <= 65535.
-template <int EPC, bool PACK16>
+// PACK16: counters of bins 2w and 2w+1 share word w (low / high 16 bits).  A
+// 16-bit counter must never reach 65536 (it would carry into its neighbour),
+// so the rows are counted in spans of kSpan16 = 32768: after each span every
+// counter that has reached 32768 is added to the global histogram and
+// cleared; any other counter can take at most 32768 more counts before the
+// next check.  The global adds are so far fewer than a flush per 65535 rows
+// (a counter of a 10000-bin histogram rarely gets near 32768).
+constexpr int64_t kSpan16 = 32768;
+
+// U: row sweeps whose loads are in flight per thread.  (With 16-bit counters
+// for 10000 bins one CTA fills an SM's shared memory; 8 or 16 sweeps in flight
+// measured slower than 4 there: that kernel is bound by its shared-memory
+// atomics, not by loads in flight.)
+template <int EPC, bool PACK16, int U>
 __global__ void __launch_bounds__(kHistThreads)
     qb_hist_vec_kernel(const float *__restrict__ s, int64_t T, int E, int64_t ld, int B,
                        uint32_t *__restrict__ hist, int n_groups, int64_t rows_per_chunk) {
@@ -43,7 +54,6 @@ __global__ void __launch_bounds__(kHistThreads)
     const int WB = PACK16 ? (B + 1) / 2 : B;   // counter words per expert
     constexpr int NQ = EPC / 4;                 // float4 per row segment
     constexpr int ROWS = kHistThreads / NQ;     // rows per sweep
-    constexpr int U = 4;                        // sweeps in flight
     const int g = blockIdx.x % n_groups;
     const int64_t chunk = blockIdx.x / n_groups;
     const int e0 = g * EPC;
@@ -61,40 +71,61 @@ __global__ void __launch_bounds__(kHistThreads)
         else
             atomicAdd(&cnt[c * WB + b], 1u);
     };
+    uint32_t *dst = hist + int64_t(e0) * B;
+    // 16-bit counters: add the halves at or above `min_count` to the global
+    // histogram and clear them (the caller synchronised the block before)
+    auto spill16 = [&](uint32_t min_count) {
+        for (int i = threadIdx.x; i < ne * WB; i += kHistThreads) {
+            const uint32_t c = cnt[i];
+            if (!c) continue;
+            const uint32_t lo = c & 0xffffu, hi = c >> 16;
+            const bool tlo = lo && lo >= min_count, thi = hi && hi >= min_count;
+            if (!(tlo || thi)) continue;
+            const int e = i / WB, b = 2 * (i % WB);
+            if (tlo) atomicAdd(&dst[int64_t(e) * B + b], lo);
+            if (thi) atomicAdd(&dst[int64_t(e) * B + b + 1], hi);   // b + 1 < B when non-zero
+            cnt[i] = (tlo ? 0u : lo) | (thi ? 0u : (hi << 16));
+        }
+    };
     const int q = threadIdx.x % NQ;
     const int rl = threadIdx.x / NQ;
     const bool qv = 4 * q < ne;
     const float *col = s + e0 + 4 * q;
-    for (int64_t r0 = r_begin; r0 < r_end; r0 += int64_t(ROWS) * U) {
-        float4 v[U];
+    const int64_t span = PACK16 ? kSpan16 : (r_end - r_begin);
+    for (int64_t s0 = r_begin; s0 < r_end; s0 += span) {
+        const int64_t s1 = min(r_end, s0 + span);
+        for (int64_t r0 = s0; r0 < s1; r0 += int64_t(ROWS) * U) {
+            float4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t row = r0 + int64_t(u) * ROWS + rl;
-            v[u] = (qv && row < r_end) ? __ldcs(reinterpret_cast<const float4 *>(col + row * ld))
-                                       : make_float4(-1.f, -1.f, -1.f, -1.f);
+            for (int u = 0; u < U; ++u) {
+                const int64_t row = r0 + int64_t(u) * ROWS + rl;
+                v[u] = (qv && row < s1) ? __ldcs(reinterpret_cast<const float4 *>(col + row * ld))
+                                        : make_float4(-1.f, -1.f, -1.f, -1.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t row = r0 + int64_t(u) * ROWS + rl;
+                if (!(qv && row < s1)) continue;
+                const int c = 4 * q;
+                count(c + 0, v[u].x);
+                count(c + 1, v[u].y);
+                count(c + 2, v[u].z);
+                count(c + 3, v[u].w);
+            }
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t row = r0 + int64_t(u) * ROWS + rl;
-            if (!(qv && row < r_end)) continue;
-            const int c = 4 * q;
-            count(c + 0, v[u].x);
-            count(c + 1, v[u].y);
-            count(c + 2, v[u].z);
-            count(c + 3, v[u].w);
+        if (PACK16 && s1 < r_end) {   // more rows follow: spill the counters that could overflow
+            __syncthreads();
+            spill16(static_cast<uint32_t>(kSpan16));
+            __syncthreads();
         }
     }
     __syncthreads();
-    uint32_t *dst = hist + int64_t(e0) * B;
-    for (int i = threadIdx.x; i < ne * WB; i += kHistThreads) {
-        const uint32_t c = cnt[i];
-        if (!c) continue;
-        if (PACK16) {
-            const int e = i / WB, b = 2 * (i % WB);
-            if (c & 0xffffu) atomicAdd(&dst[int64_t(e) * B + b], c & 0xffffu);
-            if (c >> 16) atomicAdd(&dst[int64_t(e) * B + b + 1], c >> 16);   // b + 1 < B when non-zero
-        } else {
-            atomicAdd(&dst[i], c);
+    if (PACK16) {
+        spill16(1u);
+    } else {
+        for (int i = threadIdx.x; i < ne * WB; i += kHistThreads) {
+            const uint32_t c = cnt[i];
+            if (c) atomicAdd(&dst[i], c);
         }
     }
 }
@@ -204,13 +235,15 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
         qb_hist_global_kernel<<<num_sms * 4, 512, 0, st>>>(scores, T, E, ld, B, hist);
         return cudaGetLastError();
     }
-    int epc = 32;
+    // at most 16 experts per CTA: a 64-byte piece of each row already streams
+    // well, and the smaller counter block leaves room for two CTAs per SM
+    int epc = 16;
     while (epc > 1 && size_t(epc) * per_expert > kHistSmemBudget) epc >>= 1;
     const bool vec = epc >= 4 && (E % 4 == 0) && (ld % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
     // 16-bit counters where they let a CTA hold more experts (vector path)
     const size_t per_expert16 = size_t((B + 1) / 2) * sizeof(uint32_t);
-    int epc16 = 32;
+    int epc16 = 16;
     while (epc16 > 1 && size_t(epc16) * per_expert16 > kHistSmemBudget) epc16 >>= 1;
     const bool pack16 = vec && epc16 > epc;
     if (pack16) epc = epc16;
@@ -223,8 +256,7 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     const int slots = num_sms * ctas_per_sm;
     const int64_t min_rows = 512;
     const int64_t max_chunks = (T + min_rows - 1) / min_rows;
-    // 16-bit counters: no chunk longer than 65535 rows
-    const int min_chunks = pack16 ? static_cast<int>((T + 65534) / 65535) : 1;
+    const int min_chunks = 1;
     int n_chunks = min_chunks;
     for (int c = max(min_chunks, slots / n_groups); c <= max(16, min_chunks) && c <= max(max_chunks, int64_t(min_chunks));
          ++c) {
@@ -236,28 +268,26 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     const int64_t rows_per_chunk = (T + n_chunks - 1) / n_chunks;
     const unsigned grid = static_cast<unsigned>(n_groups) * static_cast<unsigned>(n_chunks);
 
-#define LMOE_QB_VEC(N_, P_)                                                                         \
+#define LMOE_QB_VEC(N_, P_, U_)                                                                     \
     case N_:                                                                                        \
-        err = cudaFuncSetAttribute(qb_hist_vec_kernel<N_, P_>,                                      \
+        err = cudaFuncSetAttribute(qb_hist_vec_kernel<N_, P_, U_>,                                  \
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
         if (err != cudaSuccess) return err;                                                         \
-        qb_hist_vec_kernel<N_, P_><<<grid, kHistThreads, smem, st>>>(scores, T, E, ld, B, hist,      \
-                                                                     n_groups, rows_per_chunk);     \
+        qb_hist_vec_kernel<N_, P_, U_><<<grid, kHistThreads, smem, st>>>(scores, T, E, ld, B, hist,  \
+                                                                         n_groups, rows_per_chunk); \
         break;
     if (vec && pack16) {
         switch (epc) {
-            LMOE_QB_VEC(8, true)
-            LMOE_QB_VEC(16, true)
-            LMOE_QB_VEC(32, true)
+            LMOE_QB_VEC(8, true, 4)
+            LMOE_QB_VEC(16, true, 4)
             default:
                 return cudaErrorInvalidValue;
         }
     } else if (vec) {
         switch (epc) {
-            LMOE_QB_VEC(4, false)
-            LMOE_QB_VEC(8, false)
-            LMOE_QB_VEC(16, false)
-            LMOE_QB_VEC(32, false)
+            LMOE_QB_VEC(4, false, 4)
+            LMOE_QB_VEC(8, false, 4)
+            LMOE_QB_VEC(16, false, 4)
             default:
                 return cudaErrorInvalidValue;
         }

@@ -286,6 +286,20 @@ MAX_ROUTING = synth.LayerShape("max_routing", T=150, d=256, latent=128, n_expert
                                n_shared=2, shared_inter=64, seed=1011)
 
 
+# A router as wide as K3's (E = 896 = 4 x 224) at a batch large enough for the
+# router's 256-row pair tiles (T = 8200: 33 pair rows, the last one with 8
+# rows), on small widths.
+WIDE_ROUTER = synth.LayerShape("wide_router", T=8200, d=256, latent=128, n_experts=896, top_k=16, inter=64,
+                               n_shared=2, shared_inter=64, seed=1012)
+
+
+def test_wide_router_layer_stages_and_end_to_end(lm):
+    run = run_host_shape(lm, WIDE_ROUTER)
+    staged_checks(WIDE_ROUTER, run)
+    rf, mx, kept, _ = end_to_end(WIDE_ROUTER, run)
+    assert kept >= 0.5 * WIDE_ROUTER.T
+
+
 def test_max_routing_layer_stages_and_end_to_end(lm):
     run = run_host_shape(lm, MAX_ROUTING)
     staged_checks(MAX_ROUTING, run)

@@ -17,6 +17,8 @@
 // word, spilled to the global histogram before they could carry into their
 // neighbour: twice the experts per CTA, so each row segment a CTA reads is a
 // whole 32-byte sector or more.
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace lmoe {
@@ -256,14 +258,18 @@ cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t l
     const int slots = num_sms * ctas_per_sm;
     const int64_t min_rows = 512;
     const int64_t max_chunks = (T + min_rows - 1) / min_rows;
-    const int min_chunks = 1;
-    int n_chunks = min_chunks;
-    for (int c = max(min_chunks, slots / n_groups); c <= max(16, min_chunks) && c <= max(max_chunks, int64_t(min_chunks));
-         ++c) {
-        n_chunks = c;
+    // at least one wave's worth of CTAs (few expert groups: more chunks), no
+    // chunk shorter than min_rows; then up to 16 more chunks if that fills
+    // the last wave to 90%
+    const int first = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(slots / n_groups, max_chunks)));
+    int n_chunks = first;
+    for (int c = first; c <= first + 16 && c <= max_chunks; ++c) {
         const int ctas = n_groups * c;
         const int waves = (ctas + slots - 1) / slots;
-        if (ctas * 10 >= waves * slots * 9) break;
+        if (ctas * 10 >= waves * slots * 9) {
+            n_chunks = c;
+            break;
+        }
     }
     const int64_t rows_per_chunk = (T + n_chunks - 1) / n_chunks;
     const unsigned grid = static_cast<unsigned>(n_groups) * static_cast<unsigned>(n_chunks);

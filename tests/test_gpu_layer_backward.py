@@ -125,6 +125,42 @@ def test_backward_max_routing(lm):
     check_backward(MAX_ROUTING, run_backward(lm, MAX_ROUTING))
 
 
+def test_backward_single_expert(lm):
+    """E = k = 1: every token's only expert.  Here the norm cancels the gate:
+    z = g o, so r = z / sqrt(mean(z^2) + eps) depends on g only through eps,
+    and the gate's (hence the router's) true gradient is o . dz with dz =
+    dr inv - z (dr . z) inv / (L (ms + eps)), two terms that cancel to a
+    relative eps / (ms + eps).  The GPU stores dz in bf16, so its router
+    gradient is that cancellation's rounding: each token's dlogit may be off
+    by 2^-8 |sigma'(x)| |o| |dz| <= 2^-8 |sigma'(x)| |o| 2 |dr| inv.  Every
+    other gradient is compared as in the other layers; the router's against
+    that bound (element by element, summed over the tokens)."""
+    from test_gpu_layer import SINGLE_EXPERT as shape
+    run = run_backward(lm, shape)
+    cfg = oracle_cfg(shape)
+    wb = {k: synth.bits(v) for k, v in run["w_host"].items()}
+    ref = oracle.layer_backward(cfg, synth.bits(run["x_host"]), wb, run["idx"], synth.bits(run["dy_host"]))
+    compare("x", dec(host_bits(run["dx"])), ref["x"])
+    for name in oracle.BACKWARD_GRADS:
+        if name != "w_router":
+            compare(name, run["grads"][name].cpu().double().numpy(), ref[name])
+    T, L = run["x_host"].shape[0], shape.latent
+    lay = lm.lmoe_workspace_layout(run["h"], T)
+    h = dec(host_bits(ws_view(run["ws"], lay, "h", torch.bfloat16, (T, L))))
+    o = dec(host_bits(ws_view(run["ws"], lay, "o", torch.bfloat16, (T, L))))        # k = 1: one row per token
+    logit = h @ dec(wb["w_router"]).T                                                   # [T, 1]
+    dsig = 1.0 / (1.0 + np.exp(-logit)) / (1.0 + np.exp(logit))
+    dr = dec(synth.bits(run["dy_host"])) @ dec(wb["w_up"])                             # W_up^T dy per token
+    z = o                                                                              # z = the one gated row
+    inv = 1.0 / np.sqrt(np.mean(z ** 2, axis=1, keepdims=True) + shape.rms_eps)
+    per_tok = 2.0 ** -8 * np.abs(dsig) * np.linalg.norm(o, axis=1, keepdims=True) * 2.0 * \
+        np.linalg.norm(dr, axis=1, keepdims=True) * inv
+    bound = (per_tok * np.abs(h)).sum(axis=0, keepdims=True) + 1e-30
+    gw = run["grads"]["w_router"].cpu().double().numpy()
+    assert np.all(np.isfinite(gw))
+    assert np.all(np.abs(gw - ref["w_router"]) <= bound), np.max(np.abs(gw - ref["w_router"]) / bound)
+
+
 def test_backward_is_deterministic(lm):
     shape = synth.TINY
     run = run_backward(lm, shape)

@@ -27,7 +27,8 @@ def hist_np(h: torch.Tensor) -> np.ndarray:
                                    (1000, 40, 37), (1, 896, 1000),
                                    (3000, 24, 60000),    # bins beyond shared memory: global counters
                                    (200000, 64, 10000),  # 16-bit counters, several token chunks
-                                   (70001, 32, 9999)])   # 16-bit counters, odd B (last word half used)
+                                   (70001, 32, 9999),    # 16-bit counters, odd B (last word half used)
+                                   (5000, 1, 1000)])     # a single expert (scalar path)
 def test_histogram_bit_exact(lm, T, E, B):
     s = synth.qb_scores(T, E, seed=T + E + B)
     s[0, 0] = 1.0
@@ -41,8 +42,8 @@ def test_histogram_bit_exact(lm, T, E, B):
 
 def test_histogram_16bit_counters_do_not_carry(lm):
     """Large B packs two 16-bit counters per word; one bin receiving every
-    token (T > 65535) must not carry into its neighbour: token chunks are
-    capped at 65535 rows."""
+    token (T > 65535) must not carry into its neighbour: a counter that has
+    reached 32768 after a span of 32768 rows goes to the global histogram."""
     T, E, B = 140000, 32, 10000
     s = synth.qb_scores(T, E, seed=5)
     s[:, 0] = 0.5          # bin 5000: an even bin, the low half of its word

@@ -37,10 +37,24 @@
 //               the stage with cp.async.
 // All threads pass griddepcontrol.wait after the prologue (barrier init, TMEM
 // allocation), so the kernel can be a programmatic dependent launch.
+//
+// CTA pairs (CG2, dense GEMMs fed by TMA; gemm_pair.cu): a cluster of two CTAs
+// on two SMs computes a 256 x BN tile.  Each CTA's producer loads its own 128
+// rows of A and half of the B rows; both CTAs' copies complete on CTA 0's
+// stage barrier.  CTA 0's MMA thread issues tcgen05.mma.cta_group::2 (M = 256),
+// which reads the operands from both CTAs' shared memory and leaves each
+// CTA's 128 accumulator rows in that CTA's TMEM (allocated for the pair with
+// cta_group::2), and its commits arrive on the barriers of both CTAs
+// (multicast).  Each CTA's epilogue handles its own rows and releases the
+// accumulator on CTA 0's barrier (one arrival per warp).  Before leaving, each
+// CTA waits until every release aimed at it has arrived, and the pair meets at
+// a cluster barrier before freeing TMEM.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+
+#include <atomic>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -53,11 +67,14 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;  // two accumulators of up to 256 fp32 columns
 constexpr int kAccStride = 256;
 
-template <int BN, bool PAIR, bool KSEG = false>
+// CG2: the tile is 256 x BN on a CTA pair; each CTA holds 128 rows of A and
+// BN / 2 rows of B per stage.
+template <int BN, bool PAIR, bool KSEG = false, bool CG2 = false>
 struct Cfg {
     static constexpr int kSub = PAIR ? 2 : 1;           // 128-row sub-tiles per tile
     static constexpr int kABytes = kSub * kBM * kBK * 2; // 16 or 32 KB
-    static constexpr int kBBytes = BN * kBK * 2;        // 16 or 32 KB
+    static constexpr int kBRows = CG2 ? BN / 2 : BN;    // B rows per CTA and stage
+    static constexpr int kBBytes = kBRows * kBK * 2;    // 14 to 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStages = (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
     static constexpr int kBarBytes = 256;
@@ -89,8 +106,10 @@ struct Tile {
     int k0, nk;  // first K block and number of K blocks
 };
 
-template <bool GROUPED, bool KSEG = false>
-__device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
+// CG2 (dense only): M tiles are 256 rows; CTA `rank` of the pair owns rows
+// 128 * rank .. of the tile (nrows may then be <= 0: no valid rows).
+template <bool GROUPED, bool KSEG = false, bool CG2 = false>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m, uint32_t rank = 0) {
     Tile ti;
     ti.k0 = 0;
     ti.nk = a.k_blocks;
@@ -136,7 +155,7 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m) {
         const int gm = min(G, a.m_tiles - m_first);
         ti.nt = r / gm;
         const int mt = m_first + r % gm;
-        ti.row0 = mt * kBM;
+        ti.row0 = CG2 ? mt * (2 * kBM) + static_cast<int>(rank) * kBM : mt * kBM;
         ti.nrows = min(kBM, a.m_rows - ti.row0);
         ti.expert = 0;
     }
@@ -200,12 +219,12 @@ __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], i
 // A_GATHER adds four warps (6..9) that gather A rows with cp.async.
 __host__ __device__ constexpr int threads_for(int am) { return am == A_GATHER ? kThreads + 128 : kThreads; }
 
-template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR, bool KSEG = false>
+template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR, bool KSEG = false, bool CG2 = false>
 __global__ void __launch_bounds__(threads_for(AM), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const GemmArgs args) {
-    using C = Cfg<BN, PAIR, KSEG>;
+    using C = Cfg<BN, PAIR, KSEG, CG2>;
     constexpr int S = C::kStages;
     constexpr int H = BN / 2;  // GLU: features per tile
     constexpr int NSUB = C::kSub;
@@ -213,6 +232,9 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     static_assert(!PAIR || (AM == A_GATHER && GROUPED), "pair tiles are built for the gathered expert GEMM");
     static_assert(!KSEG || (GROUPED && AM == A_DENSE && BMD == B_PLAIN && EPI == EPI_F32),
                   "K segments are built for the experts' weight gradients");
+    static_assert(!CG2 || (!GROUPED && !PAIR && !KSEG && AM != A_GATHER && EPI != EPI_SITU_GLU_F8 &&
+                           EPI != EPI_SCATTER_F8 && BN % 32 == 0),
+                  "CTA pairs are built for the dense bf16 GEMMs fed by TMA");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -230,6 +252,11 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pairs: this CTA's rank in the pair, and the pair's place in the
+    // persistent tile loop (both CTAs walk the same tiles)
+    const uint32_t rank = CG2 ? cluster_ctarank() : 0u;
+    const int t_first = CG2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int t_step = CG2 ? static_cast<int>(n_clusters_x()) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -239,18 +266,29 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), 128);
+            // pairs: one arrival per epilogue warp of both CTAs (on CTA 0's barrier)
+            mbar_init(smem_u32(&tempty[b]), CG2 ? 8 : 128);
         }
         mbar_init(smem_u32(&drain[0]), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        if (CG2) {
+            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    // pairs: the other CTA's barriers must be initialised before anything
+    // arrives on them or signals them
+    if (CG2)
+        cluster_sync_all();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -266,8 +304,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = tile_at<GROUPED, KSEG>(args, t, n_m);
+        for (int t = t_first; t < total && ok; t += t_step) {
+            const Tile ti = tile_at<GROUPED, KSEG, CG2>(args, t, n_m, rank);
             constexpr uint32_t a_bytes = (AM == A_GATHER) ? 0u : C::kABytes;
             constexpr int TRB = (BMD == B_GLU) ? H : BN;     // rows per B box
             const int brow = args.b_packed ? (ti.expert * args.b_row_tiles + ti.nt) * args.k_blocks * TRB
@@ -275,12 +313,14 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             for (int kb = 0; kb < ti.nk; ++kb) {
                 // every lane waits; the warp proceeds only if all lanes saw the slot free
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
-                                                       args.err, lim))) {
+                                                       args.err, lim, true, CG2))) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_u32(&full[stage]);
-                if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + C::kBBytes);
+                // pairs: both CTAs' copies complete on CTA 0's barrier, which
+                // CTA 0 arms with the bytes of both
+                const uint32_t fb = CG2 ? mapa_shared(smem_u32(&full[stage]), 0) : smem_u32(&full[stage]);
+                if (lane == 0 && rank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), (CG2 ? 2u : 1u) * (a_bytes + C::kBBytes));
                 __syncwarp();
                 const uint32_t sa = smem_u32(smA + stage * C::kABytes);
                 const uint32_t sb = smem_u32(smB + stage * C::kBBytes);
@@ -293,7 +333,16 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 const int by = KSEG ? kabs * args.kseg_b_rows + ti.nt * TRB : args.b_packed ? brow + kabs * TRB : brow;
                 const int ax = KSEG ? 0 : kx;
                 const int ay = KSEG ? kabs * args.kseg_a_rows + ti.row0 : ti.row0;
-                if (lane == 0) {
+                if (CG2 && lane == 0) {
+                    // this CTA's 128 rows of A and its half of the B tile (GLU:
+                    // CTA 0 the W1 rows, CTA 1 the W2 rows of the tile's features)
+                    tma_load_2d_pair(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, ax, ay, fb);
+                    if (BMD == B_GLU)
+                        tma_load_2d_pair(sb, rank ? &tmB1 : &tmB0, bx, by, fb);
+                    else
+                        tma_load_2d_pair(sb, (BMD == B_SPLIT && second) ? &tmB1 : &tmB0, bx,
+                                         by + static_cast<int>(rank) * C::kBRows, fb);
+                } else if (lane == 0) {
                     if (AM != A_GATHER)
                         tma_load_2d(sa, (AM == A_SPLIT && second) ? &tmA1 : &tmA0, ax, ay, fb);
                     if (BMD == B_GLU) {
@@ -312,11 +361,23 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             }
         }
         // Never leave while a copy into this CTA's shared memory is in flight.
-        if (lane == 0) {
+        // (Pairs: CTA 0's barriers count both CTAs' copies.)
+        if (lane == 0 && rank == 0) {
             for (int s = 0; s < S; ++s)
                 if (issued_mask & (1u << s))
                     mbar_wait(smem_u32(&full[s]), (issued_parity >> s) & 1u, abort_flag, args.err,
                               lim, /*watch_abort=*/false);
+        }
+        // Pairs: every stage's last release, which the MMA thread of CTA 0
+        // signals into both CTAs, must have arrived before this CTA may exit.
+        if (CG2 && lane == 0) {
+            for (int i = 0; i < S; ++i) {
+                mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, args.err, lim, true, true);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
     } else if (AM == A_GATHER && warp >= 6) {
         // ------------------------------------------------------------ A gather
@@ -333,8 +394,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         const uint32_t sw = static_cast<uint32_t>((c ^ (rb & 7)) * 16);  // (rb + 16 j) & 7 == rb & 7
         bool ok = true;
         int g = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = tile_at<GROUPED, KSEG>(args, t, n_m);
+        for (int t = t_first; t < total && ok; t += t_step) {
+            const Tile ti = tile_at<GROUPED, KSEG, CG2>(args, t, n_m, rank);
             const uint16_t *src[8 * NSUB];
 #pragma unroll
             for (int j = 0; j < 8 * NSUB; ++j) {
@@ -365,16 +426,17 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         cp_async_wait<0>();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // pairs: only CTA 0 issues; the accumulator rows of CTA 1 land in its own TMEM
+        if (lane == 0 && rank == 0) {
             constexpr bool F8 = (EPI == EPI_SITU_GLU_F8 || EPI == EPI_SCATTER_F8);
-            constexpr uint32_t idesc = F8 ? idesc_e4m3_m128(BN) : idesc_bf16_m128(BN);
+            constexpr uint32_t idesc = F8 ? idesc_e4m3_m128(BN) : idesc_bf16(CG2 ? 2 * kBM : kBM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err, lim)) break;
+            for (int t = t_first; t < total && ok; t += t_step) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err, lim, true, CG2)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccStride);
                 // a pair tile whose second sub-tile is empty skips its MMAs
@@ -399,26 +461,48 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                                 const uint64_t adesc = sdesc_sw128(sa + sub * (kBM * kBK * 2) + k * 32);
                                 if (F8)
                                     tc_mma_e4m3(d + sub * kAccStride, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                                else if (CG2)
+                                    tc_mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
                                 else
                                     tc_mma_bf16(d + sub * kAccStride, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
                             }
                     }
-                    tc_commit(smem_u32(&empty[stage]));
+                    if (CG2)
+                        tc_commit_pair_mc(smem_u32(&empty[stage]), 0x3);   // both CTAs' producers
+                    else
+                        tc_commit(smem_u32(&empty[stage]));
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&tfull[acc]));
+                if (CG2)
+                    tc_commit_pair_mc(smem_u32(&tfull[acc]), 0x3);   // both CTAs' epilogues
+                else
+                    tc_commit(smem_u32(&tfull[acc]));
                 if (++acc == NACC) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             // All MMAs this thread issued must finish before TMEM is freed.
-            tc_commit(smem_u32(&drain[0]));
+            if (CG2)
+                tc_commit_pair_mc(smem_u32(&drain[0]), 0x1);
+            else
+                tc_commit(smem_u32(&drain[0]));
             mbar_wait(smem_u32(&drain[0]), 0, abort_flag, args.err, lim, /*watch_abort=*/false);
+            // Pairs: every accumulator's last release (four of the arrivals
+            // come from the other CTA) must have arrived before this CTA exits.
+            if (CG2) {
+                for (int b = 0; b < NACC; ++b) {
+                    mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, args.err, lim, true, true);
+                    if (++acc == NACC) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
+                }
+            }
         }
         __syncwarp();
     } else if (warp < 6) {
@@ -431,8 +515,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t n_tma_stores = 0;   // K segments without split stores: TMA stores issued by this warp
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = tile_at<GROUPED, KSEG>(args, t, n_m);
+        for (int t = t_first; t < total; t += t_step) {
+            const Tile ti = tile_at<GROUPED, KSEG, CG2>(args, t, n_m, rank);
             // Per-row metadata of this thread's rows (destination row, gate,
             // token exponent), fetched before waiting for the accumulator so
             // their latency hides behind the MMAs.
@@ -477,7 +561,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             }
             // the whole warp must agree before the warp-collective tcgen05.ld
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err, lim)))
+                            mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, args.err, lim, true, CG2)))
                 break;
             tc_fence_after();
 #pragma unroll 1
@@ -767,7 +851,13 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             }
             }  // sub-tiles
             tc_fence_before();
-            mbar_arrive(smem_u32(&tempty[acc]));
+            if (CG2) {
+                // one arrival per warp, on CTA 0's barrier
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+            } else {
+                mbar_arrive(smem_u32(&tempty[acc]));
+            }
             if (++acc == NACC) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -781,9 +871,19 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    // pairs: neither CTA frees its TMEM or leaves (its shared memory still
+    // receiving the other's arrivals) before both are done
+    if (CG2)
+        cluster_sync_all();
+    else
+        __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) {
+        if (CG2)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
+    }
 }
 
 template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR = false, bool KSEG = false>
@@ -793,6 +893,45 @@ cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(grid), dim3(threads_for(AM)), smem, st, dependent, m.a0, m.a1, m.b0, m.b1, a);
+}
+
+// CTA pairs: clusters of two CTAs, as many pairs as fit on the GPU at once
+// (at most `tiles`); the count is asked of the runtime once per device.
+template <int BN, int AM, int BMD, int EPI>
+cudaError_t launch_pair(const GemmMaps &m, const GemmArgs &a, int64_t tiles, cudaStream_t st, bool dependent) {
+    auto kern = gemm_kernel<BN, AM, BMD, EPI, false, false, false, true>;
+    const size_t smem = Cfg<BN, false, false, true>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(threads_for(AM));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> pairs_on[kMaxDev];
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    int pairs = pairs_on[dev].load(std::memory_order_relaxed);
+    if (pairs <= 0) {
+        if ((e = cudaOccupancyMaxActiveClusters(&pairs, kern, &cfg)) != cudaSuccess) return e;
+        if (pairs <= 0) return cudaErrorInvalidConfiguration;
+        pairs_on[dev].store(pairs, std::memory_order_relaxed);
+    }
+    if (tiles <= 0) return cudaSuccess;
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(tiles < pairs ? tiles : pairs));
+    cfg.numAttrs = dependent ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.b0, m.b1, a);
 }
 
 }  // namespace

@@ -75,6 +75,7 @@ __device__ __forceinline__ bool idx_ok(int64_t i, int64_t n) {
 // The debug word of each translation unit that checks indices (0 in a release
 // build); `clear` resets it.  Synchronous.
 unsigned debug_word_gemm(bool clear);
+unsigned debug_word_pair(bool clear);
 unsigned debug_word_gemm_bwd(bool clear);
 unsigned debug_word_route(bool clear);
 unsigned debug_word_backward(bool clear);
@@ -182,6 +183,16 @@ struct GemmArgs {
 cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const GemmMaps &maps,
                         const GemmArgs &args, int grid, cudaStream_t stream, bool pair = false,
                         bool dependent = true);
+
+// Dense GEMMs (A by TMA, not grouped) on CTA pairs (gemm_pair.cu): a
+// 256 x bn tile per cluster of two CTAs, `args.m_tiles` = ceil(m_rows / 256)
+// and `tiles` = m_tiles x n_tiles; the B maps' boxes are bn / 2 rows (each CTA
+// loads its half of the tile's B rows).  The grid is chosen here (two CTAs
+// per tile, at most as many pairs as fit on the GPU at once).  Compiled for
+// bn = 256 with A_DENSE/B_PLAIN/EPI_BF16 (down-projection) and
+// A_SPLIT/B_SPLIT/EPI_BF16 (up-projection); cudaErrorInvalidValue otherwise.
+cudaError_t launch_gemm_pair(int bn, AMode am, BMode bm, Epi epi, const GemmMaps &maps, const GemmArgs &args,
+                             int64_t tiles, cudaStream_t stream, bool dependent = true);
 
 // Backward-pass GEMMs (gemm_bwd.cu); same operand conventions.  With `kseg`
 // (grouped, A and B dense): `tiles` holds {expert, first K block, K blocks,

@@ -24,6 +24,8 @@ struct lmoe_handle {
     unsigned *d_status;  // device status word (bounded-wait timeouts)
     // Weight-side TMA descriptors, built once.
     int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up, bn_router;
+    // dense GEMMs on CTA pairs (256-row tiles over two SMs; B boxes of bn / 2 rows)
+    bool pair_down, pair_shared, pair_router, pair_up;
     CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
     // routed experts' weights repacked tile-contiguously (handle-owned): bf16,
     // or e4m3 codes (expert_fp8) with one int8 scale exponent per weight row
@@ -431,6 +433,14 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
     // router: 224-wide N tiles when they cover E exactly (K3: 896 = 4 x 224),
     // else 256-wide unless E fits one 128-wide tile
     h->bn_router = (E % 224 == 0) ? 224 : (E > 128) ? 256 : 128;
+    // the 256-wide down- and up-projections run on CTA pairs: per SM, half the
+    // B tile per stage, six stages instead of four.  The router (one and a half
+    // waves of tiles) and the shared experts' W1|W2 measured slower on pairs
+    // and stay on single CTAs.
+    h->pair_down = h->bn_down == 256;
+    h->pair_shared = false;
+    h->pair_router = false;
+    h->pair_up = h->bn_up == 256;
     // Repack W1, W2 (boxes of bn_exp1/2 rows) and W3 (boxes of bn_exp3 rows)
     // so each box is one contiguous block of HBM; in the FP8 variant the
     // boxes hold e4m3 codes (128 per 128-byte row) instead of bf16.
@@ -456,15 +466,15 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
         free_handle(h);
         return LMOE_ERR_CUDA;
     }
-    ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->bn_down) &&
-         make_map(&h->m_wrouter, w->w_router, E, L, L, h->bn_router) &&
+    ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->pair_down ? h->bn_down / 2 : h->bn_down) &&
+         make_map(&h->m_wrouter, w->w_router, E, L, L, h->pair_router ? h->bn_router / 2 : h->bn_router) &&
          make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
          make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
          make_map(&h->m_w1, h->w1p, E * I * kb12, 64, 64, tr12) &&
          make_map(&h->m_w2, h->w2p, E * I * kb12, 64, 64, tr12) &&
          make_map(&h->m_w3, h->w3p, E * L * kb3, 64, 64, tr3) &&
-         make_map(&h->m_wup, w->w_up, d, L, L, h->bn_up) &&
-         make_map(&h->m_ws3, w->ws3, d, S, S, h->bn_up);
+         make_map(&h->m_wup, w->w_up, d, L, L, h->pair_up ? h->bn_up / 2 : h->bn_up) &&
+         make_map(&h->m_ws3, w->ws3, d, S, S, h->pair_up ? h->bn_up / 2 : h->bn_up);
     if (!ok) {
         free_handle(h);
         return LMOE_ERR_CUDA;
@@ -595,6 +605,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         return LMOE_ERR_CUDA;
 
     const int m_tiles = static_cast<int>(ceil_div(T, kBM));
+    const int m_tiles2 = static_cast<int>(ceil_div(T, 2 * kBM));   // CTA pairs: 256-row tiles
     auto mark = [&](int stage) {
         if (h->stage_events) cudaEventRecord(h->stage_events[stage], stream);
     };
@@ -610,16 +621,19 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmMaps m{m_x, m_x, h->m_wdown, h->m_wdown};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
+        a.m_tiles = h->pair_down ? m_tiles2 : m_tiles;
         a.n_tiles = static_cast<int32_t>(ceil_div(L, h->bn_down));
         a.k_blocks = static_cast<int32_t>(d / kBK);
         a.out = hbuf;
         a.ld_out = L;
         a.out_cols = static_cast<int32_t>(L);
         // the first kernel of the forward follows a memset: ordinary stream order
-        st = gemm_status(launch_gemm(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream, /*pair=*/false,
-                                     /*dependent=*/false));
+        st = gemm_status(h->pair_down
+                             ? launch_gemm_pair(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, m, a, a.m_tiles * a.n_tiles,
+                                                stream, /*dependent=*/false)
+                             : launch_gemm(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
+                                           grid_for(int64_t(m_tiles) * a.n_tiles), stream, /*pair=*/false,
+                                           /*dependent=*/false));
         if (st) return st;
     }
     if (c.norm_after_down &&   // ablation variant: hn = h / sqrt(mean(h^2) + eps), per token
@@ -630,7 +644,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
+        a.m_tiles = h->pair_shared ? m_tiles2 : m_tiles;
         a.n_tiles = static_cast<int32_t>(S / (h->bn_shared / 2));
         a.k_blocks = static_cast<int32_t>(d / kBK);
         a.out = sact;
@@ -640,9 +654,13 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
             a.pout = spre;
             a.pout_ld = 2 * S;
             a.pout_half = static_cast<int32_t>(S);
+        }
+        if (h->pair_shared)
+            return gemm_status(launch_gemm_pair(h->bn_shared, A_DENSE, B_GLU, save ? EPI_SITU_GLU_SAVE : EPI_SITU_GLU,
+                                                m, a, a.m_tiles * a.n_tiles, s_));
+        if (save)
             return gemm_status(launch_gemm_save(h->bn_shared, A_DENSE, false, false, m, a,
                                                 grid_for(int64_t(m_tiles) * a.n_tiles), s_));
-        }
         return gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
                                        grid_for(int64_t(m_tiles) * a.n_tiles), s_));
     };
@@ -651,13 +669,16 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmMaps m{m_h, m_h, h->m_wrouter, h->m_wrouter};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
+        a.m_tiles = h->pair_router ? m_tiles2 : m_tiles;
         a.n_tiles = static_cast<int32_t>(ceil_div(E, h->bn_router));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.out = scores;
         a.lout = logit;                  // with_backward: the logits as well
         a.ld_out = E;
         a.out_cols = static_cast<int32_t>(E);
+        if (h->pair_router)
+            return gemm_status(launch_gemm_pair(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, m, a,
+                                                a.m_tiles * a.n_tiles, stream));
         return gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
                                        grid_for(int64_t(m_tiles) * a.n_tiles), stream));
     };
@@ -795,15 +816,16 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmMaps m{m_r, m_sact, h->m_wup, h->m_ws3};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
+        a.m_tiles = h->pair_up ? m_tiles2 : m_tiles;
         a.n_tiles = static_cast<int32_t>(ceil_div(d, h->bn_up));
         a.k_split = static_cast<int32_t>(L / kBK);
         a.k_blocks = static_cast<int32_t>((L + S) / kBK);
         a.out = y;
         a.ld_out = d;
         a.out_cols = static_cast<int32_t>(d);
-        st = gemm_status(launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        st = gemm_status(h->pair_up ? launch_gemm_pair(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, m, a, a.m_tiles * a.n_tiles, stream)
+                                    : launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
+                                                  grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
     mark(LMOE_NUM_STAGES);
@@ -1298,7 +1320,7 @@ int lmoe_device_status(lmoe_handle *h, cudaStream_t stream, int clear, int *devi
     }
     // a debug build's failed index checks (every translation unit's word)
     const bool cl = clear != 0;
-    const unsigned dbg = debug_word_gemm(cl) | debug_word_gemm_bwd(cl) | debug_word_route(cl) |
+    const unsigned dbg = debug_word_gemm(cl) | debug_word_pair(cl) | debug_word_gemm_bwd(cl) | debug_word_route(cl) |
                          debug_word_backward(cl) | debug_word_selftest(cl);
     if (dbg == ~0u) return LMOE_ERR_CUDA;
     *device_status = dbg ? LMOE_ERR_INDEX : (v & kDevErrTimeout) ? LMOE_ERR_TIMEOUT : LMOE_OK;

@@ -51,16 +51,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with acquire at cluster scope (for barriers that the peer CTA arrives on)
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait.  Returns false (without completing) when another thread of
 // the CTA raised `abort` (if watch_abort) or when `limit_ns` ran out; in the
 // latter case this thread raises `abort` and sets the timeout bit in *err.
+// With `cluster_scope` the wait acquires at cluster scope (for barriers that
+// the other CTA of a pair arrives on).
 static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
-                                       unsigned *err, uint64_t limit_ns, bool watch_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                       unsigned *err, uint64_t limit_ns, bool watch_abort = true,
+                                       bool cluster_scope = false) {
+    auto try_once = [&]() { return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_once()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (try_once()) return true;
         if (watch_abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1u;
@@ -238,13 +254,92 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_bf16_m128(int n) {
+// K-major, M = m (128 on one SM, 256 on a CTA pair), N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
     return (1u << 4)                                  // D format: f32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
            | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
-           | (static_cast<uint32_t>(128 >> 4) << 24); // M / 16
+           | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_m128(int n) { return idesc_bf16(128, n); }
+
+// ----------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on two SMs shares one M = 256 tile: each CTA holds
+// 128 rows of A and half of the B tile in its own shared memory, the MMA
+// thread of CTA 0 issues tcgen05.mma.cta_group::2 over both, and each CTA's
+// TMEM receives the accumulator of its own 128 rows.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t n_clusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Address in the shared::cluster window of the variable at this CTA's
+// shared address `addr`, in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier of any CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Every thread of both CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// TMA load into this CTA's shared memory, its bytes counted on `bar_cluster`,
+// an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+// TMEM allocation shared by the pair: one warp of each CTA executes it; both
+// CTAs receive the same column range.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// Arrive once on the mbarrier at shared offset `bar` in every CTA of
+// `cta_mask` when all tcgen05 ops this thread issued so far are done.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T, M = 256.
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0),

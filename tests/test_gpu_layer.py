@@ -270,6 +270,17 @@ def test_tiny_layer_ragged_token_counts(lm, T):
     end_to_end(synth.TINY, run)
 
 
+# The small widths run the down- and the up-projection on CTA pairs (latent
+# 512, d = 1024: 256-wide tiles, 256 rows per pair).  Ragged batches: T = 1
+# and 129 leave the second CTA of the only pair without rows (129: the first
+# CTA full but one row), T = 1000 ends on a pair whose second CTA holds 104.
+@pytest.mark.parametrize("T", [1, 129, 1000])
+def test_small_layer_ragged_token_counts(lm, T):
+    run = run_host_shape(lm, synth.SMALL, T=T, seed_offset=T)
+    staged_checks(synth.SMALL, run)
+    end_to_end(synth.SMALL, run, allow_empty=T == 1)   # one token may sit within the routing margin
+
+
 # Widths off the usual tiles: d and the shared width not multiples of 128 (ragged
 # N tiles), E = 10 (router tile mostly empty, E not a multiple of 8), k = 3,
 # routed intermediate 192 (three 64-feature SiTU-GLU tiles), one shared expert,
@@ -289,9 +300,10 @@ MAX_ROUTING = synth.LayerShape("max_routing", T=150, d=256, latent=128, n_expert
                                n_shared=2, shared_inter=64, seed=1011)
 
 
-# A router as wide as K3's (E = 896 = 4 x 224) at a batch large enough for the
-# router's 256-row pair tiles (T = 8200: 33 pair rows, the last one with 8
-# rows), on small widths.
+# A router as wide as K3's (E = 896 = 4 x 224) at a large batch whose last
+# tile is ragged (T = 8200: 65 row tiles of 128, the last one with 8 rows; the
+# up-projection's 256-row CTA-pair tiles: 33, the last with 8 rows in its
+# first CTA and none in its second), on small widths.
 WIDE_ROUTER = synth.LayerShape("wide_router", T=8200, d=256, latent=128, n_experts=896, top_k=16, inter=64,
                                n_shared=2, shared_inter=64, seed=1012)
 

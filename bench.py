@@ -490,8 +490,8 @@ def run_profile_case(args):
     import sparse_moe_layer_bias_gb300 as lm
     if args.backward:
         return run_profile_backward(args, lm)
-    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=2048, n_experts=256, router="zipf",
-                                expert_fp8=bool(args.fp8))
+    shape = dataclasses.replace(synth.K3_PREFILL, name="ncu_case", T=args.profile_tokens,
+                                n_experts=args.profile_experts, router="zipf", expert_fp8=bool(args.fp8))
     w = synth.layer_weights_device(shape)
     x, bias = synth.activations_device(shape)
     h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
@@ -561,6 +561,11 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=128)
     ap.add_argument("--profile-case", action="store_true",
                     help="small case for ncu captures: K3 widths, 256 experts, T=2048 (~3.3 GB)")
+    ap.add_argument("--profile-tokens", type=int, default=2048,
+                    help="with --profile-case: tokens per forward")
+    ap.add_argument("--profile-experts", type=int, default=256,
+                    help="with --profile-case: routed experts (fewer experts, more rows per expert; "
+                         "128 experts at 4096 tokens: ~512 rows each, like K3 prefill's heavy experts)")
     ap.add_argument("--fp8", action="store_true", help="with --profile-case: the FP8 expert variant")
     ap.add_argument("--backward", action="store_true",
                     help="with --profile-case: backward passes of a K3-width layer with 64 experts, T=1024")

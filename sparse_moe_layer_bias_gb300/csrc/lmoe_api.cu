@@ -24,8 +24,8 @@ struct lmoe_handle {
     unsigned *d_status;  // device status word (bounded-wait timeouts)
     // Weight-side TMA descriptors, built once.
     int bn_down, bn_shared, bn_exp1, bn_exp3, bn_up, bn_router;
-    // dense GEMMs on CTA pairs (256-row tiles over two SMs; B boxes of bn / 2 rows)
-    bool pair_down, pair_shared, pair_router, pair_up;
+    // down- / up-projection on CTA pairs (256-row tiles over two SMs; B boxes of bn / 2 rows)
+    bool pair_down, pair_up;
     CUtensorMap m_wdown, m_wrouter, m_ws1, m_ws2, m_w1, m_w2, m_w3, m_wup, m_ws3;
     // routed experts' weights repacked tile-contiguously (handle-owned): bf16,
     // or e4m3 codes (expert_fp8) with one int8 scale exponent per weight row
@@ -438,8 +438,6 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
     // waves of tiles) and the shared experts' W1|W2 measured slower on pairs
     // and stay on single CTAs.
     h->pair_down = h->bn_down == 256;
-    h->pair_shared = false;
-    h->pair_router = false;
     h->pair_up = h->bn_up == 256;
     // Repack W1, W2 (boxes of bn_exp1/2 rows) and W3 (boxes of bn_exp3 rows)
     // so each box is one contiguous block of HBM; in the FP8 variant the
@@ -467,7 +465,7 @@ int lmoe_create(const lmoe_config *cfg, const lmoe_weights *w, lmoe_handle **out
         return LMOE_ERR_CUDA;
     }
     ok = make_map(&h->m_wdown, w->w_down, L, d, d, h->pair_down ? h->bn_down / 2 : h->bn_down) &&
-         make_map(&h->m_wrouter, w->w_router, E, L, L, h->pair_router ? h->bn_router / 2 : h->bn_router) &&
+         make_map(&h->m_wrouter, w->w_router, E, L, L, h->bn_router) &&
          make_map(&h->m_ws1, w->ws1, S, d, d, h->bn_shared / 2) &&
          make_map(&h->m_ws2, w->ws2, S, d, d, h->bn_shared / 2) &&
          make_map(&h->m_w1, h->w1p, E * I * kb12, 64, 64, tr12) &&
@@ -644,7 +642,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmMaps m{m_x, m_x, h->m_ws1, h->m_ws2};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = h->pair_shared ? m_tiles2 : m_tiles;
+        a.m_tiles = m_tiles;
         a.n_tiles = static_cast<int32_t>(S / (h->bn_shared / 2));
         a.k_blocks = static_cast<int32_t>(d / kBK);
         a.out = sact;
@@ -654,13 +652,9 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
             a.pout = spre;
             a.pout_ld = 2 * S;
             a.pout_half = static_cast<int32_t>(S);
-        }
-        if (h->pair_shared)
-            return gemm_status(launch_gemm_pair(h->bn_shared, A_DENSE, B_GLU, save ? EPI_SITU_GLU_SAVE : EPI_SITU_GLU,
-                                                m, a, a.m_tiles * a.n_tiles, s_));
-        if (save)
             return gemm_status(launch_gemm_save(h->bn_shared, A_DENSE, false, false, m, a,
                                                 grid_for(int64_t(m_tiles) * a.n_tiles), s_));
+        }
         return gemm_status(launch_gemm(h->bn_shared, A_DENSE, B_GLU, EPI_SITU_GLU, false, m, a,
                                        grid_for(int64_t(m_tiles) * a.n_tiles), s_));
     };
@@ -669,16 +663,13 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         GemmMaps m{m_h, m_h, h->m_wrouter, h->m_wrouter};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = h->pair_router ? m_tiles2 : m_tiles;
+        a.m_tiles = m_tiles;
         a.n_tiles = static_cast<int32_t>(ceil_div(E, h->bn_router));
         a.k_blocks = static_cast<int32_t>(L / kBK);
         a.out = scores;
         a.lout = logit;                  // with_backward: the logits as well
         a.ld_out = E;
         a.out_cols = static_cast<int32_t>(E);
-        if (h->pair_router)
-            return gemm_status(launch_gemm_pair(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, m, a,
-                                                a.m_tiles * a.n_tiles, stream));
         return gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
                                        grid_for(int64_t(m_tiles) * a.n_tiles), stream));
     };

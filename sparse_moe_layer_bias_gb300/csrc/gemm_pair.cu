@@ -1,4 +1,5 @@
-// gemm_pair.cu -- the forward pass's down- and up-projection on CTA pairs: a
+// gemm_pair.cu -- the dense GEMMs on CTA pairs (the forward's down- and
+// up-projection; the backward's dr, dx and dense weight gradients): a
 // 256 x 256 tile per cluster of two SMs, tcgen05.mma.cta_group::2 (M = 256)
 // issued by the first CTA over both CTAs' shared memory, each CTA loading its
 // own 128 rows of A and half of the B tile.  Per SM that is 32 KB of operands
@@ -17,8 +18,10 @@ cudaError_t launch_gemm_pair(int bn, AMode am, BMode bm, Epi epi, const GemmMaps
                              int64_t tiles, cudaStream_t stream, bool dependent) {
     // a1 down-projection
     LMOE_PAIR_CASE(256, A_DENSE, B_PLAIN, EPI_BF16)
-    // a8 up-projection + shared W3 (K split over the two sources)
+    // a8 up-projection + shared W3 (K split over the two sources); backward dx
     LMOE_PAIR_CASE(256, A_SPLIT, B_SPLIT, EPI_BF16)
+    // backward: the dense weights' fp32 gradients (K = tokens)
+    LMOE_PAIR_CASE(256, A_DENSE, B_PLAIN, EPI_F32)
     return cudaErrorInvalidValue;
 }
 

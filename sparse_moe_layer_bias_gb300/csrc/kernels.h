@@ -189,8 +189,10 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
 // and `tiles` = m_tiles x n_tiles; the B maps' boxes are bn / 2 rows (each CTA
 // loads its half of the tile's B rows).  The grid is chosen here (two CTAs
 // per tile, at most as many pairs as fit on the GPU at once).  Compiled for
-// bn = 256 with A_DENSE/B_PLAIN/EPI_BF16 (down-projection) and
-// A_SPLIT/B_SPLIT/EPI_BF16 (up-projection); cudaErrorInvalidValue otherwise.
+// bn = 256 with A_DENSE/B_PLAIN/EPI_BF16 (down-projection, backward dr),
+// A_SPLIT/B_SPLIT/EPI_BF16 (up-projection, backward dx) and
+// A_DENSE/B_PLAIN/EPI_F32 (backward dense weight gradients);
+// cudaErrorInvalidValue otherwise.
 cudaError_t launch_gemm_pair(int bn, AMode am, BMode bm, Epi epi, const GemmMaps &maps, const GemmArgs &args,
                              int64_t tiles, cudaStream_t stream, bool dependent = true);
 

@@ -53,6 +53,7 @@ struct lmoe_handle {
     uint16_t *t_ups3, *t_w3, *t_w12, *t_wr, *t_wd, *t_ws12;
     CUtensorMap m_t_ups3, m_t_w3, m_t_w12, m_t_wr, m_t_wd, m_t_ws12;
     int bn_drs, bn_u, bn_s;
+    bool pair_dr;   // dr on CTA pairs (dx follows pair_up, the dense weight gradients their own width)
     // backward: fork / join events of the side-stream copies
     cudaEvent_t bev[6];
 };
@@ -312,12 +313,13 @@ bool build_transposed(lmoe_handle *h) {
               launch_transpose(w.ws2, d, 0, S, di, h->t_ws12 + S, 2 * S, 0, S, 1, nullptr, nullptr, nullptr, 0) == cudaSuccess &&
               cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) return false;
-    return make_map(&h->m_t_ups3, h->t_ups3, L + S, d, d, h->bn_drs) &&
+    h->pair_dr = h->bn_drs == 256;
+    return make_map(&h->m_t_ups3, h->t_ups3, L + S, d, d, h->pair_dr ? h->bn_drs / 2 : h->bn_drs) &&
            make_map(&h->m_t_w3, h->t_w3, E * I, L, L, h->bn_u) &&
            make_map(&h->m_t_w12, h->t_w12, E * L, 2 * I, 2 * I, h->bn_exp3) &&
            make_map(&h->m_t_wr, h->t_wr, L, Ep, Ep, h->bn_down) &&
-           make_map(&h->m_t_wd, h->t_wd, d, L, L, h->bn_up) &&
-           make_map(&h->m_t_ws12, h->t_ws12, d, 2 * S, 2 * S, h->bn_up);
+           make_map(&h->m_t_wd, h->t_wd, d, L, L, h->pair_up ? h->bn_up / 2 : h->bn_up) &&
+           make_map(&h->m_t_ws12, h->t_ws12, d, 2 * S, 2 * S, h->pair_up ? h->bn_up / 2 : h->bn_up);
 }
 
 // Backward workspace: gradients of the intermediates, their K-major
@@ -904,15 +906,18 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
     int32_t *nkt = reinterpret_cast<int32_t *>(ws + bl.nkt);
     uint16_t *doT = bf(bl.doT), *aT = bf(bl.aT), *hgT = bf(bl.hgT), *dpT = bf(bl.dpT);
 
+    auto wbox = [](int bn) { return bn == 256 ? bn / 2 : bn; };
     CUtensorMap m_dy, m_x, m_dp, m_dl, m_dh, m_dps, m_dyT, m_xT, m_rT, m_sT, m_dpsT, m_dhT, m_hT, m_dlT,
         m_doT, m_aT, m_hgT, m_dpT;
     if (!make_map(&m_dy, dy, T, d, d, kBM) || !make_map(&m_x, x, T, d, d, kBM) ||
         !make_map(&m_dp, dp, n, 2 * I, 2 * I, kBM) || !make_map(&m_dl, dl, T, Ep, Ep, kBM) ||
         !make_map(&m_dh, dhx, T, L, L, kBM) || !make_map(&m_dps, dps, T, 2 * S, 2 * S, kBM) ||
-        !make_map(&m_dyT, dyT, d, Tp, Tp, kBM) || !make_map(&m_xT, xT, d, Tp, Tp, h->bn_up) ||
-        !make_map(&m_rT, rT, L, Tp, Tp, h->bn_down) || !make_map(&m_sT, sT, S, Tp, Tp, h->bn_s) ||
+        // (B of the dense weight-gradient GEMMs: 256-wide ones run on CTA pairs,
+        // each CTA loading half of the tile's rows)
+        !make_map(&m_dyT, dyT, d, Tp, Tp, kBM) || !make_map(&m_xT, xT, d, Tp, Tp, wbox(h->bn_up)) ||
+        !make_map(&m_rT, rT, L, Tp, Tp, wbox(h->bn_down)) || !make_map(&m_sT, sT, S, Tp, Tp, wbox(h->bn_s)) ||
         !make_map(&m_dpsT, dpsT, 2 * S, Tp, Tp, kBM) ||
-        !make_map(&m_dhT, dhT, L, Tp, Tp, kBM) || !make_map(&m_hT, hT, L, Tp, Tp, h->bn_down) ||
+        !make_map(&m_dhT, dhT, L, Tp, Tp, kBM) || !make_map(&m_hT, hT, L, Tp, Tp, wbox(h->bn_down)) ||
         !make_map(&m_dlT, dlT, E, Tp, Tp, kBM) ||
         // K-block packed segment copies: [Qmax / 64 * rows][64]
         !make_map(&m_doT, doT, Qmax / 64 * L, 64, 64, kBM) || !make_map(&m_aT, aT, Qmax / 64 * I, 64, 64, h->bn_u) ||
@@ -977,14 +982,16 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         GemmMaps m{m_dy, m_dy, h->m_t_ups3, h->m_t_ups3};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
+        a.m_tiles = h->pair_dr ? static_cast<int32_t>(ceil_div(T, 2 * kBM)) : m_tiles;
         a.n_tiles = static_cast<int32_t>(ceil_div(L + S, h->bn_drs));
         a.k_blocks = static_cast<int32_t>(d / kBK);
         a.out = drs;
         a.ld_out = L + S;
         a.out_cols = static_cast<int32_t>(L + S);
-        st = gemm_status(launch_gemm(h->bn_drs, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        st = gemm_status(h->pair_dr ? launch_gemm_pair(h->bn_drs, A_DENSE, B_PLAIN, EPI_BF16, m, a,
+                                                       int64_t(a.m_tiles) * a.n_tiles, stream)
+                                    : launch_gemm(h->bn_drs, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
+                                                  grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
     mark(LMOE_BWD_STAGE_SHARED);
@@ -1093,15 +1100,17 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         GemmMaps m{m_dh, m_dps, h->m_t_wd, h->m_t_ws12};
         GemmArgs a = base_args(h);
         a.m_rows = static_cast<int32_t>(T);
-        a.m_tiles = m_tiles;
+        a.m_tiles = h->pair_up ? static_cast<int32_t>(ceil_div(T, 2 * kBM)) : m_tiles;
         a.n_tiles = static_cast<int32_t>(ceil_div(d, h->bn_up));
         a.k_split = static_cast<int32_t>(L / kBK);
         a.k_blocks = static_cast<int32_t>((L + 2 * S) / kBK);
         a.out = dx;
         a.ld_out = d;
         a.out_cols = static_cast<int32_t>(d);
-        st = gemm_status(launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
-                                     grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        st = gemm_status(h->pair_up ? launch_gemm_pair(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, m, a,
+                                                       int64_t(a.m_tiles) * a.n_tiles, stream)
+                                    : launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
+                                                  grid_for(int64_t(m_tiles) * a.n_tiles), stream));
         if (st) return st;
     }
     // ---- weight gradients of the dense weights: K = tokens (transposed operands, zero past T)
@@ -1115,8 +1124,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
                      float *out2 = nullptr, int64_t m_split = 0) {
         GemmMaps m{ma, ma, mb, mb};
         GemmArgs a = base_args(h);
+        const bool pair = bn == 256;   // (B maps made with wbox)
         a.m_rows = static_cast<int32_t>(M);
-        a.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
+        a.m_tiles = static_cast<int32_t>(ceil_div(M, pair ? 2 * kBM : kBM));
         a.n_tiles = static_cast<int32_t>(ceil_div(N, bn));
         a.k_blocks = static_cast<int32_t>(Tp / kBK);
         a.out = out;
@@ -1125,6 +1135,9 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.ld_out = N;
         a.out_cols = static_cast<int32_t>(N);
         a.accumulate = g->accumulate;
+        if (pair)
+            return gemm_status(launch_gemm_pair(bn, A_DENSE, B_PLAIN, EPI_F32, m, a, int64_t(a.m_tiles) * a.n_tiles,
+                                                stream));
         return gemm_status(launch_gemm_bwd(bn, A_DENSE, B_PLAIN, EPI_F32, false, false, m, a,
                                            grid_for(int64_t(a.m_tiles) * a.n_tiles), stream));
     };

@@ -364,9 +364,9 @@ int lmoe_set_backward_events(lmoe_handle *handle, cudaEvent_t *events, int n_eve
  * + 16*(ceil(n/128) + E)          (128-row tile list)
  * + 16*(ceil(n/256) + E)          (256-row tile list)
  * + 256                           (tile counts)
- * + 4*n                           (token of each permuted row) bytes.  It calls no cudaMalloc/cudaFree.  The first call
- * on a device looks up the array's device address (cudaGetSymbolAddress), so
- * make that first call before any stream capture.  All calls share the array:
+ * + 4*n                           (token of each permuted row) bytes.
+ * It calls no cudaMalloc/cudaFree.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress).  All calls share the array:
  * calls whose work overlaps on the GPU (other streams, other threads) race and
  * must be serialised by the caller.  1 <= top_k <= 32, top_k <= E <= 1024. */
 int lmoe_route_static(const float *scores, int64_t T, int32_t E, int32_t top_k, const float *bias,

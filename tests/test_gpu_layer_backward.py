@@ -273,8 +273,9 @@ def test_backward_k3_prefill_sampled(lm):
     sampled tokens (outlier tokens included) against the oracle, which is
     exact per token because dx_t depends on x_t and dy_t alone; dW_up and
     dWs3 on sampled columns against their definition sum_t dy_t r_t^T and
-    sum_t dy_t as_t^T on the forward's own r and shared activations; every
-    gradient finite."""
+    sum_t dy_t as_t^T on the forward's own r and shared activations; the
+    routed weight gradients of sampled experts against the oracle (below);
+    every gradient finite."""
     shape = synth.K3_PREFILL
     T, K, L = shape.T, shape.top_k, shape.latent
     S = shape.n_shared * shape.shared_inter
@@ -316,6 +317,34 @@ def test_backward_k3_prefill_sampled(lm):
     scols = np.sort(rng.choice(S, 24, replace=False))
     a_s = dec(host_bits(ws_view(ws, lay, "shared_act", torch.bfloat16, (T, S))))[:, scols]
     compare("ws3 (sampled columns)", grads["ws3"].cpu().double().numpy()[:, scols], dyd.T @ a_s)
+
+    # dW1[e], dW2[e], dW3[e] and row e of dW_r sum over the assignments to
+    # expert e alone, and with the routing held fixed each assignment's terms
+    # depend only on its own token: the oracle's backward over exactly the
+    # tokens routed to e gives them.  The other experts those tokens chose are
+    # numbered compactly (each keeps its own weights and router row, so every
+    # token's gates and aggregate are unchanged).  Three of the experts with the
+    # fewest tokens keep the oracle's fp64 gradient arrays small.
+    E = shape.n_experts
+    counts = np.bincount(idx.ravel(), minlength=E)
+    touched = np.nonzero(counts)[0]
+    picks = touched[np.argsort(counts[touched], kind="stable")[:3]]
+    for e in picks:
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        used = np.unique(idx[toks])
+        compact = {int(u): j for j, u in enumerate(used)}
+        cidx = np.vectorize(compact.get, otypes=[np.int32])(idx[toks])
+        ccfg = dataclasses.replace(cfg, n_experts=len(used))
+        cw = dict(dense)
+        cw["w_router"] = synth.bits(w["w_router"][torch.from_numpy(used).cuda()])
+        for n in ("w1", "w2", "w3"):
+            cw[n] = {compact[int(u)]: synth.bits(w[n][int(u)]) for u in used}
+        tk = torch.from_numpy(toks).cuda()
+        ref = oracle.layer_backward(ccfg, host_bits(x[tk]), cw, cidx, host_bits(dy[tk]))
+        j = compact[int(e)]
+        for n in ("w1", "w2", "w3"):
+            compare(f"{n}[{e}] ({len(toks)} tokens)", grads[n][int(e)].cpu().double().numpy(), ref[n][j])
+        compare(f"w_router[{e}]", grads["w_router"][int(e)].cpu().double().numpy(), ref["w_router"][j])
 
 
 def test_backward_with_forward_outputs_in_caller_buffers(lm):

@@ -6,6 +6,8 @@ numpy (its own tanh / exp, a dense loop over tokens and chosen experts), one
 random direction per weight and one for x, so a dropped term, a wrong sign or
 a transposed operand in any gradient fails.  The rounded mode (the gradient
 at the forward's bf16 intermediates) must stay within bf16 rounding of it."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -116,6 +118,26 @@ def test_unchosen_experts_get_no_gradient():
     for e in unused:
         for name in ("w1", "w2", "w3", "w_router"):
             assert not np.any(g[name][e]), (name, e)
+
+
+def test_expert_gradients_from_its_own_tokens_with_compact_experts():
+    """One expert's routed gradients (dW1[e], dW2[e], dW3[e], row e of dW_r)
+    from the tokens routed to it alone, the other experts those tokens chose
+    numbered compactly, equal the full batch's bit for bit: with the routing
+    held fixed each assignment's terms depend on its own token only.  The
+    sampled check of these gradients at the K3 width rests on it."""
+    cfg, w, x, dy, idx = make_case(10, n_experts=8, top_k=3)
+    full = oracle.layer_backward(cfg, x, w, idx, dy)
+    for e in np.unique(idx):
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        used = np.unique(idx[toks])
+        compact = {int(u): j for j, u in enumerate(used)}
+        cidx = np.vectorize(compact.get, otypes=[np.int32])(idx[toks])
+        cw = dict(w, w_router=w["w_router"][used], w1=w["w1"][used], w2=w["w2"][used], w3=w["w3"][used])
+        sub = oracle.layer_backward(dataclasses.replace(cfg, n_experts=len(used)), x[toks], cw, cidx, dy[toks])
+        j = compact[int(e)]
+        for name in ("w1", "w2", "w3", "w_router"):
+            np.testing.assert_array_equal(sub[name][j], full[name][e])
 
 
 def test_up_projection_gradient_is_outer_product_with_normalised_latent():

@@ -809,6 +809,23 @@ def main():
     dec_bytes = sum(v[1] for v in wdec.values())
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     assert lm.lmoe_device_status(hd) == 0
+    # decode breakdown: the same forward with an event before every stage
+    # (stream order; the stages' bytes over their times)
+    dev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(lm.STAGES) + 1)] for _ in range(nd)]
+    for evs in dev_sets:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for evs in dev_sets:
+        lm.lmoe_set_stage_events(hd, evs)
+        lm.lmoe_forward(hd, xd, bd, y=yd, workspace=wsd, expert_counts_out=cd, stream=stream)
+    torch.cuda.synchronize()
+    lm.lmoe_set_stage_events(hd, None)
+    assert lm.lmoe_device_status(hd) == 0
+    dec_stages = {}
+    for j, name in enumerate(lm.STAGES):
+        sm_ = float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in dev_sets]))
+        dec_stages[name] = {"ms": round(sm_, 4), "gbs": round(wdec[name][1] / (sm_ * 1e-3) / 1e9, 1)}
 
     # --------------------------------------------------------------- FP8 expert variant
     fp8 = fp8_experts_variant(lm, stream, args.steps, args.warmup, shape, w, x, bias, dshape, wd, xd, bd, peaks)
@@ -847,6 +864,7 @@ def main():
         "fp8_experts": fp8,
         "backward": bwd,
         "decode": {"T": dshape.T, "ms": round(dec_ms, 4), "tokens_per_s": dshape.T / (dec_ms * 1e-3),
+                   "stages": dec_stages,
                    "touched_experts": touched_d, "bytes": dec_bytes, "gbs": round(dec_gbs, 1),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,

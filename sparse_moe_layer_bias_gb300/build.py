@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblmoe.so")
 LIB_DEBUG = os.path.join(PKG, "liblmoe_debug.so")
-SOURCES = ["gemm.cu", "gemm_pair.cu", "gemm_bwd.cu", "backward.cu", "pack.cu", "route.cu", "route_static.cu", "combine.cu", "qb.cu",
+SOURCES = ["gemm.cu", "gemm_pair.cu", "splitk.cu", "gemm_bwd.cu", "backward.cu", "pack.cu", "route.cu", "route_static.cu", "combine.cu", "qb.cu",
            "selftest.cu", "lmoe_api.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", "gemm_kernel.cuh"]
 

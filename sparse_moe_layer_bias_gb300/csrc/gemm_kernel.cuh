@@ -104,6 +104,7 @@ struct Tile {
     int nt;      // N tile index
     int expert;  // grouped: expert id
     int k0, nk;  // first K block and number of K blocks
+    int ks;      // dense split-K: the K range this tile sums (0 otherwise)
 };
 
 // CG2 (dense only): M tiles are 256 rows; CTA `rank` of the pair owns rows
@@ -113,6 +114,7 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m, uint3
     Tile ti;
     ti.k0 = 0;
     ti.nk = a.k_blocks;
+    ti.ks = 0;
     if (KSEG) {
         // per-expert K segments (weight gradients): {expert, first K block,
         // K blocks, first row of the expert's output block}
@@ -146,6 +148,14 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, int t, int n_m, uint3
             ti.row0 = ti.nrows = 0;
         }
     } else {
+        // Split-K: the K ranges are the slowest index of the tile list.
+        if (a.k_splits > 1) {
+            const int base = a.m_tiles * a.n_tiles;
+            ti.ks = t / base;
+            t -= ti.ks * base;
+            ti.k0 = ti.ks * a.k_per_split;
+            ti.nk = min(a.k_per_split, a.k_blocks - ti.k0);
+        }
         // Rasterise in groups of 16 M tiles so the A rows of a group stay in L2
         // while every N tile visits them.
         constexpr int G = 16;
@@ -295,7 +305,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
     grid_dependency_wait();   // inputs of this GEMM come from earlier kernels
     int n_m = GROUPED ? *args.n_mtiles : args.m_tiles;
     if (kDebugChecks && GROUPED && args.lim_tiles > 0 && !idx_ok(n_m, args.lim_tiles + 1)) n_m = 0;   // n_m <= capacity
-    const int total = n_m * args.n_tiles;
+    const int total = n_m * args.n_tiles * ((!GROUPED && args.k_splits > 1) ? args.k_splits : 1);
     const uint64_t lim = args.wait_limit_ns;
 
     if (warp == 0) {
@@ -442,7 +452,8 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 // a pair tile whose second sub-tile is empty skips its MMAs
                 int nsub = 1;
                 if (PAIR) nsub = (tile_at<GROUPED, KSEG>(args, t, n_m).nrows > kBM) ? 2 : 1;
-                const int nkb = KSEG ? tile_at<GROUPED, KSEG>(args, t, n_m).nk : args.k_blocks;
+                const int nkb = (KSEG || (!GROUPED && args.k_splits > 1)) ? tile_at<GROUPED, KSEG, CG2>(args, t, n_m, rank).nk
+                                                                          : args.k_blocks;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.err, lim)) {
                         ok = false;
@@ -688,10 +699,11 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 // adds instead of storing (each element has one writer)
                 // with out2, rows from m_split on go to out2 (two weights' gradients
                 // of one GEMM, e.g. the shared experts' dWs1 | dWs2)
+                // (split-K: this tile's K range has its own slab of partial sums)
                 const int64_t r = ti.row0 + trow;
                 float *dst = (args.out2 && r >= args.m_split)
                                  ? reinterpret_cast<float *>(args.out2) + (r - args.m_split) * args.ld_out
-                                 : reinterpret_cast<float *>(args.out) + r * args.ld_out;
+                                 : reinterpret_cast<float *>(args.out) + ti.ks * args.split_stride + r * args.ld_out;
                 const bool vec_ok = (args.ld_out % 4) == 0;
                 const unsigned long long dbits = reinterpret_cast<unsigned long long>(dst);
 #pragma unroll 1

@@ -20,8 +20,11 @@ cudaError_t launch_gemm_pair(int bn, AMode am, BMode bm, Epi epi, const GemmMaps
     LMOE_PAIR_CASE(256, A_DENSE, B_PLAIN, EPI_BF16)
     // a8 up-projection + shared W3 (K split over the two sources); backward dx
     LMOE_PAIR_CASE(256, A_SPLIT, B_SPLIT, EPI_BF16)
-    // backward: the dense weights' fp32 gradients (K = tokens)
+    // backward: the dense weights' fp32 gradients (K = tokens); forward:
+    // split-K partial sums of the down-projection (small batches)
     LMOE_PAIR_CASE(256, A_DENSE, B_PLAIN, EPI_F32)
+    // split-K partial sums of the up-projection (small batches)
+    LMOE_PAIR_CASE(256, A_SPLIT, B_SPLIT, EPI_F32)
     return cudaErrorInvalidValue;
 }
 

@@ -76,6 +76,7 @@ __device__ __forceinline__ bool idx_ok(int64_t i, int64_t n) {
 // build); `clear` resets it.  Synchronous.
 unsigned debug_word_gemm(bool clear);
 unsigned debug_word_pair(bool clear);
+unsigned debug_word_split(bool clear);
 unsigned debug_word_gemm_bwd(bool clear);
 unsigned debug_word_route(bool clear);
 unsigned debug_word_backward(bool clear);
@@ -172,6 +173,11 @@ struct GemmArgs {
     // entries of the tile list, rows of the grouped row lists, rows of the
     // gathered source, rows of the scattered output, entries of row_scale
     int64_t lim_experts, lim_tiles, lim_rows, lim_src_rows, lim_out_rows, lim_scale;
+    // dense split-K (EPI_F32): k_splits > 1 divides K into ranges of
+    // k_per_split blocks; the tile list is m_tiles x n_tiles x k_splits and
+    // range ks writes its fp32 partial sums at out + ks * split_stride
+    int32_t k_splits, k_per_split;
+    int64_t split_stride;
 };
 
 // Launch one persistent GEMM.  `bn` in {128, 256} (224 for the router).  With `pair`, A_GATHER runs
@@ -190,11 +196,39 @@ cudaError_t launch_gemm(int bn, AMode am, BMode bm, Epi epi, bool grouped, const
 // loads its half of the tile's B rows).  The grid is chosen here (two CTAs
 // per tile, at most as many pairs as fit on the GPU at once).  Compiled for
 // bn = 256 with A_DENSE/B_PLAIN/EPI_BF16 (down-projection, backward dr),
-// A_SPLIT/B_SPLIT/EPI_BF16 (up-projection, backward dx) and
-// A_DENSE/B_PLAIN/EPI_F32 (backward dense weight gradients);
+// A_SPLIT/B_SPLIT/EPI_BF16 (up-projection, backward dx), A_DENSE/B_PLAIN/EPI_F32
+// (backward dense weight gradients; the down-projection's split-K partials)
+// and A_SPLIT/B_SPLIT/EPI_F32 (the up-projection's split-K partials);
 // cudaErrorInvalidValue otherwise.
 cudaError_t launch_gemm_pair(int bn, AMode am, BMode bm, Epi epi, const GemmMaps &maps, const GemmArgs &args,
                              int64_t tiles, cudaStream_t stream, bool dependent = true);
+
+// Split-K of the dense GEMMs for small batches (splitk.cu): the single-CTA
+// GEMM with the fp32 epilogue (args.k_splits, k_per_split, split_stride set;
+// accumulate 0), bn / modes: 128, 224, 256 with A_DENSE/B_PLAIN; 128, 256 with
+// A_DENSE/B_GLU; 128 with A_SPLIT/B_SPLIT.  (The 256-wide down- and
+// up-projection split on CTA pairs: launch_gemm_pair with EPI_F32.)
+cudaError_t launch_gemm_split(int bn, AMode am, BMode bm, const GemmMaps &maps, const GemmArgs &args, int grid,
+                              cudaStream_t stream, bool dependent = true);
+// The sum of the K ranges' partial slabs (fixed order) and the GEMM's epilogue.
+enum SplitFinMode { FIN_BF16 = 0, FIN_SIGMOID = 1, FIN_GLU = 2 };
+struct SplitFinArgs {
+    const float *part;     // slab 0 of the partial sums: [rows][ld_part] fp32
+    int64_t stride;        // elements from one slab to the next
+    int32_t ks;            // number of slabs
+    int32_t mode;          // SplitFinMode
+    int64_t rows, cols;    // output rows and columns (FIN_GLU: features)
+    int64_t ld_part;       // partial row stride (FIN_GLU: 2 x features, tile-interleaved)
+    int32_t H;             // FIN_GLU: features per GEMM tile (W1 columns, then as many W2)
+    float beta1, beta2;    // FIN_GLU
+    uint16_t *out;         // FIN_BF16 / FIN_GLU: bf16 [rows][ld_out]
+    float *outf;           // FIN_SIGMOID: sigmoid of the sums [rows][ld_out]
+    float *lout;           // FIN_SIGMOID: the sums themselves (nullable)
+    int64_t ld_out;
+    uint16_t *pout;        // FIN_GLU: p1 | p2 in bf16 (nullable)
+    int64_t pout_ld, pout_half;
+};
+cudaError_t launch_split_finalize(const SplitFinArgs &a, int num_sms, cudaStream_t stream);
 
 // Backward-pass GEMMs (gemm_bwd.cu); same operand conventions.  With `kseg`
 // (grouped, A and B dense): `tiles` holds {expert, first K block, K blocks,

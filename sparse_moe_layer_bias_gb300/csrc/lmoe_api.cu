@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 
 #include "lmoe.h"
 #include "kernels.h"
@@ -112,11 +113,53 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     size_t h, scores, idx, gates, counts, offsets, bitmap, wprefix, tiles, tiles2, nmt, perm, inv, tokrow,
-        tiles3, act, o, r, sact, hn, h8, h8e, pre, spre, logit, total;
+        tiles3, act, o, r, sact, hn, h8, h8e, pre, spre, logit, part, total;
 };
 
-Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own_idx,
+// Split-K of a dense GEMM for small batches: when its output tiles (256-row
+// tiles on CTA pairs, else 128-row) would fill less than half of the GPU,
+// K is divided into ks ranges of `per` K blocks (at least 4 each) so that
+// tiles x ks CTAs (or pairs) fill it once; ks == 1: no split.
+struct DenseSplit {
+    int ks, per;
+};
+DenseSplit plan_split(int num_sms, bool pair, int64_t T, int64_t n_tiles, int k_blocks) {
+    DenseSplit sp{1, k_blocks};
+    const int64_t base = ceil_div(T, pair ? 2 * kBM : kBM) * n_tiles;
+    const int64_t units = pair ? num_sms / 2 : num_sms;
+    if (base <= 0 || 2 * base > units) return sp;
+    const int64_t ks = std::min<int64_t>(units / base, k_blocks / 4);
+    if (ks < 2) return sp;
+    const int per = static_cast<int>(ceil_div(k_blocks, ks));
+    const int ks2 = static_cast<int>(ceil_div(k_blocks, per));
+    if (ks2 >= 2) sp = DenseSplit{ks2, per};
+    return sp;
+}
+
+// The forward's four dense GEMMs: {split, output columns of the partial sums}.
+struct DenseSplits {
+    DenseSplit down, router, shared, up;
+    int64_t n_down, n_router, n_shared, n_up;
+};
+DenseSplits plan_dense_splits(const lmoe_handle *h, int64_t T) {
+    const lmoe_config &c = h->cfg;
+    const int64_t d = c.d, L = c.latent, E = c.n_experts;
+    const int64_t S = int64_t(c.n_shared) * c.shared_inter;
+    DenseSplits p;
+    p.down = plan_split(h->num_sms, h->pair_down, T, ceil_div(L, h->bn_down), static_cast<int>(d / kBK));
+    p.router = plan_split(h->num_sms, false, T, ceil_div(E, h->bn_router), static_cast<int>(L / kBK));
+    p.shared = plan_split(h->num_sms, false, T, S / (h->bn_shared / 2), static_cast<int>(d / kBK));
+    p.up = plan_split(h->num_sms, h->pair_up, T, ceil_div(d, h->bn_up), static_cast<int>((L + S) / kBK));
+    p.n_down = L;
+    p.n_router = E;
+    p.n_shared = 2 * S;
+    p.n_up = d;
+    return p;
+}
+
+Layout compute_layout(const lmoe_handle *h, int64_t T, bool own_scores, bool own_idx,
                       bool own_gates, bool own_counts) {
+    const lmoe_config &c = h->cfg;
     Layout l{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -156,6 +199,16 @@ Layout compute_layout(const lmoe_config &c, int64_t T, bool own_scores, bool own
     l.pre = c.with_backward ? take(size_t(n * 2 * I * 2)) : none;
     l.spre = c.with_backward ? take(size_t(T * 2 * S * 2)) : none;
     l.logit = c.with_backward ? take(size_t(T * E * 4)) : none;   // the router's fp32 logits
+    // small batches: the dense GEMMs' split-K partial sums (one slab per K
+    // range, fp32; the four GEMMs use the slot one after another)
+    {
+        const DenseSplits p = plan_dense_splits(h, T);
+        int64_t pe = 0;
+        for (auto [sp, nc] : {std::pair<DenseSplit, int64_t>{p.down, p.n_down}, {p.router, p.n_router},
+                              {p.shared, p.n_shared}, {p.up, p.n_up}})
+            if (sp.ks > 1) pe = std::max(pe, int64_t(sp.ks) * T * nc);
+        l.part = pe ? take(size_t(pe * 4)) : none;
+    }
     l.total = off;
     return l;
 }
@@ -207,6 +260,38 @@ GemmArgs base_args(const lmoe_handle *h) {
 }
 
 int gemm_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
+
+// A dense GEMM of a small batch as split-K: the GEMM's fp32 epilogue writes
+// each K range's partial sums into its slab of `part`, then the finalize adds
+// the slabs in a fixed order and applies the GEMM's own epilogue (`fin`: its
+// mode and outputs).  `a` carries the operands and the shape (n_tiles,
+// k_blocks, k_split); `n_cols` is the partial sums' row length.
+int run_split(const lmoe_handle *h, const GemmMaps &m, GemmArgs a, int bn, AMode am, BMode bm, bool pair,
+              const DenseSplit &sp, int64_t T, int64_t n_cols, float *part, SplitFinArgs fin, cudaStream_t s,
+              bool dependent) {
+    a.m_rows = static_cast<int32_t>(T);
+    a.m_tiles = static_cast<int32_t>(ceil_div(T, pair ? 2 * kBM : kBM));
+    a.k_splits = sp.ks;
+    a.k_per_split = sp.per;
+    a.split_stride = T * n_cols;
+    a.out = part;
+    a.ld_out = n_cols;
+    a.out_cols = static_cast<int32_t>(n_cols);
+    a.lout = nullptr;
+    a.pout = nullptr;
+    a.accumulate = 0;
+    const int64_t tiles = int64_t(a.m_tiles) * a.n_tiles * sp.ks;
+    const cudaError_t e =
+        pair ? launch_gemm_pair(bn, am, bm, EPI_F32, m, a, tiles, s, dependent)
+             : launch_gemm_split(bn, am, bm, m, a, static_cast<int>(std::min<int64_t>(tiles, h->num_sms)), s, dependent);
+    if (e != cudaSuccess) return LMOE_ERR_CUDA;
+    fin.part = part;
+    fin.stride = T * n_cols;
+    fin.ks = sp.ks;
+    fin.rows = T;
+    fin.ld_part = n_cols;
+    return gemm_status(launch_split_finalize(fin, h->num_sms, s));
+}
 
 // Staging slot of lmoe_forward_host: x [max_tokens][d] bf16, bias [E] fp32,
 // y [max_tokens][d] bf16.
@@ -512,14 +597,14 @@ int lmoe_destroy(lmoe_handle *h) {
 int lmoe_workspace_size(const lmoe_handle *h, int64_t T, size_t *bytes) {
     if (!h || !bytes || T < 0) return LMOE_ERR_INVALID_ARG;
     if (T > h->cfg.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
-    *bytes = compute_layout(h->cfg, T, true, true, true, true).total;
+    *bytes = compute_layout(h, T, true, true, true, true).total;
     return LMOE_OK;
 }
 
 int lmoe_workspace_layout(const lmoe_handle *h, int64_t T, lmoe_ws_layout *out) {
     if (!h || !out || T < 0) return LMOE_ERR_INVALID_ARG;
     if (T > h->cfg.max_tokens) return LMOE_ERR_UNSUPPORTED_SHAPE;
-    const Layout l = compute_layout(h->cfg, T, true, true, true, true);
+    const Layout l = compute_layout(h, T, true, true, true, true);
     out->h = int64_t(l.h);
     out->scores = int64_t(l.scores);
     out->topk_idx = int64_t(l.idx);
@@ -557,7 +642,7 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         return LMOE_ERR_ALIGNMENT;
     // The workspace is sized for every intermediate; caller-provided outputs
     // simply leave their slot unused, so the documented offsets never move.
-    const Layout l = compute_layout(c, T, true, true, true, true);
+    const Layout l = compute_layout(h, T, true, true, true, true);
     if (workspace_bytes < l.total) return LMOE_ERR_WORKSPACE;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -595,6 +680,9 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     uint16_t *pre = save ? reinterpret_cast<uint16_t *>(ws + l.pre) : nullptr;
     uint16_t *spre = save ? reinterpret_cast<uint16_t *>(ws + l.spre) : nullptr;
     float *logit = save ? reinterpret_cast<float *>(ws + l.logit) : nullptr;
+    // small batches: the dense GEMMs split over K (partial sums in the workspace)
+    const DenseSplits dsp = plan_dense_splits(h, T);
+    float *part = l.part != SIZE_MAX ? reinterpret_cast<float *>(ws + l.part) : nullptr;
 
     // Activation-side TMA descriptors for this T and workspace.
     CUtensorMap m_x, m_h, m_act, m_r, m_sact;
@@ -628,12 +716,22 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.ld_out = L;
         a.out_cols = static_cast<int32_t>(L);
         // the first kernel of the forward follows a memset: ordinary stream order
-        st = gemm_status(h->pair_down
-                             ? launch_gemm_pair(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, m, a, a.m_tiles * a.n_tiles,
-                                                stream, /*dependent=*/false)
-                             : launch_gemm(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
-                                           grid_for(int64_t(m_tiles) * a.n_tiles), stream, /*pair=*/false,
-                                           /*dependent=*/false));
+        if (dsp.down.ks > 1) {
+            SplitFinArgs f{};
+            f.mode = FIN_BF16;
+            f.cols = L;
+            f.out = hbuf;
+            f.ld_out = L;
+            st = run_split(h, m, a, h->bn_down, A_DENSE, B_PLAIN, h->pair_down, dsp.down, T, dsp.n_down, part, f,
+                           stream, /*dependent=*/false);
+        } else {
+            st = gemm_status(h->pair_down
+                                 ? launch_gemm_pair(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, m, a,
+                                                    a.m_tiles * a.n_tiles, stream, /*dependent=*/false)
+                                 : launch_gemm(h->bn_down, A_DENSE, B_PLAIN, EPI_BF16, false, m, a,
+                                               grid_for(int64_t(m_tiles) * a.n_tiles), stream, /*pair=*/false,
+                                               /*dependent=*/false));
+        }
         if (st) return st;
     }
     if (c.norm_after_down &&   // ablation variant: hn = h / sqrt(mean(h^2) + eps), per token
@@ -650,6 +748,21 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = sact;
         a.ld_out = S;
         a.out_cols = static_cast<int32_t>(S);
+        if (dsp.shared.ks > 1) {
+            SplitFinArgs f{};
+            f.mode = FIN_GLU;
+            f.cols = S;
+            f.H = h->bn_shared / 2;
+            f.beta1 = c.beta1;
+            f.beta2 = c.beta2;
+            f.out = sact;
+            f.ld_out = S;
+            f.pout = save ? spre : nullptr;
+            f.pout_ld = 2 * S;
+            f.pout_half = S;
+            return run_split(h, m, a, h->bn_shared, A_DENSE, B_GLU, false, dsp.shared, T, dsp.n_shared, part, f, s_,
+                             true);
+        }
         if (save) {
             a.pout = spre;
             a.pout_ld = 2 * S;
@@ -672,6 +785,16 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.lout = logit;                  // with_backward: the logits as well
         a.ld_out = E;
         a.out_cols = static_cast<int32_t>(E);
+        if (dsp.router.ks > 1) {
+            SplitFinArgs f{};
+            f.mode = FIN_SIGMOID;
+            f.cols = E;
+            f.outf = scores;
+            f.lout = logit;
+            f.ld_out = E;
+            return run_split(h, m, a, h->bn_router, A_DENSE, B_PLAIN, false, dsp.router, T, dsp.n_router, part, f,
+                             stream, true);
+        }
         return gemm_status(launch_gemm(h->bn_router, A_DENSE, B_PLAIN, EPI_SIGMOID_F32, false, m, a,
                                        grid_for(int64_t(m_tiles) * a.n_tiles), stream));
     };
@@ -816,9 +939,19 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         a.out = y;
         a.ld_out = d;
         a.out_cols = static_cast<int32_t>(d);
-        st = gemm_status(h->pair_up ? launch_gemm_pair(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, m, a, a.m_tiles * a.n_tiles, stream)
-                                    : launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
-                                                  grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        if (dsp.up.ks > 1) {
+            SplitFinArgs f{};
+            f.mode = FIN_BF16;
+            f.cols = d;
+            f.out = y;
+            f.ld_out = d;
+            st = run_split(h, m, a, h->bn_up, A_SPLIT, B_SPLIT, h->pair_up, dsp.up, T, dsp.n_up, part, f, stream, true);
+        } else {
+            st = gemm_status(h->pair_up ? launch_gemm_pair(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, m, a,
+                                                           a.m_tiles * a.n_tiles, stream)
+                                        : launch_gemm(h->bn_up, A_SPLIT, B_SPLIT, EPI_BF16, false, m, a,
+                                                      grid_for(int64_t(m_tiles) * a.n_tiles), stream));
+        }
         if (st) return st;
     }
     mark(LMOE_NUM_STAGES);
@@ -852,7 +985,7 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
         (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u))
         return LMOE_ERR_ALIGNMENT;
-    const Layout fl = compute_layout(c, T, true, true, true, true);
+    const Layout fl = compute_layout(h, T, true, true, true, true);
     const BwdLayout bl = bwd_layout(h, T);
     if (fwd_workspace_bytes < fl.total || workspace_bytes < bl.total) return LMOE_ERR_WORKSPACE;
 
@@ -1228,7 +1361,7 @@ int lmoe_forward_host(lmoe_handle *h, const uint16_t *x_host, int64_t T, const f
     if (reinterpret_cast<uintptr_t>(io_dev) & 255u) return LMOE_ERR_ALIGNMENT;
     const IoSlot sl = io_slot(c);
     if (io_bytes < 2 * sl.bytes) return LMOE_ERR_WORKSPACE;
-    if (workspace_bytes < compute_layout(c, T, true, true, true, true).total) return LMOE_ERR_WORKSPACE;
+    if (workspace_bytes < compute_layout(h, T, true, true, true, true).total) return LMOE_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || (scores_out && !aligned16(scores_out)) ||
         (topk_idx_out && !aligned16(topk_idx_out)) || (gates_out && !aligned16(gates_out)) ||
         (expert_counts_out && !aligned16(expert_counts_out)))
@@ -1324,7 +1457,7 @@ int lmoe_device_status(lmoe_handle *h, cudaStream_t stream, int clear, int *devi
     }
     // a debug build's failed index checks (every translation unit's word)
     const bool cl = clear != 0;
-    const unsigned dbg = debug_word_gemm(cl) | debug_word_pair(cl) | debug_word_gemm_bwd(cl) | debug_word_route(cl) |
+    const unsigned dbg = debug_word_gemm(cl) | debug_word_pair(cl) | debug_word_split(cl) | debug_word_gemm_bwd(cl) | debug_word_route(cl) |
                          debug_word_backward(cl) | debug_word_selftest(cl);
     if (dbg == ~0u) return LMOE_ERR_CUDA;
     *device_status = dbg ? LMOE_ERR_INDEX : (v & kDevErrTimeout) ? LMOE_ERR_TIMEOUT : LMOE_OK;

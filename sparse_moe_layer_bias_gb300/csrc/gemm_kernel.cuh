@@ -578,6 +578,9 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 #pragma unroll 1
             for (int sub = 0; sub < NSUB; ++sub) {
             if (sub * kBM >= ti.nrows) break;  // uniform across the CTA
+            // this warp's 32 rows all lie past the tile's valid rows: nothing
+            // to read or write (uniform across the warp)
+            if (sub * kBM + q * 32 >= ti.nrows) continue;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>((acc + sub) * kAccStride);
             const int trow = sub * kBM + row;    // row of the tile (pair tiles: 0..255)

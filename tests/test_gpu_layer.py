@@ -315,6 +315,23 @@ def test_wide_router_layer_stages_and_end_to_end(lm):
     assert kept >= 0.5 * WIDE_ROUTER.T
 
 
+# Split-K on the single-CTA GEMM variants (the small widths split the 256-wide
+# down- and up-projection on CTA pairs): at T = 50 every dense GEMM has a few
+# output tiles and at least 8 K blocks, so each splits in two.  The
+# up-projection runs 128-wide tiles (d = 576: a ragged last N tile) and its
+# second K range straddles the switch from r to the shared activations; the
+# shared experts run 64 features per tile (S = 192); the router's 30 columns
+# are stored element by element (30 is not a multiple of 4).
+ODD_SPLIT = synth.LayerShape("odd_split", T=50, d=576, latent=512, n_experts=30, top_k=5, inter=128,
+                             n_shared=1, shared_inter=192, seed=1014)
+
+
+def test_odd_split_layer_stages_and_end_to_end(lm):
+    run = run_host_shape(lm, ODD_SPLIT)
+    staged_checks(ODD_SPLIT, run)
+    end_to_end(ODD_SPLIT, run)
+
+
 # The degenerate routing: one routed expert, chosen by every token (E = k = 1;
 # 300 tokens: one pair tile of 256 rows and one of 44 in the W1|W2 GEMM).
 SINGLE_EXPERT = synth.LayerShape("single_expert", T=300, d=256, latent=128, n_experts=1, top_k=1, inter=64,

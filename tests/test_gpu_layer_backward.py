@@ -112,6 +112,13 @@ def test_backward_odd_shape(lm):
     check_backward(ODD, run_backward(lm, ODD))
 
 
+def test_backward_odd_split(lm):
+    """The training forward and backward with every dense GEMM of the forward
+    split over K on the single-CTA variants (see test_gpu_layer.ODD_SPLIT)."""
+    from test_gpu_layer import ODD_SPLIT
+    check_backward(ODD_SPLIT, run_backward(lm, ODD_SPLIT))
+
+
 def test_backward_all_experts(lm):
     """k = E: every expert holds all T rows (several 128-row tiles and K
     segments per expert)."""

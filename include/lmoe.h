@@ -131,7 +131,10 @@ int lmoe_destroy(lmoe_handle *handle);
 
 /* Bytes of caller-provided device workspace lmoe_forward needs for T tokens
  * (0 <= T <= max_tokens).  The workspace holds the routing maps and the
- * intermediate activations; see lmoe_workspace_layout. */
+ * intermediate activations (see lmoe_workspace_layout) and, for batches
+ * small enough that the dense GEMMs are split over K, their fp32 partial
+ * sums in an internal slot after the documented ones.  The size depends on
+ * the handle's device (its number of SMs). */
 int lmoe_workspace_size(const lmoe_handle *handle, int64_t T, size_t *bytes);
 
 /* Byte offsets, inside the workspace, of the intermediates a forward of T

@@ -886,12 +886,16 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
         st = gemm_status(w12(/*pair=*/false, grid_for(E * a.n_tiles)));
         if (st) return st;
         mark(LMOE_STAGE_EXPERT_W12_HEAVY);
-        a.tiles = tiles2;
-        a.n_mtiles = nmt + 1;
-        a.lim_tiles = ceil_div(n, 2 * kBM) + E;
-        const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
-        st = gemm_status(w12(/*pair=*/true, grid_for(max_pairs)));
-        if (st) return st;
+        // an expert holds at most one row per token, so with T <= 128 no
+        // expert is heavy and the pair-tile list is empty: no launch
+        if (T > kBM) {
+            a.tiles = tiles2;
+            a.n_mtiles = nmt + 1;
+            a.lim_tiles = ceil_div(n, 2 * kBM) + E;
+            const int64_t max_pairs = (ceil_div(n, 2 * kBM) + E) * a.n_tiles;
+            st = gemm_status(w12(/*pair=*/true, grid_for(max_pairs)));
+            if (st) return st;
+        }
     }
     mark(LMOE_STAGE_EXPERT_W3);
     {   // a6: o[a] = gate[a] * W3[e] act, written back in assignment order

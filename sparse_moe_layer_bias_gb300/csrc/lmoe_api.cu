@@ -1155,7 +1155,8 @@ int lmoe_backward(lmoe_handle *h, const uint16_t *x, int64_t T, const uint16_t *
         a.ld_out = I;
         a.out_cols = static_cast<int32_t>(I);
         // 128-row tiles for every expert (pair tiles, which hold the whole
-        // TMEM, measured slower here: their epilogue cannot overlap the MMAs)
+        // TMEM, measured slower here, for every expert and for those with
+        // more than 128 rows alike: their epilogue cannot overlap the MMAs)
         a.tiles = tiles;
         a.n_mtiles = nmt;
         a.lim_tiles = ceil_div(n, kBM) + E;

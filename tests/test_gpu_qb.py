@@ -104,6 +104,27 @@ def test_quantile_bias_matches_oracle(lm, B):
     assert np.array_equal(b.cpu().numpy(), b_ref)
 
 
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_histogram_and_quantile_with_very_few_bins(lm, B):
+    """B = 1 (every score in one bin: the quantile is the rank's fraction of
+    it), B = 2 and 3, with scores on the bin edges (s = k/B) and s = 1.0 (the
+    last bin), at the level extremes 0 and 1, one half and 1 - k/E."""
+    rng = np.random.default_rng(100 + B)
+    T, E = 3001, 40
+    s = rng.random((T, E)).astype(np.float32)
+    s[:: 7] = np.float32(1.0)
+    for j in range(B + 1):
+        s[j + 1:: 11, j % E] = np.float32(j / B)
+    h = lm.qb_histogram(torch.from_numpy(s).cuda(), B)
+    hist = oracle.qb_histogram(s, B)
+    assert np.array_equal(h.cpu().numpy().view(np.uint32), hist)
+    for level in (0.0, 0.5, 1 - 16 / 896, 1.0):
+        q, b = lm.qb_quantile_bias(h, level)
+        q_ref, b_ref = oracle.qb_quantile_bias(hist, level)
+        assert np.array_equal(q.cpu().numpy(), q_ref), level
+        assert np.array_equal(b.cpu().numpy(), b_ref), level
+
+
 def test_quantile_within_one_bin_of_exact_sort(lm):
     T, E, B = 65536, 896, 1000
     s = synth.qb_scores(T, E, seed=11)

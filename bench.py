@@ -45,7 +45,7 @@ QB_B = 1000
 # DRAM read+write / algorithmic bytes, measured with ncu on `--profile-case`
 # for the kernels that can be the step's dominant one; a kernel changed since
 # its counters were taken has no entry (its traffic is reported as null)
-TRAFFIC_RATIO = {"expert_w3": 1.228, "expert_w12_light": 1.021, "expert_w12_heavy": 1.062}
+TRAFFIC_RATIO = {"expert_w3": 1.228, "expert_w12_light": 1.021, "expert_w12_heavy": 1.061}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

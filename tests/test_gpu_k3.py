@@ -16,7 +16,8 @@ import oracle
 from sparse_moe_layer_bias_gb300 import synth
 
 from layer_check import (ACC_REL, check_layer_output, check_o, check_r_from_o, check_y_stage, e4m3_table,
-                         score_tol, dec, host_bits, oracle_cfg, rel_fro, to_e4m3, ulp_bf16, ws_view)
+                         latent_ambiguity, routing_robust_norm_after_down, score_tol, dec, host_bits, oracle_cfg,
+                         rel_fro, to_e4m3, ulp_bf16, ws_view)
 
 pytestmark = pytest.mark.gpu
 
@@ -102,19 +103,25 @@ def check_k3(shape, run, extra, n_min=128):
     exact_h = X @ Wd.T
     h_gpu = host_bits(ws_view(ws, lay, "h", torch.bfloat16, (T, L))[smc])
     assert np.all(np.abs(dec(h_gpu) - exact_h) <= ulp_bf16(exact_h) + ACC_REL * (np.abs(X) @ np.abs(Wd).T))
+    # the routed latent: h, or in the norm-after-down variant RMSNorm(h), which
+    # both sides round once from the fp64 quotient (bit-equal on the GPU's h)
+    h_lat = h_gpu
+    if shape.norm_after_down:
+        h_lat = host_bits(ws_view(ws, lay, "h_norm", torch.bfloat16, (T, L))[smc])
+        assert np.array_equal(h_lat, oracle.rms_rows(cfg, h_gpu))
     wr = synth.bits(w["w_router"])
-    s_ref = oracle.router(cfg, h_gpu, wr)
-    absum_s = np.abs(dec(h_gpu)) @ np.abs(dec(wr)).T
+    s_ref = oracle.router(cfg, h_lat, wr)
+    absum_s = np.abs(dec(h_lat)) @ np.abs(dec(wr)).T
     assert np.all(np.abs(s_gpu[sm] - s_ref) <= score_tol(s_ref, absum_s))
 
     used = np.unique(idx_gpu[sm])
     we = {n: {int(e): synth.bits(w[n][int(e)]) for e in used} for n in ("w1", "w2", "w3")}
-    rt = oracle.routed(cfg, h_gpu, idx_gpu[sm], g_gpu[sm], we["w1"], we["w2"], we["w3"], want_act=True)
+    rt = oracle.routed(cfg, h_lat, idx_gpu[sm], g_gpu[sm], we["w1"], we["w2"], we["w3"], want_act=True)
     rows = (sm[:, None] * K + np.arange(K)[None, :]).reshape(-1)       # assignment ids
     prow = inv[rows]                                                    # their permuted rows
     act_bits = host_bits(ws_view(ws, lay, "act", torch.bfloat16, (T * K, I))[torch.from_numpy(prow).cuda()])
     act_gpu, act_ref = dec(act_bits), dec(rt["act"])
-    Hd = np.abs(dec(h_gpu))
+    Hd = np.abs(dec(h_lat))
     acc_tol = np.zeros_like(act_ref)
     ex = idx_gpu[sm].reshape(-1)
     for e in np.unique(ex):
@@ -140,16 +147,25 @@ def check_k3(shape, run, extra, n_min=128):
 
     # end to end on the sampled tokens, with the oracle's own routing
     h_o = oracle.down_proj(cfg, xb, wd)
-    s_o = oracle.router(cfg, h_o, wr)
+    h_lat_o = oracle.rms_rows(cfg, h_o) if shape.norm_after_down else h_o
+    s_o = oracle.router(cfg, h_lat_o, wr)
     idx_o, g_o, margin = oracle.topk(cfg, s_o, bias)
     used_o = np.unique(idx_o)
     we_o = {n: {int(e): we[n][int(e)] if int(e) in we[n] else synth.bits(w[n][int(e)]) for e in used_o}
             for n in ("w1", "w2", "w3")}
-    rt_o = oracle.routed(cfg, h_o, idx_o, g_o, we_o["w1"], we_o["w2"], we_o["w3"])
+    rt_o = oracle.routed(cfg, h_lat_o, idx_o, g_o, we_o["w1"], we_o["w2"], we_o["w3"])
     y_o = oracle.up_shared(cfg, rt_o["r"], oracle.shared_act(cfg, xb, ws1, ws2), wup, ws3)
     keep = margin > 1e-4
+    also = None
+    if shape.norm_after_down:
+        # RMSNorm(h) depends on the whole row of h: leave out, on the oracle's
+        # data alone, the tokens whose routing a last-bit change of an
+        # ambiguous element of h would move
+        amb, alt = latent_ambiguity(cfg, xb, wd, h_o)
+        also = routing_robust_norm_after_down(cfg, h_o, amb, alt, wr, bias, idx_o)
+        keep &= also
     assert keep.sum() >= 0.5 * len(sm)
-    check_layer_output(y_gpu, y_o, margin)
+    check_layer_output(y_gpu, y_o, margin, also_keep=also)
     # on those tokens the GPU chose the same experts
     assert np.array_equal(np.sort(idx_gpu[sm][keep], 1), np.sort(idx_o[keep], 1))
     return counts
@@ -166,6 +182,14 @@ def test_k3_decode_layer(lm):
     counts = check_k3(shape, run, list(range(shape.T)), n_min=shape.T)   # every decode token
     touched = int((counts > 0).sum())
     assert 500 <= touched <= 700            # ~613 distinct experts expected for 64 x 16 picks
+
+
+def test_k3_decode_layer_norm_after_down(lm):
+    """The norm-after-down variant at K3 widths (RMSNorm of the 3584-wide
+    latent before the router and the experts), every decode token."""
+    shape = dataclasses.replace(synth.K3_DECODE, name="k3_decode_norm_after_down", norm_after_down=True)
+    run = run_k3(lm, shape)
+    check_k3(shape, run, list(range(shape.T)), n_min=shape.T)
 
 
 def test_k3_prefill_layer(lm):

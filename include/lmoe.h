@@ -134,7 +134,8 @@ int lmoe_destroy(lmoe_handle *handle);
  * intermediate activations (see lmoe_workspace_layout) and, for batches
  * small enough that the dense GEMMs are split over K, their fp32 partial
  * sums in an internal slot after the documented ones.  The size depends on
- * the handle's device (its number of SMs). */
+ * the handle's device (its number of SMs) and never decreases with T: a
+ * workspace sized for T (e.g. for max_tokens) serves every smaller batch. */
 int lmoe_workspace_size(const lmoe_handle *handle, int64_t T, size_t *bytes);
 
 /* Byte offsets, inside the workspace, of the intermediates a forward of T

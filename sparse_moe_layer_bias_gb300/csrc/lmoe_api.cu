@@ -157,6 +157,27 @@ DenseSplits plan_dense_splits(const lmoe_handle *h, int64_t T) {
     return p;
 }
 
+// fp32 elements of the split-K slot for a batch of T tokens: the largest
+// need of any batch of at most T tokens, so that a workspace sized for T (for
+// instance for max_tokens) also serves every smaller batch -- a smaller batch
+// can split more ways (fewer tiles) and need more.  For a fixed number of
+// row tiles the need grows with the batch, so T and the multiples of 128 below
+// it cover every case.  A GEMM splits only while twice its row tiles fit in
+// the SMs (pairs: in half of them), i.e. for at most 64 rows per SM.
+int64_t split_slot_elems(const lmoe_handle *h, int64_t T) {
+    int64_t pe = 0;
+    auto at = [&](int64_t t) {
+        const DenseSplits p = plan_dense_splits(h, t);
+        for (auto [sp, nc] : {std::pair<DenseSplit, int64_t>{p.down, p.n_down}, {p.router, p.n_router},
+                              {p.shared, p.n_shared}, {p.up, p.n_up}})
+            if (sp.ks > 1) pe = std::max(pe, int64_t(sp.ks) * t * nc);
+    };
+    if (T > 0) at(T);
+    const int64_t t_max = std::min<int64_t>(T - 1, int64_t(h->num_sms) * kBM);
+    for (int64_t t = kBM; t <= t_max; t += kBM) at(t);
+    return pe;
+}
+
 Layout compute_layout(const lmoe_handle *h, int64_t T, bool own_scores, bool own_idx,
                       bool own_gates, bool own_counts) {
     const lmoe_config &c = h->cfg;
@@ -202,11 +223,7 @@ Layout compute_layout(const lmoe_handle *h, int64_t T, bool own_scores, bool own
     // small batches: the dense GEMMs' split-K partial sums (one slab per K
     // range, fp32; the four GEMMs use the slot one after another)
     {
-        const DenseSplits p = plan_dense_splits(h, T);
-        int64_t pe = 0;
-        for (auto [sp, nc] : {std::pair<DenseSplit, int64_t>{p.down, p.n_down}, {p.router, p.n_router},
-                              {p.shared, p.n_shared}, {p.up, p.n_up}})
-            if (sp.ks > 1) pe = std::max(pe, int64_t(sp.ks) * T * nc);
+        const int64_t pe = split_slot_elems(h, T);
         l.part = pe ? take(size_t(pe * 4)) : none;
     }
     l.total = off;

@@ -363,6 +363,30 @@ def test_odd_shape_layer_stages_and_end_to_end(lm):
     end_to_end(ODD, run)
 
 
+def test_workspace_for_max_tokens_serves_every_smaller_batch(lm):
+    """A workspace sized for max_tokens is large enough for every smaller
+    batch, although a smaller batch may split its dense GEMMs over K more
+    ways (fewer tiles) and need more partial sums: at the K3 router width
+    (E = 896, latent 3584) the router splits 14 ways at 256 tokens and 12 at
+    257.  The forward in such a workspace gives the same bits as in one sized
+    for its own T."""
+    shape = synth.LayerShape("k3_router_width", T=600, d=256, latent=3584, n_experts=896, top_k=16, inter=64,
+                             n_shared=1, shared_inter=64, seed=1015)
+    w = synth.layer_weights_device(shape)
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
+    big = lm.lmoe_workspace_size(h, shape.T)
+    sizes = [lm.lmoe_workspace_size(h, t) for t in range(0, shape.T + 1)]
+    assert max(sizes) == big and all(a <= b for a, b in zip(sizes, sizes[1:]))
+    ws_big = lm.alloc_workspace(h, shape.T)
+    x, b = synth.activations_device(shape)
+    for t in (64, 255, 256, 257, 384, 512, 513):
+        y_big = lm.lmoe_forward(h, x[:t], b, workspace=ws_big)
+        y_own = lm.lmoe_forward(h, x[:t], b, workspace=lm.alloc_workspace(h, t))
+        torch.cuda.synchronize()
+        assert torch.equal(y_big.view(torch.int16), y_own.view(torch.int16)), t
+    assert lm.lmoe_device_status(h) == 0
+
+
 def test_forward_is_deterministic(lm):
     """Two forwards of the same batch into two workspaces give the same bits:
     y and every intermediate (no sum depends on thread timing)."""
@@ -409,18 +433,21 @@ def test_host_errors_enqueue_nothing(lm):
     assert y.shape[0] == 0
 
 
-def test_host_io_pipeline_matches_device_forward(lm):
+@pytest.mark.parametrize("name,T0", [("tiny", 512), ("small", 300)])
+def test_host_io_pipeline_matches_device_forward(lm, name, T0):
     """lmoe_forward_host over several queued batches (ragged T, distinct
-    inputs, both staging slots reused) gives the device forward's bits."""
-    shape = synth.TINY
+    inputs, both staging slots reused) gives the device forward's bits.  At
+    the small widths and these batch sizes every dense GEMM splits over K, so
+    the queued forwards also share the workspace's partial-sum slot."""
+    shape = synth.SHAPES[name]
     w = {k: v.cuda() for k, v in synth.layer_weights_host(shape).items()}
-    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=shape.T)
-    ws = lm.alloc_workspace(h, shape.T)
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=T0)
+    ws = lm.alloc_workspace(h, T0)
     io = lm.alloc_host_io(h)
     xs, bs, ys = [], [], []
     for i in range(5):
-        x, b = synth.activations_host(shape, seed_offset=100 + i)
-        T = shape.T - 37 * i
+        x, b = synth.activations_host(shape, T=T0, seed_offset=100 + i)
+        T = T0 - 37 * i
         xs.append(x[:T].contiguous().pin_memory())
         bs.append(b.pin_memory())
         ys.append(torch.empty_like(xs[-1]).pin_memory())

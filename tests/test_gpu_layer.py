@@ -387,6 +387,39 @@ def test_workspace_for_max_tokens_serves_every_smaller_batch(lm):
     assert lm.lmoe_device_status(h) == 0
 
 
+@pytest.mark.parametrize("T", [300, 4096])
+def test_caller_output_buffers_get_the_workspace_bits(lm, T):
+    """Scores, top-k ids, gates and expert counts written to caller buffers
+    equal what a forward without them leaves in its workspace, bit for bit,
+    and y is unchanged; at T = 300 the router splits over K, so its scores
+    come from the split's finalize."""
+    shape = synth.SMALL
+    E, K = shape.n_experts, shape.top_k
+    w = synth.layer_weights_device(shape)
+    x, b = synth.activations_device(shape, T=T, seed_offset=5)
+    h = lm.lmoe_create(shape.layer_dict(), w, max_tokens=T)
+    ws = lm.alloc_workspace(h, T)
+    y0 = lm.lmoe_forward(h, x, b, workspace=ws)
+    torch.cuda.synchronize()
+    lay = lm.lmoe_workspace_layout(h, T)
+    ref = {"scores": ws_view(ws, lay, "scores", torch.float32, (T, E)).clone(),
+           "topk_idx": ws_view(ws, lay, "topk_idx", torch.int32, (T, K)).clone(),
+           "gates": ws_view(ws, lay, "gates", torch.float32, (T, K)).clone(),
+           "counts": ws_view(ws, lay, "counts", torch.int32, (E,)).clone()}
+    s_out = torch.full((T, E), float("nan"), device="cuda")
+    i_out = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
+    g_out = torch.full((T, K), float("nan"), device="cuda")
+    c_out = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    ws2 = lm.alloc_workspace(h, T)
+    y1 = lm.lmoe_forward(h, x, b, workspace=ws2, scores_out=s_out, topk_idx_out=i_out, gates_out=g_out,
+                         expert_counts_out=c_out)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(h) == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    for got, key in ((s_out, "scores"), (i_out, "topk_idx"), (g_out, "gates"), (c_out, "counts")):
+        assert torch.equal(got.view(torch.int32), ref[key].view(torch.int32)), key
+
+
 def test_forward_is_deterministic(lm):
     """Two forwards of the same batch into two workspaces give the same bits:
     y and every intermediate (no sum depends on thread timing)."""

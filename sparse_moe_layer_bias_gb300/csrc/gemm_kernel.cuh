@@ -95,6 +95,7 @@ struct Cfg {
     static constexpr size_t kSmem =
         KSEG ? 1024 + kTmaStgOffset + 4 * kTmaStgWarpBytes
              : 1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes;
+    static_assert(kSmem <= 232448, "more dynamic shared memory than a CTA may have (227 KB)");
 };
 
 struct Tile {

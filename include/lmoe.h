@@ -417,7 +417,8 @@ int lmoe_selftest_index(cudaStream_t stream);
  * (sigmoid scores need no further map).  hist: [E][B] uint32.
  *   bin(s) = min(B-1, floor(fp32(s*B)))  (fp32 multiply; s < 0 -> bin 0)
  *   hist[e][bin(scores[t][e])] += 1 for all t < T.
- * accumulate = 0 clears hist first; 1 adds to it (histograms are additive).
+ * accumulate = 0 replaces hist's contents (every bin is written); 1 adds to
+ * it (histograms are additive).
  * Constraints: T >= 0, 1 <= E <= ld, 1 <= B <= 65536.  NaN scores are not
  * allowed (their bin is undefined). */
 int qb_histogram(const float *scores, int64_t T, int32_t E, int64_t ld, int32_t B,

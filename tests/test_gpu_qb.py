@@ -72,6 +72,21 @@ def test_histogram_accumulates(lm):
     assert np.array_equal(hist_np(hg), oracle.qb_histogram(s.numpy(), B))
 
 
+def test_histogram_overwrites_a_dirty_buffer_then_accumulates(lm):
+    """E = 896, B = 1000 (56 groups of 16 experts, a few token chunks each):
+    without accumulate every bin is replaced, zeros included, whatever the
+    buffer held; with accumulate the counts are added to it."""
+    T, E, B = 9000, 896, 1000
+    s = synth.qb_scores(T, E, seed=11)
+    hg = torch.full((E, B), 0x5A5A5A5A, dtype=torch.int32, device="cuda")   # not zeroed
+    lm.qb_histogram(s[:4000].cuda(), B, hist=hg)
+    torch.cuda.synchronize()
+    assert np.array_equal(hist_np(hg), oracle.qb_histogram(s[:4000].numpy(), B))
+    lm.qb_histogram(s[4000:].cuda(), B, hist=hg, accumulate=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(hist_np(hg), oracle.qb_histogram(s.numpy(), B))
+
+
 def test_histogram_full_size_sampled(lm):
     """T = 2^20 x 896 (the largest sweep point): every row sums to T and a
     sample of expert columns matches the oracle bit for bit."""

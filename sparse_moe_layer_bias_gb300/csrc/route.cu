@@ -5,8 +5,14 @@
 // token picks, not how their outputs are weighted.  Per token, one warp:
 //   u_e = fp32(s_e + b_e); take the top_k largest u (ties: lower expert id),
 //   gate_j = s at the chosen expert (unbiased).
-// Each round takes two warp reductions (max of the lanes' best keys, then the
-// lowest expert id among the lanes holding it).
+// The k-th largest of the 32 lanes' largest keys is a lower bound tau on the
+// token's k-th largest key (k lanes each hold a key at least that large), so
+// every key of the top k is >= tau.  Typically only ~20 keys are; they are
+// gathered into one per lane and put in order by one bitonic sort over the
+// warp (key descending, expert id ascending).  A token with more than 32 such
+// keys (e.g. a row of saturated scores) takes k rounds instead, each of two
+// warp reductions (max of the lanes' best keys, then the lowest expert id
+// among the lanes holding it).  Both give the same, exact result.
 // a4: the T*top_k assignments are grouped by expert with a deterministic,
 // stable counting sort.  A token picks an expert at most once, so "stable by
 // assignment id" is "ordered by token": each expert keeps a bitmap over
@@ -29,15 +35,53 @@ __device__ __forceinline__ uint32_t order_key(float u) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Bitonic sort of one value per lane, largest in lane 0.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+            // runs of `size` lanes alternate direction; the last run (all
+            // 32 lanes) is descending, where the lower lane keeps the larger
+            const bool desc = (lane & size) == 0;
+            const bool lower = (lane & stride) == 0;
+            v = (lower == desc) ? max(v, o) : min(v, o);
+        }
+    }
+    return v;
+}
+
+// The same over (key, id) pairs, best first: larger key, then lower id (all
+// ids distinct, so no two pairs compare equal).
+__device__ __forceinline__ void warp_sort_pairs_desc(uint32_t &key, uint32_t &id, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
+            const uint32_t oi = __shfl_xor_sync(0xffffffffu, id, stride);
+            const bool other_better = ok > key || (ok == key && oi < id);
+            const bool keep_better = ((lane & stride) == 0) == ((lane & size) == 0);
+            if (keep_better == other_better) {
+                key = ok;
+                id = oi;
+            }
+        }
+    }
+}
+
 template <int V>  // experts per lane (E <= 32*V)
 __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, int64_t T, int E,
                 int k, int32_t *__restrict__ idx, float *__restrict__ gate,
                 uint32_t *__restrict__ bitmap, int words) {
     grid_dependency_wait();
+    __shared__ uint2 s_cand[kTopkWarps][32];   // a warp's candidates: (key, expert)
     const int lane = threadIdx.x & 31;
-    const int64_t t = int64_t(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
-    if (t >= T) return;
+    const int wib = threadIdx.x >> 5;
+    const int64_t t = int64_t(blockIdx.x) * kTopkWarps + wib;
+    if (t >= T) return;   // the whole warp; nothing below synchronises the block
     const float *srow = scores + t * E;
     uint32_t key[V];
 #pragma unroll
@@ -46,26 +90,62 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
         key[i] = (e < E) ? order_key(__fadd_rn(srow[e], bias[e])) : 0u;
     }
     int my_e = -1;
-    for (int j = 0; j < k; ++j) {
-        // lane-local best: largest key, lowest expert id (= lowest i) on ties
-        uint32_t bk = 0u;
-        int bi = 0;
+    // tau: the k-th largest of the lanes' largest keys.  Lanes 0 .. min(E,32)-1
+    // each hold an expert and k <= E, so tau is a real key (> 0), and the
+    // experts past E (key 0) are never candidates.
+    uint32_t lmax = 0u;
 #pragma unroll
-        for (int i = V - 1; i >= 0; --i)
-            if (key[i] >= bk) {
-                bk = key[i];
-                bi = i;
-            }
-        // warp: the largest key, then the lowest expert id holding it
-        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
-        const int cand = (bk == wk && bk != 0u) ? bi * 32 + lane : 0x7fffffff;
-        const int we = __reduce_min_sync(0xffffffffu, cand);
-        if ((we & 31) == lane) {
+    for (int i = 0; i < V; ++i) lmax = max(lmax, key[i]);
+    const uint32_t tau = __shfl_sync(0xffffffffu, warp_sort_desc(lmax, lane), k - 1);
+    uint32_t cmask = 0u;   // bit i: key[i] is a candidate (V <= 32)
 #pragma unroll
-            for (int i = 0; i < V; ++i)
-                if (i == (we >> 5)) key[i] = 0u;
+    for (int i = 0; i < V; ++i) cmask |= (key[i] >= tau ? 1u : 0u) << i;
+    const int c = __popc(cmask);
+    const int n_cand = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(c)));
+    if (n_cand <= 32) {
+        int incl = c;   // inclusive prefix of the lanes' candidate counts
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
         }
-        if (lane == j) my_e = we;
+        const int pos0 = incl - c;   // the lane's candidates go to pos0, pos0 + 1, ...
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if ((cmask >> i) & 1u)
+                s_cand[wib][pos0 + __popc(cmask & ((1u << i) - 1u))] =
+                    make_uint2(key[i], static_cast<uint32_t>(i * 32 + lane));
+        __syncwarp();
+        // one candidate per lane; the empty lanes rank last (key 0, ids
+        // above every expert's)
+        uint32_t ck = 0u, ce = 0x10000u + static_cast<uint32_t>(lane);
+        if (lane < n_cand) {
+            const uint2 cv = s_cand[wib][lane];
+            ck = cv.x;
+            ce = cv.y;
+        }
+        warp_sort_pairs_desc(ck, ce, lane);
+        my_e = static_cast<int>(ce);
+    } else {
+        uint32_t taken = 0u;   // bit i: key[i] was chosen in an earlier round
+        for (int j = 0; j < k; ++j) {
+            // lane-local best: largest key not yet taken, lowest expert id (=
+            // lowest i) on ties
+            uint32_t bk = 0u;
+            int bi = 0;
+#pragma unroll
+            for (int i = V - 1; i >= 0; --i)
+                if (!((taken >> i) & 1u) && key[i] >= bk) {
+                    bk = key[i];
+                    bi = i;
+                }
+            // warp: the largest key, then the lowest expert id holding it
+            const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+            const int cand = (bk == wk && bk != 0u) ? bi * 32 + lane : 0x7fffffff;
+            const int we = __reduce_min_sync(0xffffffffu, cand);
+            if (we != 0x7fffffff && (we & 31) == lane) taken |= 1u << (we >> 5);
+            if (lane == j) my_e = we;
+        }
     }
     if (lane < k) {
         idx[t * k + lane] = my_e;

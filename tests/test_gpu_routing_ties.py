@@ -5,7 +5,9 @@ u = fp32(s + b); among equal u the lower expert id wins, and the chosen ids
 are listed by descending u, then ascending id (a reading: the pages do not
 say how ties break).  Random scores almost never tie, so the ties are planted:
 duplicated score columns, rows of all-equal scores, biases that make two
-experts' u equal, and bias steps too small to survive the fp32 add."""
+experts' u equal, bias steps too small to survive the fp32 add, a tie across
+the k-th place, and a tie of 40 experts at the top (more candidates than the
+selection's one-sort path takes)."""
 import numpy as np
 import pytest
 import torch
@@ -54,9 +56,23 @@ def with_boundary_tie(s, b, k):
     return s, b
 
 
+def with_wide_tie(s, b):
+    """Row 5: experts 8 .. 47 tie at u = 0.99 above every other expert.  Each
+    of the 32 lanes then holds a key equal to the k-th largest, so more than
+    32 keys reach the selection's threshold and the token takes the
+    round-by-round path; the lowest ids win.  (E >= 48 only: with E <= 32
+    every lane holds one key and the threshold never admits more than 32.)"""
+    E = s.shape[1]
+    if E >= 48:
+        b[8:48] = 0.0
+        s[5, :] = (s[5, :] * 0.2).astype(np.float32)
+        s[5, 8:48] = 0.99
+    return s, b
+
+
 @pytest.mark.parametrize("T,E,k,seed", [(300, 896, 16, 1), (257, 64, 8, 2), (40, 12, 5, 3)])
 def test_route_static_ties_match_the_oracle(lm, T, E, k, seed):
-    s, b = with_boundary_tie(*planted(T, E, seed), k)
+    s, b = with_wide_tie(*with_boundary_tie(*planted(T, E, seed), k))
     cfg = oracle.LayerConfig(d=64, latent=128, n_experts=E, top_k=k, inter=64, n_shared=1, shared_inter=64)
     u = (s + b[None, :]).astype(np.float32)
     assert any(len(set(row.tolist())) < E for row in u)      # the planting made ties
@@ -68,6 +84,8 @@ def test_route_static_ties_match_the_oracle(lm, T, E, k, seed):
     idx = got["topk_idx"].cpu().numpy()
     assert np.array_equal(idx, idx_ref)
     assert np.array_equal(idx[3], np.arange(k))          # the boundary tie: lower ids win
+    if E >= 48:
+        assert np.array_equal(idx[5], np.arange(8, 8 + k))   # the wide tie
     assert np.array_equal(got["gates"].cpu().numpy().view(np.uint32), gate_ref.view(np.uint32))
     for key, ref in (("counts", counts), ("offsets", offsets), ("perm", perm), ("inv", inv)):
         assert np.array_equal(got[key].cpu().numpy(), ref), key

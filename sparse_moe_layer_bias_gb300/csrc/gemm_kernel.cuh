@@ -69,14 +69,18 @@ constexpr int kAccStride = 256;
 
 // CG2: the tile is 256 x BN on a CTA pair; each CTA holds 128 rows of A and
 // BN / 2 rows of B per stage.
-template <int BN, bool PAIR, bool KSEG = false, bool CG2 = false>
+template <int BN, bool PAIR, bool KSEG = false, bool CG2 = false, int EW = 4>
 struct Cfg {
     static constexpr int kSub = PAIR ? 2 : 1;           // 128-row sub-tiles per tile
     static constexpr int kABytes = kSub * kBM * kBK * 2; // 16 or 32 KB
     static constexpr int kBRows = CG2 ? BN / 2 : BN;    // B rows per CTA and stage
     static constexpr int kBBytes = kBRows * kBK * 2;    // 14 to 32 KB
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
+    // (eight epilogue warps, with their staging buffers, leave room for five
+    // 32 KB or three 48 KB stages)
+    static constexpr int kStages = EW == 8 ? ((kStageBytes <= 32768) ? 5 : 3)
+                                           : (kStageBytes <= 32768) ? 6 : (kStageBytes <= 49152) ? 4 : 3;
+    static constexpr int kEpiWarps = EW;
     static constexpr int kBarBytes = 256;
     // per epilogue warp: 32 rows x 64 bf16, row pitch 144 B (16 B of padding
     // keeps the 16-byte row writes and the 128-byte row reads conflict-free)
@@ -94,7 +98,7 @@ struct Cfg {
     static constexpr int kTmaStgWarpBytes = 2 * 4096;
     static constexpr size_t kSmem =
         KSEG ? 1024 + kTmaStgOffset + 4 * kTmaStgWarpBytes
-             : 1024 + size_t(kStages) * kStageBytes + kBarBytes + 4 * kStgWarpBytes + 4 * kColWarpBytes;
+             : 1024 + size_t(kStages) * kStageBytes + kBarBytes + EW * kStgWarpBytes + EW * kColWarpBytes;
     static_assert(kSmem <= 232448, "more dynamic shared memory than a CTA may have (227 KB)");
 };
 
@@ -227,20 +231,29 @@ __device__ __forceinline__ void store_f32_32(float *dst, const float (&v)[32], i
     }
 }
 
-// A_GATHER adds four warps (6..9) that gather A rows with cp.async.
-__host__ __device__ constexpr int threads_for(int am) { return am == A_GATHER ? kThreads + 128 : kThreads; }
+// Epilogue warps: eight for the e4m3 experts' W3 (its scaled bf16 epilogue,
+// not its loads, sets its pace; warps 6..9 are free in a TMA-fed GEMM), four
+// otherwise.
+__host__ __device__ constexpr int epi_warps(int epi) { return epi == EPI_SCATTER_F8 ? 8 : 4; }
+// A_GATHER adds four warps (6..9) that gather A rows with cp.async; eight
+// epilogue warps take warps 6..9 instead.
+__host__ __device__ constexpr int threads_for(int am, int epi = EPI_BF16) {
+    return (am == A_GATHER || epi_warps(epi) == 8) ? kThreads + 128 : kThreads;
+}
 
 template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR, bool KSEG = false, bool CG2 = false>
-__global__ void __launch_bounds__(threads_for(AM), 1)
+__global__ void __launch_bounds__(threads_for(AM, EPI), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const GemmArgs args) {
-    using C = Cfg<BN, PAIR, KSEG, CG2>;
+    using C = Cfg<BN, PAIR, KSEG, CG2, epi_warps(EPI)>;
     constexpr int S = C::kStages;
     constexpr int H = BN / 2;  // GLU: features per tile
     constexpr int NSUB = C::kSub;
     constexpr int NACC = PAIR ? 1 : 2;  // TMEM accumulator buffers (each NSUB x 256 columns)
     static_assert(!PAIR || (AM == A_GATHER && GROUPED), "pair tiles are built for the gathered expert GEMM");
+    static_assert(C::kEpiWarps == 4 || (AM != A_GATHER && !KSEG && !CG2 && !PAIR),
+                  "eight epilogue warps need warps 6..9 free");
     static_assert(!KSEG || (GROUPED && AM == A_DENSE && BMD == B_PLAIN && EPI == EPI_F32),
                   "K segments are built for the experts' weight gradients");
     static_assert(!CG2 || (!GROUPED && !PAIR && !KSEG && AM != A_GATHER && EPI != EPI_SITU_GLU_F8 &&
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
         for (int b = 0; b < NACC; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
             // pairs: one arrival per epilogue warp of both CTAs (on CTA 0's barrier)
-            mbar_init(smem_u32(&tempty[b]), CG2 ? 8 : 128);
+            mbar_init(smem_u32(&tempty[b]), CG2 ? 8 : 32 * C::kEpiWarps);
         }
         mbar_init(smem_u32(&drain[0]), 1);
         *abort_flag = 0u;
@@ -517,13 +530,15 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
+    } else if (warp < 2 + C::kEpiWarps) {
         // ------------------------------------------------------------ epilogue
+        // (eight warps: warps 2..5 take the first half of each tile's output
+        // columns, warps 6..9 the second; both sets cover all lane quarters)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;       // row of the tile held by this thread
         uint8_t *stg = smem + S * C::kStageBytes + C::kBarBytes + (warp - 2) * C::kStgWarpBytes;
-        float *cscale = reinterpret_cast<float *>(smem + S * C::kStageBytes + C::kBarBytes + 4 * C::kStgWarpBytes +
-                                                  (warp - 2) * C::kColWarpBytes);
+        float *cscale = reinterpret_cast<float *>(smem + S * C::kStageBytes + C::kBarBytes +
+                                                  C::kEpiWarps * C::kStgWarpBytes + (warp - 2) * C::kColWarpBytes);
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t n_tma_stores = 0;   // K segments without split stores: TMA stores issued by this warp
@@ -797,8 +812,10 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
                 const int64_t col0 = int64_t(ti.nt) * NOUT;
                 const float b1 = args.beta1, b2 = args.beta2;
                 const float ib1 = 1.0f / b1, ib2 = 1.0f / b2;
+                constexpr int CW = NOUT / (C::kEpiWarps / 4);   // columns per warp set
+                const int c_begin = ((warp - 2) >> 2) * CW;
 #pragma unroll 1
-                for (int c = 0; c < NOUT; c += 64) {
+                for (int c = c_begin; c < c_begin + CW; c += 64) {
                     uint32_t packed[32];
                     float va[32], vb[32];
                     if (!GLU) tmem_ld32x2(taddr + c, taddr + c + 32, va, vb);   // both halves
@@ -905,10 +922,10 @@ __global__ void __launch_bounds__(threads_for(AM), 1)
 template <int BN, int AM, int BMD, int EPI, bool GROUPED, bool PAIR = false, bool KSEG = false>
 cudaError_t launch_one(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t st, bool dependent) {
     auto kern = gemm_kernel<BN, AM, BMD, EPI, GROUPED, PAIR, KSEG>;
-    const size_t smem = Cfg<BN, PAIR, KSEG>::kSmem;
+    const size_t smem = Cfg<BN, PAIR, KSEG, false, epi_warps(EPI)>::kSmem;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, dim3(grid), dim3(threads_for(AM)), smem, st, dependent, m.a0, m.a1, m.b0, m.b1, a);
+    return launch_kernel(kern, dim3(grid), dim3(threads_for(AM, EPI)), smem, st, dependent, m.a0, m.a1, m.b0, m.b1, a);
 }
 
 // CTA pairs: clusters of two CTAs, as many pairs as fit on the GPU at once
@@ -921,7 +938,7 @@ cudaError_t launch_pair(const GemmMaps &m, const GemmArgs &a, int64_t tiles, cud
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(threads_for(AM));
+    cfg.blockDim = dim3(threads_for(AM, EPI));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

@@ -7,9 +7,15 @@
 //   r_t = z_t / sqrt(mean(z_t^2) + eps)   -> bf16
 // One CTA per token; each thread keeps VPT vectors of 8 latent channels in
 // fp32 registers, so z is read once from the k expert rows and never stored.
+// A token's k rows are contiguous (assignment order), and the kernel is bound
+// by the bytes it keeps in flight: where they fit in shared memory they
+// arrive there by bulk copies (one per row, all in flight at once: 112 KB
+// per token at K3 widths, two tokens per SM), else each thread loads four
+// rows at a time into registers.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace lmoe {
 
@@ -24,6 +30,97 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &w) {
         acc[2 * i] += __uint_as_float(u[i] << 16);
         acc[2 * i + 1] += __uint_as_float(u[i] & 0xffff0000u);
     }
+}
+
+// z (this thread's VPT vectors of 8 channels, fp32) -> r = z / sqrt(mean z^2
+// + eps) in bf16: the sum of squares over the row by warp shuffles and one
+// shared-memory step (the whole CTA takes part).
+template <int VPT>
+__device__ __forceinline__ void store_rms_row(const float (&acc)[VPT][8], int L, float eps, uint16_t *row) {
+    const int nvec = L / 8;
+    float ss = 0.0f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss += acc[v][i] * acc[v][i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    __shared__ float part[kCombineThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) part[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kCombineThreads / 32; ++w) tot += part[w];
+    const float inv_rms = 1.0f / sqrtf(tot / static_cast<float>(L) + eps);
+
+    uint4 *out = reinterpret_cast<uint4 *>(row);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int vi = threadIdx.x + v * kCombineThreads;
+        if (vi >= nvec) continue;
+        uint32_t p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(acc[v][2 * i] * inv_rms, acc[v][2 * i + 1] * inv_rms);
+            p[i] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        out[vi] = make_uint4(p[0], p[1], p[2], p[3]);
+    }
+}
+
+constexpr size_t kBulkRowsOffset = 64;          // the mbarrier and the abort flag come first
+constexpr size_t kBulkSmemMax = 227 * 1024;
+
+// The same with the token's k rows in shared memory: warp 0's lanes issue one
+// bulk copy per row onto one mbarrier (armed first with all the bytes), every
+// thread waits for it (bounded), then sums its channels over the rows in the
+// same order as the kernel above (so both give the same bits).
+template <int VPT>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_rmsnorm_bulk_kernel(const uint16_t *__restrict__ o, int k, int L, float eps,
+                                uint16_t *__restrict__ r, unsigned *err, uint64_t wait_limit_ns) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + 8);
+    const uint4 *rows = reinterpret_cast<const uint4 *>(smem + kBulkRowsOffset);
+    const int64_t t = blockIdx.x;
+    const int nvec = L / 8;
+    const uint32_t row_bytes = static_cast<uint32_t>(L) * 2u;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(bar), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    grid_dependency_wait();
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(smem_u32(bar), row_bytes * static_cast<uint32_t>(k));
+        __syncwarp();
+        for (int j = threadIdx.x; j < k; j += 32)
+            bulk_load(smem_u32(smem + kBulkRowsOffset + size_t(j) * row_bytes), o + (t * k + j) * int64_t(L),
+                      row_bytes, smem_u32(bar));
+    }
+    const bool landed = mbar_wait(smem_u32(bar), 0u, abort_flag, err, wait_limit_ns, /*watch_abort=*/false);
+    if (!__syncthreads_and(landed ? 1 : 0)) {
+        // the copies did not land in time (the status bit is set): leave no
+        // copy in flight into this CTA's shared memory, then give up the token
+        if (threadIdx.x == 0) mbar_wait(smem_u32(bar), 0u, abort_flag, err, wait_limit_ns, false);
+        __syncthreads();
+        return;
+    }
+    float acc[VPT][8];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[v][i] = 0.0f;
+    for (int j = 0; j < k; ++j)
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int vi = threadIdx.x + v * kCombineThreads;
+            if (vi < nvec) add_bf16x8(acc[v], rows[int64_t(j) * nvec + vi]);
+        }
+    store_rms_row<VPT>(acc, L, eps, r + t * int64_t(L));
 }
 
 template <int VPT>
@@ -62,35 +159,7 @@ __global__ void __launch_bounds__(kCombineThreads)
             if (vi < nvec) add_bf16x8(acc[v], __ldg(base + (int64_t)j * nvec + vi));
         }
 
-    float ss = 0.0f;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss += acc[v][i] * acc[v][i];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    __shared__ float part[kCombineThreads / 32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) part[warp] = ss;
-    __syncthreads();
-    float tot = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kCombineThreads / 32; ++w) tot += part[w];
-    const float inv_rms = 1.0f / sqrtf(tot / static_cast<float>(L) + eps);
-
-    uint4 *out = reinterpret_cast<uint4 *>(r + t * int64_t(L));
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        const int vi = threadIdx.x + v * kCombineThreads;
-        if (vi >= nvec) continue;
-        uint32_t p[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(acc[v][2 * i] * inv_rms, acc[v][2 * i + 1] * inv_rms);
-            p[i] = *reinterpret_cast<uint32_t *>(&b);
-        }
-        out[vi] = make_uint4(p[0], p[1], p[2], p[3]);
-    }
+    store_rms_row<VPT>(acc, L, eps, r + t * int64_t(L));
 }
 
 // Ablation variant's norm after the down-projection ("Kimi-K3-Architecture-
@@ -163,12 +232,23 @@ cudaError_t launch_rms_rows(const uint16_t *h, int64_t T, int L, double eps, uin
 }
 
 cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,
-                                   uint16_t *r, cudaStream_t st) {
+                                   uint16_t *r, unsigned *err, uint64_t wait_limit_ns, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const int nvec = L / 8;
     const int vpt = (nvec + kCombineThreads - 1) / kCombineThreads;
     const dim3 grid(static_cast<unsigned>(T));
     const dim3 block(kCombineThreads);
+    const size_t smem = kBulkRowsOffset + size_t(k) * size_t(L) * 2;
+    if (L % 8 == 0 && (reinterpret_cast<uintptr_t>(o) % 16) == 0 && smem <= kBulkSmemMax) {
+        auto bulk = [&](auto kern) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            return launch_kernel(kern, grid, block, smem, st, true, o, k, L, eps, r, err, wait_limit_ns);
+        };
+        if (vpt <= 1) return bulk(combine_rmsnorm_bulk_kernel<1>);
+        if (vpt <= 2) return bulk(combine_rmsnorm_bulk_kernel<2>);
+        if (vpt <= 4) return bulk(combine_rmsnorm_bulk_kernel<4>);
+    }
     if (vpt <= 1) return launch_kernel(combine_rmsnorm_kernel<1>, grid, block, 0, st, true, o, k, L, eps, r);
     if (vpt <= 2) return launch_kernel(combine_rmsnorm_kernel<2>, grid, block, 0, st, true, o, k, L, eps, r);
     if (vpt <= 4) return launch_kernel(combine_rmsnorm_kernel<4>, grid, block, 0, st, true, o, k, L, eps, r);

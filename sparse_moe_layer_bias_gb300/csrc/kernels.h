@@ -279,7 +279,7 @@ cudaError_t launch_fp8_quantize_rows(const uint16_t *src, int64_t R, int K, uint
 // Row RMSNorm of bf16 rows (fp64 arithmetic, one rounding to bf16); L % 8 == 0.
 cudaError_t launch_rms_rows(const uint16_t *h, int64_t T, int L, double eps, uint16_t *out, cudaStream_t stream);
 cudaError_t launch_combine_rmsnorm(const uint16_t *o, int64_t T, int k, int L, float eps,
-                                   uint16_t *r, cudaStream_t stream);
+                                   uint16_t *r, unsigned *err, uint64_t wait_limit_ns, cudaStream_t stream);
 
 // ------------------------------------------------------------------ QB
 cudaError_t launch_qb_histogram(const float *scores, int64_t T, int E, int64_t ld, int B,

@@ -945,8 +945,8 @@ int lmoe_forward(lmoe_handle *h, const uint16_t *x, int64_t T, const float *bias
     }
     mark(LMOE_STAGE_COMBINE);
     // a7: z = sum of the token's gate-weighted expert rows; r = RMSNorm(z)
-    if (launch_combine_rmsnorm(obuf, T, static_cast<int>(K), static_cast<int>(L), c.rms_eps, rbuf,
-                               stream) != cudaSuccess)
+    if (launch_combine_rmsnorm(obuf, T, static_cast<int>(K), static_cast<int>(L), c.rms_eps, rbuf, h->d_status,
+                               kWaitLimitNs, stream) != cudaSuccess)
         return LMOE_ERR_CUDA;
     mark(LMOE_STAGE_UP);
     {   // a8: y = r W_up^T + act_s Ws3^T  (one GEMM, K split over the two sources)

@@ -112,6 +112,14 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32
                  "r"(src), "r"(x), "r"(y)
                  : "memory");
 }
+// Untiled bulk copy of `bytes` from global memory into this CTA's shared
+// memory (both addresses 16-byte aligned, bytes a multiple of 16); completes
+// `bytes` on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>

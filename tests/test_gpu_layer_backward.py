@@ -179,6 +179,29 @@ def test_backward_is_deterministic(lm):
         assert torch.equal(t, g2[n]), n
 
 
+@pytest.mark.parametrize("shape_name", ["tiny", "small"])
+def test_backward_gradients_in_16_byte_aligned_buffers(lm, shape_name):
+    """The interface promises 16-byte alignment only: gradient buffers 16
+    bytes past a 32-byte boundary (TMA store maps and 16-byte stores on them)
+    get the same bits as aligned ones."""
+    shape = {"tiny": synth.TINY, "small": synth.SMALL}[shape_name]
+    run = run_backward(lm, shape, T=300)
+    x, dy = run["x_host"].cuda(), run["dy_host"].cuda()
+    off = {}
+    for n, s in lm.grad_shapes(run["h"]).items():
+        numel = int(np.prod(s))
+        flat = torch.empty(numel + 8, dtype=torch.float32, device="cuda")
+        assert flat.data_ptr() % 32 == 0
+        off[n] = flat[4:4 + numel].view(s)
+        assert off[n].data_ptr() % 32 == 16
+    dx2, _ = lm.lmoe_backward(run["h"], x, dy, run["ws"], grads=off)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_status(run["h"]) == 0
+    assert torch.equal(run["dx"], dx2)
+    for n, t in run["grads"].items():
+        assert torch.equal(t, off[n]), n
+
+
 def test_backward_unused_experts_get_zero(lm):
     # few tokens: most of the 32 experts are chosen by none
     shape = synth.TINY

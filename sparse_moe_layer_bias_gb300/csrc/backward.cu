@@ -364,12 +364,30 @@ __device__ __forceinline__ void tanh_and_slope(float y, float &t, float &slope) 
 // da is the activation's gradient; returns act = SiTU softcap as well.
 __device__ __forceinline__ void situ_glu_bwd(float p1, float p2, float da, float b1, float ib1, float b2,
                                              float ib2, float &dp1, float &dp2, float &act) {
-    float t1, s1, t2, s2;
-    tanh_and_slope(p1 * ib1, t1, s1);
+    float t2, s2;
     tanh_and_slope(p2 * ib2, t2, s2);
-    const float sig = __fdividef(1.0f, 1.0f + __expf(-p1));   // 0 once e^(-p1) passes 2^126
-    const float situ = b1 * t1 * sig;
-    const float dsitu = s1 * sig + situ * (1.0f - sig);
+    float situ, dsitu;
+    if (b1 == 4.0f) {
+        // beta1 = 4 (K3): with u = e^(-x/2) and D = (1 + u)(1 + u^2),
+        // tanh(x/4) = (1 - u)/(1 + u) and sigma(x) = 1/(1 + u^2), so
+        //   SiTU  = 4 (1 - u) / D
+        //   SiTU' = (1 - tanh^2) sigma + SiTU (1 - sigma)
+        //         = 4 (u / D) ((1 + u + u^2 - u^3) / D)
+        // from one exponential and one reciprocal; the two factors stay in
+        // range where 1/D^2 alone would underflow.  x is floored at -50 as
+        // in the forward (there |SiTU'| < 1e-21).
+        const float u = __expf(-0.5f * fmaxf(p1, -50.0f));
+        const float u2 = u * u;
+        const float inv_d = __fdividef(1.0f, (1.0f + u) * (1.0f + u2));
+        situ = 4.0f * (1.0f - u) * inv_d;
+        dsitu = 4.0f * (u * inv_d) * (fmaf(u2, 1.0f - u, 1.0f + u) * inv_d);
+    } else {
+        float t1, s1;
+        tanh_and_slope(p1 * ib1, t1, s1);
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-p1));   // 0 once e^(-p1) passes 2^126
+        situ = b1 * t1 * sig;
+        dsitu = s1 * sig + situ * (1.0f - sig);
+    }
     const float cap = b2 * t2;
     dp1 = da * dsitu * cap;
     dp2 = da * situ * s2;

@@ -332,6 +332,20 @@ def test_odd_split_layer_stages_and_end_to_end(lm):
     end_to_end(ODD_SPLIT, run)
 
 
+# A latent of 8192 (the interface's largest) with k = 16: a token's 16 rows of
+# o (256 KB) exceed a CTA's shared memory, so the combine takes its register
+# path instead of the bulk copies the other shapes use.
+WIDE_LATENT = synth.LayerShape("wide_latent", T=96, d=512, latent=8192, n_experts=24, top_k=16, inter=64,
+                               n_shared=1, shared_inter=64, seed=1015)
+
+
+def test_wide_latent_layer_stages_and_end_to_end(lm):
+    assert WIDE_LATENT.top_k * WIDE_LATENT.latent * 2 > 227 * 1024
+    run = run_host_shape(lm, WIDE_LATENT)
+    staged_checks(WIDE_LATENT, run)
+    end_to_end(WIDE_LATENT, run)
+
+
 # The degenerate routing: one routed expert, chosen by every token (E = k = 1;
 # 300 tokens: one pair tile of 256 rows and one of 44 in the W1|W2 GEMM).
 SINGLE_EXPERT = synth.LayerShape("single_expert", T=300, d=256, latent=128, n_experts=1, top_k=1, inter=64,

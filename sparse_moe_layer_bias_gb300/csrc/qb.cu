@@ -175,45 +175,60 @@ __global__ void qb_hist_global_kernel(const float *__restrict__ s, int64_t T, in
 }
 
 // One warp per expert: N, the rank r, the first bin whose cumulative count
-// reaches r, and the in-bin linear interpolation, all in fp64.
+// reaches r (found in two levels: the lanes' spans of bins, then the bins of
+// one span), and the in-bin linear interpolation, all in fp64.
 __global__ void qb_quantile_kernel(const uint32_t *__restrict__ hist, int E, int B, double level,
                                    float *__restrict__ q_out, float *__restrict__ b_out) {
     const int lane = threadIdx.x & 31;
     const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (e >= E) return;
     const uint32_t *row = hist + int64_t(e) * B;
-    unsigned long long n = 0;
-    for (int j = lane; j < B; j += 32) n += row[j];
+    // Two levels: lane l sums the bins of its span [l*span, (l+1)*span); one
+    // scan over the lanes gives n and the span holding the r-th count; the
+    // warp then scans that span alone for the first bin whose cumulative
+    // count reaches r.
+    const int span = (B + 31) / 32;
+    const int s0 = min(B, lane * span), s1 = min(B, s0 + span);
+    unsigned long long part = 0;
+    for (int j = s0; j < s1; ++j) part += row[j];
+    unsigned long long incl = part;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const unsigned long long n = __shfl_sync(0xffffffffu, incl, 31);
     double q = 0.0;
     if (n > 0) {
         double rr = ceil(level * static_cast<double>(n));
         if (rr < 1.0) rr = 1.0;
         if (rr > static_cast<double>(n)) rr = static_cast<double>(n);
         const unsigned long long r = static_cast<unsigned long long>(rr);
-        unsigned long long below = 0;  // cumulative count before this chunk
-        for (int j0 = 0; j0 < B; j0 += 32) {
+        // the first span whose cumulative count reaches r (lane 31's is n >= r)
+        const int fs = __ffs(__ballot_sync(0xffffffffu, incl >= r)) - 1;
+        unsigned long long below = __shfl_sync(0xffffffffu, incl - part, fs);   // counts before that span
+        const int j_begin = __shfl_sync(0xffffffffu, s0, fs), j_end = __shfl_sync(0xffffffffu, s1, fs);
+        for (int j0 = j_begin; j0 < j_end; j0 += 32) {
             const int j = j0 + lane;
-            const unsigned long long c = (j < B) ? row[j] : 0ull;
-            unsigned long long incl = c;
+            const unsigned long long c = (j < j_end) ? row[j] : 0ull;
+            unsigned long long inc = c;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
+                const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += o;
             }
-            const unsigned ballot = __ballot_sync(0xffffffffu, j < B && below + incl >= r);
+            const unsigned ballot = __ballot_sync(0xffffffffu, j < j_end && below + inc >= r);
             if (ballot) {
                 const int f = __ffs(ballot) - 1;
                 const unsigned long long cf = __shfl_sync(0xffffffffu, c, f);
-                const unsigned long long inf = __shfl_sync(0xffffffffu, incl, f);
+                const unsigned long long inf = __shfl_sync(0xffffffffu, inc, f);
                 const unsigned long long before = below + inf - cf;  // C_{j*-1}
                 q = (static_cast<double>(j0 + f) +
                      static_cast<double>(r - before) / static_cast<double>(cf)) /
                     static_cast<double>(B);
                 break;
             }
-            below += __shfl_sync(0xffffffffu, incl, 31);
+            below += __shfl_sync(0xffffffffu, inc, 31);
         }
     }
     if (lane == 0) {
